@@ -1,0 +1,341 @@
+/*
+ * Paged-KV GQA attention oracle: a plain, slow, fp64 CPU statement of what
+ * libpagedattn computes.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA path; nothing in the product calls it.
+ *
+ * Sources (page title, section):
+ *   [P1] "Модуль 12: Финальный проект: мини-движок инференса" (LLM Inference
+ *        Systems course), task 12.1 and the qwen_serve/paged.py listing
+ *        (PagedKVCache docstring, PagedKVCache.write, PagedKVCache.read) and the
+ *        qwen_serve/model.py listing (Qwen3Model.forward, attention loop).
+ *   [P2] "Модуль 04: KV-кэш и арифметика памяти", section 1 (the attention
+ *        output formula), kv_cache.py section 2 (attend: GQA by repeating KV
+ *        heads, mask on absolute positions k_pos <= q_pos).
+ *   [P3] "Phase 10: LLMs from Scratch — Inference Optimization", step 2
+ *        (scaled dot-product attention with a causal mask).
+ *
+ * Every floating-point input arrives as raw 16-bit patterns (IEEE binary16 or
+ * bfloat16) and is widened exactly to double.  Nothing is rounded on the way:
+ * scores, softmax and the weighted sum of values are all fp64, and masked keys
+ * are excluded from the sums rather than filled with a large negative number.
+ *
+ * Layout of one layer's pool [P1, PagedKVCache docstring]: K and V each as
+ * [num_blocks][block_size][num_kv_heads][head_dim]; block b is the outer
+ * index, the in-block slot the next one.  A flat slot number is
+ * block * block_size + offset.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
+
+/* ---- exact widening of the 16-bit formats --------------------------------- */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_f16_to_f64(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int f = h & 0x3ff;
+  double mag;
+  if (e == 0) {
+    mag = ldexp((double)f, -24);               /* subnormal: f * 2^-14 * 2^-10 */
+  } else if (e == 31) {
+    mag = f ? NAN : INFINITY;
+  } else {
+    mag = ldexp((double)(1024 + f), e - 25);   /* (1 + f/1024) * 2^(e-15) */
+  }
+  return sign ? -mag : mag;
+}
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+double oracle_bf16_to_f64(uint16_t b) {
+  int sign = (b >> 15) & 1;
+  int e = (b >> 7) & 0xff;
+  int f = b & 0x7f;
+  double mag;
+  if (e == 0) {
+    mag = ldexp((double)f, -133);              /* f * 2^-126 * 2^-7 */
+  } else if (e == 255) {
+    mag = f ? NAN : INFINITY;
+  } else {
+    mag = ldexp((double)(128 + f), e - 134);   /* (1 + f/128) * 2^(e-127) */
+  }
+  return sign ? -mag : mag;
+}
+
+static double widen(uint16_t bits, int dtype) {
+  return dtype == ORACLE_BF16 ? oracle_bf16_to_f64(bits) : oracle_f16_to_f64(bits);
+}
+
+/* ---- KV write [P1, PagedKVCache.write] ------------------------------------- */
+
+/*
+ * For each new token t in order, copy its K and V rows (num_kv_heads x
+ * head_dim 16-bit values) into flat slot slot_mapping[t] of the pool.  Tokens
+ * are processed in order, so a repeated slot keeps the last token's row (the
+ * page's sequential loop).  A slot outside [0, num_blocks*block_size) is
+ * skipped and counted; the return value is the number of skipped tokens.
+ */
+int64_t oracle_kv_cache_write(uint16_t *k_cache, uint16_t *v_cache,
+                              int64_t num_blocks, int32_t block_size,
+                              int32_t num_kv_heads, int32_t head_dim,
+                              const uint16_t *k, const uint16_t *v,
+                              const int64_t *slot_mapping, int64_t num_tokens) {
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  int64_t skipped = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= num_blocks * block_size) {
+      ++skipped;
+      continue;
+    }
+    int64_t block = slot / block_size, offset = slot % block_size;
+    int64_t dst = (block * block_size + offset) * row;
+    for (int64_t x = 0; x < row; ++x) {
+      k_cache[dst + x] = k[t * row + x];
+      v_cache[dst + x] = v[t * row + x];
+    }
+  }
+  return skipped;
+}
+
+/* ---- gather read [P1, PagedKVCache.read] ----------------------------------- */
+
+/*
+ * Rows of positions [0, upto) of one KV head, gathered through a block table:
+ * logical position j lives in block table entry j / block_size at in-block
+ * offset j % block_size.  Writes upto*head_dim doubles to k_out and v_out.
+ * Returns 0, or -1 if a needed block id is outside [0, num_blocks).
+ */
+int oracle_gather_head(const uint16_t *k_cache, const uint16_t *v_cache, int dtype,
+                       int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                       int32_t head_dim, const int32_t *block_table_row,
+                       int32_t kv_head, int32_t upto, double *k_out, double *v_out) {
+  for (int32_t j = 0; j < upto; ++j) {
+    int32_t entry = j / block_size, offset = j % block_size;
+    int64_t block = block_table_row[entry];
+    if (block < 0 || block >= num_blocks) return -1;
+    int64_t base = ((block * block_size + offset) * num_kv_heads + kv_head) * (int64_t)head_dim;
+    for (int32_t x = 0; x < head_dim; ++x) {
+      k_out[(int64_t)j * head_dim + x] = widen(k_cache[base + x], dtype);
+      v_out[(int64_t)j * head_dim + x] = widen(v_cache[base + x], dtype);
+    }
+  }
+  return 0;
+}
+
+/* ---- one query row of attention [P1 Qwen3Model.forward; P2 section 1] ------ */
+
+/*
+ * out = sum_j p_j v_j with p_j = exp(S_j - max S) / sum_i exp(S_i - max S) and
+ * S_j = scale * <q, k_j>, over the n visible keys (rows 0..n-1 of kk / vv).
+ * The max is subtracted as the pages' softmax does; in exact arithmetic it
+ * cancels.  s is scratch of n doubles.
+ */
+static void attend_row(const double *q, const double *kk, const double *vv,
+                       int32_t n, int32_t d, double scale, double *s, double *out) {
+  double m = -INFINITY;
+  for (int32_t j = 0; j < n; ++j) {
+    double dot = 0.0;
+    for (int32_t x = 0; x < d; ++x) dot += q[x] * kk[(int64_t)j * d + x];
+    s[j] = scale * dot;
+    if (s[j] > m) m = s[j];
+  }
+  double z = 0.0;
+  for (int32_t j = 0; j < n; ++j) {
+    s[j] = exp(s[j] - m);
+    z += s[j];
+  }
+  for (int32_t x = 0; x < d; ++x) out[x] = 0.0;
+  for (int32_t j = 0; j < n; ++j) {
+    double p = s[j] / z;
+    for (int32_t x = 0; x < d; ++x) out[x] += p * vv[(int64_t)j * d + x];
+  }
+}
+
+/* ---- shared problem description and a small thread pool ------------------- */
+
+typedef struct {
+  const uint16_t *q;            /* [rows][num_q_heads][head_dim] */
+  int dtype;
+  const uint16_t *k_cache, *v_cache;
+  int64_t num_blocks;
+  int32_t block_size, num_kv_heads, head_dim;
+  const int32_t *block_tables;  /* [num_groups][max_blocks_per_seq] */
+  int32_t max_blocks_per_seq;
+  int32_t num_q_heads;
+  double scale;
+  double *out;                  /* [rows][num_q_heads][head_dim] */
+  /* One "group" is a decode sequence or a prefill chunk: a block-table row
+   * plus the query rows [row0, row0 + nrows) whose absolute positions are
+   * pos0 + i, i < nrows.  Query row i sees keys [0, pos0 + i]. */
+  int32_t num_groups;
+  const int32_t *group_row0, *group_nrows, *group_pos0;
+  int64_t next;                 /* work counter: (group, kv head) items */
+  pthread_mutex_t lock;
+  int error;
+} problem_t;
+
+static void run_item(problem_t *P, int32_t g, int32_t h, double *kk, double *vv,
+                     double *s, double *qd) {
+  const int32_t d = P->head_dim;
+  const int32_t G = P->num_q_heads / P->num_kv_heads;
+  const int32_t nrows = P->group_nrows[g], row0 = P->group_row0[g], pos0 = P->group_pos0[g];
+  const int32_t nkeys = pos0 + nrows;   /* keys the last row of the group sees */
+  if (oracle_gather_head(P->k_cache, P->v_cache, P->dtype, P->num_blocks, P->block_size,
+                         P->num_kv_heads, d, P->block_tables + (int64_t)g * P->max_blocks_per_seq,
+                         h, nkeys, kk, vv) != 0) {
+    pthread_mutex_lock(&P->lock);
+    P->error = -1;
+    pthread_mutex_unlock(&P->lock);
+    return;
+  }
+  /* Query head qh reads KV head qh / G: the G query heads of one KV head are
+   * contiguous [P1 model.py view(T, n_kv, group, D); P2 attend np.repeat]. */
+  for (int32_t qh = h * G; qh < (h + 1) * G; ++qh) {
+    for (int32_t i = 0; i < nrows; ++i) {
+      const int64_t base = ((int64_t)(row0 + i) * P->num_q_heads + qh) * d;
+      for (int32_t x = 0; x < d; ++x) qd[x] = widen(P->q[base + x], P->dtype);
+      attend_row(qd, kk, vv, pos0 + i + 1, d, P->scale, s, P->out + base);
+    }
+  }
+}
+
+static void *worker(void *arg) {
+  problem_t *P = (problem_t *)arg;
+  int32_t maxkeys = 0;
+  for (int32_t g = 0; g < P->num_groups; ++g)
+    if (P->group_pos0[g] + P->group_nrows[g] > maxkeys) maxkeys = P->group_pos0[g] + P->group_nrows[g];
+  const int32_t d = P->head_dim;
+  double *kk = (double *)malloc(sizeof(double) * (size_t)(maxkeys > 0 ? maxkeys : 1) * d);
+  double *vv = (double *)malloc(sizeof(double) * (size_t)(maxkeys > 0 ? maxkeys : 1) * d);
+  double *s = (double *)malloc(sizeof(double) * (size_t)(maxkeys > 0 ? maxkeys : 1));
+  double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+  if (!kk || !vv || !s || !qd) {
+    pthread_mutex_lock(&P->lock);
+    P->error = -2;
+    pthread_mutex_unlock(&P->lock);
+  } else {
+    for (;;) {
+      pthread_mutex_lock(&P->lock);
+      int64_t item = P->next++;
+      pthread_mutex_unlock(&P->lock);
+      if (item >= (int64_t)P->num_groups * P->num_kv_heads) break;
+      run_item(P, (int32_t)(item / P->num_kv_heads), (int32_t)(item % P->num_kv_heads), kk, vv, s, qd);
+    }
+  }
+  free(kk);
+  free(vv);
+  free(s);
+  free(qd);
+  return NULL;
+}
+
+static int run_problem(problem_t *P, int32_t num_threads) {
+  if (P->num_kv_heads <= 0 || P->num_q_heads % P->num_kv_heads != 0) return -3;
+  if (num_threads <= 0) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    num_threads = n > 0 ? (int32_t)n : 1;
+  }
+  int64_t items = (int64_t)P->num_groups * P->num_kv_heads;
+  if (num_threads > items) num_threads = items > 0 ? (int32_t)items : 1;
+  P->next = 0;
+  P->error = 0;
+  pthread_mutex_init(&P->lock, NULL);
+  pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)num_threads);
+  int started = 0;
+  for (int32_t i = 0; i < num_threads; ++i)
+    if (pthread_create(&th[i], NULL, worker, P) == 0) ++started;
+  if (started == 0) worker(P);
+  for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+  free(th);
+  pthread_mutex_destroy(&P->lock);
+  return P->error;
+}
+
+/* ---- decode [P1 Qwen3Model.forward with T = 1] ------------------------------ */
+
+/*
+ * One query token per sequence s, at absolute position context_lens[s] - 1,
+ * already present in the pool: q[s][qh] attends to keys 0 .. context_lens[s]-1
+ * of KV head qh / (num_q_heads / num_kv_heads).  Output [num_seqs][Hq][d] fp64.
+ * Returns 0, -1 for a block id out of range, -3 for a bad head split, -4 for a
+ * context length < 1 or beyond the block table.
+ */
+int oracle_paged_attn_decode(const uint16_t *q, int32_t dtype,
+                             const uint16_t *k_cache, const uint16_t *v_cache,
+                             int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                             int32_t head_dim, const int32_t *block_tables,
+                             int32_t max_blocks_per_seq, const int32_t *context_lens,
+                             int32_t num_seqs, int32_t num_q_heads, double scale,
+                             double *out, int32_t num_threads) {
+  int32_t *row0 = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1));
+  int32_t *nrows = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1));
+  int32_t *pos0 = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1));
+  int rc = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    int32_t n = context_lens[s];
+    if (n < 1 || n > max_blocks_per_seq * block_size) rc = -4;
+    row0[s] = s;
+    nrows[s] = 1;
+    pos0[s] = n - 1;
+  }
+  if (rc == 0) {
+    problem_t P = {q, dtype, k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim,
+                   block_tables, max_blocks_per_seq, num_q_heads, scale, out,
+                   num_seqs, row0, nrows, pos0};
+    rc = run_problem(&P, num_threads);
+  }
+  free(row0);
+  free(nrows);
+  free(pos0);
+  return rc;
+}
+
+/* ---- chunked prefill [P1 Qwen3Model.forward with T > 1; P2 attend mask] ----- */
+
+/*
+ * Chunk c holds chunk_lens[c] new query tokens at absolute positions
+ * chunk_starts[c] + i; their rows are packed in chunk order (chunk c starts at
+ * row sum_{c' < c} chunk_lens[c']).  Row i of chunk c sees keys
+ * 0 .. chunk_starts[c] + i (key position <= query position), read through
+ * block-table row c.  context_lens[c] must equal chunk_starts[c] +
+ * chunk_lens[c] (the chunk's own K/V are written before attending).
+ * Returns 0, -1 for a block id out of range, -3 for a bad head split, -4 for
+ * inconsistent chunk metadata.
+ */
+int oracle_paged_attn_prefill(const uint16_t *q, int32_t dtype,
+                              const uint16_t *k_cache, const uint16_t *v_cache,
+                              int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                              int32_t head_dim, const int32_t *chunk_starts,
+                              const int32_t *chunk_lens, const int32_t *block_tables,
+                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                              int32_t num_chunks, int32_t num_q_heads, double scale,
+                              double *out, int32_t num_threads) {
+  int32_t *row0 = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_chunks > 0 ? num_chunks : 1));
+  int rc = 0;
+  int32_t acc = 0;
+  for (int32_t c = 0; c < num_chunks; ++c) {
+    row0[c] = acc;
+    acc += chunk_lens[c];
+    if (chunk_lens[c] < 1 || chunk_starts[c] < 0 ||
+        context_lens[c] != chunk_starts[c] + chunk_lens[c] ||
+        context_lens[c] > max_blocks_per_seq * block_size)
+      rc = -4;
+  }
+  if (rc == 0) {
+    problem_t P = {q, dtype, k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim,
+                   block_tables, max_blocks_per_seq, num_q_heads, scale, out,
+                   num_chunks, row0, chunk_lens, chunk_starts};
+    rc = run_problem(&P, num_threads);
+  }
+  free(row0);
+  return rc;
+}
