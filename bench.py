@@ -1,0 +1,428 @@
+"""Benchmark of the paged-KV GQA attention hot path on GB300.
+
+Workload (default): the Qwen3-0.6B decode step over 28 layers — 8 sequences
+with context lengths uniform in [512, 1024], 16 query / 8 KV heads, head_dim
+128, fp16, one 512-block pool per layer (896 MiB of KV in total, larger than
+L2, so every step streams its KV from HBM).  One step = for each of the 28
+layers: kv_cache_write of the 8 new tokens, then paged_attn_decode.
+
+Printed JSON line (rank 0):
+  value      KV GB/s of the whole step (algorithmic bytes: every visible K/V
+             row read once, plus the new rows read and written) over the step
+             time measured with CUDA events around a CUDA graph of K steps;
+  e2e        the same metric through the Python binding with the step's
+             inputs copied from pinned host memory and its outputs read back
+             inside the timed region;
+  roofline   the decode call (split + combine kernels) timed alone per layer,
+             algorithmic bytes per launch over its duration, against the
+             measured HBM copy bandwidth;
+  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample.
+
+``--impl reference`` times the oracle itself (the only reference this method
+has) on the same workload and prints the same line with "impl": "reference".
+Multi-GPU (``torchrun --nproc-per-node N``) runs N independent replicas
+(sequences are independent; no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import contextlib
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode paged-attn KV GB/s (% of GB300 HBM peak); prefill-chunk TFLOP/s; tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of the cpu_baseline leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---- distributed plumbing (replicas only) -------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a host float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and getattr(device, "type", "cpu") == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---- clocks during the timed region ----------------------------------------------------
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                     timeout=5).stdout.strip()
+                if out:
+                    self.rows.append([x.strip() for x in out.split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        self._t.join(timeout=10)
+        return False
+
+    def summary(self):
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def committed_traffic(kernel_source: str, summary_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (the summary records the source's sha256)."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    try:
+        text = open(path).read()
+        src = open(os.path.join(ROOT, "paged_kv_gqa_cache_gb300", "csrc", kernel_source), "rb").read()
+    except OSError:
+        return None
+    want = hashlib.sha256(src).hexdigest()[:16]
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != want:
+        return None
+    return int(m_bytes.group(1))
+
+
+# ---- the workload ----------------------------------------------------------------------------
+
+class DecodeStep:
+    """The Qwen3-0.6B 28-layer decode step on device-resident inputs."""
+
+    def __init__(self, device):
+        import torch
+        import paged_kv_gqa_cache_gb300 as pa
+        import workloads
+        self.pa = pa
+        self.case = workloads.config2(device=device, nan_fill=False)
+        c = self.case
+        self.L = c.n_layers
+        self.out = [torch.empty_like(q) for q in c.q]
+        self.ws = pa.alloc_decode_workspace(c.q[0].shape[0], c.hq, c.hkv, c.max_context_len, device)
+        lens = c.meta["decode_lens"]
+        self.S = len(lens)
+        self.decode_bytes_layer = workloads.decode_kv_bytes(lens, c.hkv)
+        self.write_bytes_layer = 2 * c.k_new[0].numel() * 2 * 2     # K and V rows, read + write
+        self.step_bytes = self.L * (self.decode_bytes_layer + self.write_bytes_layer)
+        self.kernels_per_step = self.L * 3                          # write, split, combine
+
+    def write(self, l):
+        c = self.case
+        self.pa.kv_cache_write(c.k_new[l], c.v_new[l], c.slot_mapping, c.k_cache[l], c.v_cache[l])
+
+    def decode(self, l):
+        c = self.case
+        self.pa.paged_attn_decode(c.q[l], c.k_cache[l], c.v_cache[l], c.block_tables, c.context_lens, c.scale,
+                                  out=self.out[l], workspace=self.ws, max_context_len=c.max_context_len)
+
+    def run(self):
+        for l in range(self.L):
+            self.write(l)
+            self.decode(l)
+
+    def run_decode_only(self):
+        for l in range(self.L):
+            self.decode(l)
+
+
+def graph_of(fn, reps: int, stream):
+    import torch
+    fn()                                  # warm once outside capture (kernel attributes, caches)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_replays(g, n: int, stream) -> float:
+    """Milliseconds for n replays of graph g, by CUDA events on its stream."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream):
+    """Same metric through the public API with host buffers: per step, copy
+    q / new K,V / slots / tables / lengths from pinned host memory, run the 28
+    layers, read the outputs back to pinned host memory."""
+    import torch
+    c = step.case
+    host_in = {
+        "q": [t.cpu().pin_memory() for t in c.q],
+        "k": [t.cpu().pin_memory() for t in c.k_new],
+        "v": [t.cpu().pin_memory() for t in c.v_new],
+        "slots": c.slot_mapping.cpu().pin_memory(),
+        "bt": c.block_tables.cpu().pin_memory(),
+        "ctx": c.context_lens.cpu().pin_memory(),
+    }
+    host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in step.out]
+    h2d = sum(t.numel() * t.element_size() for k in ("q", "k", "v") for t in host_in[k])
+    h2d += sum(host_in[k].numel() * host_in[k].element_size() for k in ("slots", "bt", "ctx"))
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def one():
+        for l in range(step.L):
+            c.q[l].copy_(host_in["q"][l], non_blocking=True)
+            c.k_new[l].copy_(host_in["k"][l], non_blocking=True)
+            c.v_new[l].copy_(host_in["v"][l], non_blocking=True)
+        c.slot_mapping.copy_(host_in["slots"], non_blocking=True)
+        c.block_tables.copy_(host_in["bt"], non_blocking=True)
+        c.context_lens.copy_(host_in["ctx"], non_blocking=True)
+        step.run()
+        for l in range(step.L):
+            host_out[l].copy_(step.out[l], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+def cpu_baseline(step: DecodeStep, seconds: float):
+    """The fp64 oracle, as it stands, on the host cores: one decode layer at a
+    time of the same workload, until `seconds` of CPU time or one full step."""
+    import numpy as np
+    import torch
+    import oracle
+    c = step.case
+    threads = os.cpu_count() or 1
+    bt, ctx = c.block_tables.cpu().numpy(), c.context_lens.cpu().numpy()
+    done_bytes, t_total, layers = 0, 0.0, 0
+    for l in range(step.L):
+        kh = c.k_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
+        vh = c.v_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
+        qh = c.q[l].cpu().view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        oracle.paged_attn_decode(qh, kh, vh, bt, ctx, c.scale, oracle.F16, num_threads=threads)
+        t_total += time.perf_counter() - t0
+        done_bytes += step.decode_bytes_layer
+        layers += 1
+        if t_total >= seconds:
+            break
+    return {"value": done_bytes / t_total / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{layers} of {step.L} decode layers of the workload (fp64 C oracle, "
+                      f"{threads} threads), {t_total:.2f} s"}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_gqa_cache_gb300 as pa
+
+    step = DecodeStep(dev)
+    stream = torch.cuda.Stream(device=dev)
+    reps = 1
+    g_step = graph_of(step.run, reps, stream)
+    g_dec = graph_of(step.run_decode_only, reps, stream)
+    st, detail = pa.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {pa.STATUS.get(st, st)} at {detail}")
+
+    # warm-up, then K timed steps bracketed by barrier + synchronize
+    time_replays(g_step, max(args.warmup, 3), stream)
+    barrier(dev)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        ms_total = time_replays(g_step, args.steps, stream)
+        torch.cuda.synchronize()
+        barrier(dev)
+        # the dominant kernel alone: 28 decode calls per replay
+        ms_dec = time_replays(g_dec, max(args.steps // 2, 10), stream) / max(args.steps // 2, 10)
+    ms_total = reduce_max(ms_total, dev)
+    ms_step = ms_total / args.steps
+    hbm, bf16, peak_kind = measured_peaks()
+    value = world * step.step_bytes / (ms_step * 1e-3) / 1e9
+
+    dec_launch_ms = ms_dec / step.L
+    achieved = step.decode_bytes_layer / (dec_launch_ms * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = e2e_measure(step, max(args.steps // 20, 10), 3, stream)
+    e2e_ms = reduce_max(e2e_ms, dev)
+    st, detail = pa.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {pa.STATUS.get(st, st)} at {detail}")
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": "Qwen3-0.6B decode step, 28 layers: 8 seqs, ctx U[512,1024], Hq=16, Hkv=8, d=128, "
+                               "fp16, 512-block pool per layer",
+                   "global_batch": 8 * world, "seq_len": step.case.max_context_len,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (28 x 32 MiB pools = 896 MiB streamed per step)",
+                   "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
+        "pct_of_hbm_peak": round(100.0 * value / world / hbm, 1),
+        "tokens_per_s": round(world * step.S / (ms_step * 1e-3), 1),
+        "gpu_launches": step.kernels_per_step * args.steps,
+        "e2e": {"value": round(world * step.step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 3), "peak_kind": peak_kind,
+                     "kernel": "paged_attn_decode (split + combine) per layer",
+                     "bytes_per_launch": step.decode_bytes_layer, "launch_ms": round(dec_launch_ms, 5),
+                     "traffic": committed_traffic("decode.cu", "decode_split_qwen3_0.6b_decode.md")},
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(step, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle (the pages print no runnable
+    implementation of this path) timed on the host cores, one decode layer of
+    the workload per step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    import oracle
+    import workloads
+    case = workloads.config2(device="cpu", n_layers=1, nan_fill=False)
+    threads = os.cpu_count() or 1
+    kh = case.k_cache[0].view(torch.int16).numpy().view(np.uint16)
+    vh = case.v_cache[0].view(torch.int16).numpy().view(np.uint16)
+    qh = case.q[0].view(torch.int16).numpy().view(np.uint16)
+    bt, ctx = case.block_tables.numpy(), case.context_lens.numpy()
+    lay_bytes = workloads.decode_kv_bytes(case.meta["decode_lens"], case.hkv)
+    for _ in range(max(args.warmup, 1)):
+        oracle.paged_attn_decode(qh, kh, vh, bt, ctx, case.scale, oracle.F16, num_threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_attn_decode(qh, kh, vh, bt, ctx, case.scale, oracle.F16, num_threads=threads)
+    dt = time.perf_counter() - t0
+    ms_step = dt * 1e3 / args.steps
+    value = lay_bytes / (dt / args.steps) / 1e9
+    sample = f"1 of 28 decode layers of the workload per step (fp64 C oracle, {threads} threads)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "Qwen3-0.6B decode step, 28 layers: 8 seqs, ctx U[512,1024], Hq=16, Hkv=8, d=128, "
+                               "fp16, 512-block pool per layer", "global_batch": 8, "seq_len": case.max_context_len,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

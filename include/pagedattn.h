@@ -1,0 +1,182 @@
+/*
+ * libpagedattn — GQA attention over a paged KV cache, for GB300 (sm_103a).
+ *
+ * The operations follow two course pages:
+ *   [P1] "Модуль 12: Финальный проект: мини-движок инференса" (LLM Inference
+ *        Systems course): task 12.1 and the qwen_serve/paged.py listing
+ *        (PagedKVCache: pool layout, write, read) and the qwen_serve/model.py
+ *        listing (Qwen3Model.forward: GQA attention over the cached prefix,
+ *        causal mask on absolute positions for multi-token steps).
+ *   [P2] "Модуль 04: KV-кэш и арифметика памяти": section 1 (the attention
+ *        output over cached K/V), section 3.4 (chunked prefill keeps its KV
+ *        between chunks), task 04.1 (positions belong to the caller; the mask
+ *        compares absolute positions).
+ *
+ * Conventions for every call:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *     `pool` (a host pointer to a small descriptor read during the call).
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  The library allocates no memory per call.
+ *   - Host-detectable errors (NULL pointers, unsupported shapes, misaligned
+ *     pointers, workspace too small) are returned before anything is
+ *     enqueued.  Errors found in the data on the device (a block id outside
+ *     the pool, a slot outside the pool, a context length of 0 or beyond the
+ *     block table, inconsistent chunk metadata) are recorded in a per-device
+ *     error word, the offending row or page is skipped, and nothing traps;
+ *     read and clear the word with pa_get_device_error().
+ *   - head_dim is 128 and block_size is 16.  q, the pool and out share one
+ *     dtype (fp16 or bf16).  Accumulation is fp32.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+#define PA_HEAD_DIM 128
+#define PA_BLOCK_SIZE 16
+#define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+typedef void *pa_stream_t; /* a cudaStream_t */
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_NULL = -1,        /* a required pointer is NULL */
+  PA_ERR_SHAPE = -2,       /* a size is negative, inconsistent or over a limit */
+  PA_ERR_DTYPE = -3,       /* dtype is neither PA_F16 nor PA_BF16 */
+  PA_ERR_UNSUPPORTED = -4, /* head_dim != 128, block_size != 16, or an unsupported head ratio */
+  PA_ERR_WORKSPACE = -5,   /* workspace missing or smaller than the size query returns */
+  PA_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed (see pa_last_cuda_error) */
+  PA_ERR_RANGE = -7,       /* device: block id / slot / context length out of range */
+  PA_ERR_TIMEOUT = -8,     /* device: a bounded wait on an asynchronous copy gave up */
+  PA_ERR_ALIGN = -9        /* a pointer is not 16-byte aligned */
+} pa_status;
+
+/*
+ * One layer's KV pool [P1, qwen_serve/paged.py, PagedKVCache docstring]:
+ * k_cache and v_cache are each [num_blocks][block_size][num_kv_heads][head_dim]
+ * contiguous; block b is the outer index, the in-block slot the next one.
+ * The flat slot of (block b, offset o) is b * block_size + o.
+ */
+typedef struct {
+  void *k_cache;
+  void *v_cache;
+  int32_t num_blocks;
+  int32_t block_size;   /* must be 16 */
+  int32_t num_kv_heads;
+  int32_t head_dim;     /* must be 128 */
+  int32_t dtype;        /* pa_dtype */
+} pa_kv_pool;
+
+/*
+ * kv_cache_write — [P1, qwen_serve/paged.py, PagedKVCache.write]: copy the
+ * K and V rows of num_tokens new tokens into their slots.
+ *   k, v          [num_tokens][num_kv_heads][128], pool dtype.
+ *   slot_mapping  int64 [num_tokens]: flat slot (block * 16 + offset) of each
+ *                 token, composed by the caller from its block table as
+ *                 table[pos / 16] * 16 + pos % 16.
+ * A bit copy: the pool afterwards holds exactly the input bits.  A slot outside
+ * [0, num_blocks * 16) records PA_ERR_RANGE and that token is skipped.  Two
+ * tokens with the same slot in one call race (undefined which one lands).
+ * num_tokens == 0 is a no-op.
+ */
+PA_API pa_status pa_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
+                            int32_t num_tokens, const pa_kv_pool *pool, pa_stream_t stream);
+
+/*
+ * Size in bytes of the scratch workspace pa_paged_attn_decode needs for up to
+ * num_seqs sequences (split-K partial results plus a small index).  Depends
+ * only on its arguments; returns 0 for invalid arguments.
+ */
+PA_API size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t max_context_len);
+
+/*
+ * paged_attn_decode — [P1, qwen_serve/model.py, Qwen3Model.forward with one
+ * new token per sequence; P2 section 1]: for each sequence s and query head g,
+ *   out[s][g] = softmax_j(scale * q[s][g] . K_j) V_j  over j < context_lens[s],
+ * where K_j, V_j are KV head g / (num_q_heads / num_kv_heads) of logical
+ * position j, read from block block_tables[s][j / 16] at in-block offset j % 16.
+ * The new token's K/V must already be in the pool (write first), so
+ * context_lens[s] counts it.
+ *   q             [num_seqs][num_q_heads][128], pool dtype.
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                 ceil(context_lens[s] / 16) are never read.
+ *   context_lens  int32 [num_seqs], each in [1, max_blocks_per_seq * 16].
+ *   max_context_len  host-side upper bound on context_lens (sizes the launch
+ *                 and the workspace; a larger length is still computed).
+ *   out           [num_seqs][num_q_heads][128], pool dtype.
+ *   workspace     at least pa_decode_workspace_bytes(num_seqs, num_q_heads,
+ *                 num_kv_heads, max_context_len) bytes, 16-byte aligned; its
+ *                 contents need no initialisation and are clobbered.
+ * num_q_heads / num_kv_heads must be 1, 2, 4 or 8.  A sequence whose length is
+ * 0 or beyond its table records PA_ERR_RANGE; its output rows are untouched.
+ */
+PA_API pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                               float scale, void *out, void *workspace, size_t workspace_bytes,
+                               pa_stream_t stream);
+
+/*
+ * paged_attn_prefill_chunk — [P1, qwen_serve/model.py, Qwen3Model.forward
+ * with T > 1: causal mask kpos <= qpos on absolute positions; P2 section 3.4
+ * and task 04.1]: chunk c has chunk_lens[c] new query tokens at absolute
+ * positions chunk_starts[c] + i, attending to keys 0 .. chunk_starts[c] + i
+ * of its own sequence, read through block_tables[c].
+ *   q             [total_q_tokens][num_q_heads][128]: the chunks' rows packed
+ *                 in chunk order (chunk c starts at row sum_{c'<c} chunk_lens[c']).
+ *   chunk_starts, chunk_lens, context_lens  int32 [num_chunks];
+ *                 context_lens[c] must equal chunk_starts[c] + chunk_lens[c]
+ *                 (the chunk's own K/V are written first), and
+ *                 1 <= chunk_lens[c] <= max_chunk_len.
+ *   block_tables  int32 [num_chunks][max_blocks_per_seq].
+ *   max_chunk_len host-side bound on chunk_lens, at most 512.
+ *   out           [total_q_tokens][num_q_heads][128], pool dtype.
+ * QK^T and PV run on the tensor cores (bf16 or fp16 operands, fp32
+ * accumulation); the probabilities enter PV rounded to the input dtype.
+ * num_q_heads / num_kv_heads must be 1, 2, 4 or 8.  A chunk with inconsistent
+ * metadata records PA_ERR_RANGE and its rows are untouched.
+ */
+PA_API pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts,
+                                      const int32_t *chunk_lens, const pa_kv_pool *pool,
+                                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t *context_lens, int32_t num_chunks,
+                                      int32_t num_q_heads, int32_t total_q_tokens,
+                                      int32_t max_chunk_len, float scale, void *out,
+                                      pa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error
+ * word (PA_OK if no kernel recorded an error).  If `detail` is not NULL it
+ * receives the index (token, sequence or chunk) of the first error.
+ */
+PA_API pa_status pa_get_device_error(pa_stream_t stream, int32_t *detail);
+
+/* Human-readable name of a status code (static storage). */
+PA_API const char *pa_status_string(int32_t status);
+
+/* The last CUDA error code the library saw on this thread (0 if none). */
+PA_API int32_t pa_last_cuda_error(void);
+
+/* PA_ABI_VERSION of the loaded library. */
+PA_API int32_t pa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

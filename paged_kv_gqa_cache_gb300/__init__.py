@@ -1,0 +1,229 @@
+"""Python binding of libpagedattn (GQA attention over a paged KV cache, GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libpagedattn.so`` (built in-tree by ``_build.build()``).  Tensors
+must be CUDA tensors; calls are enqueued on ``torch.cuda.current_stream()``.
+There is no fallback: if the shared library is missing this module raises.
+
+Calls (see include/pagedattn.h for the full contract):
+
+* ``kv_cache_write(k, v, slot_mapping, k_cache, v_cache)``
+* ``paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ...)``
+* ``paged_attn_prefill_chunk(q, chunk_starts, chunk_lens, k_cache, v_cache,
+  block_tables, context_lens, scale, ...)``
+* ``get_device_error()``
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedattn.so")
+
+PA_F16, PA_BF16 = 0, 1
+PA_OK = 0
+STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_DTYPE", -4: "PA_ERR_UNSUPPORTED",
+          -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_CUDA", -7: "PA_ERR_RANGE", -8: "PA_ERR_TIMEOUT",
+          -9: "PA_ERR_ALIGN"}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_decode",
+           "pa_paged_attn_prefill_chunk", "pa_get_device_error", "pa_status_string",
+           "pa_last_cuda_error", "pa_abi_version")
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({_status_string(status)})")
+
+
+class KVPool(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libpagedattn.so and declare the C signatures.  Works without a GPU
+    (nothing is called); raises OSError if the library has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise OSError(f"libpagedattn.so not built at {path}; run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        pool_p = ctypes.POINTER(KVPool)
+        lib.pa_kv_cache_write.argtypes = [P, P, P, i32, pool_p, P]
+        lib.pa_kv_cache_write.restype = i32
+        lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        lib.pa_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.pa_paged_attn_decode.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P,
+                                             ctypes.c_size_t, P]
+        lib.pa_paged_attn_decode.restype = i32
+        lib.pa_paged_attn_prefill_chunk.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
+                                                    ctypes.c_float, P, P]
+        lib.pa_paged_attn_prefill_chunk.restype = i32
+        lib.pa_get_device_error.argtypes = [P, ctypes.POINTER(i32)]
+        lib.pa_get_device_error.restype = i32
+        lib.pa_status_string.argtypes = [i32]
+        lib.pa_status_string.restype = ctypes.c_char_p
+        lib.pa_last_cuda_error.argtypes = []
+        lib.pa_last_cuda_error.restype = i32
+        lib.pa_abi_version.argtypes = []
+        lib.pa_abi_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _status_string(status: int) -> str:
+    try:
+        return load_library().pa_status_string(status).decode()
+    except OSError:
+        return "library not loaded"
+
+
+def _check(status: int, what: str):
+    if status != PA_OK:
+        raise PagedAttnError(status, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"expected float16 or bfloat16, got {t.dtype}")
+
+
+def _need(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def make_pool(k_cache: torch.Tensor, v_cache: torch.Tensor) -> KVPool:
+    """Descriptor of one layer's pool: k_cache, v_cache [num_blocks, 16, Hkv, 128]."""
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache", k_cache.dtype)
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must both be [num_blocks, block_size, num_kv_heads, head_dim]")
+    nb, bs, hkv, d = k_cache.shape
+    return KVPool(k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, hkv, d, _dtype_code(k_cache))
+
+
+def kv_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, stream=None) -> None:
+    """Write new K/V rows [T, Hkv, 128] into flat slots ``slot_mapping`` (int64 [T])."""
+    pool = make_pool(k_cache, v_cache)
+    _need(k, "k", k_cache.dtype)
+    _need(v, "v", k_cache.dtype)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    T = slot_mapping.numel()
+    if k.shape != (T, pool.num_kv_heads, pool.head_dim) or v.shape != k.shape:
+        raise ValueError(f"k, v must be [{T}, {pool.num_kv_heads}, {pool.head_dim}]")
+    lib = load_library()
+    _check(lib.pa_kv_cache_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                                 ctypes.byref(pool), _stream(stream)), "pa_kv_cache_write")
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int) -> int:
+    return int(load_library().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, max_context_len))
+
+
+def alloc_decode_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int,
+                           device=None) -> torch.Tensor:
+    n = decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, max_context_len)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                      out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                      max_context_len: Optional[int] = None, stream=None) -> torch.Tensor:
+    """Decode attention: q [S, Hq, 128] → out [S, Hq, 128] (pool dtype).
+
+    ``max_context_len`` is a host-side bound on ``context_lens`` (no device
+    sync is made to find it); it defaults to the block table's capacity."""
+    pool = make_pool(k_cache, v_cache)
+    _need(q, "q", k_cache.dtype)
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    S, hq, d = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks], context_lens [S]")
+    mb = block_tables.shape[1]
+    mcl = int(max_context_len) if max_context_len is not None else mb * pool.block_size
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype)
+    if workspace is None:
+        workspace = alloc_decode_workspace(S, hq, pool.num_kv_heads, mcl, q.device)
+    _need(workspace, "workspace")
+    lib = load_library()
+    _check(lib.pa_paged_attn_decode(q.data_ptr(), ctypes.byref(pool), block_tables.data_ptr(), mb,
+                                    context_lens.data_ptr(), S, hq, mcl, float(scale), out.data_ptr(),
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)), "pa_paged_attn_decode")
+    return out
+
+
+def paged_attn_prefill_chunk(q: torch.Tensor, chunk_starts: torch.Tensor, chunk_lens: torch.Tensor,
+                             k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                             context_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                             max_chunk_len: int = 512, stream=None) -> torch.Tensor:
+    """Causal chunked-prefill attention: q [sum(chunk_lens), Hq, 128] → out (pool dtype)."""
+    pool = make_pool(k_cache, v_cache)
+    _need(q, "q", k_cache.dtype)
+    for name, t in (("chunk_starts", chunk_starts), ("chunk_lens", chunk_lens),
+                    ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need(t, name, torch.int32)
+    C = chunk_starts.numel()
+    if chunk_lens.numel() != C or context_lens.numel() != C or block_tables.dim() != 2 \
+            or block_tables.shape[0] != C:
+        raise ValueError("chunk metadata must have one entry (block-table row) per chunk")
+    rows, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype)
+    lib = load_library()
+    _check(lib.pa_paged_attn_prefill_chunk(q.data_ptr(), chunk_starts.data_ptr(), chunk_lens.data_ptr(),
+                                           ctypes.byref(pool), block_tables.data_ptr(), block_tables.shape[1],
+                                           context_lens.data_ptr(), C, hq, rows, int(max_chunk_len),
+                                           float(scale), out.data_ptr(), _stream(stream)),
+           "pa_paged_attn_prefill_chunk")
+    return out
+
+
+def get_device_error(stream=None) -> Tuple[int, int]:
+    """Synchronise the stream and return (status, detail) of the device error
+    word, clearing it."""
+    detail = ctypes.c_int32(0)
+    st = load_library().pa_get_device_error(_stream(stream), ctypes.byref(detail))
+    return int(st), int(detail.value)
+
+
+def raise_device_error(stream=None) -> None:
+    st, detail = get_device_error(stream)
+    if st != PA_OK:
+        raise PagedAttnError(st, f"device error (index {detail})")

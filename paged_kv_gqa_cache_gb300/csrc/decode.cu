@@ -1,0 +1,502 @@
+// Split-K paged GQA decode for sm_103a.
+//
+// Computes, for every sequence s and query head g (page "Модуль 12: Финальный
+// проект: мини-движок инференса", qwen_serve/model.py, Qwen3Model.forward with
+// one new token; page "Модуль 04: KV-кэш и арифметика памяти", section 1):
+//     out[s][g] = softmax_j(scale * q[s][g] . K_j) V_j,   j < context_lens[s],
+// with K_j, V_j taken from KV head g / G of logical position j, which lives in
+// block block_tables[s][j / 16] at in-block offset j % 16.
+//
+// Work decomposition.  The unit of work is one 16-token page of one KV head
+// of one sequence ("page" below); a (sequence, KV head) pair is an "item".
+// Pages are numbered globally, sequence-major then KV head then page, and the
+// W warps of the launch each take one contiguous, equal-sized range of that
+// numbering (stream-K style), so every warp moves the same number of bytes
+// whatever the length mix.  A warp whose range covers a whole item writes the
+// final output itself; otherwise each piece ("fragment") of an item writes an
+// unnormalised partial (m, l, o) into slot item + warp of the workspace, and
+// the combine kernel merges the fragments of each item with log-sum-exp
+// weights.  Every CTA recomputes the per-sequence page prefix sums from
+// context_lens, so no planning pass or atomic counter is needed.
+//
+// Per warp, K/V pages stream through a ring of shared-memory stages filled by
+// TMA (one 4-D tensor map per pool, 128-byte swizzle, four 2 KB boxes per
+// page) and guarded by one mbarrier each.  One page of K feeds all G query
+// heads of its KV head: the scores for G heads come from a single read of K.
+// All arithmetic is fp32 on the CUDA cores: decode reads each K/V byte once and
+// does G multiply-adds per element, far below the tensor-core ridge point.
+#include "pa_device.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int NW = kDecodeWarps;
+constexpr int STAGE = kDecodeStageBytes;
+constexpr int kStages = 3;  // TMA stages per warp
+constexpr unsigned FULL = 0xffffffffu;
+
+// Lane layout of the score (QK) phase: NQ lanes split the 128 dims of one key,
+// NT keys are scored per pass, NP passes cover a 16-token page.
+template <int G>
+struct Layout {
+  static constexpr int NQ = (G >= 8) ? 8 : 4;
+  static constexpr int NT = 32 / NQ;
+  static constexpr int NP = 16 / NT;
+  static constexpr int DPL = 128 / NQ;  // dims per lane
+  static constexpr int CPL = DPL / 8;   // 16-byte chunks per lane
+};
+
+__device__ __forceinline__ int pages_of(const DecodeParams &p, int s, bool report) {
+  const int ctx = __ldg(p.context_lens + s);
+  if (ctx < 1 || ctx > p.max_blocks_per_seq * kBlock) {
+    if (report) set_error(p.err, PA_ERR_RANGE, s);
+    return 0;
+  }
+  return (ctx + kBlock - 1) / kBlock;
+}
+
+// Exclusive prefix of pages over sequences into prefix[0..S]; whole CTA.
+__device__ void scan_pages(const DecodeParams &p, int32_t *prefix, int *warp_tot) {
+  const int n = p.num_seqs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (n + NW * 32 - 1) / (NW * 32);
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  const bool report = blockIdx.x == 0;
+  int sum = 0;
+  for (int s = lo; s < hi; ++s) sum += pages_of(p, s, report);
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int y = __shfl_up_sync(FULL, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0, total = 0;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    base += (i < warp) ? warp_tot[i] : 0;
+    total += warp_tot[i];
+  }
+  int run = base + incl - sum;
+  for (int s = lo; s < hi; ++s) {
+    prefix[s] = run;
+    run += pages_of(p, s, false);
+  }
+  if (tid == 0) prefix[n] = total;
+  __syncthreads();
+}
+
+struct Cursor {
+  int s, h, page, pages;
+};
+
+__device__ __forceinline__ Cursor locate(const int32_t *prefix, int n, int hkv, int64_t x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)hkv * prefix[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  Cursor c;
+  c.s = lo;
+  c.pages = prefix[lo + 1] - prefix[lo];
+  const int64_t r = x - (int64_t)hkv * prefix[lo];
+  c.h = (int)(r / c.pages);
+  c.page = (int)(r % c.pages);
+  return c;
+}
+
+__device__ __forceinline__ void advance(Cursor &c, const int32_t *prefix, int n, int hkv) {
+  if (++c.page < c.pages) return;
+  c.page = 0;
+  if (++c.h < hkv) return;
+  c.h = 0;
+  do {
+    ++c.s;
+  } while (c.s < n && prefix[c.s + 1] == prefix[c.s]);
+  c.pages = (c.s < n) ? prefix[c.s + 1] - prefix[c.s] : 1;
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(NW * 32)
+decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                    const DecodeParams p) {
+  using Ly = Layout<G>;
+  constexpr int NT = Ly::NT, NP = Ly::NP, DPL = Ly::DPL, CPL = Ly::CPL;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ int warp_tot[NW];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *stages = smem + warp * kStages * STAGE;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * kStages * STAGE) + warp * kStages;
+  float *pbuf = reinterpret_cast<float *>(smem + NW * kStages * STAGE + NW * kStages * 8) + warp * 16 * G;
+  int32_t *prefix = reinterpret_cast<int32_t *>(smem + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * G * 4);
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
+    fence_mbar_init();
+  }
+  scan_pages(p, prefix, warp_tot);
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= p.num_seqs; i += NW * 32) p.meta[i] = prefix[i];
+
+  const int n = p.num_seqs, hkv = p.num_kv_heads;
+  const int64_t P = (int64_t)prefix[n] * hkv;
+  const int w = blockIdx.x * NW + warp;
+  const int64_t x0 = (int64_t)w * P / p.num_workers;
+  const int64_t x1 = (int64_t)(w + 1) * P / p.num_workers;
+  if (x0 >= x1) return;
+  const int64_t npages = x1 - x0;
+
+  // lane roles
+  const int qd = lane / NT;  // which dim slice of a key this lane scores
+  const int tk = lane % NT;  // which key of a pass
+
+  Cursor ic = locate(prefix, n, hkv, x0);
+  Cursor cc = ic;
+
+  // ---- producer (lane 0 issues; all lanes track the cursor) --------------------
+  int win_s = -1, win_base = -1;
+  int32_t win = -1;
+  uint32_t bad_mask = 0;
+  auto issue = [&](int st) {
+    const int base = ic.page & ~31;
+    if (ic.s != win_s || base != win_base) {
+      win_s = ic.s;
+      win_base = base;
+      const int pg = base + lane;
+      win = (pg < ic.pages) ? __ldg(p.block_tables + (int64_t)ic.s * p.max_blocks_per_seq + pg) : -1;
+    }
+    const int blk = __shfl_sync(FULL, win, ic.page & 31);
+    const bool ok = (unsigned)blk < (unsigned)p.num_blocks;
+    if (lane == 0) {
+      if (ok) {
+        uint8_t *dst = stages + st * STAGE;
+        mbar_arrive_expect_tx(&bars[st], STAGE);
+        tma_load_4d(dst, &kmap, &bars[st], 0, ic.h, 0, blk);
+        tma_load_4d(dst + 2048, &kmap, &bars[st], 64, ic.h, 0, blk);
+        tma_load_4d(dst + 4096, &vmap, &bars[st], 0, ic.h, 0, blk);
+        tma_load_4d(dst + 6144, &vmap, &bars[st], 64, ic.h, 0, blk);
+      } else {
+        set_error(p.err, PA_ERR_RANGE, ic.s);
+        mbar_arrive(&bars[st]);
+      }
+    }
+    bad_mask = ok ? (bad_mask & ~(1u << st)) : (bad_mask | (1u << st));
+    advance(ic, prefix, n, hkv);
+  };
+
+  const int npre = (int)(npages < kStages ? npages : kStages);
+  for (int g = 0; g < npre; ++g) issue(g);
+
+  // ---- consumer state ---------------------------------------------------------
+  float q[G][DPL];
+  float o[G][4];
+  float m[G], l[G];
+  int ctx = 0;
+  bool open = false, whole = false;
+  const float neg_inf = -INFINITY;
+
+  for (int64_t g = 0; g < npages; ++g) {
+    const int st = (int)(g % kStages);
+    if (!open) {
+      // new item: load its G query rows (pre-scaled into the log2 domain)
+      const T *qp = reinterpret_cast<const T *>(p.q) +
+                    ((int64_t)cc.s * p.num_q_heads + (int64_t)cc.h * G) * kHeadDim;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const uint4 u = *reinterpret_cast<const uint4 *>(qp + gg * kHeadDim + (qd * CPL + i) * 8);
+          const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = Pack<T>::to_f2(wd[e]);
+            q[gg][i * 8 + 2 * e] = f.x * p.scale_log2;
+            q[gg][i * 8 + 2 * e + 1] = f.y * p.scale_log2;
+          }
+        }
+        m[gg] = neg_inf;
+        l[gg] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[gg][e] = 0.f;
+      }
+      ctx = __ldg(p.context_lens + cc.s);
+      whole = (cc.page == 0);
+      open = true;
+    }
+
+    if (!mbar_wait(&bars[st], (uint32_t)((g / kStages) & 1))) {
+      if (lane == 0) set_error(p.err, PA_ERR_TIMEOUT, cc.s);
+      // give the copies still in flight a short, bounded chance to land
+      for (int64_t r = g + 1; r < (npages < g + kStages ? npages : g + kStages); ++r)
+        mbar_wait(&bars[r % kStages], (uint32_t)((r / kStages) & 1), kWaitLimitNs / 8);
+      return;
+    }
+
+    if (!((bad_mask >> st) & 1u)) {
+      const int nv = min(kBlock, ctx - cc.page * kBlock);  // valid keys in this page
+      const uint8_t *kst = stages + st * STAGE;
+      const uint8_t *vst = kst + 4096;
+
+      // scores: NP passes of NT keys; lanes of one key hold slices of its dims
+      float sc[NP][G];
+#pragma unroll
+      for (int ps = 0; ps < NP; ++ps) {
+        const int t = ps * NT + tk;
+        float acc[G];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) acc[gg] = 0.f;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int cg = qd * CPL + i;
+          const uint4 u = *reinterpret_cast<const uint4 *>(kst + (cg >> 3) * 2048 + t * 128 +
+                                                          (((cg & 7) ^ (t & 7)) << 4));
+          const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = Pack<T>::to_f2(wd[e]);
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+              acc[gg] = fmaf(q[gg][i * 8 + 2 * e], f.x, acc[gg]);
+              acc[gg] = fmaf(q[gg][i * 8 + 2 * e + 1], f.y, acc[gg]);
+            }
+          }
+        }
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+#pragma unroll
+          for (int off = NT; off < 32; off <<= 1) acc[gg] += __shfl_xor_sync(FULL, acc[gg], off);
+          sc[ps][gg] = (t < nv) ? acc[gg] : neg_inf;
+        }
+      }
+
+      // online softmax update (log2 domain)
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        float mp = sc[0][gg];
+#pragma unroll
+        for (int ps = 1; ps < NP; ++ps) mp = fmaxf(mp, sc[ps][gg]);
+#pragma unroll
+        for (int off = 1; off < NT; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(FULL, mp, off));
+        const float mn = fmaxf(m[gg], mp);
+        const float alpha = exp2f(m[gg] - mn);
+        m[gg] = mn;
+        float ls = 0.f;
+#pragma unroll
+        for (int ps = 0; ps < NP; ++ps) {
+          const float pr = exp2f(sc[ps][gg] - mn);
+          ls += pr;
+          if (qd == 0) pbuf[(ps * NT + tk) * G + gg] = pr;
+        }
+        l[gg] = l[gg] * alpha + ls;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[gg][e] *= alpha;
+      }
+      __syncwarp();
+
+      // weighted sum of values: this lane owns dims [4 * lane, 4 * lane + 4)
+      const int vh = lane >> 4, vc = (lane & 15) >> 1, vsub = (lane & 1) * 8;
+#pragma unroll
+      for (int t = 0; t < kBlock; ++t) {
+        if (t < nv) {
+          const uint2 u = *reinterpret_cast<const uint2 *>(vst + vh * 2048 + t * 128 + ((vc ^ (t & 7)) << 4) + vsub);
+          const float2 v01 = Pack<T>::to_f2(u.x);
+          const float2 v23 = Pack<T>::to_f2(u.y);
+          float pr[G];
+          if constexpr (G == 1) {
+            pr[0] = pbuf[t];
+          } else if constexpr (G == 2) {
+            const float2 x = *reinterpret_cast<const float2 *>(pbuf + t * 2);
+            pr[0] = x.x; pr[1] = x.y;
+          } else {
+#pragma unroll
+            for (int gg = 0; gg < G; gg += 4) {
+              const float4 x = *reinterpret_cast<const float4 *>(pbuf + t * G + gg);
+              pr[gg] = x.x; pr[gg + 1] = x.y; pr[gg + 2] = x.z; pr[gg + 3] = x.w;
+            }
+          }
+#pragma unroll
+          for (int gg = 0; gg < G; ++gg) {
+            o[gg][0] = fmaf(pr[gg], v01.x, o[gg][0]);
+            o[gg][1] = fmaf(pr[gg], v01.y, o[gg][1]);
+            o[gg][2] = fmaf(pr[gg], v23.x, o[gg][2]);
+            o[gg][3] = fmaf(pr[gg], v23.y, o[gg][3]);
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane is done with this stage and with pbuf
+
+    if (g + kStages < npages) issue(st);
+
+    const bool last_of_item = (cc.page == cc.pages - 1);
+    if (last_of_item || g == npages - 1) {
+      const int item = cc.s * hkv + cc.h;
+      const bool final_out = whole && last_of_item;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        float lt = l[gg];
+#pragma unroll
+        for (int off = 1; off < NT; off <<= 1) lt += __shfl_xor_sync(FULL, lt, off);
+        if (final_out) {
+          const float inv = 1.f / lt;
+          T *op = reinterpret_cast<T *>(p.out) +
+                  ((int64_t)cc.s * p.num_q_heads + cc.h * G + gg) * kHeadDim + 4 * lane;
+          uint2 pk;
+          pk.x = Pack<T>::from_f2(o[gg][0] * inv, o[gg][1] * inv);
+          pk.y = Pack<T>::from_f2(o[gg][2] * inv, o[gg][3] * inv);
+          *reinterpret_cast<uint2 *>(op) = pk;
+        } else {
+          const int64_t slot = ((int64_t)item + w) * G + gg;
+          *reinterpret_cast<float4 *>(p.ws_o + slot * kHeadDim + 4 * lane) =
+              make_float4(o[gg][0], o[gg][1], o[gg][2], o[gg][3]);
+          if (lane == 0) *reinterpret_cast<float2 *>(p.ws_ml + slot * 2) = make_float2(m[gg], lt);
+        }
+      }
+      open = false;
+    }
+    advance(cc, prefix, n, hkv);
+  }
+}
+
+// Warp of the launch whose page range contains global page x.
+__device__ __forceinline__ int worker_of(int64_t x, int64_t P, int W) {
+  const int64_t w = ((x + 1) * W + P - 1) / P - 1;
+  return (int)(w < W - 1 ? w : W - 1);
+}
+
+// Log-sum-exp merge of the fragments of every item a single warp did not finish.
+// One warp per (sequence, query head); lane owns dims [4 * lane, 4 * lane + 4).
+template <typename T, int G>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (gw >= p.num_seqs * p.num_q_heads) return;
+  const int s = gw / p.num_q_heads, qh = gw % p.num_q_heads;
+  const int h = qh / G, gg = qh % G;
+  const int hkv = p.num_kv_heads;
+  const int pages = p.meta[s + 1] - p.meta[s];
+  if (pages == 0) return;
+  const int64_t P = (int64_t)p.meta[p.num_seqs] * hkv;
+  const int64_t A = (int64_t)hkv * p.meta[s] + (int64_t)h * pages;
+  const int wf = worker_of(A, P, p.num_workers), wl = worker_of(A + pages - 1, P, p.num_workers);
+  if (wf == wl) return;  // the split kernel wrote this output directly
+  const int item = s * hkv + h;
+  float M = -INFINITY, L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int w = wf; w <= wl; ++w) {
+    const int64_t slot = ((int64_t)item + w) * G + gg;
+    const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + slot * 2);
+    if (!(ml.x > -INFINITY)) continue;  // a fragment with no valid page
+    const float4 ov = *reinterpret_cast<const float4 *>(p.ws_o + slot * kHeadDim + 4 * lane);
+    const float Mn = fmaxf(M, ml.x);
+    const float a = exp2f(M - Mn), b = exp2f(ml.x - Mn);
+    L = L * a + ml.y * b;
+    O.x = O.x * a + ov.x * b;
+    O.y = O.y * a + ov.y * b;
+    O.z = O.z * a + ov.z * b;
+    O.w = O.w * a + ov.w * b;
+    M = Mn;
+  }
+  const float inv = 1.f / L;
+  T *op = reinterpret_cast<T *>(p.out) + ((int64_t)s * p.num_q_heads + qh) * kHeadDim + 4 * lane;
+  uint2 pk;
+  pk.x = Pack<T>::from_f2(O.x * inv, O.y * inv);
+  pk.y = Pack<T>::from_f2(O.z * inv, O.w * inv);
+  *reinterpret_cast<uint2 *>(op) = pk;
+}
+
+int split_smem_bytes(int group, int num_seqs) {
+  return 1024 + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * group * 4 + (num_seqs + 1) * 4;
+}
+
+template <typename T, int G>
+cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                         int max_workers, cudaStream_t stream) {
+  DecodeParams p = p0;
+  const int smem = split_smem_bytes(G, p.num_seqs);
+  // Per instantiation: raise the dynamic shared-memory limit and cache the
+  // occupancy for the largest size seen (launch-time API calls stay out of
+  // the hot path and out of CUDA-graph capture after the first call).
+  static int configured_smem = 0, cached_per_sm = 0;
+  if (smem > configured_smem) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<T, G>, NW * 32, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    configured_smem = smem;
+    cached_per_sm = per_sm;
+  }
+  const int per_sm = cached_per_sm;
+  cudaError_t e;
+  int grid = sm_count() * per_sm;
+  const int want = (max_workers + NW - 1) / NW;
+  if (want < grid) grid = want;
+  if (grid < 1) grid = 1;
+  if (grid * NW > kDecodeMaxWorkers) grid = kDecodeMaxWorkers / NW;
+  p.num_workers = grid * NW;
+  decode_split_kernel<T, G><<<grid, NW * 32, smem, stream>>>(kmap, vmap, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int cgrid = (p.num_seqs * p.num_q_heads + 3) / 4;
+  decode_combine_kernel<T, G><<<cgrid, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads) {
+  const int group = num_q_heads / num_kv_heads;
+  const size_t slots = (size_t)num_seqs * num_kv_heads + kDecodeMaxWorkers;
+  const size_t meta = (((size_t)num_seqs + 1) * 4 + 255) & ~(size_t)255;
+  const size_t ml = (slots * group * 2 * 4 + 255) & ~(size_t)255;
+  const size_t o = slots * group * kHeadDim * 4;
+  return meta + ml + o;
+}
+
+bool decode_workspace_carve(void *ws, size_t bytes, int num_seqs, int num_q_heads, int num_kv_heads,
+                            DecodeParams &p) {
+  if (bytes < decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads)) return false;
+  const int group = num_q_heads / num_kv_heads;
+  const size_t slots = (size_t)num_seqs * num_kv_heads + kDecodeMaxWorkers;
+  uint8_t *b = static_cast<uint8_t *>(ws);
+  const size_t meta = (((size_t)num_seqs + 1) * 4 + 255) & ~(size_t)255;
+  const size_t ml = (slots * group * 2 * 4 + 255) & ~(size_t)255;
+  p.meta = reinterpret_cast<int32_t *>(b);
+  p.ws_ml = reinterpret_cast<float *>(b + meta);
+  p.ws_o = reinterpret_cast<float *>(b + meta + ml);
+  return true;
+}
+
+int decode_max_seqs_for_smem() { return 0; }
+
+cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                          int dtype, int group, int max_workers, cudaStream_t stream) {
+#define PA_DECODE_CASE(T, G)                                                     \
+  if (group == G) return launch_typed<T, G>(p, kmap, vmap, max_workers, stream);
+  if (dtype == PA_BF16) {
+    PA_DECODE_CASE(__nv_bfloat16, 1)
+    PA_DECODE_CASE(__nv_bfloat16, 2)
+    PA_DECODE_CASE(__nv_bfloat16, 4)
+    PA_DECODE_CASE(__nv_bfloat16, 8)
+  } else {
+    PA_DECODE_CASE(__half, 1)
+    PA_DECODE_CASE(__half, 2)
+    PA_DECODE_CASE(__half, 4)
+    PA_DECODE_CASE(__half, 8)
+  }
+#undef PA_DECODE_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

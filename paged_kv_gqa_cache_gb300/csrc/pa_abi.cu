@@ -1,0 +1,301 @@
+// The C-ABI of libpagedattn: argument validation, per-device state (SM count,
+// error word), TMA tensor-map encoding, and dispatch to the kernels.  Every
+// check that can be made on the host is made here, before anything is
+// enqueued; see include/pagedattn.h for the contract of each call.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+// err[0]: first status recorded by a kernel on this device, err[1]: its detail.
+__device__ int g_error_word[2];
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  int *err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+pa_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return PA_ERR_CUDA;
+}
+
+// Set-up once per device, with that device current.
+pa_status device_state(DeviceState **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState &d = g_devices[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // The host-side name of a __device__ variable is not a device address;
+    // ask the runtime for the real one.
+    e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_error_word);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (!g_encode) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cuda_fail(e);
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return PA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+pa_status check_pool(const pa_kv_pool *pool) {
+  if (!pool || !pool->k_cache || !pool->v_cache) return PA_ERR_NULL;
+  if (pool->dtype != PA_F16 && pool->dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (pool->block_size != kBlock || pool->head_dim != kHeadDim) return PA_ERR_UNSUPPORTED;
+  if (pool->num_blocks < 1 || pool->num_kv_heads < 1 || pool->num_kv_heads > 256) return PA_ERR_SHAPE;
+  if (!aligned16(pool->k_cache) || !aligned16(pool->v_cache)) return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+pa_status check_group(int num_q_heads, int num_kv_heads, int *group) {
+  if (num_q_heads < 1 || num_q_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
+  const int g = num_q_heads / num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return PA_ERR_UNSUPPORTED;
+  *group = g;
+  return PA_OK;
+}
+
+CUtensorMapDataType map_dtype(int dtype) {
+  return dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// The pool as a 4-D tensor {dim, kv head, in-block slot, block}, boxes of
+// {64 dims, 1 head, 16 slots, 1 block} with 128-byte swizzle: one box is half
+// of a page of one KV head (16 rows x 128 bytes = 2 KB).
+bool pool_map(CUtensorMap *map, const pa_kv_pool *pool, void *base) {
+  const uint64_t hkv = (uint64_t)pool->num_kv_heads;
+  const uint64_t dims[4] = {(uint64_t)kHeadDim, hkv, (uint64_t)kBlock, (uint64_t)pool->num_blocks};
+  const uint64_t strides[3] = {kHeadDim * 2ull, hkv * kHeadDim * 2ull, kBlock * hkv * kHeadDim * 2ull};
+  const uint32_t box[4] = {64, 1, (uint32_t)kBlock, 1};
+  return encode_tensor_map(map, map_dtype(pool->dtype), 4, base, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+int sm_count() {
+  DeviceState *d = nullptr;
+  if (device_state(&d) != PA_OK) return 1;
+  return d->sm_count;
+}
+
+bool encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, int rank, void *base,
+                       const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                       CUtensorMapSwizzle swizzle) {
+  if (!g_encode) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, dtype, (cuuint32_t)rank, base, reinterpret_cast<const cuuint64_t *>(dims),
+                        reinterpret_cast<const cuuint64_t *>(strides_bytes),
+                        reinterpret_cast<const cuuint32_t *>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
+
+int32_t pa_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char *pa_status_string(int32_t status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_NULL: return "PA_ERR_NULL: a required pointer is NULL";
+    case PA_ERR_SHAPE: return "PA_ERR_SHAPE: a size is negative, inconsistent or over a limit";
+    case PA_ERR_DTYPE: return "PA_ERR_DTYPE: dtype must be PA_F16 or PA_BF16";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: head_dim 128, block 16 and head ratio 1/2/4/8 only";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: a CUDA call failed";
+    case PA_ERR_RANGE: return "PA_ERR_RANGE: block id, slot or length out of range";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded wait gave up";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: a pointer is not 16-byte aligned";
+    default: return "unknown pa_status";
+  }
+}
+
+pa_status pa_kv_cache_write(const void *k, const void *v, const int64_t *slot_mapping, int32_t num_tokens,
+                            const pa_kv_pool *pool, pa_stream_t stream) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping) return PA_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)) return PA_ERR_ALIGN;
+  DeviceState *d = nullptr;
+  if ((st = device_state(&d)) != PA_OK) return st;
+  WriteParams p;
+  p.k = k;
+  p.v = v;
+  p.slots = slot_mapping;
+  p.k_cache = pool->k_cache;
+  p.v_cache = pool->v_cache;
+  p.num_slots = (int64_t)pool->num_blocks * kBlock;
+  p.num_tokens = num_tokens;
+  p.row_vecs = pool->num_kv_heads * kHeadDim * 2 / 16;
+  p.err = d->err;
+  cudaError_t e = launch_kv_write(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t max_context_len) {
+  if (num_seqs < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0 ||
+      max_context_len < 0)
+    return 0;
+  return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads);
+}
+
+pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                               int32_t num_q_heads, int32_t max_context_len, float scale, void *out,
+                               void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0) return PA_ERR_SHAPE;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  if (!workspace) return PA_ERR_WORKSPACE;
+  int group = 0;
+  if ((st = check_group(num_q_heads, pool->num_kv_heads, &group)) != PA_OK) return st;
+  if (max_blocks_per_seq < 1 || max_context_len < 1 ||
+      (int64_t)max_context_len > (int64_t)max_blocks_per_seq * kBlock)
+    return PA_ERR_SHAPE;
+  if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || !aligned4(block_tables) ||
+      !aligned4(context_lens))
+    return PA_ERR_ALIGN;
+  if (workspace_bytes < decode_workspace_bytes(num_seqs, num_q_heads, pool->num_kv_heads))
+    return PA_ERR_WORKSPACE;
+  DeviceState *d = nullptr;
+  if ((st = device_state(&d)) != PA_OK) return st;
+
+  DecodeParams p{};
+  if (!decode_workspace_carve(workspace, workspace_bytes, num_seqs, num_q_heads, pool->num_kv_heads, p))
+    return PA_ERR_WORKSPACE;
+  p.q = q;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.err = d->err;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_kv_heads = pool->num_kv_heads;
+  p.num_q_heads = num_q_heads;
+  p.num_blocks = pool->num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  CUtensorMap kmap, vmap;
+  if (!pool_map(&kmap, pool, pool->k_cache) || !pool_map(&vmap, pool, pool->v_cache)) return PA_ERR_CUDA;
+
+  // Upper bound on the pages of the call; aim for at least 4 pages per warp.
+  const int64_t pages_hint = (int64_t)num_seqs * pool->num_kv_heads * ((max_context_len + kBlock - 1) / kBlock);
+  int64_t workers = (pages_hint + 3) / 4;
+  if (workers > kDecodeMaxWorkers) workers = kDecodeMaxWorkers;
+  cudaError_t e = launch_decode(p, kmap, vmap, pool->dtype, group, (int)workers,
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts, const int32_t *chunk_lens,
+                                      const pa_kv_pool *pool, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      int32_t num_chunks, int32_t num_q_heads, int32_t total_q_tokens,
+                                      int32_t max_chunk_len, float scale, void *out, pa_stream_t stream) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  if (num_chunks < 0 || total_q_tokens < 0) return PA_ERR_SHAPE;
+  if (num_chunks == 0) return PA_OK;
+  if (!q || !chunk_starts || !chunk_lens || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  int group = 0;
+  if ((st = check_group(num_q_heads, pool->num_kv_heads, &group)) != PA_OK) return st;
+  if (max_chunk_len < 1 || max_chunk_len > PA_MAX_CHUNK_LEN || max_blocks_per_seq < 1) return PA_ERR_SHAPE;
+  if (total_q_tokens < 1) return PA_ERR_SHAPE;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(block_tables) || !aligned4(context_lens) ||
+      !aligned4(chunk_starts) || !aligned4(chunk_lens))
+    return PA_ERR_ALIGN;
+  DeviceState *d = nullptr;
+  if ((st = device_state(&d)) != PA_OK) return st;
+
+  PrefillParams p{};
+  p.q = q;
+  p.chunk_starts = chunk_starts;
+  p.chunk_lens = chunk_lens;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.err = d->err;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_chunks = num_chunks;
+  p.num_kv_heads = pool->num_kv_heads;
+  p.num_q_heads = num_q_heads;
+  p.num_blocks = pool->num_blocks;
+  p.total_q_tokens = total_q_tokens;
+  p.max_chunk_len = max_chunk_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  CUtensorMap kmap, vmap, qmap;
+  if (!pool_map(&kmap, pool, pool->k_cache) || !pool_map(&vmap, pool, pool->v_cache)) return PA_ERR_CUDA;
+  // q as a 3-D tensor {dim, query head, token}; boxes of {64 dims, G heads,
+  // 128/G tokens} give 128 rows (token-major, head-minor) of 128 bytes.
+  {
+    const uint64_t dims[3] = {(uint64_t)kHeadDim, (uint64_t)num_q_heads, (uint64_t)total_q_tokens};
+    const uint64_t strides[2] = {kHeadDim * 2ull, (uint64_t)num_q_heads * kHeadDim * 2ull};
+    const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)(128 / group)};
+    if (!encode_tensor_map(&qmap, map_dtype(pool->dtype), 3, const_cast<void *>(q), dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return PA_ERR_CUDA;
+  }
+  cudaError_t e = launch_prefill(p, kmap, vmap, qmap, pool->dtype, group, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_get_device_error(pa_stream_t stream, int32_t *detail) {
+  DeviceState *d = nullptr;
+  pa_status st = device_state(&d);
+  if (st != PA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host[2] = {0, 0};
+  cudaError_t e = cudaMemcpyAsync(host, d->err, sizeof(host), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d->err, 0, sizeof(host), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (detail) *detail = host[1];
+  return static_cast<pa_status>(host[0]);
+}
+
+}  // extern "C"

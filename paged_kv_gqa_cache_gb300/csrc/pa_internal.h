@@ -1,0 +1,96 @@
+// Internal interface between the C-ABI layer (pa_abi.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedattn.h"
+
+namespace pa {
+
+// Every bounded wait gives up after this long (then PA_ERR_TIMEOUT).
+constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+constexpr int kHeadDim = 128;
+constexpr int kBlock = 16;
+
+// ---- kv_cache_write ------------------------------------------------------------
+struct WriteParams {
+  const void *k;
+  const void *v;
+  const int64_t *slots;
+  void *k_cache;
+  void *v_cache;
+  int64_t num_slots;   // num_blocks * 16
+  int32_t num_tokens;
+  int32_t row_vecs;    // 16-byte vectors per token row = Hkv * 128 * 2 / 16
+  int *err;
+};
+cudaError_t launch_kv_write(const WriteParams &p, cudaStream_t stream);
+
+// ---- decode (split-K over a balanced page range per warp) -----------------------
+constexpr int kDecodeWarps = 4;         // warps per CTA; each warp is an independent worker
+constexpr int kDecodeMaxWorkers = 8192; // upper bound on workers (warps) per launch
+constexpr int kDecodeStageBytes = 8192; // one 16-token page of K and V for one KV head
+
+struct DecodeParams {
+  const void *q;             // [S][Hq][128]
+  const int32_t *block_tables;
+  const int32_t *context_lens;
+  void *out;                 // [S][Hq][128]
+  int32_t *meta;             // workspace: page prefix over sequences [S + 1]
+  float *ws_ml;              // workspace: (m, l) per partial slot and head of the group
+  float *ws_o;               // workspace: o[128] per partial slot and head of the group
+  int *err;
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t num_kv_heads;
+  int32_t num_q_heads;
+  int32_t num_blocks;
+  int32_t num_workers;       // warps in the launch
+  float scale_log2;          // scale * log2(e)
+};
+
+struct DecodeLaunch {
+  int grid;          // CTAs
+  int smem_bytes;    // dynamic shared memory per CTA
+};
+
+// Plans and launches the split and combine kernels.  `group` = Hq / Hkv.
+cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                          int dtype, int group, int max_workers, cudaStream_t stream);
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads);
+// Carves the workspace into meta / ml / o; returns false if it is too small.
+bool decode_workspace_carve(void *ws, size_t bytes, int num_seqs, int num_q_heads, int num_kv_heads,
+                            DecodeParams &p);
+
+// ---- chunked prefill (tcgen05 tensor cores) -------------------------------------
+struct PrefillParams {
+  const void *q;             // [rows][Hq][128]
+  const int32_t *chunk_starts;
+  const int32_t *chunk_lens;
+  const int32_t *block_tables;
+  const int32_t *context_lens;
+  void *out;
+  int *err;
+  int32_t max_blocks_per_seq;
+  int32_t num_chunks;
+  int32_t num_kv_heads;
+  int32_t num_q_heads;
+  int32_t num_blocks;
+  int32_t total_q_tokens;
+  int32_t max_chunk_len;
+  float scale_log2;
+};
+cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                           const CUtensorMap &qmap, int dtype, int group, cudaStream_t stream);
+
+// ---- shared host helpers (pa_abi.cu) ------------------------------------------
+int sm_count();
+bool encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, int rank, void *base,
+                       const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                       CUtensorMapSwizzle swizzle);
+
+}  // namespace pa

@@ -1,0 +1,132 @@
+"""Host-side checks of the C-ABI (no GPU needed): the library loads, exports
+every entry point include/pagedattn.h declares, and rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_gqa_cache_gb300 as pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_gqa_cache_gb300 import _build
+    _build.build()
+    return pa.load_library()
+
+
+def declared_entry_points():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]*?\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls_and_helpers():
+    names = declared_entry_points()
+    for n in ("pa_kv_cache_write", "pa_paged_attn_decode", "pa_paged_attn_prefill_chunk",
+              "pa_decode_workspace_bytes", "pa_get_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_entry_points():
+        assert hasattr(lib, name), f"{name} declared in pagedattn.h but not exported"
+    assert set(pa.EXPORTS) <= set(declared_entry_points())
+
+
+def test_only_c_entry_points_are_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", pa.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {s for s in exported if s.startswith("pa_")}
+    assert ours == set(declared_entry_points())
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.pa_abi_version() == 1
+    for code in range(0, -10, -1):
+        assert lib.pa_status_string(code).decode().startswith(pa.STATUS[code])
+
+
+def _pool(**kw):
+    d = dict(k_cache=4096, v_cache=8192, num_blocks=64, block_size=16, num_kv_heads=8, head_dim=128, dtype=0)
+    d.update(kw)
+    return pa.KVPool(**d)
+
+
+P = 1 << 20  # a fake, 16-byte aligned "device" address; never dereferenced by these calls
+
+
+@pytest.mark.parametrize("pool,expected", [
+    (None, -1),
+    (_pool(k_cache=0), -1),
+    (_pool(dtype=7), -3),
+    (_pool(block_size=32), -4),
+    (_pool(head_dim=64), -4),
+    (_pool(num_blocks=0), -2),
+    (_pool(k_cache=4100), -9),
+])
+def test_write_rejects_bad_pools(lib, pool, expected):
+    ref = ctypes.byref(pool) if pool is not None else None
+    assert lib.pa_kv_cache_write(P, P, P, 4, ref, None) == expected
+
+
+def test_write_rejects_bad_arguments(lib):
+    pool = _pool()
+    assert lib.pa_kv_cache_write(P, P, P, -1, ctypes.byref(pool), None) == -2
+    assert lib.pa_kv_cache_write(P, P, P, 0, ctypes.byref(pool), None) == 0      # empty: no-op
+    assert lib.pa_kv_cache_write(0, P, P, 4, ctypes.byref(pool), None) == -1
+    assert lib.pa_kv_cache_write(P + 8, P, P, 4, ctypes.byref(pool), None) == -9
+    assert lib.pa_kv_cache_write(P, P, P + 4, 4, ctypes.byref(pool), None) == -9
+
+
+def test_decode_rejects_bad_arguments(lib):
+    pool = _pool()
+    ws = lib.pa_decode_workspace_bytes(4, 16, 8, 256)
+    call = lambda **kw: lib.pa_paged_attn_decode(
+        kw.get("q", P), ctypes.byref(kw.get("pool", pool)), kw.get("bt", P), kw.get("mb", 16), kw.get("ctx", P),
+        kw.get("S", 4), kw.get("hq", 16), kw.get("mcl", 256), kw.get("scale", 0.088), kw.get("out", P),
+        kw.get("ws", P), kw.get("wsb", ws), None)
+    assert call(S=0) == 0
+    assert call(S=-1) == -2
+    assert call(q=0) == -1
+    assert call(ws=0) == -5
+    assert call(wsb=ws - 1) == -5       # checked before any CUDA call
+    assert call(hq=12) == -2            # 12 % 8 != 0
+    assert call(hq=24) == -4            # group of 3
+    assert call(pool=_pool(num_kv_heads=2), hq=32) == -4      # group of 16
+    assert call(mcl=300) == -2          # beyond the block table (16 * 16)
+    assert call(mcl=0) == -2
+    assert call(scale=float("nan")) == -2
+    assert call(scale=0.0) == -2
+    assert call(out=P + 2) == -9
+    assert call(bt=P + 2) == -9
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    pool = _pool()
+    call = lambda **kw: lib.pa_paged_attn_prefill_chunk(
+        kw.get("q", P), kw.get("cs", P), kw.get("cl", P), ctypes.byref(kw.get("pool", pool)), kw.get("bt", P),
+        kw.get("mb", 128), kw.get("ctx", P), kw.get("C", 3), kw.get("hq", 16), kw.get("T", 1536),
+        kw.get("mcl", 512), kw.get("scale", 0.088), kw.get("out", P), None)
+    assert call(C=0) == 0
+    assert call(C=-1) == -2
+    assert call(mcl=513) == -2          # chunks are at most 512 tokens
+    assert call(mcl=0) == -2
+    assert call(cs=0) == -1
+    assert call(hq=20) == -2
+    assert call(T=0) == -2
+    assert call(q=P + 8) == -9
+    assert call(pool=_pool(dtype=2)) == -3
+
+
+def test_workspace_size_is_pure_host_and_monotone(lib):
+    a = lib.pa_decode_workspace_bytes(8, 16, 8, 1024)
+    b = lib.pa_decode_workspace_bytes(64, 32, 8, 4096)
+    assert 0 < a < b
+    assert lib.pa_decode_workspace_bytes(8, 12, 8, 1024) == 0
+    assert lib.pa_decode_workspace_bytes(-1, 16, 8, 1024) == 0
