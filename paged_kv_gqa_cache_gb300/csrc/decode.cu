@@ -148,11 +148,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     for (int i = threadIdx.x; i <= p.num_seqs; i += NW * 32) p.meta[i] = prefix[i];
 
   const int n = p.num_seqs, hkv = p.num_kv_heads;
+  // With fewer pages than warps only the first P warps work, one page each,
+  // so every working warp's range is non-empty (the combine relies on it).
   const int64_t P = (int64_t)prefix[n] * hkv;
+  const int64_t W = P < p.num_workers ? P : p.num_workers;
   const int w = blockIdx.x * NW + warp;
-  const int64_t x0 = (int64_t)w * P / p.num_workers;
-  const int64_t x1 = (int64_t)(w + 1) * P / p.num_workers;
-  if (x0 >= x1) return;
+  if (w >= W) return;
+  const int64_t x0 = (int64_t)w * P / W;
+  const int64_t x1 = (int64_t)(w + 1) * P / W;
   const int64_t npages = x1 - x0;
 
   // lane roles
@@ -367,8 +370,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   }
 }
 
-// Warp of the launch whose page range contains global page x.
-__device__ __forceinline__ int worker_of(int64_t x, int64_t P, int W) {
+// Warp of the launch whose page range contains global page x, when W warps
+// (W <= P) split P pages as [floor(w P / W), floor((w + 1) P / W)).
+__device__ __forceinline__ int worker_of(int64_t x, int64_t P, int64_t W) {
   const int64_t w = ((x + 1) * W + P - 1) / P - 1;
   return (int)(w < W - 1 ? w : W - 1);
 }
@@ -385,8 +389,9 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   const int pages = p.meta[s + 1] - p.meta[s];
   if (pages == 0) return;
   const int64_t P = (int64_t)p.meta[p.num_seqs] * hkv;
+  const int64_t W = P < p.num_workers ? P : p.num_workers;
   const int64_t A = (int64_t)hkv * p.meta[s] + (int64_t)h * pages;
-  const int wf = worker_of(A, P, p.num_workers), wl = worker_of(A + pages - 1, P, p.num_workers);
+  const int wf = worker_of(A, P, W), wl = worker_of(A + pages - 1, P, W);
   if (wf == wl) return;  // the split kernel wrote this output directly
   const int item = s * hkv + h;
   float M = -INFINITY, L = 0.f;
