@@ -54,6 +54,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
+                    help="2 = the Qwen3-0.6B 28-layer decode step (default); 3, 4, 5 = the mixed prefill "
+                         "step, the Qwen3-8B decode and the prefix-shared long tail (diagnostic lines)")
     return ap.parse_args(argv)
 
 
@@ -170,34 +173,54 @@ def committed_traffic(kernel_source: str, summary_name: str):
 
 # ---- the workload ----------------------------------------------------------------------------
 
-class DecodeStep:
-    """The Qwen3-0.6B 28-layer decode step on device-resident inputs."""
+WORKLOADS = {
+    2: ("Qwen3-0.6B decode step, 28 layers: 8 seqs, ctx U[512,1024], Hq=16, Hkv=8, d=128, fp16, "
+        "512-block pool per layer", 28, 28),
+    4: ("Qwen3-8B decode, 36 layers: 64 seqs x 4096 ctx, Hq=32, Hkv=8, d=128, bf16, 16384-block pool "
+        "(1 GiB K+V) per layer; 4 distinct pools cycled", 4, 36),
+    5: ("Prefix-shared long-tail decode, Qwen3-8B geometry: 32 seqs sharing 13 blocks + suffixes "
+        "log-U[16,32768], bf16; 4 distinct pools cycled over 8 calls", 4, 8),
+}
 
-    def __init__(self, device):
+
+class DecodeStep:
+    """A decode step on device-resident inputs: for each of `calls` layers,
+    kv_cache_write of the new tokens then paged_attn_decode (layer pools are
+    cycled when fewer distinct pools than calls are held)."""
+
+    def __init__(self, device, workload: int = 2):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
         self.pa = pa
-        self.case = workloads.config2(device=device, nan_fill=False)
+        self.workload = workload
+        self.desc, pools, self.L = WORKLOADS[workload]
+        maker = workloads.CONFIGS[workload]
+        self.case = maker(device=device, n_layers=pools, nan_fill=False)
         c = self.case
-        self.L = c.n_layers
         self.out = [torch.empty_like(q) for q in c.q]
         self.ws = pa.alloc_decode_workspace(c.q[0].shape[0], c.hq, c.hkv, c.max_context_len, device)
         lens = c.meta["decode_lens"]
         self.S = len(lens)
-        self.decode_bytes_layer = workloads.decode_kv_bytes(lens, c.hkv)
+        self.dtype = c.dtype
+        if c.meta.get("shared_prefix_blocks"):
+            shared_tokens = 16 * c.meta["shared_prefix_blocks"]
+            unique = sum(lens) - shared_tokens * (len(lens) - 1)
+            self.decode_bytes_layer = workloads.decode_kv_bytes(lens, c.hkv, unique_tokens=unique)
+        else:
+            self.decode_bytes_layer = workloads.decode_kv_bytes(lens, c.hkv)
         self.write_bytes_layer = 2 * c.k_new[0].numel() * 2 * 2     # K and V rows, read + write
         self.step_bytes = self.L * (self.decode_bytes_layer + self.write_bytes_layer)
         self.kernels_per_step = self.L * 3                          # write, split, combine
 
     def write(self, l):
-        c = self.case
-        self.pa.kv_cache_write(c.k_new[l], c.v_new[l], c.slot_mapping, c.k_cache[l], c.v_cache[l])
+        c, i = self.case, l % self.case.n_layers
+        self.pa.kv_cache_write(c.k_new[i], c.v_new[i], c.slot_mapping, c.k_cache[i], c.v_cache[i])
 
     def decode(self, l):
-        c = self.case
-        self.pa.paged_attn_decode(c.q[l], c.k_cache[l], c.v_cache[l], c.block_tables, c.context_lens, c.scale,
-                                  out=self.out[l], workspace=self.ws, max_context_len=c.max_context_len)
+        c, i = self.case, l % self.case.n_layers
+        self.pa.paged_attn_decode(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens, c.scale,
+                                  out=self.out[i], workspace=self.ws, max_context_len=c.max_context_len)
 
     def run(self):
         for l in range(self.L):
@@ -207,6 +230,45 @@ class DecodeStep:
     def run_decode_only(self):
         for l in range(self.L):
             self.decode(l)
+
+
+class MixedStep:
+    """The Qwen3-0.6B mixed chunked-prefill step (budget 2048): per layer,
+    kv_cache_write of 2048 new tokens, prefill of 3 chunks of 512 (prefixes 0,
+    512, 1536) and decode of 512 sequences; 2 distinct pools cycled over 28."""
+
+    def __init__(self, device):
+        import torch
+        import paged_kv_gqa_cache_gb300 as pa
+        import workloads
+        self.pa, self.L = pa, 28
+        self.case = c = workloads.config3(device=device, n_layers=2, nan_fill=False)
+        self.out_d = [torch.empty_like(q) for q in c.q]
+        self.out_p = [torch.empty_like(q) for q in c.q_chunks]
+        self.ws = pa.alloc_decode_workspace(c.q[0].shape[0], c.hq, c.hkv, c.max_context_len, device)
+        self.flops_layer = workloads.prefill_flops(c.meta["chunks"], c.hq)
+        self.decode_bytes_layer = workloads.decode_kv_bytes(c.meta["decode_lens"], c.hkv)
+        self.tokens = c.slot_mapping.numel()
+
+    def prefill(self, l):
+        c, i = self.case, l % 2
+        self.pa.paged_attn_prefill_chunk(c.q_chunks[i], c.chunk_starts, c.chunk_lens, c.k_cache[i], c.v_cache[i],
+                                         c.chunk_block_tables, c.chunk_context_lens, c.scale, out=self.out_p[i],
+                                         max_chunk_len=512)
+
+    def run(self):
+        c = self.case
+        for l in range(self.L):
+            i = l % 2
+            self.pa.kv_cache_write(c.k_new[i], c.v_new[i], c.slot_mapping, c.k_cache[i], c.v_cache[i])
+            self.prefill(l)
+            self.pa.paged_attn_decode(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
+                                      c.scale, out=self.out_d[i], workspace=self.ws,
+                                      max_context_len=c.max_context_len)
+
+    def run_prefill_only(self):
+        for l in range(self.L):
+            self.prefill(l)
 
 
 def graph_of(fn, reps: int, stream):
@@ -236,35 +298,36 @@ def time_replays(g, n: int, stream) -> float:
 
 
 def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream):
-    """Same metric through the public API with host buffers: per step, copy
-    q / new K,V / slots / tables / lengths from pinned host memory, run the 28
-    layers, read the outputs back to pinned host memory."""
+    """Same metric through the public API with host buffers: per step, for
+    each layer call copy q / new K,V from pinned host memory (and once per step
+    the slots, block tables and lengths), run write + decode, and read the
+    output back to pinned host memory."""
     import torch
     c = step.case
-    host_in = {
-        "q": [t.cpu().pin_memory() for t in c.q],
-        "k": [t.cpu().pin_memory() for t in c.k_new],
-        "v": [t.cpu().pin_memory() for t in c.v_new],
-        "slots": c.slot_mapping.cpu().pin_memory(),
-        "bt": c.block_tables.cpu().pin_memory(),
-        "ctx": c.context_lens.cpu().pin_memory(),
-    }
+    n = c.n_layers
+    host_q = [t.cpu().pin_memory() for t in c.q]
+    host_k = [t.cpu().pin_memory() for t in c.k_new]
+    host_v = [t.cpu().pin_memory() for t in c.v_new]
+    host_meta = [(c.slot_mapping, c.slot_mapping.cpu().pin_memory()),
+                 (c.block_tables, c.block_tables.cpu().pin_memory()),
+                 (c.context_lens, c.context_lens.cpu().pin_memory())]
     host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in step.out]
-    h2d = sum(t.numel() * t.element_size() for k in ("q", "k", "v") for t in host_in[k])
-    h2d += sum(host_in[k].numel() * host_in[k].element_size() for k in ("slots", "bt", "ctx"))
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    nbytes = lambda t: t.numel() * t.element_size()
+    h2d = sum(nbytes(host_q[l % n]) + nbytes(host_k[l % n]) + nbytes(host_v[l % n]) for l in range(step.L))
+    h2d += sum(nbytes(h) for _, h in host_meta)
+    d2h = sum(nbytes(host_out[l % n]) for l in range(step.L))
 
     def one():
+        for dev_t, host_t in host_meta:
+            dev_t.copy_(host_t, non_blocking=True)
         for l in range(step.L):
-            c.q[l].copy_(host_in["q"][l], non_blocking=True)
-            c.k_new[l].copy_(host_in["k"][l], non_blocking=True)
-            c.v_new[l].copy_(host_in["v"][l], non_blocking=True)
-        c.slot_mapping.copy_(host_in["slots"], non_blocking=True)
-        c.block_tables.copy_(host_in["bt"], non_blocking=True)
-        c.context_lens.copy_(host_in["ctx"], non_blocking=True)
-        step.run()
-        for l in range(step.L):
-            host_out[l].copy_(step.out[l], non_blocking=True)
+            i = l % n
+            c.q[i].copy_(host_q[i], non_blocking=True)
+            c.k_new[i].copy_(host_k[i], non_blocking=True)
+            c.v_new[i].copy_(host_v[i], non_blocking=True)
+            step.write(l)
+            step.decode(l)
+            host_out[i].copy_(step.out[i], non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -276,8 +339,7 @@ def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream):
             one()
         e1.record(stream)
         e1.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    return ms, h2d, d2h
+    return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
 def cpu_baseline(step: DecodeStep, seconds: float):
@@ -290,7 +352,7 @@ def cpu_baseline(step: DecodeStep, seconds: float):
     threads = os.cpu_count() or 1
     bt, ctx = c.block_tables.cpu().numpy(), c.context_lens.cpu().numpy()
     done_bytes, t_total, layers = 0, 0.0, 0
-    for l in range(step.L):
+    for l in range(c.n_layers):
         kh = c.k_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
         vh = c.v_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
         qh = c.q[l].cpu().view(torch.int16).numpy().view(np.uint16)
@@ -302,8 +364,14 @@ def cpu_baseline(step: DecodeStep, seconds: float):
         if t_total >= seconds:
             break
     return {"value": done_bytes / t_total / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{layers} of {step.L} decode layers of the workload (fp64 C oracle, "
+            "sample": f"{layers} decode layer call(s) of the workload (fp64 C oracle, "
                       f"{threads} threads), {t_total:.2f} s"}
+
+
+def _device_error_check(pa):
+    st, detail = pa.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {pa.STATUS.get(st, st)} at {detail}")
 
 
 def run_ours(args):
@@ -315,15 +383,14 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
     import paged_kv_gqa_cache_gb300 as pa
+    if args.workload == 3:
+        return run_mixed(args, dev, pa)
 
-    step = DecodeStep(dev)
+    step = DecodeStep(dev, args.workload)
     stream = torch.cuda.Stream(device=dev)
-    reps = 1
-    g_step = graph_of(step.run, reps, stream)
-    g_dec = graph_of(step.run_decode_only, reps, stream)
-    st, detail = pa.get_device_error()
-    if st != 0:
-        raise RuntimeError(f"device error {pa.STATUS.get(st, st)} at {detail}")
+    g_step = graph_of(step.run, 1, stream)
+    g_dec = graph_of(step.run_decode_only, 1, stream)
+    _device_error_check(pa)
 
     # warm-up, then K timed steps bracketed by barrier + synchronize
     time_replays(g_step, max(args.warmup, 3), stream)
@@ -333,8 +400,9 @@ def run_ours(args):
         ms_total = time_replays(g_step, args.steps, stream)
         torch.cuda.synchronize()
         barrier(dev)
-        # the dominant kernel alone: 28 decode calls per replay
-        ms_dec = time_replays(g_dec, max(args.steps // 2, 10), stream) / max(args.steps // 2, 10)
+        # the dominant kernel alone: the step's decode calls, back to back
+        n_dec = max(args.steps // 2, 10)
+        ms_dec = time_replays(g_dec, n_dec, stream) / n_dec
     ms_total = reduce_max(ms_total, dev)
     ms_step = ms_total / args.steps
     hbm, bf16, peak_kind = measured_peaks()
@@ -344,19 +412,17 @@ def run_ours(args):
     achieved = step.decode_bytes_layer / (dec_launch_ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = e2e_measure(step, max(args.steps // 20, 10), 3, stream)
     e2e_ms = reduce_max(e2e_ms, dev)
-    st, detail = pa.get_device_error()
-    if st != 0:
-        raise RuntimeError(f"device error {pa.STATUS.get(st, st)} at {detail}")
+    _device_error_check(pa)
 
+    pool_mib = 2 * step.case.k_cache[0].numel() * 2 / 2**20
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": "Qwen3-0.6B decode step, 28 layers: 8 seqs, ctx U[512,1024], Hq=16, Hkv=8, d=128, "
-                               "fp16, 512-block pool per layer",
-                   "global_batch": 8 * world, "seq_len": step.case.max_context_len,
+        "vs_baseline": None, "dtype": step.dtype, "data": "synthetic",
+        "config": {"workload": step.desc, "global_batch": step.S * world, "seq_len": step.case.max_context_len,
                    "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (28 x 32 MiB pools = 896 MiB streamed per step)",
+                   "l2": f"inputs larger than L2 ({step.case.n_layers} distinct pools of {pool_mib:.0f} MiB "
+                         f"cycled over {step.L} calls per step)",
                    "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
         "pct_of_hbm_peak": round(100.0 * value / world / hbm, 1),
         "tokens_per_s": round(world * step.S / (ms_step * 1e-3), 1),
@@ -367,11 +433,51 @@ def run_ours(args):
                      "frac": round(achieved / hbm, 3), "peak_kind": peak_kind,
                      "kernel": "paged_attn_decode (split + combine) per layer",
                      "bytes_per_launch": step.decode_bytes_layer, "launch_ms": round(dec_launch_ms, 5),
-                     "traffic": committed_traffic("decode.cu", "decode_split_qwen3_0.6b_decode.md")},
+                     "traffic": committed_traffic("decode.cu", f"decode_split_workload{args.workload}.md")},
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(step, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_mixed(args, dev, pa):
+    """Diagnostic line for the mixed chunked-prefill step (28 layers)."""
+    import torch
+    rank, world, _ = dist_env()
+    step = MixedStep(dev)
+    stream = torch.cuda.Stream(device=dev)
+    g_step = graph_of(step.run, 1, stream)
+    g_pre = graph_of(step.run_prefill_only, 1, stream)
+    _device_error_check(pa)
+    time_replays(g_step, max(args.warmup, 3), stream)
+    barrier(dev)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        ms_step = time_replays(g_step, args.steps, stream) / args.steps
+        n_pre = max(args.steps // 2, 10)
+        ms_pre = time_replays(g_pre, n_pre, stream) / n_pre / step.L
+    ms_step = reduce_max(ms_step, dev)
+    _device_error_check(pa)
+    hbm, bf16, peak_kind = measured_peaks()
+    tflops = step.flops_layer / (ms_pre * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(world * step.tokens / (ms_step * 1e-3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "Qwen3-0.6B mixed chunked-prefill step, 28 layers: chunks (0,512), (512,512), "
+                               "(1536,512) + 512 decode seqs ctx U[16,1024], bf16; 2 distinct pools cycled",
+                   "global_batch": 515 * world, "parallelism": f"replicas x{world}",
+                   "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
+        "gpu_launches": 28 * 4 * args.steps,
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": bf16, "unit": "TFLOP/s",
+                     "frac": round(tflops / bf16, 3), "peak_kind": peak_kind,
+                     "kernel": "paged_attn_prefill_chunk per layer", "flops_per_launch": step.flops_layer,
+                     "launch_ms": round(ms_pre, 5),
+                     "traffic": committed_traffic("prefill.cu", "prefill_workload3.md")},
+        "clocks": clk.summary(),
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -143,6 +143,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
     fence_mbar_init();
   }
+  griddep_wait();
   scan_pages(p, prefix, warp_tot);
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i <= p.num_seqs; i += NW * 32) p.meta[i] = prefix[i];
@@ -153,7 +154,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int64_t P = (int64_t)prefix[n] * hkv;
   const int64_t W = P < p.num_workers ? P : p.num_workers;
   const int w = blockIdx.x * NW + warp;
-  if (w >= W) return;
+  if (w >= W) {
+    griddep_launch_dependents();
+    return;
+  }
   const int64_t x0 = (int64_t)w * P / W;
   const int64_t x1 = (int64_t)(w + 1) * P / W;
   const int64_t npages = x1 - x0;
@@ -368,6 +372,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     }
     advance(cc, prefix, n, hkv);
   }
+  griddep_launch_dependents();
 }
 
 // Warp of the launch whose page range contains global page x, when W warps
@@ -379,43 +384,71 @@ __device__ __forceinline__ int worker_of(int64_t x, int64_t P, int64_t W) {
 
 // Log-sum-exp merge of the fragments of every item a single warp did not finish.
 // One warp per (sequence, query head); lane owns dims [4 * lane, 4 * lane + 4).
+// The (m, l) of up to 32 fragments are read at once (one per lane); the o
+// partials are then streamed with independent loads.
 template <typename T, int G>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+  griddep_wait();
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (gw >= p.num_seqs * p.num_q_heads) return;
-  const int s = gw / p.num_q_heads, qh = gw % p.num_q_heads;
-  const int h = qh / G, gg = qh % G;
-  const int hkv = p.num_kv_heads;
-  const int pages = p.meta[s + 1] - p.meta[s];
-  if (pages == 0) return;
-  const int64_t P = (int64_t)p.meta[p.num_seqs] * hkv;
-  const int64_t W = P < p.num_workers ? P : p.num_workers;
-  const int64_t A = (int64_t)hkv * p.meta[s] + (int64_t)h * pages;
-  const int wf = worker_of(A, P, W), wl = worker_of(A + pages - 1, P, W);
-  if (wf == wl) return;  // the split kernel wrote this output directly
-  const int item = s * hkv + h;
-  float M = -INFINITY, L = 0.f;
-  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int w = wf; w <= wl; ++w) {
-    const int64_t slot = ((int64_t)item + w) * G + gg;
-    const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + slot * 2);
-    if (!(ml.x > -INFINITY)) continue;  // a fragment with no valid page
-    const float4 ov = *reinterpret_cast<const float4 *>(p.ws_o + slot * kHeadDim + 4 * lane);
-    const float Mn = fmaxf(M, ml.x);
-    const float a = exp2f(M - Mn), b = exp2f(ml.x - Mn);
-    L = L * a + ml.y * b;
-    O.x = O.x * a + ov.x * b;
-    O.y = O.y * a + ov.y * b;
-    O.z = O.z * a + ov.z * b;
-    O.w = O.w * a + ov.w * b;
-    M = Mn;
+  if (gw < p.num_seqs * p.num_q_heads) {
+    const int s = gw / p.num_q_heads, qh = gw % p.num_q_heads;
+    const int h = qh / G, gg = qh % G;
+    const int hkv = p.num_kv_heads;
+    const int pages = p.meta[s + 1] - p.meta[s];
+    const int64_t P = (int64_t)p.meta[p.num_seqs] * hkv;
+    const int64_t W = P < p.num_workers ? P : p.num_workers;
+    const int64_t A = (int64_t)hkv * p.meta[s] + (int64_t)h * pages;
+    const int wf = pages ? worker_of(A, P, W) : 0;
+    const int wl = pages ? worker_of(A + pages - 1, P, W) : 0;
+    if (pages != 0 && wf != wl) {  // otherwise the split kernel wrote this output directly
+      const int64_t slot0 = (int64_t)s * hkv + h + wf;
+      const int nf = wl - wf + 1;
+      float M = -INFINITY, L = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int base = 0; base < nf; base += 32) {
+        const int f = base + lane;
+        float mf = -INFINITY, lf = 0.f;
+        if (f < nf) {
+          const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + ((slot0 + f) * G + gg) * 2);
+          mf = ml.x;
+          lf = ml.y;
+        }
+        float mc = mf;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(FULL, mc, off));
+        const float Mn = fmaxf(M, mc);
+        if (Mn == -INFINITY) continue;  // no valid fragment yet (uniform)
+        const float so = exp2f(M - Mn);
+        const float wgt = (mf > -INFINITY) ? exp2f(mf - Mn) : 0.f;
+        float lw = lf * wgt;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(FULL, lw, off);
+        L = L * so + lw;
+        O.x *= so; O.y *= so; O.z *= so; O.w *= so;
+        M = Mn;
+        const int cnt = min(32, nf - base);
+#pragma unroll 4
+        for (int j = 0; j < cnt; ++j) {
+          const float wj = __shfl_sync(FULL, wgt, j);
+          const float4 ov =
+              *reinterpret_cast<const float4 *>(p.ws_o + ((slot0 + base + j) * G + gg) * kHeadDim + 4 * lane);
+          if (wj > 0.f) {
+            O.x = fmaf(wj, ov.x, O.x);
+            O.y = fmaf(wj, ov.y, O.y);
+            O.z = fmaf(wj, ov.z, O.z);
+            O.w = fmaf(wj, ov.w, O.w);
+          }
+        }
+      }
+      const float inv = 1.f / L;
+      T *op = reinterpret_cast<T *>(p.out) + ((int64_t)s * p.num_q_heads + qh) * kHeadDim + 4 * lane;
+      uint2 pk;
+      pk.x = Pack<T>::from_f2(O.x * inv, O.y * inv);
+      pk.y = Pack<T>::from_f2(O.z * inv, O.w * inv);
+      *reinterpret_cast<uint2 *>(op) = pk;
+    }
   }
-  const float inv = 1.f / L;
-  T *op = reinterpret_cast<T *>(p.out) + ((int64_t)s * p.num_q_heads + qh) * kHeadDim + 4 * lane;
-  uint2 pk;
-  pk.x = Pack<T>::from_f2(O.x * inv, O.y * inv);
-  pk.y = Pack<T>::from_f2(O.z * inv, O.w * inv);
-  *reinterpret_cast<uint2 *>(op) = pk;
+  griddep_launch_dependents();
 }
 
 int split_smem_bytes(int group, int num_seqs) {
@@ -450,12 +483,10 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
   if (grid < 1) grid = 1;
   if (grid * NW > kDecodeMaxWorkers) grid = kDecodeMaxWorkers / NW;
   p.num_workers = grid * NW;
-  decode_split_kernel<T, G><<<grid, NW * 32, smem, stream>>>(kmap, vmap, p);
-  e = cudaGetLastError();
+  e = launch_pdl(decode_split_kernel<T, G>, dim3(grid), dim3(NW * 32), smem, stream, kmap, vmap, p);
   if (e != cudaSuccess) return e;
   const int cgrid = (p.num_seqs * p.num_q_heads + 3) / 4;
-  decode_combine_kernel<T, G><<<cgrid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_combine_kernel<T, G>, dim3(cgrid), dim3(128), 0, stream, p);
 }
 
 }  // namespace

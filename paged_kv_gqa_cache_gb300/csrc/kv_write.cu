@@ -13,6 +13,7 @@ namespace pa {
 namespace {
 
 __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
+  griddep_wait();
   const int64_t total = (int64_t)p.num_tokens * p.row_vecs;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
@@ -28,6 +29,7 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
     st_v4(static_cast<uint4 *>(p.k_cache) + slot * p.row_vecs + vi, kv);
     st_v4(static_cast<uint4 *>(p.v_cache) + slot * p.row_vecs + vi, vv);
   }
+  griddep_launch_dependents();
 }
 
 }  // namespace
@@ -38,8 +40,7 @@ cudaError_t launch_kv_write(const WriteParams &p, cudaStream_t stream) {
   const int64_t cap = (int64_t)sm_count() * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  kv_write_kernel<<<(int)grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kv_write_kernel, dim3((unsigned)grid), dim3(256), 0, stream, p);
 }
 
 }  // namespace pa

@@ -22,6 +22,17 @@ __device__ __forceinline__ void set_error(int *err, int code, int detail) {
   if (atomicCAS(err, 0, code) == 0) atomicExch(err + 1, detail);
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may start while the previous kernel in the stream is
+// finishing, and waits here, before its first read of global memory, until
+// that kernel has completed and its writes are visible.  It lets the next
+// kernel launch once all of its CTAs have passed `griddep_launch_dependents`.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- address helpers --------------------------------------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

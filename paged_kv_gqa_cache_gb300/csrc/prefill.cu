@@ -18,8 +18,11 @@
 //   S  = Q K^T   tcgen05.mma kind::f16, A and B K-major, fp32 in TMEM (S0/S1)
 //   softmax      warps 0-3 (thread r owns TMEM lane r = row r): masked row
 //                max, P = exp2(S * scale * log2 e - m), row sums; P is written
-//                to shared memory in the input dtype (K-major, 128-byte swizzle)
-//   O_t = P V    tcgen05.mma, B = V tile MN-major, fp32 in TMEM (O0/O1)
+//                to shared memory as two terms in the input dtype, P_hi =
+//                round(P) and P_lo = round(P - P_hi) (K-major, 128-byte
+//                swizzle), so the tensor-core product sees P to ~16 bits
+//   O_t = P V    tcgen05.mma P_hi V + P_lo V, B = V tile MN-major, fp32 in
+//                TMEM (O0/O1)
 //   O  = O * alpha + O_t  accumulated in registers of the softmax threads.
 // Warp 4 issues the TMA loads, warp 5 owns TMEM and issues the MMAs (one
 // thread each); mbarriers hand tiles between the roles and every wait is
@@ -39,8 +42,8 @@ constexpr int kHalf = 16384;                      // 128 rows x 64 elements x 2 
 constexpr int OFF_Q = 0;                          // Q: two 64-dim halves
 constexpr int OFF_KV = 2 * kHalf;                 // 2 stages of {K lo, K hi, V lo, V hi}
 constexpr int STAGE_BYTES = 4 * kHalf;
-constexpr int OFF_P = OFF_KV + 2 * STAGE_BYTES;   // P: two 64-key halves
-constexpr int OFF_BAR = OFF_P + 2 * kHalf;
+constexpr int OFF_P = OFF_KV + 2 * STAGE_BYTES;   // P_hi then P_lo, each two 64-key halves
+constexpr int OFF_BAR = OFF_P + 4 * kHalf;
 constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;  // + barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;               // S0, S1, O0, O1: 128 columns each
 
@@ -79,6 +82,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars &bars = *reinterpret_cast<Bars *>(smem + OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();
 
   // Heaviest tiles first: last chunk, last query tile.
   const int c = p.num_chunks - 1 - (int)blockIdx.z;
@@ -91,10 +95,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                    ctx > p.max_blocks_per_seq * kBlock || row0 + len > p.total_q_tokens;
   if (bad) {
     if (mt == 0 && h == 0 && threadIdx.x == 0) set_error(p.err, PA_ERR_RANGE, c);
+    griddep_launch_dependents();
     return;
   }
   const int t0 = mt * TQ;
-  if (t0 >= len) return;
+  if (t0 >= len) {
+    griddep_launch_dependents();
+    return;
+  }
   const int last_key = min(start + t0 + TQ - 1, ctx - 1);  // largest key any row of the tile sees
   const int nkt = last_key / 128 + 1;
   const int kt_ctx = (ctx - 1) / 128;                       // key tile holding the sequence's last key
@@ -211,9 +219,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           tc::fence_after_sync();
           const uint32_t va = smem_u32(smem + OFF_KV + b * STAGE_BYTES + 2 * kHalf);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            tc::mma_f16(tmem + 256 + b * 128, tc::desc_sw128(pa_ + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024),
-                        tc::desc_sw128(va + kk * 2048, kHalf, 1024), IDESC_O, kk > 0);
+          for (int kk = 0; kk < 16; ++kk) {  // P_hi (kk < 8), then P_lo, against the same V
+            const uint32_t aoff = (kk >> 3) * 2 * kHalf + ((kk >> 2) & 1) * kHalf + (kk & 3) * 32;
+            tc::mma_f16(tmem + 256 + b * 128, tc::desc_sw128(pa_ + aoff, 16, 1024),
+                        tc::desc_sw128(va + (kk & 7) * 2048, kHalf, 1024), IDESC_O, kk > 0);
           }
           tc::commit(&bars.pv_done[b]);
         }
@@ -272,20 +281,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         uint32_t v[32];
         tc::ld_32x32b_x32(s_addr + cch * 32, v);
         tc::wait_ld();
-        uint32_t pk[16];
+        uint32_t hi[16], lo[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const int key = kbase + cch * 32 + j;
           const float p0 = (key <= lim) ? exp2f(fmaf(__uint_as_float(v[j]), sl2, -m_new)) : 0.f;
           const float p1 = (key + 1 <= lim) ? exp2f(fmaf(__uint_as_float(v[j + 1]), sl2, -m_new)) : 0.f;
           ls += p0 + p1;
-          pk[j >> 1] = Pack<T>::from_f2(p0, p1);
+          hi[j >> 1] = Pack<T>::from_f2(p0, p1);
+          const float2 h2 = Pack<T>::to_f2(hi[j >> 1]);
+          lo[j >> 1] = Pack<T>::from_f2(p0 - h2.x, p1 - h2.y);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int q = cch * 4 + i, half = q >> 3, cc = q & 7;
-          *reinterpret_cast<uint4 *>(prow + half * kHalf + ((cc ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          uint8_t *dst = prow + half * kHalf + ((cc ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
+          *reinterpret_cast<uint4 *>(dst + 2 * kHalf) =
+              make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
         }
       }
       l_run = l_run * a_new + ls;
@@ -343,6 +356,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  griddep_launch_dependents();
 }
 
 template <typename T, int G>
@@ -357,8 +371,7 @@ cudaError_t launch_typed(const PrefillParams &p, const CUtensorMap &kmap, const 
   }
   constexpr int TQ = 128 / G;
   dim3 grid((p.max_chunk_len + TQ - 1) / TQ, p.num_kv_heads, p.num_chunks);
-  prefill_kernel<T, G><<<grid, kThreads, SMEM_BYTES, stream>>>(kmap, vmap, qmap, p);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel<T, G>, grid, dim3(kThreads), SMEM_BYTES, stream, kmap, vmap, qmap, p);
 }
 
 }  // namespace

@@ -1,0 +1,65 @@
+"""Host-side pieces of bench.py: argument defaults, the peak-file reader, the
+committed-traffic lookup, and the multi-rank plumbing (max over ranks and the
+barrier) on world_size 2 with the gloo backend on CPU."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_default_arguments_are_one_gpu_and_the_decode_step():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.workload == 2 and a.impl == "ours" and a.warmup >= 3 and a.steps > 0
+
+
+def test_peaks_come_from_the_measured_file_or_the_fallback():
+    hbm, bf16, kind = bench.measured_peaks()
+    assert hbm > 1000 and bf16 > 100 and kind in ("measured", "fallback")
+
+
+def test_committed_traffic_is_ignored_when_the_kernel_changed(tmp_path, monkeypatch):
+    assert bench.committed_traffic("decode.cu", "no_such_summary.md") is None
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    r, w = bench.dist_init("gloo")
+    assert (r, w) == (rank, world)
+    bench.barrier()
+    got = bench.reduce_max(float(10 * rank + 1))
+    q.put((rank, got))
+    bench.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res == {0: 11.0, 1: 11.0}
+
+
+def test_reduce_max_without_a_process_group_is_the_identity():
+    assert not dist.is_initialized()
+    assert bench.reduce_max(3.5) == 3.5
