@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pools", type=int, default=0,
+                    help="distinct layer pools held on the device (0 = the workload's default)")
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
                     help="2 = the Qwen3-0.6B 28-layer decode step (default); 3, 4, 5 = the mixed prefill "
                          "step, the Qwen3-8B decode and the prefix-shared long tail (diagnostic lines)")
@@ -188,13 +190,14 @@ class DecodeStep:
     kv_cache_write of the new tokens then paged_attn_decode (layer pools are
     cycled when fewer distinct pools than calls are held)."""
 
-    def __init__(self, device, workload: int = 2):
+    def __init__(self, device, workload: int = 2, pools: int = 0):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
         self.pa = pa
         self.workload = workload
-        self.desc, pools, self.L = WORKLOADS[workload]
+        self.desc, default_pools, self.L = WORKLOADS[workload]
+        pools = pools or default_pools
         maker = workloads.CONFIGS[workload]
         self.case = maker(device=device, n_layers=pools, nan_fill=False)
         c = self.case
@@ -386,7 +389,7 @@ def run_ours(args):
     if args.workload == 3:
         return run_mixed(args, dev, pa)
 
-    step = DecodeStep(dev, args.workload)
+    step = DecodeStep(dev, args.workload, args.pools)
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_dec = graph_of(step.run_decode_only, 1, stream)

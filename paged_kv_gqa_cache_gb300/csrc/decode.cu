@@ -131,8 +131,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t *stages = smem + warp * kStages * STAGE;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * kStages * STAGE) + warp * kStages;
-  float *pbuf = reinterpret_cast<float *>(smem + NW * kStages * STAGE + NW * kStages * 8) + warp * 16 * G;
-  int32_t *prefix = reinterpret_cast<int32_t *>(smem + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * G * 4);
+  float *pbuf = reinterpret_cast<float *>(smem + NW * kStages * STAGE + NW * kStages * 8) + warp * 16 * G * 2;
+  int32_t *prefix = reinterpret_cast<int32_t *>(smem + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * G * 8);
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&kmap);
@@ -204,12 +204,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   for (int g = 0; g < npre; ++g) issue(g);
 
   // ---- consumer state ---------------------------------------------------------
-  float q[G][DPL];
-  float o[G][4];
+  // Packed fp32x2 arithmetic (FFMA2): q and the partial scores pair adjacent
+  // dims, the output accumulators pair adjacent dims of one head.
+  float2 q[G][DPL / 2];
+  float2 o[G][2];
   float m[G], l[G];
   int ctx = 0;
   bool open = false, whole = false;
   const float neg_inf = -INFINITY;
+  float2 *pbuf2 = reinterpret_cast<float2 *>(pbuf);  // [16 keys][G] of (p, p)
 
   for (int64_t g = 0; g < npages; ++g) {
     const int st = (int)(g % kStages);
@@ -226,14 +229,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 f = Pack<T>::to_f2(wd[e]);
-            q[gg][i * 8 + 2 * e] = f.x * p.scale_log2;
-            q[gg][i * 8 + 2 * e + 1] = f.y * p.scale_log2;
+            q[gg][i * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
           }
         }
         m[gg] = neg_inf;
         l[gg] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[gg][e] = 0.f;
+        o[gg][0] = make_float2(0.f, 0.f);
+        o[gg][1] = make_float2(0.f, 0.f);
       }
       ctx = __ldg(p.context_lens + cc.s);
       whole = (cc.page == 0);
@@ -258,9 +260,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 #pragma unroll
       for (int ps = 0; ps < NP; ++ps) {
         const int t = ps * NT + tk;
-        float acc[G];
+        float2 acc[G];
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) acc[gg] = 0.f;
+        for (int gg = 0; gg < G; ++gg) acc[gg] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
           const int cg = qd * CPL + i;
@@ -269,19 +271,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 f = Pack<T>::to_f2(wd[e]);
+            const float2 k2 = Pack<T>::to_f2(wd[e]);
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-              acc[gg] = fmaf(q[gg][i * 8 + 2 * e], f.x, acc[gg]);
-              acc[gg] = fmaf(q[gg][i * 8 + 2 * e + 1], f.y, acc[gg]);
-            }
+            for (int gg = 0; gg < G; ++gg) acc[gg] = __ffma2_rn(q[gg][i * 4 + e], k2, acc[gg]);
           }
         }
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
+          float a = acc[gg].x + acc[gg].y;
 #pragma unroll
-          for (int off = NT; off < 32; off <<= 1) acc[gg] += __shfl_xor_sync(FULL, acc[gg], off);
-          sc[ps][gg] = (t < nv) ? acc[gg] : neg_inf;
+          for (int off = NT; off < 32; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
+          sc[ps][gg] = (t < nv) ? a : neg_inf;
         }
       }
 
@@ -301,43 +301,43 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         for (int ps = 0; ps < NP; ++ps) {
           const float pr = exp2f(sc[ps][gg] - mn);
           ls += pr;
-          if (qd == 0) pbuf[(ps * NT + tk) * G + gg] = pr;
+          if (qd == 0) pbuf2[(ps * NT + tk) * G + gg] = make_float2(pr, pr);
         }
         l[gg] = l[gg] * alpha + ls;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[gg][e] *= alpha;
+        const float2 a2 = make_float2(alpha, alpha);
+        o[gg][0] = __fmul2_rn(o[gg][0], a2);
+        o[gg][1] = __fmul2_rn(o[gg][1], a2);
       }
       __syncwarp();
 
       // weighted sum of values: this lane owns dims [4 * lane, 4 * lane + 4)
       const int vh = lane >> 4, vc = (lane & 15) >> 1, vsub = (lane & 1) * 8;
+      auto pv_token = [&](int t) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(vst + vh * 2048 + t * 128 + ((vc ^ (t & 7)) << 4) + vsub);
+        const float2 v01 = Pack<T>::to_f2(u.x);
+        const float2 v23 = Pack<T>::to_f2(u.y);
+        float2 pp[G];
+        if constexpr (G == 1) {
+          pp[0] = pbuf2[t];
+        } else {
 #pragma unroll
-      for (int t = 0; t < kBlock; ++t) {
-        if (t < nv) {
-          const uint2 u = *reinterpret_cast<const uint2 *>(vst + vh * 2048 + t * 128 + ((vc ^ (t & 7)) << 4) + vsub);
-          const float2 v01 = Pack<T>::to_f2(u.x);
-          const float2 v23 = Pack<T>::to_f2(u.y);
-          float pr[G];
-          if constexpr (G == 1) {
-            pr[0] = pbuf[t];
-          } else if constexpr (G == 2) {
-            const float2 x = *reinterpret_cast<const float2 *>(pbuf + t * 2);
-            pr[0] = x.x; pr[1] = x.y;
-          } else {
-#pragma unroll
-            for (int gg = 0; gg < G; gg += 4) {
-              const float4 x = *reinterpret_cast<const float4 *>(pbuf + t * G + gg);
-              pr[gg] = x.x; pr[gg + 1] = x.y; pr[gg + 2] = x.z; pr[gg + 3] = x.w;
-            }
-          }
-#pragma unroll
-          for (int gg = 0; gg < G; ++gg) {
-            o[gg][0] = fmaf(pr[gg], v01.x, o[gg][0]);
-            o[gg][1] = fmaf(pr[gg], v01.y, o[gg][1]);
-            o[gg][2] = fmaf(pr[gg], v23.x, o[gg][2]);
-            o[gg][3] = fmaf(pr[gg], v23.y, o[gg][3]);
+          for (int gg = 0; gg < G; gg += 2) {
+            const float4 x = *reinterpret_cast<const float4 *>(pbuf2 + t * G + gg);
+            pp[gg] = make_float2(x.x, x.y);
+            pp[gg + 1] = make_float2(x.z, x.w);
           }
         }
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          o[gg][0] = __ffma2_rn(pp[gg], v01, o[gg][0]);
+          o[gg][1] = __ffma2_rn(pp[gg], v23, o[gg][1]);
+        }
+      };
+      if (nv == kBlock) {
+#pragma unroll
+        for (int t = 0; t < kBlock; ++t) pv_token(t);
+      } else {
+        for (int t = 0; t < nv; ++t) pv_token(t);
       }
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
@@ -358,13 +358,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           T *op = reinterpret_cast<T *>(p.out) +
                   ((int64_t)cc.s * p.num_q_heads + cc.h * G + gg) * kHeadDim + 4 * lane;
           uint2 pk;
-          pk.x = Pack<T>::from_f2(o[gg][0] * inv, o[gg][1] * inv);
-          pk.y = Pack<T>::from_f2(o[gg][2] * inv, o[gg][3] * inv);
+          pk.x = Pack<T>::from_f2(o[gg][0].x * inv, o[gg][0].y * inv);
+          pk.y = Pack<T>::from_f2(o[gg][1].x * inv, o[gg][1].y * inv);
           *reinterpret_cast<uint2 *>(op) = pk;
         } else {
           const int64_t slot = ((int64_t)item + w) * G + gg;
           *reinterpret_cast<float4 *>(p.ws_o + slot * kHeadDim + 4 * lane) =
-              make_float4(o[gg][0], o[gg][1], o[gg][2], o[gg][3]);
+              make_float4(o[gg][0].x, o[gg][0].y, o[gg][1].x, o[gg][1].y);
           if (lane == 0) *reinterpret_cast<float2 *>(p.ws_ml + slot * 2) = make_float2(m[gg], lt);
         }
       }
@@ -427,16 +427,20 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
         O.x *= so; O.y *= so; O.z *= so; O.w *= so;
         M = Mn;
         const int cnt = min(32, nf - base);
-#pragma unroll 4
-        for (int j = 0; j < cnt; ++j) {
+        // issue every load of this chunk before using any of them
+        float4 ov[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < cnt)
+            ov[j] = *reinterpret_cast<const float4 *>(p.ws_o + ((slot0 + base + j) * G + gg) * kHeadDim + 4 * lane);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
           const float wj = __shfl_sync(FULL, wgt, j);
-          const float4 ov =
-              *reinterpret_cast<const float4 *>(p.ws_o + ((slot0 + base + j) * G + gg) * kHeadDim + 4 * lane);
-          if (wj > 0.f) {
-            O.x = fmaf(wj, ov.x, O.x);
-            O.y = fmaf(wj, ov.y, O.y);
-            O.z = fmaf(wj, ov.z, O.z);
-            O.w = fmaf(wj, ov.w, O.w);
+          if (j < cnt && wj > 0.f) {
+            O.x = fmaf(wj, ov[j].x, O.x);
+            O.y = fmaf(wj, ov[j].y, O.y);
+            O.z = fmaf(wj, ov[j].z, O.z);
+            O.w = fmaf(wj, ov[j].w, O.w);
           }
         }
       }
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
 }
 
 int split_smem_bytes(int group, int num_seqs) {
-  return 1024 + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * group * 4 + (num_seqs + 1) * 4;
+  return 1024 + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * group * 8 + (num_seqs + 1) * 4;
 }
 
 template <typename T, int G>

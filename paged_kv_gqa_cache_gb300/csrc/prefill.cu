@@ -166,8 +166,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         // A page whose block id is out of range is not loaded; zero it so the
         // products stay finite (the error word already reports the chunk).
         bool zeroed = false;
-        for (int j = 0; j < np; ++j) {
-          if (blk[j] >= 0) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j >= np || blk[j] >= 0) continue;
           for (int part = 0; part < 4; ++part) {
             uint4 *z = reinterpret_cast<uint4 *>(st + part * kHalf + j * 2048);
             for (int i = 0; i < 128; ++i) z[i] = make_uint4(0, 0, 0, 0);
