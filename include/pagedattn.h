@@ -132,6 +132,30 @@ PA_API pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, con
                                pa_stream_t stream);
 
 /*
+ * paged_attn_decode_noalloc — no counterpart on the pages: a library addition
+ * for callers that cannot allocate device memory or pass a workspace (a
+ * plugin inside a host application that owns all device memory, a serving
+ * step that must not allocate).  Same arguments and result as
+ * pa_paged_attn_decode without the workspace: the split-K scratch is one
+ * fixed array of PA_NOALLOC_SCRATCH_BYTES inside the library, held by every
+ * GPU that loads the library until the process exits.  A call whose
+ * pa_decode_workspace_bytes(...) exceeds PA_NOALLOC_SCRATCH_BYTES returns
+ * PA_ERR_WORKSPACE and enqueues nothing (with 8 KV heads this admits head
+ * ratios up to 4: e.g. up to ~7900 (sequence, KV head) pairs at ratio 4; a
+ * ratio of 8 never fits).  It calls no allocator.  The first call on a device
+ * (with that device current) looks up the array's device address once; make
+ * it before any stream capture.  All calls share the array, which keeps the
+ * last call's contents (nothing in it needs to start at zero); calls that
+ * overlap on the GPU race on it, so serialise them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+PA_API pa_status pa_paged_attn_decode_noalloc(const void *q, const pa_kv_pool *pool,
+                                              const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                              const int32_t *context_lens, int32_t num_seqs,
+                                              int32_t num_q_heads, int32_t max_context_len, float scale,
+                                              void *out, pa_stream_t stream);
+
+/*
  * paged_attn_prefill_chunk — [P1, qwen_serve/model.py, Qwen3Model.forward
  * with T > 1: causal mask kpos <= qpos on absolute positions; P2 section 3.4
  * and task 04.1]: chunk c has chunk_lens[c] new query tokens at absolute

@@ -33,7 +33,7 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_DTYPE",
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_decode",
            "pa_paged_attn_prefill_chunk", "pa_get_device_error", "pa_status_string",
-           "pa_last_cuda_error", "pa_abi_version")
+           "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc")
 
 
 class PagedAttnError(RuntimeError):
@@ -73,6 +73,8 @@ def load_library(path: str = LIB_PATH):
         lib.pa_paged_attn_decode.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P,
                                              ctypes.c_size_t, P]
         lib.pa_paged_attn_decode.restype = i32
+        lib.pa_paged_attn_decode_noalloc.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P]
+        lib.pa_paged_attn_decode_noalloc.restype = i32
         lib.pa_paged_attn_prefill_chunk.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
                                                     ctypes.c_float, P, P]
         lib.pa_paged_attn_prefill_chunk.restype = i32
@@ -185,6 +187,32 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                                     context_lens.data_ptr(), S, hq, mcl, float(scale), out.data_ptr(),
                                     workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                     _stream(stream)), "pa_paged_attn_decode")
+    return out
+
+
+def paged_attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                              out: Optional[torch.Tensor] = None, max_context_len: Optional[int] = None,
+                              stream=None) -> torch.Tensor:
+    """Decode attention for callers that cannot allocate device memory or pass
+    a workspace: the library's fixed scratch array stands in for it (see
+    include/pagedattn.h for its size limit and the set-up on first use).
+    ``out`` should be preallocated by such callers."""
+    pool = make_pool(k_cache, v_cache)
+    _need(q, "q", k_cache.dtype)
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    S, hq, d = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks], context_lens [S]")
+    mb = block_tables.shape[1]
+    mcl = int(max_context_len) if max_context_len is not None else mb * pool.block_size
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype)
+    _check(load_library().pa_paged_attn_decode_noalloc(
+        q.data_ptr(), ctypes.byref(pool), block_tables.data_ptr(), mb, context_lens.data_ptr(), S, hq, mcl,
+        float(scale), out.data_ptr(), _stream(stream)), "pa_paged_attn_decode_noalloc")
     return out
 
 
