@@ -13,21 +13,28 @@
 // consecutive tokens of the chunk x the G query heads sharing that KV head,
 // so every K/V tile it reads serves all G heads.  Row r of the tile is token
 // t0 + r / G, head h * G + r % G (the Q tile is one TMA box per 64-dim half).
-// The keys stream in tiles of N = 128 (8 pages, each page one TMA box per
-// 64-dim half), double-buffered.  Per key tile:
-//   S  = Q K^T   tcgen05.mma kind::f16, A and B K-major, fp32 in TMEM (S0/S1)
-//   softmax      warps 0-3 (thread r owns TMEM lane r = row r): masked row
-//                max, P = exp2(S * scale * log2 e - m), row sums; P is written
-//                to shared memory as two terms in the input dtype, P_hi =
-//                round(P) and P_lo = round(P - P_hi) (K-major, 128-byte
-//                swizzle), so the tensor-core product sees P to ~16 bits
-//   O_t = P V    tcgen05.mma P_hi V + P_lo V, B = V tile MN-major, fp32 in
-//                TMEM (O0/O1)
-//   O  = O * alpha + O_t  accumulated in registers of the softmax threads.
-// Warp 4 issues the TMA loads, warp 5 owns TMEM and issues the MMAs (one
-// thread each); mbarriers hand tiles between the roles and every wait is
-// bounded.  Keys above the diagonal are masked per element on the tiles that
-// cross it and never loaded past the tile holding the tile's last query.
+// Keys stream in tiles of N = 128 (8 pages, one TMA box per page and 64-dim
+// half), double-buffered.  Per key tile kt:
+//   S = Q K^T     tcgen05.mma kind::f16, A and B from shared memory (K-major),
+//                 fp32 into TMEM columns S[kt % 2].
+//   softmax       8 warps: the two warps on TMEM lane quarter q own rows
+//                 32q .. 32q + 31, one the keys 0..63 and the other 64..127
+//                 of the tile; they exchange row maxima through shared memory.
+//                 P = exp2(S * scale * log2 e - m) is written back into the
+//                 same TMEM columns as two terms of the input dtype, P_hi =
+//                 round(P) and P_lo = round(P - P_hi) (each 32-key chunk of S
+//                 becomes 16 columns of P_hi pairs then 16 of P_lo pairs, so
+//                 no S value is overwritten before it is read).
+//   O += P V      tcgen05.mma with A = P_hi, then P_lo, read from TMEM, and B =
+//                 the V tile (MN-major) from shared memory; O (fp32) stays in
+//                 TMEM for the whole key loop.
+// m is a per-row reference maximum: it only moves (rescaling O in TMEM and the
+// row sum) when a tile's maximum exceeds it by more than 2^8, so O is rarely
+// touched by the threads.  Warp 8 issues the TMA loads, warp 9 owns TMEM and
+// issues the MMAs (one thread each); mbarriers hand tiles between the roles
+// and every wait is bounded.  Keys above the diagonal are masked per element
+// on the tiles that cross it (a warp-uniform test picks the unmasked path
+// elsewhere) and never loaded past the tile holding the tile's last query.
 // Value rows past the sequence's last key are zeroed in shared memory before
 // the PV product so that a zero probability never meets a non-finite value.
 #include <type_traits>
@@ -37,37 +44,33 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kHalf = 16384;                      // 128 rows x 64 elements x 2 bytes
-constexpr int OFF_Q = 0;                          // Q: two 64-dim halves
-constexpr int OFF_KV = 2 * kHalf;                 // 2 stages of {K lo, K hi, V lo, V hi}
+constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kWarpTma = kSoftmaxWarps, kWarpMma = kSoftmaxWarps + 1;
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kHalf = 16384;                       // 128 rows x 64 elements x 2 bytes
+constexpr int kStages = 2;
+constexpr int OFF_Q = 0;                           // Q: two 64-dim halves
+constexpr int OFF_KV = 2 * kHalf;                  // stages of {K lo, K hi, V lo, V hi}
 constexpr int STAGE_BYTES = 4 * kHalf;
-constexpr int OFF_P = OFF_KV + 2 * STAGE_BYTES;   // P_hi then P_lo, each two 64-key halves
-constexpr int OFF_BAR = OFF_P + 4 * kHalf;
-constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;  // + barriers + alignment slack
-constexpr uint32_t kTmemCols = 512;               // S0, S1, O0, O1: 128 columns each
+constexpr int OFF_X = OFF_KV + kStages * STAGE_BYTES;  // row-max / row-sum exchange [2][2][128] fp32
+constexpr int OFF_BAR = OFF_X + 2 * 2 * 128 * 4;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;   // + barriers (< 256 B) + alignment slack   // + barriers + alignment slack
+constexpr uint32_t kTmemCols = 512;                // S/P 0, S/P 1, O, (unused)
+constexpr uint32_t kColO = 256;
+constexpr float kRescale = 8.f;                    // log2 of the largest P before O is rescaled
 
+// Every barrier that signals once per key tile comes in a pair indexed by the
+// tile's parity, so no waiter can be overtaken by two phases.
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[2];
+  uint64_t kv_full[kStages];
   uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full;
+  uint64_t p_full[2];
   uint64_t pv_done[2];
+  uint64_t x_full[2];  // row-max / row-sum exchange between the two halves of a row
   uint32_t tmem_base;
 };
-
-// o = o * alpha + (the 128 fp32 columns of this thread's TMEM lane at taddr)
-__device__ __forceinline__ void accumulate_o(float (&o)[128], uint32_t taddr, float alpha) {
-#pragma unroll
-  for (int cch = 0; cch < 4; ++cch) {
-    uint32_t v[32];
-    tc::ld_32x32b_x32(taddr + cch * 32, v);
-    tc::wait_ld();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) o[cch * 32 + j] = fmaf(o[cch * 32 + j], alpha, __uint_as_float(v[j]));
-  }
-}
 
 template <typename T, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -77,10 +80,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t IDESC_S = tc::idesc_f16(kBF16, 128, 128, false);
   constexpr uint32_t IDESC_O = tc::idesc_f16(kBF16, 128, 128, true);
+  constexpr unsigned FULL = 0xffffffffu;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars &bars = *reinterpret_cast<Bars *>(smem + OFF_BAR);
+  float *xbuf = reinterpret_cast<float *>(smem + OFF_X);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_wait();
 
@@ -114,16 +119,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     tma_prefetch_desc(&vmap);
     tma_prefetch_desc(&qmap);
     mbar_init(&bars.q_full, 1);
+    for (int b = 0; b < kStages; ++b) mbar_init(&bars.kv_full[b], 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars.kv_full[b], 1);
       mbar_init(&bars.s_full[b], 1);
-      mbar_init(&bars.s_free[b], 128);
       mbar_init(&bars.pv_done[b], 1);
+      mbar_init(&bars.p_full[b], kSoftmaxThreads);
+      mbar_init(&bars.x_full[b], kSoftmaxThreads);
     }
-    mbar_init(&bars.p_full, 128);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc::tmem_alloc(&bars.tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -133,17 +138,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
   bool timed_out = false;
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf);
       tma_load_3d(smem + OFF_Q, &qmap, &bars.q_full, 0, h * G, row0 + t0);
       tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
       for (int kt = 0; kt < nkt; ++kt) {
-        const int b = kt & 1;
-        if (kt >= 2 && !mbar_wait(&bars.pv_done[b], ((kt - 2) >> 1) & 1)) {
-          timed_out = true;
-          break;
+        const int b = kt % kStages;
+        // the stage is free once the PV product of the tile that used it is done
+        if (kt >= kStages) {
+          const int j = kt - kStages;
+          if (!mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
+            timed_out = true;
+            break;
+          }
         }
         uint8_t *st = smem + OFF_KV + b * STAGE_BYTES;
         const int pg0 = kt * 8;
@@ -187,17 +196,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       if (!mbar_wait(&bars.q_full, 0)) timed_out = true;
       const uint32_t qa = smem_u32(smem + OFF_Q);
-      const uint32_t pa_ = smem_u32(smem + OFF_P);
       for (int kt = 0; kt <= nkt && !timed_out; ++kt) {
         if (kt < nkt) {
-          const int b = kt & 1;
-          if (!mbar_wait(&bars.kv_full[b], (kt >> 1) & 1) ||
-              (kt >= 2 && !mbar_wait(&bars.s_free[b], ((kt - 2) >> 1) & 1))) {
+          const int b = kt % kStages, sb = kt & 1;
+          if (!mbar_wait(&bars.kv_full[b], (kt / kStages) & 1)) {
             timed_out = true;
             break;
           }
@@ -206,143 +213,184 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            tc::mma_f16(tmem + b * 128, tc::desc_sw128(qa + off, 16, 1024), tc::desc_sw128(ka + off, 16, 1024),
+            tc::mma_f16(tmem + sb * 128, tc::desc_sw128(qa + off, 16, 1024), tc::desc_sw128(ka + off, 16, 1024),
                         IDESC_S, kk > 0);
           }
-          tc::commit(&bars.s_full[b]);
+          tc::commit(&bars.s_full[sb]);
         }
-        if (kt >= 1) {
-          const int j = kt - 1, b = j & 1;
-          if (!mbar_wait(&bars.p_full, j & 1)) {
+        if (kt >= 1) {  // O += P V of the previous tile
+          const int j = kt - 1, sj = j & 1;
+          if (!mbar_wait(&bars.p_full[sj], (j >> 1) & 1)) {
             timed_out = true;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t va = smem_u32(smem + OFF_KV + b * STAGE_BYTES + 2 * kHalf);
+          const uint32_t va = smem_u32(smem + OFF_KV + (j % kStages) * STAGE_BYTES + 2 * kHalf);
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {  // P_hi (kk < 8), then P_lo, against the same V
-            const uint32_t aoff = (kk >> 3) * 2 * kHalf + ((kk >> 2) & 1) * kHalf + (kk & 3) * 32;
-            tc::mma_f16(tmem + 256 + b * 128, tc::desc_sw128(pa_ + aoff, 16, 1024),
-                        tc::desc_sw128(va + (kk & 7) * 2048, kHalf, 1024), IDESC_O, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a_hi = tmem + sj * 128 + 32 * (kk >> 1) + 8 * (kk & 1);
+            const uint64_t bdesc = tc::desc_sw128(va + kk * 2048, kHalf, 1024);
+            tc::mma_f16_ts(tmem + kColO, a_hi, bdesc, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_f16_ts(tmem + kColO, a_hi + 16, bdesc, IDESC_O, 1u);
           }
-          tc::commit(&bars.pv_done[b]);
+          tc::commit(&bars.pv_done[sj]);
         }
       }
     }
   } else {
-    // ---------------- softmax + epilogue (warps 0..3) ----------------
-    const int r = threadIdx.x;
+    // ---------------- softmax + epilogue (warps 0..7) ----------------
+    const int quad = warp & 3, ch = warp >> 2;       // TMEM lane quarter, key half of the tile
+    const int r = quad * 32 + lane;                  // tile row = TMEM lane
+    const int tid = warp * 32 + lane;                // 0 .. 255
     const int tq = t0 + r / G;                       // query token within the chunk
     const int head = h * G + r % G;
     const int lim = min(start + tq, ctx - 1);        // last visible key position of this row
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f, alpha = 0.f;
-    float o[128];
-#pragma unroll
-    for (int j = 0; j < 128; ++j) o[j] = 0.f;
-    uint8_t *prow = smem + OFF_P + r * 128;
+    float m_ref = -INFINITY, l = 0.f;
 
     for (int kt = 0; kt < nkt; ++kt) {
-      const int b = kt & 1;
-      if (!mbar_wait(&bars.s_full[b], (kt >> 1) & 1)) {
+      const int sb = kt & 1;
+      if (!mbar_wait(&bars.s_full[sb], (kt >> 1) & 1)) {
         timed_out = true;
         break;
       }
       tc::fence_after_sync();
-      const uint32_t s_addr = tmem + lane_base + b * 128;
-      const int kbase = kt * 128;
+      const uint32_t s_addr = tmem + lane_base + sb * 128 + ch * 64;
+      const int kbase = kt * 128 + ch * 64;          // first key of this thread's half
+      uint32_t v[2][32];
+      tc::ld_32x32b_x32(s_addr, v[0]);
+      tc::ld_32x32b_x32(s_addr + 32, v[1]);
+      tc::wait_ld();
+      const bool full = __all_sync(FULL, kbase + 63 <= lim);
 
       float mx = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int cch = 0; cch < 4; ++cch) {
-        uint32_t v[32];
-        tc::ld_32x32b_x32(s_addr + cch * 32, v);
-        tc::wait_ld();
+        for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (kbase + cch * 32 + j <= lim) mx = fmaxf(mx, __uint_as_float(v[j]));
+          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[cc][j]));
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (kbase + cc * 32 + j <= lim) mx = fmaxf(mx, __uint_as_float(v[cc][j]));
       }
-      const float m_new = fmaxf(m_run, mx * sl2);
-      const float a_new = exp2f(m_run - m_new);
-
-      if (kt >= 1) {  // fold the previous tile's P V in before P is overwritten
-        const int j = kt - 1;
-        if (!mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
-          timed_out = true;
-          break;
+      float *xb = xbuf + (kt & 1) * 256;
+      xb[ch * 128 + r] = mx;
+      mbar_arrive(&bars.x_full[kt & 1]);
+      if (!mbar_wait(&bars.x_full[kt & 1], (kt >> 1) & 1)) {
+        timed_out = true;
+        break;
+      }
+      mx = fmaxf(mx, xb[(1 - ch) * 128 + r]);
+      const float mc = mx * sl2;
+      if (kt == 0) {
+        m_ref = mc;  // every row sees key 0, so the first tile's maximum is finite
+      } else {
+        const bool need = mc > m_ref + kRescale;
+        if (__any_sync(FULL, need)) {  // warp-uniform: the TMEM accesses below are warp-wide
+          const float f = need ? exp2f(m_ref - mc) : 1.f;
+          if (need) {
+            l *= f;
+            m_ref = mc;
+          }
+          // every earlier P V has landed in O: scale this thread's half of its row
+          const int j = kt - 1;
+          if (!mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
+            timed_out = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t o_addr = tmem + lane_base + kColO + ch * 64;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t ov[32];
+            tc::ld_32x32b_x32(o_addr + cc * 32, ov);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+            tc::st_32x32b_x32(o_addr + cc * 32, ov);
+          }
         }
-        tc::fence_after_sync();
-        accumulate_o(o, tmem + lane_base + 256 + (j & 1) * 128, alpha);
       }
 
+      // P in two terms of the input dtype, written over this half's S columns
       float ls = 0.f;
 #pragma unroll
-      for (int cch = 0; cch < 4; ++cch) {
-        uint32_t v[32];
-        tc::ld_32x32b_x32(s_addr + cch * 32, v);
-        tc::wait_ld();
-        uint32_t hi[16], lo[16];
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const int key = kbase + cch * 32 + j;
-          const float p0 = (key <= lim) ? exp2f(fmaf(__uint_as_float(v[j]), sl2, -m_new)) : 0.f;
-          const float p1 = (key + 1 <= lim) ? exp2f(fmaf(__uint_as_float(v[j + 1]), sl2, -m_new)) : 0.f;
+        for (int j = 0; j < 16; ++j) {
+          const float s0 = __uint_as_float(v[cc][2 * j]), s1 = __uint_as_float(v[cc][2 * j + 1]);
+          float p0 = exp2f(fmaf(s0, sl2, -m_ref));
+          float p1 = exp2f(fmaf(s1, sl2, -m_ref));
+          if (!full) {
+            const int key = kbase + cc * 32 + 2 * j;
+            p0 = (key <= lim) ? p0 : 0.f;
+            p1 = (key + 1 <= lim) ? p1 : 0.f;
+          }
           ls += p0 + p1;
-          hi[j >> 1] = Pack<T>::from_f2(p0, p1);
-          const float2 h2 = Pack<T>::to_f2(hi[j >> 1]);
-          lo[j >> 1] = Pack<T>::from_f2(p0 - h2.x, p1 - h2.y);
+          pk[j] = Pack<T>::from_f2(p0, p1);
+          const float2 h2 = Pack<T>::to_f2(pk[j]);
+          pk[16 + j] = Pack<T>::from_f2(p0 - h2.x, p1 - h2.y);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int q = cch * 4 + i, half = q >> 3, cc = q & 7;
-          uint8_t *dst = prow + half * kHalf + ((cc ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4 *>(dst) = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
-          *reinterpret_cast<uint4 *>(dst + 2 * kHalf) =
-              make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
-        }
+        tc::st_32x32b_x32(s_addr + cc * 32, pk);
       }
-      l_run = l_run * a_new + ls;
-      m_run = m_new;
-      alpha = a_new;
-      tc::fence_before_sync();
-      mbar_arrive(&bars.s_free[b]);
+      tc::wait_st();
+      l += ls;
 
       if (kt == kt_ctx) {
         // value rows of keys >= ctx (partial last page, pages past the end)
-        if (!mbar_wait(&bars.kv_full[b], (kt >> 1) & 1)) {
+        if (!mbar_wait(&bars.kv_full[kt % kStages], (kt / kStages) & 1)) {
           timed_out = true;
           break;
         }
-        const int z0 = ctx - kbase;
-        uint8_t *vbase = smem + OFF_KV + b * STAGE_BYTES + 2 * kHalf;
-        for (int idx = r; idx < (128 - z0) * 16; idx += 128) {
+        const int z0 = ctx - kt * 128;
+        uint8_t *vbase = smem + OFF_KV + (kt % kStages) * STAGE_BYTES + 2 * kHalf;
+        for (int idx = tid; idx < (128 - z0) * 16; idx += kSoftmaxThreads) {
           const int row = z0 + (idx >> 4), part = idx & 15;
           *reinterpret_cast<uint4 *>(vbase + (part >> 3) * kHalf + row * 128 + (part & 7) * 16) =
               make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars.p_full);
+      tc::fence_before_sync();
+      mbar_arrive(&bars.p_full[kt & 1]);
     }
 
     if (!timed_out) {
       const int j = nkt - 1;
       if (mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
         tc::fence_after_sync();
-        accumulate_o(o, tmem + lane_base + 256 + (j & 1) * 128, alpha);
-        if (tq < len) {
-          const float inv = 1.f / l_run;
-          T *op = reinterpret_cast<T *>(p.out) + ((int64_t)(row0 + tq) * p.num_q_heads + head) * kHeadDim;
+        // row sum: the two halves exchange theirs (next phase of the exchange barriers)
+        float *xl = xbuf + (nkt & 1) * 256;
+        xl[ch * 128 + r] = l;
+        mbar_arrive(&bars.x_full[nkt & 1]);
+        if (mbar_wait(&bars.x_full[nkt & 1], (nkt >> 1) & 1)) {
+          const float inv = 1.f / (l + xl[(1 - ch) * 128 + r]);
+          T *op = reinterpret_cast<T *>(p.out) + ((int64_t)(row0 + tq) * p.num_q_heads + head) * kHeadDim + ch * 64;
+          const uint32_t o_addr = tmem + lane_base + kColO + ch * 64;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            uint4 v;
-            v.x = Pack<T>::from_f2(o[8 * i + 0] * inv, o[8 * i + 1] * inv);
-            v.y = Pack<T>::from_f2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
-            v.z = Pack<T>::from_f2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
-            v.w = Pack<T>::from_f2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
-            *reinterpret_cast<uint4 *>(op + 8 * i) = v;
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t ov[32];
+            tc::ld_32x32b_x32(o_addr + cc * 32, ov);  // warp-wide; only rows of the chunk are stored
+            tc::wait_ld();
+            if (tq < len) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint4 w;
+                w.x = Pack<T>::from_f2(__uint_as_float(ov[8 * i + 0]) * inv, __uint_as_float(ov[8 * i + 1]) * inv);
+                w.y = Pack<T>::from_f2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
+                w.z = Pack<T>::from_f2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
+                w.w = Pack<T>::from_f2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
+                *reinterpret_cast<uint4 *>(op + cc * 32 + 8 * i) = w;
+              }
+            }
           }
+        } else {
+          timed_out = true;
         }
       } else {
         timed_out = true;
@@ -353,7 +401,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (timed_out) set_error(p.err, PA_ERR_TIMEOUT, c);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
