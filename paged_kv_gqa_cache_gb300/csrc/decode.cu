@@ -20,8 +20,9 @@
 // context_lens, so no planning pass or atomic counter is needed.
 //
 // Per warp, K/V pages stream through a ring of shared-memory stages filled by
-// TMA (one 4-D tensor map per pool, 128-byte swizzle, four 2 KB boxes per
-// page) and guarded by one mbarrier each.  One page of K feeds all G query
+// TMA (one 4-D tensor map per pool; one 4 KB box {128 dims, 1 head, 16 slots}
+// per page of K and one of V: the TMA engine's cost grows with the number of
+// boxes, so a page is never split) and guarded by one mbarrier each.  One page of K feeds all G query
 // heads of its KV head: the scores for G heads come from a single read of K.
 // All arithmetic is fp32 on the CUDA cores: decode reads each K/V byte once and
 // does G multiply-adds per element, far below the tensor-core ridge point.
@@ -35,8 +36,12 @@ constexpr int STAGE = kDecodeStageBytes;
 constexpr int kStages = 3;  // TMA stages per warp
 constexpr unsigned FULL = 0xffffffffu;
 
-// Lane layout of the score (QK) phase: NQ lanes split the 128 dims of one key,
-// NT keys are scored per pass, NP passes cover a 16-token page.
+// Lane layout of the score (QK) phase: NQ adjacent lanes split the 128 dims of
+// one key (lane = key * NQ + qd), NT keys are scored per pass, NP passes cover a
+// 16-token page.  Lane qd owns the 16-byte chunks qd + NQ * k (k < CPL) of a
+// key row; on iteration i it reads chunk qd + NQ * ((i + key) % CPL), so the
+// NQ lanes of one key and those of the next key hit disjoint banks of the
+// unswizzled 256-byte rows (an 8-lane shared-memory phase covers all 32 banks).
 template <int G>
 struct Layout {
   static constexpr int NQ = (G >= 8) ? 8 : 4;
@@ -122,7 +127,7 @@ __global__ void __launch_bounds__(NW * 32)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const DecodeParams p) {
   using Ly = Layout<G>;
-  constexpr int NT = Ly::NT, NP = Ly::NP, DPL = Ly::DPL, CPL = Ly::CPL;
+  constexpr int NQ = Ly::NQ, NT = Ly::NT, NP = Ly::NP, DPL = Ly::DPL, CPL = Ly::CPL;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -163,8 +168,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int64_t npages = x1 - x0;
 
   // lane roles
-  const int qd = lane / NT;  // which dim slice of a key this lane scores
-  const int tk = lane % NT;  // which key of a pass
+  const int qd = lane % NQ;  // which dim slice of a key this lane scores
+  const int tk = lane / NQ;  // which key of a pass
+  const int rot = tk % CPL;  // chunk rotation of this lane's keys (NT is a multiple of CPL)
 
   Cursor ic = locate(prefix, n, hkv, x0);
   Cursor cc = ic;
@@ -188,9 +194,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         uint8_t *dst = stages + st * STAGE;
         mbar_arrive_expect_tx(&bars[st], STAGE);
         tma_load_4d(dst, &kmap, &bars[st], 0, ic.h, 0, blk);
-        tma_load_4d(dst + 2048, &kmap, &bars[st], 64, ic.h, 0, blk);
         tma_load_4d(dst + 4096, &vmap, &bars[st], 0, ic.h, 0, blk);
-        tma_load_4d(dst + 6144, &vmap, &bars[st], 64, ic.h, 0, blk);
       } else {
         set_error(p.err, PA_ERR_RANGE, ic.s);
         mbar_arrive(&bars[st]);
@@ -224,7 +228,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       for (int gg = 0; gg < G; ++gg) {
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
-          const uint4 u = *reinterpret_cast<const uint4 *>(qp + gg * kHeadDim + (qd * CPL + i) * 8);
+          const int chunk = qd + NQ * ((i + rot) % CPL);
+          const uint4 u = *reinterpret_cast<const uint4 *>(qp + gg * kHeadDim + chunk * 8);
           const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -265,9 +270,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         for (int gg = 0; gg < G; ++gg) acc[gg] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
-          const int cg = qd * CPL + i;
-          const uint4 u = *reinterpret_cast<const uint4 *>(kst + (cg >> 3) * 2048 + t * 128 +
-                                                          (((cg & 7) ^ (t & 7)) << 4));
+          const int chunk = qd + NQ * ((i + rot) % CPL);
+          const uint4 u = *reinterpret_cast<const uint4 *>(kst + t * 256 + chunk * 16);
           const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -280,7 +284,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         for (int gg = 0; gg < G; ++gg) {
           float a = acc[gg].x + acc[gg].y;
 #pragma unroll
-          for (int off = NT; off < 32; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
+          for (int off = 1; off < NQ; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
           sc[ps][gg] = (t < nv) ? a : neg_inf;
         }
       }
@@ -292,7 +296,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 #pragma unroll
         for (int ps = 1; ps < NP; ++ps) mp = fmaxf(mp, sc[ps][gg]);
 #pragma unroll
-        for (int off = 1; off < NT; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(FULL, mp, off));
+        for (int off = NQ; off < 32; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(FULL, mp, off));
         const float mn = fmaxf(m[gg], mp);
         const float alpha = exp2f(m[gg] - mn);
         m[gg] = mn;
@@ -311,9 +315,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       __syncwarp();
 
       // weighted sum of values: this lane owns dims [4 * lane, 4 * lane + 4)
-      const int vh = lane >> 4, vc = (lane & 15) >> 1, vsub = (lane & 1) * 8;
       auto pv_token = [&](int t) {
-        const uint2 u = *reinterpret_cast<const uint2 *>(vst + vh * 2048 + t * 128 + ((vc ^ (t & 7)) << 4) + vsub);
+        const uint2 u = *reinterpret_cast<const uint2 *>(vst + t * 256 + 8 * lane);
         const float2 v01 = Pack<T>::to_f2(u.x);
         const float2 v23 = Pack<T>::to_f2(u.y);
         float2 pp[G];
@@ -352,7 +355,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       for (int gg = 0; gg < G; ++gg) {
         float lt = l[gg];
 #pragma unroll
-        for (int off = 1; off < NT; off <<= 1) lt += __shfl_xor_sync(FULL, lt, off);
+        for (int off = NQ; off < 32; off <<= 1) lt += __shfl_xor_sync(FULL, lt, off);
         if (final_out) {
           const float inv = 1.f / lt;
           T *op = reinterpret_cast<T *>(p.out) +

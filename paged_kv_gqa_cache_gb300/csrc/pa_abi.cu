@@ -86,16 +86,18 @@ CUtensorMapDataType map_dtype(int dtype) {
   return dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-// The pool as a 4-D tensor {dim, kv head, in-block slot, block}, boxes of
-// {64 dims, 1 head, 16 slots, 1 block} with 128-byte swizzle: one box is half
-// of a page of one KV head (16 rows x 128 bytes = 2 KB).
-bool pool_map(CUtensorMap *map, const pa_kv_pool *pool, void *base) {
+// The pool as a 4-D tensor {dim, kv head, in-block slot, block}.  The prefill
+// kernel feeds tensor cores and needs the 128-byte swizzled layout, so its
+// boxes are {64 dims, 1 head, 16 slots, 1 block} (half a page of one KV head,
+// 2 KB); the decode kernel reads with CUDA cores and takes a whole page of one
+// KV head per box, {128, 1, 16, 1} unswizzled (4 KB).
+bool pool_map(CUtensorMap *map, const pa_kv_pool *pool, void *base, bool whole_page_box) {
   const uint64_t hkv = (uint64_t)pool->num_kv_heads;
   const uint64_t dims[4] = {(uint64_t)kHeadDim, hkv, (uint64_t)kBlock, (uint64_t)pool->num_blocks};
   const uint64_t strides[3] = {kHeadDim * 2ull, hkv * kHeadDim * 2ull, kBlock * hkv * kHeadDim * 2ull};
-  const uint32_t box[4] = {64, 1, (uint32_t)kBlock, 1};
+  const uint32_t box[4] = {whole_page_box ? 128u : 64u, 1, (uint32_t)kBlock, 1};
   return encode_tensor_map(map, map_dtype(pool->dtype), 4, base, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B);
+                           whole_page_box ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
@@ -217,7 +219,8 @@ pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, const int3
   p.scale_log2 = scale * 1.4426950408889634f;
 
   CUtensorMap kmap, vmap;
-  if (!pool_map(&kmap, pool, pool->k_cache) || !pool_map(&vmap, pool, pool->v_cache)) return PA_ERR_CUDA;
+  if (!pool_map(&kmap, pool, pool->k_cache, true) || !pool_map(&vmap, pool, pool->v_cache, true))
+    return PA_ERR_CUDA;
 
   // Upper bound on the pages of the call; aim for at least 4 pages per warp.
   const int64_t pages_hint = (int64_t)num_seqs * pool->num_kv_heads * ((max_context_len + kBlock - 1) / kBlock);
@@ -267,7 +270,8 @@ pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts
   p.scale_log2 = scale * 1.4426950408889634f;
 
   CUtensorMap kmap, vmap, qmap;
-  if (!pool_map(&kmap, pool, pool->k_cache) || !pool_map(&vmap, pool, pool->v_cache)) return PA_ERR_CUDA;
+  if (!pool_map(&kmap, pool, pool->k_cache, false) || !pool_map(&vmap, pool, pool->v_cache, false))
+    return PA_ERR_CUDA;
   // q as a 3-D tensor {dim, query head, token}; boxes of {64 dims, G heads,
   // 128/G tokens} give 128 rows (token-major, head-minor) of 128 bytes.
   {

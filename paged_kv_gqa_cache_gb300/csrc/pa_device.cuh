@@ -148,6 +148,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32: a few ulp, inputs
+// below -126 flush to +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---- 16-bit → fp32 conversion of packed pairs --------------------------------
 
 template <typename T>

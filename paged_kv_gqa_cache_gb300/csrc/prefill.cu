@@ -14,29 +14,34 @@
 // so every K/V tile it reads serves all G heads.  Row r of the tile is token
 // t0 + r / G, head h * G + r % G (the Q tile is one TMA box per 64-dim half).
 // Keys stream in tiles of N = 128 (8 pages, one TMA box per page and 64-dim
-// half), double-buffered.  Per key tile kt:
+// half): K through a 3-stage ring released as soon as S is computed, V
+// through a 2-stage ring released after the PV product.  Per key tile kt:
 //   S = Q K^T     tcgen05.mma kind::f16, A and B from shared memory (K-major),
 //                 fp32 into TMEM columns S[kt % 2].
-//   softmax       8 warps: the two warps on TMEM lane quarter q own rows
-//                 32q .. 32q + 31, one the keys 0..63 and the other 64..127
-//                 of the tile; they exchange row maxima through shared memory.
-//                 P = exp2(S * scale * log2 e - m) is written back into the
-//                 same TMEM columns as two terms of the input dtype, P_hi =
-//                 round(P) and P_lo = round(P - P_hi) (each 32-key chunk of S
-//                 becomes 16 columns of P_hi pairs then 16 of P_lo pairs, so
-//                 no S value is overwritten before it is read).
-//   O += P V      tcgen05.mma with A = P_hi, then P_lo, read from TMEM, and B =
-//                 the V tile (MN-major) from shared memory; O (fp32) stays in
-//                 TMEM for the whole key loop.
-// m is a per-row reference maximum: it only moves (rescaling O in TMEM and the
-// row sum) when a tile's maximum exceeds it by more than 2^8, so O is rarely
-// touched by the threads.  Warp 8 issues the TMA loads, warp 9 owns TMEM and
-// issues the MMAs (one thread each); mbarriers hand tiles between the roles
-// and every wait is bounded.  Keys above the diagonal are masked per element
-// on the tiles that cross it (a warp-uniform test picks the unmasked path
-// elsewhere) and never loaded past the tile holding the tile's last query.
-// Value rows past the sequence's last key are zeroed in shared memory before
-// the PV product so that a zero probability never meets a non-finite value.
+//   softmax       8 warps; the two warps on TMEM lane quarter q own rows
+//                 32q .. 32q + 31, warp half 0 the keys 0..63 of every tile,
+//                 half 1 the keys 64..127.  Each half keeps its own per-row
+//                 reference maximum m, row sum l and output accumulator O_half,
+//                 so the halves never synchronise inside the key loop.
+//                 P = 2^(S * scale * log2 e - m) goes back into the same TMEM
+//                 columns as two terms of the input dtype, P_hi = round(P) and
+//                 P_lo = round(P - P_hi) (each 32-key chunk of S becomes 16
+//                 columns of P_hi pairs then 16 of P_lo pairs, so no S value is
+//                 overwritten before it is read).
+//   O_half += P V tcgen05.mma with A = P_hi, then P_lo, read from TMEM, and B =
+//                 the V rows of that half (MN-major) from shared memory; both
+//                 O accumulators (fp32) stay in TMEM for the whole key loop.
+// m only moves (rescaling that half's O and l) when a tile's maximum exceeds
+// it by more than 2^8, so the threads rarely touch O.  The epilogue merges the
+// two halves of each row, O = O_0 2^(m_0 - M) + O_1 2^(m_1 - M) over
+// l_0 2^(m_0 - M) + l_1 2^(m_1 - M), and stores it in the input dtype.
+// Warp 8 issues the TMA loads, warp 9 owns TMEM and issues the MMAs (one thread
+// each); mbarriers hand tiles between the roles and every wait is bounded.
+// Keys above the diagonal are masked per element on the tiles that cross it (a
+// warp-uniform test picks the unmasked path elsewhere) and never loaded past
+// the tile holding the tile's last query.  Value rows past the sequence's last
+// key are zeroed in shared memory before the PV product so that a zero
+// probability never meets a non-finite value.
 #include <type_traits>
 
 #include "tcgen05.cuh"
@@ -48,29 +53,59 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kWarpTma = kSoftmaxWarps, kWarpMma = kSoftmaxWarps + 1;
 constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
-constexpr int kHalf = 16384;                       // 128 rows x 64 elements x 2 bytes
-constexpr int kStages = 2;
-constexpr int OFF_Q = 0;                           // Q: two 64-dim halves
-constexpr int OFF_KV = 2 * kHalf;                  // stages of {K lo, K hi, V lo, V hi}
-constexpr int STAGE_BYTES = 4 * kHalf;
-constexpr int OFF_X = OFF_KV + kStages * STAGE_BYTES;  // row-max / row-sum exchange [2][2][128] fp32
-constexpr int OFF_BAR = OFF_X + 2 * 2 * 128 * 4;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;   // + barriers (< 256 B) + alignment slack   // + barriers + alignment slack
-constexpr uint32_t kTmemCols = 512;                // S/P 0, S/P 1, O, (unused)
+constexpr int kHalf = 16384;                        // 128 rows x 64 elements x 2 bytes
+constexpr int kKStages = 3, kVStages = 2;
+constexpr int OFF_Q = 0;                            // Q: two 64-dim halves
+constexpr int OFF_K = 2 * kHalf;                    // K stages: {lo, hi} halves
+constexpr int OFF_V = OFF_K + kKStages * 2 * kHalf; // V stages: {lo, hi} halves
+constexpr int OFF_X = OFF_V + kVStages * 2 * kHalf; // epilogue (m, l) exchange [2][128] float2
+constexpr int kBtCache = 2048;                      // block ids of the chunk cached in shared memory
+constexpr int OFF_BT = OFF_X + 2 * 128 * 8;
+constexpr int OFF_BAR = OFF_BT + kBtCache * 4;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;    // + barriers (< 256 B) + alignment slack
+constexpr uint32_t kTmemCols = 512;                 // S/P 0, S/P 1, O_0, O_1
 constexpr uint32_t kColO = 256;
-constexpr float kRescale = 8.f;                    // log2 of the largest P before O is rescaled
+constexpr float kRescale = 8.f;                     // log2 of the largest P before O is rescaled
 
-// Every barrier that signals once per key tile comes in a pair indexed by the
-// tile's parity, so no waiter can be overtaken by two phases.
+// Barriers that signal once per key tile come in pairs indexed by the tile's
+// parity (or one per ring stage), so no waiter can be overtaken by two phases.
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
+  uint64_t k_full[kKStages];
+  uint64_t k_free[kKStages];
+  uint64_t v_full[kVStages];
   uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
-  uint64_t x_full[2];  // row-max / row-sum exchange between the two halves of a row
+  uint64_t p_full[2][2];  // [key half][tile parity]
+  uint64_t pv_done[2];    // also frees the V stage of that tile
+  uint64_t x_full;
   uint32_t tmem_base;
 };
+
+// Fetch the 8 pages of key tile kt of one pool into `dst` (two 64-dim half
+// boxes per page), completing on `bar`; called by the whole producer warp:
+// lane j < 16 loads half j % 2 of page j / 2.  Pages past the sequence are
+// skipped; a page whose block id is out of range is zeroed and reported.
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int kt, int h,
+                                          int npages, const int32_t *sbt, const int32_t *bt,
+                                          const PrefillParams &p, int c, int lane) {
+  const int page = lane >> 1, half = lane & 1;
+  const int pg = kt * 8 + page;
+  const bool in = lane < 16 && pg < npages;
+  int id = -1;
+  if (in) id = pg < kBtCache ? sbt[pg] : __ldg(bt + pg);
+  const bool ok = in && (unsigned)id < (unsigned)p.num_blocks;
+  const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+  uint8_t *box = dst + half * kHalf + page * 2048;
+  if (in && !ok) {  // rare: keep the products finite; the error word reports the chunk
+    if (half == 0) set_error(p.err, PA_ERR_RANGE, c);
+    uint4 *z = reinterpret_cast<uint4 *>(box);
+    for (int i = 0; i < 128; ++i) z[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(okmask) * 2048u);
+  __syncwarp();
+  if (ok) tma_load_4d(box, map, bar, half * 64, h, 0, id);
+}
 
 template <typename T, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -85,7 +120,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars &bars = *reinterpret_cast<Bars *>(smem + OFF_BAR);
-  float *xbuf = reinterpret_cast<float *>(smem + OFF_X);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_wait();
 
@@ -119,13 +153,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     tma_prefetch_desc(&vmap);
     tma_prefetch_desc(&qmap);
     mbar_init(&bars.q_full, 1);
-    for (int b = 0; b < kStages; ++b) mbar_init(&bars.kv_full[b], 1);
+    for (int b = 0; b < kKStages; ++b) {
+      mbar_init(&bars.k_full[b], 1);
+      mbar_init(&bars.k_free[b], 1);
+    }
+    for (int b = 0; b < kVStages; ++b) mbar_init(&bars.v_full[b], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.s_full[b], 1);
       mbar_init(&bars.pv_done[b], 1);
-      mbar_init(&bars.p_full[b], kSoftmaxThreads);
-      mbar_init(&bars.x_full[b], kSoftmaxThreads);
+      mbar_init(&bars.p_full[0][b], kSoftmaxThreads / 2);
+      mbar_init(&bars.p_full[1][b], kSoftmaxThreads / 2);
     }
+    mbar_init(&bars.x_full, kSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -139,62 +178,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   bool timed_out = false;
 
   if (warp == kWarpTma) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer warp: K two tiles ahead, V as its stage frees ----------------
+    int32_t *sbt = reinterpret_cast<int32_t *>(smem + OFF_BT);
+    const int cached = min(min(npages, nkt * 8), kBtCache);
+    for (int i = lane; i < cached; i += 32) sbt[i] = __ldg(bt + i);
+    __syncwarp();
     if (lane == 0) {
       mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf);
       tma_load_3d(smem + OFF_Q, &qmap, &bars.q_full, 0, h * G, row0 + t0);
       tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
-      for (int kt = 0; kt < nkt; ++kt) {
-        const int b = kt % kStages;
-        // the stage is free once the PV product of the tile that used it is done
-        if (kt >= kStages) {
-          const int j = kt - kStages;
-          if (!mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
-            timed_out = true;
-            break;
-          }
+    }
+    for (int i = 0; i < 2 && i < nkt; ++i)
+      load_tile(smem + OFF_K + i * 2 * kHalf, &kmap, &bars.k_full[i], i, h, npages, sbt, bt, p, c, lane);
+    for (int kt = 0; kt < nkt; ++kt) {
+      const int kn = kt + 2;
+      if (kn < nkt) {
+        const int b = kn % kKStages;
+        if (kn >= kKStages && !mbar_wait(&bars.k_free[b], ((kn - kKStages) / kKStages) & 1)) {
+          timed_out = true;
+          break;
         }
-        uint8_t *st = smem + OFF_KV + b * STAGE_BYTES;
-        const int pg0 = kt * 8;
-        const int np = min(8, npages - pg0);
-        int blk[8];
-        int nvalid = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          blk[j] = -1;
-          if (j < np) {
-            const int id = __ldg(bt + pg0 + j);
-            if ((unsigned)id < (unsigned)p.num_blocks) {
-              blk[j] = id;
-              ++nvalid;
-            } else {
-              set_error(p.err, PA_ERR_RANGE, c);
-            }
-          }
-        }
-        // A page whose block id is out of range is not loaded; zero it so the
-        // products stay finite (the error word already reports the chunk).
-        bool zeroed = false;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j >= np || blk[j] >= 0) continue;
-          for (int part = 0; part < 4; ++part) {
-            uint4 *z = reinterpret_cast<uint4 *>(st + part * kHalf + j * 2048);
-            for (int i = 0; i < 128; ++i) z[i] = make_uint4(0, 0, 0, 0);
-          }
-          zeroed = true;
-        }
-        if (zeroed) fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars.kv_full[b], (uint32_t)nvalid * 4u * 2048u);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (blk[j] < 0) continue;
-          tma_load_4d(st + 0 * kHalf + j * 2048, &kmap, &bars.kv_full[b], 0, h, 0, blk[j]);
-          tma_load_4d(st + 1 * kHalf + j * 2048, &kmap, &bars.kv_full[b], 64, h, 0, blk[j]);
-          tma_load_4d(st + 2 * kHalf + j * 2048, &vmap, &bars.kv_full[b], 0, h, 0, blk[j]);
-          tma_load_4d(st + 3 * kHalf + j * 2048, &vmap, &bars.kv_full[b], 64, h, 0, blk[j]);
+        load_tile(smem + OFF_K + b * 2 * kHalf, &kmap, &bars.k_full[b], kn, h, npages, sbt, bt, p, c, lane);
+      }
+      const int vb = kt % kVStages;
+      if (kt >= kVStages) {
+        const int j = kt - kVStages;
+        if (!mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
+          timed_out = true;
+          break;
         }
       }
+      load_tile(smem + OFF_V + vb * 2 * kHalf, &vmap, &bars.v_full[vb], kt, h, npages, sbt, bt, p, c, lane);
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
@@ -203,13 +217,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       const uint32_t qa = smem_u32(smem + OFF_Q);
       for (int kt = 0; kt <= nkt && !timed_out; ++kt) {
         if (kt < nkt) {
-          const int b = kt % kStages, sb = kt & 1;
-          if (!mbar_wait(&bars.kv_full[b], (kt / kStages) & 1)) {
+          const int b = kt % kKStages, sb = kt & 1;
+          if (!mbar_wait(&bars.k_full[b], (kt / kKStages) & 1)) {
             timed_out = true;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t ka = smem_u32(smem + OFF_KV + b * STAGE_BYTES);
+          const uint32_t ka = smem_u32(smem + OFF_K + b * 2 * kHalf);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -217,35 +231,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                         IDESC_S, kk > 0);
           }
           tc::commit(&bars.s_full[sb]);
+          tc::commit(&bars.k_free[b]);
         }
-        if (kt >= 1) {  // O += P V of the previous tile
+        if (kt >= 1) {  // O_half += P V of the previous tile, one key half at a time
           const int j = kt - 1, sj = j & 1;
-          if (!mbar_wait(&bars.p_full[sj], (j >> 1) & 1)) {
+          if (!mbar_wait(&bars.v_full[j % kVStages], (j / kVStages) & 1)) {
             timed_out = true;
             break;
           }
-          tc::fence_after_sync();
-          const uint32_t va = smem_u32(smem + OFF_KV + (j % kStages) * STAGE_BYTES + 2 * kHalf);
+          const uint32_t va = smem_u32(smem + OFF_V + (j % kVStages) * 2 * kHalf);
+          for (int half = 0; half < 2 && !timed_out; ++half) {
+            if (!mbar_wait(&bars.p_full[half][sj], (j >> 1) & 1)) {
+              timed_out = true;
+              break;
+            }
+            tc::fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t a_hi = tmem + sj * 128 + 32 * (kk >> 1) + 8 * (kk & 1);
-            const uint64_t bdesc = tc::desc_sw128(va + kk * 2048, kHalf, 1024);
-            tc::mma_f16_ts(tmem + kColO, a_hi, bdesc, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-            tc::mma_f16_ts(tmem + kColO, a_hi + 16, bdesc, IDESC_O, 1u);
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int kk = half * 4 + k4;  // 16-key step within the tile
+              const uint32_t a_hi = tmem + sj * 128 + 32 * (kk >> 1) + 8 * (kk & 1);
+              const uint64_t bdesc = tc::desc_sw128(va + kk * 2048, kHalf, 1024);
+              tc::mma_f16_ts(tmem + kColO + half * 128, a_hi, bdesc, IDESC_O, (j > 0 || k4 > 0) ? 1u : 0u);
+              tc::mma_f16_ts(tmem + kColO + half * 128, a_hi + 16, bdesc, IDESC_O, 1u);
+            }
           }
+          if (timed_out) break;
           tc::commit(&bars.pv_done[sj]);
         }
       }
     }
   } else {
     // ---------------- softmax + epilogue (warps 0..7) ----------------
-    const int quad = warp & 3, ch = warp >> 2;       // TMEM lane quarter, key half of the tile
+    const int quad = warp & 3, ch = warp >> 2;       // TMEM lane quarter, key half of every tile
     const int r = quad * 32 + lane;                  // tile row = TMEM lane
     const int tid = warp * 32 + lane;                // 0 .. 255
     const int tq = t0 + r / G;                       // query token within the chunk
     const int head = h * G + r % G;
     const int lim = min(start + tq, ctx - 1);        // last visible key position of this row
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t o_self = tmem + lane_base + kColO + ch * 128;
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
 
@@ -269,7 +293,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[cc][j]));
+          for (int j = 0; j < 32; j += 2)
+            mx = fmaxf(mx, fmaxf(__uint_as_float(v[cc][j]), __uint_as_float(v[cc][j + 1])));
       } else {
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
@@ -277,79 +302,71 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           for (int j = 0; j < 32; ++j)
             if (kbase + cc * 32 + j <= lim) mx = fmaxf(mx, __uint_as_float(v[cc][j]));
       }
-      float *xb = xbuf + (kt & 1) * 256;
-      xb[ch * 128 + r] = mx;
-      mbar_arrive(&bars.x_full[kt & 1]);
-      if (!mbar_wait(&bars.x_full[kt & 1], (kt >> 1) & 1)) {
-        timed_out = true;
-        break;
-      }
-      mx = fmaxf(mx, xb[(1 - ch) * 128 + r]);
-      const float mc = mx * sl2;
-      if (kt == 0) {
-        m_ref = mc;  // every row sees key 0, so the first tile's maximum is finite
-      } else {
-        const bool need = mc > m_ref + kRescale;
-        if (__any_sync(FULL, need)) {  // warp-uniform: the TMEM accesses below are warp-wide
-          const float f = need ? exp2f(m_ref - mc) : 1.f;
-          if (need) {
-            l *= f;
-            m_ref = mc;
-          }
-          // every earlier P V has landed in O: scale this thread's half of its row
-          const int j = kt - 1;
-          if (!mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
-            timed_out = true;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t o_addr = tmem + lane_base + kColO + ch * 64;
+      const float mc = mx * sl2;   // -inf if no key of this half is visible yet
+      const bool first = (m_ref == -INFINITY);             // nothing accumulated for this row yet
+      const bool need = !first && (mc > m_ref + kRescale);
+      if (__any_sync(FULL, need)) {  // warp-uniform: the TMEM accesses below are warp-wide
+        const float f = need ? ex2(m_ref - mc) : 1.f;
+        if (need) {
+          l *= f;
+          m_ref = mc;
+        }
+        const int j = kt - 1;       // (kt >= 1 here) every earlier P V has landed in O
+        if (!mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
+          timed_out = true;
+          break;
+        }
+        tc::fence_after_sync();
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t ov[32];
-            tc::ld_32x32b_x32(o_addr + cc * 32, ov);
-            tc::wait_ld();
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t ov[32];
+          tc::ld_32x32b_x32(o_self + cc * 32, ov);
+          tc::wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
-            tc::st_32x32b_x32(o_addr + cc * 32, ov);
-          }
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+          tc::st_32x32b_x32(o_self + cc * 32, ov);
         }
       }
+      if (first) m_ref = mc;
 
       // P in two terms of the input dtype, written over this half's S columns
-      float ls = 0.f;
+      const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_ref, -m_ref);
+      const float2 neg1 = make_float2(-1.f, -1.f);
+      float2 ls = make_float2(0.f, 0.f);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float s0 = __uint_as_float(v[cc][2 * j]), s1 = __uint_as_float(v[cc][2 * j + 1]);
-          float p0 = exp2f(fmaf(s0, sl2, -m_ref));
-          float p1 = exp2f(fmaf(s1, sl2, -m_ref));
+          const float2 e = __ffma2_rn(make_float2(__uint_as_float(v[cc][2 * j]), __uint_as_float(v[cc][2 * j + 1])),
+                                      sl2v, negm);
+          float2 pr = make_float2(ex2(e.x), ex2(e.y));
           if (!full) {
             const int key = kbase + cc * 32 + 2 * j;
-            p0 = (key <= lim) ? p0 : 0.f;
-            p1 = (key + 1 <= lim) ? p1 : 0.f;
+            pr.x = (key <= lim) ? pr.x : 0.f;
+            pr.y = (key + 1 <= lim) ? pr.y : 0.f;
           }
-          ls += p0 + p1;
-          pk[j] = Pack<T>::from_f2(p0, p1);
-          const float2 h2 = Pack<T>::to_f2(pk[j]);
-          pk[16 + j] = Pack<T>::from_f2(p0 - h2.x, p1 - h2.y);
+          ls = __fadd2_rn(ls, pr);
+          pk[j] = Pack<T>::from_f2(pr.x, pr.y);
+          const float2 lo = __ffma2_rn(Pack<T>::to_f2(pk[j]), neg1, pr);  // P - P_hi, exact
+          pk[16 + j] = Pack<T>::from_f2(lo.x, lo.y);
         }
         tc::st_32x32b_x32(s_addr + cc * 32, pk);
       }
       tc::wait_st();
-      l += ls;
+      l += ls.x + ls.y;
 
       if (kt == kt_ctx) {
-        // value rows of keys >= ctx (partial last page, pages past the end)
-        if (!mbar_wait(&bars.kv_full[kt % kStages], (kt / kStages) & 1)) {
+        // value rows of keys >= ctx in this half (partial last page, pages past
+        // the end); this half's P V product is the only one that reads them
+        const int vb = kt % kVStages;
+        if (!mbar_wait(&bars.v_full[vb], (kt / kVStages) & 1)) {
           timed_out = true;
           break;
         }
-        const int z0 = ctx - kt * 128;
-        uint8_t *vbase = smem + OFF_KV + (kt % kStages) * STAGE_BYTES + 2 * kHalf;
-        for (int idx = tid; idx < (128 - z0) * 16; idx += kSoftmaxThreads) {
+        const int z0 = max(ctx - kt * 128, ch * 64), z1 = ch * 64 + 64;
+        uint8_t *vbase = smem + OFF_V + vb * 2 * kHalf;
+        for (int idx = tid - ch * 128; idx < (z1 - z0) * 16; idx += kSoftmaxThreads / 2) {
           const int row = z0 + (idx >> 4), part = idx & 15;
           *reinterpret_cast<uint4 *>(vbase + (part >> 3) * kHalf + row * 128 + (part & 7) * 16) =
               make_uint4(0, 0, 0, 0);
@@ -357,34 +374,46 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         fence_proxy_async_smem();
       }
       tc::fence_before_sync();
-      mbar_arrive(&bars.p_full[kt & 1]);
+      mbar_arrive(&bars.p_full[ch][sb]);
     }
 
     if (!timed_out) {
       const int j = nkt - 1;
       if (mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
         tc::fence_after_sync();
-        // row sum: the two halves exchange theirs (next phase of the exchange barriers)
-        float *xl = xbuf + (nkt & 1) * 256;
-        xl[ch * 128 + r] = l;
-        mbar_arrive(&bars.x_full[nkt & 1]);
-        if (mbar_wait(&bars.x_full[nkt & 1], (nkt >> 1) & 1)) {
-          const float inv = 1.f / (l + xl[(1 - ch) * 128 + r]);
+        // merge the two halves of the row
+        float2 *xm = reinterpret_cast<float2 *>(smem + OFF_X);
+        xm[ch * 128 + r] = make_float2(m_ref, l);
+        mbar_arrive(&bars.x_full);
+        if (mbar_wait(&bars.x_full, 0)) {
+          const float2 other = xm[(1 - ch) * 128 + r];
+          const float m0 = ch == 0 ? m_ref : other.x, l0 = ch == 0 ? l : other.y;
+          const float m1 = ch == 0 ? other.x : m_ref, l1 = ch == 0 ? other.y : l;
+          const float M = fmaxf(m0, m1);
+          const float f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M);
+          const float f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M);
+          const float inv = 1.f / (l0 * f0 + l1 * f1);
+          const float g0 = f0 * inv, g1 = f1 * inv;
           T *op = reinterpret_cast<T *>(p.out) + ((int64_t)(row0 + tq) * p.num_q_heads + head) * kHeadDim + ch * 64;
-          const uint32_t o_addr = tmem + lane_base + kColO + ch * 64;
+          const uint32_t o0 = tmem + lane_base + kColO + ch * 64, o1 = o0 + 128;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            uint32_t ov[32];
-            tc::ld_32x32b_x32(o_addr + cc * 32, ov);  // warp-wide; only rows of the chunk are stored
+            uint32_t a[32], b[32];
+            tc::ld_32x32b_x32(o0 + cc * 32, a);  // warp-wide; only rows of the chunk are stored
+            tc::ld_32x32b_x32(o1 + cc * 32, b);
             tc::wait_ld();
             if (tq < len) {
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  y[e] = __uint_as_float(a[8 * i + e]) * g0 + __uint_as_float(b[8 * i + e]) * g1;
                 uint4 w;
-                w.x = Pack<T>::from_f2(__uint_as_float(ov[8 * i + 0]) * inv, __uint_as_float(ov[8 * i + 1]) * inv);
-                w.y = Pack<T>::from_f2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
-                w.z = Pack<T>::from_f2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
-                w.w = Pack<T>::from_f2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
+                w.x = Pack<T>::from_f2(y[0], y[1]);
+                w.y = Pack<T>::from_f2(y[2], y[3]);
+                w.z = Pack<T>::from_f2(y[4], y[5]);
+                w.w = Pack<T>::from_f2(y[6], y[7]);
                 *reinterpret_cast<uint4 *>(op + cc * 32 + 8 * i) = w;
               }
             }
