@@ -254,6 +254,8 @@ pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts
 
   PrefillParams p{};
   p.q = q;
+  p.k_cache = pool->k_cache;
+  p.v_cache = pool->v_cache;
   p.chunk_starts = chunk_starts;
   p.chunk_lens = chunk_lens;
   p.block_tables = block_tables;

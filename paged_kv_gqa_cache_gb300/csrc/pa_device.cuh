@@ -142,6 +142,16 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// 16-byte asynchronous global → shared copy; bytes past `src_bytes` (0 or 16)
+// are zero-filled and not read.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor cores reading operands written by threads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -71,6 +71,8 @@ bool decode_workspace_carve(void *ws, size_t bytes, int num_seqs, int num_q_head
 // ---- chunked prefill (tcgen05 tensor cores) -------------------------------------
 struct PrefillParams {
   const void *q;             // [rows][Hq][128]
+  const void *k_cache;       // pool [num_blocks][16][Hkv][128]
+  const void *v_cache;
   const int32_t *chunk_starts;
   const int32_t *chunk_lens;
   const int32_t *block_tables;

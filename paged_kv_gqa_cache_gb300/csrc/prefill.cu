@@ -13,9 +13,11 @@
 // consecutive tokens of the chunk x the G query heads sharing that KV head,
 // so every K/V tile it reads serves all G heads.  Row r of the tile is token
 // t0 + r / G, head h * G + r % G (the Q tile is one TMA box per 64-dim half).
-// Keys stream in tiles of N = 128 (8 pages, one TMA box per page and 64-dim
-// half): K through a 3-stage ring released as soon as S is computed, V
-// through a 2-stage ring released after the PV product.  Per key tile kt:
+// Keys stream in tiles of N = 128 (8 pages, two 2 KB TMA boxes per page: the
+// 64-dim halves of 16 keys, 128-byte swizzled): K through a 3-stage ring
+// released as soon as S is computed, V through a 2-stage ring released after
+// the PV product, each filled by its own loader warp whose lanes issue the
+// boxes of a tile in parallel.  Per key tile kt:
 //   S = Q K^T     tcgen05.mma kind::f16, A and B from shared memory (K-major),
 //                 fp32 into TMEM columns S[kt % 2].
 //   softmax       8 warps; the two warps on TMEM lane quarter q own rows
@@ -35,13 +37,13 @@
 // it by more than 2^8, so the threads rarely touch O.  The epilogue merges the
 // two halves of each row, O = O_0 2^(m_0 - M) + O_1 2^(m_1 - M) over
 // l_0 2^(m_0 - M) + l_1 2^(m_1 - M), and stores it in the input dtype.
-// Warp 8 issues the TMA loads, warp 9 owns TMEM and issues the MMAs (one thread
-// each); mbarriers hand tiles between the roles and every wait is bounded.
-// Keys above the diagonal are masked per element on the tiles that cross it (a
-// warp-uniform test picks the unmasked path elsewhere) and never loaded past
-// the tile holding the tile's last query.  Value rows past the sequence's last
-// key are zeroed in shared memory before the PV product so that a zero
-// probability never meets a non-finite value.
+// Warps 8 and 9 load K (and the Q tile) and V, warp 10 owns TMEM and issues the
+// MMAs (one thread); mbarriers hand tiles between the roles and every wait is
+// bounded.  Keys above the diagonal are masked per element on the tiles that
+// cross it (a warp-uniform test picks the unmasked path elsewhere) and never
+// loaded past the tile holding the tile's last query.  Value rows past the
+// sequence's last key are zeroed in shared memory before the PV product so that
+// a zero probability never meets a non-finite value.
 #include <type_traits>
 
 #include "tcgen05.cuh"
@@ -51,8 +53,8 @@ namespace {
 
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kWarpTma = kSoftmaxWarps, kWarpMma = kSoftmaxWarps + 1;
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kWarpLoadK = kSoftmaxWarps, kWarpLoadV = kSoftmaxWarps + 1, kWarpMma = kSoftmaxWarps + 2;
+constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
 constexpr int kHalf = 16384;                        // 128 rows x 64 elements x 2 bytes
 constexpr int kKStages = 3, kVStages = 2;
 constexpr int OFF_Q = 0;                            // Q: two 64-dim halves
@@ -82,9 +84,9 @@ struct Bars {
 };
 
 // Fetch the 8 pages of key tile kt of one pool into `dst` (two 64-dim half
-// boxes per page), completing on `bar`; called by the whole producer warp:
-// lane j < 16 loads half j % 2 of page j / 2.  Pages past the sequence are
-// skipped; a page whose block id is out of range is zeroed and reported.
+// boxes per page), completing on `bar`; called by a whole loader warp: lane
+// j < 16 loads half j % 2 of page j / 2.  Pages past the sequence are skipped;
+// a page whose block id is out of range is zeroed and reported.
 __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int kt, int h,
                                           int npages, const int32_t *sbt, const int32_t *bt,
                                           const PrefillParams &p, int c, int lane) {
@@ -177,38 +179,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
   bool timed_out = false;
 
-  if (warp == kWarpTma) {
-    // ---------------- TMA producer warp: K two tiles ahead, V as its stage frees ----------------
+  if (warp == kWarpLoadK || warp == kWarpLoadV) {
+    // ---------------- loader warps: K two tiles ahead, V as its stage frees ----------------
+    const bool is_k = warp == kWarpLoadK;
     int32_t *sbt = reinterpret_cast<int32_t *>(smem + OFF_BT);
     const int cached = min(min(npages, nkt * 8), kBtCache);
-    for (int i = lane; i < cached; i += 32) sbt[i] = __ldg(bt + i);
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf);
-      tma_load_3d(smem + OFF_Q, &qmap, &bars.q_full, 0, h * G, row0 + t0);
-      tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
+    if (is_k) {
+      for (int i = lane; i < cached; i += 32) sbt[i] = __ldg(bt + i);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf);
+        tma_load_3d(smem + OFF_Q, &qmap, &bars.q_full, 0, h * G, row0 + t0);
+        tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
+      }
     }
-    for (int i = 0; i < 2 && i < nkt; ++i)
-      load_tile(smem + OFF_K + i * 2 * kHalf, &kmap, &bars.k_full[i], i, h, npages, sbt, bt, p, c, lane);
-    for (int kt = 0; kt < nkt; ++kt) {
-      const int kn = kt + 2;
-      if (kn < nkt) {
-        const int b = kn % kKStages;
-        if (kn >= kKStages && !mbar_wait(&bars.k_free[b], ((kn - kKStages) / kKStages) & 1)) {
-          timed_out = true;
-          break;
-        }
-        load_tile(smem + OFF_K + b * 2 * kHalf, &kmap, &bars.k_full[b], kn, h, npages, sbt, bt, p, c, lane);
-      }
-      const int vb = kt % kVStages;
-      if (kt >= kVStages) {
-        const int j = kt - kVStages;
-        if (!mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
+    // the V loader reads the block ids the K loader cached (both are inside the producer pair)
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    const CUtensorMap *map = is_k ? &kmap : &vmap;
+    const int nst = is_k ? kKStages : kVStages;
+    uint8_t *ring = smem + (is_k ? OFF_K : OFF_V);
+    uint64_t *full = is_k ? bars.k_full : bars.v_full;
+    for (int t = 0; t < nkt; ++t) {
+      const int st = t % nst;
+      if (t >= nst) {  // the stage's previous tile must be consumed
+        const int j = t - nst;
+        const bool ok = is_k ? mbar_wait(&bars.k_free[st], (j / nst) & 1)
+                             : mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1);
+        if (!ok) {
           timed_out = true;
           break;
         }
       }
-      load_tile(smem + OFF_V + vb * 2 * kHalf, &vmap, &bars.v_full[vb], kt, h, npages, sbt, bt, p, c, lane);
+      load_tile(ring + st * 2 * kHalf, map, &full[st], t, h, npages, sbt, bt, p, c, lane);
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
@@ -264,7 +265,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // ---------------- softmax + epilogue (warps 0..7) ----------------
     const int quad = warp & 3, ch = warp >> 2;       // TMEM lane quarter, key half of every tile
     const int r = quad * 32 + lane;                  // tile row = TMEM lane
-    const int tid = warp * 32 + lane;                // 0 .. 255
     const int tq = t0 + r / G;                       // query token within the chunk
     const int head = h * G + r % G;
     const int lim = min(start + tq, ctx - 1);        // last visible key position of this row
@@ -366,7 +366,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         const int z0 = max(ctx - kt * 128, ch * 64), z1 = ch * 64 + 64;
         uint8_t *vbase = smem + OFF_V + vb * 2 * kHalf;
-        for (int idx = tid - ch * 128; idx < (z1 - z0) * 16; idx += kSoftmaxThreads / 2) {
+        for (int idx = (warp & 3) * 32 + lane; idx < (z1 - z0) * 16; idx += kSoftmaxThreads / 2) {
           const int row = z0 + (idx >> 4), part = idx & 15;
           *reinterpret_cast<uint4 *>(vbase + (part >> 3) * kHalf + row * 128 + (part & 7) * 16) =
               make_uint4(0, 0, 0, 0);
