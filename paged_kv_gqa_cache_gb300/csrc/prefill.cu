@@ -213,9 +213,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
+    // Descriptors are built once; a k-step or a ring stage only moves the start
+    // address field (bits 0..13, address >> 4), so each MMA costs a 64-bit add.
+    // Shared-memory offsets stay below 256 KB, so the field never carries over.
     if (lane == 0) {
       if (!mbar_wait(&bars.q_full, 0)) timed_out = true;
-      const uint32_t qa = smem_u32(smem + OFF_Q);
+      const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
+      const uint64_t kdesc0 = tc::desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
+      const uint64_t vdesc0 = tc::desc_sw128(smem_u32(smem + OFF_V), kHalf, 1024);
+      constexpr uint64_t kStageStep = (2 * kHalf) >> 4;   // one ring stage
+      constexpr uint64_t kHalfStep = kHalf >> 4;          // the other 64-dim half
       for (int kt = 0; kt <= nkt && !timed_out; ++kt) {
         if (kt < nkt) {
           const int b = kt % kKStages, sb = kt & 1;
@@ -224,12 +231,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             break;
           }
           tc::fence_after_sync();
-          const uint32_t ka = smem_u32(smem + OFF_K + b * 2 * kHalf);
+          const uint64_t kdesc = kdesc0 + (uint64_t)b * kStageStep;
+          const uint32_t s_col = tmem + sb * 128;
+          tc::mma_f16(s_col, qdesc, kdesc, IDESC_S, 0u);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            tc::mma_f16(tmem + sb * 128, tc::desc_sw128(qa + off, 16, 1024), tc::desc_sw128(ka + off, 16, 1024),
-                        IDESC_S, kk > 0);
+          for (int kk = 1; kk < 8; ++kk) {
+            const uint64_t off = (uint64_t)((kk >> 2) * kHalfStep + (kk & 3) * 2);   // 16-element k-step
+            tc::mma_f16(s_col, qdesc + off, kdesc + off, IDESC_S, 1u);
           }
           tc::commit(&bars.s_full[sb]);
           tc::commit(&bars.k_free[b]);
@@ -240,20 +248,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             timed_out = true;
             break;
           }
-          const uint32_t va = smem_u32(smem + OFF_V + (j % kVStages) * 2 * kHalf);
-          for (int half = 0; half < 2 && !timed_out; ++half) {
+          const uint64_t vdesc = vdesc0 + (uint64_t)(j % kVStages) * kStageStep;
+          const uint32_t p_col = tmem + sj * 128;
+          const uint32_t first = j > 0 ? 1u : 0u;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
             if (!mbar_wait(&bars.p_full[half][sj], (j >> 1) & 1)) {
               timed_out = true;
               break;
             }
             tc::fence_after_sync();
+            const uint32_t o_col = tmem + kColO + half * 128;
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-              const int kk = half * 4 + k4;  // 16-key step within the tile
-              const uint32_t a_hi = tmem + sj * 128 + 32 * (kk >> 1) + 8 * (kk & 1);
-              const uint64_t bdesc = tc::desc_sw128(va + kk * 2048, kHalf, 1024);
-              tc::mma_f16_ts(tmem + kColO + half * 128, a_hi, bdesc, IDESC_O, (j > 0 || k4 > 0) ? 1u : 0u);
-              tc::mma_f16_ts(tmem + kColO + half * 128, a_hi + 16, bdesc, IDESC_O, 1u);
+              const int kk = half * 4 + k4;  // 16-key step within the tile: V rows 16 kk .. 16 kk + 15
+              const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
+              const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
+              tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, k4 > 0 ? 1u : first);
+              tc::mma_f16_ts(o_col, a_hi + 16, bdesc, IDESC_O, 1u);
             }
           }
           if (timed_out) break;
