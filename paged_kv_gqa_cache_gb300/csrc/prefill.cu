@@ -63,8 +63,11 @@ constexpr int OFF_V = OFF_K + kKStages * 2 * kHalf; // V stages: {lo, hi} halves
 constexpr int OFF_X = OFF_V + kVStages * 2 * kHalf; // epilogue (m, l) exchange [2][128] float2
 constexpr int kBtCache = 2048;                      // block ids of the chunk cached in shared memory
 constexpr int OFF_BT = OFF_X + 2 * 128 * 8;
-constexpr int OFF_BAR = OFF_BT + kBtCache * 4;
+constexpr int OFF_STAGE = OFF_BT + kBtCache * 4;     // epilogue: 1 KB of staging per softmax warp
+constexpr int kStageBytes = 1024;
+constexpr int OFF_BAR = OFF_STAGE + kSoftmaxWarps * kStageBytes;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;    // + barriers (< 256 B) + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;                 // S/P 0, S/P 1, O_0, O_1
 constexpr uint32_t kColO = 256;
 constexpr float kRescale = 8.f;                     // log2 of the largest P before O is rescaled
@@ -107,6 +110,35 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, 
   if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(okmask) * 2048u);
   __syncwarp();
   if (ok) tma_load_4d(box, map, bar, half * 64, h, 0, id);
+}
+
+// Each lane of a warp holds 64 contiguous output bytes of its own row (rows are
+// 256 bytes to kilobytes apart in memory).  Store them 16 rows at a time through
+// the warp's 1 KB staging area, so that 4 lanes write each row's 64 bytes
+// together; the 16-byte pieces are XOR-swizzled by row against bank conflicts.
+__device__ __forceinline__ void store_rows_coalesced(uint4 *stage, void *dst, bool ok, const uint4 (&v)[4],
+                                                     int lane) {
+  constexpr unsigned FULL = 0xffffffffu;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    if ((lane >> 4) == pass) {
+      const int row = lane & 15;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) stage[row * 4 + (i ^ (row & 3))] = v[i];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int idx = lane + 32 * k;  // 64 pieces: row idx / 4, piece idx % 4
+      const int row = idx >> 2, piece = idx & 3;
+      const int src = pass * 16 + row;
+      uint4 *d = reinterpret_cast<uint4 *>(__shfl_sync(FULL, reinterpret_cast<unsigned long long>(dst), src));
+      const bool okr = __shfl_sync(FULL, ok ? 1 : 0, src) != 0;
+      const uint4 w = stage[row * 4 + (piece ^ (row & 3))];
+      if (okr) d[piece] = w;
+    }
+    __syncwarp();
+  }
 }
 
 template <typename T, int G>
@@ -414,21 +446,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             tc::ld_32x32b_x32(o0 + cc * 32, a);  // warp-wide; only rows of the chunk are stored
             tc::ld_32x32b_x32(o1 + cc * 32, b);
             tc::wait_ld();
-            if (tq < len) {
+            uint4 w[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                float y[8];
+            for (int i = 0; i < 4; ++i) {
+              float y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  y[e] = __uint_as_float(a[8 * i + e]) * g0 + __uint_as_float(b[8 * i + e]) * g1;
-                uint4 w;
-                w.x = Pack<T>::from_f2(y[0], y[1]);
-                w.y = Pack<T>::from_f2(y[2], y[3]);
-                w.z = Pack<T>::from_f2(y[4], y[5]);
-                w.w = Pack<T>::from_f2(y[6], y[7]);
-                *reinterpret_cast<uint4 *>(op + cc * 32 + 8 * i) = w;
-              }
+              for (int e = 0; e < 8; ++e)
+                y[e] = __uint_as_float(a[8 * i + e]) * g0 + __uint_as_float(b[8 * i + e]) * g1;
+              w[i].x = Pack<T>::from_f2(y[0], y[1]);
+              w[i].y = Pack<T>::from_f2(y[2], y[3]);
+              w[i].z = Pack<T>::from_f2(y[4], y[5]);
+              w[i].w = Pack<T>::from_f2(y[6], y[7]);
             }
+            // warp-wide (every lane takes part); rows past the chunk are not stored
+            store_rows_coalesced(reinterpret_cast<uint4 *>(smem + OFF_STAGE + warp * kStageBytes), op + cc * 32,
+                                 tq < len, w, lane);
           }
         } else {
           timed_out = true;

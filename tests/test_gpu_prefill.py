@@ -116,3 +116,31 @@ def test_prefill_inconsistent_chunk_is_reported_and_untouched():
     assert torch.count_nonzero(out[40:]) == 0
     ref = oracle_prefill(case, kc, vc)
     check_close(out[:40], ref[:40], "valid chunk")
+
+
+def test_prefill_long_prefixes():
+    # few query tiles, each reading many key tiles (6000- and 3000-token prefixes)
+    case = workloads.build_case("long-prefix", "bf16", 32, 8, seed=16, device=DEV, chunks=[(6000, 64), (3000, 33)])
+    prefill_and_check(case, "long prefixes")
+
+
+def test_prefill_is_deterministic():
+    case = workloads.build_case("repeat", "bf16", 16, 8, seed=21, device=DEV, chunks=[(700, 300), (0, 200)])
+    out1, kc, vc = run_prefill(case)
+    out2 = pa.paged_attn_prefill_chunk(case.q_chunks[0], case.chunk_starts, case.chunk_lens, kc, vc,
+                                       case.chunk_block_tables, case.chunk_context_lens, case.scale,
+                                       max_chunk_len=300)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+
+
+def test_prefill_many_small_chunks():
+    rng = np.random.default_rng(17)
+    chunks = [(int(rng.integers(0, 900)), int(rng.integers(1, 8))) for _ in range(300)]
+    case = workloads.build_case("many-chunks", "f16", 16, 8, seed=17, device=DEV, chunks=chunks)
+    prefill_and_check(case, "300 chunks", max_chunk_len=8)
+
+
+def test_prefill_single_short_chunk():
+    case = workloads.build_case("tiny", "bf16", 8, 8, seed=18, device=DEV, chunks=[(0, 3)])
+    prefill_and_check(case, "one 3-token chunk")
