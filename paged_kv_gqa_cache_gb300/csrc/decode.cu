@@ -122,12 +122,113 @@ __device__ __forceinline__ void advance(Cursor &c, const int32_t *prefix, int n,
   c.pages = (c.s < n) ? prefix[c.s + 1] - prefix[c.s] : 1;
 }
 
+// Scores, online-softmax update and P V of one 16-key page for the G query
+// heads of a KV head: K at kst, V at kst + 4096 (one warp; nv valid keys).
+// q holds this lane's dims of the G query rows (pre-scaled, log2 domain);
+// (m, l, o) is the running state (m warp-uniform, l per lane, o for the lane's
+// 4 dims).  pbuf2 is the warp's [16 keys][G] scratch for the probabilities.
+template <typename T, int G>
+__device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const float2 (&q)[G][Layout<G>::DPL / 2],
+                                            float2 (&o)[G][2], float (&m)[G], float (&l)[G], float2 *pbuf2,
+                                            int lane) {
+  using Ly = Layout<G>;
+  constexpr int NQ = Ly::NQ, NT = Ly::NT, NP = Ly::NP, CPL = Ly::CPL;
+  const int qd = lane % NQ;  // which dim slice of a key this lane scores
+  const int tk = lane / NQ;  // which key of a pass
+  const int rot = tk % CPL;  // chunk rotation of this lane's keys (NT is a multiple of CPL)
+  const float neg_inf = -INFINITY;
+  const uint8_t *vst = kst + 4096;
+
+  // scores: NP passes of NT keys; lanes of one key hold slices of its dims
+  float sc[NP][G];
+#pragma unroll
+  for (int ps = 0; ps < NP; ++ps) {
+    const int t = ps * NT + tk;
+    float2 acc[G];
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) acc[gg] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int chunk = qd + NQ * ((i + rot) % CPL);
+      const uint4 u = *reinterpret_cast<const uint4 *>(kst + t * 256 + chunk * 16);
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 k2 = Pack<T>::to_f2(wd[e]);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) acc[gg] = __ffma2_rn(q[gg][i * 4 + e], k2, acc[gg]);
+      }
+    }
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      float a = acc[gg].x + acc[gg].y;
+#pragma unroll
+      for (int off = 1; off < NQ; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
+      sc[ps][gg] = (t < nv) ? a : neg_inf;
+    }
+  }
+
+  // online softmax update (log2 domain)
+#pragma unroll
+  for (int gg = 0; gg < G; ++gg) {
+    float mp = sc[0][gg];
+#pragma unroll
+    for (int ps = 1; ps < NP; ++ps) mp = fmaxf(mp, sc[ps][gg]);
+#pragma unroll
+    for (int off = NQ; off < 32; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(FULL, mp, off));
+    const float mn = fmaxf(m[gg], mp);
+    const float alpha = exp2f(m[gg] - mn);
+    m[gg] = mn;
+    float ls = 0.f;
+#pragma unroll
+    for (int ps = 0; ps < NP; ++ps) {
+      const float pr = exp2f(sc[ps][gg] - mn);
+      ls += pr;
+      if (qd == 0) pbuf2[(ps * NT + tk) * G + gg] = make_float2(pr, pr);
+    }
+    l[gg] = l[gg] * alpha + ls;
+    const float2 a2 = make_float2(alpha, alpha);
+    o[gg][0] = __fmul2_rn(o[gg][0], a2);
+    o[gg][1] = __fmul2_rn(o[gg][1], a2);
+  }
+  __syncwarp();
+
+  // weighted sum of values: this lane owns dims [4 * lane, 4 * lane + 4)
+  auto pv_token = [&](int t) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(vst + t * 256 + 8 * lane);
+    const float2 v01 = Pack<T>::to_f2(u.x);
+    const float2 v23 = Pack<T>::to_f2(u.y);
+    float2 pp[G];
+    if constexpr (G == 1) {
+      pp[0] = pbuf2[t];
+    } else {
+#pragma unroll
+      for (int gg = 0; gg < G; gg += 2) {
+        const float4 x = *reinterpret_cast<const float4 *>(pbuf2 + t * G + gg);
+        pp[gg] = make_float2(x.x, x.y);
+        pp[gg + 1] = make_float2(x.z, x.w);
+      }
+    }
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      o[gg][0] = __ffma2_rn(pp[gg], v01, o[gg][0]);
+      o[gg][1] = __ffma2_rn(pp[gg], v23, o[gg][1]);
+    }
+  };
+  if (nv == kBlock) {
+#pragma unroll
+    for (int t = 0; t < kBlock; ++t) pv_token(t);
+  } else {
+    for (int t = 0; t < nv; ++t) pv_token(t);
+  }
+}
+
 template <typename T, int G>
 __global__ void __launch_bounds__(NW * 32)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const DecodeParams p) {
   using Ly = Layout<G>;
-  constexpr int NQ = Ly::NQ, NT = Ly::NT, NP = Ly::NP, DPL = Ly::DPL, CPL = Ly::CPL;
+  constexpr int NQ = Ly::NQ, DPL = Ly::DPL, CPL = Ly::CPL;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -257,91 +358,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 
     if (!((bad_mask >> st) & 1u)) {
       const int nv = min(kBlock, ctx - cc.page * kBlock);  // valid keys in this page
-      const uint8_t *kst = stages + st * STAGE;
-      const uint8_t *vst = kst + 4096;
-
-      // scores: NP passes of NT keys; lanes of one key hold slices of its dims
-      float sc[NP][G];
-#pragma unroll
-      for (int ps = 0; ps < NP; ++ps) {
-        const int t = ps * NT + tk;
-        float2 acc[G];
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) acc[gg] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-          const int chunk = qd + NQ * ((i + rot) % CPL);
-          const uint4 u = *reinterpret_cast<const uint4 *>(kst + t * 256 + chunk * 16);
-          const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 k2 = Pack<T>::to_f2(wd[e]);
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg) acc[gg] = __ffma2_rn(q[gg][i * 4 + e], k2, acc[gg]);
-          }
-        }
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          float a = acc[gg].x + acc[gg].y;
-#pragma unroll
-          for (int off = 1; off < NQ; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
-          sc[ps][gg] = (t < nv) ? a : neg_inf;
-        }
-      }
-
-      // online softmax update (log2 domain)
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        float mp = sc[0][gg];
-#pragma unroll
-        for (int ps = 1; ps < NP; ++ps) mp = fmaxf(mp, sc[ps][gg]);
-#pragma unroll
-        for (int off = NQ; off < 32; off <<= 1) mp = fmaxf(mp, __shfl_xor_sync(FULL, mp, off));
-        const float mn = fmaxf(m[gg], mp);
-        const float alpha = exp2f(m[gg] - mn);
-        m[gg] = mn;
-        float ls = 0.f;
-#pragma unroll
-        for (int ps = 0; ps < NP; ++ps) {
-          const float pr = exp2f(sc[ps][gg] - mn);
-          ls += pr;
-          if (qd == 0) pbuf2[(ps * NT + tk) * G + gg] = make_float2(pr, pr);
-        }
-        l[gg] = l[gg] * alpha + ls;
-        const float2 a2 = make_float2(alpha, alpha);
-        o[gg][0] = __fmul2_rn(o[gg][0], a2);
-        o[gg][1] = __fmul2_rn(o[gg][1], a2);
-      }
-      __syncwarp();
-
-      // weighted sum of values: this lane owns dims [4 * lane, 4 * lane + 4)
-      auto pv_token = [&](int t) {
-        const uint2 u = *reinterpret_cast<const uint2 *>(vst + t * 256 + 8 * lane);
-        const float2 v01 = Pack<T>::to_f2(u.x);
-        const float2 v23 = Pack<T>::to_f2(u.y);
-        float2 pp[G];
-        if constexpr (G == 1) {
-          pp[0] = pbuf2[t];
-        } else {
-#pragma unroll
-          for (int gg = 0; gg < G; gg += 2) {
-            const float4 x = *reinterpret_cast<const float4 *>(pbuf2 + t * G + gg);
-            pp[gg] = make_float2(x.x, x.y);
-            pp[gg + 1] = make_float2(x.z, x.w);
-          }
-        }
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          o[gg][0] = __ffma2_rn(pp[gg], v01, o[gg][0]);
-          o[gg][1] = __ffma2_rn(pp[gg], v23, o[gg][1]);
-        }
-      };
-      if (nv == kBlock) {
-#pragma unroll
-        for (int t = 0; t < kBlock; ++t) pv_token(t);
-      } else {
-        for (int t = 0; t < nv; ++t) pv_token(t);
-      }
+      decode_page<T, G>(stages + st * STAGE, nv, q, o, m, l, pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
 
@@ -458,14 +475,245 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   griddep_launch_dependents();
 }
 
+// ---- one cluster per item (few items: every item gets one or two SMs) ------------
+// The item's pages are dealt round-robin to the kItemWarps warps of each CTA of
+// a cluster of 1 or 2 CTAs, each warp streaming its pages through its own TMA
+// ring (two CTAs double the bytes in flight for the item).  The
+// warps' states (m, l, o) are then written to their own CTA's shared memory
+// (reusing the stage buffers) and merged by CTA 0, which reads the other CTA's
+// through distributed shared memory, and writes the item's output.  No
+// workspace and no second kernel.
+constexpr int kItemWarps = 8;
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kItemWarps * 32, 1)
+decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                   const DecodeParams p) {
+  using Ly = Layout<G>;
+  constexpr int NQ = Ly::NQ, DPL = Ly::DPL, CPL = Ly::CPL;
+  constexpr int kMerge = 4 + kHeadDim;  // floats per (warp, head): m, l, 2 unused, o[128] (16-byte aligned)
+  static_assert(G * kMerge * 4 <= kStages * STAGE, "merge buffer fits a warp's stages");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *stages = smem + warp * kStages * STAGE;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kItemWarps * kStages * STAGE) + warp * kStages;
+  float2 *pbuf2 = reinterpret_cast<float2 *>(smem + kItemWarps * kStages * STAGE + kItemWarps * kStages * 8) +
+                  warp * 16 * G;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
+    fence_mbar_init();
+  }
+  griddep_wait();
+
+  const int ncta = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+  const int item = blockIdx.x / ncta;
+  const int hkv = p.num_kv_heads;
+  const int s = item / hkv, h = item % hkv;
+  // Warp gw of the item's nw warps takes pages gw, gw + nw, gw + 2 nw, ...: its
+  // first block ids do not depend on the length, so the length, the block ids
+  // and q are all fetched at once.
+  const int gw = rank * kItemWarps + warp, nw = ncta * kItemWarps;
+  const int32_t *bt = p.block_tables + (int64_t)s * p.max_blocks_per_seq;
+  const int ctx = __ldg(p.context_lens + s);
+  int win_base = 0;  // window of 32 block ids: lane j holds page gw + nw (win_base + j)
+  int32_t win = (gw + nw * lane < p.max_blocks_per_seq) ? __ldg(bt + gw + nw * lane) : -1;
+
+  const int qd = lane % NQ, tk = lane / NQ, rot = tk % CPL;
+  float2 q[G][DPL / 2];
+  float2 o[G][2];
+  float m[G], l[G];
+  {
+    const T *qp = reinterpret_cast<const T *>(p.q) + ((int64_t)s * p.num_q_heads + (int64_t)h * G) * kHeadDim;
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int chunk = qd + NQ * ((i + rot) % CPL);
+        const uint4 u = *reinterpret_cast<const uint4 *>(qp + gg * kHeadDim + chunk * 8);
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = Pack<T>::to_f2(wd[e]);
+          q[gg][i * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+        }
+      }
+      m[gg] = -INFINITY;
+      l[gg] = 0.f;
+      o[gg][0] = make_float2(0.f, 0.f);
+      o[gg][1] = make_float2(0.f, 0.f);
+    }
+  }
+  if (ctx < 1 || ctx > p.max_blocks_per_seq * kBlock) {  // uniform over the cluster; output untouched
+    if (h == 0 && rank == 0 && threadIdx.x == 0) set_error(p.err, PA_ERR_RANGE, s);
+    griddep_launch_dependents();
+    return;
+  }
+  const int pages = (ctx + kBlock - 1) / kBlock;
+  const int n = pages > gw ? (pages - gw + nw - 1) / nw : 0;  // pages of this warp
+
+  uint32_t bad_mask = 0;
+  auto issue = [&](int i, int st) {
+    const int pg = gw + nw * i;
+    if ((i & ~31) != win_base) {
+      win_base = i & ~31;
+      const int pj = gw + nw * (win_base + lane);
+      win = (pj < pages) ? __ldg(bt + pj) : -1;
+    }
+    const int blk = __shfl_sync(FULL, win, i & 31);
+    const bool ok = (unsigned)blk < (unsigned)p.num_blocks;
+    if (lane == 0) {
+      if (ok) {
+        uint8_t *dst = stages + st * STAGE;
+        mbar_arrive_expect_tx(&bars[st], STAGE);
+        tma_load_4d(dst, &kmap, &bars[st], 0, h, 0, blk);
+        tma_load_4d(dst + 4096, &vmap, &bars[st], 0, h, 0, blk);
+      } else {
+        set_error(p.err, PA_ERR_RANGE, s);
+        mbar_arrive(&bars[st]);
+      }
+    }
+    bad_mask = ok ? (bad_mask & ~(1u << st)) : (bad_mask | (1u << st));
+  };
+
+  const int npre = n < kStages ? n : kStages;
+  for (int i = 0; i < npre; ++i) issue(i, i);
+  bool timed_out = false;
+  for (int i = 0; i < n; ++i) {
+    const int st = i % kStages;
+    if (!mbar_wait(&bars[st], (uint32_t)((i / kStages) & 1))) {
+      if (lane == 0) set_error(p.err, PA_ERR_TIMEOUT, s);
+      // give the copies still in flight a short, bounded chance to land
+      for (int r = i + 1; r < (n < i + kStages ? n : i + kStages); ++r)
+        mbar_wait(&bars[r % kStages], (uint32_t)((r / kStages) & 1), kWaitLimitNs / 8);
+      timed_out = true;
+      break;
+    }
+    if (!((bad_mask >> st) & 1u)) {
+      const int nv = min(kBlock, ctx - (gw + nw * i) * kBlock);  // valid keys in this page
+      decode_page<T, G>(stages + st * STAGE, nv, q, o, m, l, pbuf2, lane);
+    }
+    __syncwarp();  // every lane is done with this stage and with pbuf
+    if (i + kStages < n) issue(i + kStages, st);
+  }
+
+  // ---- merge the warps' states in shared memory (the stage buffers are idle now) ----
+  __syncthreads();
+  float *mine = reinterpret_cast<float *>(stages);
+#pragma unroll
+  for (int gg = 0; gg < G; ++gg) {
+    float lt = l[gg];
+#pragma unroll
+    for (int off = NQ; off < 32; off <<= 1) lt += __shfl_xor_sync(FULL, lt, off);
+    float *dst = mine + gg * kMerge;
+    if (lane == 0) {
+      dst[0] = m[gg];
+      dst[1] = lt;
+    }
+    *reinterpret_cast<float4 *>(dst + 4 + 4 * lane) = make_float4(o[gg][0].x, o[gg][0].y, o[gg][1].x, o[gg][1].y);
+  }
+  if (ncta > 1) cluster_sync();  // the partials of both CTAs are written and visible
+  else __syncthreads();
+  if (rank == 0 && warp < G && !timed_out) {
+    const int gg = warp;
+    // state of warp w of CTA r (r = 0: own shared memory, else the peer's)
+    auto part = [&](int r, int w, int off) -> uint32_t {
+      const float *a = reinterpret_cast<const float *>(smem + w * kStages * STAGE) + gg * kMerge + off;
+      return r == 0 ? smem_u32(a) : map_to_rank(a, (uint32_t)r);
+    };
+    // every load first (they are independent), then the arithmetic
+    constexpr int kParts = 2 * kItemWarps;
+    float mv[kParts], lv[kParts];
+    float4 ov[kParts];
+#pragma unroll
+    for (int i = 0; i < kParts; ++i) {
+      const int r = i / kItemWarps, w = i % kItemWarps;
+      if (r < ncta) {
+        mv[i] = ld_cluster_f32(part(r, w, 0));
+        lv[i] = ld_cluster_f32(part(r, w, 1));
+        ov[i] = ld_cluster_v4(part(r, w, 4 + 4 * lane));
+      } else {
+        mv[i] = -INFINITY;
+        lv[i] = 0.f;
+        ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kParts; ++i) M = fmaxf(M, mv[i]);
+    float L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kParts; ++i) {
+      const float wgt = (mv[i] == -INFINITY) ? 0.f : exp2f(mv[i] - M);  // a warp without pages: weight 0
+      L += lv[i] * wgt;
+      O.x = fmaf(wgt, ov[i].x, O.x);
+      O.y = fmaf(wgt, ov[i].y, O.y);
+      O.z = fmaf(wgt, ov[i].z, O.z);
+      O.w = fmaf(wgt, ov[i].w, O.w);
+    }
+    const float inv = 1.f / L;
+    T *op = reinterpret_cast<T *>(p.out) + ((int64_t)s * p.num_q_heads + h * G + gg) * kHeadDim + 4 * lane;
+    uint2 pk;
+    pk.x = Pack<T>::from_f2(O.x * inv, O.y * inv);
+    pk.y = Pack<T>::from_f2(O.z * inv, O.w * inv);
+    *reinterpret_cast<uint2 *>(op) = pk;
+  }
+  if (ncta > 1) cluster_sync();  // CTA 0 has read the peer's shared memory: both may exit
+  griddep_launch_dependents();
+}
+
+int item_smem_bytes(int group) {
+  return 1024 + kItemWarps * kStages * STAGE + kItemWarps * kStages * 8 + kItemWarps * 16 * group * 8;
+}
+
 int split_smem_bytes(int group, int num_seqs) {
   return 1024 + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * group * 8 + (num_seqs + 1) * 4;
 }
 
+// A cluster per item pays off when every item gets its own SMs (two when they
+// fit) and the longest possible item, streamed by them (and the whole call
+// through HBM), still ends before the split path: the whole call spread over
+// all SMs, plus its fixed cost of a second launch and a merge through global
+// memory.  The per-SM and whole-GPU rates are conservative round numbers for
+// this part.  Returns the CTAs per item (1 or 2), or 0 for the split path.
+int item_ctas(int items, int max_pages_per_item) {
+  const int sms = sm_count();
+  if (items > sms) return 0;
+  const int ctas = 2 * items <= sms ? 2 : 1;
+  const double page_bytes = 2.0 * kBlock * kHeadDim * 2;
+  const double total_us = (double)items * max_pages_per_item * page_bytes / 6e6;         // ~6 TB/s of HBM
+  const double one_item_us = max_pages_per_item * page_bytes / (ctas * 250e3);          // ~250 GB/s per SM
+  const double item_us = 3.0 + (one_item_us > total_us ? one_item_us : total_us);
+  const double split_us = 8.0 + total_us;
+  return item_us < split_us ? ctas : 0;
+}
+
 template <typename T, int G>
 cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                         int max_workers, cudaStream_t stream) {
+                         int max_workers, int max_pages_per_item, cudaStream_t stream) {
   DecodeParams p = p0;
+  const int items = p.num_seqs * p.num_kv_heads;
+  const int ctas = item_ctas(items, max_pages_per_item);
+  if (ctas > 0) {
+    const int ismem = item_smem_bytes(G);
+    static bool item_configured = false;
+    if (!item_configured) {
+      cudaError_t e = cudaFuncSetAttribute(decode_item_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           ismem);
+      if (e != cudaSuccess) return e;
+      item_configured = true;
+    }
+    return launch_pdl_cluster(decode_item_kernel<T, G>, dim3(items * ctas), dim3(kItemWarps * 32), ismem, ctas,
+                              stream, kmap, vmap, p);
+  }
   const int smem = split_smem_bytes(G, p.num_seqs);
   // Per instantiation: raise the dynamic shared-memory limit and cache the
   // occupancy for the largest size seen (launch-time API calls stay out of
@@ -521,12 +769,10 @@ bool decode_workspace_carve(void *ws, size_t bytes, int num_seqs, int num_q_head
   return true;
 }
 
-int decode_max_seqs_for_smem() { return 0; }
-
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          int dtype, int group, int max_workers, cudaStream_t stream) {
+                          int dtype, int group, int max_workers, int max_pages_per_item, cudaStream_t stream) {
 #define PA_DECODE_CASE(T, G)                                                     \
-  if (group == G) return launch_typed<T, G>(p, kmap, vmap, max_workers, stream);
+  if (group == G) return launch_typed<T, G>(p, kmap, vmap, max_workers, max_pages_per_item, stream);
   if (dtype == PA_BF16) {
     PA_DECODE_CASE(__nv_bfloat16, 1)
     PA_DECODE_CASE(__nv_bfloat16, 2)

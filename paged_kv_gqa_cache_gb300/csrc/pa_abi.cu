@@ -227,7 +227,7 @@ pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, const int3
   int64_t workers = (pages_hint + 3) / 4;
   if (workers > kDecodeMaxWorkers) workers = kDecodeMaxWorkers;
   cudaError_t e = launch_decode(p, kmap, vmap, pool->dtype, group, (int)workers,
-                                static_cast<cudaStream_t>(stream));
+                                (max_context_len + kBlock - 1) / kBlock, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

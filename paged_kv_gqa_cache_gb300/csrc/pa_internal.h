@@ -60,9 +60,11 @@ struct DecodeLaunch {
   int smem_bytes;    // dynamic shared memory per CTA
 };
 
-// Plans and launches the split and combine kernels.  `group` = Hq / Hkv.
+// Plans and launches the decode: one CTA per (sequence, KV head) item when the
+// items are few, else the split and combine kernels.  `group` = Hq / Hkv;
+// max_pages_per_item bounds each item's pages (from the host-side max length).
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          int dtype, int group, int max_workers, cudaStream_t stream);
+                          int dtype, int group, int max_workers, int max_pages_per_item, cudaStream_t stream);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads);
 // Carves the workspace into meta / ml / o; returns false if it is too small.
 bool decode_workspace_carve(void *ws, size_t bytes, int num_seqs, int num_q_heads, int num_kv_heads,
@@ -106,6 +108,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Same, with thread-block clusters of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, int cluster_x,
+                               cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

@@ -222,3 +222,39 @@ def test_decode_empty_batch_is_a_no_op():
                                case.context_lens[:0], case.scale, max_context_len=16)
     torch.cuda.synchronize()
     assert out.shape[0] == 0
+
+
+def test_decode_workspace_reused_across_batch_sizes():
+    # one workspace sized for the largest call serves smaller and larger batches in turn
+    big = workloads.config4(device=DEV)
+    kc, vc = big.k_cache[0].clone(), big.v_cache[0].clone()
+    pa.kv_cache_write(big.k_new[0], big.v_new[0], big.slot_mapping, kc, vc)
+    ref = oracle.paged_attn_decode(bits(big.q[0]), bits(kc), bits(vc), big.block_tables.cpu().numpy(),
+                                   big.context_lens.cpu().numpy(), big.scale, oracle.BF16)
+    ws = pa.alloc_decode_workspace(64, 32, 8, 4096, DEV)
+    for n in (64, 5, 64, 17):
+        out = pa.paged_attn_decode(big.q[0][:n].contiguous(), kc, vc,
+                                   big.block_tables[:n].contiguous(), big.context_lens[:n].contiguous(),
+                                   big.scale, workspace=ws, max_context_len=4096)
+        torch.cuda.synchronize()
+        check_close(out, ref[:n], f"{n} sequences on a reused workspace")
+
+
+@pytest.mark.parametrize("dtype,hq,hkv", [("bf16", 16, 8), ("f16", 32, 8), ("bf16", 8, 8), ("bf16", 64, 8)])
+def test_decode_one_cta_per_item_and_split_paths_agree(dtype, hq, hkv):
+    # two sequences, 2 x Hkv items: the exact length bound selects one CTA per
+    # item; a loose bound (16K tokens, too many pages for one SM) selects the
+    # split kernels.  Both must match the oracle on the same inputs.
+    lens = [700, 1024]
+    case = workloads.build_case(f"paths-{dtype}-{hq}x{hkv}", dtype, hq, hkv, seed=31 + hq, device=DEV,
+                                decode_lens=lens)
+    kc, vc = case.k_cache[0].clone(), case.v_cache[0].clone()
+    pa.kv_cache_write(case.k_new[0], case.v_new[0], case.slot_mapping, kc, vc)
+    ref = oracle.paged_attn_decode(bits(case.q[0]), bits(kc), bits(vc), case.block_tables.cpu().numpy(),
+                                   case.context_lens.cpu().numpy(), case.scale, ORACLE_DTYPE[case.dtype])
+    wide = torch.full((2, 1024), -1, dtype=torch.int32, device=DEV)      # room for a 16K-token bound
+    wide[:, :case.block_tables.shape[1]] = case.block_tables
+    for bound in (max(lens), 16384):
+        out = pa.paged_attn_decode(case.q[0], kc, vc, wide, case.context_lens, case.scale, max_context_len=bound)
+        torch.cuda.synchronize()
+        check_close(out, ref, f"{case.name}, length bound {bound}")
