@@ -604,6 +604,9 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     if (i + kStages < n) issue(i + kStages, st);
   }
 
+  // the next kernel may start its set-up while the item is merged (it still
+  // waits for this grid to complete before reading anything)
+  griddep_launch_dependents();
   // ---- merge the warps' states in shared memory (the stage buffers are idle now) ----
   __syncthreads();
   float *mine = reinterpret_cast<float *>(stages);
@@ -667,7 +670,6 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     *reinterpret_cast<uint2 *>(op) = pk;
   }
   if (ncta > 1) cluster_sync();  // CTA 0 has read the peer's shared memory: both may exit
-  griddep_launch_dependents();
 }
 
 int item_smem_bytes(int group) {

@@ -14,6 +14,9 @@ namespace {
 
 __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
   griddep_wait();
+  // the next kernel may start its set-up now; it still waits for this grid to
+  // complete before it reads anything (griddep_wait)
+  griddep_launch_dependents();
   const int64_t total = (int64_t)p.num_tokens * p.row_vecs;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
@@ -29,7 +32,6 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
     st_v4(static_cast<uint4 *>(p.k_cache) + slot * p.row_vecs + vi, kv);
     st_v4(static_cast<uint4 *>(p.v_cache) + slot * p.row_vecs + vi, vv);
   }
-  griddep_launch_dependents();
 }
 
 }  // namespace
