@@ -13,7 +13,8 @@ Printed JSON line (rank 0):
   e2e        the same metric through the Python binding with the step's
              inputs copied from pinned host memory and its outputs read back
              inside the timed region;
-  roofline   the decode call (split + combine kernels) timed alone per layer,
+  roofline   the decode call timed alone per layer (one kernel when every
+             sequence and KV head gets its own SMs, else split + combine),
              algorithmic bytes per launch over its duration, against the
              measured HBM copy bandwidth;
   cpu_baseline  the fp64 oracle on the host cores, on a bounded sample.
@@ -214,7 +215,8 @@ class DecodeStep:
             self.decode_bytes_layer = workloads.decode_kv_bytes(lens, c.hkv)
         self.write_bytes_layer = 2 * c.k_new[0].numel() * 2 * 2     # K and V rows, read + write
         self.step_bytes = self.L * (self.decode_bytes_layer + self.write_bytes_layer)
-        self.kernels_per_step = self.L * 3                          # write, split, combine
+        self.decode_kernels = pa.decode_kernel_launches(self.S, c.hkv, c.max_context_len)
+        self.kernels_per_step = self.L * (1 + self.decode_kernels)  # write, then the decode's kernels
 
     def write(self, l):
         c, i = self.case, l % self.case.n_layers
@@ -252,6 +254,8 @@ class MixedStep:
         self.flops_layer = workloads.prefill_flops(c.meta["chunks"], c.hq)
         self.decode_bytes_layer = workloads.decode_kv_bytes(c.meta["decode_lens"], c.hkv)
         self.tokens = c.slot_mapping.numel()
+        lens = c.meta["decode_lens"]
+        self.kernels_per_layer = 2 + pa.decode_kernel_launches(len(lens), c.hkv, c.max_context_len)
 
     def prefill(self, l):
         c, i = self.case, l % 2
@@ -434,9 +438,11 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "peak_kind": peak_kind,
-                     "kernel": "paged_attn_decode (split + combine) per layer",
+                     "kernel": "paged_attn_decode per layer (" + ("one cluster per sequence and KV head"
+                                                                  if step.decode_kernels == 1
+                                                                  else "split + combine") + ")",
                      "bytes_per_launch": step.decode_bytes_layer, "launch_ms": round(dec_launch_ms, 5),
-                     "traffic": committed_traffic("decode.cu", f"decode_split_workload{args.workload}.md")},
+                     "traffic": committed_traffic("decode.cu", f"decode_workload{args.workload}.md")},
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -473,7 +479,7 @@ def run_mixed(args, dev, pa):
                                "(1536,512) + 512 decode seqs ctx U[16,1024], bf16; 2 distinct pools cycled",
                    "global_batch": 515 * world, "parallelism": f"replicas x{world}",
                    "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
-        "gpu_launches": 28 * 4 * args.steps,
+        "gpu_launches": step.L * step.kernels_per_layer * args.steps,
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(tflops / bf16, 3), "peak_kind": peak_kind,
                      "kernel": "paged_attn_prefill_chunk per layer", "flops_per_launch": step.flops_layer,

@@ -132,6 +132,19 @@ PA_API pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, con
                                pa_stream_t stream);
 
 /*
+ * Number of kernels one pa_paged_attn_decode (or _noalloc) call with these
+ * arguments launches on the current device: 1 when every (sequence, KV head)
+ * pair gets its own SMs and a pair of max_context_len tokens, streamed by
+ * them, would still end before a split launch over the whole GPU (the pair
+ * merges its warps' partial results on chip); 2 (split-K pass, then the
+ * combine pass) otherwise.  With 8 KV heads on 152 SMs: up to 9 sequences of
+ * up to 3072 tokens, or up to 19 of up to 1488 tokens, take one launch.  The
+ * choice depends only on these arguments and the device's SM count.
+ * Returns 0 for arguments the call would reject or with no work (num_seqs 0).
+ */
+PA_API int32_t pa_decode_kernel_launches(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len);
+
+/*
  * paged_attn_decode_noalloc — no counterpart on the pages: a library addition
  * for callers that cannot allocate device memory or pass a workspace (a
  * plugin inside a host application that owns all device memory, a serving

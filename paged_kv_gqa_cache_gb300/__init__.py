@@ -33,7 +33,8 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_DTYPE",
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_decode",
            "pa_paged_attn_prefill_chunk", "pa_get_device_error", "pa_status_string",
-           "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc")
+           "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc",
+           "pa_decode_kernel_launches")
 
 
 class PagedAttnError(RuntimeError):
@@ -70,6 +71,8 @@ def load_library(path: str = LIB_PATH):
         lib.pa_kv_cache_write.restype = i32
         lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
         lib.pa_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.pa_decode_kernel_launches.argtypes = [i32, i32, i32]
+        lib.pa_decode_kernel_launches.restype = i32
         lib.pa_paged_attn_decode.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P,
                                              ctypes.c_size_t, P]
         lib.pa_paged_attn_decode.restype = i32
@@ -151,6 +154,12 @@ def kv_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int) -> int:
     return int(load_library().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, max_context_len))
+
+
+def decode_kernel_launches(num_seqs: int, num_kv_heads: int, max_context_len: int) -> int:
+    """Kernels one decode call with these sizes launches on the current device
+    (1: one cluster per sequence and KV head; 2: split-K then combine)."""
+    return int(load_library().pa_decode_kernel_launches(num_seqs, num_kv_heads, max_context_len))
 
 
 def alloc_decode_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int,

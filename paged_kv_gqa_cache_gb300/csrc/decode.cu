@@ -680,30 +680,34 @@ int split_smem_bytes(int group, int num_seqs) {
   return 1024 + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * group * 8 + (num_seqs + 1) * 4;
 }
 
+}  // namespace
+
 // A cluster per item pays off when every item gets its own SMs (two when they
-// fit) and the longest possible item, streamed by them (and the whole call
-// through HBM), still ends before the split path: the whole call spread over
-// all SMs, plus its fixed cost of a second launch and a merge through global
-// memory.  The per-SM and whole-GPU rates are conservative round numbers for
-// this part.  Returns the CTAs per item (1 or 2), or 0 for the split path.
-int item_ctas(int items, int max_pages_per_item) {
+// fit) and the longest item the length bound allows, streamed by them, still
+// ends before the split path would end in its best case, that item alone
+// spread over all SMs (the batch may be that skewed: only the bound is known
+// on the host).  The split path pays a second launch and a merge through
+// global memory.  Rates are round measured figures for this part: ~150 GB/s
+// per SM for TMA page streams, ~6 TB/s of HBM for the whole GPU.  Returns the
+// CTAs per item (1 or 2), or 0 for the split path.
+int decode_item_ctas(int items, int max_pages_per_item) {
   const int sms = sm_count();
   if (items > sms) return 0;
   const int ctas = 2 * items <= sms ? 2 : 1;
-  const double page_bytes = 2.0 * kBlock * kHeadDim * 2;
-  const double total_us = (double)items * max_pages_per_item * page_bytes / 6e6;         // ~6 TB/s of HBM
-  const double one_item_us = max_pages_per_item * page_bytes / (ctas * 250e3);          // ~250 GB/s per SM
-  const double item_us = 3.0 + (one_item_us > total_us ? one_item_us : total_us);
-  const double split_us = 8.0 + total_us;
+  const double item_bytes = (double)max_pages_per_item * 2.0 * kBlock * kHeadDim * 2;
+  const double item_us = 3.0 + item_bytes / (ctas * 150e3);
+  const double split_us = 8.0 + item_bytes / 6e6;
   return item_us < split_us ? ctas : 0;
 }
+
+namespace {
 
 template <typename T, int G>
 cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          int max_workers, int max_pages_per_item, cudaStream_t stream) {
   DecodeParams p = p0;
   const int items = p.num_seqs * p.num_kv_heads;
-  const int ctas = item_ctas(items, max_pages_per_item);
+  const int ctas = decode_item_ctas(items, max_pages_per_item);
   if (ctas > 0) {
     const int ismem = item_smem_bytes(G);
     static bool item_configured = false;

@@ -178,6 +178,12 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
   return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads);
 }
 
+int32_t pa_decode_kernel_launches(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len) {
+  if (num_seqs < 1 || num_seqs > 16384 || num_kv_heads < 1 || max_context_len < 1) return 0;
+  if (sm_count() < 1) return 0;
+  return decode_item_ctas(num_seqs * num_kv_heads, (max_context_len + kBlock - 1) / kBlock) > 0 ? 1 : 2;
+}
+
 pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
                                int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                                int32_t num_q_heads, int32_t max_context_len, float scale, void *out,

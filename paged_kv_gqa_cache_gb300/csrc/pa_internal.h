@@ -66,6 +66,8 @@ struct DecodeLaunch {
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
                           int dtype, int group, int max_workers, int max_pages_per_item, cudaStream_t stream);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads);
+// CTAs per item of the one-launch decode (1 or 2), or 0 when the split path runs.
+int decode_item_ctas(int items, int max_pages_per_item);
 // Carves the workspace into meta / ml / o; returns false if it is too small.
 bool decode_workspace_carve(void *ws, size_t bytes, int num_seqs, int num_q_heads, int num_kv_heads,
                             DecodeParams &p);

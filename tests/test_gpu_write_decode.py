@@ -254,6 +254,8 @@ def test_decode_one_cta_per_item_and_split_paths_agree(dtype, hq, hkv):
                                    case.context_lens.cpu().numpy(), case.scale, ORACLE_DTYPE[case.dtype])
     wide = torch.full((2, 1024), -1, dtype=torch.int32, device=DEV)      # room for a 16K-token bound
     wide[:, :case.block_tables.shape[1]] = case.block_tables
+    assert pa.decode_kernel_launches(2, hkv, max(lens)) == 1
+    assert pa.decode_kernel_launches(2, hkv, 16384) == 2
     for bound in (max(lens), 16384):
         out = pa.paged_attn_decode(case.q[0], kc, vc, wide, case.context_lens, case.scale, max_context_len=bound)
         torch.cuda.synchronize()
