@@ -26,13 +26,17 @@
 //                 reference maximum m, row sum l and output accumulator O_half,
 //                 so the halves never synchronise inside the key loop.
 //                 P = 2^(S * scale * log2 e - m) goes back into the same TMEM
-//                 columns as two terms of the input dtype, P_hi = round(P) and
-//                 P_lo = round(P - P_hi) (each 32-key chunk of S becomes 16
-//                 columns of P_hi pairs then 16 of P_lo pairs, so no S value is
-//                 overwritten before it is read).
-//   O_half += P V tcgen05.mma with A = P_hi, then P_lo, read from TMEM, and B =
-//                 the V rows of that half (MN-major) from shared memory; both
-//                 O accumulators (fp32) stay in TMEM for the whole key loop.
+//                 columns rounded to the input dtype, P_hi = round(P) (each
+//                 32-key chunk of S becomes 16 columns of P_hi pairs, so no S
+//                 value is overwritten before it is read).  Rows that see
+//                 fewer than 128 keys (all of them in key tile 0) average the
+//                 rounding errors of too few probabilities, so on key tile 0
+//                 of a query tile that holds such rows P also gets its second
+//                 term P_lo = round(P - P_hi), in the next 16 columns.
+//   O_half += P V tcgen05.mma with A = P_hi (then P_lo where it exists), read
+//                 from TMEM, and B = the V rows of that half (MN-major) from
+//                 shared memory; both O accumulators (fp32) stay in TMEM for
+//                 the whole key loop.
 // m only moves (rescaling that half's O and l) when a tile's maximum exceeds
 // it by more than 2^8, so the threads rarely touch O.  The epilogue merges the
 // two halves of each row, O = O_0 2^(m_0 - M) + O_1 2^(m_1 - M) over
@@ -141,6 +145,45 @@ __device__ __forceinline__ void store_rows_coalesced(uint4 *stage, void *dst, bo
   }
 }
 
+// P = 2^(S * scale_log2 - m) for this thread's 64 keys of one tile (two
+// 32-column chunks v[0], v[1]), masked past `lim` unless `full`, written over
+// the chunk's first 16 columns as pairs of the input dtype; with LO, the
+// rounding remainder goes into the next 16.  Returns the row sum of P.
+template <typename T, bool LO>
+__device__ __forceinline__ float exp_pack_store(const uint32_t (&v)[2][32], uint32_t s_addr, float sl2, float m_ref,
+                                                bool full, int kbase, int lim) {
+  const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_ref, -m_ref);
+  const float2 neg1 = make_float2(-1.f, -1.f);
+  float2 ls = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    uint32_t pk[LO ? 32 : 16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float2 e = __ffma2_rn(make_float2(__uint_as_float(v[cc][2 * j]), __uint_as_float(v[cc][2 * j + 1])),
+                                  sl2v, negm);
+      float2 pr = make_float2(ex2(e.x), ex2(e.y));
+      if (!full) {
+        const int key = kbase + cc * 32 + 2 * j;
+        pr.x = (key <= lim) ? pr.x : 0.f;
+        pr.y = (key + 1 <= lim) ? pr.y : 0.f;
+      }
+      ls = __fadd2_rn(ls, pr);
+      pk[j] = Pack<T>::from_f2(pr.x, pr.y);
+      if constexpr (LO) {
+        const float2 lo = __ffma2_rn(Pack<T>::to_f2(pk[j]), neg1, pr);  // P - P_hi, exact
+        pk[16 + j] = Pack<T>::from_f2(lo.x, lo.y);
+      }
+    }
+    if constexpr (LO) {
+      tc::st_32x32b_x32(s_addr + cc * 32, pk);
+    } else {
+      tc::st_32x32b_x16(s_addr + cc * 32, pk);
+    }
+  }
+  return ls.x + ls.y;
+}
+
 template <typename T, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -181,6 +224,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const int kt_ctx = (ctx - 1) / 128;                       // key tile holding the sequence's last key
   const int npages = (ctx + kBlock - 1) / kBlock;
   const int32_t *bt = p.block_tables + (int64_t)c * p.max_blocks_per_seq;
+  const bool lo_tile0 = start + t0 < 127;  // the tile's first row sees fewer than 128 keys
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&kmap);
@@ -297,7 +341,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
               const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
               tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, k4 > 0 ? 1u : first);
-              tc::mma_f16_ts(o_col, a_hi + 16, bdesc, IDESC_O, 1u);
+              if (j == 0 && lo_tile0) tc::mma_f16_ts(o_col, a_hi + 16, bdesc, IDESC_O, 1u);
             }
           }
           if (timed_out) break;
@@ -373,32 +417,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
       if (first) m_ref = mc;
 
-      // P in two terms of the input dtype, written over this half's S columns
-      const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_ref, -m_ref);
-      const float2 neg1 = make_float2(-1.f, -1.f);
-      float2 ls = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float2 e = __ffma2_rn(make_float2(__uint_as_float(v[cc][2 * j]), __uint_as_float(v[cc][2 * j + 1])),
-                                      sl2v, negm);
-          float2 pr = make_float2(ex2(e.x), ex2(e.y));
-          if (!full) {
-            const int key = kbase + cc * 32 + 2 * j;
-            pr.x = (key <= lim) ? pr.x : 0.f;
-            pr.y = (key + 1 <= lim) ? pr.y : 0.f;
-          }
-          ls = __fadd2_rn(ls, pr);
-          pk[j] = Pack<T>::from_f2(pr.x, pr.y);
-          const float2 lo = __ffma2_rn(Pack<T>::to_f2(pk[j]), neg1, pr);  // P - P_hi, exact
-          pk[16 + j] = Pack<T>::from_f2(lo.x, lo.y);
-        }
-        tc::st_32x32b_x32(s_addr + cc * 32, pk);
-      }
+      // P in the input dtype (two terms where the tile needs them), over this half's S columns
+      l += (kt == 0 && lo_tile0) ? exp_pack_store<T, true>(v, s_addr, sl2, m_ref, full, kbase, lim)
+                                 : exp_pack_store<T, false>(v, s_addr, sl2, m_ref, full, kbase, lim);
       tc::wait_st();
-      l += ls.x + ls.y;
 
       if (kt == kt_ctx) {
         // value rows of keys >= ctx in this half (partial last page, pages past

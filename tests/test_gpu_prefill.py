@@ -144,3 +144,16 @@ def test_prefill_many_small_chunks():
 def test_prefill_single_short_chunk():
     case = workloads.build_case("tiny", "bf16", 8, 8, seed=18, device=DEV, chunks=[(0, 3)])
     prefill_and_check(case, "one 3-token chunk")
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (64, 8)])
+@pytest.mark.parametrize("seed", [41, 42, 43])
+def test_prefill_rows_just_past_the_second_term_threshold(hq, hkv, seed):
+    # Query tiles whose first row sees 128 keys or more take P in one term of
+    # the input dtype (bf16 here, the coarser one); the rounding errors of P
+    # then average over at least 128 probabilities.  Rows with 128 .. ~700
+    # visible keys, and tiles straddling the threshold, must stay inside the
+    # tolerance as well as the rows that get the second term.
+    case = workloads.build_case(f"threshold-{hq}x{hkv}-{seed}", "bf16", hq, hkv, seed=seed, device=DEV,
+                                chunks=[(0, 400), (100, 200), (126, 64), (127, 1), (128, 40)])
+    prefill_and_check(case)
