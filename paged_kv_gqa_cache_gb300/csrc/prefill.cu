@@ -15,9 +15,11 @@
 // t0 + r / G, head h * G + r % G (the Q tile is one TMA box per 64-dim half).
 // Keys stream in tiles of N = 128 (8 pages, two 2 KB TMA boxes per page: the
 // 64-dim halves of 16 keys, 128-byte swizzled): K through a 3-stage ring
-// released as soon as S is computed, V through a 2-stage ring released after
-// the PV product, each filled by its own loader warp whose lanes issue the
-// boxes of a tile in parallel.  Per key tile kt:
+// released as soon as S is computed, V through a 3-stage ring released after
+// the PV product.  Three loader warps fill both rings, each issuing a third
+// of every tile's boxes from parallel lanes: the TMA engine serves each
+// issuing warp at a fixed cost per box, so the warps, not the ring depth, set
+// the ingest rate.  Per key tile kt:
 //   S = Q K^T     tcgen05.mma kind::f16, A and B from shared memory (K-major),
 //                 fp32 into TMEM columns S[kt % 2].
 //   softmax       8 warps; the two warps on TMEM lane quarter q own rows
@@ -41,7 +43,7 @@
 // it by more than 2^8, so the threads rarely touch O.  The epilogue merges the
 // two halves of each row, O = O_0 2^(m_0 - M) + O_1 2^(m_1 - M) over
 // l_0 2^(m_0 - M) + l_1 2^(m_1 - M), and stores it in the input dtype.
-// Warps 8 and 9 load K (and the Q tile) and V, warp 10 owns TMEM and issues the
+// Warps 8..10 load Q, K and V, warp 11 owns TMEM and issues the
 // MMAs (one thread); mbarriers hand tiles between the roles and every wait is
 // bounded.  Keys above the diagonal are masked per element on the tiles that
 // cross it (a warp-uniform test picks the unmasked path elsewhere) and never
@@ -57,19 +59,23 @@ namespace {
 
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kWarpLoadK = kSoftmaxWarps, kWarpLoadV = kSoftmaxWarps + 1, kWarpMma = kSoftmaxWarps + 2;
-constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
+constexpr int kLoadWarps = 3;  // each issues a third of the boxes of every K and V tile
+constexpr int kWarpLoad0 = kSoftmaxWarps, kWarpMma = kSoftmaxWarps + kLoadWarps;
+constexpr int kThreads = (kSoftmaxWarps + kLoadWarps + 1) * 32;
 constexpr int kHalf = 16384;                        // 128 rows x 64 elements x 2 bytes
-constexpr int kKStages = 3, kVStages = 2;
+constexpr int kKStages = 3, kVStages = 3;
 constexpr int OFF_Q = 0;                            // Q: two 64-dim halves
 constexpr int OFF_K = 2 * kHalf;                    // K stages: {lo, hi} halves
 constexpr int OFF_V = OFF_K + kKStages * 2 * kHalf; // V stages: {lo, hi} halves
-constexpr int OFF_X = OFF_V + kVStages * 2 * kHalf; // epilogue (m, l) exchange [2][128] float2
-constexpr int kBtCache = 2048;                      // block ids of the chunk cached in shared memory
-constexpr int OFF_BT = OFF_X + 2 * 128 * 8;
-constexpr int OFF_STAGE = OFF_BT + kBtCache * 4;     // epilogue: 1 KB of staging per softmax warp
+constexpr int kBtCache = 256;                       // block ids of the chunk cached in shared memory
+constexpr int OFF_BT = OFF_V + kVStages * 2 * kHalf;
+constexpr int OFF_BAR = OFF_BT + kBtCache * 4;
+// The epilogue runs once every QK^T product has completed, so it borrows the
+// K ring: the (m, l) exchange [2][128] float2, then 1 KB of staging per softmax warp.
+constexpr int OFF_X = OFF_K;
+constexpr int OFF_STAGE = OFF_X + 2 * 128 * 8;
 constexpr int kStageBytes = 1024;
-constexpr int OFF_BAR = OFF_STAGE + kSoftmaxWarps * kStageBytes;
+static_assert(OFF_STAGE + kSoftmaxWarps * kStageBytes <= OFF_V, "epilogue areas fit in the K ring");
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;    // + barriers (< 256 B) + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;                 // S/P 0, S/P 1, O_0, O_1
@@ -83,23 +89,28 @@ struct Bars {
   uint64_t k_full[kKStages];
   uint64_t k_free[kKStages];
   uint64_t v_full[kVStages];
+  uint64_t v_free[kVStages];
   uint64_t s_full[2];
   uint64_t p_full[2][2];  // [key half][tile parity]
-  uint64_t pv_done[2];    // also frees the V stage of that tile
+  uint64_t pv_done[2];    // [tile parity]: O holds every P V up to that tile
   uint64_t x_full;
   uint32_t tmem_base;
 };
 
-// Fetch the 8 pages of key tile kt of one pool into `dst` (two 64-dim half
-// boxes per page), completing on `bar`; called by a whole loader warp: lane
-// j < 16 loads half j % 2 of page j / 2.  Pages past the sequence are skipped;
-// a page whose block id is out of range is zeroed and reported.
-__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int kt, int h,
-                                          int npages, const int32_t *sbt, const int32_t *bt,
-                                          const PrefillParams &p, int c, int lane) {
-  const int page = lane >> 1, half = lane & 1;
+// Key tile kt of one pool is 16 boxes of 2 KB, box b being the 64-dim half
+// b % 2 of page b / 2, fetched into `dst` and completing on `bar` (which
+// expects one arrival per loader warp).  A TMA engine serves each issuing warp
+// at about one small box per 50 ns, so the boxes are spread over the loader
+// warps: this warp's lane i issues box b0 + kLoadWarps * i.  Pages past the
+// sequence are skipped; a page whose block id is out of range is zeroed and
+// reported.
+__device__ __forceinline__ void load_boxes(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int kt, int b0,
+                                           int h, int npages, const int32_t *sbt, const int32_t *bt,
+                                           const PrefillParams &p, int c, int lane) {
+  const int b = b0 + kLoadWarps * lane;
+  const int page = b >> 1, half = b & 1;
   const int pg = kt * 8 + page;
-  const bool in = lane < 16 && pg < npages;
+  const bool in = b < 16 && pg < npages;
   int id = -1;
   if (in) id = pg < kBtCache ? sbt[pg] : __ldg(bt + pg);
   const bool ok = in && (unsigned)id < (unsigned)p.num_blocks;
@@ -232,10 +243,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     tma_prefetch_desc(&qmap);
     mbar_init(&bars.q_full, 1);
     for (int b = 0; b < kKStages; ++b) {
-      mbar_init(&bars.k_full[b], 1);
+      mbar_init(&bars.k_full[b], kLoadWarps);
       mbar_init(&bars.k_free[b], 1);
     }
-    for (int b = 0; b < kVStages; ++b) mbar_init(&bars.v_full[b], 1);
+    for (int b = 0; b < kVStages; ++b) {
+      mbar_init(&bars.v_full[b], kLoadWarps);
+      mbar_init(&bars.v_free[b], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.s_full[b], 1);
       mbar_init(&bars.pv_done[b], 1);
@@ -255,37 +269,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
   bool timed_out = false;
 
-  if (warp == kWarpLoadK || warp == kWarpLoadV) {
-    // ---------------- loader warps: K two tiles ahead, V as its stage frees ----------------
-    const bool is_k = warp == kWarpLoadK;
+  if (warp >= kWarpLoad0 && warp < kWarpMma) {
+    // ---------------- loader warps: each tile's K and V boxes, a third per warp ----------------
+    const int lw = warp - kWarpLoad0;
     int32_t *sbt = reinterpret_cast<int32_t *>(smem + OFF_BT);
     const int cached = min(min(npages, nkt * 8), kBtCache);
-    if (is_k) {
-      for (int i = lane; i < cached; i += 32) sbt[i] = __ldg(bt + i);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf);
-        tma_load_3d(smem + OFF_Q, &qmap, &bars.q_full, 0, h * G, row0 + t0);
-        tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
-      }
+    for (int i = lw * 32 + lane; i < cached; i += kLoadWarps * 32) sbt[i] = __ldg(bt + i);
+    if (lw == 0 && lane == 0) {
+      mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf);
+      tma_load_3d(smem + OFF_Q, &qmap, &bars.q_full, 0, h * G, row0 + t0);
+      tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
     }
-    // the V loader reads the block ids the K loader cached (both are inside the producer pair)
-    asm volatile("bar.sync 1, 64;" ::: "memory");
-    const CUtensorMap *map = is_k ? &kmap : &vmap;
-    const int nst = is_k ? kKStages : kVStages;
-    uint8_t *ring = smem + (is_k ? OFF_K : OFF_V);
-    uint64_t *full = is_k ? bars.k_full : bars.v_full;
+    named_barrier(1, kLoadWarps * 32);  // the cached block ids are complete
+    const int kb0 = lw, vb0 = (lw + kLoadWarps - 1) % kLoadWarps;  // balances the boxes per warp
     for (int t = 0; t < nkt; ++t) {
-      const int st = t % nst;
-      if (t >= nst) {  // the stage's previous tile must be consumed
-        const int j = t - nst;
-        const bool ok = is_k ? mbar_wait(&bars.k_free[st], (j / nst) & 1)
-                             : mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1);
-        if (!ok) {
-          timed_out = true;
-          break;
-        }
+      const int ks = t % kKStages, vs = t % kVStages;
+      if (t >= kKStages && !mbar_wait(&bars.k_free[ks], ((t - kKStages) / kKStages) & 1)) {
+        timed_out = true;
+        break;
       }
-      load_tile(ring + st * 2 * kHalf, map, &full[st], t, h, npages, sbt, bt, p, c, lane);
+      load_boxes(smem + OFF_K + ks * 2 * kHalf, &kmap, &bars.k_full[ks], t, kb0, h, npages, sbt, bt, p, c, lane);
+      if (t >= kVStages && !mbar_wait(&bars.v_free[vs], ((t - kVStages) / kVStages) & 1)) {
+        timed_out = true;
+        break;
+      }
+      load_boxes(smem + OFF_V + vs * 2 * kHalf, &vmap, &bars.v_full[vs], t, vb0, h, npages, sbt, bt, p, c, lane);
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
@@ -318,7 +326,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           tc::commit(&bars.s_full[sb]);
           tc::commit(&bars.k_free[b]);
         }
-        if (kt >= 1) {  // O_half += P V of the previous tile, one key half at a time
+        if (kt >= 1) {  // O_half += P V of the previous tile: keys 0..63 into O_0, 64..127 into O_1
           const int j = kt - 1, sj = j & 1;
           if (!mbar_wait(&bars.v_full[j % kVStages], (j / kVStages) & 1)) {
             timed_out = true;
@@ -327,25 +335,33 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           const uint64_t vdesc = vdesc0 + (uint64_t)(j % kVStages) * kStageStep;
           const uint32_t p_col = tmem + sj * 128;
           const uint32_t first = j > 0 ? 1u : 0u;
+          // both halves of P first: the tensor core keeps its full rate only
+          // when the MMAs arrive back to back, with no branch or wait between them
+          if (!mbar_wait(&bars.p_full[0][sj], (j >> 1) & 1) || !mbar_wait(&bars.p_full[1][sj], (j >> 1) & 1)) {
+            timed_out = true;
+            break;
+          }
+          tc::fence_after_sync();
+          if (j == 0 && lo_tile0) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            if (!mbar_wait(&bars.p_full[half][sj], (j >> 1) & 1)) {
-              timed_out = true;
-              break;
-            }
-            tc::fence_after_sync();
-            const uint32_t o_col = tmem + kColO + half * 128;
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-              const int kk = half * 4 + k4;  // 16-key step within the tile: V rows 16 kk .. 16 kk + 15
+            for (int kk = 0; kk < 8; ++kk) {  // 16-key step: V rows 16 kk .. 16 kk + 15, into O of key half kk / 4
+              const uint32_t o_col = tmem + kColO + (kk >> 2) * 128;
               const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
               const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
-              tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, k4 > 0 ? 1u : first);
-              if (j == 0 && lo_tile0) tc::mma_f16_ts(o_col, a_hi + 16, bdesc, IDESC_O, 1u);
+              tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
+              tc::mma_f16_ts(o_col, a_hi + 16, bdesc, IDESC_O, 1u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t o_col = tmem + kColO + (kk >> 2) * 128;
+              const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
+              const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
+              tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
             }
           }
-          if (timed_out) break;
           tc::commit(&bars.pv_done[sj]);
+          tc::commit(&bars.v_free[j % kVStages]);
         }
       }
     }
