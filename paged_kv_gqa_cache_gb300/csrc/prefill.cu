@@ -82,17 +82,18 @@ constexpr uint32_t kTmemCols = 512;                 // S/P 0, S/P 1, O_0, O_1
 constexpr uint32_t kColO = 256;
 constexpr float kRescale = 8.f;                     // log2 of the largest P before O is rescaled
 
-// Barriers that signal once per key tile come in pairs indexed by the tile's
-// parity (or one per ring stage), so no waiter can be overtaken by two phases.
+// Every per-tile barrier exists once per ring stage (tile kt uses stage
+// kt % 3) and completes once per tile of that stage.  No waiter can be
+// overtaken by two phases: the next tile of a stage needs, through the rings
+// or the MMA order, the very step each waiter of the stage is waiting for.
+static_assert(kKStages == kVStages, "QK^T and P V barriers share the stage index");
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[kKStages];
-  uint64_t k_free[kKStages];
-  uint64_t v_full[kVStages];
-  uint64_t v_free[kVStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2][2];  // [key half][tile parity]
-  uint64_t pv_done[2];    // [tile parity]: O holds every P V up to that tile
+  uint64_t k_full[kKStages];   // K tile landed (one arrival per loader warp + TMA bytes)
+  uint64_t v_full[kVStages];   // V tile landed
+  uint64_t s_full[kKStages];   // QK^T of the tile done: S readable, K stage free
+  uint64_t p_full[kVStages];   // P of the tile written by every softmax thread, each of which saw V land
+  uint64_t pv_done[kVStages];  // P V of the tile done: O holds it, V stage free
   uint64_t x_full;
   uint32_t tmem_base;
 };
@@ -244,17 +245,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     mbar_init(&bars.q_full, 1);
     for (int b = 0; b < kKStages; ++b) {
       mbar_init(&bars.k_full[b], kLoadWarps);
-      mbar_init(&bars.k_free[b], 1);
-    }
-    for (int b = 0; b < kVStages; ++b) {
       mbar_init(&bars.v_full[b], kLoadWarps);
-      mbar_init(&bars.v_free[b], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.s_full[b], 1);
+      mbar_init(&bars.p_full[b], kSoftmaxThreads);
       mbar_init(&bars.pv_done[b], 1);
-      mbar_init(&bars.p_full[0][b], kSoftmaxThreads / 2);
-      mbar_init(&bars.p_full[1][b], kSoftmaxThreads / 2);
     }
     mbar_init(&bars.x_full, kSoftmaxThreads);
     fence_mbar_init();
@@ -284,12 +278,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     const int kb0 = lw, vb0 = (lw + kLoadWarps - 1) % kLoadWarps;  // balances the boxes per warp
     for (int t = 0; t < nkt; ++t) {
       const int ks = t % kKStages, vs = t % kVStages;
-      if (t >= kKStages && !mbar_wait(&bars.k_free[ks], ((t - kKStages) / kKStages) & 1)) {
+      if (t >= kKStages && !mbar_wait(&bars.s_full[ks], ((t - kKStages) / kKStages) & 1)) {
         timed_out = true;
         break;
       }
       load_boxes(smem + OFF_K + ks * 2 * kHalf, &kmap, &bars.k_full[ks], t, kb0, h, npages, sbt, bt, p, c, lane);
-      if (t >= kVStages && !mbar_wait(&bars.v_free[vs], ((t - kVStages) / kVStages) & 1)) {
+      if (t >= kVStages && !mbar_wait(&bars.pv_done[vs], ((t - kVStages) / kVStages) & 1)) {
         timed_out = true;
         break;
       }
@@ -300,6 +294,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // Descriptors are built once; a k-step or a ring stage only moves the start
     // address field (bits 0..13, address >> 4), so each MMA costs a 64-bit add.
     // Shared-memory offsets stay below 256 KB, so the field never carries over.
+    // The tensor core queues only a few MMAs, so any latency in this thread
+    // between two batches leaves it idle: the barriers of the next batch are
+    // probed without blocking two MMAs before the end of the current one, when
+    // the answer is back by the time it is needed.  Only a barrier that really
+    // is not complete yet costs a (bounded) blocking wait.
     if (lane == 0) {
       if (!mbar_wait(&bars.q_full, 0)) timed_out = true;
       const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
@@ -307,10 +306,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       const uint64_t vdesc0 = tc::desc_sw128(smem_u32(smem + OFF_V), kHalf, 1024);
       constexpr uint64_t kStageStep = (2 * kHalf) >> 4;   // one ring stage
       constexpr uint64_t kHalfStep = kHalf >> 4;          // the other 64-dim half
+      bool k_ok = mbar_test_wait(&bars.k_full[0], 0);      // K tile of the next QK^T batch has landed
+      bool pv_ok = false;                                  // P (and so V) of the next P V batch is ready
       for (int kt = 0; kt <= nkt && !timed_out; ++kt) {
+        const int j = kt - 1, sj = j & 1;                  // the tile whose P V is issued in this iteration
+        const int jv = j % kVStages;
         if (kt < nkt) {
           const int b = kt % kKStages, sb = kt & 1;
-          if (!mbar_wait(&bars.k_full[b], (kt / kKStages) & 1)) {
+          if (!k_ok && !mbar_wait(&bars.k_full[b], (kt / kKStages) & 1)) {
             timed_out = true;
             break;
           }
@@ -319,29 +322,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           const uint32_t s_col = tmem + sb * 128;
           tc::mma_f16(s_col, qdesc, kdesc, IDESC_S, 0u);
 #pragma unroll
-          for (int kk = 1; kk < 8; ++kk) {
+          for (int kk = 1; kk < 6; ++kk) {
             const uint64_t off = (uint64_t)((kk >> 2) * kHalfStep + (kk & 3) * 2);   // 16-element k-step
             tc::mma_f16(s_col, qdesc + off, kdesc + off, IDESC_S, 1u);
           }
-          tc::commit(&bars.s_full[sb]);
-          tc::commit(&bars.k_free[b]);
+          if (kt >= 1) {
+            pv_ok = mbar_test_wait(&bars.p_full[jv], (j / kVStages) & 1);
+          } else {
+            k_ok = mbar_test_wait(&bars.k_full[1 % kKStages], (1 / kKStages) & 1) & (nkt > 1);
+          }
+#pragma unroll
+          for (int kk = 6; kk < 8; ++kk) {
+            const uint64_t off = (uint64_t)((kk >> 2) * kHalfStep + (kk & 3) * 2);
+            tc::mma_f16(s_col, qdesc + off, kdesc + off, IDESC_S, 1u);
+          }
+          tc::commit(&bars.s_full[b]);
+        } else {
+          pv_ok = false;
         }
         if (kt >= 1) {  // O_half += P V of the previous tile: keys 0..63 into O_0, 64..127 into O_1
-          const int j = kt - 1, sj = j & 1;
-          if (!mbar_wait(&bars.v_full[j % kVStages], (j / kVStages) & 1)) {
-            timed_out = true;
-            break;
-          }
-          const uint64_t vdesc = vdesc0 + (uint64_t)(j % kVStages) * kStageStep;
-          const uint32_t p_col = tmem + sj * 128;
-          const uint32_t first = j > 0 ? 1u : 0u;
-          // both halves of P first: the tensor core keeps its full rate only
-          // when the MMAs arrive back to back, with no branch or wait between them
-          if (!mbar_wait(&bars.p_full[0][sj], (j >> 1) & 1) || !mbar_wait(&bars.p_full[1][sj], (j >> 1) & 1)) {
+          if (!pv_ok && !mbar_wait(&bars.p_full[jv], (j / kVStages) & 1)) {
             timed_out = true;
             break;
           }
           tc::fence_after_sync();
+          const uint64_t vdesc = vdesc0 + (uint64_t)jv * kStageStep;
+          const uint32_t p_col = tmem + sj * 128;
+          const uint32_t first = j > 0 ? 1u : 0u;
+          const int kn = kt + 1;                           // the next QK^T batch
           if (j == 0 && lo_tile0) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {  // 16-key step: V rows 16 kk .. 16 kk + 15, into O of key half kk / 4
@@ -349,6 +357,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
               const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
               tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
+              if (kk == 7) k_ok = mbar_test_wait(&bars.k_full[kn % kKStages], (kn / kKStages) & 1) & (kn < nkt);
               tc::mma_f16_ts(o_col, a_hi + 16, bdesc, IDESC_O, 1u);
             }
           } else {
@@ -357,11 +366,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               const uint32_t o_col = tmem + kColO + (kk >> 2) * 128;
               const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
               const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
+              if (kk == 6) k_ok = mbar_test_wait(&bars.k_full[kn % kKStages], (kn / kKStages) & 1) & (kn < nkt);
               tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
             }
           }
-          tc::commit(&bars.pv_done[sj]);
-          tc::commit(&bars.v_free[j % kVStages]);
+          tc::commit(&bars.pv_done[jv]);
         }
       }
     }
@@ -379,7 +388,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 
     for (int kt = 0; kt < nkt; ++kt) {
       const int sb = kt & 1;
-      if (!mbar_wait(&bars.s_full[sb], (kt >> 1) & 1)) {
+      if (!mbar_wait(&bars.s_full[kt % kKStages], (kt / kKStages) & 1)) {
         timed_out = true;
         break;
       }
@@ -416,7 +425,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           m_ref = mc;
         }
         const int j = kt - 1;       // (kt >= 1 here) every earlier P V has landed in O
-        if (!mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
+        if (!mbar_wait(&bars.pv_done[j % kVStages], (j / kVStages) & 1)) {
           timed_out = true;
           break;
         }
@@ -456,12 +465,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         fence_proxy_async_smem();
       }
       tc::fence_before_sync();
-      mbar_arrive(&bars.p_full[ch][sb]);
+      // the P V batch waits on this barrier alone, so it must also imply that V landed
+      if (kt != kt_ctx && !mbar_wait(&bars.v_full[kt % kVStages], (kt / kVStages) & 1)) {
+        timed_out = true;
+        break;
+      }
+      mbar_arrive(&bars.p_full[kt % kVStages]);
     }
 
     if (!timed_out) {
       const int j = nkt - 1;
-      if (mbar_wait(&bars.pv_done[j & 1], (j >> 1) & 1)) {
+      if (mbar_wait(&bars.pv_done[j % kVStages], (j / kVStages) & 1)) {
         tc::fence_after_sync();
         // merge the two halves of the row
         float2 *xm = reinterpret_cast<float2 *>(smem + OFF_X);
