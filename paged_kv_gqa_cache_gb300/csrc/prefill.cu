@@ -295,10 +295,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // address field (bits 0..13, address >> 4), so each MMA costs a 64-bit add.
     // Shared-memory offsets stay below 256 KB, so the field never carries over.
     // The tensor core queues only a few MMAs, so any latency in this thread
-    // between two batches leaves it idle: the barriers of the next batch are
-    // probed without blocking two MMAs before the end of the current one, when
-    // the answer is back by the time it is needed.  Only a barrier that really
-    // is not complete yet costs a (bounded) blocking wait.
+    // between two batches leaves it idle: the P barrier of the next P V batch
+    // is probed without blocking two MMAs before the end of the QK^T batch,
+    // when the answer is back by the time it is needed; only a P that really
+    // is not ready yet costs a (bounded) blocking wait.  (The K barrier is not
+    // probed: a probe of a barrier that TMA is still updating costs more than
+    // the wait it saves.)
     if (lane == 0) {
       if (!mbar_wait(&bars.q_full, 0)) timed_out = true;
       const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
@@ -306,14 +308,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       const uint64_t vdesc0 = tc::desc_sw128(smem_u32(smem + OFF_V), kHalf, 1024);
       constexpr uint64_t kStageStep = (2 * kHalf) >> 4;   // one ring stage
       constexpr uint64_t kHalfStep = kHalf >> 4;          // the other 64-dim half
-      bool k_ok = mbar_test_wait(&bars.k_full[0], 0);      // K tile of the next QK^T batch has landed
       bool pv_ok = false;                                  // P (and so V) of the next P V batch is ready
       for (int kt = 0; kt <= nkt && !timed_out; ++kt) {
         const int j = kt - 1, sj = j & 1;                  // the tile whose P V is issued in this iteration
         const int jv = j % kVStages;
         if (kt < nkt) {
           const int b = kt % kKStages, sb = kt & 1;
-          if (!k_ok && !mbar_wait(&bars.k_full[b], (kt / kKStages) & 1)) {
+          if (!mbar_wait(&bars.k_full[b], (kt / kKStages) & 1)) {
             timed_out = true;
             break;
           }
@@ -326,11 +327,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             const uint64_t off = (uint64_t)((kk >> 2) * kHalfStep + (kk & 3) * 2);   // 16-element k-step
             tc::mma_f16(s_col, qdesc + off, kdesc + off, IDESC_S, 1u);
           }
-          if (kt >= 1) {
-            pv_ok = mbar_test_wait(&bars.p_full[jv], (j / kVStages) & 1);
-          } else {
-            k_ok = mbar_test_wait(&bars.k_full[1 % kKStages], (1 / kKStages) & 1) & (nkt > 1);
-          }
+          if (kt >= 1) pv_ok = mbar_test_wait(&bars.p_full[jv], (j / kVStages) & 1);
 #pragma unroll
           for (int kk = 6; kk < 8; ++kk) {
             const uint64_t off = (uint64_t)((kk >> 2) * kHalfStep + (kk & 3) * 2);
@@ -349,7 +346,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           const uint64_t vdesc = vdesc0 + (uint64_t)jv * kStageStep;
           const uint32_t p_col = tmem + sj * 128;
           const uint32_t first = j > 0 ? 1u : 0u;
-          const int kn = kt + 1;                           // the next QK^T batch
           if (j == 0 && lo_tile0) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {  // 16-key step: V rows 16 kk .. 16 kk + 15, into O of key half kk / 4
@@ -357,7 +353,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
               const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
               tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
-              if (kk == 7) k_ok = mbar_test_wait(&bars.k_full[kn % kKStages], (kn / kKStages) & 1) & (kn < nkt);
               tc::mma_f16_ts(o_col, a_hi + 16, bdesc, IDESC_O, 1u);
             }
           } else {
@@ -366,7 +361,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               const uint32_t o_col = tmem + kColO + (kk >> 2) * 128;
               const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
               const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
-              if (kk == 6) k_ok = mbar_test_wait(&bars.k_full[kn % kKStages], (kn / kKStages) & 1) & (kn < nkt);
               tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
             }
           }
