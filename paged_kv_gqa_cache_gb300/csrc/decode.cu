@@ -478,11 +478,11 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
 // ---- one cluster per item (few items: every item gets one or two SMs) ------------
 // The item's pages are dealt round-robin to the kItemWarps warps of each CTA of
 // a cluster of 1 or 2 CTAs, each warp streaming its pages through its own TMA
-// ring (two CTAs double the bytes in flight for the item).  The
-// warps' states (m, l, o) are then written to their own CTA's shared memory
-// (reusing the stage buffers) and merged by CTA 0, which reads the other CTA's
-// through distributed shared memory, and writes the item's output.  No
-// workspace and no second kernel.
+// ring (two CTAs double the bytes in flight for the item).  Each CTA then
+// merges its warps' states (m, l, o) in its own shared memory (reusing the
+// stage buffers), all threads at once; CTA 1 stores its merged state into CTA
+// 0's shared memory through the cluster and exits, and CTA 0 merges the two
+// and writes the item's output.  No workspace and no second kernel.
 constexpr int kItemWarps = 8;
 
 template <typename T, int G>
@@ -501,6 +501,9 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kItemWarps * kStages * STAGE) + warp * kStages;
   float2 *pbuf2 = reinterpret_cast<float2 *>(smem + kItemWarps * kStages * STAGE + kItemWarps * kStages * 8) +
                   warp * 16 * G;
+  // CTA 0 only: CTA 1's merged state, [G][kMerge] floats
+  float *peer = reinterpret_cast<float *>(smem + kItemWarps * kStages * STAGE + kItemWarps * kStages * 8 +
+                                          kItemWarps * 16 * G * 8);
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&kmap);
@@ -511,20 +514,23 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
     fence_mbar_init();
   }
-  griddep_wait();
 
   const int ncta = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
   const int item = blockIdx.x / ncta;
   const int hkv = p.num_kv_heads;
   const int s = item / hkv, h = item % hkv;
   // Warp gw of the item's nw warps takes pages gw, gw + nw, gw + 2 nw, ...: its
-  // first block ids do not depend on the length, so the length, the block ids
-  // and q are all fetched at once.
+  // first block ids do not depend on the length, so the length and the block
+  // ids are fetched at once.  No kernel of this library writes the block
+  // tables or the lengths, so they are read before waiting for the previous
+  // kernel (that wait covers the pool, which a KV write fills, and q, which may
+  // be another call's output); their latency overlaps the previous kernel.
   const int gw = rank * kItemWarps + warp, nw = ncta * kItemWarps;
   const int32_t *bt = p.block_tables + (int64_t)s * p.max_blocks_per_seq;
   const int ctx = __ldg(p.context_lens + s);
   int win_base = 0;  // window of 32 block ids: lane j holds page gw + nw (win_base + j)
   int32_t win = (gw + nw * lane < p.max_blocks_per_seq) ? __ldg(bt + gw + nw * lane) : -1;
+  griddep_wait();
 
   const int qd = lane % NQ, tk = lane / NQ, rot = tk % CPL;
   float2 q[G][DPL / 2];
@@ -607,7 +613,8 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   // the next kernel may start its set-up while the item is merged (it still
   // waits for this grid to complete before reading anything)
   griddep_launch_dependents();
-  // ---- merge the warps' states in shared memory (the stage buffers are idle now) ----
+  // ---- merge: the warps of each CTA in its shared memory (the stage buffers
+  // are idle now), then CTA 1's state into CTA 0 through the cluster ----
   __syncthreads();
   float *mine = reinterpret_cast<float *>(stages);
 #pragma unroll
@@ -622,58 +629,72 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     }
     *reinterpret_cast<float4 *>(dst + 4 + 4 * lane) = make_float4(o[gg][0].x, o[gg][0].y, o[gg][1].x, o[gg][1].y);
   }
-  if (ncta > 1) cluster_sync();  // the partials of both CTAs are written and visible
-  else __syncthreads();
-  if (rank == 0 && warp < G && !timed_out) {
-    const int gg = warp;
-    // state of warp w of CTA r (r = 0: own shared memory, else the peer's)
-    auto part = [&](int r, int w, int off) -> uint32_t {
-      const float *a = reinterpret_cast<const float *>(smem + w * kStages * STAGE) + gg * kMerge + off;
-      return r == 0 ? smem_u32(a) : map_to_rank(a, (uint32_t)r);
-    };
-    // every load first (they are independent), then the arithmetic
-    constexpr int kParts = 2 * kItemWarps;
-    float mv[kParts], lv[kParts];
-    float4 ov[kParts];
+  const bool any_timeout = __syncthreads_or(timed_out ? 1 : 0) != 0;
+  // thread (warp mg, lane) merges head mg, dims 4 lane .. 4 lane + 3, over the CTA's warps in order
+  const int mg = warp;
+  float M = -INFINITY, L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mg < G) {
+    float mv[kItemWarps], lv[kItemWarps];
+    float4 ov[kItemWarps];
 #pragma unroll
-    for (int i = 0; i < kParts; ++i) {
-      const int r = i / kItemWarps, w = i % kItemWarps;
-      if (r < ncta) {
-        mv[i] = ld_cluster_f32(part(r, w, 0));
-        lv[i] = ld_cluster_f32(part(r, w, 1));
-        ov[i] = ld_cluster_v4(part(r, w, 4 + 4 * lane));
-      } else {
-        mv[i] = -INFINITY;
-        lv[i] = 0.f;
-        ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < kItemWarps; ++w) {  // every load first (they are independent), then the arithmetic
+      const float *a = reinterpret_cast<const float *>(smem + w * kStages * STAGE) + mg * kMerge;
+      mv[w] = a[0];
+      lv[w] = a[1];
+      ov[w] = *reinterpret_cast<const float4 *>(a + 4 + 4 * lane);
+    }
+#pragma unroll
+    for (int w = 0; w < kItemWarps; ++w) M = fmaxf(M, mv[w]);
+#pragma unroll
+    for (int w = 0; w < kItemWarps; ++w) {
+      const float wgt = (mv[w] == -INFINITY) ? 0.f : exp2f(mv[w] - M);  // a warp without pages: weight 0
+      L += lv[w] * wgt;
+      O.x = fmaf(wgt, ov[w].x, O.x);
+      O.y = fmaf(wgt, ov[w].y, O.y);
+      O.z = fmaf(wgt, ov[w].z, O.z);
+      O.w = fmaf(wgt, ov[w].w, O.w);
+    }
+  }
+  if (ncta > 1) {
+    if (rank != 0) {  // hand the state to CTA 0 and leave
+      if (mg < G) {
+        const uint32_t dst = map_to_rank(peer + mg * kMerge, 0);
+        if (lane == 0) {
+          st_cluster_f32(dst, M);
+          st_cluster_f32(dst + 4, L);
+        }
+        st_cluster_v4(dst + 4 * (4 + 4 * lane), O);
       }
+      cluster_arrive();  // release: CTA 0 sees the stores once its wait returns
+      return;
     }
-    float M = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kParts; ++i) M = fmaxf(M, mv[i]);
-    float L = 0.f;
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < kParts; ++i) {
-      const float wgt = (mv[i] == -INFINITY) ? 0.f : exp2f(mv[i] - M);  // a warp without pages: weight 0
-      L += lv[i] * wgt;
-      O.x = fmaf(wgt, ov[i].x, O.x);
-      O.y = fmaf(wgt, ov[i].y, O.y);
-      O.z = fmaf(wgt, ov[i].z, O.z);
-      O.w = fmaf(wgt, ov[i].w, O.w);
+    cluster_arrive();
+    cluster_wait();
+    if (mg < G) {
+      const float *a = peer + mg * kMerge;
+      const float M1 = a[0], L1 = a[1];
+      const float4 O1 = *reinterpret_cast<const float4 *>(a + 4 + 4 * lane);
+      const float Mx = fmaxf(M, M1);
+      const float w0 = (M == -INFINITY) ? 0.f : exp2f(M - Mx), w1 = (M1 == -INFINITY) ? 0.f : exp2f(M1 - Mx);
+      L = L * w0 + L1 * w1;
+      O = make_float4(fmaf(w1, O1.x, O.x * w0), fmaf(w1, O1.y, O.y * w0), fmaf(w1, O1.z, O.z * w0),
+                      fmaf(w1, O1.w, O.w * w0));
     }
+  }
+  if (mg < G && !any_timeout) {
     const float inv = 1.f / L;
-    T *op = reinterpret_cast<T *>(p.out) + ((int64_t)s * p.num_q_heads + h * G + gg) * kHeadDim + 4 * lane;
+    T *op = reinterpret_cast<T *>(p.out) + ((int64_t)s * p.num_q_heads + h * G + mg) * kHeadDim + 4 * lane;
     uint2 pk;
     pk.x = Pack<T>::from_f2(O.x * inv, O.y * inv);
     pk.y = Pack<T>::from_f2(O.z * inv, O.w * inv);
     *reinterpret_cast<uint2 *>(op) = pk;
   }
-  if (ncta > 1) cluster_sync();  // CTA 0 has read the peer's shared memory: both may exit
 }
 
 int item_smem_bytes(int group) {
-  return 1024 + kItemWarps * kStages * STAGE + kItemWarps * kStages * 8 + kItemWarps * 16 * group * 8;
+  return 1024 + kItemWarps * kStages * STAGE + kItemWarps * kStages * 8 + kItemWarps * 16 * group * 8 +
+         group * (4 + kHeadDim) * 4;
 }
 
 int split_smem_bytes(int group, int num_seqs) {

@@ -66,6 +66,14 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync(), for a CTA that only signals (arrive, then
+// exit) while another waits.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
   uint32_t a;
@@ -78,6 +86,15 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   float v;
   asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
   return v;
+}
+// Stores into (possibly another CTA's) shared memory; a cluster_arrive()
+// after them makes them visible to a CTA that then passes cluster_wait().
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
 }
 __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
   float4 v;

@@ -210,7 +210,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars &bars = *reinterpret_cast<Bars *>(smem + OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  griddep_wait();
+  // No kernel of this library writes the chunk metadata or the block tables,
+  // so they are read, and shared and tensor memory set up, while the previous
+  // kernel may still run; only the loader warps, before their first copy of
+  // Q, K or V, wait for it (every other warp consumes what the loaders fetch,
+  // so its output stores also come after that wait).
 
   // Heaviest tiles first: last chunk, last query tile.
   const int c = p.num_chunks - 1 - (int)blockIdx.z;
@@ -269,12 +273,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     int32_t *sbt = reinterpret_cast<int32_t *>(smem + OFF_BT);
     const int cached = min(min(npages, nkt * 8), kBtCache);
     for (int i = lw * 32 + lane; i < cached; i += kLoadWarps * 32) sbt[i] = __ldg(bt + i);
+    named_barrier(1, kLoadWarps * 32);  // the cached block ids are complete
+    griddep_wait();                     // Q, K and V may come from the previous kernel
     if (lw == 0 && lane == 0) {
       mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf);
       tma_load_3d(smem + OFF_Q, &qmap, &bars.q_full, 0, h * G, row0 + t0);
       tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
     }
-    named_barrier(1, kLoadWarps * 32);  // the cached block ids are complete
     const int kb0 = lw, vb0 = (lw + kLoadWarps - 1) % kLoadWarps;  // balances the boxes per warp
     for (int t = 0; t < nkt; ++t) {
       const int ks = t % kKStages, vs = t % kVStages;
