@@ -13,7 +13,8 @@ Sources are cited by page title and section:
   (Qwen3Model.forward attention loop) — layout, slot addressing, GQA map,
   causal mask on absolute positions.
 * "Модуль 04: KV-кэш и арифметика памяти", section 1 (output formula),
-  section 2.1 (KV byte formula), kv_cache.py ``attend`` (GQA by repeat).
+  section 2.1 (KV byte formula), kv_cache.py ``attend`` (GQA by repeat),
+  section 5 (``KV8Cache``: int8 codes with one fp32 scale per token and head).
 * "Phase 10: LLMs from Scratch — Inference Optimization", step 2 (causal SDPA).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against things
@@ -71,6 +72,13 @@ def open_library(path: str):
     lib.oracle_paged_attn_prefill.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P,
                                               i32, P, i32, i32, f64, P, i32]
     lib.oracle_paged_attn_prefill.restype = ctypes.c_int
+    lib.oracle_kv_cache_write_q8.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P, i32, P, i64]
+    lib.oracle_kv_cache_write_q8.restype = i64
+    lib.oracle_gather_head_q8.argtypes = [P, P, P, P, i64, i32, i32, i32, P, i32, i32, P, P]
+    lib.oracle_gather_head_q8.restype = ctypes.c_int
+    lib.oracle_paged_attn_decode_q8.argtypes = [P, i32, P, P, P, P, i64, i32, i32, i32, P, i32, P,
+                                                i32, i32, f64, P, i32]
+    lib.oracle_paged_attn_decode_q8.restype = ctypes.c_int
     return lib
 
 
@@ -201,6 +209,61 @@ def paged_attn_prefill(q, k_cache, v_cache, chunk_starts, chunk_lens, block_tabl
                                            cs.shape[0], hq, float(scale), _ptr(out), num_threads)
     if rc != 0:
         raise ValueError(f"oracle prefill rejected its inputs (code {rc})")
+    return out
+
+
+def kv_cache_write_q8(k_codes, v_codes, k_scale, v_scale, k, v, dtype: int, slot_mapping) -> int:
+    """In-place quantising write into an int8 pool ("Модуль 04: KV-кэш и
+    арифметика памяти", section 5, ``KV8Cache.write``).
+
+    k_codes, v_codes: int8 [num_blocks, block_size, Hkv, d]; k_scale, v_scale:
+    float32 [num_blocks, Hkv, block_size] (modified in place).  k, v: [T, Hkv, d]
+    16-bit patterns of ``dtype``; slot_mapping: int64 [T].  Returns #skipped slots.
+    """
+    for a in (k_codes, v_codes):
+        assert a.dtype == np.int8 and a.flags.c_contiguous
+    for a in (k_scale, v_scale):
+        assert a.dtype == np.float32 and a.flags.c_contiguous
+    nb, bs, hkv, d = k_codes.shape
+    assert k_scale.shape == (nb, hkv, bs)
+    kb, vb = _bits(k), _bits(v)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    return int(_load().oracle_kv_cache_write_q8(_ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+                                                nb, bs, hkv, d, _ptr(kb), _ptr(vb), dtype, _ptr(sm),
+                                                sm.shape[0]))
+
+
+def gather_head_q8(k_codes, v_codes, k_scale, v_scale, block_table_row, kv_head: int, upto: int):
+    """Dequantised fp32 K/V rows (as fp64) of positions [0, upto) for one KV head."""
+    nb, bs, hkv, d = k_codes.shape
+    bt = np.ascontiguousarray(block_table_row, dtype=np.int32)
+    ko = np.zeros((upto, d), np.float64)
+    vo = np.zeros((upto, d), np.float64)
+    rc = _load().oracle_gather_head_q8(_ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale), nb, bs,
+                                       hkv, d, _ptr(bt), kv_head, upto, _ptr(ko), _ptr(vo))
+    if rc != 0:
+        raise IndexError("block id outside the pool")
+    return ko, vo
+
+
+def paged_attn_decode_q8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale: float,
+                         dtype: int, num_threads: int = 0) -> np.ndarray:
+    """fp64 decode attention over an int8 pool: q [S, Hq, d] 16-bit → out [S, Hq, d]."""
+    qb = _bits(q)
+    nb, bs, hkv, d = k_codes.shape
+    s, hq, dq = qb.shape
+    assert dq == d and k_scale.shape == (nb, hkv, bs)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    assert bt.shape[0] == s and ctx.shape == (s,)
+    out = np.zeros((s, hq, d), np.float64)
+    kc, vc = np.ascontiguousarray(k_codes), np.ascontiguousarray(v_codes)
+    ks, vs = np.ascontiguousarray(k_scale, dtype=np.float32), np.ascontiguousarray(v_scale, dtype=np.float32)
+    rc = _load().oracle_paged_attn_decode_q8(_ptr(qb), dtype, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb, bs,
+                                             hkv, d, _ptr(bt), bt.shape[1], _ptr(ctx), s, hq, float(scale),
+                                             _ptr(out), num_threads)
+    if rc != 0:
+        raise ValueError(f"oracle decode rejected its inputs (code {rc})")
     return out
 
 

@@ -26,6 +26,11 @@
  * [num_blocks][block_size][num_kv_heads][head_dim]; block b is the outer
  * index, the in-block slot the next one.  A flat slot number is
  * block * block_size + offset.
+ *
+ * The int8 pool [P2 section 5, KV8Cache]: K and V codes int8 in the same
+ * layout, one fp32 scale per (token, KV head) for K and one for V.  The
+ * quantising write and the dequantising read follow the pages' fp32 steps
+ * exactly; attention then runs in fp64 on the dequantised values.
  */
 #include <math.h>
 #include <pthread.h>
@@ -131,6 +136,82 @@ int oracle_gather_head(const uint16_t *k_cache, const uint16_t *v_cache, int dty
   return 0;
 }
 
+/* ---- int8 pool: quantising write and dequantising read [P2 section 5] ------- */
+
+/*
+ * Scales are stored [num_blocks][num_kv_heads][block_size]: the scale of the
+ * token in slot (block, offset) for KV head h is at (block * num_kv_heads + h)
+ * * block_size + offset.  (The pages keep one scale per (position, head) of a
+ * contiguous cache; this head-major order inside a block is the library's
+ * paged layout of the same numbers.)
+ *
+ * Write, per token and KV head, for K and for V [KV8Cache.write]: the 16-bit
+ * values x are widened exactly to fp32; scale = max |x| / 127 + 1e-8 and
+ * code = clip(rint(x / scale), -127, 127), each an fp32 operation rounded to
+ * nearest (rint: ties to even).  Returns the number of skipped slots (outside
+ * the pool).
+ */
+int64_t oracle_kv_cache_write_q8(int8_t *k_cache, int8_t *v_cache, float *k_scale, float *v_scale,
+                                 int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                 int32_t head_dim, const uint16_t *k, const uint16_t *v, int32_t dtype,
+                                 const int64_t *slot_mapping, int64_t num_tokens) {
+  int64_t skipped = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= num_blocks * block_size) {
+      ++skipped;
+      continue;
+    }
+    const int64_t block = slot / block_size, offset = slot % block_size;
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      for (int pass = 0; pass < 2; ++pass) {
+        const uint16_t *src = (pass == 0 ? k : v) + (t * num_kv_heads + h) * (int64_t)head_dim;
+        int8_t *dst = (pass == 0 ? k_cache : v_cache) + (slot * num_kv_heads + h) * (int64_t)head_dim;
+        float *scl = pass == 0 ? k_scale : v_scale;
+        float amax = 0.0f;
+        for (int32_t x = 0; x < head_dim; ++x) {
+          const float a = fabsf((float)widen(src[x], dtype));
+          if (a > amax) amax = a;
+        }
+        float scale = amax / 127.0f;
+        scale = scale + 1e-8f;
+        for (int32_t x = 0; x < head_dim; ++x) {
+          float c = rintf((float)widen(src[x], dtype) / scale);
+          if (c > 127.0f) c = 127.0f;
+          if (c < -127.0f) c = -127.0f;
+          dst[x] = (int8_t)c;
+        }
+        scl[(block * num_kv_heads + h) * block_size + offset] = scale;
+      }
+    }
+  }
+  return skipped;
+}
+
+/* Read [KV8Cache.read]: rows of positions [0, upto) of one KV head, each value
+ * code * scale as an fp32 product, widened to double.  Returns 0 or -1 (block
+ * id outside the pool). */
+int oracle_gather_head_q8(const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
+                          const float *v_scale, int64_t num_blocks, int32_t block_size,
+                          int32_t num_kv_heads, int32_t head_dim, const int32_t *block_table_row,
+                          int32_t kv_head, int32_t upto, double *k_out, double *v_out) {
+  for (int32_t j = 0; j < upto; ++j) {
+    int32_t entry = j / block_size, offset = j % block_size;
+    int64_t block = block_table_row[entry];
+    if (block < 0 || block >= num_blocks) return -1;
+    const int64_t base = ((block * block_size + offset) * num_kv_heads + kv_head) * (int64_t)head_dim;
+    const int64_t sidx = (block * num_kv_heads + kv_head) * block_size + offset;
+    const float ks = k_scale[sidx], vs = v_scale[sidx];
+    for (int32_t x = 0; x < head_dim; ++x) {
+      const float kf = (float)k_cache[base + x] * ks;
+      const float vf = (float)v_cache[base + x] * vs;
+      k_out[(int64_t)j * head_dim + x] = (double)kf;
+      v_out[(int64_t)j * head_dim + x] = (double)vf;
+    }
+  }
+  return 0;
+}
+
 /* ---- one query row of attention [P1 Qwen3Model.forward; P2 section 1] ------ */
 
 /*
@@ -181,6 +262,9 @@ typedef struct {
   int64_t next;                 /* work counter: (group, kv head) items */
   pthread_mutex_t lock;
   int error;
+  /* int8 pool instead of k_cache / v_cache when k8 is not NULL */
+  const int8_t *k8, *v8;
+  const float *k_scale, *v_scale;
 } problem_t;
 
 static void run_item(problem_t *P, int32_t g, int32_t h, double *kk, double *vv,
@@ -189,9 +273,12 @@ static void run_item(problem_t *P, int32_t g, int32_t h, double *kk, double *vv,
   const int32_t G = P->num_q_heads / P->num_kv_heads;
   const int32_t nrows = P->group_nrows[g], row0 = P->group_row0[g], pos0 = P->group_pos0[g];
   const int32_t nkeys = pos0 + nrows;   /* keys the last row of the group sees */
-  if (oracle_gather_head(P->k_cache, P->v_cache, P->dtype, P->num_blocks, P->block_size,
-                         P->num_kv_heads, d, P->block_tables + (int64_t)g * P->max_blocks_per_seq,
-                         h, nkeys, kk, vv) != 0) {
+  const int32_t *bt_row = P->block_tables + (int64_t)g * P->max_blocks_per_seq;
+  const int grc = P->k8 ? oracle_gather_head_q8(P->k8, P->v8, P->k_scale, P->v_scale, P->num_blocks,
+                                                P->block_size, P->num_kv_heads, d, bt_row, h, nkeys, kk, vv)
+                        : oracle_gather_head(P->k_cache, P->v_cache, P->dtype, P->num_blocks, P->block_size,
+                                             P->num_kv_heads, d, bt_row, h, nkeys, kk, vv);
+  if (grc != 0) {
     pthread_mutex_lock(&P->lock);
     P->error = -1;
     pthread_mutex_unlock(&P->lock);
@@ -269,6 +356,9 @@ static int run_problem(problem_t *P, int32_t num_threads) {
  * Returns 0, -1 for a block id out of range, -3 for a bad head split, -4 for a
  * context length < 1 or beyond the block table.
  */
+static int decode_problem(problem_t *P, const int32_t *context_lens, int32_t num_seqs,
+                          int32_t num_threads);
+
 int oracle_paged_attn_decode(const uint16_t *q, int32_t dtype,
                              const uint16_t *k_cache, const uint16_t *v_cache,
                              int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
@@ -276,6 +366,31 @@ int oracle_paged_attn_decode(const uint16_t *q, int32_t dtype,
                              int32_t max_blocks_per_seq, const int32_t *context_lens,
                              int32_t num_seqs, int32_t num_q_heads, double scale,
                              double *out, int32_t num_threads) {
+  problem_t P = {q, dtype, k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim,
+                 block_tables, max_blocks_per_seq, num_q_heads, scale, out};
+  return decode_problem(&P, context_lens, num_seqs, num_threads);
+}
+
+/* The same decode on the int8 pool [P2 section 5]: keys and values are the
+ * dequantised fp32 numbers of KV8Cache.read. */
+int oracle_paged_attn_decode_q8(const uint16_t *q, int32_t dtype, const int8_t *k_cache,
+                                const int8_t *v_cache, const float *k_scale, const float *v_scale,
+                                int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                int32_t head_dim, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                double scale, double *out, int32_t num_threads) {
+  problem_t P = {q, dtype, NULL, NULL, num_blocks, block_size, num_kv_heads, head_dim,
+                 block_tables, max_blocks_per_seq, num_q_heads, scale, out};
+  P.k8 = k_cache;
+  P.v8 = v_cache;
+  P.k_scale = k_scale;
+  P.v_scale = v_scale;
+  return decode_problem(&P, context_lens, num_seqs, num_threads);
+}
+
+static int decode_problem(problem_t *P, const int32_t *context_lens, int32_t num_seqs,
+                          int32_t num_threads) {
+  const int32_t max_blocks_per_seq = P->max_blocks_per_seq, block_size = P->block_size;
   int32_t *row0 = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1));
   int32_t *nrows = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1));
   int32_t *pos0 = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1));
@@ -288,10 +403,11 @@ int oracle_paged_attn_decode(const uint16_t *q, int32_t dtype,
     pos0[s] = n - 1;
   }
   if (rc == 0) {
-    problem_t P = {q, dtype, k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim,
-                   block_tables, max_blocks_per_seq, num_q_heads, scale, out,
-                   num_seqs, row0, nrows, pos0};
-    rc = run_problem(&P, num_threads);
+    P->num_groups = num_seqs;
+    P->group_row0 = row0;
+    P->group_nrows = nrows;
+    P->group_pos0 = pos0;
+    rc = run_problem(P, num_threads);
   }
   free(row0);
   free(nrows);
