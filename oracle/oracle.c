@@ -196,7 +196,8 @@ int oracle_gather_head_q8(const int8_t *k_cache, const int8_t *v_cache, const fl
                           int32_t num_kv_heads, int32_t head_dim, const int32_t *block_table_row,
                           int32_t kv_head, int32_t upto, double *k_out, double *v_out) {
   for (int32_t j = 0; j < upto; ++j) {
-    int32_t entry = j / block_size, offset = j % block_size;
+    const int32_t entry = j / block_size;
+    const int32_t offset = j % block_size;
     int64_t block = block_table_row[entry];
     if (block < 0 || block >= num_blocks) return -1;
     const int64_t base = ((block * block_size + offset) * num_kv_heads + kv_head) * (int64_t)head_dim;

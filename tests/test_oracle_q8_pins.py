@@ -201,6 +201,7 @@ MUTATIONS = {
     "read-uses-k-scale-for-v": ("const float ks = k_scale[sidx], vs = v_scale[sidx];",
                                 "const float ks = k_scale[sidx], vs = k_scale[sidx];"),
     "range-divisor-128": ("float scale = amax / 127.0f;", "float scale = amax / 128.0f;"),
+    "read-offset-shifted": ("const int32_t offset = j % block_size;", "const int32_t offset = (j + 1) % block_size;"),
 }
 
 
