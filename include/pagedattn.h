@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 #define PA_HEAD_DIM 128
 #define PA_BLOCK_SIZE 16
 #define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
@@ -195,6 +195,52 @@ PA_API pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk
                                       int32_t num_q_heads, int32_t total_q_tokens,
                                       int32_t max_chunk_len, float scale, void *out,
                                       pa_stream_t stream);
+
+/*
+ * ---- int8 KV pool [P2 section 5, KV8Cache] ----------------------------------
+ * One layer's pool with int8 codes instead of 16-bit values: K and V codes
+ * [num_blocks][16][num_kv_heads][128] (the same slot addressing), and one fp32
+ * scale per (token, KV head) for K and one for V, stored
+ * [num_blocks][num_kv_heads][16] (head-major inside a block, so the 16 scales
+ * of one page of one KV head are 64 contiguous bytes).  Half the bytes of a
+ * 16-bit pool plus 8 bytes per token and KV head.  All four arrays are
+ * caller-owned device memory, 16-byte aligned.
+ */
+typedef struct {
+  void *k_cache;        /* int8 codes */
+  void *v_cache;
+  float *k_scale;       /* fp32 scales */
+  float *v_scale;
+  int32_t num_blocks;
+  int32_t block_size;   /* must be 16 */
+  int32_t num_kv_heads;
+  int32_t head_dim;     /* must be 128 */
+} pa_kv_pool_q8;
+
+/*
+ * kv_cache_write_q8 — [P2 section 5, KV8Cache.write]: quantise the K and V
+ * rows of num_tokens new tokens into their slots of an int8 pool.  For each
+ * token and KV head, separately for K and V: scale = max |x| / 127 + 1e-8 and
+ * code = clip(rint(x / scale), -127, 127), in fp32 with every operation
+ * rounded to nearest (ties to even), so codes and scales are bit-exact.
+ *   k, v          [num_tokens][num_kv_heads][128] in `dtype` (PA_F16 / PA_BF16).
+ *   slot_mapping  int64 [num_tokens] as for pa_kv_cache_write; a slot outside
+ *                 the pool records PA_ERR_RANGE and is skipped.
+ */
+PA_API pa_status pa_kv_cache_write_q8(const void *k, const void *v, int32_t dtype, const int64_t *slot_mapping,
+                                      int32_t num_tokens, const pa_kv_pool_q8 *pool, pa_stream_t stream);
+
+/*
+ * paged_attn_decode_q8 — pa_paged_attn_decode over an int8 pool: keys and
+ * values are the dequantised numbers code * scale [P2 section 5,
+ * KV8Cache.read]; q and out are `dtype` (PA_F16 / PA_BF16).  Arguments,
+ * workspace (pa_decode_workspace_bytes) and errors as pa_paged_attn_decode.
+ */
+PA_API pa_status pa_paged_attn_decode_q8(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_context_len, float scale, void *out, void *workspace,
+                                         size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's error

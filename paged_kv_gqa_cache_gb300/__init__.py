@@ -11,6 +11,8 @@ Calls (see include/pagedattn.h for the full contract):
 * ``paged_attn_decode(q, k_cache, v_cache, block_tables, context_lens, scale, ...)``
 * ``paged_attn_prefill_chunk(q, chunk_starts, chunk_lens, k_cache, v_cache,
   block_tables, context_lens, scale, ...)``
+* ``kv_cache_write_q8`` / ``paged_attn_decode_q8`` on an int8 pool
+  (``alloc_pool_q8``: codes plus one fp32 scale per token and KV head)
 * ``get_device_error()``
 """
 from __future__ import annotations
@@ -34,7 +36,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_decode",
            "pa_paged_attn_prefill_chunk", "pa_get_device_error", "pa_status_string",
            "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc",
-           "pa_decode_kernel_launches")
+           "pa_decode_kernel_launches", "pa_kv_cache_write_q8", "pa_paged_attn_decode_q8")
 
 
 class PagedAttnError(RuntimeError):
@@ -48,6 +50,13 @@ class KVPool(ctypes.Structure):
                 ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32)]
+
+
+class KVPoolQ8(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
 
 _lib = None
@@ -67,6 +76,12 @@ def load_library(path: str = LIB_PATH):
         lib = ctypes.CDLL(path)
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         pool_p = ctypes.POINTER(KVPool)
+        q8_p = ctypes.POINTER(KVPoolQ8)
+        lib.pa_kv_cache_write_q8.argtypes = [P, P, i32, P, i32, q8_p, P]
+        lib.pa_kv_cache_write_q8.restype = i32
+        lib.pa_paged_attn_decode_q8.argtypes = [P, i32, q8_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P,
+                                                ctypes.c_size_t, P]
+        lib.pa_paged_attn_decode_q8.restype = i32
         lib.pa_kv_cache_write.argtypes = [P, P, P, i32, pool_p, P]
         lib.pa_kv_cache_write.restype = i32
         lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -150,6 +165,71 @@ def kv_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     lib = load_library()
     _check(lib.pa_kv_cache_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
                                  ctypes.byref(pool), _stream(stream)), "pa_kv_cache_write")
+
+
+def alloc_pool_q8(num_blocks: int, num_kv_heads: int, device=None):
+    """An int8 pool ("Модуль 04: KV-кэш и арифметика памяти", section 5): K and V
+    codes int8 [num_blocks, 16, Hkv, 128] and fp32 scales [num_blocks, Hkv, 16]."""
+    dev = device or "cuda"
+    codes = lambda: torch.zeros((num_blocks, 16, num_kv_heads, 128), dtype=torch.int8, device=dev)
+    scales = lambda: torch.zeros((num_blocks, num_kv_heads, 16), dtype=torch.float32, device=dev)
+    return codes(), codes(), scales(), scales()
+
+
+def make_pool_q8(k_codes, v_codes, k_scale, v_scale) -> KVPoolQ8:
+    _need(k_codes, "k_codes", torch.int8)
+    _need(v_codes, "v_codes", torch.int8)
+    _need(k_scale, "k_scale", torch.float32)
+    _need(v_scale, "v_scale", torch.float32)
+    if k_codes.dim() != 4 or k_codes.shape != v_codes.shape:
+        raise ValueError("k_codes and v_codes must both be [num_blocks, block_size, num_kv_heads, head_dim]")
+    nb, bs, hkv, d = k_codes.shape
+    if k_scale.shape != (nb, hkv, bs) or v_scale.shape != k_scale.shape:
+        raise ValueError(f"k_scale and v_scale must be [{nb}, {hkv}, {bs}]")
+    return KVPoolQ8(k_codes.data_ptr(), v_codes.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(), nb, bs, hkv, d)
+
+
+def kv_cache_write_q8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_codes: torch.Tensor,
+                      v_codes: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor, stream=None) -> None:
+    """Quantise new K/V rows [T, Hkv, 128] (fp16 / bf16) into flat slots of an int8 pool."""
+    pool = make_pool_q8(k_codes, v_codes, k_scale, v_scale)
+    _need(k, "k")
+    _need(v, "v", k.dtype)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    T = slot_mapping.numel()
+    if k.shape != (T, pool.num_kv_heads, pool.head_dim) or v.shape != k.shape:
+        raise ValueError(f"k, v must be [{T}, {pool.num_kv_heads}, {pool.head_dim}]")
+    lib = load_library()
+    _check(lib.pa_kv_cache_write_q8(k.data_ptr(), v.data_ptr(), _dtype_code(k), slot_mapping.data_ptr(), T,
+                                    ctypes.byref(pool), _stream(stream)), "pa_kv_cache_write_q8")
+
+
+def paged_attn_decode_q8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor, k_scale: torch.Tensor,
+                         v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                         scale: float, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                         max_context_len: Optional[int] = None, stream=None) -> torch.Tensor:
+    """Decode attention over an int8 pool: q [S, Hq, 128] (fp16 / bf16) → out, same dtype."""
+    pool = make_pool_q8(k_codes, v_codes, k_scale, v_scale)
+    _need(q, "q")
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    S, hq, d = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks], context_lens [S]")
+    mb = block_tables.shape[1]
+    mcl = int(max_context_len) if max_context_len is not None else mb * pool.block_size
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype)
+    if workspace is None:
+        workspace = alloc_decode_workspace(S, hq, pool.num_kv_heads, mcl, q.device)
+    _need(workspace, "workspace")
+    lib = load_library()
+    _check(lib.pa_paged_attn_decode_q8(q.data_ptr(), _dtype_code(q), ctypes.byref(pool), block_tables.data_ptr(),
+                                       mb, context_lens.data_ptr(), S, hq, mcl, float(scale), out.data_ptr(),
+                                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)), "pa_paged_attn_decode_q8")
+    return out
 
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int) -> int:

@@ -122,12 +122,40 @@ __device__ __forceinline__ void advance(Cursor &c, const int32_t *prefix, int n,
   c.pages = (c.s < n) ? prefix[c.s + 1] - prefix[c.s] : 1;
 }
 
+// A stage holds one page of one KV head.  16-bit pools: K rows (256 B) at 0,
+// V rows at 4096.  int8 pools ("Модуль 04: KV-кэш и арифметика памяти",
+// section 5, KV8Cache: one fp32 scale per token and KV head): K codes (128 B
+// rows) at 0, V codes at 2048, the page's 16 K scales at 4096 and 16 V scales
+// at 4160.
+constexpr int kQ8V = 2048, kQ8KS = 4096, kQ8VS = 4160, kQ8StageBytes = 4224;
+static_assert(kQ8StageBytes <= STAGE, "an int8 page fits a stage");
+
+// Fetch page blk of KV head h into the stage at dst, completing on bar.
+template <bool Q8>
+__device__ __forceinline__ void load_page(uint8_t *dst, const CUtensorMap *kmap, const CUtensorMap *vmap,
+                                          uint64_t *bar, const DecodeParams &p, int h, int blk) {
+  if constexpr (Q8) {
+    mbar_arrive_expect_tx(bar, kQ8StageBytes);
+    tma_load_4d(dst, kmap, bar, 0, h, 0, blk);
+    tma_load_4d(dst + kQ8V, vmap, bar, 0, h, 0, blk);
+    const int64_t si = ((int64_t)blk * p.num_kv_heads + h) * kBlock;  // scales of (block, head): 64 B
+    bulk_load(dst + kQ8KS, p.k_scale + si, kBlock * 4, bar);
+    bulk_load(dst + kQ8VS, p.v_scale + si, kBlock * 4, bar);
+  } else {
+    mbar_arrive_expect_tx(bar, STAGE);
+    tma_load_4d(dst, kmap, bar, 0, h, 0, blk);
+    tma_load_4d(dst + 4096, vmap, bar, 0, h, 0, blk);
+  }
+}
+
 // Scores, online-softmax update and P V of one 16-key page for the G query
-// heads of a KV head: K at kst, V at kst + 4096 (one warp; nv valid keys).
-// q holds this lane's dims of the G query rows (pre-scaled, log2 domain);
-// (m, l, o) is the running state (m warp-uniform, l per lane, o for the lane's
-// 4 dims).  pbuf2 is the warp's [16 keys][G] scratch for the probabilities.
-template <typename T, int G>
+// heads of a KV head, from a stage laid out as above (one warp; nv valid
+// keys).  q holds this lane's dims of the G query rows (pre-scaled, log2
+// domain); (m, l, o) is the running state (m warp-uniform, l per lane, o for
+// the lane's 4 dims).  pbuf2 is the warp's [16 keys][G] scratch for the
+// probabilities.  With int8 codes a key's scale multiplies its dot product
+// once, and a value's scale multiplies its probability before the sum.
+template <typename T, int G, bool Q8>
 __device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const float2 (&q)[G][Layout<G>::DPL / 2],
                                             float2 (&o)[G][2], float (&m)[G], float (&l)[G], float2 *pbuf2,
                                             int lane) {
@@ -137,7 +165,9 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const fl
   const int tk = lane / NQ;  // which key of a pass
   const int rot = tk % CPL;  // chunk rotation of this lane's keys (NT is a multiple of CPL)
   const float neg_inf = -INFINITY;
-  const uint8_t *vst = kst + 4096;
+  const uint8_t *vst = kst + (Q8 ? kQ8V : 4096);
+  const float *kscale = reinterpret_cast<const float *>(kst + kQ8KS);
+  const float *vscale = reinterpret_cast<const float *>(kst + kQ8VS);
 
   // scores: NP passes of NT keys; lanes of one key hold slices of its dims
   float sc[NP][G];
@@ -149,21 +179,32 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const fl
     for (int gg = 0; gg < G; ++gg) acc[gg] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      const int chunk = qd + NQ * ((i + rot) % CPL);
-      const uint4 u = *reinterpret_cast<const uint4 *>(kst + t * 256 + chunk * 16);
-      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+      const int chunk = qd + NQ * ((i + rot) % CPL);  // dims 8 chunk .. 8 chunk + 7
+      if constexpr (Q8) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(kst + t * 128 + chunk * 8);
+        const float2 k2[4] = {s8x2_to_f2<0>(u.x), s8x2_to_f2<1>(u.x), s8x2_to_f2<0>(u.y), s8x2_to_f2<1>(u.y)};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 k2 = Pack<T>::to_f2(wd[e]);
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) acc[gg] = __ffma2_rn(q[gg][i * 4 + e], k2, acc[gg]);
+          for (int gg = 0; gg < G; ++gg) acc[gg] = __ffma2_rn(q[gg][i * 4 + e], k2[e], acc[gg]);
+      } else {
+        const uint4 u = *reinterpret_cast<const uint4 *>(kst + t * 256 + chunk * 16);
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 k2 = Pack<T>::to_f2(wd[e]);
+#pragma unroll
+          for (int gg = 0; gg < G; ++gg) acc[gg] = __ffma2_rn(q[gg][i * 4 + e], k2, acc[gg]);
+        }
       }
     }
+    const float ksc = Q8 ? kscale[t] : 1.f;
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
       float a = acc[gg].x + acc[gg].y;
 #pragma unroll
       for (int off = 1; off < NQ; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
+      if constexpr (Q8) a *= ksc;
       sc[ps][gg] = (t < nv) ? a : neg_inf;
     }
   }
@@ -184,7 +225,8 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const fl
     for (int ps = 0; ps < NP; ++ps) {
       const float pr = exp2f(sc[ps][gg] - mn);
       ls += pr;
-      if (qd == 0) pbuf2[(ps * NT + tk) * G + gg] = make_float2(pr, pr);
+      const float pv = Q8 ? pr * vscale[ps * NT + tk] : pr;  // the value's scale rides on its weight
+      if (qd == 0) pbuf2[(ps * NT + tk) * G + gg] = make_float2(pv, pv);
     }
     l[gg] = l[gg] * alpha + ls;
     const float2 a2 = make_float2(alpha, alpha);
@@ -195,9 +237,16 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const fl
 
   // weighted sum of values: this lane owns dims [4 * lane, 4 * lane + 4)
   auto pv_token = [&](int t) {
-    const uint2 u = *reinterpret_cast<const uint2 *>(vst + t * 256 + 8 * lane);
-    const float2 v01 = Pack<T>::to_f2(u.x);
-    const float2 v23 = Pack<T>::to_f2(u.y);
+    float2 v01, v23;
+    if constexpr (Q8) {
+      const uint32_t w = *reinterpret_cast<const uint32_t *>(vst + t * 128 + 4 * lane);
+      v01 = s8x2_to_f2<0>(w);
+      v23 = s8x2_to_f2<1>(w);
+    } else {
+      const uint2 u = *reinterpret_cast<const uint2 *>(vst + t * 256 + 8 * lane);
+      v01 = Pack<T>::to_f2(u.x);
+      v23 = Pack<T>::to_f2(u.y);
+    }
     float2 pp[G];
     if constexpr (G == 1) {
       pp[0] = pbuf2[t];
@@ -223,7 +272,7 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const fl
   }
 }
 
-template <typename T, int G>
+template <typename T, int G, bool Q8>
 __global__ void __launch_bounds__(NW * 32)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const DecodeParams p) {
@@ -292,10 +341,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     const bool ok = (unsigned)blk < (unsigned)p.num_blocks;
     if (lane == 0) {
       if (ok) {
-        uint8_t *dst = stages + st * STAGE;
-        mbar_arrive_expect_tx(&bars[st], STAGE);
-        tma_load_4d(dst, &kmap, &bars[st], 0, ic.h, 0, blk);
-        tma_load_4d(dst + 4096, &vmap, &bars[st], 0, ic.h, 0, blk);
+        load_page<Q8>(stages + st * STAGE, &kmap, &vmap, &bars[st], p, ic.h, blk);
       } else {
         set_error(p.err, PA_ERR_RANGE, ic.s);
         mbar_arrive(&bars[st]);
@@ -358,7 +404,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 
     if (!((bad_mask >> st) & 1u)) {
       const int nv = min(kBlock, ctx - cc.page * kBlock);  // valid keys in this page
-      decode_page<T, G>(stages + st * STAGE, nv, q, o, m, l, pbuf2, lane);
+      decode_page<T, G, Q8>(stages + st * STAGE, nv, q, o, m, l, pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
 
@@ -485,7 +531,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
 // and writes the item's output.  No workspace and no second kernel.
 constexpr int kItemWarps = 8;
 
-template <typename T, int G>
+template <typename T, int G, bool Q8>
 __global__ void __launch_bounds__(kItemWarps * 32, 1)
 decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                    const DecodeParams p) {
@@ -567,7 +613,6 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 
   uint32_t bad_mask = 0;
   auto issue = [&](int i, int st) {
-    const int pg = gw + nw * i;
     if ((i & ~31) != win_base) {
       win_base = i & ~31;
       const int pj = gw + nw * (win_base + lane);
@@ -577,10 +622,7 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     const bool ok = (unsigned)blk < (unsigned)p.num_blocks;
     if (lane == 0) {
       if (ok) {
-        uint8_t *dst = stages + st * STAGE;
-        mbar_arrive_expect_tx(&bars[st], STAGE);
-        tma_load_4d(dst, &kmap, &bars[st], 0, h, 0, blk);
-        tma_load_4d(dst + 4096, &vmap, &bars[st], 0, h, 0, blk);
+        load_page<Q8>(stages + st * STAGE, &kmap, &vmap, &bars[st], p, h, blk);
       } else {
         set_error(p.err, PA_ERR_RANGE, s);
         mbar_arrive(&bars[st]);
@@ -604,7 +646,7 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     }
     if (!((bad_mask >> st) & 1u)) {
       const int nv = min(kBlock, ctx - (gw + nw * i) * kBlock);  // valid keys in this page
-      decode_page<T, G>(stages + st * STAGE, nv, q, o, m, l, pbuf2, lane);
+      decode_page<T, G, Q8>(stages + st * STAGE, nv, q, o, m, l, pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
     if (i + kStages < n) issue(i + kStages, st);
@@ -723,7 +765,7 @@ int decode_item_ctas(int items, int max_pages_per_item) {
 
 namespace {
 
-template <typename T, int G>
+template <typename T, int G, bool Q8>
 cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          int max_workers, int max_pages_per_item, cudaStream_t stream) {
   DecodeParams p = p0;
@@ -733,12 +775,12 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
     const int ismem = item_smem_bytes(G);
     static bool item_configured = false;
     if (!item_configured) {
-      cudaError_t e = cudaFuncSetAttribute(decode_item_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(decode_item_kernel<T, G, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            ismem);
       if (e != cudaSuccess) return e;
       item_configured = true;
     }
-    return launch_pdl_cluster(decode_item_kernel<T, G>, dim3(items * ctas), dim3(kItemWarps * 32), ismem, ctas,
+    return launch_pdl_cluster(decode_item_kernel<T, G, Q8>, dim3(items * ctas), dim3(kItemWarps * 32), ismem, ctas,
                               stream, kmap, vmap, p);
   }
   const int smem = split_smem_bytes(G, p.num_seqs);
@@ -747,11 +789,11 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
   // the hot path and out of CUDA-graph capture after the first call).
   static int configured_smem = 0, cached_per_sm = 0;
   if (smem > configured_smem) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, G>,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, G, Q8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<T, G>, NW * 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<T, G, Q8>, NW * 32, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     configured_smem = smem;
@@ -765,7 +807,7 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
   if (grid < 1) grid = 1;
   if (grid * NW > kDecodeMaxWorkers) grid = kDecodeMaxWorkers / NW;
   p.num_workers = grid * NW;
-  e = launch_pdl(decode_split_kernel<T, G>, dim3(grid), dim3(NW * 32), smem, stream, kmap, vmap, p);
+  e = launch_pdl(decode_split_kernel<T, G, Q8>, dim3(grid), dim3(NW * 32), smem, stream, kmap, vmap, p);
   if (e != cudaSuccess) return e;
   const int cgrid = (p.num_seqs * p.num_q_heads + 3) / 4;
   return launch_pdl(decode_combine_kernel<T, G>, dim3(cgrid), dim3(128), 0, stream, p);
@@ -797,9 +839,12 @@ bool decode_workspace_carve(void *ws, size_t bytes, int num_seqs, int num_q_head
 }
 
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          int dtype, int group, int max_workers, int max_pages_per_item, cudaStream_t stream) {
-#define PA_DECODE_CASE(T, G)                                                     \
-  if (group == G) return launch_typed<T, G>(p, kmap, vmap, max_workers, max_pages_per_item, stream);
+                          int dtype, int group, int max_workers, int max_pages_per_item, bool q8,
+                          cudaStream_t stream) {
+#define PA_DECODE_CASE(T, G)                                                                    \
+  if (group == G)                                                                               \
+    return q8 ? launch_typed<T, G, true>(p, kmap, vmap, max_workers, max_pages_per_item, stream) \
+              : launch_typed<T, G, false>(p, kmap, vmap, max_workers, max_pages_per_item, stream);
   if (dtype == PA_BF16) {
     PA_DECODE_CASE(__nv_bfloat16, 1)
     PA_DECODE_CASE(__nv_bfloat16, 2)

@@ -34,7 +34,63 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
   }
 }
 
+// Quantising write into an int8 pool ("Модуль 04: KV-кэш и арифметика памяти",
+// section 5, KV8Cache.write): for each new token and KV head, and for K and V
+// separately, scale = max |x| / 127 + 1e-8 and code = clip(rint(x / scale),
+// -127, 127), every step in fp32 rounded to nearest (an IEEE division, ties of
+// rint to even), so the codes are exactly the ones the method defines.  One
+// warp per (token, KV head) row of 128 values: lane j owns values 4j .. 4j + 3,
+// the row maximum is a warp reduction, each lane stores its 4 codes as one
+// 32-bit word and lane 0 stores the scale.
+template <typename T>
+__global__ void __launch_bounds__(256) kv_write_q8_kernel(const WriteQ8Params p) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)p.num_tokens * p.num_kv_heads;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += wstride) {
+    const int t = (int)(r / p.num_kv_heads), h = (int)(r % p.num_kv_heads);
+    const int64_t slot = __ldg(p.slots + t);
+    if (slot < 0 || slot >= p.num_slots) {
+      if (h == 0 && lane == 0) set_error(p.err, PA_ERR_RANGE, t);
+      continue;
+    }
+    const int64_t si = ((slot >> 4) * p.num_kv_heads + h) * kBlock + (slot & 15);
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2 *>(pass == 0 ? p.k : p.v) + r * (kHeadDim / 4) + lane);
+      const float2 a = Pack<T>::to_f2(u.x), b = Pack<T>::to_f2(u.y);
+      float amax = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, off));
+      const float scale = __fadd_rn(__fdiv_rn(amax, 127.f), 1e-8f);
+      const float x[4] = {a.x, a.y, b.x, b.y};
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float c = fminf(fmaxf(rintf(__fdiv_rn(x[e], scale)), -127.f), 127.f);
+        word |= ((uint32_t)(int)c & 0xffu) << (8 * e);
+      }
+      int8_t *dst = pass == 0 ? p.k_cache : p.v_cache;
+      reinterpret_cast<uint32_t *>(dst + (slot * p.num_kv_heads + h) * kHeadDim)[lane] = word;
+      if (lane == 0) (pass == 0 ? p.k_scale : p.v_scale)[si] = scale;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_write_q8(const WriteQ8Params &p, int dtype, cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.num_tokens * p.num_kv_heads;
+  int64_t grid = (rows + 7) / 8;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  return dtype == PA_BF16 ? launch_pdl(kv_write_q8_kernel<__nv_bfloat16>, dim3((unsigned)grid), dim3(256), 0, stream, p)
+                          : launch_pdl(kv_write_q8_kernel<__half>, dim3((unsigned)grid), dim3(256), 0, stream, p);
+}
 
 cudaError_t launch_kv_write(const WriteParams &p, cudaStream_t stream) {
   const int64_t total = (int64_t)p.num_tokens * p.row_vecs;

@@ -100,6 +100,86 @@ bool pool_map(CUtensorMap *map, const pa_kv_pool *pool, void *base, bool whole_p
                            whole_page_box ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// int8 pool [P2 section 5]: codes as a 4-D tensor of bytes {dim, kv head,
+// slot, block}; the decode takes one page of one KV head per box (2 KB).
+pa_status check_pool_q8(const pa_kv_pool_q8 *pool) {
+  if (!pool || !pool->k_cache || !pool->v_cache || !pool->k_scale || !pool->v_scale) return PA_ERR_NULL;
+  if (pool->block_size != kBlock || pool->head_dim != kHeadDim) return PA_ERR_UNSUPPORTED;
+  if (pool->num_blocks < 1 || pool->num_kv_heads < 1 || pool->num_kv_heads > 256) return PA_ERR_SHAPE;
+  if (!aligned16(pool->k_cache) || !aligned16(pool->v_cache) || !aligned16(pool->k_scale) ||
+      !aligned16(pool->v_scale))
+    return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+bool pool_map_q8(CUtensorMap *map, const pa_kv_pool_q8 *pool, void *base) {
+  const uint64_t hkv = (uint64_t)pool->num_kv_heads;
+  const uint64_t dims[4] = {(uint64_t)kHeadDim, hkv, (uint64_t)kBlock, (uint64_t)pool->num_blocks};
+  const uint64_t strides[3] = {kHeadDim * 1ull, hkv * kHeadDim, kBlock * hkv * kHeadDim};
+  const uint32_t box[4] = {128u, 1, (uint32_t)kBlock, 1};
+  return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// The decode call on a 16-bit pool (pool16) or an int8 pool (pool8), after the
+// pool's own checks: every other argument is checked before any CUDA call.
+pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const pa_kv_pool_q8 *pool8,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len, float scale, void *out,
+                      void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const bool q8 = pool8 != nullptr;
+  const int num_kv_heads = q8 ? pool8->num_kv_heads : pool16->num_kv_heads;
+  const int num_blocks = q8 ? pool8->num_blocks : pool16->num_blocks;
+  if (num_seqs < 0) return PA_ERR_SHAPE;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  if (!workspace) return PA_ERR_WORKSPACE;
+  int group = 0;
+  pa_status st = check_group(num_q_heads, num_kv_heads, &group);
+  if (st != PA_OK) return st;
+  if (max_blocks_per_seq < 1 || max_context_len < 1 ||
+      (int64_t)max_context_len > (int64_t)max_blocks_per_seq * kBlock)
+    return PA_ERR_SHAPE;
+  if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || !aligned4(block_tables) ||
+      !aligned4(context_lens))
+    return PA_ERR_ALIGN;
+  if (workspace_bytes < decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads)) return PA_ERR_WORKSPACE;
+  DeviceState *d = nullptr;
+  if ((st = device_state(&d)) != PA_OK) return st;  // also readies the tensor-map encoder
+  CUtensorMap kmap, vmap;
+  const bool maps = q8 ? pool_map_q8(&kmap, pool8, pool8->k_cache) && pool_map_q8(&vmap, pool8, pool8->v_cache)
+                       : pool_map(&kmap, pool16, pool16->k_cache, true) &&
+                             pool_map(&vmap, pool16, pool16->v_cache, true);
+  if (!maps) return PA_ERR_CUDA;
+
+  DecodeParams p{};
+  if (!decode_workspace_carve(workspace, workspace_bytes, num_seqs, num_q_heads, num_kv_heads, p))
+    return PA_ERR_WORKSPACE;
+  p.q = q;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.err = d->err;
+  p.k_scale = q8 ? pool8->k_scale : nullptr;
+  p.v_scale = q8 ? pool8->v_scale : nullptr;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_kv_heads = num_kv_heads;
+  p.num_q_heads = num_q_heads;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  // Upper bound on the pages of the call; aim for at least 4 pages per warp.
+  const int64_t pages_hint = (int64_t)num_seqs * num_kv_heads * ((max_context_len + kBlock - 1) / kBlock);
+  int64_t workers = (pages_hint + 3) / 4;
+  if (workers > kDecodeMaxWorkers) workers = kDecodeMaxWorkers;
+  cudaError_t e = launch_decode(p, kmap, vmap, dtype, group, (int)workers, (max_context_len + kBlock - 1) / kBlock,
+                                q8, stream);
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 int sm_count() {
@@ -190,51 +270,49 @@ pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, const int3
                                void *workspace, size_t workspace_bytes, pa_stream_t stream) {
   pa_status st = check_pool(pool);
   if (st != PA_OK) return st;
-  if (num_seqs < 0) return PA_ERR_SHAPE;
-  if (num_seqs == 0) return PA_OK;
-  if (!q || !block_tables || !context_lens || !out) return PA_ERR_NULL;
-  if (!workspace) return PA_ERR_WORKSPACE;
-  int group = 0;
-  if ((st = check_group(num_q_heads, pool->num_kv_heads, &group)) != PA_OK) return st;
-  if (max_blocks_per_seq < 1 || max_context_len < 1 ||
-      (int64_t)max_context_len > (int64_t)max_blocks_per_seq * kBlock)
-    return PA_ERR_SHAPE;
-  if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
-  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || !aligned4(block_tables) ||
-      !aligned4(context_lens))
-    return PA_ERR_ALIGN;
-  if (workspace_bytes < decode_workspace_bytes(num_seqs, num_q_heads, pool->num_kv_heads))
-    return PA_ERR_WORKSPACE;
+  return decode_call(q, pool->dtype, pool, nullptr, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, max_context_len, scale, out, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_kv_cache_write_q8(const void *k, const void *v, int32_t dtype, const int64_t *slot_mapping,
+                               int32_t num_tokens, const pa_kv_pool_q8 *pool, pa_stream_t stream) {
+  pa_status st = check_pool_q8(pool);
+  if (st != PA_OK) return st;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping) return PA_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)) return PA_ERR_ALIGN;
   DeviceState *d = nullptr;
   if ((st = device_state(&d)) != PA_OK) return st;
-
-  DecodeParams p{};
-  if (!decode_workspace_carve(workspace, workspace_bytes, num_seqs, num_q_heads, pool->num_kv_heads, p))
-    return PA_ERR_WORKSPACE;
-  p.q = q;
-  p.block_tables = block_tables;
-  p.context_lens = context_lens;
-  p.out = out;
-  p.err = d->err;
-  p.max_blocks_per_seq = max_blocks_per_seq;
-  p.num_seqs = num_seqs;
+  WriteQ8Params p;
+  p.k = k;
+  p.v = v;
+  p.slots = slot_mapping;
+  p.k_cache = static_cast<int8_t *>(pool->k_cache);
+  p.v_cache = static_cast<int8_t *>(pool->v_cache);
+  p.k_scale = pool->k_scale;
+  p.v_scale = pool->v_scale;
+  p.num_slots = (int64_t)pool->num_blocks * kBlock;
+  p.num_tokens = num_tokens;
   p.num_kv_heads = pool->num_kv_heads;
-  p.num_q_heads = num_q_heads;
-  p.num_blocks = pool->num_blocks;
-  p.scale_log2 = scale * 1.4426950408889634f;
-
-  CUtensorMap kmap, vmap;
-  if (!pool_map(&kmap, pool, pool->k_cache, true) || !pool_map(&vmap, pool, pool->v_cache, true))
-    return PA_ERR_CUDA;
-
-  // Upper bound on the pages of the call; aim for at least 4 pages per warp.
-  const int64_t pages_hint = (int64_t)num_seqs * pool->num_kv_heads * ((max_context_len + kBlock - 1) / kBlock);
-  int64_t workers = (pages_hint + 3) / 4;
-  if (workers > kDecodeMaxWorkers) workers = kDecodeMaxWorkers;
-  cudaError_t e = launch_decode(p, kmap, vmap, pool->dtype, group, (int)workers,
-                                (max_context_len + kBlock - 1) / kBlock, static_cast<cudaStream_t>(stream));
+  p.err = d->err;
+  cudaError_t e = launch_kv_write_q8(p, dtype, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_paged_attn_decode_q8(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_context_len, float scale, void *out, void *workspace,
+                                  size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = check_pool_q8(pool);
+  if (st != PA_OK) return st;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  return decode_call(q, dtype, nullptr, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, max_context_len, scale, out, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream));
 }
 
 pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts, const int32_t *chunk_lens,

@@ -166,6 +166,16 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 }
 
 // 4-D tiled load into shared memory, completing on `bar` (transaction bytes).
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar` (transaction bytes).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
                                             int c1, int c2, int c3) {
   asm volatile(
@@ -230,6 +240,20 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---- signed 8-bit codes → fp32 ------------------------------------------------
+// Codes 2i and 2i + 1 of the word w, exactly: with the bias 128 a code c is the
+// unsigned byte c + 128, which placed in the low mantissa byte of 2^23 gives
+// the float 2^23 + c + 128; subtracting 2^23 + 128 leaves c.  (A byte permute
+// and a packed add, no conversion unit.)
+template <int I>
+__device__ __forceinline__ float2 s8x2_to_f2(uint32_t w) {
+  static_assert(I == 0 || I == 1, "pair index");
+  const uint32_t u = w ^ 0x80808080u;
+  const float lo = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u + 2 * I));
+  const float hi = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541u + 2 * I));
+  return __fadd2_rn(make_float2(lo, hi), make_float2(-8388736.f, -8388736.f));
 }
 
 // ---- 16-bit → fp32 conversion of packed pairs --------------------------------

@@ -32,6 +32,23 @@ struct WriteParams {
 };
 cudaError_t launch_kv_write(const WriteParams &p, cudaStream_t stream);
 
+// Quantising write into an int8 pool: one fp32 scale per (token, KV head) for
+// K and for V, codes int8 [num_blocks][16][Hkv][128], scales [num_blocks][Hkv][16].
+struct WriteQ8Params {
+  const void *k;             // [T][Hkv][128] in `dtype`
+  const void *v;
+  const int64_t *slots;
+  int8_t *k_cache;
+  int8_t *v_cache;
+  float *k_scale;
+  float *v_scale;
+  int64_t num_slots;
+  int32_t num_tokens;
+  int32_t num_kv_heads;
+  int *err;
+};
+cudaError_t launch_kv_write_q8(const WriteQ8Params &p, int dtype, cudaStream_t stream);
+
 // ---- decode (split-K over a balanced page range per warp) -----------------------
 constexpr int kDecodeWarps = 4;         // warps per CTA; each warp is an independent worker
 constexpr int kDecodeMaxWorkers = 8192; // upper bound on workers (warps) per launch
@@ -46,6 +63,8 @@ struct DecodeParams {
   float *ws_ml;              // workspace: (m, l) per partial slot and head of the group
   float *ws_o;               // workspace: o[128] per partial slot and head of the group
   int *err;
+  const float *k_scale;      // int8 pools only: [num_blocks][Hkv][16] scales of K and V
+  const float *v_scale;
   int32_t max_blocks_per_seq;
   int32_t num_seqs;
   int32_t num_kv_heads;
@@ -62,9 +81,11 @@ struct DecodeLaunch {
 
 // Plans and launches the decode: one CTA per (sequence, KV head) item when the
 // items are few, else the split and combine kernels.  `group` = Hq / Hkv;
-// max_pages_per_item bounds each item's pages (from the host-side max length).
+// max_pages_per_item bounds each item's pages (from the host-side max length);
+// q8: the pool holds int8 codes with per-token scales (p.k_scale, p.v_scale).
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          int dtype, int group, int max_workers, int max_pages_per_item, cudaStream_t stream);
+                          int dtype, int group, int max_workers, int max_pages_per_item, bool q8,
+                          cudaStream_t stream);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads);
 // CTAs per item of the one-launch decode (1 or 2), or 0 when the split path runs.
 int decode_item_ctas(int items, int max_pages_per_item);

@@ -47,7 +47,7 @@ def test_only_c_entry_points_are_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 1
+    assert lib.pa_abi_version() == 2
     for code in range(0, -10, -1):
         assert lib.pa_status_string(code).decode().startswith(pa.STATUS[code])
 
@@ -130,3 +130,45 @@ def test_workspace_size_is_pure_host_and_monotone(lib):
     assert 0 < a < b
     assert lib.pa_decode_workspace_bytes(8, 12, 8, 1024) == 0
     assert lib.pa_decode_workspace_bytes(-1, 16, 8, 1024) == 0
+
+
+def _pool_q8(**kw):
+    f = dict(k_cache=P, v_cache=P + 4096, k_scale=P + 8192, v_scale=P + 12288, num_blocks=64, block_size=16,
+             num_kv_heads=8, head_dim=128)
+    f.update(kw)
+    return pa.KVPoolQ8(**f)
+
+
+def test_write_q8_rejects_bad_arguments(lib):
+    call = lambda pool=None, **kw: lib.pa_kv_cache_write_q8(
+        kw.get("k", P), kw.get("v", P), kw.get("dtype", 0), kw.get("slots", P), kw.get("n", 4),
+        ctypes.byref(pool or _pool_q8()), None)
+    assert call(n=0) == 0
+    assert call(n=-1) == -2
+    assert call(k=0) == -1
+    assert call(pool=_pool_q8(k_scale=0)) == -1
+    assert call(dtype=2) == -3
+    assert call(pool=_pool_q8(block_size=32)) == -4
+    assert call(pool=_pool_q8(head_dim=64)) == -4
+    assert call(pool=_pool_q8(v_scale=P + 4)) == -9
+    assert call(slots=P + 4) == -9
+    assert call(k=P + 2) == -9
+
+
+def test_decode_q8_rejects_bad_arguments(lib):
+    ws = lib.pa_decode_workspace_bytes(4, 16, 8, 256)
+    call = lambda pool=None, **kw: lib.pa_paged_attn_decode_q8(
+        kw.get("q", P), kw.get("dtype", 1), ctypes.byref(pool or _pool_q8()), kw.get("bt", P), kw.get("mb", 16),
+        kw.get("ctx", P), kw.get("S", 4), kw.get("hq", 16), kw.get("mcl", 256), kw.get("scale", 0.088),
+        kw.get("out", P), kw.get("ws", P), kw.get("wsb", ws), None)
+    assert call(S=0) == 0
+    assert call(S=-1) == -2
+    assert call(q=0) == -1
+    assert call(dtype=5) == -3
+    assert call(pool=_pool_q8(v_cache=0)) == -1
+    assert call(ws=0) == -5
+    assert call(wsb=ws - 1) == -5
+    assert call(hq=24) == -4
+    assert call(mcl=300) == -2
+    assert call(scale=float("inf")) == -2
+    assert call(out=P + 2) == -9
