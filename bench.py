@@ -57,6 +57,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pools", type=int, default=0,
                     help="distinct layer pools held on the device (0 = the workload's default)")
+    ap.add_argument("--kv", choices=["16bit", "int8"], default="16bit",
+                    help="decode workloads: the workload's 16-bit pool, or an int8 pool (codes + one fp32 scale "
+                         "per token and KV head) holding the same tokens quantised")
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
                     help="2 = the Qwen3-0.6B 28-layer decode step (default); 3, 4, 5 = the mixed prefill "
                          "step, the Qwen3-8B decode and the prefix-shared long tail (diagnostic lines)")
@@ -237,6 +240,49 @@ class DecodeStep:
             self.decode(l)
 
 
+class DecodeStepQ8(DecodeStep):
+    """The same decode step over int8 pools ("Модуль 04: KV-кэш и арифметика
+    памяти", section 5): every cached token of each 16-bit layer pool is
+    quantised once into an int8 pool by the library's own write; each layer of
+    the step then quantises the new tokens into their slots and decodes."""
+
+    def __init__(self, device, workload: int = 2, pools: int = 0):
+        import numpy as np
+        import torch
+        super().__init__(device, workload, pools)
+        c = self.case
+        bt = c.block_tables.cpu().numpy()
+        slots = []
+        for s_, n in enumerate(c.context_lens.cpu().numpy()):
+            j = np.arange(int(n) - 1)                      # cached positions; the new token is written per step
+            slots.append(bt[s_, j // 16].astype(np.int64) * 16 + j % 16)
+        sl = torch.from_numpy(np.unique(np.concatenate(slots))).to(device)
+        self.q8 = []
+        for i in range(c.n_layers):
+            pool = self.pa.alloc_pool_q8(c.num_blocks, c.hkv, device)
+            rows_k = c.k_cache[i].view(-1, c.hkv, 128)[sl].contiguous()
+            rows_v = c.v_cache[i].view(-1, c.hkv, 128)[sl].contiguous()
+            self.pa.kv_cache_write_q8(rows_k, rows_v, sl, *pool)
+            self.q8.append(pool)
+            del rows_k, rows_v
+        torch.cuda.synchronize()
+        per_token = c.hkv * (2 * 128 + 2 * 4)              # codes of K and V, one fp32 scale each
+        self.decode_bytes_layer = self.decode_bytes_layer // (2 * c.hkv * 128 * 2) * per_token
+        T = c.k_new[0].shape[0]
+        self.write_bytes_layer = T * c.hkv * (2 * 128 * 2 + per_token // c.hkv)   # 16-bit rows in, codes out
+        self.step_bytes = self.L * (self.decode_bytes_layer + self.write_bytes_layer)
+        self.pool_bytes = sum(t.numel() * t.element_size() for t in self.q8[0])
+
+    def write(self, l):
+        c, i = self.case, l % self.case.n_layers
+        self.pa.kv_cache_write_q8(c.k_new[i], c.v_new[i], c.slot_mapping, *self.q8[i])
+
+    def decode(self, l):
+        c, i = self.case, l % self.case.n_layers
+        self.pa.paged_attn_decode_q8(c.q[i], *self.q8[i], c.block_tables, c.context_lens, c.scale,
+                                     out=self.out[i], workspace=self.ws, max_context_len=c.max_context_len)
+
+
 class MixedStep:
     """The Qwen3-0.6B mixed chunked-prefill step (budget 2048): per layer,
     kv_cache_write of 2048 new tokens, prefill of 3 chunks of 512 (prefixes 0,
@@ -358,13 +404,20 @@ def cpu_baseline(step: DecodeStep, seconds: float):
     c = step.case
     threads = os.cpu_count() or 1
     bt, ctx = c.block_tables.cpu().numpy(), c.context_lens.cpu().numpy()
+    odt = oracle.BF16 if c.dtype == "bf16" else oracle.F16
+    q8 = getattr(step, "q8", None)
     done_bytes, t_total, layers = 0, 0.0, 0
     for l in range(c.n_layers):
-        kh = c.k_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
-        vh = c.v_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
         qh = c.q[l].cpu().view(torch.int16).numpy().view(np.uint16)
-        t0 = time.perf_counter()
-        oracle.paged_attn_decode(qh, kh, vh, bt, ctx, c.scale, oracle.F16, num_threads=threads)
+        if q8 is not None:
+            host = [t.cpu().numpy() for t in q8[l]]
+            t0 = time.perf_counter()
+            oracle.paged_attn_decode_q8(qh, *host, bt, ctx, c.scale, odt, num_threads=threads)
+        else:
+            kh = c.k_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
+            vh = c.v_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
+            t0 = time.perf_counter()
+            oracle.paged_attn_decode(qh, kh, vh, bt, ctx, c.scale, odt, num_threads=threads)
         t_total += time.perf_counter() - t0
         done_bytes += step.decode_bytes_layer
         layers += 1
@@ -393,7 +446,7 @@ def run_ours(args):
     if args.workload == 3:
         return run_mixed(args, dev, pa)
 
-    step = DecodeStep(dev, args.workload, args.pools)
+    step = (DecodeStepQ8 if args.kv == "int8" else DecodeStep)(dev, args.workload, args.pools)
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_dec = graph_of(step.run_decode_only, 1, stream)
@@ -421,12 +474,15 @@ def run_ours(args):
     e2e_ms = reduce_max(e2e_ms, dev)
     _device_error_check(pa)
 
-    pool_mib = 2 * step.case.k_cache[0].numel() * 2 / 2**20
+    q8 = isinstance(step, DecodeStepQ8)
+    pool_mib = (step.pool_bytes if q8 else 2 * step.case.k_cache[0].numel() * 2) / 2**20
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": step.dtype, "data": "synthetic",
-        "config": {"workload": step.desc, "global_batch": step.S * world, "seq_len": step.case.max_context_len,
+        "vs_baseline": None, "dtype": "int8" if q8 else step.dtype, "data": "synthetic",
+        "config": {"workload": step.desc + (", int8 KV pool (codes + one fp32 scale per token and KV head), "
+                                            f"{step.dtype} q and out" if q8 else ""),
+                   "global_batch": step.S * world, "seq_len": step.case.max_context_len,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({step.case.n_layers} distinct pools of {pool_mib:.0f} MiB "
                          f"cycled over {step.L} calls per step)",
@@ -438,11 +494,11 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "peak_kind": peak_kind,
-                     "kernel": "paged_attn_decode per layer (" + ("one cluster per sequence and KV head"
-                                                                  if step.decode_kernels == 1
-                                                                  else "split + combine") + ")",
+                     "kernel": ("paged_attn_decode_q8" if q8 else "paged_attn_decode") + " per layer ("
+                               + ("one cluster per sequence and KV head" if step.decode_kernels == 1
+                                  else "split + combine") + ")",
                      "bytes_per_launch": step.decode_bytes_layer, "launch_ms": round(dec_launch_ms, 5),
-                     "traffic": committed_traffic("decode.cu", f"decode_workload{args.workload}.md")},
+                     "traffic": committed_traffic("decode.cu", f"decode{'_q8' if q8 else ''}_workload{args.workload}.md")},
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
