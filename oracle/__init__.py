@@ -72,6 +72,12 @@ def open_library(path: str):
     lib.oracle_paged_attn_prefill.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P,
                                               i32, P, i32, i32, f64, P, i32]
     lib.oracle_paged_attn_prefill.restype = ctypes.c_int
+    lib.oracle_paged_attn_decode_window.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, i32, P,
+                                                    i32, i32, f64, i32, P, i32]
+    lib.oracle_paged_attn_decode_window.restype = ctypes.c_int
+    lib.oracle_paged_attn_prefill_window.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P,
+                                                     i32, P, i32, i32, f64, i32, P, i32]
+    lib.oracle_paged_attn_prefill_window.restype = ctypes.c_int
     lib.oracle_kv_cache_write_q8.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P, i32, P, i64]
     lib.oracle_kv_cache_write_q8.restype = i64
     lib.oracle_gather_head_q8.argtypes = [P, P, P, P, i64, i32, i32, i32, P, i32, i32, P, P]
@@ -207,6 +213,47 @@ def paged_attn_prefill(q, k_cache, v_cache, chunk_starts, chunk_lens, block_tabl
     rc = _load().oracle_paged_attn_prefill(_ptr(qb), dtype, _ptr(kc), _ptr(vc), nb, bs, hkv, d,
                                            _ptr(cs), _ptr(cl), _ptr(bt), bt.shape[1], _ptr(ctx),
                                            cs.shape[0], hq, float(scale), _ptr(out), num_threads)
+    if rc != 0:
+        raise ValueError(f"oracle prefill rejected its inputs (code {rc})")
+    return out
+
+
+def paged_attn_decode_window(q, k_cache, v_cache, block_tables, context_lens, scale: float, window: int,
+                             dtype: int, num_threads: int = 0) -> np.ndarray:
+    """fp64 decode attention with a sliding window of ``window`` keys ("Модуль 04:
+    KV-кэш и арифметика памяти", sections 4 and 5.2): sequence s sees positions
+    max(0, ctx - window) .. ctx - 1; blocks wholly before them are never read."""
+    qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+    nb, bs, hkv, d = kc.shape
+    s, hq, dq = qb.shape
+    assert dq == d
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros((s, hq, d), np.float64)
+    rc = _load().oracle_paged_attn_decode_window(_ptr(qb), dtype, _ptr(kc), _ptr(vc), nb, bs, hkv, d,
+                                                 _ptr(bt), bt.shape[1], _ptr(ctx), s, hq, float(scale),
+                                                 int(window), _ptr(out), num_threads)
+    if rc != 0:
+        raise ValueError(f"oracle decode rejected its inputs (code {rc})")
+    return out
+
+
+def paged_attn_prefill_window(q, k_cache, v_cache, chunk_starts, chunk_lens, block_tables, context_lens,
+                              scale: float, window: int, dtype: int, num_threads: int = 0) -> np.ndarray:
+    """fp64 causal chunked prefill with a sliding window: the row at position p
+    sees keys max(0, p - window + 1) .. p (window 0: no window)."""
+    qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+    nb, bs, hkv, d = kc.shape
+    rows, hq, dq = qb.shape
+    cs = np.ascontiguousarray(chunk_starts, dtype=np.int32)
+    cl = np.ascontiguousarray(chunk_lens, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros((rows, hq, d), np.float64)
+    rc = _load().oracle_paged_attn_prefill_window(_ptr(qb), dtype, _ptr(kc), _ptr(vc), nb, bs, hkv, d,
+                                                  _ptr(cs), _ptr(cl), _ptr(bt), bt.shape[1], _ptr(ctx),
+                                                  cs.shape[0], hq, float(scale), int(window), _ptr(out),
+                                                  num_threads)
     if rc != 0:
         raise ValueError(f"oracle prefill rejected its inputs (code {rc})")
     return out

@@ -27,6 +27,11 @@
  * index, the in-block slot the next one.  A flat slot number is
  * block * block_size + offset.
  *
+ * Sliding window [P2 section 4 (ring buffer of capacity W) and section 5.2]:
+ * with a window W > 0 the query at absolute position p sees only the keys at
+ * positions max(0, p - W + 1) .. p (the mask stays on absolute positions);
+ * blocks wholly before that range are never read.
+ *
  * The int8 pool [P2 section 5, KV8Cache]: K and V codes int8 in the same
  * layout, one fp32 scale per (token, KV head) for K and one for V.  The
  * quantising write and the dequantising read follow the pages' fp32 steps
@@ -119,11 +124,27 @@ int64_t oracle_kv_cache_write(uint16_t *k_cache, uint16_t *v_cache,
  * offset j % block_size.  Writes upto*head_dim doubles to k_out and v_out.
  * Returns 0, or -1 if a needed block id is outside [0, num_blocks).
  */
+static int gather_range(const uint16_t *k_cache, const uint16_t *v_cache, int dtype, int64_t num_blocks,
+                        int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                        const int32_t *block_table_row, int32_t kv_head, int32_t from, int32_t upto,
+                        double *k_out, double *v_out);
+
 int oracle_gather_head(const uint16_t *k_cache, const uint16_t *v_cache, int dtype,
                        int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                        int32_t head_dim, const int32_t *block_table_row,
                        int32_t kv_head, int32_t upto, double *k_out, double *v_out) {
-  for (int32_t j = 0; j < upto; ++j) {
+  return gather_range(k_cache, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, block_table_row,
+                      kv_head, 0, upto, k_out, v_out);
+}
+
+/* Rows of positions [from, upto), written from row 0 of k_out / v_out. */
+static int gather_range(const uint16_t *k_cache, const uint16_t *v_cache, int dtype, int64_t num_blocks,
+                        int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                        const int32_t *block_table_row, int32_t kv_head, int32_t from, int32_t upto,
+                        double *k_out, double *v_out) {
+  k_out -= (int64_t)from * head_dim;
+  v_out -= (int64_t)from * head_dim;
+  for (int32_t j = from; j < upto; ++j) {
     int32_t entry = j / block_size, offset = j % block_size;
     int64_t block = block_table_row[entry];
     if (block < 0 || block >= num_blocks) return -1;
@@ -191,11 +212,26 @@ int64_t oracle_kv_cache_write_q8(int8_t *k_cache, int8_t *v_cache, float *k_scal
 /* Read [KV8Cache.read]: rows of positions [0, upto) of one KV head, each value
  * code * scale as an fp32 product, widened to double.  Returns 0 or -1 (block
  * id outside the pool). */
+static int gather_range_q8(const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
+                           const float *v_scale, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                           int32_t head_dim, const int32_t *block_table_row, int32_t kv_head, int32_t from,
+                           int32_t upto, double *k_out, double *v_out);
+
 int oracle_gather_head_q8(const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
                           const float *v_scale, int64_t num_blocks, int32_t block_size,
                           int32_t num_kv_heads, int32_t head_dim, const int32_t *block_table_row,
                           int32_t kv_head, int32_t upto, double *k_out, double *v_out) {
-  for (int32_t j = 0; j < upto; ++j) {
+  return gather_range_q8(k_cache, v_cache, k_scale, v_scale, num_blocks, block_size, num_kv_heads, head_dim,
+                         block_table_row, kv_head, 0, upto, k_out, v_out);
+}
+
+static int gather_range_q8(const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
+                           const float *v_scale, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                           int32_t head_dim, const int32_t *block_table_row, int32_t kv_head, int32_t from,
+                           int32_t upto, double *k_out, double *v_out) {
+  k_out -= (int64_t)from * head_dim;
+  v_out -= (int64_t)from * head_dim;
+  for (int32_t j = from; j < upto; ++j) {
     const int32_t entry = j / block_size;
     const int32_t offset = j % block_size;
     int64_t block = block_table_row[entry];
@@ -266,6 +302,8 @@ typedef struct {
   /* int8 pool instead of k_cache / v_cache when k8 is not NULL */
   const int8_t *k8, *v8;
   const float *k_scale, *v_scale;
+  /* sliding window W (0: none): row at position p sees keys max(0, p - W + 1) .. p */
+  int32_t window;
 } problem_t;
 
 static void run_item(problem_t *P, int32_t g, int32_t h, double *kk, double *vv,
@@ -274,11 +312,13 @@ static void run_item(problem_t *P, int32_t g, int32_t h, double *kk, double *vv,
   const int32_t G = P->num_q_heads / P->num_kv_heads;
   const int32_t nrows = P->group_nrows[g], row0 = P->group_row0[g], pos0 = P->group_pos0[g];
   const int32_t nkeys = pos0 + nrows;   /* keys the last row of the group sees */
+  /* first key any row of the group sees (the first row's window start) */
+  const int32_t glo = (P->window > 0 && pos0 - P->window + 1 > 0) ? pos0 - P->window + 1 : 0;
   const int32_t *bt_row = P->block_tables + (int64_t)g * P->max_blocks_per_seq;
-  const int grc = P->k8 ? oracle_gather_head_q8(P->k8, P->v8, P->k_scale, P->v_scale, P->num_blocks,
-                                                P->block_size, P->num_kv_heads, d, bt_row, h, nkeys, kk, vv)
-                        : oracle_gather_head(P->k_cache, P->v_cache, P->dtype, P->num_blocks, P->block_size,
-                                             P->num_kv_heads, d, bt_row, h, nkeys, kk, vv);
+  const int grc = P->k8 ? gather_range_q8(P->k8, P->v8, P->k_scale, P->v_scale, P->num_blocks, P->block_size,
+                                          P->num_kv_heads, d, bt_row, h, glo, nkeys, kk, vv)
+                        : gather_range(P->k_cache, P->v_cache, P->dtype, P->num_blocks, P->block_size,
+                                       P->num_kv_heads, d, bt_row, h, glo, nkeys, kk, vv);
   if (grc != 0) {
     pthread_mutex_lock(&P->lock);
     P->error = -1;
@@ -291,7 +331,10 @@ static void run_item(problem_t *P, int32_t g, int32_t h, double *kk, double *vv,
     for (int32_t i = 0; i < nrows; ++i) {
       const int64_t base = ((int64_t)(row0 + i) * P->num_q_heads + qh) * d;
       for (int32_t x = 0; x < d; ++x) qd[x] = widen(P->q[base + x], P->dtype);
-      attend_row(qd, kk, vv, pos0 + i + 1, d, P->scale, s, P->out + base);
+      const int32_t p = pos0 + i;
+      const int32_t lo = (P->window > 0 && p - P->window + 1 > 0) ? p - P->window + 1 : 0;
+      attend_row(qd, kk + (int64_t)(lo - glo) * d, vv + (int64_t)(lo - glo) * d, p - lo + 1, d, P->scale, s,
+                 P->out + base);
     }
   }
 }
@@ -372,6 +415,21 @@ int oracle_paged_attn_decode(const uint16_t *q, int32_t dtype,
   return decode_problem(&P, context_lens, num_seqs, num_threads);
 }
 
+/* Decode with a sliding window of W keys [P2 sections 4 and 5.2]: sequence s
+ * sees positions max(0, context_lens[s] - W) .. context_lens[s] - 1. */
+int oracle_paged_attn_decode_window(const uint16_t *q, int32_t dtype, const uint16_t *k_cache,
+                                    const uint16_t *v_cache, int64_t num_blocks, int32_t block_size,
+                                    int32_t num_kv_heads, int32_t head_dim, const int32_t *block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                                    int32_t num_q_heads, double scale, int32_t window, double *out,
+                                    int32_t num_threads) {
+  if (window < 1) return -4;
+  problem_t P = {q, dtype, k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim,
+                 block_tables, max_blocks_per_seq, num_q_heads, scale, out};
+  P.window = window;
+  return decode_problem(&P, context_lens, num_seqs, num_threads);
+}
+
 /* The same decode on the int8 pool [P2 section 5]: keys and values are the
  * dequantised fp32 numbers of KV8Cache.read. */
 int oracle_paged_attn_decode_q8(const uint16_t *q, int32_t dtype, const int8_t *k_cache,
@@ -428,6 +486,14 @@ static int decode_problem(problem_t *P, const int32_t *context_lens, int32_t num
  * Returns 0, -1 for a block id out of range, -3 for a bad head split, -4 for
  * inconsistent chunk metadata.
  */
+int oracle_paged_attn_prefill_window(const uint16_t *q, int32_t dtype, const uint16_t *k_cache,
+                                     const uint16_t *v_cache, int64_t num_blocks, int32_t block_size,
+                                     int32_t num_kv_heads, int32_t head_dim, const int32_t *chunk_starts,
+                                     const int32_t *chunk_lens, const int32_t *block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_chunks,
+                                     int32_t num_q_heads, double scale, int32_t window, double *out,
+                                     int32_t num_threads);
+
 int oracle_paged_attn_prefill(const uint16_t *q, int32_t dtype,
                               const uint16_t *k_cache, const uint16_t *v_cache,
                               int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
@@ -436,6 +502,22 @@ int oracle_paged_attn_prefill(const uint16_t *q, int32_t dtype,
                               int32_t max_blocks_per_seq, const int32_t *context_lens,
                               int32_t num_chunks, int32_t num_q_heads, double scale,
                               double *out, int32_t num_threads) {
+  return oracle_paged_attn_prefill_window(q, dtype, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
+                                          head_dim, chunk_starts, chunk_lens, block_tables, max_blocks_per_seq,
+                                          context_lens, num_chunks, num_q_heads, scale, 0, out, num_threads);
+}
+
+/* Chunked prefill with a sliding window of W keys (W = 0: none) [P2 sections
+ * 4 and 5.2]: row i of chunk c, at position p = chunk_starts[c] + i, sees keys
+ * max(0, p - W + 1) .. p. */
+int oracle_paged_attn_prefill_window(const uint16_t *q, int32_t dtype, const uint16_t *k_cache,
+                                     const uint16_t *v_cache, int64_t num_blocks, int32_t block_size,
+                                     int32_t num_kv_heads, int32_t head_dim, const int32_t *chunk_starts,
+                                     const int32_t *chunk_lens, const int32_t *block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_chunks,
+                                     int32_t num_q_heads, double scale, int32_t window, double *out,
+                                     int32_t num_threads) {
+  if (window < 0) return -4;
   int32_t *row0 = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_chunks > 0 ? num_chunks : 1));
   int rc = 0;
   int32_t acc = 0;
@@ -451,6 +533,7 @@ int oracle_paged_attn_prefill(const uint16_t *q, int32_t dtype,
     problem_t P = {q, dtype, k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim,
                    block_tables, max_blocks_per_seq, num_q_heads, scale, out,
                    num_chunks, row0, chunk_lens, chunk_starts};
+    P.window = window;
     rc = run_problem(&P, num_threads);
   }
   free(row0);

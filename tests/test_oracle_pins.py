@@ -409,7 +409,7 @@ def _battery():
 MUTATIONS = {
     "gqa-map-interleaved": ("for (int32_t qh = h * G; qh < (h + 1) * G; ++qh)",
                             "for (int32_t qh = h; qh < P->num_q_heads; qh += P->num_kv_heads)"),
-    "causal-excludes-self": ("attend_row(qd, kk, vv, pos0 + i + 1,", "attend_row(qd, kk, vv, pos0 + i + (i > 0),"),
+    "causal-excludes-self": ("p - lo + 1, d, P->scale, s,", "p - lo + (i == 0), d, P->scale, s,"),
     "scale-dropped": ("s[j] = scale * dot;", "s[j] = dot;"),
     "values-from-keys": ("out[x] += p * vv[(int64_t)j * d + x];", "out[x] += p * kk[(int64_t)j * d + x];"),
     "slot-offset-shifted": ("int32_t entry = j / block_size, offset = j % block_size;",
