@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 2
+#define PA_ABI_VERSION 3
 #define PA_HEAD_DIM 128
 #define PA_BLOCK_SIZE 16
 #define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
@@ -241,6 +241,43 @@ PA_API pa_status pa_paged_attn_decode_q8(const void *q, int32_t dtype, const pa_
                                          const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                                          int32_t max_context_len, float scale, void *out, void *workspace,
                                          size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * ---- sliding window [P2 section 4 (a ring of capacity W keeps the last W
+ * tokens; the mask stays on absolute positions) and section 5.2 (window
+ * attention)] -------------------------------------------------------------------
+ * With window W >= 1 a query at absolute position p attends only to keys
+ * max(0, p - W + 1) .. p; window 0 means no window (the plain calls).  Blocks
+ * wholly before a sequence's (or chunk's first query's) window are never read:
+ * their block-table entries may already hold -1 or point at reused blocks.
+ */
+
+/*
+ * paged_attn_decode_window — pa_paged_attn_decode with a sliding window of
+ * `window` keys: sequence s attends to j in [max(0, context_lens[s] - window),
+ * context_lens[s]).  Arguments, workspace and errors as pa_paged_attn_decode;
+ * window < 0 returns PA_ERR_SHAPE.
+ */
+PA_API pa_status pa_paged_attn_decode_window(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                             int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                                             float scale, int32_t window, void *out, void *workspace,
+                                             size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * paged_attn_prefill_chunk_window — pa_paged_attn_prefill_chunk with a
+ * sliding window of `window` keys: the query at position chunk_starts[c] + i
+ * attends to keys max(0, chunk_starts[c] + i - window + 1) ..
+ * chunk_starts[c] + i.  Arguments and errors as pa_paged_attn_prefill_chunk;
+ * window < 0 returns PA_ERR_SHAPE.
+ */
+PA_API pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t *chunk_starts,
+                                                    const int32_t *chunk_lens, const pa_kv_pool *pool,
+                                                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                    const int32_t *context_lens, int32_t num_chunks,
+                                                    int32_t num_q_heads, int32_t total_q_tokens,
+                                                    int32_t max_chunk_len, float scale, int32_t window,
+                                                    void *out, pa_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's error

@@ -36,7 +36,8 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_decode",
            "pa_paged_attn_prefill_chunk", "pa_get_device_error", "pa_status_string",
            "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc",
-           "pa_decode_kernel_launches", "pa_kv_cache_write_q8", "pa_paged_attn_decode_q8")
+           "pa_decode_kernel_launches", "pa_kv_cache_write_q8", "pa_paged_attn_decode_q8",
+           "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window")
 
 
 class PagedAttnError(RuntimeError):
@@ -91,11 +92,17 @@ def load_library(path: str = LIB_PATH):
         lib.pa_paged_attn_decode.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P,
                                              ctypes.c_size_t, P]
         lib.pa_paged_attn_decode.restype = i32
+        lib.pa_paged_attn_decode_window.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, i32, P,
+                                                    P, ctypes.c_size_t, P]
+        lib.pa_paged_attn_decode_window.restype = i32
         lib.pa_paged_attn_decode_noalloc.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P]
         lib.pa_paged_attn_decode_noalloc.restype = i32
         lib.pa_paged_attn_prefill_chunk.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
                                                     ctypes.c_float, P, P]
         lib.pa_paged_attn_prefill_chunk.restype = i32
+        lib.pa_paged_attn_prefill_chunk_window.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
+                                                           ctypes.c_float, i32, P, P]
+        lib.pa_paged_attn_prefill_chunk_window.restype = i32
         lib.pa_get_device_error.argtypes = [P, ctypes.POINTER(i32)]
         lib.pa_get_device_error.restype = i32
         lib.pa_status_string.argtypes = [i32]
@@ -256,6 +263,22 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
 
     ``max_context_len`` is a host-side bound on ``context_lens`` (no device
     sync is made to find it); it defaults to the block table's capacity."""
+    return _decode(q, k_cache, v_cache, block_tables, context_lens, scale, 0, out, workspace, max_context_len,
+                   stream)
+
+
+def paged_attn_decode_window(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, window: int,
+                             out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                             max_context_len: Optional[int] = None, stream=None) -> torch.Tensor:
+    """Decode attention over the last ``window`` keys of each sequence (window
+    0: all of them); otherwise as :func:`paged_attn_decode`."""
+    return _decode(q, k_cache, v_cache, block_tables, context_lens, scale, int(window), out, workspace,
+                   max_context_len, stream)
+
+
+def _decode(q, k_cache, v_cache, block_tables, context_lens, scale, window, out, workspace, max_context_len,
+            stream):
     pool = make_pool(k_cache, v_cache)
     _need(q, "q", k_cache.dtype)
     _need(block_tables, "block_tables", torch.int32)
@@ -272,10 +295,15 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         workspace = alloc_decode_workspace(S, hq, pool.num_kv_heads, mcl, q.device)
     _need(workspace, "workspace")
     lib = load_library()
-    _check(lib.pa_paged_attn_decode(q.data_ptr(), ctypes.byref(pool), block_tables.data_ptr(), mb,
-                                    context_lens.data_ptr(), S, hq, mcl, float(scale), out.data_ptr(),
-                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                    _stream(stream)), "pa_paged_attn_decode")
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    if window:
+        _check(lib.pa_paged_attn_decode_window(q.data_ptr(), ctypes.byref(pool), block_tables.data_ptr(), mb,
+                                               context_lens.data_ptr(), S, hq, mcl, float(scale), window,
+                                               out.data_ptr(), *ws), "pa_paged_attn_decode_window")
+    else:
+        _check(lib.pa_paged_attn_decode(q.data_ptr(), ctypes.byref(pool), block_tables.data_ptr(), mb,
+                                        context_lens.data_ptr(), S, hq, mcl, float(scale), out.data_ptr(), *ws),
+               "pa_paged_attn_decode")
     return out
 
 
@@ -310,6 +338,23 @@ def paged_attn_prefill_chunk(q: torch.Tensor, chunk_starts: torch.Tensor, chunk_
                              context_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
                              max_chunk_len: int = 512, stream=None) -> torch.Tensor:
     """Causal chunked-prefill attention: q [sum(chunk_lens), Hq, 128] → out (pool dtype)."""
+    return _prefill(q, chunk_starts, chunk_lens, k_cache, v_cache, block_tables, context_lens, scale, 0, out,
+                    max_chunk_len, stream)
+
+
+def paged_attn_prefill_chunk_window(q: torch.Tensor, chunk_starts: torch.Tensor, chunk_lens: torch.Tensor,
+                                    k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                    context_lens: torch.Tensor, scale: float, window: int,
+                                    out: Optional[torch.Tensor] = None, max_chunk_len: int = 512,
+                                    stream=None) -> torch.Tensor:
+    """Chunked prefill where the query at position p sees keys p - window + 1 .. p
+    (window 0: all earlier keys); otherwise as :func:`paged_attn_prefill_chunk`."""
+    return _prefill(q, chunk_starts, chunk_lens, k_cache, v_cache, block_tables, context_lens, scale, int(window),
+                    out, max_chunk_len, stream)
+
+
+def _prefill(q, chunk_starts, chunk_lens, k_cache, v_cache, block_tables, context_lens, scale, window, out,
+             max_chunk_len, stream):
     pool = make_pool(k_cache, v_cache)
     _need(q, "q", k_cache.dtype)
     for name, t in (("chunk_starts", chunk_starts), ("chunk_lens", chunk_lens),
@@ -324,11 +369,15 @@ def paged_attn_prefill_chunk(q: torch.Tensor, chunk_starts: torch.Tensor, chunk_
         out = torch.empty_like(q)
     _need(out, "out", q.dtype)
     lib = load_library()
-    _check(lib.pa_paged_attn_prefill_chunk(q.data_ptr(), chunk_starts.data_ptr(), chunk_lens.data_ptr(),
-                                           ctypes.byref(pool), block_tables.data_ptr(), block_tables.shape[1],
-                                           context_lens.data_ptr(), C, hq, rows, int(max_chunk_len),
-                                           float(scale), out.data_ptr(), _stream(stream)),
-           "pa_paged_attn_prefill_chunk")
+    args = (q.data_ptr(), chunk_starts.data_ptr(), chunk_lens.data_ptr(), ctypes.byref(pool),
+            block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), C, hq, rows,
+            int(max_chunk_len), float(scale))
+    if window:
+        _check(lib.pa_paged_attn_prefill_chunk_window(*args, window, out.data_ptr(), _stream(stream)),
+               "pa_paged_attn_prefill_chunk_window")
+    else:
+        _check(lib.pa_paged_attn_prefill_chunk(*args, out.data_ptr(), _stream(stream)),
+               "pa_paged_attn_prefill_chunk")
     return out
 
 

@@ -5,7 +5,9 @@
 // one new token; page "Модуль 04: KV-кэш и арифметика памяти", section 1):
 //     out[s][g] = softmax_j(scale * q[s][g] . K_j) V_j,   j < context_lens[s],
 // with K_j, V_j taken from KV head g / G of logical position j, which lives in
-// block block_tables[s][j / 16] at in-block offset j % 16.
+// block block_tables[s][j / 16] at in-block offset j % 16.  With a sliding
+// window of W keys (same page, sections 4 and 5.2) only j >= context_lens[s] - W
+// are visible, and pages wholly before the window are never read.
 //
 // Work decomposition.  The unit of work is one 16-token page of one KV head
 // of one sequence ("page" below); a (sequence, KV head) pair is an "item".
@@ -51,13 +53,20 @@ struct Layout {
   static constexpr int CPL = DPL / 8;   // 16-byte chunks per lane
 };
 
+// First key position a sequence of length ctx attends to: with a sliding
+// window of W keys ("Модуль 04: KV-кэш и арифметика памяти", sections 4 and
+// 5.2) only the last W positions, else all.  Pages wholly before it are never
+// read (their table entries may already be freed).
+__device__ __forceinline__ int window_lo(int ctx, int window) { return window > 0 && ctx > window ? ctx - window : 0; }
+
+// Pages of sequence s that hold visible keys (from its window's first page).
 __device__ __forceinline__ int pages_of(const DecodeParams &p, int s, bool report) {
   const int ctx = __ldg(p.context_lens + s);
   if (ctx < 1 || ctx > p.max_blocks_per_seq * kBlock) {
     if (report) set_error(p.err, PA_ERR_RANGE, s);
     return 0;
   }
-  return (ctx + kBlock - 1) / kBlock;
+  return (ctx + kBlock - 1) / kBlock - window_lo(ctx, p.window) / kBlock;
 }
 
 // Exclusive prefix of pages over sequences into prefix[0..S]; whole CTA.
@@ -149,14 +158,15 @@ __device__ __forceinline__ void load_page(uint8_t *dst, const CUtensorMap *kmap,
 }
 
 // Scores, online-softmax update and P V of one 16-key page for the G query
-// heads of a KV head, from a stage laid out as above (one warp; nv valid
-// keys).  q holds this lane's dims of the G query rows (pre-scaled, log2
+// heads of a KV head, from a stage laid out as above (one warp; keys nlo ..
+// nv - 1 of the page are visible).  q holds this lane's dims of the G query rows (pre-scaled, log2
 // domain); (m, l, o) is the running state (m warp-uniform, l per lane, o for
 // the lane's 4 dims).  pbuf2 is the warp's [16 keys][G] scratch for the
 // probabilities.  With int8 codes a key's scale multiplies its dot product
 // once, and a value's scale multiplies its probability before the sum.
 template <typename T, int G, bool Q8>
-__device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const float2 (&q)[G][Layout<G>::DPL / 2],
+__device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
+                                            const float2 (&q)[G][Layout<G>::DPL / 2],
                                             float2 (&o)[G][2], float (&m)[G], float (&l)[G], float2 *pbuf2,
                                             int lane) {
   using Ly = Layout<G>;
@@ -205,7 +215,7 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const fl
 #pragma unroll
       for (int off = 1; off < NQ; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
       if constexpr (Q8) a *= ksc;
-      sc[ps][gg] = (t < nv) ? a : neg_inf;
+      sc[ps][gg] = (t >= nlo && t < nv) ? a : neg_inf;
     }
   }
 
@@ -264,11 +274,11 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nv, const fl
       o[gg][1] = __ffma2_rn(pp[gg], v23, o[gg][1]);
     }
   };
-  if (nv == kBlock) {
+  if (nlo == 0 && nv == kBlock) {
 #pragma unroll
     for (int t = 0; t < kBlock; ++t) pv_token(t);
   } else {
-    for (int t = 0; t < nv; ++t) pv_token(t);
+    for (int t = nlo; t < nv; ++t) pv_token(t);
   }
 }
 
@@ -326,16 +336,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   Cursor cc = ic;
 
   // ---- producer (lane 0 issues; all lanes track the cursor) --------------------
-  int win_s = -1, win_base = -1;
+  int win_s = -1, win_base = -1, win_first = 0;
   int32_t win = -1;
   uint32_t bad_mask = 0;
   auto issue = [&](int st) {
     const int base = ic.page & ~31;
     if (ic.s != win_s || base != win_base) {
+      if (ic.s != win_s) win_first = p.window > 0 ? window_lo(__ldg(p.context_lens + ic.s), p.window) / kBlock : 0;
       win_s = ic.s;
       win_base = base;
       const int pg = base + lane;
-      win = (pg < ic.pages) ? __ldg(p.block_tables + (int64_t)ic.s * p.max_blocks_per_seq + pg) : -1;
+      win = (pg < ic.pages)
+                ? __ldg(p.block_tables + (int64_t)ic.s * p.max_blocks_per_seq + win_first + pg)
+                : -1;
     }
     const int blk = __shfl_sync(FULL, win, ic.page & 31);
     const bool ok = (unsigned)blk < (unsigned)p.num_blocks;
@@ -360,7 +373,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   float2 q[G][DPL / 2];
   float2 o[G][2];
   float m[G], l[G];
-  int ctx = 0;
+  int ctx = 0, first = 0, lo_in_first = 0;  // first visible page and key of the item
   bool open = false, whole = false;
   const float neg_inf = -INFINITY;
   float2 *pbuf2 = reinterpret_cast<float2 *>(pbuf);  // [16 keys][G] of (p, p)
@@ -390,6 +403,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         o[gg][1] = make_float2(0.f, 0.f);
       }
       ctx = __ldg(p.context_lens + cc.s);
+      first = window_lo(ctx, p.window) / kBlock;
+      lo_in_first = window_lo(ctx, p.window) - first * kBlock;
       whole = (cc.page == 0);
       open = true;
     }
@@ -403,8 +418,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     }
 
     if (!((bad_mask >> st) & 1u)) {
-      const int nv = min(kBlock, ctx - cc.page * kBlock);  // valid keys in this page
-      decode_page<T, G, Q8>(stages + st * STAGE, nv, q, o, m, l, pbuf2, lane);
+      const int nv = min(kBlock, ctx - (first + cc.page) * kBlock);  // keys of the sequence in this page
+      decode_page<T, G, Q8>(stages + st * STAGE, cc.page == 0 ? lo_in_first : 0, nv, q, o, m, l, pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
 
@@ -565,9 +580,10 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   const int item = blockIdx.x / ncta;
   const int hkv = p.num_kv_heads;
   const int s = item / hkv, h = item % hkv;
-  // Warp gw of the item's nw warps takes pages gw, gw + nw, gw + 2 nw, ...: its
-  // first block ids do not depend on the length, so the length and the block
-  // ids are fetched at once.  No kernel of this library writes the block
+  // Warp gw of the item's nw warps takes the visible pages gw, gw + nw, gw +
+  // 2 nw, ... (counted from the first page of the sliding window, if any):
+  // without a window its first block ids do not depend on the length, so the
+  // length and the block ids are fetched at once.  No kernel of this library writes the block
   // tables or the lengths, so they are read before waiting for the previous
   // kernel (that wait covers the pool, which a KV write fills, and q, which may
   // be another call's output); their latency overlaps the previous kernel.
@@ -608,15 +624,17 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     griddep_launch_dependents();
     return;
   }
-  const int pages = (ctx + kBlock - 1) / kBlock;
-  const int n = pages > gw ? (pages - gw + nw - 1) / nw : 0;  // pages of this warp
+  const int lo = window_lo(ctx, p.window), first = lo / kBlock;  // first visible key and its page
+  const int pages = (ctx + kBlock - 1) / kBlock - first;            // visible pages
+  const int n = pages > gw ? (pages - gw + nw - 1) / nw : 0;       // pages of this warp
+  if (first != 0) win = (gw + nw * lane < pages) ? __ldg(bt + first + gw + nw * lane) : -1;
 
   uint32_t bad_mask = 0;
   auto issue = [&](int i, int st) {
     if ((i & ~31) != win_base) {
       win_base = i & ~31;
       const int pj = gw + nw * (win_base + lane);
-      win = (pj < pages) ? __ldg(bt + pj) : -1;
+      win = (pj < pages) ? __ldg(bt + first + pj) : -1;
     }
     const int blk = __shfl_sync(FULL, win, i & 31);
     const bool ok = (unsigned)blk < (unsigned)p.num_blocks;
@@ -645,8 +663,9 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       break;
     }
     if (!((bad_mask >> st) & 1u)) {
-      const int nv = min(kBlock, ctx - (gw + nw * i) * kBlock);  // valid keys in this page
-      decode_page<T, G, Q8>(stages + st * STAGE, nv, q, o, m, l, pbuf2, lane);
+      const int pg = gw + nw * i;                              // visible page
+      const int nv = min(kBlock, ctx - (first + pg) * kBlock);  // keys of the sequence in this page
+      decode_page<T, G, Q8>(stages + st * STAGE, pg == 0 ? lo - first * kBlock : 0, nv, q, o, m, l, pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
     if (i + kStages < n) issue(i + kStages, st);

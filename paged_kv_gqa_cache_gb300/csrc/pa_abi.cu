@@ -125,8 +125,8 @@ bool pool_map_q8(CUtensorMap *map, const pa_kv_pool_q8 *pool, void *base) {
 // pool's own checks: every other argument is checked before any CUDA call.
 pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const pa_kv_pool_q8 *pool8,
                       const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
-                      int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len, float scale, void *out,
-                      void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+                      int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
+                      void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
   const bool q8 = pool8 != nullptr;
   const int num_kv_heads = q8 ? pool8->num_kv_heads : pool16->num_kv_heads;
   const int num_blocks = q8 ? pool8->num_blocks : pool16->num_blocks;
@@ -142,6 +142,7 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
     return PA_ERR_SHAPE;
   if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
+  if (window < 0) return PA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || !aligned4(block_tables) ||
       !aligned4(context_lens))
     return PA_ERR_ALIGN;
@@ -169,14 +170,17 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
   p.num_kv_heads = num_kv_heads;
   p.num_q_heads = num_q_heads;
   p.num_blocks = num_blocks;
+  p.window = window;
   p.scale_log2 = scale * 1.4426950408889634f;
 
-  // Upper bound on the pages of the call; aim for at least 4 pages per warp.
-  const int64_t pages_hint = (int64_t)num_seqs * num_kv_heads * ((max_context_len + kBlock - 1) / kBlock);
+  // Upper bound on the pages of one item (a window of W keys spans at most
+  // (W - 1) / 16 + 2 pages) and of the call; aim for at least 4 pages per warp.
+  int item_pages = (max_context_len + kBlock - 1) / kBlock;
+  if (window > 0 && (window - 1) / kBlock + 2 < item_pages) item_pages = (window - 1) / kBlock + 2;
+  const int64_t pages_hint = (int64_t)num_seqs * num_kv_heads * item_pages;
   int64_t workers = (pages_hint + 3) / 4;
   if (workers > kDecodeMaxWorkers) workers = kDecodeMaxWorkers;
-  cudaError_t e = launch_decode(p, kmap, vmap, dtype, group, (int)workers, (max_context_len + kBlock - 1) / kBlock,
-                                q8, stream);
+  cudaError_t e = launch_decode(p, kmap, vmap, dtype, group, (int)workers, item_pages, q8, stream);
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
@@ -271,7 +275,18 @@ pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, const int3
   pa_status st = check_pool(pool);
   if (st != PA_OK) return st;
   return decode_call(q, pool->dtype, pool, nullptr, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                     num_q_heads, max_context_len, scale, out, workspace, workspace_bytes,
+                     num_q_heads, max_context_len, scale, 0, out, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_paged_attn_decode_window(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
+                                      void *out, void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  return decode_call(q, pool->dtype, pool, nullptr, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, max_context_len, scale, window, out, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream));
 }
 
@@ -311,18 +326,19 @@ pa_status pa_paged_attn_decode_q8(const void *q, int32_t dtype, const pa_kv_pool
   if (st != PA_OK) return st;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
   return decode_call(q, dtype, nullptr, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                     num_q_heads, max_context_len, scale, out, workspace, workspace_bytes,
+                     num_q_heads, max_context_len, scale, 0, out, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream));
 }
 
-pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts, const int32_t *chunk_lens,
-                                      const pa_kv_pool *pool, const int32_t *block_tables,
-                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
-                                      int32_t num_chunks, int32_t num_q_heads, int32_t total_q_tokens,
-                                      int32_t max_chunk_len, float scale, void *out, pa_stream_t stream) {
+pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t *chunk_starts,
+                                             const int32_t *chunk_lens, const pa_kv_pool *pool,
+                                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                             const int32_t *context_lens, int32_t num_chunks, int32_t num_q_heads,
+                                             int32_t total_q_tokens, int32_t max_chunk_len, float scale,
+                                             int32_t window, void *out, pa_stream_t stream) {
   pa_status st = check_pool(pool);
   if (st != PA_OK) return st;
-  if (num_chunks < 0 || total_q_tokens < 0) return PA_ERR_SHAPE;
+  if (num_chunks < 0 || total_q_tokens < 0 || window < 0) return PA_ERR_SHAPE;
   if (num_chunks == 0) return PA_OK;
   if (!q || !chunk_starts || !chunk_lens || !block_tables || !context_lens || !out) return PA_ERR_NULL;
   int group = 0;
@@ -353,6 +369,7 @@ pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts
   p.num_blocks = pool->num_blocks;
   p.total_q_tokens = total_q_tokens;
   p.max_chunk_len = max_chunk_len;
+  p.window = window;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   CUtensorMap kmap, vmap, qmap;
@@ -371,6 +388,16 @@ pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts
   cudaError_t e = launch_prefill(p, kmap, vmap, qmap, pool->dtype, group, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts, const int32_t *chunk_lens,
+                                      const pa_kv_pool *pool, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      int32_t num_chunks, int32_t num_q_heads, int32_t total_q_tokens,
+                                      int32_t max_chunk_len, float scale, void *out, pa_stream_t stream) {
+  return pa_paged_attn_prefill_chunk_window(q, chunk_starts, chunk_lens, pool, block_tables, max_blocks_per_seq,
+                                            context_lens, num_chunks, num_q_heads, total_q_tokens, max_chunk_len,
+                                            scale, 0, out, stream);
 }
 
 pa_status pa_get_device_error(pa_stream_t stream, int32_t *detail) {

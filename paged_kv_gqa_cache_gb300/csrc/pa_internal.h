@@ -71,6 +71,7 @@ struct DecodeParams {
   int32_t num_q_heads;
   int32_t num_blocks;
   int32_t num_workers;       // warps in the launch
+  int32_t window;            // sliding window in keys (0: none)
   float scale_log2;          // scale * log2(e)
 };
 
@@ -111,6 +112,7 @@ struct PrefillParams {
   int32_t num_blocks;
   int32_t total_q_tokens;
   int32_t max_chunk_len;
+  int32_t window;            // sliding window in keys (0: none)
   float scale_log2;
 };
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,

@@ -7,7 +7,11 @@
 // Финальный проект: мини-движок инференса", qwen_serve/model.py,
 // Qwen3Model.forward with T > 1: mask kpos <= qpos on absolute positions;
 // page "Модуль 04: KV-кэш и арифметика памяти", section 3.4: the prefix KV
-// lives in the cache between chunks).
+// lives in the cache between chunks).  With a sliding window of W keys
+// (page "Модуль 04: KV-кэш и арифметика памяти", sections 4 and 5.2) the
+// query at position p sees only keys p - W + 1 .. p: a tile's key loop starts
+// at the key tile of its first row's lowest key, and pages wholly below that
+// key are never read.
 //
 // One CTA computes one M = 128 tile of query rows for one KV head: 128 / G
 // consecutive tokens of the chunk x the G query heads sharing that KV head,
@@ -103,26 +107,30 @@ struct Bars {
 // expects one arrival per loader warp).  A TMA engine serves each issuing warp
 // at about one small box per 50 ns, so the boxes are spread over the loader
 // warps: this warp's lane i issues box b0 + kLoadWarps * i.  Pages past the
-// sequence are skipped; a page whose block id is out of range is zeroed and
-// reported.
+// sequence are skipped; pages below pg0 (wholly before the sliding window)
+// are skipped too and, with `zero_below`, zeroed (value rows meet zero
+// probabilities and must stay finite); a page whose block id is out of range
+// is zeroed and reported.  sbt caches the block ids of pages pg0 ...
 __device__ __forceinline__ void load_boxes(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int kt, int b0,
-                                           int h, int npages, const int32_t *sbt, const int32_t *bt,
-                                           const PrefillParams &p, int c, int lane) {
+                                           int h, int pg0, int npages, bool zero_below, const int32_t *sbt,
+                                           const int32_t *bt, const PrefillParams &p, int c, int lane) {
   const int b = b0 + kLoadWarps * lane;
   const int page = b >> 1, half = b & 1;
   const int pg = kt * 8 + page;
-  const bool in = b < 16 && pg < npages;
+  const bool in = b < 16 && pg >= pg0 && pg < npages;
   int id = -1;
-  if (in) id = pg < kBtCache ? sbt[pg] : __ldg(bt + pg);
+  if (in) id = pg - pg0 < kBtCache ? sbt[pg - pg0] : __ldg(bt + pg);
   const bool ok = in && (unsigned)id < (unsigned)p.num_blocks;
   const unsigned okmask = __ballot_sync(0xffffffffu, ok);
   uint8_t *box = dst + half * kHalf + page * 2048;
-  if (in && !ok) {  // rare: keep the products finite; the error word reports the chunk
-    if (half == 0) set_error(p.err, PA_ERR_RANGE, c);
+  const bool zero = (in && !ok) || (zero_below && b < 16 && pg < pg0);
+  if (zero) {  // rare: keep the products finite
+    if (in && half == 0) set_error(p.err, PA_ERR_RANGE, c);  // the error word reports the chunk
     uint4 *z = reinterpret_cast<uint4 *>(box);
     for (int i = 0; i < 128; ++i) z[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
+  __syncwarp();  // the zeroed boxes are written before the arrival below releases them
   if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(okmask) * 2048u);
   __syncwarp();
   if (ok) tma_load_4d(box, map, bar, half * 64, h, 0, id);
@@ -158,12 +166,13 @@ __device__ __forceinline__ void store_rows_coalesced(uint4 *stage, void *dst, bo
 }
 
 // P = 2^(S * scale_log2 - m) for this thread's 64 keys of one tile (two
-// 32-column chunks v[0], v[1]), masked past `lim` unless `full`, written over
+// 32-column chunks v[0], v[1]), unless `full` masked outside the row's visible
+// keys (key kb + i of the half is visible when 0 <= kb + i <= span), written over
 // the chunk's first 16 columns as pairs of the input dtype; with LO, the
 // rounding remainder goes into the next 16.  Returns the row sum of P.
 template <typename T, bool LO>
 __device__ __forceinline__ float exp_pack_store(const uint32_t (&v)[2][32], uint32_t s_addr, float sl2, float m_ref,
-                                                bool full, int kbase, int lim) {
+                                                bool full, int kb, int span) {
   const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_ref, -m_ref);
   const float2 neg1 = make_float2(-1.f, -1.f);
   float2 ls = make_float2(0.f, 0.f);
@@ -176,9 +185,9 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t (&v)[2][32], uint
                                   sl2v, negm);
       float2 pr = make_float2(ex2(e.x), ex2(e.y));
       if (!full) {
-        const int key = kbase + cc * 32 + 2 * j;
-        pr.x = (key <= lim) ? pr.x : 0.f;
-        pr.y = (key + 1 <= lim) ? pr.y : 0.f;
+        const int key = kb + cc * 32 + 2 * j;
+        pr.x = ((unsigned)key <= (unsigned)span) ? pr.x : 0.f;
+        pr.y = ((unsigned)(key + 1) <= (unsigned)span) ? pr.y : 0.f;
       }
       ls = __fadd2_rn(ls, pr);
       pk[j] = Pack<T>::from_f2(pr.x, pr.y);
@@ -240,7 +249,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const int kt_ctx = (ctx - 1) / 128;                       // key tile holding the sequence's last key
   const int npages = (ctx + kBlock - 1) / kBlock;
   const int32_t *bt = p.block_tables + (int64_t)c * p.max_blocks_per_seq;
-  const bool lo_tile0 = start + t0 < 127;  // the tile's first row sees fewer than 128 keys
+  // Sliding window: the smallest key any row of the tile sees, the key tile
+  // the loop starts at (tiles are counted from it: i = kt - kt0 indexes the
+  // rings, the S buffers and the barrier phases) and the first page read.
+  const int win = p.window;
+  const int klo = (win > 0 && start + t0 - win + 1 > 0) ? start + t0 - win + 1 : 0;
+  const int kt0 = klo / 128, pg0 = klo / kBlock, ntl = nkt - kt0;
+  // Rows that see fewer than 128 keys average the rounding errors of too few
+  // probabilities; they get the two-term P on the tiles where they occur: key
+  // tile 0 for the tile's first rows, every tile under a window shorter than
+  // 128.  Tiles i < lo_tiles (counted from kt0) take it.
+  const int lo_tiles = (win > 0 && win < 128) ? ntl : (start + t0 < 127 ? 1 : 0);
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&kmap);
@@ -271,8 +290,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // ---------------- loader warps: each tile's K and V boxes, a third per warp ----------------
     const int lw = warp - kWarpLoad0;
     int32_t *sbt = reinterpret_cast<int32_t *>(smem + OFF_BT);
-    const int cached = min(min(npages, nkt * 8), kBtCache);
-    for (int i = lw * 32 + lane; i < cached; i += kLoadWarps * 32) sbt[i] = __ldg(bt + i);
+    const int cached = min(min(npages, nkt * 8) - pg0, kBtCache);
+    for (int i = lw * 32 + lane; i < cached; i += kLoadWarps * 32) sbt[i] = __ldg(bt + pg0 + i);
     named_barrier(1, kLoadWarps * 32);  // the cached block ids are complete
     griddep_wait();                     // Q, K and V may come from the previous kernel
     if (lw == 0 && lane == 0) {
@@ -281,18 +300,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
     }
     const int kb0 = lw, vb0 = (lw + kLoadWarps - 1) % kLoadWarps;  // balances the boxes per warp
-    for (int t = 0; t < nkt; ++t) {
+    for (int t = 0; t < ntl; ++t) {
       const int ks = t % kKStages, vs = t % kVStages;
       if (t >= kKStages && !mbar_wait(&bars.s_full[ks], ((t - kKStages) / kKStages) & 1)) {
         timed_out = true;
         break;
       }
-      load_boxes(smem + OFF_K + ks * 2 * kHalf, &kmap, &bars.k_full[ks], t, kb0, h, npages, sbt, bt, p, c, lane);
+      load_boxes(smem + OFF_K + ks * 2 * kHalf, &kmap, &bars.k_full[ks], kt0 + t, kb0, h, pg0, npages, false, sbt,
+                 bt, p, c, lane);
       if (t >= kVStages && !mbar_wait(&bars.pv_done[vs], ((t - kVStages) / kVStages) & 1)) {
         timed_out = true;
         break;
       }
-      load_boxes(smem + OFF_V + vs * 2 * kHalf, &vmap, &bars.v_full[vs], t, vb0, h, npages, sbt, bt, p, c, lane);
+      load_boxes(smem + OFF_V + vs * 2 * kHalf, &vmap, &bars.v_full[vs], kt0 + t, vb0, h, pg0, npages, true, sbt,
+                 bt, p, c, lane);
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
@@ -314,10 +335,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       constexpr uint64_t kStageStep = (2 * kHalf) >> 4;   // one ring stage
       constexpr uint64_t kHalfStep = kHalf >> 4;          // the other 64-dim half
       bool pv_ok = false;                                  // P (and so V) of the next P V batch is ready
-      for (int kt = 0; kt <= nkt && !timed_out; ++kt) {
+      for (int kt = 0; kt <= ntl && !timed_out; ++kt) {   // kt: tile index from kt0
         const int j = kt - 1, sj = j & 1;                  // the tile whose P V is issued in this iteration
         const int jv = j % kVStages;
-        if (kt < nkt) {
+        if (kt < ntl) {
           const int b = kt % kKStages, sb = kt & 1;
           if (!mbar_wait(&bars.k_full[b], (kt / kKStages) & 1)) {
             timed_out = true;
@@ -351,7 +372,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           const uint64_t vdesc = vdesc0 + (uint64_t)jv * kStageStep;
           const uint32_t p_col = tmem + sj * 128;
           const uint32_t first = j > 0 ? 1u : 0u;
-          if (j == 0 && lo_tile0) {
+          if (j < lo_tiles) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {  // 16-key step: V rows 16 kk .. 16 kk + 15, into O of key half kk / 4
               const uint32_t o_col = tmem + kColO + (kk >> 2) * 128;
@@ -379,13 +400,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     const int r = quad * 32 + lane;                  // tile row = TMEM lane
     const int tq = t0 + r / G;                       // query token within the chunk
     const int head = h * G + r % G;
-    const int lim = min(start + tq, ctx - 1);        // last visible key position of this row
+    // visible keys of this row: rlo .. lim; kb0 = first key of this thread's
+    // half of the loop's first tile, relative to rlo; span = lim - rlo
+    const int lim = min(start + tq, ctx - 1);
+    const int rlo = (win > 0 && start + tq - win + 1 > 0) ? start + tq - win + 1 : 0;
+    const bool none = lim < rlo;  // a row past the chunk under a short window: no key at all
+    const int kb0 = none ? -(1 << 30) : kt0 * 128 + ch * 64 - rlo, span = none ? 0 : lim - rlo;
+    const int kt_last = kt_ctx - kt0;                // tile (from kt0) holding the sequence's last key
+    const int zrow = ctx - kt_ctx * 128;             // its first row past the sequence
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t o_self = tmem + lane_base + kColO + ch * 128;
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
 
-    for (int kt = 0; kt < nkt; ++kt) {
+    for (int kt = 0; kt < ntl; ++kt) {               // kt: tile index from kt0
       const int sb = kt & 1;
       if (!mbar_wait(&bars.s_full[kt % kKStages], (kt / kKStages) & 1)) {
         timed_out = true;
@@ -393,12 +421,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
       tc::fence_after_sync();
       const uint32_t s_addr = tmem + lane_base + sb * 128 + ch * 64;
-      const int kbase = kt * 128 + ch * 64;          // first key of this thread's half
+      const int kb = kb0 + kt * 128;                 // first key of this thread's half, from rlo
       uint32_t v[2][32];
       tc::ld_32x32b_x32(s_addr, v[0]);
       tc::ld_32x32b_x32(s_addr + 32, v[1]);
       tc::wait_ld();
-      const bool full = __all_sync(FULL, kbase + 63 <= lim);
+      const bool full = __all_sync(FULL, kb >= 0 && kb + 63 <= span);
 
       float mx = -INFINITY;
       if (full) {
@@ -412,7 +440,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (kbase + cc * 32 + j <= lim) mx = fmaxf(mx, __uint_as_float(v[cc][j]));
+            if ((unsigned)(kb + cc * 32 + j) <= (unsigned)span) mx = fmaxf(mx, __uint_as_float(v[cc][j]));
       }
       const float mc = mx * sl2;   // -inf if no key of this half is visible yet
       const bool first = (m_ref == -INFINITY);             // nothing accumulated for this row yet
@@ -442,11 +470,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (first) m_ref = mc;
 
       // P in the input dtype (two terms where the tile needs them), over this half's S columns
-      l += (kt == 0 && lo_tile0) ? exp_pack_store<T, true>(v, s_addr, sl2, m_ref, full, kbase, lim)
-                                 : exp_pack_store<T, false>(v, s_addr, sl2, m_ref, full, kbase, lim);
+      l += (kt < lo_tiles) ? exp_pack_store<T, true>(v, s_addr, sl2, m_ref, full, kb, span)
+                           : exp_pack_store<T, false>(v, s_addr, sl2, m_ref, full, kb, span);
       tc::wait_st();
 
-      if (kt == kt_ctx) {
+      if (kt == kt_last) {
         // value rows of keys >= ctx in this half (partial last page, pages past
         // the end); this half's P V product is the only one that reads them
         const int vb = kt % kVStages;
@@ -454,7 +482,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           timed_out = true;
           break;
         }
-        const int z0 = max(ctx - kt * 128, ch * 64), z1 = ch * 64 + 64;
+        const int z0 = max(zrow, ch * 64), z1 = ch * 64 + 64;
         uint8_t *vbase = smem + OFF_V + vb * 2 * kHalf;
         for (int idx = (warp & 3) * 32 + lane; idx < (z1 - z0) * 16; idx += kSoftmaxThreads / 2) {
           const int row = z0 + (idx >> 4), part = idx & 15;
@@ -465,7 +493,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
       tc::fence_before_sync();
       // the P V batch waits on this barrier alone, so it must also imply that V landed
-      if (kt != kt_ctx && !mbar_wait(&bars.v_full[kt % kVStages], (kt / kVStages) & 1)) {
+      if (kt != kt_last && !mbar_wait(&bars.v_full[kt % kVStages], (kt / kVStages) & 1)) {
         timed_out = true;
         break;
       }
@@ -473,7 +501,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
 
     if (!timed_out) {
-      const int j = nkt - 1;
+      const int j = ntl - 1;
       if (mbar_wait(&bars.pv_done[j % kVStages], (j / kVStages) & 1)) {
         tc::fence_after_sync();
         // merge the two halves of the row

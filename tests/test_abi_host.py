@@ -47,7 +47,7 @@ def test_only_c_entry_points_are_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 2
+    assert lib.pa_abi_version() == 3
     for code in range(0, -10, -1):
         assert lib.pa_status_string(code).decode().startswith(pa.STATUS[code])
 
@@ -172,3 +172,15 @@ def test_decode_q8_rejects_bad_arguments(lib):
     assert call(mcl=300) == -2
     assert call(scale=float("inf")) == -2
     assert call(out=P + 2) == -9
+
+
+def test_window_calls_check_their_arguments(lib):
+    pool = _pool()
+    ws = lib.pa_decode_workspace_bytes(4, 16, 8, 256)
+    dec = lambda w, out=P: lib.pa_paged_attn_decode_window(P, ctypes.byref(pool), P, 16, P, 4, 16, 256, 0.088, w,
+                                                           out, P, ws, None)
+    pre = lambda w, q=P: lib.pa_paged_attn_prefill_chunk_window(q, P, P, ctypes.byref(pool), P, 128, P, 3, 16,
+                                                                1536, 512, 0.088, w, P, None)
+    assert dec(-1) == -2 and pre(-1) == -2      # a negative window
+    assert dec(40, out=P + 2) == -9             # the plain calls' checks still apply, before any CUDA call
+    assert pre(40, q=P + 8) == -9
