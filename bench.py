@@ -60,10 +60,16 @@ def parse_args(argv=None):
     ap.add_argument("--kv", choices=["16bit", "int8"], default="16bit",
                     help="decode workloads: the workload's 16-bit pool, or an int8 pool (codes + one fp32 scale "
                          "per token and KV head) holding the same tokens quantised")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window of W keys for the attention calls of workloads 2, 3 and 4 (0 = none); "
+                         "the bytes or FLOPs counted are those of the visible keys")
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
                     help="2 = the Qwen3-0.6B 28-layer decode step (default); 3, 4, 5 = the mixed prefill "
                          "step, the Qwen3-8B decode and the prefix-shared long tail (diagnostic lines)")
-    return ap.parse_args(argv)
+    args = ap.parse_args(argv)
+    if args.window < 0 or (args.window and (args.workload == 5 or args.kv == "int8")):
+        ap.error("--window takes W >= 0, with workloads 2, 3 and 4 on the 16-bit pool")
+    return args
 
 
 # ---- distributed plumbing (replicas only) -------------------------------------------
@@ -194,12 +200,13 @@ class DecodeStep:
     kv_cache_write of the new tokens then paged_attn_decode (layer pools are
     cycled when fewer distinct pools than calls are held)."""
 
-    def __init__(self, device, workload: int = 2, pools: int = 0):
+    def __init__(self, device, workload: int = 2, pools: int = 0, window: int = 0):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
         self.pa = pa
         self.workload = workload
+        self.window = window
         self.desc, default_pools, self.L = WORKLOADS[workload]
         pools = pools or default_pools
         maker = workloads.CONFIGS[workload]
@@ -214,11 +221,12 @@ class DecodeStep:
             shared_tokens = 16 * c.meta["shared_prefix_blocks"]
             unique = sum(lens) - shared_tokens * (len(lens) - 1)
             self.decode_bytes_layer = workloads.decode_kv_bytes(lens, c.hkv, unique_tokens=unique)
-        else:
-            self.decode_bytes_layer = workloads.decode_kv_bytes(lens, c.hkv)
+        else:   # the visible rows: the last `window` of each sequence under a window
+            self.decode_bytes_layer = workloads.decode_kv_bytes([min(n, window) if window else n for n in lens],
+                                                                c.hkv)
         self.write_bytes_layer = 2 * c.k_new[0].numel() * 2 * 2     # K and V rows, read + write
         self.step_bytes = self.L * (self.decode_bytes_layer + self.write_bytes_layer)
-        self.decode_kernels = pa.decode_kernel_launches(self.S, c.hkv, c.max_context_len)
+        self.decode_kernels = pa.decode_kernel_launches(self.S, c.hkv, c.max_context_len, window)
         self.kernels_per_step = self.L * (1 + self.decode_kernels)  # write, then the decode's kernels
 
     def write(self, l):
@@ -227,8 +235,14 @@ class DecodeStep:
 
     def decode(self, l):
         c, i = self.case, l % self.case.n_layers
-        self.pa.paged_attn_decode(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens, c.scale,
-                                  out=self.out[i], workspace=self.ws, max_context_len=c.max_context_len)
+        if self.window:
+            self.pa.paged_attn_decode_window(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
+                                             c.scale, self.window, out=self.out[i], workspace=self.ws,
+                                             max_context_len=c.max_context_len)
+        else:
+            self.pa.paged_attn_decode(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
+                                      c.scale, out=self.out[i], workspace=self.ws,
+                                      max_context_len=c.max_context_len)
 
     def run(self):
         for l in range(self.L):
@@ -288,26 +302,25 @@ class MixedStep:
     kv_cache_write of 2048 new tokens, prefill of 3 chunks of 512 (prefixes 0,
     512, 1536) and decode of 512 sequences; 2 distinct pools cycled over 28."""
 
-    def __init__(self, device):
+    def __init__(self, device, window: int = 0):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
-        self.pa, self.L = pa, 28
+        self.pa, self.L, self.window = pa, 28, window
         self.case = c = workloads.config3(device=device, n_layers=2, nan_fill=False)
         self.out_d = [torch.empty_like(q) for q in c.q]
         self.out_p = [torch.empty_like(q) for q in c.q_chunks]
         self.ws = pa.alloc_decode_workspace(c.q[0].shape[0], c.hq, c.hkv, c.max_context_len, device)
-        self.flops_layer = workloads.prefill_flops(c.meta["chunks"], c.hq)
-        self.decode_bytes_layer = workloads.decode_kv_bytes(c.meta["decode_lens"], c.hkv)
+        self.flops_layer = workloads.prefill_flops(c.meta["chunks"], c.hq, window=window)
         self.tokens = c.slot_mapping.numel()
         lens = c.meta["decode_lens"]
-        self.kernels_per_layer = 2 + pa.decode_kernel_launches(len(lens), c.hkv, c.max_context_len)
+        self.kernels_per_layer = 2 + pa.decode_kernel_launches(len(lens), c.hkv, c.max_context_len, window)
 
     def prefill(self, l):
         c, i = self.case, l % 2
-        self.pa.paged_attn_prefill_chunk(c.q_chunks[i], c.chunk_starts, c.chunk_lens, c.k_cache[i], c.v_cache[i],
-                                         c.chunk_block_tables, c.chunk_context_lens, c.scale, out=self.out_p[i],
-                                         max_chunk_len=512)
+        self.pa.paged_attn_prefill_chunk_window(c.q_chunks[i], c.chunk_starts, c.chunk_lens, c.k_cache[i],
+                                                c.v_cache[i], c.chunk_block_tables, c.chunk_context_lens, c.scale,
+                                                self.window, out=self.out_p[i], max_chunk_len=512)
 
     def run(self):
         c = self.case
@@ -315,9 +328,9 @@ class MixedStep:
             i = l % 2
             self.pa.kv_cache_write(c.k_new[i], c.v_new[i], c.slot_mapping, c.k_cache[i], c.v_cache[i])
             self.prefill(l)
-            self.pa.paged_attn_decode(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
-                                      c.scale, out=self.out_d[i], workspace=self.ws,
-                                      max_context_len=c.max_context_len)
+            self.pa.paged_attn_decode_window(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
+                                             c.scale, self.window, out=self.out_d[i], workspace=self.ws,
+                                             max_context_len=c.max_context_len)
 
     def run_prefill_only(self):
         for l in range(self.L):
@@ -417,7 +430,10 @@ def cpu_baseline(step: DecodeStep, seconds: float):
             kh = c.k_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
             vh = c.v_cache[l].cpu().view(torch.int16).numpy().view(np.uint16)
             t0 = time.perf_counter()
-            oracle.paged_attn_decode(qh, kh, vh, bt, ctx, c.scale, odt, num_threads=threads)
+            if getattr(step, "window", 0):
+                oracle.paged_attn_decode_window(qh, kh, vh, bt, ctx, c.scale, step.window, odt, num_threads=threads)
+            else:
+                oracle.paged_attn_decode(qh, kh, vh, bt, ctx, c.scale, odt, num_threads=threads)
         t_total += time.perf_counter() - t0
         done_bytes += step.decode_bytes_layer
         layers += 1
@@ -446,7 +462,8 @@ def run_ours(args):
     if args.workload == 3:
         return run_mixed(args, dev, pa)
 
-    step = (DecodeStepQ8 if args.kv == "int8" else DecodeStep)(dev, args.workload, args.pools)
+    step = (DecodeStepQ8(dev, args.workload, args.pools) if args.kv == "int8"
+            else DecodeStep(dev, args.workload, args.pools, args.window))
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_dec = graph_of(step.run_decode_only, 1, stream)
@@ -476,12 +493,15 @@ def run_ours(args):
 
     q8 = isinstance(step, DecodeStepQ8)
     pool_mib = (step.pool_bytes if q8 else 2 * step.case.k_cache[0].numel() * 2) / 2**20
+    win = getattr(step, "window", 0)
+    tag = "_q8" if q8 else (f"_window{win}" if win else "")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8" if q8 else step.dtype, "data": "synthetic",
         "config": {"workload": step.desc + (", int8 KV pool (codes + one fp32 scale per token and KV head), "
-                                            f"{step.dtype} q and out" if q8 else ""),
+                                            f"{step.dtype} q and out" if q8 else "")
+                               + (f", sliding window of {win} keys (bytes of the visible rows)" if win else ""),
                    "global_batch": step.S * world, "seq_len": step.case.max_context_len,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({step.case.n_layers} distinct pools of {pool_mib:.0f} MiB "
@@ -494,11 +514,11 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "peak_kind": peak_kind,
-                     "kernel": ("paged_attn_decode_q8" if q8 else "paged_attn_decode") + " per layer ("
+                     "kernel": "paged_attn_decode" + tag + " per layer ("
                                + ("one cluster per sequence and KV head" if step.decode_kernels == 1
                                   else "split + combine") + ")",
                      "bytes_per_launch": step.decode_bytes_layer, "launch_ms": round(dec_launch_ms, 5),
-                     "traffic": committed_traffic("decode.cu", f"decode{'_q8' if q8 else ''}_workload{args.workload}.md")},
+                     "traffic": committed_traffic("decode.cu", f"decode{tag}_workload{args.workload}.md")},
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -511,7 +531,7 @@ def run_mixed(args, dev, pa):
     """Diagnostic line for the mixed chunked-prefill step (28 layers)."""
     import torch
     rank, world, _ = dist_env()
-    step = MixedStep(dev)
+    step = MixedStep(dev, args.window)
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_pre = graph_of(step.run_prefill_only, 1, stream)
@@ -532,15 +552,19 @@ def run_mixed(args, dev, pa):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "Qwen3-0.6B mixed chunked-prefill step, 28 layers: chunks (0,512), (512,512), "
-                               "(1536,512) + 512 decode seqs ctx U[16,1024], bf16; 2 distinct pools cycled",
+                               "(1536,512) + 512 decode seqs ctx U[16,1024], bf16; 2 distinct pools cycled"
+                               + (f"; sliding window of {args.window} keys (FLOPs of the visible pairs)"
+                                  if args.window else ""),
                    "global_batch": 515 * world, "parallelism": f"replicas x{world}",
                    "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
         "gpu_launches": step.L * step.kernels_per_layer * args.steps,
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(tflops / bf16, 3), "peak_kind": peak_kind,
-                     "kernel": "paged_attn_prefill_chunk per layer", "flops_per_launch": step.flops_layer,
+                     "kernel": "paged_attn_prefill_chunk" + (f"_window (W={args.window})" if args.window else "")
+                               + " per layer", "flops_per_launch": step.flops_layer,
                      "launch_ms": round(ms_pre, 5),
-                     "traffic": committed_traffic("prefill.cu", "prefill_workload3.md")},
+                     "traffic": committed_traffic("prefill.cu", f"prefill{f'_window{args.window}' if args.window else ''}"
+                                                                f"_workload3.md")},
         "clocks": clk.summary(),
     }
     if rank == 0:

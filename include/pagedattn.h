@@ -256,7 +256,10 @@ PA_API pa_status pa_paged_attn_decode_q8(const void *q, int32_t dtype, const pa_
  * paged_attn_decode_window — pa_paged_attn_decode with a sliding window of
  * `window` keys: sequence s attends to j in [max(0, context_lens[s] - window),
  * context_lens[s]).  Arguments, workspace and errors as pa_paged_attn_decode;
- * window < 0 returns PA_ERR_SHAPE.
+ * window < 0 returns PA_ERR_SHAPE.  A sequence's window spans at most
+ * (window - 1) / 16 + 2 pages, so the call launches the kernels
+ * pa_decode_kernel_launches gives for max_context_len =
+ * min(max_context_len, 16 * ((window - 1) / 16 + 2)).
  */
 PA_API pa_status pa_paged_attn_decode_window(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
                                              int32_t max_blocks_per_seq, const int32_t *context_lens,

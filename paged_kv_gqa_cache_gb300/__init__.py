@@ -243,9 +243,13 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, m
     return int(load_library().pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, max_context_len))
 
 
-def decode_kernel_launches(num_seqs: int, num_kv_heads: int, max_context_len: int) -> int:
+def decode_kernel_launches(num_seqs: int, num_kv_heads: int, max_context_len: int, window: int = 0) -> int:
     """Kernels one decode call with these sizes launches on the current device
-    (1: one cluster per sequence and KV head; 2: split-K then combine)."""
+    (1: one cluster per sequence and KV head; 2: split-K then combine).  A
+    window call plans like a plain call bounded by the window's pages (see
+    pa_paged_attn_decode_window)."""
+    if window > 0:
+        max_context_len = min(max_context_len, 16 * ((window - 1) // 16 + 2))
     return int(load_library().pa_decode_kernel_launches(num_seqs, num_kv_heads, max_context_len))
 
 

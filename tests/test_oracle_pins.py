@@ -379,6 +379,16 @@ def test_prefill_flop_count_of_the_mixed_step():
     assert workloads.prefill_flops([(0, 512), (512, 512), (1536, 512)], 16) == 11_817_451_520
 
 
+def test_prefill_flop_count_under_a_window():
+    chunks = [(0, 512), (512, 512), (1536, 512)]
+    full = workloads.prefill_flops(chunks, 16)
+    assert workloads.prefill_flops(chunks, 16, window=2048) == full    # no row sees more than 2048 keys
+    # W = 512: every row of the last two chunks sees 512 keys; row i of the first sees i + 1
+    pairs = 512 * 513 // 2 + 2 * 512 * 512
+    assert workloads.prefill_flops(chunks, 16, window=512) == 4 * 128 * 16 * pairs
+    assert workloads.prefill_flops([(5, 3)], 1, window=1) == 4 * 128 * 3
+
+
 # ---- planted mistakes: the battery must catch each -------------------------------
 
 def _battery():

@@ -283,8 +283,13 @@ def decode_kv_bytes(context_lens: Sequence[int], hkv: int, elt: int = 2, unique_
     return kv_bytes(1, hkv, HEAD_DIM, tokens, elt)
 
 
-def prefill_flops(chunks: Sequence[tuple], hq: int, head_dim: int = HEAD_DIM) -> int:
+def prefill_flops(chunks: Sequence[tuple], hq: int, head_dim: int = HEAD_DIM, window: int = 0) -> int:
     """Algorithmic FLOPs of causal chunk attention: 2 matmuls (QK^T and PV) x
-    2 flops per multiply-add x head_dim x query heads x visible (query, key) pairs."""
-    pairs = sum(n * s + n * (n + 1) // 2 for s, n in chunks)
+    2 flops per multiply-add x head_dim x query heads x visible (query, key)
+    pairs (with a sliding window of W keys the query at position p sees
+    min(p + 1, W) keys)."""
+    if window > 0:
+        pairs = sum(min(s + i + 1, window) for s, n in chunks for i in range(n))
+    else:
+        pairs = sum(n * s + n * (n + 1) // 2 for s, n in chunks)
     return 4 * head_dim * hq * pairs
