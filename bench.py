@@ -63,6 +63,9 @@ def parse_args(argv=None):
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window of W keys for the attention calls of workloads 2, 3 and 4 (0 = none); "
                          "the bytes or FLOPs counted are those of the visible keys")
+    ap.add_argument("--block-copy", action="store_true",
+                    help="diagnostic line for the copy-on-write block copy: 64 (src, dst) pairs over the 28 "
+                         "layer pools of the Qwen3-0.6B geometry (512 blocks of 16 x 8 x 128 fp16 each)")
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
                     help="2 = the Qwen3-0.6B 28-layer decode step (default); 3, 4, 5 = the mixed prefill "
                          "step, the Qwen3-8B decode and the prefix-shared long tail (diagnostic lines)")
@@ -459,6 +462,8 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
     import paged_kv_gqa_cache_gb300 as pa
+    if args.block_copy:
+        return run_block_copy(args, dev, pa)
     if args.workload == 3:
         return run_mixed(args, dev, pa)
 
@@ -565,6 +570,61 @@ def run_mixed(args, dev, pa):
                      "launch_ms": round(ms_pre, 5),
                      "traffic": committed_traffic("prefill.cu", f"prefill{f'_window{args.window}' if args.window else ''}"
                                                                 f"_workload3.md")},
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_block_copy(args, dev, pa):
+    """Diagnostic line for the copy-on-write block copy over every layer."""
+    import numpy as np
+    import torch
+    rank, world, _ = dist_env()
+    layers, nb, hkv, npairs = 28, 512, 8, 64
+    g = torch.Generator(device=dev).manual_seed(7)
+    pools = [(torch.randn((nb, 16, hkv, 128), generator=g, device=dev).to(torch.float16),
+              torch.randn((nb, 16, hkv, 128), generator=g, device=dev).to(torch.float16)) for _ in range(layers)]
+    perm = np.random.default_rng(7).permutation(nb)
+    # alternate two disjoint pair sets so consecutive copies never touch the same blocks
+    sets = [torch.from_numpy(np.stack([perm[i * 2 * npairs:i * 2 * npairs + npairs],
+                                       perm[i * 2 * npairs + npairs:(i + 1) * 2 * npairs]], 1).astype(np.int32)
+                             ).to(dev) for i in range(2)]
+    stream = torch.cuda.Stream(device=dev)
+    launches = -(-layers // 64)
+
+    def step():
+        for pr in sets:
+            pa.kv_block_copy(pools, pr)
+
+    g_step = graph_of(step, 1, stream)
+    _device_error_check(pa)
+    time_replays(g_step, max(args.warmup, 3), stream)
+    barrier(dev)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        ms_step = time_replays(g_step, args.steps, stream) / args.steps
+    ms_step = reduce_max(ms_step, dev)
+    _device_error_check(pa)
+    hbm, _, peak_kind = measured_peaks()
+    block_bytes = 16 * hkv * 128 * 2
+    step_bytes = 2 * npairs * layers * 2 * block_bytes * 2     # 2 sets x pairs x layers x (K, V) x (read + write)
+    gbs = step_bytes / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": "KV block copy GB/s (copy-on-write, every layer)", "value": round(world * gbs, 1),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"copy-on-write of {npairs} blocks x 2 pair sets over {layers} layer pools "
+                               f"({nb} blocks of 16 x {hkv} x 128 fp16 each, 896 MiB in total)",
+                   "l2": "each step touches 2 x 64 x 28 distinct 32 KB block copies (117 MB read, 117 MB "
+                         "written); the pools (896 MiB) exceed L2",
+                   "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
+        "gpu_launches": 2 * launches * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs / hbm, 3), "peak_kind": peak_kind, "kernel": "kv_block_copy",
+                     "bytes_per_launch": step_bytes // 2, "launch_ms": round(ms_step / 2, 5),
+                     "traffic": None},
         "clocks": clk.summary(),
     }
     if rank == 0:

@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 3
+#define PA_ABI_VERSION 4
 #define PA_HEAD_DIM 128
 #define PA_BLOCK_SIZE 16
 #define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
@@ -62,7 +62,10 @@ typedef enum {
   PA_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed (see pa_last_cuda_error) */
   PA_ERR_RANGE = -7,       /* device: block id / slot / context length out of range */
   PA_ERR_TIMEOUT = -8,     /* device: a bounded wait on an asynchronous copy gave up */
-  PA_ERR_ALIGN = -9        /* a pointer is not 16-byte aligned */
+  PA_ERR_ALIGN = -9,       /* a pointer is not 16-byte aligned */
+  PA_ERR_NO_BLOCKS = -10,  /* allocator: not enough free blocks (nothing was allocated) */
+  PA_ERR_STATE = -11       /* allocator: a call out of order (release of a free block, commit beyond
+                              the reservation, adopt or fork into a non-empty sequence, ...) */
 } pa_status;
 
 /*
@@ -281,6 +284,115 @@ PA_API pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t
                                                     int32_t num_q_heads, int32_t total_q_tokens,
                                                     int32_t max_chunk_len, float scale, int32_t window,
                                                     void *out, pa_stream_t stream);
+
+/*
+ * ---- copy-on-write and the block-table builder [P1, qwen_serve/paged.py:
+ * BlockAllocator, SequenceCache.fork_from / _cow_copy / adopt_prefix /
+ * reserve / commit; task 12.1 worked examples and acceptance item 5] --------
+ */
+
+/*
+ * kv_block_copy — [P1, SequenceCache._cow_copy: k[:, dst] = k[:, src] and the
+ * same for v, over every layer]: for each pair i and each of num_layers
+ * pools, copy physical block pairs[2i] (src) onto block pairs[2i + 1] (dst)
+ * in both k_cache and v_cache.  A bit copy.
+ *   pools      HOST array [num_layers] of layer pools with one geometry
+ *              (num_blocks, num_kv_heads, dtype); read during the call.
+ *   pairs      DEVICE int32 [num_pairs][2] (src, dst).  The dst blocks must
+ *              be distinct and none may be a src of the same call (as with
+ *              blocks fresh from the allocator); otherwise the result is
+ *              undefined.  src == dst is a no-op.
+ * A pair with a block outside [0, num_blocks) records PA_ERR_RANGE (detail:
+ * the pair index) and is skipped.  num_pairs == 0 is a no-op.
+ */
+PA_API pa_status pa_kv_block_copy(const pa_kv_pool *pools, int32_t num_layers, const int32_t *pairs,
+                                  int32_t num_pairs, pa_stream_t stream);
+
+/*
+ * Host-side block allocator and per-sequence block tables (pure host code:
+ * none of these calls touches the GPU; not thread-safe — one thread per
+ * allocator and its sequences).
+ *
+ * pa_allocator: a pool of num_blocks block ids with a reference count each;
+ * free ids are handed out first-in first-out (ids 0, 1, 2, ... on a new
+ * allocator) and a released id goes to the back of the free list.
+ * pa_sequence: one request's block table and committed length.  reserve()
+ * makes room for the next tokens and returns their flat slots; the caller
+ * writes their K/V (pa_kv_cache_write) and then commit()s them.  fork()
+ * shares every block of another sequence by reference (+1 each); the first
+ * reserve() that writes into a shared, partly filled block replaces it with a
+ * fresh copy (copy-on-write): the allocator records the (src, dst) pair,
+ * which the caller takes with pa_allocator_take_copies() and enqueues with
+ * pa_kv_block_copy() before that step's KV write.
+ */
+typedef struct pa_allocator pa_allocator;
+typedef struct pa_sequence pa_sequence;
+
+typedef struct {
+  int32_t total;         /* num_blocks */
+  int32_t free;          /* ids in the free list */
+  int32_t used;          /* ids with refcount > 0 (used + free == total) */
+  int32_t shared;        /* ids with refcount > 1 */
+  int64_t n_allocated;   /* ids handed out so far */
+  int64_t n_cow;         /* copy-on-write events so far */
+} pa_allocator_stats;
+
+/* A new allocator of num_blocks (>= 1) ids, all free; *out receives it. */
+PA_API pa_status pa_allocator_create(int32_t num_blocks, pa_allocator **out);
+/* Frees the allocator (its sequences must be destroyed first). */
+PA_API void pa_allocator_destroy(pa_allocator *alloc);
+/* n ids with refcount 1 into out[0..n); all or nothing: PA_ERR_NO_BLOCKS if
+ * fewer than n are free (the pages' OutOfBlocks). */
+PA_API pa_status pa_allocator_allocate(pa_allocator *alloc, int32_t n, int32_t *out);
+/* +1 on an id in use; PA_ERR_STATE on a free id, PA_ERR_RANGE outside the pool. */
+PA_API pa_status pa_allocator_retain(pa_allocator *alloc, int32_t block);
+/* -1; at 0 the id returns to the back of the free list.  PA_ERR_STATE on a free id. */
+PA_API pa_status pa_allocator_release(pa_allocator *alloc, int32_t block);
+/* Reference count of an id (-1 outside the pool). */
+PA_API int32_t pa_allocator_refcount(const pa_allocator *alloc, int32_t block);
+PA_API pa_status pa_allocator_stats_get(const pa_allocator *alloc, pa_allocator_stats *out);
+/* Moves the recorded copy-on-write pairs (src, dst) into pairs[0 .. 2 *num):
+ * *num receives their count.  If capacity (in pairs) is too small, nothing
+ * is moved, *num receives the count needed and PA_ERR_SHAPE is returned. */
+PA_API pa_status pa_allocator_take_copies(pa_allocator *alloc, int32_t *pairs, int32_t capacity, int32_t *num);
+
+/* A new, empty sequence on `alloc`; *out receives it. */
+PA_API pa_status pa_sequence_create(pa_allocator *alloc, pa_sequence **out);
+/* Releases the sequence's blocks and frees it. */
+PA_API void pa_sequence_destroy(pa_sequence *seq);
+/* Room for n more tokens after the committed and already reserved ones:
+ * allocates the blocks they need (and the copy of a shared partly filled
+ * block they would write into); writes the n flat slots (block * 16 +
+ * offset) into slots (may be NULL).  All or nothing (PA_ERR_NO_BLOCKS). */
+PA_API pa_status pa_sequence_reserve(pa_sequence *seq, int32_t n, int64_t *slots);
+/* Marks the first n reserved tokens as written (n <= reserved, else PA_ERR_STATE). */
+PA_API pa_status pa_sequence_commit(pa_sequence *seq, int32_t n);
+/* Starts an empty sequence on n full blocks in use elsewhere (a shared
+ * prefix): each gains a reference; length = 16 n.  PA_ERR_STATE if the
+ * sequence is not empty or a block is free. */
+PA_API pa_status pa_sequence_adopt_prefix(pa_sequence *seq, const int32_t *blocks, int32_t n);
+/* Makes the empty sequence `seq` a copy of `other` (same allocator, nothing
+ * reserved): every block is shared by reference, the length is copied. */
+PA_API pa_status pa_sequence_fork(pa_sequence *seq, const pa_sequence *other);
+/* Releases every block; the sequence is empty again. */
+PA_API pa_status pa_sequence_release(pa_sequence *seq);
+/* Committed tokens, reserved-but-uncommitted tokens, and blocks held. */
+PA_API int32_t pa_sequence_length(const pa_sequence *seq);
+PA_API int32_t pa_sequence_reserved(const pa_sequence *seq);
+PA_API int32_t pa_sequence_num_blocks(const pa_sequence *seq);
+/* Copies the block ids into out[0 .. num_blocks) (capacity must suffice). */
+PA_API pa_status pa_sequence_blocks(const pa_sequence *seq, int32_t *out, int32_t capacity);
+/*
+ * The step's metadata for the attention calls, into HOST arrays: for
+ * sequence i, block_tables[i][0 .. max_blocks) = its block ids padded with -1,
+ * chunk_starts[i] = committed length, chunk_lens[i] = reserved tokens and
+ * context_lens[i] = their sum (a decode sequence reserves 1).  Any of the
+ * last three may be NULL.  PA_ERR_SHAPE if a sequence holds more than
+ * max_blocks blocks.
+ */
+PA_API pa_status pa_build_step_tables(const pa_sequence *const *seqs, int32_t num_seqs, int32_t max_blocks,
+                                      int32_t *block_tables, int32_t *chunk_starts, int32_t *chunk_lens,
+                                      int32_t *context_lens);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's error

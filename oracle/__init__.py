@@ -64,6 +64,8 @@ def open_library(path: str):
     lib.oracle_bf16_to_f64.restype = f64
     lib.oracle_kv_cache_write.argtypes = [P, P, i64, i32, i32, i32, P, P, P, i64]
     lib.oracle_kv_cache_write.restype = i64
+    lib.oracle_kv_block_copy.argtypes = [P, P, i64, i32, i32, i32, P, i64]
+    lib.oracle_kv_block_copy.restype = i64
     lib.oracle_gather_head.argtypes = [P, P, ctypes.c_int, i64, i32, i32, i32, P, i32, i32, P, P]
     lib.oracle_gather_head.restype = ctypes.c_int
     lib.oracle_paged_attn_decode.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, i32, P,
@@ -162,6 +164,23 @@ def kv_cache_write(k_cache, v_cache, k, v, slot_mapping) -> int:
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     return int(_load().oracle_kv_cache_write(_ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d,
                                              _ptr(kb), _ptr(vb), _ptr(sm), sm.shape[0]))
+
+
+def kv_block_copy(k_pools, v_pools, pairs) -> int:
+    """Copy-on-write block copy ("Модуль 12", qwen_serve/paged.py,
+    SequenceCache._cow_copy): in every layer's pool (uint16 bit arrays
+    [num_blocks, block_size, Hkv, d], modified in place) block dst receives
+    block src, for each (src, dst) row of ``pairs`` in order.  Returns the
+    number of pairs skipped (a block id outside the pool)."""
+    pr = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+    skipped = 0
+    for k_cache, v_cache in zip(k_pools, v_pools):
+        assert k_cache.dtype == np.uint16 and v_cache.dtype == np.uint16
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous and k_cache.shape == v_cache.shape
+        nb, bs, hkv, d = k_cache.shape
+        skipped = int(_load().oracle_kv_block_copy(_ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d, _ptr(pr),
+                                                   pr.shape[0]))
+    return skipped
 
 
 def gather_head(k_cache, v_cache, dtype: int, block_table_row, kv_head: int, upto: int):

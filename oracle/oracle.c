@@ -116,6 +116,33 @@ int64_t oracle_kv_cache_write(uint16_t *k_cache, uint16_t *v_cache,
   return skipped;
 }
 
+/* ---- copy-on-write block copy [P1, SequenceCache._cow_copy] --------------- */
+
+/*
+ * The page copies a shared block for the sequence that writes into it: the
+ * fresh block receives every layer's K and V of the old one, k[:, dst] =
+ * k[:, src].  This is one layer of that: for each pair i in order, block
+ * pairs[2i + 1] of k_cache and v_cache receives block pairs[2i].  Returns the
+ * number of pairs skipped because a block id lies outside [0, num_blocks).
+ */
+int64_t oracle_kv_block_copy(uint16_t *k_cache, uint16_t *v_cache, int64_t num_blocks, int32_t block_size,
+                             int32_t num_kv_heads, int32_t head_dim, const int32_t *pairs, int64_t num_pairs) {
+  const int64_t per_block = (int64_t)block_size * num_kv_heads * head_dim;
+  int64_t skipped = 0;
+  for (int64_t i = 0; i < num_pairs; ++i) {
+    const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      ++skipped;
+      continue;
+    }
+    for (int64_t x = 0; x < per_block; ++x) {
+      k_cache[dst * per_block + x] = k_cache[src * per_block + x];
+      v_cache[dst * per_block + x] = v_cache[src * per_block + x];
+    }
+  }
+  return skipped;
+}
+
 /* ---- gather read [P1, PagedKVCache.read] ----------------------------------- */
 
 /*

@@ -13,6 +13,10 @@ Calls (see include/pagedattn.h for the full contract):
   block_tables, context_lens, scale, ...)``
 * ``kv_cache_write_q8`` / ``paged_attn_decode_q8`` on an int8 pool
   (``alloc_pool_q8``: codes plus one fp32 scale per token and KV head)
+* ``paged_attn_decode_window`` / ``paged_attn_prefill_chunk_window``: sliding window
+* ``kv_block_copy(pools, pairs)``: copy-on-write block copy over every layer
+* ``BlockAllocator`` / ``Sequence`` / ``build_step_tables``: the host-side block
+  allocator and block-table builder (native code in the same library; no GPU)
 * ``get_device_error()``
 """
 from __future__ import annotations
@@ -31,13 +35,18 @@ PA_F16, PA_BF16 = 0, 1
 PA_OK = 0
 STATUS = {0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_DTYPE", -4: "PA_ERR_UNSUPPORTED",
           -5: "PA_ERR_WORKSPACE", -6: "PA_ERR_CUDA", -7: "PA_ERR_RANGE", -8: "PA_ERR_TIMEOUT",
-          -9: "PA_ERR_ALIGN"}
+          -9: "PA_ERR_ALIGN", -10: "PA_ERR_NO_BLOCKS", -11: "PA_ERR_STATE"}
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_decode",
            "pa_paged_attn_prefill_chunk", "pa_get_device_error", "pa_status_string",
            "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc",
            "pa_decode_kernel_launches", "pa_kv_cache_write_q8", "pa_paged_attn_decode_q8",
-           "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window")
+           "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
+           "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
+           "pa_allocator_release", "pa_allocator_refcount", "pa_allocator_stats_get", "pa_allocator_take_copies",
+           "pa_sequence_create", "pa_sequence_destroy", "pa_sequence_reserve", "pa_sequence_commit",
+           "pa_sequence_adopt_prefix", "pa_sequence_fork", "pa_sequence_release", "pa_sequence_length",
+           "pa_sequence_reserved", "pa_sequence_num_blocks", "pa_sequence_blocks", "pa_build_step_tables")
 
 
 class PagedAttnError(RuntimeError):
@@ -58,6 +67,11 @@ class KVPoolQ8(ctypes.Structure):
                 ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
                 ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class AllocatorStats(ctypes.Structure):
+    _fields_ = [("total", ctypes.c_int32), ("free", ctypes.c_int32), ("used", ctypes.c_int32),
+                ("shared", ctypes.c_int32), ("n_allocated", ctypes.c_int64), ("n_cow", ctypes.c_int64)]
 
 
 _lib = None
@@ -103,6 +117,24 @@ def load_library(path: str = LIB_PATH):
         lib.pa_paged_attn_prefill_chunk_window.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
                                                            ctypes.c_float, i32, P, P]
         lib.pa_paged_attn_prefill_chunk_window.restype = i32
+        lib.pa_kv_block_copy.argtypes = [pool_p, i32, P, i32, P]
+        lib.pa_kv_block_copy.restype = i32
+        ip = ctypes.POINTER(i32)
+        for name, args, res in (
+                ("pa_allocator_create", [i32, ctypes.POINTER(P)], i32), ("pa_allocator_destroy", [P], None),
+                ("pa_allocator_allocate", [P, i32, ip], i32), ("pa_allocator_retain", [P, i32], i32),
+                ("pa_allocator_release", [P, i32], i32), ("pa_allocator_refcount", [P, i32], i32),
+                ("pa_allocator_stats_get", [P, ctypes.POINTER(AllocatorStats)], i32),
+                ("pa_allocator_take_copies", [P, ip, i32, ip], i32),
+                ("pa_sequence_create", [P, ctypes.POINTER(P)], i32), ("pa_sequence_destroy", [P], None),
+                ("pa_sequence_reserve", [P, i32, ctypes.POINTER(i64)], i32),
+                ("pa_sequence_commit", [P, i32], i32), ("pa_sequence_adopt_prefix", [P, ip, i32], i32),
+                ("pa_sequence_fork", [P, P], i32), ("pa_sequence_release", [P], i32),
+                ("pa_sequence_length", [P], i32), ("pa_sequence_reserved", [P], i32),
+                ("pa_sequence_num_blocks", [P], i32), ("pa_sequence_blocks", [P, ip, i32], i32),
+                ("pa_build_step_tables", [ctypes.POINTER(P), i32, i32, ip, ip, ip, ip], i32)):
+            fn = getattr(lib, name)
+            fn.argtypes, fn.restype = args, res
         lib.pa_get_device_error.argtypes = [P, ctypes.POINTER(i32)]
         lib.pa_get_device_error.restype = i32
         lib.pa_status_string.argtypes = [i32]
@@ -397,3 +429,149 @@ def raise_device_error(stream=None) -> None:
     st, detail = get_device_error(stream)
     if st != PA_OK:
         raise PagedAttnError(st, f"device error (index {detail})")
+
+
+# ---- copy-on-write block copy and the host-side block-table builder ---------------------
+
+def kv_block_copy(pools, pairs: torch.Tensor, stream=None) -> None:
+    """Copy block src onto block dst in K and V of every layer pool, for each
+    row (src, dst) of ``pairs`` (int32 [n, 2] on the device).  ``pools`` is a
+    sequence of (k_cache, v_cache) layer pools of one geometry."""
+    descs = [make_pool(k, v) for k, v in pools]
+    _need(pairs, "pairs", torch.int32)
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be [n, 2] (src, dst)")
+    arr = (KVPool * max(len(descs), 1))(*descs)
+    _check(load_library().pa_kv_block_copy(arr, len(descs), pairs.data_ptr(), pairs.shape[0], _stream(stream)),
+           "pa_kv_block_copy")
+
+
+class BlockAllocator:
+    """Host-side pool of ``num_blocks`` block ids with reference counts (the
+    library's native allocator; no GPU involved)."""
+
+    def __init__(self, num_blocks: int):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check(self._lib.pa_allocator_create(num_blocks, ctypes.byref(h)), "pa_allocator_create")
+        self._h = h
+        self._seqs = []
+
+    @property
+    def handle(self):
+        return self._h
+
+    def allocate(self, n: int = 1):
+        out = (ctypes.c_int32 * max(n, 1))()
+        _check(self._lib.pa_allocator_allocate(self._h, n, out), "pa_allocator_allocate")
+        return list(out[:n])
+
+    def retain(self, block: int) -> None:
+        _check(self._lib.pa_allocator_retain(self._h, block), "pa_allocator_retain")
+
+    def release(self, block: int) -> None:
+        _check(self._lib.pa_allocator_release(self._h, block), "pa_allocator_release")
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pa_allocator_refcount(self._h, block))
+
+    def stats(self) -> dict:
+        st = AllocatorStats()
+        _check(self._lib.pa_allocator_stats_get(self._h, ctypes.byref(st)), "pa_allocator_stats_get")
+        return {name: int(getattr(st, name)) for name, _ in AllocatorStats._fields_}
+
+    def take_copies(self):
+        """The recorded copy-on-write pairs [(src, dst), ...], cleared."""
+        n = ctypes.c_int32()
+        st = self._lib.pa_allocator_take_copies(self._h, None, 0, ctypes.byref(n))
+        if st == PA_OK and n.value == 0:
+            return []
+        buf = (ctypes.c_int32 * (2 * n.value))()
+        _check(self._lib.pa_allocator_take_copies(self._h, buf, n.value, ctypes.byref(n)),
+               "pa_allocator_take_copies")
+        return [(buf[2 * i], buf[2 * i + 1]) for i in range(n.value)]
+
+    def sequence(self) -> "Sequence":
+        return Sequence(self)
+
+    def close(self) -> None:
+        if self._h:
+            for s in self._seqs:
+                s.close()
+            self._lib.pa_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Sequence:
+    """One request's block table and committed length on a BlockAllocator."""
+
+    def __init__(self, alloc: BlockAllocator):
+        self._lib, self.alloc = alloc._lib, alloc
+        h = ctypes.c_void_p()
+        _check(self._lib.pa_sequence_create(alloc.handle, ctypes.byref(h)), "pa_sequence_create")
+        self._h = h
+        alloc._seqs.append(self)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def reserve(self, n: int):
+        """Room for n more tokens; returns their flat slots (block * 16 + offset)."""
+        slots = (ctypes.c_int64 * max(n, 1))()
+        _check(self._lib.pa_sequence_reserve(self._h, n, slots), "pa_sequence_reserve")
+        return list(slots[:n])
+
+    def commit(self, n: int) -> None:
+        _check(self._lib.pa_sequence_commit(self._h, n), "pa_sequence_commit")
+
+    def adopt_prefix(self, blocks) -> None:
+        arr = (ctypes.c_int32 * max(len(blocks), 1))(*blocks)
+        _check(self._lib.pa_sequence_adopt_prefix(self._h, arr, len(blocks)), "pa_sequence_adopt_prefix")
+
+    def fork_from(self, other: "Sequence") -> None:
+        _check(self._lib.pa_sequence_fork(self._h, other.handle), "pa_sequence_fork")
+
+    def release(self) -> None:
+        _check(self._lib.pa_sequence_release(self._h), "pa_sequence_release")
+
+    @property
+    def length(self) -> int:
+        return int(self._lib.pa_sequence_length(self._h))
+
+    @property
+    def reserved(self) -> int:
+        return int(self._lib.pa_sequence_reserved(self._h))
+
+    @property
+    def blocks(self):
+        n = int(self._lib.pa_sequence_num_blocks(self._h))
+        out = (ctypes.c_int32 * max(n, 1))()
+        _check(self._lib.pa_sequence_blocks(self._h, out, n), "pa_sequence_blocks")
+        return list(out[:n])
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.pa_sequence_destroy(self._h)
+            self._h = None
+
+
+def build_step_tables(seqs, max_blocks: int):
+    """Host int32 arrays for the step's attention calls: block tables
+    [n, max_blocks] (-1 padded), chunk starts (committed lengths), chunk lens
+    (reserved tokens) and context lens (their sums)."""
+    import numpy as np
+    n = len(seqs)
+    bt = np.empty((max(n, 1), max_blocks), np.int32)
+    starts, lens, ctx = (np.empty(max(n, 1), np.int32) for _ in range(3))
+    handles = (ctypes.c_void_p * max(n, 1))(*[s.handle for s in seqs])
+    ip = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    _check(load_library().pa_build_step_tables(handles, n, max_blocks, ip(bt), ip(starts), ip(lens), ip(ctx)),
+           "pa_build_step_tables")
+    return bt[:n], starts[:n], lens[:n], ctx[:n]

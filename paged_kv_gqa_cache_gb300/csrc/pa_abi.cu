@@ -226,6 +226,8 @@ const char *pa_status_string(int32_t status) {
     case PA_ERR_RANGE: return "PA_ERR_RANGE: block id, slot or length out of range";
     case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded wait gave up";
     case PA_ERR_ALIGN: return "PA_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case PA_ERR_NO_BLOCKS: return "PA_ERR_NO_BLOCKS: not enough free blocks";
+    case PA_ERR_STATE: return "PA_ERR_STATE: allocator call out of order";
     default: return "unknown pa_status";
   }
 }
@@ -398,6 +400,39 @@ pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts
   return pa_paged_attn_prefill_chunk_window(q, chunk_starts, chunk_lens, pool, block_tables, max_blocks_per_seq,
                                             context_lens, num_chunks, num_q_heads, total_q_tokens, max_chunk_len,
                                             scale, 0, out, stream);
+}
+
+pa_status pa_kv_block_copy(const pa_kv_pool *pools, int32_t num_layers, const int32_t *pairs, int32_t num_pairs,
+                           pa_stream_t stream) {
+  if (num_layers < 0 || num_pairs < 0) return PA_ERR_SHAPE;
+  if (num_layers == 0 || num_pairs == 0) return PA_OK;
+  if (!pools || !pairs) return PA_ERR_NULL;
+  if (!aligned4(pairs)) return PA_ERR_ALIGN;
+  for (int32_t l = 0; l < num_layers; ++l) {
+    pa_status st = check_pool(&pools[l]);
+    if (st != PA_OK) return st;
+    if (pools[l].num_blocks != pools[0].num_blocks || pools[l].num_kv_heads != pools[0].num_kv_heads ||
+        pools[l].dtype != pools[0].dtype)
+      return PA_ERR_SHAPE;
+  }
+  DeviceState *d = nullptr;
+  pa_status st = device_state(&d);
+  if (st != PA_OK) return st;
+  BlockCopyParams p{};
+  p.pairs = pairs;
+  p.err = d->err;
+  p.num_blocks = pools[0].num_blocks;
+  p.block_vecs = kBlock * pools[0].num_kv_heads * kHeadDim * 2 / 16;
+  for (int32_t l0 = 0; l0 < num_layers; l0 += kCopyLayers) {  // up to kCopyLayers layers per launch
+    const int n = num_layers - l0 < kCopyLayers ? num_layers - l0 : kCopyLayers;
+    for (int i = 0; i < n; ++i) {
+      p.k[i] = pools[l0 + i].k_cache;
+      p.v[i] = pools[l0 + i].v_cache;
+    }
+    cudaError_t e = launch_block_copy(p, n, num_pairs, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return PA_OK;
 }
 
 pa_status pa_get_device_error(pa_stream_t stream, int32_t *detail) {

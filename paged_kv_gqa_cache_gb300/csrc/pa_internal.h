@@ -49,6 +49,18 @@ struct WriteQ8Params {
 };
 cudaError_t launch_kv_write_q8(const WriteQ8Params &p, int dtype, cudaStream_t stream);
 
+// ---- copy-on-write block copy ---------------------------------------------------------
+constexpr int kCopyLayers = 64;          // layer pools per launch
+struct BlockCopyParams {
+  void *k[kCopyLayers];                  // per layer: pool base addresses
+  void *v[kCopyLayers];
+  const int32_t *pairs;                  // [num_pairs][2] (src, dst)
+  int *err;
+  int32_t num_blocks;
+  int32_t block_vecs;                    // 16-byte vectors per block (16 * Hkv * 128 * 2 / 16)
+};
+cudaError_t launch_block_copy(const BlockCopyParams &p, int num_layers, int num_pairs, cudaStream_t stream);
+
 // ---- decode (split-K over a balanced page range per warp) -----------------------
 constexpr int kDecodeWarps = 4;         // warps per CTA; each warp is an independent worker
 constexpr int kDecodeMaxWorkers = 8192; // upper bound on workers (warps) per launch
