@@ -66,6 +66,9 @@ def parse_args(argv=None):
     ap.add_argument("--block-copy", action="store_true",
                     help="diagnostic line for the copy-on-write block copy: 64 (src, dst) pairs over the 28 "
                          "layer pools of the Qwen3-0.6B geometry (512 blocks of 16 x 8 x 128 fp16 each)")
+    ap.add_argument("--fused-write", action="store_true",
+                    help="diagnostic line for q/k RMSNorm + rotary embedding fused into the KV write: the mixed "
+                         "step's 2048 new tokens (Qwen3-0.6B: 16 query / 8 KV heads, bf16) in each of 28 layers")
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
                     help="2 = the Qwen3-0.6B 28-layer decode step (default); 3, 4, 5 = the mixed prefill "
                          "step, the Qwen3-8B decode and the prefix-shared long tail (diagnostic lines)")
@@ -464,6 +467,8 @@ def run_ours(args):
     import paged_kv_gqa_cache_gb300 as pa
     if args.block_copy:
         return run_block_copy(args, dev, pa)
+    if args.fused_write:
+        return run_fused_write(args, dev, pa)
     if args.workload == 3:
         return run_mixed(args, dev, pa)
 
@@ -625,6 +630,69 @@ def run_block_copy(args, dev, pa):
                      "frac": round(gbs / hbm, 3), "peak_kind": peak_kind, "kernel": "kv_block_copy",
                      "bytes_per_launch": step_bytes // 2, "launch_ms": round(ms_step / 2, 5),
                      "traffic": None},
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_fused_write(args, dev, pa):
+    """Diagnostic line for the q/k RMSNorm + rotary embedding fused into the KV write."""
+    import numpy as np
+    import torch
+    rank, world, _ = dist_env()
+    layers, T, hq, hkv, nb, max_pos = 28, 2048, 16, 8, 512, 4096
+    g = torch.Generator(device=dev).manual_seed(11)
+    bf = torch.bfloat16
+    ins = [dict(q=torch.randn((T, hq, 128), generator=g, device=dev).to(bf),
+                k=torch.randn((T, hkv, 128), generator=g, device=dev).to(bf),
+                v=torch.randn((T, hkv, 128), generator=g, device=dev).to(bf),
+                wq=(1 + 0.1 * torch.randn(128, generator=g, device=dev)).to(bf),
+                wk=(1 + 0.1 * torch.randn(128, generator=g, device=dev)).to(bf),
+                kc=torch.zeros((nb, 16, hkv, 128), device=dev, dtype=bf),
+                vc=torch.zeros((nb, 16, hkv, 128), device=dev, dtype=bf)) for _ in range(layers)]
+    q_out = [torch.empty_like(x["q"]) for x in ins]
+    inv = 1.0 / (1e6 ** (torch.arange(0, 128, 2, dtype=torch.float32) / 128))
+    f = torch.outer(torch.arange(max_pos, dtype=torch.float32), inv)
+    cos = torch.cat([f.cos(), f.cos()], -1).to(bf).to(dev)
+    sin = torch.cat([f.sin(), f.sin()], -1).to(bf).to(dev)
+    rng = np.random.default_rng(11)
+    pos = torch.from_numpy(np.concatenate([np.arange(0, 512), np.arange(512, 1024), np.arange(1536, 2048),
+                                           rng.integers(16, 1024, size=512)]).astype(np.int32)).to(dev)
+    slots = torch.from_numpy(rng.permutation(nb * 16)[:T].astype(np.int64)).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for l, x in enumerate(ins):
+            pa.qk_norm_rope_kv_write(x["q"], x["k"], x["v"], x["wq"], x["wk"], 1e-6, cos, sin, pos, slots,
+                                     x["kc"], x["vc"], q_out=q_out[l])
+
+    g_step = graph_of(step, 1, stream)
+    _device_error_check(pa)
+    time_replays(g_step, max(args.warmup, 3), stream)
+    barrier(dev)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        ms_step = time_replays(g_step, args.steps, stream) / args.steps
+    ms_step = reduce_max(ms_step, dev)
+    _device_error_check(pa)
+    hbm, _, peak_kind = measured_peaks()
+    # q read + q_out written, k and v read + written into the pool, each token's cos and sin rows read
+    launch_bytes = T * (2 * hq * 256 + 4 * hkv * 256 + 2 * 256)
+    gbs = layers * launch_bytes / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": "q/k RMSNorm + RoPE + KV write GB/s", "value": round(world * gbs, 1), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{T} new tokens per layer (chunks of 512 at prefixes 0, 512, 1536 + 512 decode "
+                               f"tokens), Hq={hq}, Hkv={hkv}, d=128, bf16, {layers} layers with their own inputs "
+                               f"and pools, rotary tables of {max_pos} positions (theta 1e6)",
+                   "l2": f"{layers} layers x {launch_bytes / 1e6:.1f} MB of distinct inputs and outputs per step",
+                   "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
+        "gpu_launches": layers * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs / hbm, 3), "peak_kind": peak_kind, "kernel": "qk_norm_rope_kv_write",
+                     "bytes_per_launch": launch_bytes, "launch_ms": round(ms_step / layers, 5), "traffic": None},
         "clocks": clk.summary(),
     }
     if rank == 0:

@@ -286,6 +286,36 @@ PA_API pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t
                                                     void *out, pa_stream_t stream);
 
 /*
+ * qk_norm_rope_kv_write — [P1, qwen_serve/model.py: rms_norm, _rotate_half,
+ * apply_rope and Qwen3Model.forward (q_norm / k_norm, then the rotary embedding
+ * at each token's absolute position, then PagedKVCache.write); P2 section 4:
+ * the key is rotated before it is stored]: for each new token t,
+ *   q_out[t][g] = rope(rms_norm(q[t][g], q_norm_weight), positions[t])  (every query head g),
+ *   slot_mapping[t] receives K = rope(rms_norm(k[t][h], k_norm_weight), positions[t]) and V = v[t][h].
+ * rms_norm(x, w) = round(round(x * inv) * w), inv = rsqrt(mean(x^2) + eps) in
+ * fp32 (the fp32 mean nearest the exact one, a correctly rounded reciprocal
+ * square root); rope(z) = round(round(z * cos) + round(rotate_half(z) * sin))
+ * with rotate_half(z) = (-z[64..128), z[0..64)) (NeoX layout), the tables'
+ * row positions[t]; round() is to the pool dtype, ties to even, and every
+ * product and sum is exact in fp32 before it.  The result is bit-exact.
+ *   q, q_out      [num_tokens][num_q_heads][128], pool dtype; q_out may be q.
+ *   k, v          [num_tokens][num_kv_heads][128], pool dtype.
+ *   q_norm_weight, k_norm_weight  [128], pool dtype.
+ *   cos_table, sin_table  [max_position][128], pool dtype (the caller's
+ *                 rotary tables, e.g. theta^(-2i/128) frequencies, halves duplicated).
+ *   positions     int32 [num_tokens] absolute positions; slot_mapping int64
+ *                 [num_tokens] as for pa_kv_cache_write.
+ * A token whose position lies outside [0, max_position) or whose slot lies
+ * outside the pool records PA_ERR_RANGE (detail: the token) and nothing of it
+ * is written.  All pointers 16-byte aligned (positions 4, slot_mapping 8).
+ */
+PA_API pa_status pa_qk_norm_rope_kv_write(const void *q, const void *k, const void *v, const void *q_norm_weight,
+                                          const void *k_norm_weight, float eps, const void *cos_table,
+                                          const void *sin_table, int32_t max_position, const int32_t *positions,
+                                          const int64_t *slot_mapping, int32_t num_tokens, int32_t num_q_heads,
+                                          void *q_out, const pa_kv_pool *pool, pa_stream_t stream);
+
+/*
  * ---- copy-on-write and the block-table builder [P1, qwen_serve/paged.py:
  * BlockAllocator, SequenceCache.fork_from / _cow_copy / adopt_prefix /
  * reserve / commit; task 12.1 worked examples and acceptance item 5] --------

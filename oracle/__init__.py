@@ -64,6 +64,11 @@ def open_library(path: str):
     lib.oracle_bf16_to_f64.restype = f64
     lib.oracle_kv_cache_write.argtypes = [P, P, i64, i32, i32, i32, P, P, P, i64]
     lib.oracle_kv_cache_write.restype = i64
+    lib.oracle_f64_to_16.argtypes = [f64, ctypes.c_int]
+    lib.oracle_f64_to_16.restype = ctypes.c_uint16
+    lib.oracle_qk_norm_rope_kv_write.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, i32, P, P, i64, i32, i32,
+                                                 P, P, P, i64, i32, i32, i32]
+    lib.oracle_qk_norm_rope_kv_write.restype = i64
     lib.oracle_kv_block_copy.argtypes = [P, P, i64, i32, i32, i32, P, i64]
     lib.oracle_kv_block_copy.restype = i64
     lib.oracle_gather_head.argtypes = [P, P, ctypes.c_int, i64, i32, i32, i32, P, i32, i32, P, P]
@@ -164,6 +169,35 @@ def kv_cache_write(k_cache, v_cache, k, v, slot_mapping) -> int:
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     return int(_load().oracle_kv_cache_write(_ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d,
                                              _ptr(kb), _ptr(vb), _ptr(sm), sm.shape[0]))
+
+
+def f64_to_16(x: float, dtype: int) -> int:
+    """The 16-bit pattern nearest to x (ties to even)."""
+    return int(_load().oracle_f64_to_16(float(x), dtype))
+
+
+def qk_norm_rope_kv_write(q, k, v, q_weight, k_weight, eps: float, cos_table, sin_table, positions,
+                          slot_mapping, k_cache, v_cache, dtype: int):
+    """q/k RMSNorm and rotary embedding at absolute positions, then the KV write
+    ("Модуль 12", qwen_serve/model.py rms_norm / apply_rope / Qwen3Model.forward;
+    "Модуль 04" section 4: rotate before storing), at the page's rounding points.
+
+    q [T, Hq, d], k, v [T, Hkv, d], weights [d], tables [max_position, d]: 16-bit
+    bit patterns.  k_cache, v_cache (uint16 pools) are modified in place.
+    Returns (q_out bits [T, Hq, d], number of skipped tokens)."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    wq, wk, cs, sn = _bits(q_weight), _bits(k_weight), _bits(cos_table), _bits(sin_table)
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    T, hq, d = qb.shape
+    nb, bs, hkv, dk = k_cache.shape
+    assert dk == d and kb.shape == (T, hkv, d) and vb.shape == (T, hkv, d) and cs.shape[1] == d
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    out = np.zeros_like(qb)
+    skipped = _load().oracle_qk_norm_rope_kv_write(
+        _ptr(qb), _ptr(kb), _ptr(vb), _ptr(wq), _ptr(wk), eps, _ptr(cs), _ptr(sn), cs.shape[0], _ptr(pos),
+        _ptr(sm), T, hq, dtype, _ptr(out), _ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d)
+    return out, int(skipped)
 
 
 def kv_block_copy(k_pools, v_pools, pairs) -> int:

@@ -36,6 +36,14 @@
  * layout, one fp32 scale per (token, KV head) for K and one for V.  The
  * quantising write and the dequantising read follow the pages' fp32 steps
  * exactly; attention then runs in fp64 on the dequantised values.
+ *
+ * q/k RMSNorm and rotary embedding before the write [P1 qwen_serve/model.py:
+ * rms_norm, _rope_tables, _rotate_half, apply_rope and their use in
+ * Qwen3Model.forward; P2 section 4: the key is rotated to its absolute position
+ * before it is stored].  These steps have their precision fixed by the page:
+ * the mean of squares and the reciprocal square root in fp32, every other
+ * operation a 16-bit tensor operation (computed exactly, rounded once to the
+ * 16-bit format, ties to even).  The oracle takes the same rounding points.
  */
 #include <math.h>
 #include <pthread.h>
@@ -84,6 +92,39 @@ static double widen(uint16_t bits, int dtype) {
   return dtype == ORACLE_BF16 ? oracle_bf16_to_f64(bits) : oracle_f16_to_f64(bits);
 }
 
+/*
+ * The 16-bit value nearest to x, ties to even (IEEE round to nearest): with f
+ * fraction bits and exponent bias b, a finite value of magnitude in
+ * [2^(e), 2^(e+1)) for e >= 1 - b is a multiple of 2^(e - f); below 2^(1 - b)
+ * (subnormal) of 2^(1 - b - f).  Magnitudes that round beyond the largest
+ * finite value become infinity.
+ */
+uint16_t oracle_f64_to_16(double x, int dtype) {
+  const int f = dtype == ORACLE_BF16 ? 7 : 10;
+  const int b = dtype == ORACLE_BF16 ? 127 : 15;
+  const int emax = dtype == ORACLE_BF16 ? 127 : 15;          /* largest unbiased exponent */
+  const uint16_t sign = signbit(x) ? (uint16_t)0x8000 : 0;
+  const uint16_t inf = (uint16_t)((2 * emax + 1) << f);      /* exponent field all ones */
+  if (isnan(x)) return (uint16_t)(sign | inf | (1 << (f - 1)));
+  double a = fabs(x);
+  if (isinf(a)) return (uint16_t)(sign | inf);
+  int e2;
+  frexp(a, &e2);                                             /* a = m 2^e2, m in [0.5, 1) */
+  int e = a == 0.0 ? 1 - b : e2 - 1;
+  if (e < 1 - b) e = 1 - b;
+  const double quantum = ldexp(1.0, e - f);
+  const double r = nearbyint(a / quantum) * quantum;         /* round to nearest, ties to even */
+  if (r == 0.0) return sign;
+  frexp(r, &e2);
+  e = e2 - 1;
+  if (e > emax) return (uint16_t)(sign | inf);
+  if (e < 1 - b) return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, 1 - b - f)));   /* subnormal */
+  const uint16_t frac = (uint16_t)(r / ldexp(1.0, e - f) - ldexp(1.0, f));
+  return (uint16_t)(sign | ((e + b) << f) | frac);
+}
+
+static uint16_t narrow(double x, int dtype) { return oracle_f64_to_16(x, dtype); }
+
 /* ---- KV write [P1, PagedKVCache.write] ------------------------------------- */
 
 /*
@@ -113,6 +154,94 @@ int64_t oracle_kv_cache_write(uint16_t *k_cache, uint16_t *v_cache,
       v_cache[dst + x] = v[t * row + x];
     }
   }
+  return skipped;
+}
+
+/* ---- q/k RMSNorm + rotary embedding, then the KV write ---------------------- */
+
+/*
+ * rms_norm of one head row of head_dim 16-bit values [P1 model.py rms_norm]:
+ * var = mean(x^2) and inv = rsqrt(var + eps), both fp32 (each the fp32 value
+ * nearest the exact one); y = (x * inv) in fp32, rounded to the 16-bit format;
+ * out = y * weight, a 16-bit product.
+ */
+static void rms_norm_row(const uint16_t *x, const uint16_t *weight, float eps, int32_t head_dim, int dtype,
+                         uint16_t *out) {
+  double ss = 0.0;
+  for (int32_t i = 0; i < head_dim; ++i) {
+    const double xi = widen(x[i], dtype);
+    ss += xi * xi;
+  }
+  const float var = (float)(ss / head_dim);
+  const float s = var + eps;
+  const float inv = (float)(1.0 / sqrt((double)s));
+  for (int32_t i = 0; i < head_dim; ++i) {
+    const float y = (float)widen(x[i], dtype) * inv;
+    const uint16_t yb = narrow((double)y, dtype);
+    out[i] = narrow(widen(yb, dtype) * widen(weight[i], dtype), dtype);
+  }
+}
+
+/*
+ * Rotary embedding of one head row at one position [P1 model.py apply_rope,
+ * _rotate_half; tables from _rope_tables, NeoX layout]: with h = head_dim / 2
+ * and rotate_half(z) = (-z[h..), z[..h)), out = z * cos + rotate_half(z) * sin,
+ * each product and the sum a 16-bit tensor operation.
+ */
+static void rope_row(const uint16_t *z, const uint16_t *cos_row, const uint16_t *sin_row, int32_t head_dim,
+                     int dtype, uint16_t *out) {
+  const int32_t h = head_dim / 2;
+  for (int32_t i = 0; i < head_dim; ++i) {
+    const double rot = i < h ? -widen(z[i + h], dtype) : widen(z[i - h], dtype);
+    const uint16_t a = narrow(widen(z[i], dtype) * widen(cos_row[i], dtype), dtype);
+    const uint16_t b = narrow(rot * widen(sin_row[i], dtype), dtype);
+    const float sum = (float)(widen(a, dtype) + widen(b, dtype));
+    out[i] = narrow((double)sum, dtype);
+  }
+}
+
+/*
+ * For each token t in order [P1 Qwen3Model.forward: q_norm/k_norm, then
+ * apply_rope at the token's absolute position, then PagedKVCache.write of the
+ * rotated k and the unchanged v; P2 section 4: rotate before storing]:
+ *   q_out[t][g] = rope(rms_norm(q[t][g], q_weight), positions[t]) for each query head g,
+ *   the pool slot slot_mapping[t] receives rope(rms_norm(k[t][h], k_weight)) and v[t][h].
+ * A token whose position lies outside [0, max_position) or whose slot lies
+ * outside the pool is skipped entirely (nothing written); returns the number
+ * of skipped tokens.
+ */
+int64_t oracle_qk_norm_rope_kv_write(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                     const uint16_t *q_weight, const uint16_t *k_weight, float eps,
+                                     const uint16_t *cos_table, const uint16_t *sin_table, int32_t max_position,
+                                     const int32_t *positions, const int64_t *slot_mapping, int64_t num_tokens,
+                                     int32_t num_q_heads, int32_t dtype, uint16_t *q_out, uint16_t *k_cache,
+                                     uint16_t *v_cache, int64_t num_blocks, int32_t block_size,
+                                     int32_t num_kv_heads, int32_t head_dim) {
+  int64_t skipped = 0;
+  uint16_t *normed = malloc(sizeof(uint16_t) * (size_t)head_dim);
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int32_t pos = positions[t];
+    const int64_t slot = slot_mapping[t];
+    if (pos < 0 || pos >= max_position || slot < 0 || slot >= num_blocks * block_size) {
+      ++skipped;
+      continue;
+    }
+    const uint16_t *cos_row = cos_table + (int64_t)pos * head_dim;
+    const uint16_t *sin_row = sin_table + (int64_t)pos * head_dim;
+    for (int32_t g = 0; g < num_q_heads; ++g) {
+      const int64_t row = (t * num_q_heads + g) * (int64_t)head_dim;
+      rms_norm_row(q + row, q_weight, eps, head_dim, dtype, normed);
+      rope_row(normed, cos_row, sin_row, head_dim, dtype, q_out + row);
+    }
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      const int64_t src = (t * num_kv_heads + h) * (int64_t)head_dim;
+      const int64_t dst = (slot * num_kv_heads + h) * (int64_t)head_dim;
+      rms_norm_row(k + src, k_weight, eps, head_dim, dtype, normed);
+      rope_row(normed, cos_row, sin_row, head_dim, dtype, k_cache + dst);
+      for (int32_t x = 0; x < head_dim; ++x) v_cache[dst + x] = v[src + x];
+    }
+  }
+  free(normed);
   return skipped;
 }
 

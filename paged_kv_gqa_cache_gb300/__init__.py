@@ -14,6 +14,7 @@ Calls (see include/pagedattn.h for the full contract):
 * ``kv_cache_write_q8`` / ``paged_attn_decode_q8`` on an int8 pool
   (``alloc_pool_q8``: codes plus one fp32 scale per token and KV head)
 * ``paged_attn_decode_window`` / ``paged_attn_prefill_chunk_window``: sliding window
+* ``qk_norm_rope_kv_write``: q/k RMSNorm + rotary embedding fused into the KV write
 * ``kv_block_copy(pools, pairs)``: copy-on-write block copy over every layer
 * ``BlockAllocator`` / ``Sequence`` / ``build_step_tables``: the host-side block
   allocator and block-table builder (native code in the same library; no GPU)
@@ -42,6 +43,7 @@ EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_deco
            "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc",
            "pa_decode_kernel_launches", "pa_kv_cache_write_q8", "pa_paged_attn_decode_q8",
            "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
+           "pa_qk_norm_rope_kv_write",
            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
            "pa_allocator_release", "pa_allocator_refcount", "pa_allocator_stats_get", "pa_allocator_take_copies",
            "pa_sequence_create", "pa_sequence_destroy", "pa_sequence_reserve", "pa_sequence_commit",
@@ -117,6 +119,9 @@ def load_library(path: str = LIB_PATH):
         lib.pa_paged_attn_prefill_chunk_window.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
                                                            ctypes.c_float, i32, P, P]
         lib.pa_paged_attn_prefill_chunk_window.restype = i32
+        lib.pa_qk_norm_rope_kv_write.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, i32, P, P, i32, i32, P,
+                                                 pool_p, P]
+        lib.pa_qk_norm_rope_kv_write.restype = i32
         lib.pa_kv_block_copy.argtypes = [pool_p, i32, P, i32, P]
         lib.pa_kv_block_copy.restype = i32
         ip = ctypes.POINTER(i32)
@@ -429,6 +434,34 @@ def raise_device_error(stream=None) -> None:
     st, detail = get_device_error(stream)
     if st != PA_OK:
         raise PagedAttnError(st, f"device error (index {detail})")
+
+
+def qk_norm_rope_kv_write(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, q_norm_weight: torch.Tensor,
+                          k_norm_weight: torch.Tensor, eps: float, cos_table: torch.Tensor, sin_table: torch.Tensor,
+                          positions: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, q_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """q/k RMSNorm and rotary embedding at absolute positions, fused into the
+    KV write: returns q_out (normed, rotated q; may be ``q`` itself) and stores
+    the normed, rotated k and the unchanged v into their slots."""
+    pool = make_pool(k_cache, v_cache)
+    for name, t in (("q", q), ("k", k), ("v", v), ("q_norm_weight", q_norm_weight),
+                    ("k_norm_weight", k_norm_weight), ("cos_table", cos_table), ("sin_table", sin_table)):
+        _need(t, name, k_cache.dtype)
+    _need(positions, "positions", torch.int32)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    T, hq, d = q.shape
+    if k.shape != (T, pool.num_kv_heads, d) or v.shape != k.shape or positions.shape != (T,) \
+            or slot_mapping.shape != (T,) or cos_table.dim() != 2 or cos_table.shape != sin_table.shape:
+        raise ValueError("q [T, Hq, 128], k/v [T, Hkv, 128], positions/slot_mapping [T], tables [max_pos, 128]")
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    _need(q_out, "q_out", q.dtype)
+    _check(load_library().pa_qk_norm_rope_kv_write(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), q_norm_weight.data_ptr(), k_norm_weight.data_ptr(), float(eps),
+        cos_table.data_ptr(), sin_table.data_ptr(), cos_table.shape[0], positions.data_ptr(),
+        slot_mapping.data_ptr(), T, hq, q_out.data_ptr(), ctypes.byref(pool), _stream(stream)),
+        "pa_qk_norm_rope_kv_write")
+    return q_out
 
 
 # ---- copy-on-write block copy and the host-side block-table builder ---------------------

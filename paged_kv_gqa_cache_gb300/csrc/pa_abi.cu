@@ -402,6 +402,51 @@ pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts
                                             scale, 0, out, stream);
 }
 
+pa_status pa_qk_norm_rope_kv_write(const void *q, const void *k, const void *v, const void *q_norm_weight,
+                                   const void *k_norm_weight, float eps, const void *cos_table,
+                                   const void *sin_table, int32_t max_position, const int32_t *positions,
+                                   const int64_t *slot_mapping, int32_t num_tokens, int32_t num_q_heads,
+                                   void *q_out, const pa_kv_pool *pool, pa_stream_t stream) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!q || !k || !v || !q_norm_weight || !k_norm_weight || !cos_table || !sin_table || !positions ||
+      !slot_mapping || !q_out)
+    return PA_ERR_NULL;
+  if (num_q_heads < 1 || num_q_heads > 1024 || max_position < 1 || !(eps >= 0.f) || !isfinite(eps))
+    return PA_ERR_SHAPE;
+  if ((int64_t)num_tokens * (num_q_heads + 2 * pool->num_kv_heads) > INT32_MAX) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(q_norm_weight) ||
+      !aligned16(k_norm_weight) || !aligned16(cos_table) || !aligned16(sin_table) || !aligned4(positions) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PA_ERR_ALIGN;
+  DeviceState *d = nullptr;
+  if ((st = device_state(&d)) != PA_OK) return st;
+  RopeWriteParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.q_weight = q_norm_weight;
+  p.k_weight = k_norm_weight;
+  p.cos_table = cos_table;
+  p.sin_table = sin_table;
+  p.positions = positions;
+  p.slots = slot_mapping;
+  p.q_out = q_out;
+  p.k_cache = pool->k_cache;
+  p.v_cache = pool->v_cache;
+  p.err = d->err;
+  p.num_slots = (int64_t)pool->num_blocks * kBlock;
+  p.num_tokens = num_tokens;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = pool->num_kv_heads;
+  p.max_position = max_position;
+  p.eps = eps;
+  cudaError_t e = launch_rope_write(p, pool->dtype, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 pa_status pa_kv_block_copy(const pa_kv_pool *pools, int32_t num_layers, const int32_t *pairs, int32_t num_pairs,
                            pa_stream_t stream) {
   if (num_layers < 0 || num_pairs < 0) return PA_ERR_SHAPE;

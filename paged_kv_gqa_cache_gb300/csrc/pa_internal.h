@@ -49,6 +49,30 @@ struct WriteQ8Params {
 };
 cudaError_t launch_kv_write_q8(const WriteQ8Params &p, int dtype, cudaStream_t stream);
 
+// ---- q/k RMSNorm + rotary embedding fused into the KV write -------------------------------
+struct RopeWriteParams {
+  const void *q;             // [T][Hq][128]
+  const void *k;             // [T][Hkv][128]
+  const void *v;
+  const void *q_weight;      // [128]
+  const void *k_weight;
+  const void *cos_table;     // [max_position][128]
+  const void *sin_table;
+  const int32_t *positions;  // [T]
+  const int64_t *slots;      // [T]
+  void *q_out;               // [T][Hq][128]
+  void *k_cache;
+  void *v_cache;
+  int *err;
+  int64_t num_slots;
+  int32_t num_tokens;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t max_position;
+  float eps;
+};
+cudaError_t launch_rope_write(const RopeWriteParams &p, int dtype, cudaStream_t stream);
+
 // ---- copy-on-write block copy ---------------------------------------------------------
 constexpr int kCopyLayers = 64;          // layer pools per launch
 struct BlockCopyParams {

@@ -184,3 +184,20 @@ def test_window_calls_check_their_arguments(lib):
     assert dec(-1) == -2 and pre(-1) == -2      # a negative window
     assert dec(40, out=P + 2) == -9             # the plain calls' checks still apply, before any CUDA call
     assert pre(40, q=P + 8) == -9
+
+
+def test_fused_rope_write_checks_its_arguments(lib):
+    pool = _pool()
+    call = lambda **kw: lib.pa_qk_norm_rope_kv_write(
+        kw.get("q", P), P, P, P, P, kw.get("eps", 1e-6), P, P, kw.get("maxpos", 4096), P, kw.get("slots", P),
+        kw.get("T", 4), kw.get("hq", 16), kw.get("q_out", P), ctypes.byref(kw.get("pool", pool)), None)
+    assert call(T=0) == 0
+    assert call(T=-1) == -2
+    assert call(q=0) == -1
+    assert call(hq=0) == -2
+    assert call(maxpos=0) == -2
+    assert call(eps=float("nan")) == -2
+    assert call(eps=-1.0) == -2
+    assert call(q_out=P + 8) == -9
+    assert call(slots=P + 4) == -9
+    assert call(pool=_pool(dtype=3)) == -3
