@@ -54,10 +54,32 @@ __device__ __forceinline__ void pair_add(float &hi, float &lo, float xhi, float 
   fast_two_sum(s, __fadd_rn(__fadd_rn(lo, xlo), e), hi, lo);
 }
 
-// The 16-bit rounding of two fp32 values, back in fp32.
+// Packed 16-bit products and sums, each the exact result rounded once to the
+// 16-bit format (ties to even) — a 16-bit tensor operation.  For a sum this
+// equals rounding the fp32 sum to 16 bits: two 16-bit values add exactly in
+// fp32 unless their exponents differ by more than 13 bits, and then the
+// smaller is below half a 16-bit ulp of the larger either way.
 template <typename T>
-__device__ __forceinline__ float2 round16(float a, float b) {
-  return Pack<T>::to_f2(Pack<T>::from_f2(a, b));
+struct Packed;
+template <>
+struct Packed<__nv_bfloat16> {
+  using V = __nv_bfloat162;
+};
+template <>
+struct Packed<__half> {
+  using V = __half2;
+};
+template <typename T>
+__device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
+  using V = typename Packed<T>::V;
+  const V r = __hmul2_rn(*reinterpret_cast<const V *>(&a), *reinterpret_cast<const V *>(&b));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+template <typename T>
+__device__ __forceinline__ uint32_t add2(uint32_t a, uint32_t b) {
+  using V = typename Packed<T>::V;
+  const V r = __hadd2_rn(*reinterpret_cast<const V *>(&a), *reinterpret_cast<const V *>(&b));
+  return *reinterpret_cast<const uint32_t *>(&r);
 }
 
 // inv = rsqrt(mean(x^2) + eps) in fp32 for the 4 rows of a unit (this lane's
@@ -72,11 +94,17 @@ __device__ __forceinline__ void rows_rsqrt4(const uint2 (&raw)[4], float eps, in
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 a = Pack<T>::to_f2(raw[i].x), b = Pack<T>::to_f2(raw[i].y);
-    hi[i] = __fmul_rn(a.x, a.x);  // squares of 16-bit values are exact in fp32
+    // squares of 16-bit values are exact in fp32; the local pair is renormalised at the first level below
+    hi[i] = __fmul_rn(a.x, a.x);
     lo[i] = 0.f;
-    pair_add(hi[i], lo[i], __fmul_rn(a.y, a.y), 0.f);
-    pair_add(hi[i], lo[i], __fmul_rn(b.x, b.x), 0.f);
-    pair_add(hi[i], lo[i], __fmul_rn(b.y, b.y), 0.f);
+    const float sq[3] = {__fmul_rn(a.y, a.y), __fmul_rn(b.x, b.x), __fmul_rn(b.y, b.y)};
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      float sum, err;
+      two_sum(hi[i], sq[k], sum, err);
+      hi[i] = sum;
+      lo[i] = __fadd_rn(lo[i], err);
+    }
   }
   const bool up16 = lane & 16, up8 = lane & 8;
   // level 16: keep rows (0, 1) below lane 16, (2, 3) above; send the other two
@@ -108,31 +136,21 @@ __device__ __forceinline__ void rows_rsqrt4(const uint2 (&raw)[4], float eps, in
   for (int i = 0; i < 4; ++i) inv[i] = __shfl_sync(FULL, mine, 8 * i);
 }
 
-// One head row after its inverse RMS: scale, weight w, then the rotation with
-// this lane's cos/sin values (dims 4 lane .. 4 lane + 3).
+// One head row after its inverse RMS: y = x inv (fp32, rounded to 16 bits),
+// z = y w, then out = z cos + rotate_half(z) sin, rotate_half(z)[i] =
+// -z[i + 64] (i < 64), z[i - 64] (i >= 64); this lane holds dims 4 lane ..
+// 4 lane + 3, and dims i and i + 64 sit on lanes l and l ^ 16.
 template <typename T>
 __device__ __forceinline__ uint2 norm_rope_row(uint2 raw, float inv, uint2 wr, uint2 cr, uint2 sr, int lane) {
   const float2 x01 = Pack<T>::to_f2(raw.x), x23 = Pack<T>::to_f2(raw.y);
-  const float2 y01 = round16<T>(__fmul_rn(x01.x, inv), __fmul_rn(x01.y, inv));
-  const float2 y23 = round16<T>(__fmul_rn(x23.x, inv), __fmul_rn(x23.y, inv));
-  const float2 w01 = Pack<T>::to_f2(wr.x), w23 = Pack<T>::to_f2(wr.y);
-  const uint32_t z01 = Pack<T>::from_f2(__fmul_rn(y01.x, w01.x), __fmul_rn(y01.y, w01.y));
-  const uint32_t z23 = Pack<T>::from_f2(__fmul_rn(y23.x, w23.x), __fmul_rn(y23.y, w23.y));
-  // ---- rotary embedding: out = z cos + rotate_half(z) sin, rotate_half(z)[i] = -z[i + 64] (i < 64),
-  //      z[i - 64] (i >= 64); dims i and i + 64 sit on lanes l and l ^ 16 ----
-  const uint32_t p01 = __shfl_xor_sync(FULL, z01, 16), p23 = __shfl_xor_sync(FULL, z23, 16);
-  const float sgn = lane < 16 ? -1.f : 1.f;
-  const float2 z0 = Pack<T>::to_f2(z01), z1 = Pack<T>::to_f2(z23);
-  const float2 q0 = Pack<T>::to_f2(p01), q1 = Pack<T>::to_f2(p23);
-  const float2 c0 = Pack<T>::to_f2(cr.x), c1 = Pack<T>::to_f2(cr.y);
-  const float2 s0 = Pack<T>::to_f2(sr.x), s1 = Pack<T>::to_f2(sr.y);
-  const float2 a0 = round16<T>(__fmul_rn(z0.x, c0.x), __fmul_rn(z0.y, c0.y));
-  const float2 a1 = round16<T>(__fmul_rn(z1.x, c1.x), __fmul_rn(z1.y, c1.y));
-  const float2 b0 = round16<T>(__fmul_rn(sgn * q0.x, s0.x), __fmul_rn(sgn * q0.y, s0.y));
-  const float2 b1 = round16<T>(__fmul_rn(sgn * q1.x, s1.x), __fmul_rn(sgn * q1.y, s1.y));
+  const uint32_t y01 = Pack<T>::from_f2(__fmul_rn(x01.x, inv), __fmul_rn(x01.y, inv));
+  const uint32_t y23 = Pack<T>::from_f2(__fmul_rn(x23.x, inv), __fmul_rn(x23.y, inv));
+  const uint32_t z01 = mul2<T>(y01, wr.x), z23 = mul2<T>(y23, wr.y);
+  const uint32_t neg = lane < 16 ? 0x80008000u : 0u;  // rotate_half's sign, on both halves of a pair
+  const uint32_t p01 = __shfl_xor_sync(FULL, z01, 16) ^ neg, p23 = __shfl_xor_sync(FULL, z23, 16) ^ neg;
   uint2 out;
-  out.x = Pack<T>::from_f2(__fadd_rn(a0.x, b0.x), __fadd_rn(a0.y, b0.y));
-  out.y = Pack<T>::from_f2(__fadd_rn(a1.x, b1.x), __fadd_rn(a1.y, b1.y));
+  out.x = add2<T>(mul2<T>(z01, cr.x), mul2<T>(p01, sr.x));
+  out.y = add2<T>(mul2<T>(z23, cr.y), mul2<T>(p23, sr.y));
   return out;
 }
 
@@ -152,13 +170,13 @@ __global__ void __launch_bounds__(kRopeThreads) rope_write_kernel(const RopeWrit
   const uint2 wq = *reinterpret_cast<const uint2 *>(static_cast<const T *>(p.q_weight) + 4 * lane);
   const uint2 wk = *reinterpret_cast<const uint2 *>(static_cast<const T *>(p.k_weight) + 4 * lane);
 
-  for (int u = (int)((blockIdx.x * kRopeThreads) >> 5) + (int)(threadIdx.x >> 5); u < units; u += nwarps) {
-    const int t = u / units_per_token, j0 = (u - t * units_per_token) * kRowsPerUnit;
-    const int pos = __ldg(p.positions + t);
-    const int64_t slot = __ldg(p.slots + t);
-    uint2 raw[kRowsPerUnit];
+  // the unit (token t, first row j0): its rows, position and slot; the rows' loads
+  // do not depend on the position or slot
+  auto fetch = [&](int t, int j0, uint2 (&raw)[kRowsPerUnit], int &pos, int64_t &slot) {
+    pos = __ldg(p.positions + t);
+    slot = __ldg(p.slots + t);
 #pragma unroll
-    for (int i = 0; i < kRowsPerUnit; ++i) {  // the rows' loads do not depend on the position or slot
+    for (int i = 0; i < kRowsPerUnit; ++i) {
       const int j = j0 + i;
       raw[i] = make_uint2(0, 0);
       if (j < rows_per_token) {
@@ -168,6 +186,30 @@ __global__ void __launch_bounds__(kRopeThreads) rope_write_kernel(const RopeWrit
         raw[i] = *reinterpret_cast<const uint2 *>(src + 4 * lane);
       }
     }
+  };
+  // software pipeline: the next unit's loads are in flight while this one is computed.
+  // Unit u is (token u / units_per_token, group u % units_per_token); the warp's
+  // units advance by nwarps, tracked as a token step and a group step.
+  int u = (int)((blockIdx.x * kRopeThreads) >> 5) + (int)(threadIdx.x >> 5);
+  const int dt = nwarps / units_per_token, dg = nwarps - dt * units_per_token;
+  int t_next = u / units_per_token, g_next = u - t_next * units_per_token;
+  uint2 raw[kRowsPerUnit], raw_next[kRowsPerUnit];
+  int pos = 0, pos_next = 0;
+  int64_t slot = 0, slot_next = 0;
+  if (u < units) fetch(t_next, g_next * kRowsPerUnit, raw_next, pos_next, slot_next);
+  for (; u < units; u += nwarps) {
+#pragma unroll
+    for (int i = 0; i < kRowsPerUnit; ++i) raw[i] = raw_next[i];
+    pos = pos_next;
+    slot = slot_next;
+    const int t = t_next, j0 = g_next * kRowsPerUnit;
+    t_next += dt;
+    g_next += dg;
+    if (g_next >= units_per_token) {
+      g_next -= units_per_token;
+      ++t_next;
+    }
+    if (u + nwarps < units) fetch(t_next, g_next * kRowsPerUnit, raw_next, pos_next, slot_next);
     const bool ok = pos >= 0 && pos < p.max_position && slot >= 0 && slot < p.num_slots;
     const int64_t prow = (int64_t)(ok ? pos : 0) * kHeadDim + 4 * lane;
     const uint2 cr = *reinterpret_cast<const uint2 *>(static_cast<const T *>(p.cos_table) + prow);
