@@ -60,6 +60,9 @@ def parse_args(argv=None):
     ap.add_argument("--kv", choices=["16bit", "int8"], default="16bit",
                     help="decode workloads: the workload's 16-bit pool, or an int8 pool (codes + one fp32 scale "
                          "per token and KV head) holding the same tokens quantised")
+    ap.add_argument("--append", action="store_true",
+                    help="decode workloads: each layer's KV write fused into its decode call "
+                         "(paged_attn_decode_append) instead of a separate kv_cache_write")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window of W keys for the attention calls of workloads 2, 3 and 4 (0 = none); "
                          "the bytes or FLOPs counted are those of the visible keys")
@@ -75,6 +78,8 @@ def parse_args(argv=None):
     args = ap.parse_args(argv)
     if args.window < 0 or (args.window and (args.workload == 5 or args.kv == "int8")):
         ap.error("--window takes W >= 0, with workloads 2, 3 and 4 on the 16-bit pool")
+    if args.append and (args.window or args.kv == "int8" or args.workload == 3):
+        ap.error("--append applies to the 16-bit decode workloads 2, 4 and 5 without a window")
     return args
 
 
@@ -206,13 +211,14 @@ class DecodeStep:
     kv_cache_write of the new tokens then paged_attn_decode (layer pools are
     cycled when fewer distinct pools than calls are held)."""
 
-    def __init__(self, device, workload: int = 2, pools: int = 0, window: int = 0):
+    def __init__(self, device, workload: int = 2, pools: int = 0, window: int = 0, append: bool = False):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
         self.pa = pa
         self.workload = workload
         self.window = window
+        self.append = append
         self.desc, default_pools, self.L = WORKLOADS[workload]
         pools = pools or default_pools
         maker = workloads.CONFIGS[workload]
@@ -233,7 +239,8 @@ class DecodeStep:
         self.write_bytes_layer = 2 * c.k_new[0].numel() * 2 * 2     # K and V rows, read + write
         self.step_bytes = self.L * (self.decode_bytes_layer + self.write_bytes_layer)
         self.decode_kernels = pa.decode_kernel_launches(self.S, c.hkv, c.max_context_len, window)
-        self.kernels_per_step = self.L * (1 + self.decode_kernels)  # write, then the decode's kernels
+        # write, then the decode's kernels (the write runs inside the decode with append)
+        self.kernels_per_step = self.L * ((0 if append else 1) + self.decode_kernels)
 
     def write(self, l):
         c, i = self.case, l % self.case.n_layers
@@ -241,7 +248,11 @@ class DecodeStep:
 
     def decode(self, l):
         c, i = self.case, l % self.case.n_layers
-        if self.window:
+        if self.append:
+            self.pa.paged_attn_decode_append(c.q[i], c.k_new[i], c.v_new[i], c.k_cache[i], c.v_cache[i],
+                                             c.block_tables, c.context_lens, c.scale, out=self.out[i],
+                                             workspace=self.ws, max_context_len=c.max_context_len)
+        elif self.window:
             self.pa.paged_attn_decode_window(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
                                              c.scale, self.window, out=self.out[i], workspace=self.ws,
                                              max_context_len=c.max_context_len)
@@ -252,7 +263,8 @@ class DecodeStep:
 
     def run(self):
         for l in range(self.L):
-            self.write(l)
+            if not self.append:
+                self.write(l)
             self.decode(l)
 
     def run_decode_only(self):
@@ -397,7 +409,8 @@ def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream):
             c.q[i].copy_(host_q[i], non_blocking=True)
             c.k_new[i].copy_(host_k[i], non_blocking=True)
             c.v_new[i].copy_(host_v[i], non_blocking=True)
-            step.write(l)
+            if not getattr(step, "append", False):
+                step.write(l)
             step.decode(l)
             host_out[i].copy_(step.out[i], non_blocking=True)
 
@@ -473,7 +486,7 @@ def run_ours(args):
         return run_mixed(args, dev, pa)
 
     step = (DecodeStepQ8(dev, args.workload, args.pools) if args.kv == "int8"
-            else DecodeStep(dev, args.workload, args.pools, args.window))
+            else DecodeStep(dev, args.workload, args.pools, args.window, args.append))
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_dec = graph_of(step.run_decode_only, 1, stream)
@@ -496,7 +509,9 @@ def run_ours(args):
     value = world * step.step_bytes / (ms_step * 1e-3) / 1e9
 
     dec_launch_ms = ms_dec / step.L
-    achieved = step.decode_bytes_layer / (dec_launch_ms * 1e-3) / 1e9
+    # with append the decode call also moves the new rows (read, written into the pool)
+    launch_bytes = step.decode_bytes_layer + (step.write_bytes_layer if getattr(step, "append", False) else 0)
+    achieved = launch_bytes / (dec_launch_ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = e2e_measure(step, max(args.steps // 20, 10), 3, stream)
     e2e_ms = reduce_max(e2e_ms, dev)
     _device_error_check(pa)
@@ -504,14 +519,15 @@ def run_ours(args):
     q8 = isinstance(step, DecodeStepQ8)
     pool_mib = (step.pool_bytes if q8 else 2 * step.case.k_cache[0].numel() * 2) / 2**20
     win = getattr(step, "window", 0)
-    tag = "_q8" if q8 else (f"_window{win}" if win else "")
+    tag = "_q8" if q8 else (f"_window{win}" if win else ("_append" if getattr(step, "append", False) else ""))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8" if q8 else step.dtype, "data": "synthetic",
         "config": {"workload": step.desc + (", int8 KV pool (codes + one fp32 scale per token and KV head), "
                                             f"{step.dtype} q and out" if q8 else "")
-                               + (f", sliding window of {win} keys (bytes of the visible rows)" if win else ""),
+                               + (f", sliding window of {win} keys (bytes of the visible rows)" if win else "")
+                               + (", KV write fused into the decode call" if getattr(step, "append", False) else ""),
                    "global_batch": step.S * world, "seq_len": step.case.max_context_len,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({step.case.n_layers} distinct pools of {pool_mib:.0f} MiB "
@@ -527,7 +543,7 @@ def run_ours(args):
                      "kernel": "paged_attn_decode" + tag + " per layer ("
                                + ("one cluster per sequence and KV head" if step.decode_kernels == 1
                                   else "split + combine") + ")",
-                     "bytes_per_launch": step.decode_bytes_layer, "launch_ms": round(dec_launch_ms, 5),
+                     "bytes_per_launch": launch_bytes, "launch_ms": round(dec_launch_ms, 5),
                      "traffic": committed_traffic("decode.cu", f"decode{tag}_workload{args.workload}.md")},
         "clocks": clk.summary(),
     }

@@ -135,6 +135,25 @@ PA_API pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, con
                                pa_stream_t stream);
 
 /*
+ * paged_attn_decode_append — the KV write of each sequence's new token fused
+ * into the decode: equivalent to pa_kv_cache_write of k_new[s], v_new[s] into
+ * slot block_tables[s][(context_lens[s] - 1) / 16] * 16 + (context_lens[s] - 1) % 16
+ * (the position after the cached ones, [P1 PagedKVCache.write]) followed by
+ * pa_paged_attn_decode, in one launch (or two on the split path): the warp
+ * that streams a sequence's last page writes the new row into the pool and
+ * into its copy of that page.  16-bit pools only.
+ *   k_new, v_new  [num_seqs][num_kv_heads][128], pool dtype, 16-byte aligned.
+ * Other arguments, workspace and errors as pa_paged_attn_decode; a sequence
+ * whose length is out of range writes nothing.
+ */
+PA_API pa_status pa_paged_attn_decode_append(const void *q, const void *k_new, const void *v_new,
+                                             const pa_kv_pool *pool, const int32_t *block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                             int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                                             float scale, void *out, void *workspace, size_t workspace_bytes,
+                                             pa_stream_t stream);
+
+/*
  * Number of kernels one pa_paged_attn_decode (or _noalloc) call with these
  * arguments launches on the current device: 1 when every (sequence, KV head)
  * pair gets its own SMs and a pair of max_context_len tokens, streamed by

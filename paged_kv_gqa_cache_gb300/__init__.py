@@ -43,7 +43,7 @@ EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_deco
            "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc",
            "pa_decode_kernel_launches", "pa_kv_cache_write_q8", "pa_paged_attn_decode_q8",
            "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
-           "pa_qk_norm_rope_kv_write",
+           "pa_qk_norm_rope_kv_write", "pa_paged_attn_decode_append",
            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
            "pa_allocator_release", "pa_allocator_refcount", "pa_allocator_stats_get", "pa_allocator_take_copies",
            "pa_sequence_create", "pa_sequence_destroy", "pa_sequence_reserve", "pa_sequence_commit",
@@ -111,6 +111,9 @@ def load_library(path: str = LIB_PATH):
         lib.pa_paged_attn_decode_window.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, i32, P,
                                                     P, ctypes.c_size_t, P]
         lib.pa_paged_attn_decode_window.restype = i32
+        lib.pa_paged_attn_decode_append.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P,
+                                                    P, ctypes.c_size_t, P]
+        lib.pa_paged_attn_decode_append.restype = i32
         lib.pa_paged_attn_decode_noalloc.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P]
         lib.pa_paged_attn_decode_noalloc.restype = i32
         lib.pa_paged_attn_prefill_chunk.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
@@ -318,8 +321,24 @@ def paged_attn_decode_window(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
                    max_context_len, stream)
 
 
+def paged_attn_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                             v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                             scale: float, out: Optional[torch.Tensor] = None,
+                             workspace: Optional[torch.Tensor] = None, max_context_len: Optional[int] = None,
+                             stream=None) -> torch.Tensor:
+    """Write each sequence's new token (k_new, v_new [S, Hkv, 128]) at position
+    context_lens[s] - 1 of its block table and decode, in one call; otherwise
+    as :func:`paged_attn_decode`."""
+    _need(k_new, "k_new", k_cache.dtype)
+    _need(v_new, "v_new", k_cache.dtype)
+    if k_new.shape != (q.shape[0], k_cache.shape[2], q.shape[2]) or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must be [S, Hkv, 128]")
+    return _decode(q, k_cache, v_cache, block_tables, context_lens, scale, 0, out, workspace, max_context_len,
+                   stream, append=(k_new, v_new))
+
+
 def _decode(q, k_cache, v_cache, block_tables, context_lens, scale, window, out, workspace, max_context_len,
-            stream):
+            stream, append=None):
     pool = make_pool(k_cache, v_cache)
     _need(q, "q", k_cache.dtype)
     _need(block_tables, "block_tables", torch.int32)
@@ -337,7 +356,12 @@ def _decode(q, k_cache, v_cache, block_tables, context_lens, scale, window, out,
     _need(workspace, "workspace")
     lib = load_library()
     ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
-    if window:
+    if append is not None:
+        _check(lib.pa_paged_attn_decode_append(q.data_ptr(), append[0].data_ptr(), append[1].data_ptr(),
+                                               ctypes.byref(pool), block_tables.data_ptr(), mb,
+                                               context_lens.data_ptr(), S, hq, mcl, float(scale), out.data_ptr(),
+                                               *ws), "pa_paged_attn_decode_append")
+    elif window:
         _check(lib.pa_paged_attn_decode_window(q.data_ptr(), ctypes.byref(pool), block_tables.data_ptr(), mb,
                                                context_lens.data_ptr(), S, hq, mcl, float(scale), window,
                                                out.data_ptr(), *ws), "pa_paged_attn_decode_window")

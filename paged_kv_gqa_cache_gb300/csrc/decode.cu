@@ -157,6 +157,26 @@ __device__ __forceinline__ void load_page(uint8_t *dst, const CUtensorMap *kmap,
   }
 }
 
+// Append: the new token of sequence s (position ctx - 1, row r of its last
+// page, block blk) for KV head h goes into that page's shared-memory stage —
+// after the page's copy has landed, so the stage holds the new row whatever
+// the copy read there — and into the pool.  One warp; every lane moves 8 of
+// the 256 bytes of the K row and of the V row.  The stage is rewritten through
+// the generic proxy, so the caller fences before a later copy reuses it.
+template <typename T>
+__device__ __forceinline__ void append_row(uint8_t *stage, const DecodeParams &p, int s, int h, int blk, int r,
+                                           int lane) {
+  const int64_t src = ((int64_t)s * p.num_kv_heads + h) * kHeadDim + 4 * lane;
+  const uint2 kr = *reinterpret_cast<const uint2 *>(static_cast<const T *>(p.k_new) + src);
+  const uint2 vr = *reinterpret_cast<const uint2 *>(static_cast<const T *>(p.v_new) + src);
+  *reinterpret_cast<uint2 *>(stage + r * (kHeadDim * 2) + lane * 8) = kr;
+  *reinterpret_cast<uint2 *>(stage + kBlock * kHeadDim * 2 + r * (kHeadDim * 2) + lane * 8) = vr;
+  const int64_t dst = (((int64_t)blk * kBlock + r) * p.num_kv_heads + h) * kHeadDim + 4 * lane;
+  *reinterpret_cast<uint2 *>(static_cast<T *>(p.k_pool) + dst) = kr;
+  *reinterpret_cast<uint2 *>(static_cast<T *>(p.v_pool) + dst) = vr;
+  __syncwarp();
+}
+
 // Scores, online-softmax update and P V of one 16-key page for the G query
 // heads of a KV head, from a stage laid out as above (one warp; keys nlo ..
 // nv - 1 of the page are visible).  q holds this lane's dims of the G query rows (pre-scaled, log2
@@ -417,11 +437,20 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       return;
     }
 
+    bool appended = false;
     if (!((bad_mask >> st) & 1u)) {
       const int nv = min(kBlock, ctx - (first + cc.page) * kBlock);  // keys of the sequence in this page
+      if constexpr (!Q8) {
+        if (p.k_new && cc.page == cc.pages - 1) {  // the page of the sequence's new token
+          const int blk = __ldg(p.block_tables + (int64_t)cc.s * p.max_blocks_per_seq + first + cc.page);
+          append_row<T>(stages + st * STAGE, p, cc.s, cc.h, blk, nv - 1, lane);
+          appended = true;
+        }
+      }
       decode_page<T, G, Q8>(stages + st * STAGE, cc.page == 0 ? lo_in_first : 0, nv, q, o, m, l, pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
+    if (appended) fence_proxy_async_smem();  // the generic writes precede the stage's next copy
 
     if (g + kStages < npages) issue(st);
 
@@ -665,6 +694,12 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     if (!((bad_mask >> st) & 1u)) {
       const int pg = gw + nw * i;                              // visible page
       const int nv = min(kBlock, ctx - (first + pg) * kBlock);  // keys of the sequence in this page
+      if constexpr (!Q8) {
+        if (p.k_new && pg == pages - 1) {  // the page of the sequence's new token (the warp's last page)
+          append_row<T>(stages + st * STAGE, p, s, h, __ldg(bt + first + pg), nv - 1, lane);
+          fence_proxy_async_smem();
+        }
+      }
       decode_page<T, G, Q8>(stages + st * STAGE, pg == 0 ? lo - first * kBlock : 0, nv, q, o, m, l, pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf

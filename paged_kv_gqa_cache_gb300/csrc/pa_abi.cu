@@ -126,7 +126,8 @@ bool pool_map_q8(CUtensorMap *map, const pa_kv_pool_q8 *pool, void *base) {
 pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const pa_kv_pool_q8 *pool8,
                       const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                       int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
-                      void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+                      void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream,
+                      const void *k_new = nullptr, const void *v_new = nullptr) {
   const bool q8 = pool8 != nullptr;
   const int num_kv_heads = q8 ? pool8->num_kv_heads : pool16->num_kv_heads;
   const int num_blocks = q8 ? pool8->num_blocks : pool16->num_blocks;
@@ -144,7 +145,7 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
   if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
   if (window < 0) return PA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) || !aligned4(block_tables) ||
-      !aligned4(context_lens))
+      !aligned4(context_lens) || !aligned16(k_new) || !aligned16(v_new))
     return PA_ERR_ALIGN;
   if (workspace_bytes < decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads)) return PA_ERR_WORKSPACE;
   DeviceState *d = nullptr;
@@ -165,6 +166,10 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
   p.err = d->err;
   p.k_scale = q8 ? pool8->k_scale : nullptr;
   p.v_scale = q8 ? pool8->v_scale : nullptr;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_pool = q8 ? nullptr : pool16->k_cache;
+  p.v_pool = q8 ? nullptr : pool16->v_cache;
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.num_seqs = num_seqs;
   p.num_kv_heads = num_kv_heads;
@@ -279,6 +284,19 @@ pa_status pa_paged_attn_decode(const void *q, const pa_kv_pool *pool, const int3
   return decode_call(q, pool->dtype, pool, nullptr, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                      num_q_heads, max_context_len, scale, 0, out, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_paged_attn_decode_append(const void *q, const void *k_new, const void *v_new, const pa_kv_pool *pool,
+                                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t max_context_len, float scale, void *out, void *workspace,
+                                      size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  if (num_seqs > 0 && (!k_new || !v_new)) return PA_ERR_NULL;
+  return decode_call(q, pool->dtype, pool, nullptr, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, max_context_len, scale, 0, out, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), k_new, v_new);
 }
 
 pa_status pa_paged_attn_decode_window(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,

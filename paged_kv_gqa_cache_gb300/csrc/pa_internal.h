@@ -101,6 +101,10 @@ struct DecodeParams {
   int *err;
   const float *k_scale;      // int8 pools only: [num_blocks][Hkv][16] scales of K and V
   const float *v_scale;
+  const void *k_new;         // append (16-bit pools only; null: none): each sequence's new token
+  const void *v_new;         //   [S][Hkv][128], written at position context_lens[s] - 1
+  void *k_pool;              //   pool base addresses for that write
+  void *v_pool;
   int32_t max_blocks_per_seq;
   int32_t num_seqs;
   int32_t num_kv_heads;

@@ -201,3 +201,15 @@ def test_fused_rope_write_checks_its_arguments(lib):
     assert call(q_out=P + 8) == -9
     assert call(slots=P + 4) == -9
     assert call(pool=_pool(dtype=3)) == -3
+
+
+def test_decode_append_checks_its_arguments(lib):
+    pool = _pool()
+    ws = lib.pa_decode_workspace_bytes(4, 16, 8, 256)
+    call = lambda **kw: lib.pa_paged_attn_decode_append(
+        P, kw.get("kn", P), kw.get("vn", P), ctypes.byref(pool), P, 16, P, kw.get("S", 4), 16, 256, 0.088, P, P,
+        ws, None)
+    assert call(S=0) == 0
+    assert call(kn=0) == -1
+    assert call(vn=0) == -1
+    assert call(kn=P + 8) == -9
