@@ -117,8 +117,10 @@ bool pool_map_q8(CUtensorMap *map, const pa_kv_pool_q8 *pool, void *base) {
   const uint64_t dims[4] = {(uint64_t)kHeadDim, hkv, (uint64_t)kBlock, (uint64_t)pool->num_blocks};
   const uint64_t strides[3] = {kHeadDim * 1ull, hkv * kHeadDim, kBlock * hkv * kHeadDim};
   const uint32_t box[4] = {128u, 1, (uint32_t)kBlock, 1};
+  // a page row of one KV head is 128 bytes here, 1 KB apart (8 heads): promoting
+  // each fetch to 256 bytes would pull in another head's row
   return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 // The decode call on a 16-bit pool (pool16) or an int8 pool (pool8), after the
@@ -199,13 +201,13 @@ int sm_count() {
 
 bool encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, int rank, void *base,
                        const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
-                       CUtensorMapSwizzle swizzle) {
+                       CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promotion) {
   if (!g_encode) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(map, dtype, (cuuint32_t)rank, base, reinterpret_cast<const cuuint64_t *>(dims),
                         reinterpret_cast<const cuuint64_t *>(strides_bytes),
                         reinterpret_cast<const cuuint32_t *>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        swizzle, promotion, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

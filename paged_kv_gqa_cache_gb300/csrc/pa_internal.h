@@ -201,6 +201,7 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 int sm_count();
 bool encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, int rank, void *base,
                        const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
-                       CUtensorMapSwizzle swizzle);
+                       CUtensorMapSwizzle swizzle,
+                       CUtensorMapL2promotion promotion = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 
 }  // namespace pa
