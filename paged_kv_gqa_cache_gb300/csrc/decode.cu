@@ -28,6 +28,8 @@
 // heads of its KV head: the scores for G heads come from a single read of K.
 // All arithmetic is fp32 on the CUDA cores: decode reads each K/V byte once and
 // does G multiply-adds per element, far below the tensor-core ridge point.
+#include <type_traits>
+
 #include "pa_device.cuh"
 
 namespace pa {
@@ -138,6 +140,12 @@ __device__ __forceinline__ void advance(Cursor &c, const int32_t *prefix, int n,
 // at 4160.
 constexpr int kQ8V = 2048, kQ8KS = 4096, kQ8VS = 4160, kQ8StageBytes = 4224;
 static_assert(kQ8StageBytes <= STAGE, "an int8 page fits a stage");
+// Stage stride in shared memory: a 16-bit page takes 8 KB, an int8 page (codes
+// and scales) 4224 bytes, rounded up to the 128-byte alignment of a tensor copy.
+template <bool Q8>
+__host__ __device__ constexpr int stage_stride() {
+  return Q8 ? (kQ8StageBytes + 127) / 128 * 128 : STAGE;
+}
 
 // Fetch page blk of KV head h into the stage at dst, completing on bar.
 template <bool Q8>
@@ -154,6 +162,54 @@ __device__ __forceinline__ void load_page(uint8_t *dst, const CUtensorMap *kmap,
     mbar_arrive_expect_tx(bar, STAGE);
     tma_load_4d(dst, kmap, bar, 0, h, 0, blk);
     tma_load_4d(dst + 4096, vmap, bar, 0, h, 0, blk);
+  }
+}
+
+// This lane's dims of the G query rows.  16-bit pools: fp32 pairs pre-scaled
+// into the log2 domain.  int8 pools: the row quantised to int16 with one fp32
+// scale per row (|error| <= scale / 2, scale = max |q| / 32767, far below the
+// 16-bit input's own resolution for every element within 2^7 of the row's
+// maximum), so that a key's dot product is exact integer arithmetic on its
+// int8 codes (dp2a: two int16 x int8 products per instruction, no code
+// conversion) and costs half the registers.
+template <bool Q8>
+using QReg = typename std::conditional<Q8, uint32_t, float2>::type;
+
+template <typename T, int G, bool Q8>
+__device__ __forceinline__ void load_q(const T *qp, float scale_log2, int lane, QReg<Q8> (&q)[G][Layout<G>::DPL / 2],
+                                       float (&qsc)[G]) {
+  using Ly = Layout<G>;
+  constexpr int NQ = Ly::NQ, CPL = Ly::CPL;
+  const int qd = lane % NQ, rot = (lane / NQ) % CPL;
+#pragma unroll
+  for (int gg = 0; gg < G; ++gg) {
+    float2 f[Ly::DPL / 2];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int chunk = qd + NQ * ((i + rot) % CPL);
+      const uint4 u = *reinterpret_cast<const uint4 *>(qp + gg * kHeadDim + chunk * 8);
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f[i * 4 + e] = Pack<T>::to_f2(wd[e]);
+    }
+    if constexpr (Q8) {
+      float amax = 0.f;
+#pragma unroll
+      for (int k = 0; k < Ly::DPL / 2; ++k) amax = fmaxf(amax, fmaxf(fabsf(f[k].x), fabsf(f[k].y)));
+#pragma unroll
+      for (int off = 1; off < NQ; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const float inv = amax > 0.f ? 32767.f / amax : 0.f;
+#pragma unroll
+      for (int k = 0; k < Ly::DPL / 2; ++k) {
+        const int a = __float2int_rn(f[k].x * inv), b = __float2int_rn(f[k].y * inv);
+        q[gg][k] = (uint32_t)(a & 0xffff) | ((uint32_t)b << 16);
+      }
+      qsc[gg] = amax * (1.f / 32767.f) * scale_log2;
+    } else {
+#pragma unroll
+      for (int k = 0; k < Ly::DPL / 2; ++k) q[gg][k] = make_float2(f[k].x * scale_log2, f[k].y * scale_log2);
+      qsc[gg] = 1.f;
+    }
   }
 }
 
@@ -186,7 +242,7 @@ __device__ __forceinline__ void append_row(uint8_t *stage, const DecodeParams &p
 // once, and a value's scale multiplies its probability before the sum.
 template <typename T, int G, bool Q8>
 __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
-                                            const float2 (&q)[G][Layout<G>::DPL / 2],
+                                            const QReg<Q8> (&q)[G][Layout<G>::DPL / 2], const float (&qsc)[G],
                                             float2 (&o)[G][2], float (&m)[G], float (&l)[G], float2 *pbuf2,
                                             int lane) {
   using Ly = Layout<G>;
@@ -205,18 +261,24 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
   for (int ps = 0; ps < NP; ++ps) {
     const int t = ps * NT + tk;
     float2 acc[G];
+    int iacc[G];
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg) acc[gg] = make_float2(0.f, 0.f);
+    for (int gg = 0; gg < G; ++gg) {
+      acc[gg] = make_float2(0.f, 0.f);
+      iacc[gg] = 0;
+    }
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
       const int chunk = qd + NQ * ((i + rot) % CPL);  // dims 8 chunk .. 8 chunk + 7
       if constexpr (Q8) {
         const uint2 u = *reinterpret_cast<const uint2 *>(kst + t * 128 + chunk * 8);
-        const float2 k2[4] = {s8x2_to_f2<0>(u.x), s8x2_to_f2<1>(u.x), s8x2_to_f2<0>(u.y), s8x2_to_f2<1>(u.y)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-          for (int gg = 0; gg < G; ++gg) acc[gg] = __ffma2_rn(q[gg][i * 4 + e], k2[e], acc[gg]);
+        for (int gg = 0; gg < G; ++gg) {  // int16 query pairs x int8 codes, exact in int32
+          iacc[gg] = __dp2a_lo((int)q[gg][i * 4 + 0], (int)u.x, iacc[gg]);
+          iacc[gg] = __dp2a_hi((int)q[gg][i * 4 + 1], (int)u.x, iacc[gg]);
+          iacc[gg] = __dp2a_lo((int)q[gg][i * 4 + 2], (int)u.y, iacc[gg]);
+          iacc[gg] = __dp2a_hi((int)q[gg][i * 4 + 3], (int)u.y, iacc[gg]);
+        }
       } else {
         const uint4 u = *reinterpret_cast<const uint4 *>(kst + t * 256 + chunk * 16);
         const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
@@ -231,10 +293,17 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
     const float ksc = Q8 ? kscale[t] : 1.f;
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
-      float a = acc[gg].x + acc[gg].y;
+      float a;
+      if constexpr (Q8) {
+        int ia = iacc[gg];  // |partial| < 2^31: 128 products of at most 2^15 x 2^7
 #pragma unroll
-      for (int off = 1; off < NQ; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
-      if constexpr (Q8) a *= ksc;
+        for (int off = 1; off < NQ; off <<= 1) ia += __shfl_xor_sync(FULL, ia, off);
+        a = (float)ia * (qsc[gg] * ksc);
+      } else {
+        a = acc[gg].x + acc[gg].y;
+#pragma unroll
+        for (int off = 1; off < NQ; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
+      }
       sc[ps][gg] = (t >= nlo && t < nv) ? a : neg_inf;
     }
   }
@@ -302,8 +371,10 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
   }
 }
 
+// int8 pools: more CTAs per SM (the int16 query leaves room) to hide the
+// latency of the heavier per-byte arithmetic; 16-bit pools: as many as fit.
 template <typename T, int G, bool Q8>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, Q8 ? (G >= 8 ? 2 : G >= 4 ? 3 : 4) : 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const DecodeParams p) {
   using Ly = Layout<G>;
@@ -314,10 +385,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   __shared__ int warp_tot[NW];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t *stages = smem + warp * kStages * STAGE;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * kStages * STAGE) + warp * kStages;
-  float *pbuf = reinterpret_cast<float *>(smem + NW * kStages * STAGE + NW * kStages * 8) + warp * 16 * G * 2;
-  int32_t *prefix = reinterpret_cast<int32_t *>(smem + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * G * 8);
+  constexpr int SST = stage_stride<Q8>();
+  uint8_t *stages = smem + warp * kStages * SST;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * kStages * SST) + warp * kStages;
+  float *pbuf = reinterpret_cast<float *>(smem + NW * kStages * SST + NW * kStages * 8) + warp * 16 * G * 2;
+  int32_t *prefix = reinterpret_cast<int32_t *>(smem + NW * kStages * SST + NW * kStages * 8 + NW * 16 * G * 8);
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&kmap);
@@ -374,7 +446,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     const bool ok = (unsigned)blk < (unsigned)p.num_blocks;
     if (lane == 0) {
       if (ok) {
-        load_page<Q8>(stages + st * STAGE, &kmap, &vmap, &bars[st], p, ic.h, blk);
+        load_page<Q8>(stages + st * SST, &kmap, &vmap, &bars[st], p, ic.h, blk);
       } else {
         set_error(p.err, PA_ERR_RANGE, ic.s);
         mbar_arrive(&bars[st]);
@@ -390,7 +462,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   // ---- consumer state ---------------------------------------------------------
   // Packed fp32x2 arithmetic (FFMA2): q and the partial scores pair adjacent
   // dims, the output accumulators pair adjacent dims of one head.
-  float2 q[G][DPL / 2];
+  QReg<Q8> q[G][DPL / 2];
+  float qsc[G];
   float2 o[G][2];
   float m[G], l[G];
   int ctx = 0, first = 0, lo_in_first = 0;  // first visible page and key of the item
@@ -404,19 +477,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // new item: load its G query rows (pre-scaled into the log2 domain)
       const T *qp = reinterpret_cast<const T *>(p.q) +
                     ((int64_t)cc.s * p.num_q_heads + (int64_t)cc.h * G) * kHeadDim;
+      load_q<T, G, Q8>(qp, p.scale_log2, lane, q, qsc);
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-          const int chunk = qd + NQ * ((i + rot) % CPL);
-          const uint4 u = *reinterpret_cast<const uint4 *>(qp + gg * kHeadDim + chunk * 8);
-          const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = Pack<T>::to_f2(wd[e]);
-            q[gg][i * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-          }
-        }
         m[gg] = neg_inf;
         l[gg] = 0.f;
         o[gg][0] = make_float2(0.f, 0.f);
@@ -443,11 +506,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       if constexpr (!Q8) {
         if (p.k_new && cc.page == cc.pages - 1) {  // the page of the sequence's new token
           const int blk = __ldg(p.block_tables + (int64_t)cc.s * p.max_blocks_per_seq + first + cc.page);
-          append_row<T>(stages + st * STAGE, p, cc.s, cc.h, blk, nv - 1, lane);
+          append_row<T>(stages + st * SST, p, cc.s, cc.h, blk, nv - 1, lane);
           appended = true;
         }
       }
-      decode_page<T, G, Q8>(stages + st * STAGE, cc.page == 0 ? lo_in_first : 0, nv, q, o, m, l, pbuf2, lane);
+      decode_page<T, G, Q8>(stages + st * SST, cc.page == 0 ? lo_in_first : 0, nv, q, qsc, o, m, l, pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
     if (appended) fence_proxy_async_smem();  // the generic writes precede the stage's next copy
@@ -582,17 +645,20 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   using Ly = Layout<G>;
   constexpr int NQ = Ly::NQ, DPL = Ly::DPL, CPL = Ly::CPL;
   constexpr int kMerge = 4 + kHeadDim;  // floats per (warp, head): m, l, 2 unused, o[128] (16-byte aligned)
-  static_assert(G * kMerge * 4 <= kStages * STAGE, "merge buffer fits a warp's stages");
+  // full 8 KB stages for int8 too: a larger footprint keeps one CTA per SM, so
+  // the two CTAs of an item (and different items) never share an SM's copy engine
+  constexpr int SST = STAGE;
+  static_assert(G * kMerge * 4 <= kStages * SST, "merge buffer fits a warp's stages");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t *stages = smem + warp * kStages * STAGE;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kItemWarps * kStages * STAGE) + warp * kStages;
-  float2 *pbuf2 = reinterpret_cast<float2 *>(smem + kItemWarps * kStages * STAGE + kItemWarps * kStages * 8) +
+  uint8_t *stages = smem + warp * kStages * SST;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kItemWarps * kStages * SST) + warp * kStages;
+  float2 *pbuf2 = reinterpret_cast<float2 *>(smem + kItemWarps * kStages * SST + kItemWarps * kStages * 8) +
                   warp * 16 * G;
   // CTA 0 only: CTA 1's merged state, [G][kMerge] floats
-  float *peer = reinterpret_cast<float *>(smem + kItemWarps * kStages * STAGE + kItemWarps * kStages * 8 +
+  float *peer = reinterpret_cast<float *>(smem + kItemWarps * kStages * SST + kItemWarps * kStages * 8 +
                                           kItemWarps * 16 * G * 8);
 
   if (threadIdx.x == 0) {
@@ -623,25 +689,15 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   int32_t win = (gw + nw * lane < p.max_blocks_per_seq) ? __ldg(bt + gw + nw * lane) : -1;
   griddep_wait();
 
-  const int qd = lane % NQ, tk = lane / NQ, rot = tk % CPL;
-  float2 q[G][DPL / 2];
+  QReg<Q8> q[G][DPL / 2];
+  float qsc[G];
   float2 o[G][2];
   float m[G], l[G];
   {
     const T *qp = reinterpret_cast<const T *>(p.q) + ((int64_t)s * p.num_q_heads + (int64_t)h * G) * kHeadDim;
+    load_q<T, G, Q8>(qp, p.scale_log2, lane, q, qsc);
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
-#pragma unroll
-      for (int i = 0; i < CPL; ++i) {
-        const int chunk = qd + NQ * ((i + rot) % CPL);
-        const uint4 u = *reinterpret_cast<const uint4 *>(qp + gg * kHeadDim + chunk * 8);
-        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = Pack<T>::to_f2(wd[e]);
-          q[gg][i * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-        }
-      }
       m[gg] = -INFINITY;
       l[gg] = 0.f;
       o[gg][0] = make_float2(0.f, 0.f);
@@ -669,7 +725,7 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     const bool ok = (unsigned)blk < (unsigned)p.num_blocks;
     if (lane == 0) {
       if (ok) {
-        load_page<Q8>(stages + st * STAGE, &kmap, &vmap, &bars[st], p, h, blk);
+        load_page<Q8>(stages + st * SST, &kmap, &vmap, &bars[st], p, h, blk);
       } else {
         set_error(p.err, PA_ERR_RANGE, s);
         mbar_arrive(&bars[st]);
@@ -680,6 +736,7 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 
   const int npre = n < kStages ? n : kStages;
   for (int i = 0; i < npre; ++i) issue(i, i);
+
   bool timed_out = false;
   for (int i = 0; i < n; ++i) {
     const int st = i % kStages;
@@ -696,11 +753,12 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
       const int nv = min(kBlock, ctx - (first + pg) * kBlock);  // keys of the sequence in this page
       if constexpr (!Q8) {
         if (p.k_new && pg == pages - 1) {  // the page of the sequence's new token (the warp's last page)
-          append_row<T>(stages + st * STAGE, p, s, h, __ldg(bt + first + pg), nv - 1, lane);
+          append_row<T>(stages + st * SST, p, s, h, __ldg(bt + first + pg), nv - 1, lane);
           fence_proxy_async_smem();
         }
       }
-      decode_page<T, G, Q8>(stages + st * STAGE, pg == 0 ? lo - first * kBlock : 0, nv, q, o, m, l, pbuf2, lane);
+      decode_page<T, G, Q8>(stages + st * SST, pg == 0 ? lo - first * kBlock : 0, nv, q, qsc, o, m, l, pbuf2,
+                            lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
     if (i + kStages < n) issue(i + kStages, st);
@@ -735,7 +793,7 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     float4 ov[kItemWarps];
 #pragma unroll
     for (int w = 0; w < kItemWarps; ++w) {  // every load first (they are independent), then the arithmetic
-      const float *a = reinterpret_cast<const float *>(smem + w * kStages * STAGE) + mg * kMerge;
+      const float *a = reinterpret_cast<const float *>(smem + w * kStages * SST) + mg * kMerge;
       mv[w] = a[0];
       lv[w] = a[1];
       ov[w] = *reinterpret_cast<const float4 *>(a + 4 + 4 * lane);
@@ -793,8 +851,9 @@ int item_smem_bytes(int group) {
          group * (4 + kHeadDim) * 4;
 }
 
-int split_smem_bytes(int group, int num_seqs) {
-  return 1024 + NW * kStages * STAGE + NW * kStages * 8 + NW * 16 * group * 8 + (num_seqs + 1) * 4;
+int split_smem_bytes(int group, int num_seqs, bool q8) {
+  const int sst = q8 ? stage_stride<true>() : stage_stride<false>();
+  return 1024 + NW * kStages * sst + NW * kStages * 8 + NW * 16 * group * 8 + (num_seqs + 1) * 4;
 }
 
 }  // namespace
@@ -837,7 +896,7 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
     return launch_pdl_cluster(decode_item_kernel<T, G, Q8>, dim3(items * ctas), dim3(kItemWarps * 32), ismem, ctas,
                               stream, kmap, vmap, p);
   }
-  const int smem = split_smem_bytes(G, p.num_seqs);
+  const int smem = split_smem_bytes(G, p.num_seqs, Q8);
   // Per instantiation: raise the dynamic shared-memory limit and cache the
   // occupancy for the largest size seen (launch-time API calls stay out of
   // the hot path and out of CUDA-graph capture after the first call).
