@@ -645,7 +645,7 @@ def run_block_copy(args, dev, pa):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs / hbm, 3), "peak_kind": peak_kind, "kernel": "kv_block_copy",
                      "bytes_per_launch": step_bytes // 2, "launch_ms": round(ms_step / 2, 5),
-                     "traffic": None},
+                     "traffic": committed_traffic("block_copy.cu", "block_copy_cow.md")},
         "clocks": clk.summary(),
     }
     if rank == 0:
@@ -708,7 +708,8 @@ def run_fused_write(args, dev, pa):
         "gpu_launches": layers * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs / hbm, 3), "peak_kind": peak_kind, "kernel": "qk_norm_rope_kv_write",
-                     "bytes_per_launch": launch_bytes, "launch_ms": round(ms_step / layers, 5), "traffic": None},
+                     "bytes_per_launch": launch_bytes, "launch_ms": round(ms_step / layers, 5),
+                     "traffic": committed_traffic("rope_write.cu", "rope_write_fused_write.md")},
         "clocks": clk.summary(),
     }
     if rank == 0:
