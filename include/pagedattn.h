@@ -450,6 +450,16 @@ PA_API pa_status pa_build_step_tables(const pa_sequence *const *seqs, int32_t nu
  */
 PA_API pa_status pa_get_device_error(pa_stream_t stream, int32_t *detail);
 
+/*
+ * Self-test of failure detection: launches one warp that waits, with the
+ * same bounded wait every kernel of the library uses on its copies and MMAs,
+ * on a barrier that nothing completes.  After limit_us microseconds (1 ..
+ * 2,000,000) the wait gives up, PA_ERR_TIMEOUT (detail -1) is recorded in the
+ * device error word and the kernel returns: pa_get_device_error() then
+ * reports it and the context stays usable.  Nothing faults, traps or hangs.
+ */
+PA_API pa_status pa_selftest_bounded_wait(uint32_t limit_us, pa_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 PA_API const char *pa_status_string(int32_t status);
 

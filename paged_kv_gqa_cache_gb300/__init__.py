@@ -43,7 +43,7 @@ EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_deco
            "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc",
            "pa_decode_kernel_launches", "pa_kv_cache_write_q8", "pa_paged_attn_decode_q8",
            "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
-           "pa_qk_norm_rope_kv_write", "pa_paged_attn_decode_append",
+           "pa_qk_norm_rope_kv_write", "pa_paged_attn_decode_append", "pa_selftest_bounded_wait",
            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
            "pa_allocator_release", "pa_allocator_refcount", "pa_allocator_stats_get", "pa_allocator_take_copies",
            "pa_sequence_create", "pa_sequence_destroy", "pa_sequence_reserve", "pa_sequence_commit",
@@ -125,6 +125,8 @@ def load_library(path: str = LIB_PATH):
         lib.pa_qk_norm_rope_kv_write.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, i32, P, P, i32, i32, P,
                                                  pool_p, P]
         lib.pa_qk_norm_rope_kv_write.restype = i32
+        lib.pa_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P]
+        lib.pa_selftest_bounded_wait.restype = i32
         lib.pa_kv_block_copy.argtypes = [pool_p, i32, P, i32, P]
         lib.pa_kv_block_copy.restype = i32
         ip = ctypes.POINTER(i32)
@@ -444,6 +446,12 @@ def _prefill(q, chunk_starts, chunk_lens, k_cache, v_cache, block_tables, contex
         _check(lib.pa_paged_attn_prefill_chunk(*args, out.data_ptr(), _stream(stream)),
                "pa_paged_attn_prefill_chunk")
     return out
+
+
+def selftest_bounded_wait(limit_us: int = 20000, stream=None) -> None:
+    """Launch the library's bounded-wait self-test (a wait that must give up
+    after ``limit_us`` and record PA_ERR_TIMEOUT); read it with get_device_error()."""
+    _check(load_library().pa_selftest_bounded_wait(int(limit_us), _stream(stream)), "pa_selftest_bounded_wait")
 
 
 def get_device_error(stream=None) -> Tuple[int, int]:

@@ -500,6 +500,15 @@ pa_status pa_kv_block_copy(const pa_kv_pool *pools, int32_t num_layers, const in
   return PA_OK;
 }
 
+pa_status pa_selftest_bounded_wait(uint32_t limit_us, pa_stream_t stream) {
+  if (limit_us < 1 || limit_us > 2000000) return PA_ERR_SHAPE;
+  DeviceState *d = nullptr;
+  pa_status st = device_state(&d);
+  if (st != PA_OK) return st;
+  cudaError_t e = launch_bounded_wait_selftest(d->err, (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 pa_status pa_get_device_error(pa_stream_t stream, int32_t *detail) {
   DeviceState *d = nullptr;
   pa_status st = device_state(&d);

@@ -73,6 +73,9 @@ struct RopeWriteParams {
 };
 cudaError_t launch_rope_write(const RopeWriteParams &p, int dtype, cudaStream_t stream);
 
+// ---- self-test of the bounded waits --------------------------------------------------------
+cudaError_t launch_bounded_wait_selftest(int *err, uint64_t limit_ns, cudaStream_t stream);
+
 // ---- copy-on-write block copy ---------------------------------------------------------
 constexpr int kCopyLayers = 64;          // layer pools per launch
 struct BlockCopyParams {
