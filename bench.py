@@ -63,6 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--append", action="store_true",
                     help="decode workloads: each layer's KV write fused into its decode call "
                          "(paged_attn_decode_append) instead of a separate kv_cache_write")
+    ap.add_argument("--overlap", action="store_true",
+                    help="workload 3: each layer's prefill on a second stream beside its decode (same work)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window of W keys for the attention calls of workloads 2, 3 and 4 (0 = none); "
                          "the bytes or FLOPs counted are those of the visible keys")
@@ -320,11 +322,13 @@ class MixedStep:
     kv_cache_write of 2048 new tokens, prefill of 3 chunks of 512 (prefixes 0,
     512, 1536) and decode of 512 sequences; 2 distinct pools cycled over 28."""
 
-    def __init__(self, device, window: int = 0):
+    def __init__(self, device, window: int = 0, overlap: bool = False):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
         self.pa, self.L, self.window = pa, 28, window
+        # overlap: each layer's prefill (tensor-bound) runs on a second stream beside its decode (HBM-bound)
+        self.side = torch.cuda.Stream(device=device) if overlap else None
         self.case = c = workloads.config3(device=device, n_layers=2, nan_fill=False)
         self.out_d = [torch.empty_like(q) for q in c.q]
         self.out_p = [torch.empty_like(q) for q in c.q_chunks]
@@ -341,14 +345,23 @@ class MixedStep:
                                                 self.window, out=self.out_p[i], max_chunk_len=512)
 
     def run(self):
+        import torch
         c = self.case
+        main = torch.cuda.current_stream()
         for l in range(self.L):
             i = l % 2
             self.pa.kv_cache_write(c.k_new[i], c.v_new[i], c.slot_mapping, c.k_cache[i], c.v_cache[i])
-            self.prefill(l)
+            if self.side is not None:  # fork after the write, join before the next layer's write
+                self.side.wait_stream(main)
+                with torch.cuda.stream(self.side):
+                    self.prefill(l)
+            else:
+                self.prefill(l)
             self.pa.paged_attn_decode_window(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
                                              c.scale, self.window, out=self.out_d[i], workspace=self.ws,
                                              max_context_len=c.max_context_len)
+            if self.side is not None:
+                main.wait_stream(self.side)
 
     def run_prefill_only(self):
         for l in range(self.L):
@@ -557,7 +570,7 @@ def run_mixed(args, dev, pa):
     """Diagnostic line for the mixed chunked-prefill step (28 layers)."""
     import torch
     rank, world, _ = dist_env()
-    step = MixedStep(dev, args.window)
+    step = MixedStep(dev, args.window, args.overlap)
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_pre = graph_of(step.run_prefill_only, 1, stream)
@@ -580,7 +593,8 @@ def run_mixed(args, dev, pa):
         "config": {"workload": "Qwen3-0.6B mixed chunked-prefill step, 28 layers: chunks (0,512), (512,512), "
                                "(1536,512) + 512 decode seqs ctx U[16,1024], bf16; 2 distinct pools cycled"
                                + (f"; sliding window of {args.window} keys (FLOPs of the visible pairs)"
-                                  if args.window else ""),
+                                  if args.window else "")
+                               + ("; prefill and decode of each layer on two streams" if args.overlap else ""),
                    "global_batch": 515 * world, "parallelism": f"replicas x{world}",
                    "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
         "gpu_launches": step.L * step.kernels_per_layer * args.steps,
