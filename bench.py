@@ -223,7 +223,7 @@ class DecodeStep:
         self.append = append
         self.desc, default_pools, self.L = WORKLOADS[workload]
         pools = pools or default_pools
-        maker = workloads.CONFIGS[workload]
+        maker = workloads.BY_INDEX[workload]
         self.case = maker(device=device, n_layers=pools, nan_fill=False)
         c = self.case
         self.out = [torch.empty_like(q) for q in c.q]
@@ -329,7 +329,7 @@ class MixedStep:
         self.pa, self.L, self.window = pa, 28, window
         # overlap: each layer's prefill (tensor-bound) runs on a second stream beside its decode (HBM-bound)
         self.side = torch.cuda.Stream(device=device) if overlap else None
-        self.case = c = workloads.config3(device=device, n_layers=2, nan_fill=False)
+        self.case = c = workloads.qwen3_0_6b_mixed_step(device=device, n_layers=2, nan_fill=False)
         self.out_d = [torch.empty_like(q) for q in c.q]
         self.out_p = [torch.empty_like(q) for q in c.q_chunks]
         self.ws = pa.alloc_decode_workspace(c.q[0].shape[0], c.hq, c.hkv, c.max_context_len, device)
@@ -741,7 +741,7 @@ def run_reference(args):
     import torch
     import oracle
     import workloads
-    case = workloads.config2(device="cpu", n_layers=1, nan_fill=False)
+    case = workloads.qwen3_0_6b_decode(device="cpu", n_layers=1, nan_fill=False)
     threads = os.cpu_count() or 1
     kh = case.k_cache[0].view(torch.int16).numpy().view(np.uint16)
     vh = case.v_cache[0].view(torch.int16).numpy().view(np.uint16)

@@ -70,7 +70,7 @@ def test_append_on_both_decode_paths(hq, hkv):
 
 
 def test_append_of_the_qwen3_0_6b_step_and_the_8b_decode():
-    for case in (workloads.config2(device=DEV, n_layers=1), workloads.config4(device=DEV)):
+    for case in (workloads.qwen3_0_6b_decode(device=DEV, n_layers=1), workloads.qwen3_8b_decode(device=DEV)):
         fused, kc, vc, sep = _both(case)
         assert torch.equal(fused.view(torch.int16), sep.view(torch.int16)), case.name
         kh, vh = oracle_write(case, 0)

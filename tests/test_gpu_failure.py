@@ -61,7 +61,7 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     pa.selftest_bounded_wait(20000)   # 20 ms
     st, detail = pa.get_device_error()
     assert st == pa.STATUS_CODE["PA_ERR_TIMEOUT"] and detail == -1
-    c = workloads.config1(device=DEV)
+    c = workloads.tiny_decode(device=DEV)
     kc, vc = c.k_cache[0].clone(), c.v_cache[0].clone()
     pa.kv_cache_write(c.k_new[0], c.v_new[0], c.slot_mapping, kc, vc)
     out = pa.paged_attn_decode(c.q[0], kc, vc, c.block_tables, c.context_lens, c.scale)

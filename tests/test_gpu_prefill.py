@@ -55,8 +55,8 @@ def test_prefill_small_two_chunks():
 
 
 def test_prefill_of_the_mixed_step():
-    case = workloads.config3(device=DEV)
-    prefill_and_check(case, "cfg3 prefill chunks")
+    case = workloads.qwen3_0_6b_mixed_step(device=DEV)
+    prefill_and_check(case, "mixed-step prefill chunks")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])

@@ -75,7 +75,7 @@ def _decode_and_check(case, gpu, host, bound=None, bt=None, what=""):
 
 
 def test_q8_tiny_workload():
-    case = workloads.config1(device=DEV)
+    case = workloads.tiny_decode(device=DEV)
     gpu, host = _quantised_pools(case)
     _check_write(gpu, host, case.name)
     _decode_and_check(case, gpu, host)
@@ -107,7 +107,7 @@ def test_q8_one_launch_and_split_paths(dtype, hq, hkv):
 
 
 def test_q8_qwen3_8b_geometry():
-    case = workloads.config4(device=DEV)
+    case = workloads.qwen3_8b_decode(device=DEV)
     gpu, host = _quantised_pools(case)
     _check_write(gpu, host, case.name)
     _decode_and_check(case, gpu, host)

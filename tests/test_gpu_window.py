@@ -167,13 +167,13 @@ def test_prefill_window_as_long_as_the_context_is_the_plain_call():
 
 def test_decode_window_on_the_qwen3_8b_workload():
     # the full Qwen3-8B decode (64 x 4096, bf16, exactly full pool) under a 1024-key window, as the bench runs it
-    case = workloads.config4(device=DEV)
+    case = workloads.qwen3_8b_decode(device=DEV)
     kc, vc = _written(case)
     assert pa.decode_kernel_launches(64, 8, 4096, 1024) == 2
     _decode_check(case, kc, vc, 1024)
 
 
 def test_prefill_window_on_the_mixed_step_chunks():
-    case = workloads.config3(device=DEV)
+    case = workloads.qwen3_0_6b_mixed_step(device=DEV)
     kc, vc = _written(case)
     check_close(_prefill(case, kc, vc, 512), _prefill_ref(case, kc, vc, 512), "mixed-step chunks, window 512")

@@ -46,7 +46,7 @@ def decode_and_check(case, layer=0, what=""):
 
 @pytest.mark.parametrize("cfg", [1, 3])
 def test_write_bit_exact_whole_pool(cfg):
-    case = workloads.CONFIGS[cfg](device=DEV)
+    case = workloads.BY_INDEX[cfg](device=DEV)
     kc, vc = gpu_write(case, 0)
     torch.cuda.synchronize()
     kh, vh = oracle_write(case, 0)
@@ -55,7 +55,7 @@ def test_write_bit_exact_whole_pool(cfg):
 
 
 def test_write_all_layers_of_the_decode_step():
-    case = workloads.config2(device=DEV)
+    case = workloads.qwen3_0_6b_decode(device=DEV)
     for layer in (0, 13, 27):
         kc, vc = gpu_write(case, layer)
         kh, vh = oracle_write(case, layer)
@@ -63,7 +63,7 @@ def test_write_all_layers_of_the_decode_step():
 
 
 def test_write_empty_and_bad_slot():
-    case = workloads.config1(device=DEV)
+    case = workloads.tiny_decode(device=DEV)
     kc, vc = case.k_cache[0].clone(), case.v_cache[0].clone()
     before = bits(kc)
     empty = torch.empty(0, 8, 128, dtype=kc.dtype, device=DEV)
@@ -85,25 +85,25 @@ def test_write_empty_and_bad_slot():
 # ---- decode: the five workloads ------------------------------------------------------
 
 def test_decode_tiny_workload():
-    decode_and_check(workloads.config1(device=DEV))
+    decode_and_check(workloads.tiny_decode(device=DEV))
 
 
 def test_decode_qwen3_0_6b_step_layers():
-    case = workloads.config2(device=DEV)
+    case = workloads.qwen3_0_6b_decode(device=DEV)
     for layer in (0, 27):
         decode_and_check(case, layer, f"{case.name} layer {layer}")
 
 
 def test_decode_part_of_mixed_step():
-    decode_and_check(workloads.config3(device=DEV))
+    decode_and_check(workloads.qwen3_0_6b_mixed_step(device=DEV))
 
 
 def test_decode_qwen3_8b_full():
-    decode_and_check(workloads.config4(device=DEV))
+    decode_and_check(workloads.qwen3_8b_decode(device=DEV))
 
 
 def test_decode_prefix_shared_long_tail():
-    decode_and_check(workloads.config5(device=DEV))
+    decode_and_check(workloads.prefix_shared_tail(device=DEV))
 
 
 # ---- decode: ragged edges, head ratios, dtypes ------------------------------------------
@@ -150,7 +150,7 @@ def test_decode_block_permutation_is_bitwise_invariant():
 
 
 def test_decode_shared_prefix_equals_private_copies():
-    a = workloads.config5(device=DEV)
+    a = workloads.prefix_shared_tail(device=DEV)
     kc, vc = gpu_write(a, 0)
     out_shared = pa.paged_attn_decode(a.q[0], kc, vc, a.block_tables, a.context_lens, a.scale,
                                       max_context_len=a.max_context_len)
@@ -216,7 +216,7 @@ def test_decode_bad_block_id_and_bad_length_are_reported():
 
 
 def test_decode_empty_batch_is_a_no_op():
-    case = workloads.config1(device=DEV)
+    case = workloads.tiny_decode(device=DEV)
     q = case.q[0][:0]
     out = pa.paged_attn_decode(q, case.k_cache[0], case.v_cache[0], case.block_tables[:0],
                                case.context_lens[:0], case.scale, max_context_len=16)
@@ -226,7 +226,7 @@ def test_decode_empty_batch_is_a_no_op():
 
 def test_decode_workspace_reused_across_batch_sizes():
     # one workspace sized for the largest call serves smaller and larger batches in turn
-    big = workloads.config4(device=DEV)
+    big = workloads.qwen3_8b_decode(device=DEV)
     kc, vc = big.k_cache[0].clone(), big.v_cache[0].clone()
     pa.kv_cache_write(big.k_new[0], big.v_new[0], big.slot_mapping, kc, vc)
     ref = oracle.paged_attn_decode(bits(big.q[0]), bits(kc), bits(vc), big.block_tables.cpu().numpy(),

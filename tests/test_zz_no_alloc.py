@@ -32,7 +32,7 @@ def _noalloc_c_call(case, kc, vc, out):
 
 @pytest.mark.parametrize("cfg", [1, 4, 5])
 def test_noalloc_decode_matches_the_workspace_entry_point_twice(cfg):
-    case = workloads.CONFIGS[cfg](device=DEV)
+    case = workloads.BY_INDEX[cfg](device=DEV)
     kc, vc = case.k_cache[0].clone(), case.v_cache[0].clone()
     pa.kv_cache_write(case.k_new[0], case.v_new[0], case.slot_mapping, kc, vc)
     ref = pa.paged_attn_decode(case.q[0], kc, vc, case.block_tables, case.context_lens, case.scale,

@@ -202,7 +202,7 @@ def build_case(name: str, dtype: str, hq: int, hkv: int, *, seed: int, device="c
 
 # ---- the five workloads -------------------------------------------------------
 
-def config1(device="cpu", nan_fill=True) -> Case:
+def tiny_decode(device="cpu", nan_fill=True) -> Case:
     """Tiny decode, one layer, Qwen3-0.6B attention geometry, fp16: 4 sequences of
     context {17, 33, 100, 250} in a 64-block pool, plus the write of their 4 new tokens."""
     lens = [17, 33, 100, 250]
@@ -214,58 +214,60 @@ def config1(device="cpu", nan_fill=True) -> Case:
     for s, p in enumerate(pages):
         bt[s, :p] = perm[cur:cur + p]
         cur += p
-    return build_case("cfg1-tiny-decode", "f16", 16, 8, seed=1, device=device, decode_lens=lens,
+    return build_case("tiny-decode", "f16", 16, 8, seed=1, device=device, decode_lens=lens,
                       num_blocks=64, fixed_bt=bt, nan_fill=nan_fill)
 
 
-def config2_lens(seed: int = 2) -> List[int]:
+def qwen3_0_6b_decode_lens(seed: int = 2) -> List[int]:
     rng = np.random.default_rng(seed)
     return [int(x) for x in rng.integers(512, 1024, size=8, endpoint=True)]
 
 
-def config2(device="cpu", n_layers=28, nan_fill=True) -> Case:
+def qwen3_0_6b_decode(device="cpu", n_layers=28, nan_fill=True) -> Case:
     """Qwen3-0.6B decode step: 8 sequences of context U[512, 1024], fp16, one
     512-block pool per layer (28 layers), block table shared by all layers."""
-    return build_case("cfg2-qwen3-0.6b-decode", "f16", 16, 8, seed=2, device=device,
-                      decode_lens=config2_lens(), num_blocks=512, n_layers=n_layers,
+    return build_case("qwen3-0.6b-decode", "f16", 16, 8, seed=2, device=device,
+                      decode_lens=qwen3_0_6b_decode_lens(), num_blocks=512, n_layers=n_layers,
                       nan_fill=nan_fill)
 
 
-def config3(device="cpu", n_layers=1, nan_fill=True) -> Case:
+def qwen3_0_6b_mixed_step(device="cpu", n_layers=1, nan_fill=True) -> Case:
     """Qwen3-0.6B mixed chunked-prefill step (budget 2048), bf16: chunks of 512
     new tokens on cached prefixes of 0, 512 and 1536 tokens, plus 512 decode
     sequences of context U[16, 1024]; pool = needed blocks + 25 % free."""
     rng = np.random.default_rng(3)
     lens = [int(x) for x in rng.integers(16, 1024, size=512, endpoint=True)]
-    return build_case("cfg3-qwen3-0.6b-mixed", "bf16", 16, 8, seed=3, device=device,
+    return build_case("qwen3-0.6b-mixed-step", "bf16", 16, 8, seed=3, device=device,
                       decode_lens=lens, chunks=[(0, 512), (512, 512), (1536, 512)],
                       n_layers=n_layers, nan_fill=nan_fill)
 
 
-def config4(device="cpu", n_layers=1, nan_fill=True) -> Case:
+def qwen3_8b_decode(device="cpu", n_layers=1, nan_fill=True) -> Case:
     """Qwen3-8B decode, bf16: 64 sequences x 4096 context in an exactly-full
     16384-block pool per layer."""
-    return build_case("cfg4-qwen3-8b-decode", "bf16", 32, 8, seed=4, device=device,
+    return build_case("qwen3-8b-decode", "bf16", 32, 8, seed=4, device=device,
                       decode_lens=[4096] * 64, num_blocks=16384, n_layers=n_layers,
                       nan_fill=nan_fill)
 
 
-def config5_lens(seed: int = 5) -> List[int]:
+def prefix_shared_tail_lens(seed: int = 5) -> List[int]:
     rng = np.random.default_rng(seed)
     suffix = np.floor(np.exp(rng.uniform(math.log(16), math.log(32768), size=32))).astype(int)
     return [208 + int(s) for s in suffix]
 
 
-def config5(device="cpu", n_layers=1, nan_fill=True) -> Case:
+def prefix_shared_tail(device="cpu", n_layers=1, nan_fill=True) -> Case:
     """Prefix-shared long-tail decode, Qwen3-8B geometry, bf16: 32 sequences whose
     first 13 blocks (208 tokens) are the same physical blocks, then private
     suffixes log-uniform in [16, 32768] tokens; pool = needed + 25 %."""
-    return build_case("cfg5-qwen3-8b-prefix-shared", "bf16", 32, 8, seed=5, device=device,
-                      decode_lens=config5_lens(), shared_prefix_blocks=13, n_layers=n_layers,
+    return build_case("qwen3-8b-prefix-shared-tail", "bf16", 32, 8, seed=5, device=device,
+                      decode_lens=prefix_shared_tail_lens(), shared_prefix_blocks=13, n_layers=n_layers,
                       nan_fill=nan_fill)
 
 
-CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+# the workloads by their index (1 tiny decode .. 5 prefix-shared tail), as bench.py --workload takes them
+BY_INDEX = {1: tiny_decode, 2: qwen3_0_6b_decode, 3: qwen3_0_6b_mixed_step, 4: qwen3_8b_decode,
+            5: prefix_shared_tail}
 
 
 # ---- byte / flop accounting used by the benchmark -------------------------------
