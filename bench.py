@@ -10,9 +10,11 @@ Printed JSON line (rank 0):
   value      KV GB/s of the whole step (algorithmic bytes: every visible K/V
              row read once, plus the new rows read and written) over the step
              time measured with CUDA events around a CUDA graph of K steps;
-  e2e        the same metric through the Python binding with the step's
-             inputs copied from pinned host memory and its outputs read back
-             inside the timed region;
+  e2e        the same metric through the Python binding, per step: one copy
+             of every layer's q and new K/V (and the step's slots, tables and
+             lengths) from pinned host memory, the step's library calls
+             replayed as a CUDA graph, one copy of every layer's output back
+             to pinned host memory;
   roofline   the decode call timed alone per layer (one kernel when every
              sequence and KV head gets its own SMs, else split + combine),
              algorithmic bytes per launch over its duration, against the
@@ -244,24 +246,29 @@ class DecodeStep:
         # write, then the decode's kernels (the write runs inside the decode with append)
         self.kernels_per_step = self.L * ((0 if append else 1) + self.decode_kernels)
 
-    def write(self, l):
+    # Layer l uses pool l % n_layers; its q, new K/V and output default to that
+    # pool's resident tensors, and the end-to-end run passes its own.
+    def write(self, l, kn=None, vn=None):
         c, i = self.case, l % self.case.n_layers
-        self.pa.kv_cache_write(c.k_new[i], c.v_new[i], c.slot_mapping, c.k_cache[i], c.v_cache[i])
+        kn, vn = (c.k_new[i], c.v_new[i]) if kn is None else (kn, vn)
+        self.pa.kv_cache_write(kn, vn, c.slot_mapping, c.k_cache[i], c.v_cache[i])
 
-    def decode(self, l):
+    def decode(self, l, q=None, out=None, kn=None, vn=None):
         c, i = self.case, l % self.case.n_layers
+        q = c.q[i] if q is None else q
+        out = self.out[i] if out is None else out
         if self.append:
-            self.pa.paged_attn_decode_append(c.q[i], c.k_new[i], c.v_new[i], c.k_cache[i], c.v_cache[i],
-                                             c.block_tables, c.context_lens, c.scale, out=self.out[i],
-                                             workspace=self.ws, max_context_len=c.max_context_len)
+            kn, vn = (c.k_new[i], c.v_new[i]) if kn is None else (kn, vn)
+            self.pa.paged_attn_decode_append(q, kn, vn, c.k_cache[i], c.v_cache[i], c.block_tables,
+                                             c.context_lens, c.scale, out=out, workspace=self.ws,
+                                             max_context_len=c.max_context_len)
         elif self.window:
-            self.pa.paged_attn_decode_window(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
-                                             c.scale, self.window, out=self.out[i], workspace=self.ws,
+            self.pa.paged_attn_decode_window(q, c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
+                                             c.scale, self.window, out=out, workspace=self.ws,
                                              max_context_len=c.max_context_len)
         else:
-            self.pa.paged_attn_decode(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
-                                      c.scale, out=self.out[i], workspace=self.ws,
-                                      max_context_len=c.max_context_len)
+            self.pa.paged_attn_decode(q, c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens, c.scale,
+                                      out=out, workspace=self.ws, max_context_len=c.max_context_len)
 
     def run(self):
         for l in range(self.L):
@@ -307,14 +314,16 @@ class DecodeStepQ8(DecodeStep):
         self.step_bytes = self.L * (self.decode_bytes_layer + self.write_bytes_layer)
         self.pool_bytes = sum(t.numel() * t.element_size() for t in self.q8[0])
 
-    def write(self, l):
+    def write(self, l, kn=None, vn=None):
         c, i = self.case, l % self.case.n_layers
-        self.pa.kv_cache_write_q8(c.k_new[i], c.v_new[i], c.slot_mapping, *self.q8[i])
+        kn, vn = (c.k_new[i], c.v_new[i]) if kn is None else (kn, vn)
+        self.pa.kv_cache_write_q8(kn, vn, c.slot_mapping, *self.q8[i])
 
-    def decode(self, l):
+    def decode(self, l, q=None, out=None, kn=None, vn=None):
         c, i = self.case, l % self.case.n_layers
-        self.pa.paged_attn_decode_q8(c.q[i], *self.q8[i], c.block_tables, c.context_lens, c.scale,
-                                     out=self.out[i], workspace=self.ws, max_context_len=c.max_context_len)
+        self.pa.paged_attn_decode_q8(c.q[i] if q is None else q, *self.q8[i], c.block_tables, c.context_lens,
+                                     c.scale, out=self.out[i] if out is None else out, workspace=self.ws,
+                                     max_context_len=c.max_context_len)
 
 
 class MixedStep:
@@ -395,37 +404,58 @@ def time_replays(g, n: int, stream) -> float:
 
 
 def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream):
-    """Same metric through the public API with host buffers: per step, for
-    each layer call copy q / new K,V from pinned host memory (and once per step
-    the slots, block tables and lengths), run write + decode, and read the
-    output back to pinned host memory."""
+    """Same metric through the public API with host buffers, the way a serving
+    loop runs a decode step: per step one host-to-device copy, from pinned host
+    memory, of every layer's q and new K/V rows and of the step's slots, block
+    tables and lengths; the step's library calls (write + decode per layer,
+    replayed as a CUDA graph of those calls); one device-to-host copy of every
+    layer's output into pinned host memory.  Every layer has its own inputs
+    and output; the pools are the resident ones the step cycles."""
     import torch
-    c = step.case
-    n = c.n_layers
-    host_q = [t.cpu().pin_memory() for t in c.q]
-    host_k = [t.cpu().pin_memory() for t in c.k_new]
-    host_v = [t.cpu().pin_memory() for t in c.v_new]
-    host_meta = [(c.slot_mapping, c.slot_mapping.cpu().pin_memory()),
-                 (c.block_tables, c.block_tables.cpu().pin_memory()),
-                 (c.context_lens, c.context_lens.cpu().pin_memory())]
-    host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in step.out]
+    c, L, n = step.case, step.L, step.case.n_layers
+    dev = c.q[0].device
+    align = lambda x: (x + 255) // 256 * 256
     nbytes = lambda t: t.numel() * t.element_size()
-    h2d = sum(nbytes(host_q[l % n]) + nbytes(host_k[l % n]) + nbytes(host_v[l % n]) for l in range(step.L))
-    h2d += sum(nbytes(h) for _, h in host_meta)
-    d2h = sum(nbytes(host_out[l % n]) for l in range(step.L))
+    # input layout: q of every layer, then new K, new V of every layer, then the step's metadata
+    parts, off = [], 0
+    for l in range(L):
+        for src in (c.q[l % n], c.k_new[l % n], c.v_new[l % n]):
+            parts.append((src, off))
+            off = align(off + nbytes(src))
+    meta = (c.slot_mapping, c.block_tables, c.context_lens)
+    for src in meta:
+        parts.append((src, off))
+        off = align(off + nbytes(src))
+    host_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dev_in = torch.empty(off, dtype=torch.uint8, device=dev)
+    views = []
+    for src, o in parts:
+        host_in[o:o + nbytes(src)].copy_(src.contiguous().view(torch.uint8).view(-1).cpu())
+        views.append(dev_in[o:o + nbytes(src)].view(src.dtype).view(src.shape))
+    out_size = align(nbytes(step.out[0]))
+    dev_out = torch.empty(L * out_size, dtype=torch.uint8, device=dev)
+    host_out = torch.empty(L * out_size, dtype=torch.uint8).pin_memory()
+    outs = [dev_out[l * out_size:l * out_size + nbytes(step.out[0])].view(step.out[0].dtype).view(step.out[0].shape)
+            for l in range(L)]
+    h2d, d2h = off, L * out_size
+
+    def calls():
+        for dst, src in zip(meta, views[3 * L:]):   # the step's metadata, staged above
+            dst.copy_(src, non_blocking=True)
+        for l in range(L):
+            q, kn, vn = views[3 * l:3 * l + 3]
+            if not getattr(step, "append", False):
+                step.write(l, kn, vn)
+            step.decode(l, q=q, out=outs[l], kn=kn, vn=vn)
+
+    dev_in.copy_(host_in)               # staged once before the graph's warm-up call and capture
+    torch.cuda.synchronize()
+    graph = graph_of(calls, 1, stream)
 
     def one():
-        for dev_t, host_t in host_meta:
-            dev_t.copy_(host_t, non_blocking=True)
-        for l in range(step.L):
-            i = l % n
-            c.q[i].copy_(host_q[i], non_blocking=True)
-            c.k_new[i].copy_(host_k[i], non_blocking=True)
-            c.v_new[i].copy_(host_v[i], non_blocking=True)
-            if not getattr(step, "append", False):
-                step.write(l)
-            step.decode(l)
-            host_out[i].copy_(step.out[i], non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
+        graph.replay()
+        host_out.copy_(dev_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
