@@ -85,6 +85,9 @@ def open_library(path: str):
     lib.oracle_paged_attn_prefill_window.argtypes = [P, i32, P, P, i64, i32, i32, i32, P, P, P,
                                                      i32, P, i32, i32, f64, i32, P, i32]
     lib.oracle_paged_attn_prefill_window.restype = ctypes.c_int
+    lib.oracle_paged_attn_prefill_q8.argtypes = [P, i32, P, P, P, P, i64, i32, i32, i32, P, P, P, i32, P, i32, i32,
+                                                 f64, P, i32]
+    lib.oracle_paged_attn_prefill_q8.restype = ctypes.c_int
     lib.oracle_kv_cache_write_q8.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P, i32, P, i64]
     lib.oracle_kv_cache_write_q8.restype = i64
     lib.oracle_gather_head_q8.argtypes = [P, P, P, P, i64, i32, i32, i32, P, i32, i32, P, P]
@@ -307,6 +310,28 @@ def paged_attn_prefill_window(q, k_cache, v_cache, chunk_starts, chunk_lens, blo
                                                   _ptr(cs), _ptr(cl), _ptr(bt), bt.shape[1], _ptr(ctx),
                                                   cs.shape[0], hq, float(scale), int(window), _ptr(out),
                                                   num_threads)
+    if rc != 0:
+        raise ValueError(f"oracle prefill rejected its inputs (code {rc})")
+    return out
+
+
+def paged_attn_prefill_q8(q, k_codes, v_codes, k_scale, v_scale, chunk_starts, chunk_lens, block_tables,
+                          context_lens, scale: float, dtype: int, num_threads: int = 0) -> np.ndarray:
+    """fp64 causal chunked prefill over an int8 pool ("Модуль 04", section 5:
+    keys and values are the dequantised fp32 numbers code * scale)."""
+    qb = _bits(q)
+    kc, vc = np.ascontiguousarray(k_codes, np.int8), np.ascontiguousarray(v_codes, np.int8)
+    ks, vs = np.ascontiguousarray(k_scale, np.float32), np.ascontiguousarray(v_scale, np.float32)
+    nb, bs, hkv, d = kc.shape
+    rows, hq, dq = qb.shape
+    cs = np.ascontiguousarray(chunk_starts, dtype=np.int32)
+    cl = np.ascontiguousarray(chunk_lens, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros((rows, hq, d), np.float64)
+    rc = _load().oracle_paged_attn_prefill_q8(_ptr(qb), dtype, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb, bs, hkv,
+                                              d, _ptr(cs), _ptr(cl), _ptr(bt), bt.shape[1], _ptr(ctx), cs.shape[0],
+                                              hq, float(scale), _ptr(out), num_threads)
     if rc != 0:
         raise ValueError(f"oracle prefill rejected its inputs (code {rc})")
     return out

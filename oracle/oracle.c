@@ -666,6 +666,9 @@ int oracle_paged_attn_prefill(const uint16_t *q, int32_t dtype,
 /* Chunked prefill with a sliding window of W keys (W = 0: none) [P2 sections
  * 4 and 5.2]: row i of chunk c, at position p = chunk_starts[c] + i, sees keys
  * max(0, p - W + 1) .. p. */
+static int prefill_problem(problem_t *P, const int32_t *chunk_starts, const int32_t *chunk_lens,
+                           const int32_t *context_lens, int32_t num_chunks, int32_t num_threads);
+
 int oracle_paged_attn_prefill_window(const uint16_t *q, int32_t dtype, const uint16_t *k_cache,
                                      const uint16_t *v_cache, int64_t num_blocks, int32_t block_size,
                                      int32_t num_kv_heads, int32_t head_dim, const int32_t *chunk_starts,
@@ -674,6 +677,33 @@ int oracle_paged_attn_prefill_window(const uint16_t *q, int32_t dtype, const uin
                                      int32_t num_q_heads, double scale, int32_t window, double *out,
                                      int32_t num_threads) {
   if (window < 0) return -4;
+  problem_t P = {q, dtype, k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim,
+                 block_tables, max_blocks_per_seq, num_q_heads, scale, out};
+  P.window = window;
+  return prefill_problem(&P, chunk_starts, chunk_lens, context_lens, num_chunks, num_threads);
+}
+
+/* The same chunked prefill on the int8 pool [P2 section 5]: keys and values
+ * are the dequantised fp32 numbers of KV8Cache.read. */
+int oracle_paged_attn_prefill_q8(const uint16_t *q, int32_t dtype, const int8_t *k_cache, const int8_t *v_cache,
+                                 const float *k_scale, const float *v_scale, int64_t num_blocks,
+                                 int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                 const int32_t *chunk_starts, const int32_t *chunk_lens,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens, int32_t num_chunks, int32_t num_q_heads,
+                                 double scale, double *out, int32_t num_threads) {
+  problem_t P = {q, dtype, NULL, NULL, num_blocks, block_size, num_kv_heads, head_dim,
+                 block_tables, max_blocks_per_seq, num_q_heads, scale, out};
+  P.k8 = k_cache;
+  P.v8 = v_cache;
+  P.k_scale = k_scale;
+  P.v_scale = v_scale;
+  return prefill_problem(&P, chunk_starts, chunk_lens, context_lens, num_chunks, num_threads);
+}
+
+static int prefill_problem(problem_t *P, const int32_t *chunk_starts, const int32_t *chunk_lens,
+                           const int32_t *context_lens, int32_t num_chunks, int32_t num_threads) {
+  const int32_t max_blocks_per_seq = P->max_blocks_per_seq, block_size = P->block_size;
   int32_t *row0 = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_chunks > 0 ? num_chunks : 1));
   int rc = 0;
   int32_t acc = 0;
@@ -686,11 +716,11 @@ int oracle_paged_attn_prefill_window(const uint16_t *q, int32_t dtype, const uin
       rc = -4;
   }
   if (rc == 0) {
-    problem_t P = {q, dtype, k_cache, v_cache, num_blocks, block_size, num_kv_heads, head_dim,
-                   block_tables, max_blocks_per_seq, num_q_heads, scale, out,
-                   num_chunks, row0, chunk_lens, chunk_starts};
-    P.window = window;
-    rc = run_problem(&P, num_threads);
+    P->num_groups = num_chunks;
+    P->group_row0 = row0;
+    P->group_nrows = chunk_lens;
+    P->group_pos0 = chunk_starts;
+    rc = run_problem(P, num_threads);
   }
   free(row0);
   return rc;
