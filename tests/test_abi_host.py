@@ -213,3 +213,39 @@ def test_decode_append_checks_its_arguments(lib):
     assert call(kn=0) == -1
     assert call(vn=0) == -1
     assert call(kn=P + 8) == -9
+
+
+def test_header_is_plain_c_and_links_against_the_library(lib, tmp_path):
+    # a C99 translation unit that includes the header, takes the address of every
+    # declared entry point, links against the library and calls the pure-host ones
+    names = declared_entry_points()
+    src = tmp_path / "use_header.c"
+    refs = "\n".join(f"  (entry_fn)&{n}," for n in names)
+    src.write_text(f"""#include <stdio.h>
+#include "pagedattn.h"
+typedef void (*entry_fn)(void);
+static const entry_fn table[] = {{
+{refs}
+}};
+int main(void) {{
+  pa_allocator *a = NULL;
+  int32_t ids[3];
+  if (pa_abi_version() != PA_ABI_VERSION) return 1;
+  if (pa_allocator_create(64, &a) != PA_OK) return 2;
+  if (pa_allocator_allocate(a, 3, ids) != PA_OK || ids[0] != 0 || ids[2] != 2) return 3;
+  pa_allocator_destroy(a);
+  printf("%d %s\\n", (int)(sizeof(table) / sizeof(table[0])), pa_status_string(PA_ERR_NO_BLOCKS));
+  return 0;
+}}
+""")
+    import subprocess
+    exe = tmp_path / "use_header"
+    include = os.path.join(ROOT, "include")
+    libdir = os.path.dirname(pa.LIB_PATH)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", include, str(src),
+                        "-o", str(exe), "-L", libdir, "-lpagedattn", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, (run.returncode, run.stdout, run.stderr)
+    assert run.stdout.split()[0] == str(len(names)) and "PA_ERR_NO_BLOCKS" in run.stdout
