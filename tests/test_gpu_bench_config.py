@@ -1,0 +1,76 @@
+"""Parity in the launch configuration the benchmark times: the bench's own step
+objects, captured as one CUDA graph of the whole step (every layer's calls,
+programmatic dependent launch between them) and replayed several times, then
+checked against the oracle: pools bit-exact after the writes, every layer's
+decode output (or each distinct pool's last one) and the mixed step's prefill
+output within tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from gpu_util import ORACLE_DTYPE, bits, check_close
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(autouse=True)
+def _clean_error_word():
+    import paged_kv_gqa_cache_gb300 as pa
+    pa.get_device_error()
+    yield
+    st, detail = pa.get_device_error()
+    assert st == 0, f"unexpected device error {pa.STATUS.get(st, st)} at index {detail}"
+
+
+def _replay(step_fn, times=3):
+    stream = torch.cuda.Stream(device=DEV)
+    g = bench.graph_of(step_fn, 1, stream)
+    bench.time_replays(g, times, stream)
+    torch.cuda.synchronize()
+
+
+def _check_decode_step(step, layers_to_check):
+    c = step.case
+    before = [(bits(c.k_cache[i]), bits(c.v_cache[i])) for i in layers_to_check]
+    _replay(step.run)
+    bt, ctx = c.block_tables.cpu().numpy(), c.context_lens.cpu().numpy()
+    for (kh, vh), i in zip(before, layers_to_check):
+        assert oracle.kv_cache_write(kh, vh, bits(c.k_new[i]), bits(c.v_new[i]), c.slot_mapping.cpu().numpy()) == 0
+        assert np.array_equal(bits(c.k_cache[i]), kh) and np.array_equal(bits(c.v_cache[i]), vh), f"pool {i}"
+        ref = oracle.paged_attn_decode(bits(c.q[i]), kh, vh, bt, ctx, c.scale, ORACLE_DTYPE[c.dtype])
+        check_close(step.out[i], ref, f"{step.desc[:40]}, pool {i}")
+
+
+def test_qwen3_0_6b_decode_step_as_benchmarked():
+    step = bench.DecodeStep(DEV, workload=2)          # 28 layers, 28 distinct pools
+    _check_decode_step(step, range(step.case.n_layers))
+
+
+def test_qwen3_0_6b_decode_step_with_the_fused_append():
+    step = bench.DecodeStep(DEV, workload=2, append=True)
+    _check_decode_step(step, range(step.case.n_layers))
+
+
+def test_qwen3_8b_decode_as_benchmarked():
+    step = bench.DecodeStep(DEV, workload=4)          # 36 layers cycling 4 pools of 1 GiB
+    _check_decode_step(step, range(step.case.n_layers))
+
+
+def test_mixed_step_as_benchmarked():
+    step = bench.MixedStep(DEV, overlap=True)         # 28 layers, 2 pools, prefill beside decode
+    c = step.case
+    before = [(bits(c.k_cache[i]), bits(c.v_cache[i])) for i in range(2)]
+    _replay(step.run)
+    for i, (kh, vh) in enumerate(before):
+        assert oracle.kv_cache_write(kh, vh, bits(c.k_new[i]), bits(c.v_new[i]), c.slot_mapping.cpu().numpy()) == 0
+        assert np.array_equal(bits(c.k_cache[i]), kh) and np.array_equal(bits(c.v_cache[i]), vh)
+        refp = oracle.paged_attn_prefill(bits(c.q_chunks[i]), kh, vh, c.chunk_starts.cpu().numpy(),
+                                         c.chunk_lens.cpu().numpy(), c.chunk_block_tables.cpu().numpy(),
+                                         c.chunk_context_lens.cpu().numpy(), c.scale, oracle.BF16)
+        check_close(step.out_p[i], refp, f"mixed step prefill, pool {i}")
+        refd = oracle.paged_attn_decode(bits(c.q[i]), kh, vh, c.block_tables.cpu().numpy(),
+                                        c.context_lens.cpu().numpy(), c.scale, oracle.BF16)
+        check_close(step.out_d[i], refd, f"mixed step decode, pool {i}")
