@@ -1,4 +1,5 @@
-// Split-K paged GQA decode for sm_103a.
+// Paged GQA decode for sm_103a: one 2-CTA cluster per (sequence, KV head) when
+// those fit on the SMs, else split-K over balanced page ranges plus a combine.
 //
 // Computes, for every sequence s and query head g (page "Модуль 12: Финальный
 // проект: мини-движок инференса", qwen_serve/model.py, Qwen3Model.forward with
@@ -26,8 +27,18 @@
 // per page of K and one of V: the TMA engine's cost grows with the number of
 // boxes, so a page is never split) and guarded by one mbarrier each.  One page of K feeds all G query
 // heads of its KV head: the scores for G heads come from a single read of K.
-// All arithmetic is fp32 on the CUDA cores: decode reads each K/V byte once and
-// does G multiply-adds per element, far below the tensor-core ridge point.
+// The arithmetic runs on the CUDA cores (fp32; exact int32 dot products for the
+// keys of an int8 pool): decode reads each K/V byte once and does G
+// multiply-adds per element, far below the tensor-core ridge point.
+//
+// The one-cluster path (decode_item_kernel) gives each (sequence, KV head) its
+// own 16 warps, interleaving its pages over them; the two CTAs merge their
+// warps in shared memory and then through the cluster, with no workspace and
+// no second launch.
+//
+// Options: an int8 pool (codes with per-token scales; "Модуль 04", section 5),
+// a sliding window, and the KV write of each sequence's new token fused into
+// the page that holds it.
 #include <type_traits>
 
 #include "pa_device.cuh"
