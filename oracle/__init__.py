@@ -69,6 +69,15 @@ def open_library(path: str):
     lib.oracle_qk_norm_rope_kv_write.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, i32, P, P, i64, i32, i32,
                                                  P, P, P, i64, i32, i32, i32]
     lib.oracle_qk_norm_rope_kv_write.restype = i64
+    lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_f64.restype = f64
+    lib.oracle_f64_to_e4m3.argtypes = [f64]
+    lib.oracle_f64_to_e4m3.restype = ctypes.c_uint8
+    lib.oracle_kv_cache_write_f8.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P, i32, P, i64]
+    lib.oracle_kv_cache_write_f8.restype = i64
+    lib.oracle_paged_attn_decode_f8.argtypes = [P, i32, P, P, P, P, i64, i32, i32, i32, P, i32, P,
+                                                i32, i32, f64, P, i32]
+    lib.oracle_paged_attn_decode_f8.restype = ctypes.c_int
     lib.oracle_kv_block_copy.argtypes = [P, P, i64, i32, i32, i32, P, i64]
     lib.oracle_kv_block_copy.restype = i64
     lib.oracle_gather_head.argtypes = [P, P, ctypes.c_int, i64, i32, i32, i32, P, i32, i32, P, P]
@@ -312,6 +321,47 @@ def paged_attn_prefill_window(q, k_cache, v_cache, chunk_starts, chunk_lens, blo
                                                   num_threads)
     if rc != 0:
         raise ValueError(f"oracle prefill rejected its inputs (code {rc})")
+    return out
+
+
+def e4m3_to_f64(code: int) -> float:
+    return float(_load().oracle_e4m3_to_f64(int(code) & 0xff))
+
+
+def f64_to_e4m3(x: float) -> int:
+    """The E4M3 pattern nearest to x (ties to even, saturating at 448)."""
+    return int(_load().oracle_f64_to_e4m3(float(x)))
+
+
+def kv_cache_write_f8(k_codes, v_codes, k_scale, v_scale, k, v, dtype: int, slot_mapping) -> int:
+    """In-place write into an fp8 (E4M3) pool: scale = max|x| / 448 + 1e-8 per
+    (token, KV head), code = e4m3(x / scale).  Codes uint8 [nb, 16, Hkv, d],
+    scales fp32 [nb, Hkv, 16] (modified in place).  Returns #skipped slots."""
+    for a, t in ((k_codes, np.uint8), (v_codes, np.uint8), (k_scale, np.float32), (v_scale, np.float32)):
+        assert a.dtype == t and a.flags.c_contiguous
+    nb, bs, hkv, d = k_codes.shape
+    kb, vb = _bits(k), _bits(v)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    return int(_load().oracle_kv_cache_write_f8(_ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale), nb, bs,
+                                                hkv, d, _ptr(kb), _ptr(vb), dtype, _ptr(sm), sm.shape[0]))
+
+
+def paged_attn_decode_f8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale: float,
+                         dtype: int, num_threads: int = 0) -> np.ndarray:
+    """fp64 decode over an fp8 (E4M3) pool: keys and values are e4m3 * scale."""
+    qb = _bits(q)
+    kc, vc = np.ascontiguousarray(k_codes, np.uint8), np.ascontiguousarray(v_codes, np.uint8)
+    ks, vs = np.ascontiguousarray(k_scale, np.float32), np.ascontiguousarray(v_scale, np.float32)
+    nb, bs, hkv, d = kc.shape
+    s, hq, dq = qb.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros((s, hq, d), np.float64)
+    rc = _load().oracle_paged_attn_decode_f8(_ptr(qb), dtype, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb, bs, hkv,
+                                             d, _ptr(bt), bt.shape[1], _ptr(ctx), s, hq, float(scale), _ptr(out),
+                                             num_threads)
+    if rc != 0:
+        raise ValueError(f"oracle decode rejected its inputs (code {rc})")
     return out
 
 

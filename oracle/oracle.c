@@ -125,6 +125,50 @@ uint16_t oracle_f64_to_16(double x, int dtype) {
 
 static uint16_t narrow(double x, int dtype) { return oracle_f64_to_16(x, dtype); }
 
+/*
+ * FP8 E4M3 (the "fn" variant: 4 exponent bits, bias 7, 3 fraction bits, no
+ * infinity, S.1111.111 is NaN, largest finite 448).  Decoding: exponent field
+ * 0 is subnormal, f * 2^-9; otherwise (1 + f / 8) * 2^(e - 7).
+ */
+double oracle_e4m3_to_f64(uint8_t c) {
+  const int sign = (c >> 7) & 1, e = (c >> 3) & 0xf, f = c & 7;
+  double mag;
+  if (e == 15 && f == 7) {
+    mag = NAN;
+  } else if (e == 0) {
+    mag = ldexp((double)f, -9);
+  } else {
+    mag = ldexp((double)(8 + f), e - 10);
+  }
+  return sign ? -mag : mag;
+}
+
+/*
+ * The E4M3 value nearest to x, ties to even; magnitudes that round beyond
+ * 448 saturate to 448 (the "satfinite" conversion).  A finite value of
+ * magnitude in [2^e, 2^(e+1)), e >= -6, is a multiple of 2^(e - 3); below 2^-6
+ * of 2^-9.
+ */
+uint8_t oracle_f64_to_e4m3(double x) {
+  const uint8_t sign = signbit(x) ? 0x80 : 0;
+  if (isnan(x)) return (uint8_t)(sign | 0x7f);
+  double a = fabs(x);
+  if (a > 448.0) a = 448.0;
+  int e2;
+  frexp(a, &e2);
+  int e = a == 0.0 ? -6 : e2 - 1;
+  if (e < -6) e = -6;
+  const double quantum = ldexp(1.0, e - 3);
+  double r = nearbyint(a / quantum) * quantum;
+  if (r > 448.0) r = 448.0;
+  if (r == 0.0) return sign;
+  frexp(r, &e2);
+  e = e2 - 1;
+  if (e < -6) return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));      /* subnormal */
+  const uint8_t frac = (uint8_t)(r / ldexp(1.0, e - 3) - 8.0);
+  return (uint8_t)(sign | ((e + 7) << 3) | frac);
+}
+
 /* ---- KV write [P1, PagedKVCache.write] ------------------------------------- */
 
 /*
@@ -371,20 +415,20 @@ int64_t oracle_kv_cache_write_q8(int8_t *k_cache, int8_t *v_cache, float *k_scal
 static int gather_range_q8(const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
                            const float *v_scale, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                            int32_t head_dim, const int32_t *block_table_row, int32_t kv_head, int32_t from,
-                           int32_t upto, double *k_out, double *v_out);
+                           int32_t upto, int fp8, double *k_out, double *v_out);
 
 int oracle_gather_head_q8(const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
                           const float *v_scale, int64_t num_blocks, int32_t block_size,
                           int32_t num_kv_heads, int32_t head_dim, const int32_t *block_table_row,
                           int32_t kv_head, int32_t upto, double *k_out, double *v_out) {
   return gather_range_q8(k_cache, v_cache, k_scale, v_scale, num_blocks, block_size, num_kv_heads, head_dim,
-                         block_table_row, kv_head, 0, upto, k_out, v_out);
+                         block_table_row, kv_head, 0, upto, 0, k_out, v_out);
 }
 
 static int gather_range_q8(const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
                            const float *v_scale, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                            int32_t head_dim, const int32_t *block_table_row, int32_t kv_head, int32_t from,
-                           int32_t upto, double *k_out, double *v_out) {
+                           int32_t upto, int fp8, double *k_out, double *v_out) {
   k_out -= (int64_t)from * head_dim;
   v_out -= (int64_t)from * head_dim;
   for (int32_t j = from; j < upto; ++j) {
@@ -396,8 +440,11 @@ static int gather_range_q8(const int8_t *k_cache, const int8_t *v_cache, const f
     const int64_t sidx = (block * num_kv_heads + kv_head) * block_size + offset;
     const float ks = k_scale[sidx], vs = v_scale[sidx];
     for (int32_t x = 0; x < head_dim; ++x) {
-      const float kf = (float)k_cache[base + x] * ks;
-      const float vf = (float)v_cache[base + x] * vs;
+      /* a code's value: the integer (int8) or the E4M3 number (fp8), times its scale in fp32 */
+      const float kc = fp8 ? (float)oracle_e4m3_to_f64((uint8_t)k_cache[base + x]) : (float)k_cache[base + x];
+      const float vc = fp8 ? (float)oracle_e4m3_to_f64((uint8_t)v_cache[base + x]) : (float)v_cache[base + x];
+      const float kf = kc * ks;
+      const float vf = vc * vs;
       k_out[(int64_t)j * head_dim + x] = (double)kf;
       v_out[(int64_t)j * head_dim + x] = (double)vf;
     }
@@ -460,6 +507,8 @@ typedef struct {
   const float *k_scale, *v_scale;
   /* sliding window W (0: none): row at position p sees keys max(0, p - W + 1) .. p */
   int32_t window;
+  /* with k8: the codes are E4M3 numbers instead of integers */
+  int fp8;
 } problem_t;
 
 static void run_item(problem_t *P, int32_t g, int32_t h, double *kk, double *vv,
@@ -472,7 +521,7 @@ static void run_item(problem_t *P, int32_t g, int32_t h, double *kk, double *vv,
   const int32_t glo = (P->window > 0 && pos0 - P->window + 1 > 0) ? pos0 - P->window + 1 : 0;
   const int32_t *bt_row = P->block_tables + (int64_t)g * P->max_blocks_per_seq;
   const int grc = P->k8 ? gather_range_q8(P->k8, P->v8, P->k_scale, P->v_scale, P->num_blocks, P->block_size,
-                                          P->num_kv_heads, d, bt_row, h, glo, nkeys, kk, vv)
+                                          P->num_kv_heads, d, bt_row, h, glo, nkeys, P->fp8, kk, vv)
                         : gather_range(P->k_cache, P->v_cache, P->dtype, P->num_blocks, P->block_size,
                                        P->num_kv_heads, d, bt_row, h, glo, nkeys, kk, vv);
   if (grc != 0) {
@@ -600,6 +649,66 @@ int oracle_paged_attn_decode_q8(const uint16_t *q, int32_t dtype, const int8_t *
   P.v8 = v_cache;
   P.k_scale = k_scale;
   P.v_scale = v_scale;
+  return decode_problem(&P, context_lens, num_seqs, num_threads);
+}
+
+/*
+ * The fp8 pool: the int8 pool's layout and per-(token, KV head) scales, with
+ * E4M3 codes.  Write, per token and KV head, for K and for V: the values x
+ * widened exactly to fp32, scale = max |x| / 448 + 1e-8 and code =
+ * e4m3(x / scale) (an fp32 division, then the nearest E4M3 value, ties to
+ * even; |x / scale| <= 448 by construction).  Read: e4m3 value * scale in fp32.
+ * Returns the number of skipped slots (outside the pool).
+ */
+int64_t oracle_kv_cache_write_f8(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
+                                 int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                 int32_t head_dim, const uint16_t *k, const uint16_t *v, int32_t dtype,
+                                 const int64_t *slot_mapping, int64_t num_tokens) {
+  int64_t skipped = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= num_blocks * block_size) {
+      ++skipped;
+      continue;
+    }
+    const int64_t block = slot / block_size, offset = slot % block_size;
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      for (int pass = 0; pass < 2; ++pass) {
+        const uint16_t *src = (pass == 0 ? k : v) + (t * num_kv_heads + h) * (int64_t)head_dim;
+        uint8_t *dst = (pass == 0 ? k_cache : v_cache) + (slot * num_kv_heads + h) * (int64_t)head_dim;
+        float *scl = pass == 0 ? k_scale : v_scale;
+        float amax = 0.0f;
+        for (int32_t x = 0; x < head_dim; ++x) {
+          const float a = fabsf((float)widen(src[x], dtype));
+          if (a > amax) amax = a;
+        }
+        float scale = amax / 448.0f;
+        scale = scale + 1e-8f;
+        for (int32_t x = 0; x < head_dim; ++x) {
+          const float y = (float)widen(src[x], dtype) / scale;
+          dst[x] = oracle_f64_to_e4m3((double)y);
+        }
+        scl[(block * num_kv_heads + h) * block_size + offset] = scale;
+      }
+    }
+  }
+  return skipped;
+}
+
+/* Decode over the fp8 pool: keys and values are e4m3 value * scale. */
+int oracle_paged_attn_decode_f8(const uint16_t *q, int32_t dtype, const uint8_t *k_cache,
+                                const uint8_t *v_cache, const float *k_scale, const float *v_scale,
+                                int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                int32_t head_dim, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                double scale, double *out, int32_t num_threads) {
+  problem_t P = {q, dtype, NULL, NULL, num_blocks, block_size, num_kv_heads, head_dim,
+                 block_tables, max_blocks_per_seq, num_q_heads, scale, out};
+  P.k8 = (const int8_t *)k_cache;
+  P.v8 = (const int8_t *)v_cache;
+  P.k_scale = k_scale;
+  P.v_scale = v_scale;
+  P.fp8 = 1;
   return decode_problem(&P, context_lens, num_seqs, num_threads);
 }
 
