@@ -683,7 +683,7 @@ int64_t oracle_kv_cache_write_f8(uint8_t *k_cache, uint8_t *v_cache, float *k_sc
           if (a > amax) amax = a;
         }
         float scale = amax / 448.0f;
-        scale = scale + 1e-8f;
+        scale += 1e-8f;
         for (int32_t x = 0; x < head_dim; ++x) {
           const float y = (float)widen(src[x], dtype) / scale;
           dst[x] = oracle_f64_to_e4m3((double)y);
