@@ -688,7 +688,8 @@ int64_t oracle_kv_cache_write_f8(uint8_t *k_cache, uint8_t *v_cache, float *k_sc
           const float y = (float)widen(src[x], dtype) / scale;
           dst[x] = oracle_f64_to_e4m3((double)y);
         }
-        scl[(block * num_kv_heads + h) * block_size + offset] = scale;
+        const int64_t sidx = (block * num_kv_heads + h) * block_size + offset;   /* [block][head][offset] */
+        scl[sidx] = scale;
       }
     }
   }
