@@ -59,9 +59,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pools", type=int, default=0,
                     help="distinct layer pools held on the device (0 = the workload's default)")
-    ap.add_argument("--kv", choices=["16bit", "int8"], default="16bit",
-                    help="decode workloads: the workload's 16-bit pool, or an int8 pool (codes + one fp32 scale "
-                         "per token and KV head) holding the same tokens quantised")
+    ap.add_argument("--kv", choices=["16bit", "int8", "fp8"], default="16bit",
+                    help="decode workloads: the workload's 16-bit pool, or an int8 / fp8 (E4M3) pool (codes + "
+                         "one fp32 scale per token and KV head) holding the same tokens quantised")
     ap.add_argument("--append", action="store_true",
                     help="decode workloads: each layer's KV write fused into its decode call "
                          "(paged_attn_decode_append) instead of a separate kv_cache_write")
@@ -80,9 +80,9 @@ def parse_args(argv=None):
                     help="2 = the Qwen3-0.6B 28-layer decode step (default); 3, 4, 5 = the mixed prefill "
                          "step, the Qwen3-8B decode and the prefix-shared long tail (diagnostic lines)")
     args = ap.parse_args(argv)
-    if args.window < 0 or (args.window and (args.workload == 5 or args.kv == "int8")):
+    if args.window < 0 or (args.window and (args.workload == 5 or args.kv != "16bit")):
         ap.error("--window takes W >= 0, with workloads 2, 3 and 4 on the 16-bit pool")
-    if args.append and (args.window or args.kv == "int8" or args.workload == 3):
+    if args.append and (args.window or args.kv != "16bit" or args.workload == 3):
         ap.error("--append applies to the 16-bit decode workloads 2, 4 and 5 without a window")
     return args
 
@@ -283,14 +283,19 @@ class DecodeStep:
 
 class DecodeStepQ8(DecodeStep):
     """The same decode step over int8 pools ("Модуль 04: KV-кэш и арифметика
-    памяти", section 5): every cached token of each 16-bit layer pool is
-    quantised once into an int8 pool by the library's own write; each layer of
-    the step then quantises the new tokens into their slots and decodes."""
+    памяти", section 5), or fp8 E4M3 pools (sections 5.1 and 5.4) with fp8:
+    every cached token of each 16-bit layer pool is quantised once into an
+    8-bit pool by the library's own write; each layer of the step then
+    quantises the new tokens into their slots and decodes."""
 
-    def __init__(self, device, workload: int = 2, pools: int = 0):
+    def __init__(self, device, workload: int = 2, pools: int = 0, fp8: bool = False):
         import numpy as np
         import torch
         super().__init__(device, workload, pools)
+        self.fp8 = fp8
+        alloc = self.pa.alloc_pool_f8 if fp8 else self.pa.alloc_pool_q8
+        self._write = self.pa.kv_cache_write_f8 if fp8 else self.pa.kv_cache_write_q8
+        self._decode = self.pa.paged_attn_decode_f8 if fp8 else self.pa.paged_attn_decode_q8
         c = self.case
         bt = c.block_tables.cpu().numpy()
         slots = []
@@ -300,10 +305,10 @@ class DecodeStepQ8(DecodeStep):
         sl = torch.from_numpy(np.unique(np.concatenate(slots))).to(device)
         self.q8 = []
         for i in range(c.n_layers):
-            pool = self.pa.alloc_pool_q8(c.num_blocks, c.hkv, device)
+            pool = alloc(c.num_blocks, c.hkv, device)
             rows_k = c.k_cache[i].view(-1, c.hkv, 128)[sl].contiguous()
             rows_v = c.v_cache[i].view(-1, c.hkv, 128)[sl].contiguous()
-            self.pa.kv_cache_write_q8(rows_k, rows_v, sl, *pool)
+            self._write(rows_k, rows_v, sl, *pool)
             self.q8.append(pool)
             del rows_k, rows_v
         torch.cuda.synchronize()
@@ -317,13 +322,12 @@ class DecodeStepQ8(DecodeStep):
     def write(self, l, kn=None, vn=None):
         c, i = self.case, l % self.case.n_layers
         kn, vn = (c.k_new[i], c.v_new[i]) if kn is None else (kn, vn)
-        self.pa.kv_cache_write_q8(kn, vn, c.slot_mapping, *self.q8[i])
+        self._write(kn, vn, c.slot_mapping, *self.q8[i])
 
     def decode(self, l, q=None, out=None, kn=None, vn=None):
         c, i = self.case, l % self.case.n_layers
-        self.pa.paged_attn_decode_q8(c.q[i] if q is None else q, *self.q8[i], c.block_tables, c.context_lens,
-                                     c.scale, out=self.out[i] if out is None else out, workspace=self.ws,
-                                     max_context_len=c.max_context_len)
+        self._decode(c.q[i] if q is None else q, *self.q8[i], c.block_tables, c.context_lens, c.scale,
+                     out=self.out[i] if out is None else out, workspace=self.ws, max_context_len=c.max_context_len)
 
 
 class MixedStep:
@@ -500,7 +504,8 @@ def cpu_baseline(step: DecodeStep, seconds: float):
             x = host(l % c.n_layers)
             t0 = time.perf_counter()
             if q8 is not None:
-                oracle.paged_attn_decode_q8(x[0], *x[1], bt, ctx, c.scale, odt, num_threads=threads)
+                (oracle.paged_attn_decode_f8 if step.fp8 else oracle.paged_attn_decode_q8)(
+                    x[0], *x[1], bt, ctx, c.scale, odt, num_threads=threads)
             elif window:
                 oracle.paged_attn_decode_window(x[0], x[1], x[2], bt, ctx, c.scale, window, odt, num_threads=threads)
             else:
@@ -537,7 +542,7 @@ def run_ours(args):
     if args.workload == 3:
         return run_mixed(args, dev, pa)
 
-    step = (DecodeStepQ8(dev, args.workload, args.pools) if args.kv == "int8"
+    step = (DecodeStepQ8(dev, args.workload, args.pools, args.kv == "fp8") if args.kv != "16bit"
             else DecodeStep(dev, args.workload, args.pools, args.window, args.append))
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
@@ -571,13 +576,15 @@ def run_ours(args):
     q8 = isinstance(step, DecodeStepQ8)
     pool_mib = (step.pool_bytes if q8 else 2 * step.case.k_cache[0].numel() * 2) / 2**20
     win = getattr(step, "window", 0)
-    tag = "_q8" if q8 else (f"_window{win}" if win else ("_append" if getattr(step, "append", False) else ""))
+    tag = (("_f8" if step.fp8 else "_q8") if q8 else
+           (f"_window{win}" if win else ("_append" if getattr(step, "append", False) else "")))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8" if q8 else step.dtype, "data": "synthetic",
-        "config": {"workload": step.desc + (", int8 KV pool (codes + one fp32 scale per token and KV head), "
-                                            f"{step.dtype} q and out" if q8 else "")
+        "vs_baseline": None, "data": "synthetic",
+        "dtype": ("fp8_e4m3" if step.fp8 else "int8") if q8 else step.dtype,
+        "config": {"workload": step.desc + (f", {'fp8 E4M3' if step.fp8 else 'int8'} KV pool (codes + one fp32 "
+                                            f"scale per token and KV head), {step.dtype} q and out" if q8 else "")
                                + (f", sliding window of {win} keys (bytes of the visible rows)" if win else "")
                                + (", KV write fused into the decode call" if getattr(step, "append", False) else ""),
                    "global_batch": step.S * world, "seq_len": step.case.max_context_len,

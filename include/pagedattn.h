@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 4
+#define PA_ABI_VERSION 5
 #define PA_HEAD_DIM 128
 #define PA_BLOCK_SIZE 16
 #define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
@@ -259,6 +259,31 @@ PA_API pa_status pa_kv_cache_write_q8(const void *k, const void *v, int32_t dtyp
  * workspace (pa_decode_workspace_bytes) and errors as pa_paged_attn_decode.
  */
 PA_API pa_status pa_paged_attn_decode_q8(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_context_len, float scale, void *out, void *workspace,
+                                         size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * ---- fp8 KV pool [P2 sections 5.1 and 5.4 (FP8 storage of K and V)] --------
+ * The pa_kv_pool_q8 layout and scales with FP8 E4M3 codes (the "fn" format:
+ * bias 7, 3 fraction bits, largest finite 448, no infinity) in k_cache and
+ * v_cache instead of int8 integers.
+ *
+ * kv_cache_write_f8 — as pa_kv_cache_write_q8 with scale = max |x| / 448 +
+ * 1e-8 and code = the E4M3 value nearest to the fp32 quotient x / scale (ties
+ * to even; the quotient never exceeds 448 in magnitude), so codes and scales
+ * are bit-exact.  Same arguments and errors.
+ */
+PA_API pa_status pa_kv_cache_write_f8(const void *k, const void *v, int32_t dtype, const int64_t *slot_mapping,
+                                      int32_t num_tokens, const pa_kv_pool_q8 *pool, pa_stream_t stream);
+
+/*
+ * paged_attn_decode_f8 — pa_paged_attn_decode over an fp8 pool: keys and
+ * values are the dequantised numbers e4m3(code) * scale.  Arguments, workspace
+ * (pa_decode_workspace_bytes) and errors as pa_paged_attn_decode_q8.
+ */
+PA_API pa_status pa_paged_attn_decode_f8(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool,
                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
                                          const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                                          int32_t max_context_len, float scale, void *out, void *workspace,

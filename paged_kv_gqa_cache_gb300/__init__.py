@@ -13,6 +13,8 @@ Calls (see include/pagedattn.h for the full contract):
   block_tables, context_lens, scale, ...)``
 * ``kv_cache_write_q8`` / ``paged_attn_decode_q8`` on an int8 pool
   (``alloc_pool_q8``: codes plus one fp32 scale per token and KV head)
+* ``kv_cache_write_f8`` / ``paged_attn_decode_f8`` on an fp8 pool
+  (``alloc_pool_f8``: the same layout with E4M3 codes held as uint8)
 * ``paged_attn_decode_window`` / ``paged_attn_prefill_chunk_window``: sliding window
 * ``qk_norm_rope_kv_write``: q/k RMSNorm + rotary embedding fused into the KV write
 * ``kv_block_copy(pools, pairs)``: copy-on-write block copy over every layer
@@ -42,6 +44,7 @@ EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_deco
            "pa_paged_attn_prefill_chunk", "pa_get_device_error", "pa_status_string",
            "pa_last_cuda_error", "pa_abi_version", "pa_paged_attn_decode_noalloc",
            "pa_decode_kernel_launches", "pa_kv_cache_write_q8", "pa_paged_attn_decode_q8",
+           "pa_kv_cache_write_f8", "pa_paged_attn_decode_f8",
            "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
            "pa_qk_norm_rope_kv_write", "pa_paged_attn_decode_append", "pa_selftest_bounded_wait",
            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
@@ -99,6 +102,10 @@ def load_library(path: str = LIB_PATH):
         lib.pa_paged_attn_decode_q8.argtypes = [P, i32, q8_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P,
                                                 ctypes.c_size_t, P]
         lib.pa_paged_attn_decode_q8.restype = i32
+        lib.pa_kv_cache_write_f8.argtypes = lib.pa_kv_cache_write_q8.argtypes
+        lib.pa_kv_cache_write_f8.restype = i32
+        lib.pa_paged_attn_decode_f8.argtypes = lib.pa_paged_attn_decode_q8.argtypes
+        lib.pa_paged_attn_decode_f8.restype = i32
         lib.pa_kv_cache_write.argtypes = [P, P, P, i32, pool_p, P]
         lib.pa_kv_cache_write.restype = i32
         lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -225,9 +232,15 @@ def alloc_pool_q8(num_blocks: int, num_kv_heads: int, device=None):
     return codes(), codes(), scales(), scales()
 
 
-def make_pool_q8(k_codes, v_codes, k_scale, v_scale) -> KVPoolQ8:
-    _need(k_codes, "k_codes", torch.int8)
-    _need(v_codes, "v_codes", torch.int8)
+def alloc_pool_f8(num_blocks: int, num_kv_heads: int, device=None):
+    """An fp8 pool: the int8 pool's layout with E4M3 codes stored as uint8."""
+    k, v, ks, vs = alloc_pool_q8(num_blocks, num_kv_heads, device)
+    return k.view(torch.uint8), v.view(torch.uint8), ks, vs
+
+
+def make_pool_q8(k_codes, v_codes, k_scale, v_scale, code_dtype=torch.int8) -> KVPoolQ8:
+    _need(k_codes, "k_codes", code_dtype)
+    _need(v_codes, "v_codes", code_dtype)
     _need(k_scale, "k_scale", torch.float32)
     _need(v_scale, "v_scale", torch.float32)
     if k_codes.dim() != 4 or k_codes.shape != v_codes.shape:
@@ -239,9 +252,10 @@ def make_pool_q8(k_codes, v_codes, k_scale, v_scale) -> KVPoolQ8:
 
 
 def kv_cache_write_q8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_codes: torch.Tensor,
-                      v_codes: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor, stream=None) -> None:
+                      v_codes: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor, stream=None,
+                      _fp8: bool = False) -> None:
     """Quantise new K/V rows [T, Hkv, 128] (fp16 / bf16) into flat slots of an int8 pool."""
-    pool = make_pool_q8(k_codes, v_codes, k_scale, v_scale)
+    pool = make_pool_q8(k_codes, v_codes, k_scale, v_scale, torch.uint8 if _fp8 else torch.int8)
     _need(k, "k")
     _need(v, "v", k.dtype)
     _need(slot_mapping, "slot_mapping", torch.int64)
@@ -249,16 +263,18 @@ def kv_cache_write_q8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tens
     if k.shape != (T, pool.num_kv_heads, pool.head_dim) or v.shape != k.shape:
         raise ValueError(f"k, v must be [{T}, {pool.num_kv_heads}, {pool.head_dim}]")
     lib = load_library()
-    _check(lib.pa_kv_cache_write_q8(k.data_ptr(), v.data_ptr(), _dtype_code(k), slot_mapping.data_ptr(), T,
-                                    ctypes.byref(pool), _stream(stream)), "pa_kv_cache_write_q8")
+    fn, name = (lib.pa_kv_cache_write_f8, "pa_kv_cache_write_f8") if _fp8 else \
+        (lib.pa_kv_cache_write_q8, "pa_kv_cache_write_q8")
+    _check(fn(k.data_ptr(), v.data_ptr(), _dtype_code(k), slot_mapping.data_ptr(), T, ctypes.byref(pool),
+              _stream(stream)), name)
 
 
 def paged_attn_decode_q8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor, k_scale: torch.Tensor,
                          v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                          scale: float, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                         max_context_len: Optional[int] = None, stream=None) -> torch.Tensor:
+                         max_context_len: Optional[int] = None, stream=None, _fp8: bool = False) -> torch.Tensor:
     """Decode attention over an int8 pool: q [S, Hq, 128] (fp16 / bf16) → out, same dtype."""
-    pool = make_pool_q8(k_codes, v_codes, k_scale, v_scale)
+    pool = make_pool_q8(k_codes, v_codes, k_scale, v_scale, torch.uint8 if _fp8 else torch.int8)
     _need(q, "q")
     _need(block_tables, "block_tables", torch.int32)
     _need(context_lens, "context_lens", torch.int32)
@@ -274,11 +290,27 @@ def paged_attn_decode_q8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.
         workspace = alloc_decode_workspace(S, hq, pool.num_kv_heads, mcl, q.device)
     _need(workspace, "workspace")
     lib = load_library()
-    _check(lib.pa_paged_attn_decode_q8(q.data_ptr(), _dtype_code(q), ctypes.byref(pool), block_tables.data_ptr(),
-                                       mb, context_lens.data_ptr(), S, hq, mcl, float(scale), out.data_ptr(),
-                                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                       _stream(stream)), "pa_paged_attn_decode_q8")
+    fn, name = (lib.pa_paged_attn_decode_f8, "pa_paged_attn_decode_f8") if _fp8 else \
+        (lib.pa_paged_attn_decode_q8, "pa_paged_attn_decode_q8")
+    _check(fn(q.data_ptr(), _dtype_code(q), ctypes.byref(pool), block_tables.data_ptr(), mb, context_lens.data_ptr(),
+              S, hq, mcl, float(scale), out.data_ptr(), workspace.data_ptr(),
+              workspace.numel() * workspace.element_size(), _stream(stream)), name)
     return out
+
+
+def kv_cache_write_f8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_codes: torch.Tensor,
+                      v_codes: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor, stream=None) -> None:
+    """Quantise new K/V rows [T, Hkv, 128] (fp16 / bf16) into flat slots of an fp8 (E4M3) pool."""
+    kv_cache_write_q8(k, v, slot_mapping, k_codes, v_codes, k_scale, v_scale, stream, _fp8=True)
+
+
+def paged_attn_decode_f8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor, k_scale: torch.Tensor,
+                         v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                         scale: float, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                         max_context_len: Optional[int] = None, stream=None) -> torch.Tensor:
+    """Decode attention over an fp8 (E4M3) pool: q [S, Hq, 128] (fp16 / bf16) → out, same dtype."""
+    return paged_attn_decode_q8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale, out,
+                                workspace, max_context_len, stream, _fp8=True)
 
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int) -> int:

@@ -251,9 +251,9 @@ __device__ __forceinline__ void append_row(uint8_t *stage, const DecodeParams &p
 // the lane's 4 dims).  pbuf2 is the warp's [16 keys][G] scratch for the
 // probabilities.  With int8 codes a key's scale multiplies its dot product
 // once, and a value's scale multiplies its probability before the sum.
-template <typename T, int G, bool Q8>
+template <typename T, int G, bool Q8, bool F8>
 __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
-                                            const QReg<Q8> (&q)[G][Layout<G>::DPL / 2], const float (&qsc)[G],
+                                            const QReg<Q8 && !F8> (&q)[G][Layout<G>::DPL / 2], const float (&qsc)[G],
                                             float2 (&o)[G][2], float (&m)[G], float (&l)[G], float2 *pbuf2,
                                             int lane) {
   using Ly = Layout<G>;
@@ -281,7 +281,14 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
       const int chunk = qd + NQ * ((i + rot) % CPL);  // dims 8 chunk .. 8 chunk + 7
-      if constexpr (Q8) {
+      if constexpr (F8) {  // E4M3 codes to fp32 (exact), then as the 16-bit path
+        const uint2 u = *reinterpret_cast<const uint2 *>(kst + t * 128 + chunk * 8);
+        const float2 k2[4] = {e4m3x2_to_f2<0>(u.x), e4m3x2_to_f2<1>(u.x), e4m3x2_to_f2<0>(u.y), e4m3x2_to_f2<1>(u.y)};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int gg = 0; gg < G; ++gg) acc[gg] = __ffma2_rn(q[gg][i * 4 + e], k2[e], acc[gg]);
+      } else if constexpr (Q8) {
         const uint2 u = *reinterpret_cast<const uint2 *>(kst + t * 128 + chunk * 8);
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {  // int16 query pairs x int8 codes, exact in int32
@@ -305,7 +312,7 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
       float a;
-      if constexpr (Q8) {
+      if constexpr (Q8 && !F8) {
         int ia = iacc[gg];  // |partial| < 2^31: 128 products of at most 2^15 x 2^7
 #pragma unroll
         for (int off = 1; off < NQ; off <<= 1) ia += __shfl_xor_sync(FULL, ia, off);
@@ -314,6 +321,7 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
         a = acc[gg].x + acc[gg].y;
 #pragma unroll
         for (int off = 1; off < NQ; off <<= 1) a += __shfl_xor_sync(FULL, a, off);
+        if constexpr (F8) a *= ksc;
       }
       sc[ps][gg] = (t >= nlo && t < nv) ? a : neg_inf;
     }
@@ -348,7 +356,11 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
   // weighted sum of values: this lane owns dims [4 * lane, 4 * lane + 4)
   auto pv_token = [&](int t) {
     float2 v01, v23;
-    if constexpr (Q8) {
+    if constexpr (F8) {
+      const uint32_t w = *reinterpret_cast<const uint32_t *>(vst + t * 128 + 4 * lane);
+      v01 = e4m3x2_to_f2<0>(w);
+      v23 = e4m3x2_to_f2<1>(w);
+    } else if constexpr (Q8) {
       const uint32_t w = *reinterpret_cast<const uint32_t *>(vst + t * 128 + 4 * lane);
       v01 = s8x2_to_f2<0>(w);
       v23 = s8x2_to_f2<1>(w);
@@ -384,8 +396,8 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
 
 // int8 pools: more CTAs per SM (the int16 query leaves room) to hide the
 // latency of the heavier per-byte arithmetic; 16-bit pools: as many as fit.
-template <typename T, int G, bool Q8>
-__global__ void __launch_bounds__(NW * 32, Q8 ? (G >= 8 ? 2 : G >= 4 ? 3 : 4) : 1)
+template <typename T, int G, bool Q8, bool F8>
+__global__ void __launch_bounds__(NW * 32, (Q8 && !F8) ? (G >= 8 ? 2 : G >= 4 ? 3 : 4) : 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const DecodeParams p) {
   using Ly = Layout<G>;
@@ -473,7 +485,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   // ---- consumer state ---------------------------------------------------------
   // Packed fp32x2 arithmetic (FFMA2): q and the partial scores pair adjacent
   // dims, the output accumulators pair adjacent dims of one head.
-  QReg<Q8> q[G][DPL / 2];
+  QReg<Q8 && !F8> q[G][DPL / 2];
   float qsc[G];
   float2 o[G][2];
   float m[G], l[G];
@@ -488,7 +500,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // new item: load its G query rows (pre-scaled into the log2 domain)
       const T *qp = reinterpret_cast<const T *>(p.q) +
                     ((int64_t)cc.s * p.num_q_heads + (int64_t)cc.h * G) * kHeadDim;
-      load_q<T, G, Q8>(qp, p.scale_log2, lane, q, qsc);
+      load_q<T, G, Q8 && !F8>(qp, p.scale_log2, lane, q, qsc);
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
         m[gg] = neg_inf;
@@ -521,7 +533,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           appended = true;
         }
       }
-      decode_page<T, G, Q8>(stages + st * SST, cc.page == 0 ? lo_in_first : 0, nv, q, qsc, o, m, l, pbuf2, lane);
+      decode_page<T, G, Q8, F8>(stages + st * SST, cc.page == 0 ? lo_in_first : 0, nv, q, qsc, o, m, l, pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
     if (appended) fence_proxy_async_smem();  // the generic writes precede the stage's next copy
@@ -649,7 +661,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
 // and writes the item's output.  No workspace and no second kernel.
 constexpr int kItemWarps = 8;
 
-template <typename T, int G, bool Q8>
+template <typename T, int G, bool Q8, bool F8>
 __global__ void __launch_bounds__(kItemWarps * 32, 1)
 decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                    const DecodeParams p) {
@@ -700,13 +712,13 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   int32_t win = (gw + nw * lane < p.max_blocks_per_seq) ? __ldg(bt + gw + nw * lane) : -1;
   griddep_wait();
 
-  QReg<Q8> q[G][DPL / 2];
+  QReg<Q8 && !F8> q[G][DPL / 2];
   float qsc[G];
   float2 o[G][2];
   float m[G], l[G];
   {
     const T *qp = reinterpret_cast<const T *>(p.q) + ((int64_t)s * p.num_q_heads + (int64_t)h * G) * kHeadDim;
-    load_q<T, G, Q8>(qp, p.scale_log2, lane, q, qsc);
+    load_q<T, G, Q8 && !F8>(qp, p.scale_log2, lane, q, qsc);
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
       m[gg] = -INFINITY;
@@ -768,7 +780,7 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
           fence_proxy_async_smem();
         }
       }
-      decode_page<T, G, Q8>(stages + st * SST, pg == 0 ? lo - first * kBlock : 0, nv, q, qsc, o, m, l, pbuf2,
+      decode_page<T, G, Q8, F8>(stages + st * SST, pg == 0 ? lo - first * kBlock : 0, nv, q, qsc, o, m, l, pbuf2,
                             lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
@@ -889,7 +901,7 @@ int decode_item_ctas(int items, int max_pages_per_item) {
 
 namespace {
 
-template <typename T, int G, bool Q8>
+template <typename T, int G, bool Q8, bool F8>
 cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          int max_workers, int max_pages_per_item, cudaStream_t stream) {
   DecodeParams p = p0;
@@ -899,12 +911,12 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
     const int ismem = item_smem_bytes(G);
     static bool item_configured = false;
     if (!item_configured) {
-      cudaError_t e = cudaFuncSetAttribute(decode_item_kernel<T, G, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(decode_item_kernel<T, G, Q8, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            ismem);
       if (e != cudaSuccess) return e;
       item_configured = true;
     }
-    return launch_pdl_cluster(decode_item_kernel<T, G, Q8>, dim3(items * ctas), dim3(kItemWarps * 32), ismem, ctas,
+    return launch_pdl_cluster(decode_item_kernel<T, G, Q8, F8>, dim3(items * ctas), dim3(kItemWarps * 32), ismem, ctas,
                               stream, kmap, vmap, p);
   }
   const int smem = split_smem_bytes(G, p.num_seqs, Q8);
@@ -913,11 +925,11 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
   // the hot path and out of CUDA-graph capture after the first call).
   static int configured_smem = 0, cached_per_sm = 0;
   if (smem > configured_smem) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, G, Q8>,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, G, Q8, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<T, G, Q8>, NW * 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<T, G, Q8, F8>, NW * 32, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     configured_smem = smem;
@@ -931,7 +943,7 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
   if (grid < 1) grid = 1;
   if (grid * NW > kDecodeMaxWorkers) grid = kDecodeMaxWorkers / NW;
   p.num_workers = grid * NW;
-  e = launch_pdl(decode_split_kernel<T, G, Q8>, dim3(grid), dim3(NW * 32), smem, stream, kmap, vmap, p);
+  e = launch_pdl(decode_split_kernel<T, G, Q8, F8>, dim3(grid), dim3(NW * 32), smem, stream, kmap, vmap, p);
   if (e != cudaSuccess) return e;
   const int cgrid = (p.num_seqs * p.num_q_heads + 3) / 4;
   return launch_pdl(decode_combine_kernel<T, G>, dim3(cgrid), dim3(128), 0, stream, p);
@@ -963,12 +975,13 @@ bool decode_workspace_carve(void *ws, size_t bytes, int num_seqs, int num_q_head
 }
 
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          int dtype, int group, int max_workers, int max_pages_per_item, bool q8,
+                          int dtype, int group, int max_workers, int max_pages_per_item, bool q8, bool f8,
                           cudaStream_t stream) {
 #define PA_DECODE_CASE(T, G)                                                                    \
   if (group == G)                                                                               \
-    return q8 ? launch_typed<T, G, true>(p, kmap, vmap, max_workers, max_pages_per_item, stream) \
-              : launch_typed<T, G, false>(p, kmap, vmap, max_workers, max_pages_per_item, stream);
+    return f8   ? launch_typed<T, G, true, true>(p, kmap, vmap, max_workers, max_pages_per_item, stream)  \
+           : q8 ? launch_typed<T, G, true, false>(p, kmap, vmap, max_workers, max_pages_per_item, stream) \
+                : launch_typed<T, G, false, false>(p, kmap, vmap, max_workers, max_pages_per_item, stream);
   if (dtype == PA_BF16) {
     PA_DECODE_CASE(__nv_bfloat16, 1)
     PA_DECODE_CASE(__nv_bfloat16, 2)

@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
 // warp per (token, KV head) row of 128 values: lane j owns values 4j .. 4j + 3,
 // the row maximum is a warp reduction, each lane stores its 4 codes as one
 // 32-bit word and lane 0 stores the scale.
-template <typename T>
+template <typename T, bool F8>
 __global__ void __launch_bounds__(256) kv_write_q8_kernel(const WriteQ8Params p) {
   griddep_wait();
   griddep_launch_dependents();
@@ -65,13 +65,22 @@ __global__ void __launch_bounds__(256) kv_write_q8_kernel(const WriteQ8Params p)
       float amax = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, off));
-      const float scale = __fadd_rn(__fdiv_rn(amax, 127.f), 1e-8f);
+      const float scale = __fadd_rn(__fdiv_rn(amax, F8 ? 448.f : 127.f), 1e-8f);
       const float x[4] = {a.x, a.y, b.x, b.y};
       uint32_t word = 0;
+      if constexpr (F8) {  // the nearest E4M3 value, ties to even (|x / scale| <= 448 by construction)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float c = fminf(fmaxf(rintf(__fdiv_rn(x[e], scale)), -127.f), 127.f);
-        word |= ((uint32_t)(int)c & 0xffu) << (8 * e);
+        for (int e = 0; e < 4; e += 2) {
+          const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(
+              make_float2(__fdiv_rn(x[e], scale), __fdiv_rn(x[e + 1], scale)), __NV_SATFINITE, __NV_E4M3);
+          word |= (uint32_t)c2 << (8 * e);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float c = fminf(fmaxf(rintf(__fdiv_rn(x[e], scale)), -127.f), 127.f);
+          word |= ((uint32_t)(int)c & 0xffu) << (8 * e);
+        }
       }
       int8_t *dst = pass == 0 ? p.k_cache : p.v_cache;
       reinterpret_cast<uint32_t *>(dst + (slot * p.num_kv_heads + h) * kHeadDim)[lane] = word;
@@ -82,14 +91,18 @@ __global__ void __launch_bounds__(256) kv_write_q8_kernel(const WriteQ8Params p)
 
 }  // namespace
 
-cudaError_t launch_kv_write_q8(const WriteQ8Params &p, int dtype, cudaStream_t stream) {
+cudaError_t launch_kv_write_q8(const WriteQ8Params &p, int dtype, bool f8, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.num_tokens * p.num_kv_heads;
   int64_t grid = (rows + 7) / 8;
   const int64_t cap = (int64_t)sm_count() * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  return dtype == PA_BF16 ? launch_pdl(kv_write_q8_kernel<__nv_bfloat16>, dim3((unsigned)grid), dim3(256), 0, stream, p)
-                          : launch_pdl(kv_write_q8_kernel<__half>, dim3((unsigned)grid), dim3(256), 0, stream, p);
+  const dim3 g((unsigned)grid), b(256);
+  if (f8)
+    return dtype == PA_BF16 ? launch_pdl(kv_write_q8_kernel<__nv_bfloat16, true>, g, b, 0, stream, p)
+                            : launch_pdl(kv_write_q8_kernel<__half, true>, g, b, 0, stream, p);
+  return dtype == PA_BF16 ? launch_pdl(kv_write_q8_kernel<__nv_bfloat16, false>, g, b, 0, stream, p)
+                          : launch_pdl(kv_write_q8_kernel<__half, false>, g, b, 0, stream, p);
 }
 
 cudaError_t launch_kv_write(const WriteParams &p, cudaStream_t stream) {

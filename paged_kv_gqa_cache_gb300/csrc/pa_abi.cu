@@ -129,7 +129,7 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
                       const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                       int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
                       void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream,
-                      const void *k_new = nullptr, const void *v_new = nullptr) {
+                      const void *k_new = nullptr, const void *v_new = nullptr, bool f8 = false) {
   const bool q8 = pool8 != nullptr;
   const int num_kv_heads = q8 ? pool8->num_kv_heads : pool16->num_kv_heads;
   const int num_blocks = q8 ? pool8->num_blocks : pool16->num_blocks;
@@ -187,7 +187,7 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
   const int64_t pages_hint = (int64_t)num_seqs * num_kv_heads * item_pages;
   int64_t workers = (pages_hint + 3) / 4;
   if (workers > kDecodeMaxWorkers) workers = kDecodeMaxWorkers;
-  cudaError_t e = launch_decode(p, kmap, vmap, dtype, group, (int)workers, item_pages, q8, stream);
+  cudaError_t e = launch_decode(p, kmap, vmap, dtype, group, (int)workers, item_pages, q8, q8 && f8, stream);
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
@@ -312,8 +312,11 @@ pa_status pa_paged_attn_decode_window(const void *q, const pa_kv_pool *pool, con
                      static_cast<cudaStream_t>(stream));
 }
 
-pa_status pa_kv_cache_write_q8(const void *k, const void *v, int32_t dtype, const int64_t *slot_mapping,
-                               int32_t num_tokens, const pa_kv_pool_q8 *pool, pa_stream_t stream) {
+namespace {
+
+// The quantising write into an 8-bit pool: int8 codes, or E4M3 codes when f8.
+pa_status write_8bit(const void *k, const void *v, int32_t dtype, const int64_t *slot_mapping, int32_t num_tokens,
+                     const pa_kv_pool_q8 *pool, bool f8, pa_stream_t stream) {
   pa_status st = check_pool_q8(pool);
   if (st != PA_OK) return st;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
@@ -335,8 +338,32 @@ pa_status pa_kv_cache_write_q8(const void *k, const void *v, int32_t dtype, cons
   p.num_tokens = num_tokens;
   p.num_kv_heads = pool->num_kv_heads;
   p.err = d->err;
-  cudaError_t e = launch_kv_write_q8(p, dtype, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_kv_write_q8(p, dtype, f8, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status decode_8bit(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                      int32_t num_q_heads, int32_t max_context_len, float scale, void *out, void *workspace,
+                      size_t workspace_bytes, bool f8, pa_stream_t stream) {
+  pa_status st = check_pool_q8(pool);
+  if (st != PA_OK) return st;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  return decode_call(q, dtype, nullptr, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, max_context_len, scale, 0, out, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), nullptr, nullptr, f8);
+}
+
+}  // namespace
+
+pa_status pa_kv_cache_write_q8(const void *k, const void *v, int32_t dtype, const int64_t *slot_mapping,
+                               int32_t num_tokens, const pa_kv_pool_q8 *pool, pa_stream_t stream) {
+  return write_8bit(k, v, dtype, slot_mapping, num_tokens, pool, false, stream);
+}
+
+pa_status pa_kv_cache_write_f8(const void *k, const void *v, int32_t dtype, const int64_t *slot_mapping,
+                               int32_t num_tokens, const pa_kv_pool_q8 *pool, pa_stream_t stream) {
+  return write_8bit(k, v, dtype, slot_mapping, num_tokens, pool, true, stream);
 }
 
 pa_status pa_paged_attn_decode_q8(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool,
@@ -344,12 +371,17 @@ pa_status pa_paged_attn_decode_q8(const void *q, int32_t dtype, const pa_kv_pool
                                   const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                                   int32_t max_context_len, float scale, void *out, void *workspace,
                                   size_t workspace_bytes, pa_stream_t stream) {
-  pa_status st = check_pool_q8(pool);
-  if (st != PA_OK) return st;
-  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
-  return decode_call(q, dtype, nullptr, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                     num_q_heads, max_context_len, scale, 0, out, workspace, workspace_bytes,
-                     static_cast<cudaStream_t>(stream));
+  return decode_8bit(q, dtype, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                     max_context_len, scale, out, workspace, workspace_bytes, false, stream);
+}
+
+pa_status pa_paged_attn_decode_f8(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_context_len, float scale, void *out, void *workspace,
+                                  size_t workspace_bytes, pa_stream_t stream) {
+  return decode_8bit(q, dtype, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                     max_context_len, scale, out, workspace, workspace_bytes, true, stream);
 }
 
 pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t *chunk_starts,

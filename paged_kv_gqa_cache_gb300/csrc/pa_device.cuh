@@ -8,6 +8,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -254,6 +255,16 @@ __device__ __forceinline__ float2 s8x2_to_f2(uint32_t w) {
   const float lo = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u + 2 * I));
   const float hi = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541u + 2 * I));
   return __fadd2_rn(make_float2(lo, hi), make_float2(-8388736.f, -8388736.f));
+}
+
+// ---- FP8 (E4M3) codes → fp32 -------------------------------------------------
+// Codes 2i and 2i + 1 of the word w, exactly (every E4M3 value is a half):
+// one packed conversion to fp16 pairs, then widening.
+template <int I>
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t w) {
+  static_assert(I == 0 || I == 1, "pair index");
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> (16 * I)), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
 // ---- 16-bit → fp32 conversion of packed pairs --------------------------------

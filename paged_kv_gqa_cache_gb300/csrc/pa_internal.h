@@ -47,7 +47,8 @@ struct WriteQ8Params {
   int32_t num_kv_heads;
   int *err;
 };
-cudaError_t launch_kv_write_q8(const WriteQ8Params &p, int dtype, cudaStream_t stream);
+// f8: E4M3 codes with scale = max |x| / 448 + 1e-8 instead of int8 codes.
+cudaError_t launch_kv_write_q8(const WriteQ8Params &p, int dtype, bool f8, cudaStream_t stream);
 
 // ---- q/k RMSNorm + rotary embedding fused into the KV write -------------------------------
 struct RopeWriteParams {
@@ -126,9 +127,10 @@ struct DecodeLaunch {
 // Plans and launches the decode: one CTA per (sequence, KV head) item when the
 // items are few, else the split and combine kernels.  `group` = Hq / Hkv;
 // max_pages_per_item bounds each item's pages (from the host-side max length);
-// q8: the pool holds int8 codes with per-token scales (p.k_scale, p.v_scale).
+// q8: the pool holds 8-bit codes with per-token scales (p.k_scale, p.v_scale):
+// int8 integers, or E4M3 numbers when f8.
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                          int dtype, int group, int max_workers, int max_pages_per_item, bool q8,
+                          int dtype, int group, int max_workers, int max_pages_per_item, bool q8, bool f8,
                           cudaStream_t stream);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads);
 // CTAs per item of the one-launch decode (1 or 2), or 0 when the split path runs.

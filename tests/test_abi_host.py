@@ -47,7 +47,7 @@ def test_only_c_entry_points_are_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 4
+    assert lib.pa_abi_version() == 5
     for code in range(0, -12, -1):
         assert lib.pa_status_string(code).decode().startswith(pa.STATUS[code])
 
@@ -139,8 +139,9 @@ def _pool_q8(**kw):
     return pa.KVPoolQ8(**f)
 
 
-def test_write_q8_rejects_bad_arguments(lib):
-    call = lambda pool=None, **kw: lib.pa_kv_cache_write_q8(
+@pytest.mark.parametrize("fn", ["pa_kv_cache_write_q8", "pa_kv_cache_write_f8"])
+def test_write_q8_rejects_bad_arguments(lib, fn):
+    call = lambda pool=None, **kw: getattr(lib, fn)(
         kw.get("k", P), kw.get("v", P), kw.get("dtype", 0), kw.get("slots", P), kw.get("n", 4),
         ctypes.byref(pool or _pool_q8()), None)
     assert call(n=0) == 0
@@ -155,9 +156,10 @@ def test_write_q8_rejects_bad_arguments(lib):
     assert call(k=P + 2) == -9
 
 
-def test_decode_q8_rejects_bad_arguments(lib):
+@pytest.mark.parametrize("fn", ["pa_paged_attn_decode_q8", "pa_paged_attn_decode_f8"])
+def test_decode_q8_rejects_bad_arguments(lib, fn):
     ws = lib.pa_decode_workspace_bytes(4, 16, 8, 256)
-    call = lambda pool=None, **kw: lib.pa_paged_attn_decode_q8(
+    call = lambda pool=None, **kw: getattr(lib, fn)(
         kw.get("q", P), kw.get("dtype", 1), ctypes.byref(pool or _pool_q8()), kw.get("bt", P), kw.get("mb", 16),
         kw.get("ctx", P), kw.get("S", 4), kw.get("hq", 16), kw.get("mcl", 256), kw.get("scale", 0.088),
         kw.get("out", P), kw.get("ws", P), kw.get("wsb", ws), None)

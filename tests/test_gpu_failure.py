@@ -114,23 +114,26 @@ def test_canaries_survive_prefill_with_a_bad_block():
     _check_all(g, "prefill")
 
 
-def test_canaries_survive_int8_write_and_decode():
+@pytest.mark.parametrize("kind", ["int8", "fp8"])
+def test_canaries_survive_int8_write_and_decode(kind):
     c = workloads.build_case("canary-q8", "f16", 16, 8, seed=5, device=DEV, decode_lens=[5, 64, 700])
-    pool = pa.alloc_pool_q8(c.num_blocks, 8, DEV)
+    f8 = kind == "fp8"
+    pool = (pa.alloc_pool_f8 if f8 else pa.alloc_pool_q8)(c.num_blocks, 8, DEV)
     g = {n: Guarded(t) for n, t in zip(("k_codes", "v_codes", "k_scale", "v_scale"), pool)}
     g["out"] = Guarded(torch.zeros_like(c.q[0]))
     slots = c.slot_mapping.clone()
     slots[0] = -1
-    pa.kv_cache_write_q8(c.k_new[0], c.v_new[0], slots, g["k_codes"].t, g["v_codes"].t, g["k_scale"].t,
-                         g["v_scale"].t)
+    (pa.kv_cache_write_f8 if f8 else pa.kv_cache_write_q8)(c.k_new[0], c.v_new[0], slots, g["k_codes"].t,
+                                                          g["v_codes"].t, g["k_scale"].t, g["v_scale"].t)
     assert pa.get_device_error() == (pa.STATUS_CODE["PA_ERR_RANGE"], 0)
     for bound in (700, 16384):
         bt = torch.full((3, 1024), -1, dtype=torch.int32, device=DEV)
         bt[:, :c.block_tables.shape[1]] = c.block_tables
-        pa.paged_attn_decode_q8(c.q[0], g["k_codes"].t, g["v_codes"].t, g["k_scale"].t, g["v_scale"].t, bt,
-                                c.context_lens, c.scale, out=g["out"].t, max_context_len=bound)
+        (pa.paged_attn_decode_f8 if f8 else pa.paged_attn_decode_q8)(
+            c.q[0], g["k_codes"].t, g["v_codes"].t, g["k_scale"].t, g["v_scale"].t, bt, c.context_lens, c.scale,
+            out=g["out"].t, max_context_len=bound)
         assert pa.get_device_error()[0] == 0
-    _check_all(g, "int8")
+    _check_all(g, kind)
 
 
 def test_canaries_survive_rope_write_and_block_copy():
