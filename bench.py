@@ -65,6 +65,10 @@ def parse_args(argv=None):
     ap.add_argument("--append", action="store_true",
                     help="decode workloads: each layer's KV write fused into its decode call "
                          "(paged_attn_decode_append) instead of a separate kv_cache_write")
+    ap.add_argument("--no-early-pages", action="store_true",
+                    help="decode workloads, 16-bit pool without a window: do not pass PA_DECODE_EARLY_PAGES. By "
+                         "default each decode call fetches its cached pages before the preceding KV write has "
+                         "finished, which the step allows: that write touches only each sequence's last page")
     ap.add_argument("--overlap", action="store_true",
                     help="workload 3: each layer's prefill on a second stream beside its decode (same work)")
     ap.add_argument("--window", type=int, default=0,
@@ -84,6 +88,7 @@ def parse_args(argv=None):
         ap.error("--window takes W >= 0, with workloads 2, 3 and 4 on the 16-bit pool")
     if args.append and (args.window or args.kv != "16bit" or args.workload == 3):
         ap.error("--append applies to the 16-bit decode workloads 2, 4 and 5 without a window")
+    args.early_pages = not args.no_early_pages and not args.window and args.kv == "16bit"
     return args
 
 
@@ -215,7 +220,8 @@ class DecodeStep:
     kv_cache_write of the new tokens then paged_attn_decode (layer pools are
     cycled when fewer distinct pools than calls are held)."""
 
-    def __init__(self, device, workload: int = 2, pools: int = 0, window: int = 0, append: bool = False):
+    def __init__(self, device, workload: int = 2, pools: int = 0, window: int = 0, append: bool = False,
+                 early_pages: bool = False):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
@@ -223,6 +229,7 @@ class DecodeStep:
         self.workload = workload
         self.window = window
         self.append = append
+        self.early_pages = early_pages
         self.desc, default_pools, self.L = WORKLOADS[workload]
         pools = pools or default_pools
         maker = workloads.BY_INDEX[workload]
@@ -261,14 +268,15 @@ class DecodeStep:
             kn, vn = (c.k_new[i], c.v_new[i]) if kn is None else (kn, vn)
             self.pa.paged_attn_decode_append(q, kn, vn, c.k_cache[i], c.v_cache[i], c.block_tables,
                                              c.context_lens, c.scale, out=out, workspace=self.ws,
-                                             max_context_len=c.max_context_len)
+                                             max_context_len=c.max_context_len, early_pages=self.early_pages)
         elif self.window:
             self.pa.paged_attn_decode_window(q, c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
                                              c.scale, self.window, out=out, workspace=self.ws,
                                              max_context_len=c.max_context_len)
         else:
             self.pa.paged_attn_decode(q, c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens, c.scale,
-                                      out=out, workspace=self.ws, max_context_len=c.max_context_len)
+                                      out=out, workspace=self.ws, max_context_len=c.max_context_len,
+                                      early_pages=self.early_pages)
 
     def run(self):
         for l in range(self.L):
@@ -543,7 +551,7 @@ def run_ours(args):
         return run_mixed(args, dev, pa)
 
     step = (DecodeStepQ8(dev, args.workload, args.pools, args.kv == "fp8") if args.kv != "16bit"
-            else DecodeStep(dev, args.workload, args.pools, args.window, args.append))
+            else DecodeStep(dev, args.workload, args.pools, args.window, args.append, args.early_pages))
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_dec = graph_of(step.run_decode_only, 1, stream)
@@ -586,7 +594,9 @@ def run_ours(args):
         "config": {"workload": step.desc + (f", {'fp8 E4M3' if step.fp8 else 'int8'} KV pool (codes + one fp32 "
                                             f"scale per token and KV head), {step.dtype} q and out" if q8 else "")
                                + (f", sliding window of {win} keys (bytes of the visible rows)" if win else "")
-                               + (", KV write fused into the decode call" if getattr(step, "append", False) else ""),
+                               + (", KV write fused into the decode call" if getattr(step, "append", False) else "")
+                               + (", cached pages fetched before the preceding write ends (PA_DECODE_EARLY_PAGES)"
+                                  if getattr(step, "early_pages", False) else ""),
                    "global_batch": step.S * world, "seq_len": step.case.max_context_len,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({step.case.n_layers} distinct pools of {pool_mib:.0f} MiB "

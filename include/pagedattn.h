@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 5
+#define PA_ABI_VERSION 6
 #define PA_HEAD_DIM 128
 #define PA_BLOCK_SIZE 16
 #define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
@@ -152,6 +152,34 @@ PA_API pa_status pa_paged_attn_decode_append(const void *q, const void *k_new, c
                                              int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
                                              float scale, void *out, void *workspace, size_t workspace_bytes,
                                              pa_stream_t stream);
+
+/*
+ * paged_attn_decode_ex — one decode call with every option:
+ *   window        sliding window in keys as pa_paged_attn_decode_window (0: none);
+ *   k_new, v_new  the fused KV write of pa_paged_attn_decode_append (both NULL:
+ *                 none; not combined with a window: PA_ERR_UNSUPPORTED);
+ *   flags         0, or PA_DECODE_EARLY_PAGES: a promise by the caller that the
+ *                 work enqueued on `stream` just before this call writes no
+ *                 pool page this call reads other than each sequence's last
+ *                 visible page (the page of position context_lens[s] - 1), as
+ *                 in a decode step whose KV write adds one token per sequence.
+ *                 When that work is a pa_kv_cache_write, which lets the next
+ *                 kernel start beside the tail of the work before it, the
+ *                 promise covers that earlier work too.  The one-launch path
+ *                 then starts fetching the other pages before that work has
+ *                 finished, overlapping it (the results do not change).
+ *                 Breaking the promise gives undefined results.  Other bits:
+ *                 PA_ERR_UNSUPPORTED.
+ * Other arguments, workspace and errors as pa_paged_attn_decode.  No
+ * counterpart on the pages: a library addition.
+ */
+#define PA_DECODE_EARLY_PAGES 1u
+PA_API pa_status pa_paged_attn_decode_ex(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                         int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                                         float scale, int32_t window, const void *k_new, const void *v_new,
+                                         uint32_t flags, void *out, void *workspace, size_t workspace_bytes,
+                                         pa_stream_t stream);
 
 /*
  * Number of kernels one pa_paged_attn_decode (or _noalloc) call with these

@@ -47,6 +47,7 @@ EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_deco
            "pa_kv_cache_write_f8", "pa_paged_attn_decode_f8",
            "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
            "pa_qk_norm_rope_kv_write", "pa_paged_attn_decode_append", "pa_selftest_bounded_wait",
+           "pa_paged_attn_decode_ex",
            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
            "pa_allocator_release", "pa_allocator_refcount", "pa_allocator_stats_get", "pa_allocator_take_copies",
            "pa_sequence_create", "pa_sequence_destroy", "pa_sequence_reserve", "pa_sequence_commit",
@@ -121,6 +122,9 @@ def load_library(path: str = LIB_PATH):
         lib.pa_paged_attn_decode_append.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P,
                                                     P, ctypes.c_size_t, P]
         lib.pa_paged_attn_decode_append.restype = i32
+        lib.pa_paged_attn_decode_ex.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, i32, P, P,
+                                                ctypes.c_uint32, P, P, ctypes.c_size_t, P]
+        lib.pa_paged_attn_decode_ex.restype = i32
         lib.pa_paged_attn_decode_noalloc.argtypes = [P, pool_p, P, i32, P, i32, i32, i32, ctypes.c_float, P, P]
         lib.pa_paged_attn_decode_noalloc.restype = i32
         lib.pa_paged_attn_prefill_chunk.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
@@ -336,13 +340,18 @@ def alloc_decode_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, m
 def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                       block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                       out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                      max_context_len: Optional[int] = None, stream=None) -> torch.Tensor:
+                      max_context_len: Optional[int] = None, stream=None,
+                      early_pages: bool = False) -> torch.Tensor:
     """Decode attention: q [S, Hq, 128] → out [S, Hq, 128] (pool dtype).
 
     ``max_context_len`` is a host-side bound on ``context_lens`` (no device
-    sync is made to find it); it defaults to the block table's capacity."""
+    sync is made to find it); it defaults to the block table's capacity.
+    ``early_pages``: the caller promises that the work enqueued just before
+    this call writes no page of a sequence but its last visible one (a
+    decode step's KV write), so the pages may be fetched before it ends
+    (``pa_paged_attn_decode_ex`` with ``PA_DECODE_EARLY_PAGES``)."""
     return _decode(q, k_cache, v_cache, block_tables, context_lens, scale, 0, out, workspace, max_context_len,
-                   stream)
+                   stream, flags=DECODE_EARLY_PAGES if early_pages else 0)
 
 
 def paged_attn_decode_window(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -359,7 +368,7 @@ def paged_attn_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.
                              v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                              scale: float, out: Optional[torch.Tensor] = None,
                              workspace: Optional[torch.Tensor] = None, max_context_len: Optional[int] = None,
-                             stream=None) -> torch.Tensor:
+                             stream=None, early_pages: bool = False) -> torch.Tensor:
     """Write each sequence's new token (k_new, v_new [S, Hkv, 128]) at position
     context_lens[s] - 1 of its block table and decode, in one call; otherwise
     as :func:`paged_attn_decode`."""
@@ -368,11 +377,14 @@ def paged_attn_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.
     if k_new.shape != (q.shape[0], k_cache.shape[2], q.shape[2]) or v_new.shape != k_new.shape:
         raise ValueError("k_new and v_new must be [S, Hkv, 128]")
     return _decode(q, k_cache, v_cache, block_tables, context_lens, scale, 0, out, workspace, max_context_len,
-                   stream, append=(k_new, v_new))
+                   stream, append=(k_new, v_new), flags=DECODE_EARLY_PAGES if early_pages else 0)
+
+
+DECODE_EARLY_PAGES = 1
 
 
 def _decode(q, k_cache, v_cache, block_tables, context_lens, scale, window, out, workspace, max_context_len,
-            stream, append=None):
+            stream, append=None, flags=0):
     pool = make_pool(k_cache, v_cache)
     _need(q, "q", k_cache.dtype)
     _need(block_tables, "block_tables", torch.int32)
@@ -390,7 +402,12 @@ def _decode(q, k_cache, v_cache, block_tables, context_lens, scale, window, out,
     _need(workspace, "workspace")
     lib = load_library()
     ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
-    if append is not None:
+    if flags:
+        kn, vn = (append[0].data_ptr(), append[1].data_ptr()) if append is not None else (None, None)
+        _check(lib.pa_paged_attn_decode_ex(q.data_ptr(), ctypes.byref(pool), block_tables.data_ptr(), mb,
+                                           context_lens.data_ptr(), S, hq, mcl, float(scale), window, kn, vn,
+                                           flags, out.data_ptr(), *ws), "pa_paged_attn_decode_ex")
+    elif append is not None:
         _check(lib.pa_paged_attn_decode_append(q.data_ptr(), append[0].data_ptr(), append[1].data_ptr(),
                                                ctypes.byref(pool), block_tables.data_ptr(), mb,
                                                context_lens.data_ptr(), S, hq, mcl, float(scale), out.data_ptr(),

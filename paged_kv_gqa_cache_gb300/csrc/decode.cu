@@ -710,31 +710,10 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
   const int ctx = __ldg(p.context_lens + s);
   int win_base = 0;  // window of 32 block ids: lane j holds page gw + nw (win_base + j)
   int32_t win = (gw + nw * lane < p.max_blocks_per_seq) ? __ldg(bt + gw + nw * lane) : -1;
-  griddep_wait();
-
-  QReg<Q8 && !F8> q[G][DPL / 2];
-  float qsc[G];
-  float2 o[G][2];
-  float m[G], l[G];
-  {
-    const T *qp = reinterpret_cast<const T *>(p.q) + ((int64_t)s * p.num_q_heads + (int64_t)h * G) * kHeadDim;
-    load_q<T, G, Q8 && !F8>(qp, p.scale_log2, lane, q, qsc);
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      m[gg] = -INFINITY;
-      l[gg] = 0.f;
-      o[gg][0] = make_float2(0.f, 0.f);
-      o[gg][1] = make_float2(0.f, 0.f);
-    }
-  }
-  if (ctx < 1 || ctx > p.max_blocks_per_seq * kBlock) {  // uniform over the cluster; output untouched
-    if (h == 0 && rank == 0 && threadIdx.x == 0) set_error(p.err, PA_ERR_RANGE, s);
-    griddep_launch_dependents();
-    return;
-  }
-  const int lo = window_lo(ctx, p.window), first = lo / kBlock;  // first visible key and its page
-  const int pages = (ctx + kBlock - 1) / kBlock - first;            // visible pages
-  const int n = pages > gw ? (pages - gw + nw - 1) / nw : 0;       // pages of this warp
+  const bool ctx_ok = ctx >= 1 && ctx <= p.max_blocks_per_seq * kBlock;  // uniform over the cluster
+  const int lo = ctx_ok ? window_lo(ctx, p.window) : 0, first = lo / kBlock;  // first visible key, its page
+  const int pages = ctx_ok ? (ctx + kBlock - 1) / kBlock - first : 0;         // visible pages
+  const int n = pages > gw ? (pages - gw + nw - 1) / nw : 0;                  // pages of this warp
   if (first != 0) win = (gw + nw * lane < pages) ? __ldg(bt + first + gw + nw * lane) : -1;
 
   uint32_t bad_mask = 0;
@@ -757,8 +736,45 @@ decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     bad_mask = ok ? (bad_mask & ~(1u << st)) : (bad_mask | (1u << st));
   };
 
+  // With early_pages the caller guarantees that the kernels still running
+  // (the one before this one and, behind a KV write, the one before that)
+  // write no page of the sequence but the last visible one (a decode step's
+  // KV write touches only the new token's page), so the first stages of the
+  // other pages are fetched before the wait and overlap those kernels.
   const int npre = n < kStages ? n : kStages;
-  for (int i = 0; i < npre; ++i) issue(i, i);
+  uint32_t deferred = (1u << npre) - 1u;
+  if (p.early_pages) {
+    for (int i = 0; i < npre; ++i) {
+      if (gw + nw * i != pages - 1) {
+        issue(i, i);
+        deferred &= ~(1u << i);
+      }
+    }
+  }
+  griddep_wait();
+  for (int i = 0; i < npre; ++i)
+    if ((deferred >> i) & 1u) issue(i, i);
+
+  QReg<Q8 && !F8> q[G][DPL / 2];
+  float qsc[G];
+  float2 o[G][2];
+  float m[G], l[G];
+  {
+    const T *qp = reinterpret_cast<const T *>(p.q) + ((int64_t)s * p.num_q_heads + (int64_t)h * G) * kHeadDim;
+    load_q<T, G, Q8 && !F8>(qp, p.scale_log2, lane, q, qsc);
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      m[gg] = -INFINITY;
+      l[gg] = 0.f;
+      o[gg][0] = make_float2(0.f, 0.f);
+      o[gg][1] = make_float2(0.f, 0.f);
+    }
+  }
+  if (!ctx_ok) {  // nothing was issued (n = 0); output untouched
+    if (h == 0 && rank == 0 && threadIdx.x == 0) set_error(p.err, PA_ERR_RANGE, s);
+    griddep_launch_dependents();
+    return;
+  }
 
   bool timed_out = false;
   for (int i = 0; i < n; ++i) {

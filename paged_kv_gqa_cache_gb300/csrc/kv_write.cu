@@ -13,10 +13,12 @@ namespace pa {
 namespace {
 
 __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
-  griddep_wait();
-  // the next kernel may start its set-up now; it still waits for this grid to
-  // complete before it reads anything (griddep_wait)
+  // The next kernel (a decode) may start its set-up at once, beside the tail
+  // of the kernel before this one; it still waits for this grid to complete,
+  // which comes after that kernel has completed, before it reads anything
+  // but what it is allowed to read early.
   griddep_launch_dependents();
+  griddep_wait();
   const int64_t total = (int64_t)p.num_tokens * p.row_vecs;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {

@@ -129,7 +129,8 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
                       const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                       int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
                       void *out, void *workspace, size_t workspace_bytes, cudaStream_t stream,
-                      const void *k_new = nullptr, const void *v_new = nullptr, bool f8 = false) {
+                      const void *k_new = nullptr, const void *v_new = nullptr, bool f8 = false,
+                      uint32_t flags = 0) {
   const bool q8 = pool8 != nullptr;
   const int num_kv_heads = q8 ? pool8->num_kv_heads : pool16->num_kv_heads;
   const int num_blocks = q8 ? pool8->num_blocks : pool16->num_blocks;
@@ -178,6 +179,7 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
   p.num_q_heads = num_q_heads;
   p.num_blocks = num_blocks;
   p.window = window;
+  p.early_pages = (flags & PA_DECODE_EARLY_PAGES) ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   // Upper bound on the pages of one item (a window of W keys spans at most
@@ -299,6 +301,21 @@ pa_status pa_paged_attn_decode_append(const void *q, const void *k_new, const vo
   return decode_call(q, pool->dtype, pool, nullptr, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                      num_q_heads, max_context_len, scale, 0, out, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), k_new, v_new);
+}
+
+pa_status pa_paged_attn_decode_ex(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_context_len, float scale, int32_t window,
+                                  const void *k_new, const void *v_new, uint32_t flags, void *out,
+                                  void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_NULL;
+  if (k_new && window != 0) return PA_ERR_UNSUPPORTED;
+  if (flags & ~(uint32_t)PA_DECODE_EARLY_PAGES) return PA_ERR_UNSUPPORTED;
+  return decode_call(q, pool->dtype, pool, nullptr, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, max_context_len, scale, window, out, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream), k_new, v_new, false, flags);
 }
 
 pa_status pa_paged_attn_decode_window(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,

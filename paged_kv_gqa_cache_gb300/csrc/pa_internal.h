@@ -116,6 +116,8 @@ struct DecodeParams {
   int32_t num_blocks;
   int32_t num_workers;       // warps in the launch
   int32_t window;            // sliding window in keys (0: none)
+  int32_t early_pages;       // 1: pages before each sequence's last one are not written by the previous
+                             //    kernel, so the one-launch decode fetches them before its dependency wait
   float scale_log2;          // scale * log2(e)
 };
 

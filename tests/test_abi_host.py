@@ -47,7 +47,7 @@ def test_only_c_entry_points_are_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 5
+    assert lib.pa_abi_version() == 6
     for code in range(0, -12, -1):
         assert lib.pa_status_string(code).decode().startswith(pa.STATUS[code])
 
@@ -174,6 +174,20 @@ def test_decode_q8_rejects_bad_arguments(lib, fn):
     assert call(mcl=300) == -2
     assert call(scale=float("inf")) == -2
     assert call(out=P + 2) == -9
+
+
+def test_decode_ex_checks_its_arguments(lib):
+    pool = _pool()
+    ws = lib.pa_decode_workspace_bytes(4, 16, 8, 256)
+    call = lambda **kw: lib.pa_paged_attn_decode_ex(
+        P, ctypes.byref(pool), P, 16, P, 4, 16, 256, 0.088, kw.get("window", 0), kw.get("kn"), kw.get("vn"),
+        kw.get("flags", 1), kw.get("out", P), P, ws, None)
+    assert call(kn=P) == -1 and call(vn=P) == -1   # k_new and v_new go together
+    assert call(kn=P, vn=P, window=64) == -4       # the fused write takes no window
+    assert call(flags=2) == -4 and call(flags=0x80000001) == -4
+    assert call(window=-1) == -2
+    assert call(out=P + 2) == -9                   # the plain call's checks still apply, before any CUDA call
+    assert call(kn=P + 8, vn=P, out=P) == -9
 
 
 def test_window_calls_check_their_arguments(lib):

@@ -44,18 +44,25 @@ def _check_decode_step(step, layers_to_check):
         check_close(step.out[i], ref, f"{step.desc[:40]}, pool {i}")
 
 
-def test_qwen3_0_6b_decode_step_as_benchmarked():
-    step = bench.DecodeStep(DEV, workload=2)          # 28 layers, 28 distinct pools
+@pytest.mark.parametrize("early", [True, False])   # the bench's default passes PA_DECODE_EARLY_PAGES
+def test_qwen3_0_6b_decode_step_as_benchmarked(early):
+    step = bench.DecodeStep(DEV, workload=2, early_pages=early)     # 28 layers, 28 distinct pools
     _check_decode_step(step, range(step.case.n_layers))
 
 
-def test_qwen3_0_6b_decode_step_with_the_fused_append():
-    step = bench.DecodeStep(DEV, workload=2, append=True)
+@pytest.mark.parametrize("early", [True, False])
+def test_qwen3_0_6b_decode_step_with_the_fused_append(early):
+    step = bench.DecodeStep(DEV, workload=2, append=True, early_pages=early)
     _check_decode_step(step, range(step.case.n_layers))
 
 
 def test_qwen3_8b_decode_as_benchmarked():
-    step = bench.DecodeStep(DEV, workload=4)          # 36 layers cycling 4 pools of 1 GiB
+    step = bench.DecodeStep(DEV, workload=4, early_pages=True)      # 36 layers cycling 4 pools of 1 GiB
+    _check_decode_step(step, range(step.case.n_layers))
+
+
+def test_prefix_shared_tail_as_benchmarked():
+    step = bench.DecodeStep(DEV, workload=5, early_pages=True)      # 8 calls cycling 4 pools
     _check_decode_step(step, range(step.case.n_layers))
 
 
