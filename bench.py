@@ -253,30 +253,31 @@ class DecodeStep:
         # write, then the decode's kernels (the write runs inside the decode with append)
         self.kernels_per_step = self.L * ((0 if append else 1) + self.decode_kernels)
 
-    # Layer l uses pool l % n_layers; its q, new K/V and output default to that
-    # pool's resident tensors, and the end-to-end run passes its own.
-    def write(self, l, kn=None, vn=None):
+    # Layer l uses pool l % n_layers; its q, new K/V, output and the step's
+    # metadata (slots, block tables, lengths) default to the resident tensors,
+    # and the end-to-end run passes the ones it copied from the host.
+    def write(self, l, kn=None, vn=None, meta=None):
         c, i = self.case, l % self.case.n_layers
         kn, vn = (c.k_new[i], c.v_new[i]) if kn is None else (kn, vn)
-        self.pa.kv_cache_write(kn, vn, c.slot_mapping, c.k_cache[i], c.v_cache[i])
+        slots = c.slot_mapping if meta is None else meta[0]
+        self.pa.kv_cache_write(kn, vn, slots, c.k_cache[i], c.v_cache[i])
 
-    def decode(self, l, q=None, out=None, kn=None, vn=None):
+    def decode(self, l, q=None, out=None, kn=None, vn=None, meta=None):
         c, i = self.case, l % self.case.n_layers
         q = c.q[i] if q is None else q
         out = self.out[i] if out is None else out
+        bt, ctx = (c.block_tables, c.context_lens) if meta is None else meta[1:]
         if self.append:
             kn, vn = (c.k_new[i], c.v_new[i]) if kn is None else (kn, vn)
-            self.pa.paged_attn_decode_append(q, kn, vn, c.k_cache[i], c.v_cache[i], c.block_tables,
-                                             c.context_lens, c.scale, out=out, workspace=self.ws,
-                                             max_context_len=c.max_context_len, early_pages=self.early_pages)
+            self.pa.paged_attn_decode_append(q, kn, vn, c.k_cache[i], c.v_cache[i], bt, ctx, c.scale, out=out,
+                                             workspace=self.ws, max_context_len=c.max_context_len,
+                                             early_pages=self.early_pages)
         elif self.window:
-            self.pa.paged_attn_decode_window(q, c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
-                                             c.scale, self.window, out=out, workspace=self.ws,
-                                             max_context_len=c.max_context_len)
+            self.pa.paged_attn_decode_window(q, c.k_cache[i], c.v_cache[i], bt, ctx, c.scale, self.window, out=out,
+                                             workspace=self.ws, max_context_len=c.max_context_len)
         else:
-            self.pa.paged_attn_decode(q, c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens, c.scale,
-                                      out=out, workspace=self.ws, max_context_len=c.max_context_len,
-                                      early_pages=self.early_pages)
+            self.pa.paged_attn_decode(q, c.k_cache[i], c.v_cache[i], bt, ctx, c.scale, out=out, workspace=self.ws,
+                                      max_context_len=c.max_context_len, early_pages=self.early_pages)
 
     def run(self):
         for l in range(self.L):
@@ -327,14 +328,15 @@ class DecodeStepQ8(DecodeStep):
         self.step_bytes = self.L * (self.decode_bytes_layer + self.write_bytes_layer)
         self.pool_bytes = sum(t.numel() * t.element_size() for t in self.q8[0])
 
-    def write(self, l, kn=None, vn=None):
+    def write(self, l, kn=None, vn=None, meta=None):
         c, i = self.case, l % self.case.n_layers
         kn, vn = (c.k_new[i], c.v_new[i]) if kn is None else (kn, vn)
-        self._write(kn, vn, c.slot_mapping, *self.q8[i])
+        self._write(kn, vn, c.slot_mapping if meta is None else meta[0], *self.q8[i])
 
-    def decode(self, l, q=None, out=None, kn=None, vn=None):
+    def decode(self, l, q=None, out=None, kn=None, vn=None, meta=None):
         c, i = self.case, l % self.case.n_layers
-        self._decode(c.q[i] if q is None else q, *self.q8[i], c.block_tables, c.context_lens, c.scale,
+        bt, ctx = (c.block_tables, c.context_lens) if meta is None else meta[1:]
+        self._decode(c.q[i] if q is None else q, *self.q8[i], bt, ctx, c.scale,
                      out=self.out[i] if out is None else out, workspace=self.ws, max_context_len=c.max_context_len)
 
 
@@ -451,14 +453,14 @@ def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream):
             for l in range(L)]
     h2d, d2h = off, L * out_size
 
+    staged_meta = tuple(views[3 * L:])   # the step's slots, block tables and lengths, as copied
+
     def calls():
-        for dst, src in zip(meta, views[3 * L:]):   # the step's metadata, staged above
-            dst.copy_(src, non_blocking=True)
         for l in range(L):
             q, kn, vn = views[3 * l:3 * l + 3]
             if not getattr(step, "append", False):
-                step.write(l, kn, vn)
-            step.decode(l, q=q, out=outs[l], kn=kn, vn=vn)
+                step.write(l, kn, vn, meta=staged_meta)
+            step.decode(l, q=q, out=outs[l], kn=kn, vn=vn, meta=staged_meta)
 
     dev_in.copy_(host_in)               # staged once before the graph's warm-up call and capture
     torch.cuda.synchronize()
@@ -479,6 +481,9 @@ def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream):
             one()
         e1.record(stream)
         e1.synchronize()
+    # the outputs of the last step as they reached the host, layer by layer
+    step.e2e_outputs = [host_out[l * out_size:l * out_size + nbytes(step.out[0])].view(step.out[0].dtype)
+                        .view(step.out[0].shape) for l in range(L)]
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 

@@ -81,3 +81,20 @@ def test_mixed_step_as_benchmarked():
         refd = oracle.paged_attn_decode(bits(c.q[i]), kh, vh, c.block_tables.cpu().numpy(),
                                         c.context_lens.cpu().numpy(), c.scale, oracle.BF16)
         check_close(step.out_d[i], refd, f"mixed step decode, pool {i}")
+
+
+@pytest.mark.parametrize("append", [False, True])
+def test_end_to_end_path_returns_the_right_outputs_to_the_host(append):
+    # the e2e leg: inputs copied from pinned host memory each step, the library
+    # calls reading the copies (metadata included), outputs copied back
+    step = bench.DecodeStep(DEV, workload=2, append=append, early_pages=True)
+    c = step.case
+    before = [(bits(c.k_cache[i]), bits(c.v_cache[i])) for i in range(c.n_layers)]
+    stream = torch.cuda.Stream(device=DEV)
+    bench.e2e_measure(step, 3, 3, stream)
+    bt, ctx = c.block_tables.cpu().numpy(), c.context_lens.cpu().numpy()
+    for l in (0, 13, step.L - 1):
+        kh, vh = before[l % c.n_layers]
+        assert oracle.kv_cache_write(kh, vh, bits(c.k_new[l]), bits(c.v_new[l]), c.slot_mapping.cpu().numpy()) == 0
+        ref = oracle.paged_attn_decode(bits(c.q[l]), kh, vh, bt, ctx, c.scale, ORACLE_DTYPE[c.dtype])
+        check_close(step.e2e_outputs[l], ref, f"e2e layer {l}")
