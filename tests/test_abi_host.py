@@ -32,6 +32,15 @@ def test_header_declares_the_three_calls_and_helpers():
         assert n in names
 
 
+def test_binding_constants_match_the_header():
+    text = open(HEADER).read()
+    defines = dict(re.findall(r"#define (PA_[A-Z0-9_]+) (\d+)u?\b", text))
+    assert int(defines["PA_DECODE_EARLY_PAGES"]) == pa.DECODE_EARLY_PAGES
+    assert int(defines["PA_HEAD_DIM"]) == 128 and int(defines["PA_BLOCK_SIZE"]) == 16
+    codes = dict((name, int(v)) for name, v in re.findall(r"(PA_(?:OK|ERR_[A-Z_]+)) = (-?\d+)", text))
+    assert codes == pa.STATUS_CODE
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_entry_points():
         assert hasattr(lib, name), f"{name} declared in pagedattn.h but not exported"
