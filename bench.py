@@ -66,7 +66,7 @@ def parse_args(argv=None):
                     help="decode workloads: each layer's KV write fused into its decode call "
                          "(paged_attn_decode_append) instead of a separate kv_cache_write")
     ap.add_argument("--no-early-pages", action="store_true",
-                    help="decode workloads, 16-bit pool without a window: do not pass PA_DECODE_EARLY_PAGES. By "
+                    help="decode workloads without a window: do not pass PA_DECODE_EARLY_PAGES. By "
                          "default each decode call fetches its cached pages before the preceding KV write has "
                          "finished, which the step allows: that write touches only each sequence's last page")
     ap.add_argument("--overlap", action="store_true",
@@ -88,7 +88,7 @@ def parse_args(argv=None):
         ap.error("--window takes W >= 0, with workloads 2, 3 and 4 on the 16-bit pool")
     if args.append and (args.window or args.kv != "16bit" or args.workload == 3):
         ap.error("--append applies to the 16-bit decode workloads 2, 4 and 5 without a window")
-    args.early_pages = not args.no_early_pages and not args.window and args.kv == "16bit"
+    args.early_pages = not args.no_early_pages and not args.window
     return args
 
 
@@ -297,10 +297,10 @@ class DecodeStepQ8(DecodeStep):
     8-bit pool by the library's own write; each layer of the step then
     quantises the new tokens into their slots and decodes."""
 
-    def __init__(self, device, workload: int = 2, pools: int = 0, fp8: bool = False):
+    def __init__(self, device, workload: int = 2, pools: int = 0, fp8: bool = False, early_pages: bool = False):
         import numpy as np
         import torch
-        super().__init__(device, workload, pools)
+        super().__init__(device, workload, pools, early_pages=early_pages)
         self.fp8 = fp8
         alloc = self.pa.alloc_pool_f8 if fp8 else self.pa.alloc_pool_q8
         self._write = self.pa.kv_cache_write_f8 if fp8 else self.pa.kv_cache_write_q8
@@ -337,7 +337,8 @@ class DecodeStepQ8(DecodeStep):
         c, i = self.case, l % self.case.n_layers
         bt, ctx = (c.block_tables, c.context_lens) if meta is None else meta[1:]
         self._decode(c.q[i] if q is None else q, *self.q8[i], bt, ctx, c.scale,
-                     out=self.out[i] if out is None else out, workspace=self.ws, max_context_len=c.max_context_len)
+                     out=self.out[i] if out is None else out, workspace=self.ws, max_context_len=c.max_context_len,
+                     early_pages=self.early_pages)
 
 
 class MixedStep:
@@ -555,7 +556,7 @@ def run_ours(args):
     if args.workload == 3:
         return run_mixed(args, dev, pa)
 
-    step = (DecodeStepQ8(dev, args.workload, args.pools, args.kv == "fp8") if args.kv != "16bit"
+    step = (DecodeStepQ8(dev, args.workload, args.pools, args.kv == "fp8", args.early_pages) if args.kv != "16bit"
             else DecodeStep(dev, args.workload, args.pools, args.window, args.append, args.early_pages))
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)

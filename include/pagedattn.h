@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 6
+#define PA_ABI_VERSION 7
 #define PA_HEAD_DIM 128
 #define PA_BLOCK_SIZE 16
 #define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
@@ -316,6 +316,25 @@ PA_API pa_status pa_paged_attn_decode_f8(const void *q, int32_t dtype, const pa_
                                          const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                                          int32_t max_context_len, float scale, void *out, void *workspace,
                                          size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * paged_attn_decode_q8_ex — the decode over an 8-bit pool with flags:
+ *   codes   PA_CODES_INT8 (as pa_paged_attn_decode_q8) or PA_CODES_E4M3 (as
+ *           pa_paged_attn_decode_f8); anything else: PA_ERR_UNSUPPORTED;
+ *   flags   0 or PA_DECODE_EARLY_PAGES, with the promise stated at
+ *           pa_paged_attn_decode_ex (pa_kv_cache_write_q8 / _f8 let the next
+ *           kernel start beside the tail of the work before them, as
+ *           pa_kv_cache_write does); other bits: PA_ERR_UNSUPPORTED.
+ * Other arguments, workspace and errors as pa_paged_attn_decode_q8.  No
+ * counterpart on the pages: a library addition.
+ */
+#define PA_CODES_INT8 0
+#define PA_CODES_E4M3 1
+PA_API pa_status pa_paged_attn_decode_q8_ex(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool, int32_t codes,
+                                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                            const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                            int32_t max_context_len, float scale, uint32_t flags, void *out,
+                                            void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * ---- sliding window [P2 section 4 (a ring of capacity W keeps the last W

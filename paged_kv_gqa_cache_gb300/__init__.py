@@ -47,7 +47,7 @@ EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_deco
            "pa_kv_cache_write_f8", "pa_paged_attn_decode_f8",
            "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
            "pa_qk_norm_rope_kv_write", "pa_paged_attn_decode_append", "pa_selftest_bounded_wait",
-           "pa_paged_attn_decode_ex",
+           "pa_paged_attn_decode_ex", "pa_paged_attn_decode_q8_ex",
            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
            "pa_allocator_release", "pa_allocator_refcount", "pa_allocator_stats_get", "pa_allocator_take_copies",
            "pa_sequence_create", "pa_sequence_destroy", "pa_sequence_reserve", "pa_sequence_commit",
@@ -107,6 +107,9 @@ def load_library(path: str = LIB_PATH):
         lib.pa_kv_cache_write_f8.restype = i32
         lib.pa_paged_attn_decode_f8.argtypes = lib.pa_paged_attn_decode_q8.argtypes
         lib.pa_paged_attn_decode_f8.restype = i32
+        lib.pa_paged_attn_decode_q8_ex.argtypes = [P, i32, q8_p, i32, P, i32, P, i32, i32, i32, ctypes.c_float,
+                                                   ctypes.c_uint32, P, P, ctypes.c_size_t, P]
+        lib.pa_paged_attn_decode_q8_ex.restype = i32
         lib.pa_kv_cache_write.argtypes = [P, P, P, i32, pool_p, P]
         lib.pa_kv_cache_write.restype = i32
         lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -276,8 +279,10 @@ def kv_cache_write_q8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tens
 def paged_attn_decode_q8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor, k_scale: torch.Tensor,
                          v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                          scale: float, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                         max_context_len: Optional[int] = None, stream=None, _fp8: bool = False) -> torch.Tensor:
-    """Decode attention over an int8 pool: q [S, Hq, 128] (fp16 / bf16) → out, same dtype."""
+                         max_context_len: Optional[int] = None, stream=None, _fp8: bool = False,
+                         early_pages: bool = False) -> torch.Tensor:
+    """Decode attention over an int8 pool: q [S, Hq, 128] (fp16 / bf16) → out, same dtype.
+    ``early_pages`` as for :func:`paged_attn_decode`."""
     pool = make_pool_q8(k_codes, v_codes, k_scale, v_scale, torch.uint8 if _fp8 else torch.int8)
     _need(q, "q")
     _need(block_tables, "block_tables", torch.int32)
@@ -294,11 +299,17 @@ def paged_attn_decode_q8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.
         workspace = alloc_decode_workspace(S, hq, pool.num_kv_heads, mcl, q.device)
     _need(workspace, "workspace")
     lib = load_library()
+    wsb = workspace.numel() * workspace.element_size()
+    if early_pages:
+        _check(lib.pa_paged_attn_decode_q8_ex(q.data_ptr(), _dtype_code(q), ctypes.byref(pool), 1 if _fp8 else 0,
+                                              block_tables.data_ptr(), mb, context_lens.data_ptr(), S, hq, mcl,
+                                              float(scale), DECODE_EARLY_PAGES, out.data_ptr(), workspace.data_ptr(),
+                                              wsb, _stream(stream)), "pa_paged_attn_decode_q8_ex")
+        return out
     fn, name = (lib.pa_paged_attn_decode_f8, "pa_paged_attn_decode_f8") if _fp8 else \
         (lib.pa_paged_attn_decode_q8, "pa_paged_attn_decode_q8")
     _check(fn(q.data_ptr(), _dtype_code(q), ctypes.byref(pool), block_tables.data_ptr(), mb, context_lens.data_ptr(),
-              S, hq, mcl, float(scale), out.data_ptr(), workspace.data_ptr(),
-              workspace.numel() * workspace.element_size(), _stream(stream)), name)
+              S, hq, mcl, float(scale), out.data_ptr(), workspace.data_ptr(), wsb, _stream(stream)), name)
     return out
 
 
@@ -311,10 +322,11 @@ def kv_cache_write_f8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tens
 def paged_attn_decode_f8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.Tensor, k_scale: torch.Tensor,
                          v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                          scale: float, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                         max_context_len: Optional[int] = None, stream=None) -> torch.Tensor:
+                         max_context_len: Optional[int] = None, stream=None,
+                         early_pages: bool = False) -> torch.Tensor:
     """Decode attention over an fp8 (E4M3) pool: q [S, Hq, 128] (fp16 / bf16) → out, same dtype."""
     return paged_attn_decode_q8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale, out,
-                                workspace, max_context_len, stream, _fp8=True)
+                                workspace, max_context_len, stream, _fp8=True, early_pages=early_pages)
 
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int) -> int:

@@ -46,8 +46,8 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const WriteParams p) {
 // 32-bit word and lane 0 stores the scale.
 template <typename T, bool F8>
 __global__ void __launch_bounds__(256) kv_write_q8_kernel(const WriteQ8Params p) {
+  griddep_launch_dependents();  // as the 16-bit write: the next kernel may start its set-up at once
   griddep_wait();
-  griddep_launch_dependents();
   constexpr unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)p.num_tokens * p.num_kv_heads;

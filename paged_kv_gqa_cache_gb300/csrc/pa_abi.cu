@@ -362,13 +362,13 @@ pa_status write_8bit(const void *k, const void *v, int32_t dtype, const int64_t 
 pa_status decode_8bit(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool, const int32_t *block_tables,
                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                       int32_t num_q_heads, int32_t max_context_len, float scale, void *out, void *workspace,
-                      size_t workspace_bytes, bool f8, pa_stream_t stream) {
+                      size_t workspace_bytes, bool f8, pa_stream_t stream, uint32_t flags = 0) {
   pa_status st = check_pool_q8(pool);
   if (st != PA_OK) return st;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
   return decode_call(q, dtype, nullptr, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                      num_q_heads, max_context_len, scale, 0, out, workspace, workspace_bytes,
-                     static_cast<cudaStream_t>(stream), nullptr, nullptr, f8);
+                     static_cast<cudaStream_t>(stream), nullptr, nullptr, f8, flags);
 }
 
 }  // namespace
@@ -390,6 +390,18 @@ pa_status pa_paged_attn_decode_q8(const void *q, int32_t dtype, const pa_kv_pool
                                   size_t workspace_bytes, pa_stream_t stream) {
   return decode_8bit(q, dtype, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
                      max_context_len, scale, out, workspace, workspace_bytes, false, stream);
+}
+
+pa_status pa_paged_attn_decode_q8_ex(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool, int32_t codes,
+                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                     int32_t max_context_len, float scale, uint32_t flags, void *out,
+                                     void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (codes != PA_CODES_INT8 && codes != PA_CODES_E4M3) return PA_ERR_UNSUPPORTED;
+  if (flags & ~(uint32_t)PA_DECODE_EARLY_PAGES) return PA_ERR_UNSUPPORTED;
+  return decode_8bit(q, dtype, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                     max_context_len, scale, out, workspace, workspace_bytes, codes == PA_CODES_E4M3, stream,
+                     flags);
 }
 
 pa_status pa_paged_attn_decode_f8(const void *q, int32_t dtype, const pa_kv_pool_q8 *pool,

@@ -56,7 +56,7 @@ def test_only_c_entry_points_are_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 6
+    assert lib.pa_abi_version() == 7
     for code in range(0, -12, -1):
         assert lib.pa_status_string(code).decode().startswith(pa.STATUS[code])
 
@@ -197,6 +197,17 @@ def test_decode_ex_checks_its_arguments(lib):
     assert call(window=-1) == -2
     assert call(out=P + 2) == -9                   # the plain call's checks still apply, before any CUDA call
     assert call(kn=P + 8, vn=P, out=P) == -9
+
+
+def test_decode_q8_ex_checks_its_arguments(lib):
+    ws = lib.pa_decode_workspace_bytes(4, 16, 8, 256)
+    call = lambda **kw: lib.pa_paged_attn_decode_q8_ex(
+        P, kw.get("dtype", 1), ctypes.byref(_pool_q8()), kw.get("codes", 0), P, 16, P, 4, 16, 256, 0.088,
+        kw.get("flags", 1), kw.get("out", P), P, ws, None)
+    assert call(codes=2) == -4 and call(codes=-1) == -4
+    assert call(flags=4) == -4
+    assert call(dtype=3) == -3
+    assert call(codes=1, out=P + 2) == -9 and call(codes=0, out=P + 2) == -9
 
 
 def test_window_calls_check_their_arguments(lib):

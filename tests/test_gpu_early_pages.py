@@ -122,3 +122,40 @@ def test_early_pages_reports_bad_lengths_and_block_ids():
     ref = oracle.paged_attn_decode(bits(case.q[0]), bits(kc), bits(vc), case.block_tables.cpu().numpy(),
                                    case.context_lens.cpu().numpy(), case.scale, ORACLE_DTYPE[case.dtype])
     check_close(out[:1], ref[:1], "the valid sequence")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("hq,hkv,dtype", [(16, 8, "f16"), (32, 8, "bf16"), (16, 2, "bf16")])
+def test_early_pages_on_8bit_pools_after_a_last_page_write(fp8, hq, hkv, dtype):
+    # every token quantised into an 8-bit pool; then the quantising write of
+    # fresh rows into every last page directly ahead of the decode
+    lens = [1, 2, 15, 16, 17, 33, 250, 512, 700, 1023]
+    case = workloads.build_case(f"early8-{fp8}-{hq}x{hkv}", dtype, hq, hkv, seed=hq + 5 * hkv + fp8, device=DEV,
+                                decode_lens=lens)
+    bt = case.block_tables.cpu().numpy()
+    allslots = np.concatenate([bt[s, np.arange(n) // BS].astype(np.int64) * BS + np.arange(n) % BS
+                               for s, n in enumerate(case.context_lens.cpu().numpy())])
+    sl = torch.from_numpy(allslots).to(DEV)
+    kc, vc = case.k_cache[0], case.v_cache[0]
+    krows = kc.view(-1, hkv, 128)[sl].contiguous()
+    vrows = vc.view(-1, hkv, 128)[sl].contiguous()
+    last = torch.from_numpy(_last_page_rows(case)).to(DEV)
+    gen = torch.Generator(device=DEV).manual_seed(7)
+    fresh = lambda: torch.randn((last.numel(), hkv, 128), generator=gen, device=DEV).to(kc.dtype)
+    kf, vf = fresh(), fresh()
+    alloc, write, decode = ((pa.alloc_pool_f8, pa.kv_cache_write_f8, pa.paged_attn_decode_f8) if fp8 else
+                            (pa.alloc_pool_q8, pa.kv_cache_write_q8, pa.paged_attn_decode_q8))
+    outs = []
+    for early in (True, False):
+        pool = alloc(case.num_blocks, hkv, DEV)
+        write(krows, vrows, sl, *pool)
+        torch.cuda.synchronize()
+        write(kf, vf, last, *pool)
+        outs.append(decode(case.q[0], *pool, case.block_tables, case.context_lens, case.scale,
+                           max_context_len=case.max_context_len, early_pages=early))
+        torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    host = tuple(t.cpu().numpy() for t in pool)
+    ref = (oracle.paged_attn_decode_f8 if fp8 else oracle.paged_attn_decode_q8)(
+        bits(case.q[0]), *host, bt, case.context_lens.cpu().numpy(), case.scale, ORACLE_DTYPE[case.dtype])
+    check_close(outs[0], ref, case.name)
