@@ -155,6 +155,21 @@ def check_state(mp, np_, mseqs, nseqs, loose):
     assert all(mp.ref[b] == 0 for b in mp.free) and len(set(mp.free)) == len(mp.free)
 
 
+def check_step_tables(mseqs, nseqs, max_blocks):
+    """pa_build_step_tables against the model: tables padded with -1, starts =
+    committed lengths, lens = reserved tokens, contexts = their sums; a sequence
+    holding more blocks than max_blocks refuses the whole call."""
+    if any(len(m.blocks) > max_blocks for m in mseqs):
+        with pytest.raises(pa.PagedAttnError) as e:
+            pa.build_step_tables(nseqs, max_blocks)
+        assert e.value.status == pa.STATUS_CODE["PA_ERR_SHAPE"]
+        return
+    bt, starts, lens, ctx = pa.build_step_tables(nseqs, max_blocks)
+    for k, m in enumerate(mseqs):
+        assert list(bt[k]) == m.blocks + [-1] * (max_blocks - len(m.blocks))
+        assert (starts[k], lens[k], ctx[k]) == (m.length, m.reserved, m.length + m.reserved)
+
+
 def _run(seed):
     """One random run of 500 operations; returns the model pool and the refusals seen."""
     rng = np.random.default_rng(seed)
@@ -162,7 +177,7 @@ def _run(seed):
     nblocks = int(rng.choice([9, 17, 40]))
     mp, np_ = ModelPool(nblocks), pa.BlockAllocator(nblocks)
     mseqs, nseqs, loose = [], [], []
-    for _ in range(500):
+    for step in range(500):
         op = rng.choice(["new", "reserve", "commit", "fork", "adopt", "release_seq", "allocate", "retain",
                          "release", "copies"], p=[.08, .27, .2, .1, .06, .07, .07, .05, .05, .05])
         i = int(rng.integers(len(mseqs))) if mseqs else None
@@ -211,6 +226,8 @@ def _run(seed):
         if res is not None and res[0] == "refused":
             refusals.append((op, res[1]))
         check_state(mp, np_, mseqs, nseqs, loose)
+        if nseqs and step % 25 == 0:
+            check_step_tables(mseqs, nseqs, int(rng.choice([2, 4, 64])))
     # a block that nothing holds any more cannot be retained or released
     free_ids = list(mp.free)
     if free_ids:
