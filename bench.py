@@ -1,30 +1,42 @@
 """Benchmark of the paged-KV GQA attention hot path on GB300.
 
-Workload (default): the Qwen3-0.6B decode step over 28 layers — 8 sequences
-with context lengths uniform in [512, 1024], 16 query / 8 KV heads, head_dim
-128, fp16, one 512-block pool per layer (896 MiB of KV in total, larger than
-L2, so every step streams its KV from HBM).  One step = for each of the 28
-layers: kv_cache_write of the 8 new tokens, then paged_attn_decode.
+Default line (rank 0 prints one JSON line): the Qwen3-8B decode step, 36
+layers of 64 sequences x 4096 tokens (16 query / 8 KV heads, head_dim 128,
+bf16), one 1 GiB pool per layer (36 GiB of KV, far larger than L2).  One step
+= for each layer: kv_cache_write of the 64 new tokens, then paged_attn_decode.
+The same line carries two sub-lines with the same keys, each timed on its own:
 
-Printed JSON line (rank 0):
-  value      KV GB/s of the whole step (algorithmic bytes: every visible K/V
-             row read once, plus the new rows read and written) over the step
-             time measured with CUDA events around a CUDA graph of K steps;
-  e2e        the same metric through the Python binding, per step: one copy
-             of every layer's q and new K/V (and the step's slots, tables and
-             lengths) from pinned host memory, the step's library calls
-             replayed as a CUDA graph, one copy of every layer's output back
-             to pinned host memory;
-  roofline   the decode call timed alone per layer (one kernel when every
-             sequence and KV head gets its own SMs, else split + combine),
-             algorithmic bytes per launch over its duration, against the
-             measured HBM copy bandwidth;
-  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample.
+  "prefill"      the Qwen3-0.6B mixed chunked-prefill step (budget 2048): per
+                 layer, the write of 2048 new tokens, prefill of 3 chunks of
+                 512 (prefixes 0, 512, 1536) beside the decode of 512
+                 sequences; value in tokens/s, roofline = the prefill call on
+                 the tensor cores (TFLOP/s);
+  "decode_0_6b"  the Qwen3-0.6B decode step (8 sequences, 512..1024 tokens,
+                 28 layers, fp16); value in KV GB/s.
 
+Per line:
+  value      the line's metric over the step time: CUDA events around K
+             replays of a CUDA graph of one step, repeated until the timed
+             region holds at least --min-seconds of GPU time (and at least 5
+             repeats); ms_per_step is the median repeat / K;
+  e2e        the same metric through the library calls with host buffers:
+             each step copies every layer's inputs (and the step's metadata)
+             from pinned host memory, replays the step's calls, and copies
+             every layer's outputs back to pinned host memory;
+  roofline   the dominant kernel timed alone (the step's attention calls back
+             to back): algorithmic bytes (or FLOPs) per launch over its
+             duration, against the measured HBM copy bandwidth (or dense bf16
+             tensor throughput);
+  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample;
+  clocks     nvidia-smi samples taken during the line's timed regions.
+
+``--workload 2|3|5``, ``--kv``, ``--window``, ``--append``, ``--block-copy``
+and ``--fused-write`` print single diagnostic lines instead.
 ``--impl reference`` times the oracle itself (the only reference this method
-has) on the same workload and prints the same line with "impl": "reference".
-Multi-GPU (``torchrun --nproc-per-node N``) runs N independent replicas
-(sequences are independent; no collective on the data path): weak scaling.
+has) on the default line's workload and prints the same line with
+"impl": "reference".  Multi-GPU (``torchrun --nproc-per-node N``) runs N
+independent replicas (sequences are independent; no collective on the data
+path): weak scaling.
 """
 from __future__ import annotations
 
@@ -52,8 +64,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="each timed region repeats its K steps until it holds at least this much GPU time "
+                         "(and at least 5 repeats); the median repeat gives ms_per_step")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -80,15 +95,20 @@ def parse_args(argv=None):
     ap.add_argument("--fused-write", action="store_true",
                     help="diagnostic line for q/k RMSNorm + rotary embedding fused into the KV write: the mixed "
                          "step's 2048 new tokens (Qwen3-0.6B: 16 query / 8 KV heads, bf16) in each of 28 layers")
-    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5],
-                    help="2 = the Qwen3-0.6B 28-layer decode step (default); 3, 4, 5 = the mixed prefill "
-                         "step, the Qwen3-8B decode and the prefix-shared long tail (diagnostic lines)")
+    ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4, 5],
+                    help="4 = the Qwen3-8B 36-layer decode step (default; with the mixed prefill step and the "
+                         "Qwen3-0.6B decode step as sub-lines); 2, 3, 5 = the Qwen3-0.6B decode step, the mixed "
+                         "prefill step and the prefix-shared long tail alone")
+    ap.add_argument("--no-sublines", action="store_true",
+                    help="default workload: print the Qwen3-8B decode line without its two sub-lines")
     args = ap.parse_args(argv)
     if args.window < 0 or (args.window and (args.workload == 5 or args.kv != "16bit")):
         ap.error("--window takes W >= 0, with workloads 2, 3 and 4 on the 16-bit pool")
     if args.append and (args.window or args.kv != "16bit" or args.workload == 3):
         ap.error("--append applies to the 16-bit decode workloads 2, 4 and 5 without a window")
     args.early_pages = not args.no_early_pages and not args.window
+    args.sublines = (args.workload == 4 and not args.no_sublines and args.kv == "16bit" and not args.window
+                     and not args.append and not args.block_copy and not args.fused_write)
     return args
 
 
@@ -130,42 +150,63 @@ def barrier(device=None):
 # ---- clocks during the timed region ----------------------------------------------------
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons every 200 ms."""
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms (one
+    `nvidia-smi -lms 200` process streaming rows) while the region runs."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, gpu):
+        self.gpu = gpu              # nvidia-smi id: the device's UUID ("GPU-...") or an index
         self.rows = []
-        self._stop = threading.Event()
+        self._proc = None
         self._t = None
 
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                out = subprocess.run(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
-                                     timeout=5).stdout.strip()
-                if out:
-                    self.rows.append([x.strip() for x in out.split(",")])
-            except Exception:
-                pass
-            self._stop.wait(0.2)
+    @staticmethod
+    def gpu_id(device) -> str:
+        """The nvidia-smi id of a torch device: its UUID when torch reports it
+        (device indices inside the process need not match nvidia-smi's)."""
+        import torch
+        try:
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            if u:
+                return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        return str(device.index if device.index is not None else 0)
+
+    def _read(self):
+        for line in self._proc.stdout:
+            line = line.strip()
+            if line:
+                self.rows.append([x.strip() for x in line.split(",")])
 
     def __enter__(self):
-        self._t = threading.Thread(target=self._run, daemon=True)
-        self._t.start()
+        try:
+            self._proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                           "--format=csv,noheader,nounits", "-lms", "200"],
+                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self._proc = None
         return self
 
     def __exit__(self, *exc):
-        self._stop.set()
-        self._t.join(timeout=10)
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=10)
+            except Exception:
+                self._proc.kill()
+            self._t.join(timeout=10)
         return False
 
     def summary(self):
-        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        num = lambda x: x.replace(".", "", 1).isdigit()
+        sm = [float(r[1]) for r in self.rows if len(r) > 2 and num(r[1])]
+        mx = [float(r[2]) for r in self.rows if len(r) > 2 and num(r[2])]
+        pw = [float(r[3]) for r in self.rows if len(r) > 3 and num(r[3])]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in self.rows:
@@ -173,7 +214,7 @@ class ClockSampler:
                 if val.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(self.rows)}
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(self.rows)}
 
 
 def measured_peaks():
@@ -208,8 +249,8 @@ def committed_traffic(kernel_source: str, summary_name: str):
 WORKLOADS = {
     2: ("Qwen3-0.6B decode step, 28 layers: 8 seqs, ctx U[512,1024], Hq=16, Hkv=8, d=128, fp16, "
         "512-block pool per layer", 28, 28),
-    4: ("Qwen3-8B decode, 36 layers: 64 seqs x 4096 ctx, Hq=32, Hkv=8, d=128, bf16, 16384-block pool "
-        "(1 GiB K+V) per layer; 4 distinct pools cycled", 4, 36),
+    4: ("Qwen3-8B decode step, 36 layers: 64 seqs x 4096 ctx, Hq=32, Hkv=8, d=128, bf16, 16384-block pool "
+        "(1 GiB K+V) per layer", 36, 36),
     5: ("Prefix-shared long-tail decode, Qwen3-8B geometry: 32 seqs sharing 13 blocks + suffixes "
         "log-U[16,32768], bf16; 4 distinct pools cycled over 8 calls", 4, 8),
 }
@@ -350,42 +391,52 @@ class MixedStep:
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
-        self.pa, self.L, self.window = pa, 28, window
+        self.pa, self.L, self.window, self.overlap = pa, 28, window, overlap
         # overlap: each layer's prefill (tensor-bound) runs on a second stream beside its decode (HBM-bound)
         self.side = torch.cuda.Stream(device=device) if overlap else None
         self.case = c = workloads.qwen3_0_6b_mixed_step(device=device, n_layers=2, nan_fill=False)
+        self.dtype = c.dtype
         self.out_d = [torch.empty_like(q) for q in c.q]
         self.out_p = [torch.empty_like(q) for q in c.q_chunks]
         self.ws = pa.alloc_decode_workspace(c.q[0].shape[0], c.hq, c.hkv, c.max_context_len, device)
         self.flops_layer = workloads.prefill_flops(c.meta["chunks"], c.hq, window=window)
         self.tokens = c.slot_mapping.numel()
         lens = c.meta["decode_lens"]
+        self.decode_bytes_layer = workloads.decode_kv_bytes([min(n, window) if window else n for n in lens], c.hkv)
         self.kernels_per_layer = 2 + pa.decode_kernel_launches(len(lens), c.hkv, c.max_context_len, window)
 
-    def prefill(self, l):
+    def prefill(self, l, qp=None, out=None, meta=None):
         c, i = self.case, l % 2
-        self.pa.paged_attn_prefill_chunk_window(c.q_chunks[i], c.chunk_starts, c.chunk_lens, c.k_cache[i],
-                                                c.v_cache[i], c.chunk_block_tables, c.chunk_context_lens, c.scale,
-                                                self.window, out=self.out_p[i], max_chunk_len=512)
+        cs, cl, cbt, cctx = ((c.chunk_starts, c.chunk_lens, c.chunk_block_tables, c.chunk_context_lens)
+                             if meta is None else meta[3:])
+        self.pa.paged_attn_prefill_chunk_window(c.q_chunks[i] if qp is None else qp, cs, cl, c.k_cache[i],
+                                                c.v_cache[i], cbt, cctx, c.scale, self.window,
+                                                out=self.out_p[i] if out is None else out, max_chunk_len=512)
+
+    def layer(self, l, q=None, qp=None, kn=None, vn=None, out_d=None, out_p=None, meta=None):
+        """One layer's calls; the end-to-end run passes the copies it made of
+        the inputs and the metadata, and its own outputs."""
+        import torch
+        c, i = self.case, l % 2
+        main = torch.cuda.current_stream()
+        slots, bt, ctx = (c.slot_mapping, c.block_tables, c.context_lens) if meta is None else meta[:3]
+        self.pa.kv_cache_write(c.k_new[i] if kn is None else kn, c.v_new[i] if vn is None else vn, slots,
+                               c.k_cache[i], c.v_cache[i])
+        if self.side is not None:  # fork after the write, join before the next layer's write
+            self.side.wait_stream(main)
+            with torch.cuda.stream(self.side):
+                self.prefill(l, qp, out_p, meta)
+        else:
+            self.prefill(l, qp, out_p, meta)
+        self.pa.paged_attn_decode_window(c.q[i] if q is None else q, c.k_cache[i], c.v_cache[i], bt, ctx, c.scale,
+                                         self.window, out=self.out_d[i] if out_d is None else out_d,
+                                         workspace=self.ws, max_context_len=c.max_context_len)
+        if self.side is not None:
+            main.wait_stream(self.side)
 
     def run(self):
-        import torch
-        c = self.case
-        main = torch.cuda.current_stream()
         for l in range(self.L):
-            i = l % 2
-            self.pa.kv_cache_write(c.k_new[i], c.v_new[i], c.slot_mapping, c.k_cache[i], c.v_cache[i])
-            if self.side is not None:  # fork after the write, join before the next layer's write
-                self.side.wait_stream(main)
-                with torch.cuda.stream(self.side):
-                    self.prefill(l)
-            else:
-                self.prefill(l)
-            self.pa.paged_attn_decode_window(c.q[i], c.k_cache[i], c.v_cache[i], c.block_tables, c.context_lens,
-                                             c.scale, self.window, out=self.out_d[i], workspace=self.ws,
-                                             max_context_len=c.max_context_len)
-            if self.side is not None:
-                main.wait_stream(self.side)
+            self.layer(l)
 
     def run_prefill_only(self):
         for l in range(self.L):
@@ -418,26 +469,38 @@ def time_replays(g, n: int, stream) -> float:
     return e0.elapsed_time(e1)
 
 
-def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream):
-    """Same metric through the public API with host buffers, the way a serving
-    loop runs a decode step: per step one host-to-device copy, from pinned host
-    memory, of every layer's q and new K/V rows and of the step's slots, block
-    tables and lengths; the step's library calls (write + decode per layer,
-    replayed as a CUDA graph of those calls); one device-to-host copy of every
-    layer's output into pinned host memory.  Every layer has its own inputs
-    and output; the pools are the resident ones the step cycles."""
+def timed_repeats(one_repeat, min_seconds: float, min_reps: int = 5, max_reps: int = 5000):
+    """Run one_repeat() (it returns the milliseconds of K timed steps) until the
+    repeats hold at least min_seconds of GPU time and number at least min_reps.
+    Returns the per-repeat milliseconds."""
+    reps = [one_repeat()]
+    while (len(reps) < min_reps or sum(reps) < 1e3 * min_seconds) and len(reps) < max_reps:
+        reps.append(one_repeat())
+    return reps
+
+
+def timing_summary(reps, steps: int) -> dict:
+    return {"repeats": len(reps), "steps_per_repeat": steps, "timed_region_s": round(sum(reps) / 1e3, 3),
+            "ms_per_step_min": round(min(reps) / steps, 5), "ms_per_step_max": round(max(reps) / steps, 5)}
+
+
+def _e2e_run(L, layer_inputs, meta, layer_outputs, calls, steps, warmup, stream, min_seconds):
+    """The end-to-end leg shared by the lines: per step one copy of every
+    layer's inputs and of the step's metadata from pinned host memory into one
+    staging buffer, the step's library calls (captured once as a CUDA graph,
+    reading the staged copies), and one copy of every layer's outputs into
+    pinned host memory.  layer_inputs[l] and layer_outputs[l] are tuples of
+    tensors; calls(l, inputs, meta, outputs) enqueues layer l's calls.
+    Returns (median ms per step, h2d bytes, d2h bytes, repeats, host outputs)."""
     import torch
-    c, L, n = step.case, step.L, step.case.n_layers
-    dev = c.q[0].device
+    dev = layer_outputs[0][0].device
     align = lambda x: (x + 255) // 256 * 256
     nbytes = lambda t: t.numel() * t.element_size()
-    # input layout: q of every layer, then new K, new V of every layer, then the step's metadata
     parts, off = [], 0
     for l in range(L):
-        for src in (c.q[l % n], c.k_new[l % n], c.v_new[l % n]):
+        for src in layer_inputs[l]:
             parts.append((src, off))
             off = align(off + nbytes(src))
-    meta = (c.slot_mapping, c.block_tables, c.context_lens)
     for src in meta:
         parts.append((src, off))
         off = align(off + nbytes(src))
@@ -447,53 +510,108 @@ def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream):
     for src, o in parts:
         host_in[o:o + nbytes(src)].copy_(src.contiguous().view(torch.uint8).view(-1).cpu())
         views.append(dev_in[o:o + nbytes(src)].view(src.dtype).view(src.shape))
-    out_size = align(nbytes(step.out[0]))
-    dev_out = torch.empty(L * out_size, dtype=torch.uint8, device=dev)
-    host_out = torch.empty(L * out_size, dtype=torch.uint8).pin_memory()
-    outs = [dev_out[l * out_size:l * out_size + nbytes(step.out[0])].view(step.out[0].dtype).view(step.out[0].shape)
-            for l in range(L)]
-    h2d, d2h = off, L * out_size
+    out_parts, ooff = [], 0
+    for l in range(L):
+        for like in layer_outputs[l]:
+            out_parts.append((like, ooff))
+            ooff = align(ooff + nbytes(like))
+    dev_out = torch.empty(ooff, dtype=torch.uint8, device=dev)
+    host_out = torch.empty(ooff, dtype=torch.uint8).pin_memory()
+    outs = [dev_out[o:o + nbytes(t)].view(t.dtype).view(t.shape) for t, o in out_parts]
+    n_in, n_out = len(layer_inputs[0]), len(layer_outputs[0])
+    meta_views = tuple(views[L * n_in:])
 
-    staged_meta = tuple(views[3 * L:])   # the step's slots, block tables and lengths, as copied
-
-    def calls():
+    def step_calls():
         for l in range(L):
-            q, kn, vn = views[3 * l:3 * l + 3]
-            if not getattr(step, "append", False):
-                step.write(l, kn, vn, meta=staged_meta)
-            step.decode(l, q=q, out=outs[l], kn=kn, vn=vn, meta=staged_meta)
+            calls(l, views[n_in * l:n_in * (l + 1)], meta_views, outs[n_out * l:n_out * (l + 1)])
 
     dev_in.copy_(host_in)               # staged once before the graph's warm-up call and capture
     torch.cuda.synchronize()
-    graph = graph_of(calls, 1, stream)
+    graph = graph_of(step_calls, 1, stream)
 
     def one():
         dev_in.copy_(host_in, non_blocking=True)
         graph.replay()
         host_out.copy_(dev_out, non_blocking=True)
 
+    def one_repeat():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                one()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1)
+
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             one()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            one()
-        e1.record(stream)
-        e1.synchronize()
-    # the outputs of the last step as they reached the host, layer by layer
-    step.e2e_outputs = [host_out[l * out_size:l * out_size + nbytes(step.out[0])].view(step.out[0].dtype)
-                        .view(step.out[0].shape) for l in range(L)]
-    return e0.elapsed_time(e1) / steps, h2d, d2h
+    torch.cuda.synchronize()
+    reps = timed_repeats(one_repeat, min_seconds)
+    host_views = [host_out[o:o + nbytes(t)].view(t.dtype).view(t.shape) for t, o in out_parts]
+    host_layers = [tuple(host_views[n_out * l:n_out * (l + 1)]) for l in range(L)]
+    return statistics.median(reps) / steps, off, ooff, len(reps), host_layers
+
+
+def e2e_measure(step: DecodeStep, steps: int, warmup: int, stream, min_seconds: float = 0.0):
+    """Same metric through the public API with host buffers, the way a serving
+    loop runs a decode step: per step one host-to-device copy, from pinned host
+    memory, of every layer's q and new K/V rows and of the step's slots, block
+    tables and lengths; the step's library calls (write + decode per layer,
+    replayed as a CUDA graph of those calls); one device-to-host copy of every
+    layer's output into pinned host memory.  Every layer has its own inputs
+    and output; the pools are the resident ones the step cycles."""
+    c, L, n = step.case, step.L, step.case.n_layers
+    append = getattr(step, "append", False)
+
+    def calls(l, ins, meta, outs):
+        q, kn, vn = ins
+        if not append:
+            step.write(l, kn, vn, meta=meta)
+        step.decode(l, q=q, out=outs[0], kn=kn, vn=vn, meta=meta)
+
+    ms, h2d, d2h, reps, host = _e2e_run(
+        L, [(c.q[l % n], c.k_new[l % n], c.v_new[l % n]) for l in range(L)],
+        (c.slot_mapping, c.block_tables, c.context_lens), [(step.out[l % n],) for l in range(L)], calls, steps,
+        warmup, stream, min_seconds)
+    step.e2e_outputs = [h[0] for h in host]      # the outputs of the last step as they reached the host
+    return ms, h2d, d2h
+
+
+def e2e_measure_mixed(step: MixedStep, steps: int, warmup: int, stream, min_seconds: float = 0.0):
+    """The end-to-end leg of the mixed step: per step every layer's decode
+    queries, chunk queries and new K/V rows plus the step's metadata (slots,
+    decode tables and lengths, chunk starts, lengths, tables and context
+    lengths) from pinned host memory, the step's calls, and every layer's
+    decode and prefill outputs back to pinned host memory."""
+    c, L = step.case, step.L
+
+    def calls(l, ins, meta, outs):
+        q, qp, kn, vn = ins
+        step.layer(l, q=q, qp=qp, kn=kn, vn=vn, out_d=outs[0], out_p=outs[1], meta=meta)
+
+    ms, h2d, d2h, reps, host = _e2e_run(
+        L, [(c.q[l % 2], c.q_chunks[l % 2], c.k_new[l % 2], c.v_new[l % 2]) for l in range(L)],
+        (c.slot_mapping, c.block_tables, c.context_lens, c.chunk_starts, c.chunk_lens, c.chunk_block_tables,
+         c.chunk_context_lens), [(step.out_d[l % 2], step.out_p[l % 2]) for l in range(L)], calls, steps, warmup,
+        stream, min_seconds)
+    step.e2e_outputs = host
+    return ms, h2d, d2h
+
+
+def _u16(t):
+    import numpy as np
+    import torch
+    return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
 def cpu_baseline(step: DecodeStep, seconds: float):
     """The fp64 oracle, as it stands, on the host cores: the workload's decode
     layer calls in order, repeated until about `seconds` of wall time (a
-    bounded sample of the same work, scaled to GB/s)."""
-    import numpy as np
-    import torch
+    bounded sample of the same work, scaled to GB/s).  At most two distinct
+    layer pools are copied to the host (each layer's pool is as large as
+    every other's; a 1 GiB pool per layer would not fit 36 times)."""
     import oracle
     c = step.case
     threads = os.cpu_count() or 1
@@ -501,21 +619,21 @@ def cpu_baseline(step: DecodeStep, seconds: float):
     odt = oracle.BF16 if c.dtype == "bf16" else oracle.F16
     q8 = getattr(step, "q8", None)
     window = getattr(step, "window", 0)
-    u16 = lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16)
+    pools = min(c.n_layers, 2)
     inputs = {}
 
     def host(i):   # a layer's host copies, made once on first use, outside the timed calls
         if i not in inputs:
             if q8 is not None:
-                inputs[i] = (u16(c.q[i]), [t.cpu().numpy() for t in q8[i]])
+                inputs[i] = (_u16(c.q[i]), [t.cpu().numpy() for t in q8[i]])
             else:
-                inputs[i] = (u16(c.q[i]), u16(c.k_cache[i]), u16(c.v_cache[i]))
+                inputs[i] = (_u16(c.q[i]), _u16(c.k_cache[i]), _u16(c.v_cache[i]))
         return inputs[i]
 
     done_bytes, t_total, calls = 0, 0.0, 0
     while t_total < seconds:
         for l in range(step.L):
-            x = host(l % c.n_layers)
+            x = host(l % pools)
             t0 = time.perf_counter()
             if q8 is not None:
                 (oracle.paged_attn_decode_f8 if step.fp8 else oracle.paged_attn_decode_q8)(
@@ -529,9 +647,55 @@ def cpu_baseline(step: DecodeStep, seconds: float):
             calls += 1
             if t_total >= seconds:
                 break
-    return {"value": done_bytes / t_total / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{calls} decode layer calls of the workload in step order (fp64 C oracle, "
-                      f"{threads} threads), {t_total:.2f} s"}
+    return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{calls} decode layer calls of the workload in step order over {pools} distinct layer "
+                      f"pools (fp64 C oracle, {threads} threads), {t_total:.2f} s"}
+
+
+def cpu_baseline_mixed(step: MixedStep, seconds: float):
+    """The fp64 oracle on the host cores for the mixed step: per layer the KV
+    write, the prefill of the three chunks and the decode of the 512
+    sequences, layers in step order until about `seconds` of wall time; scaled
+    to tokens/s of the 28-layer step (2048 tokens per step), with the prefill
+    part also in TFLOP/s."""
+    import numpy as np
+    import oracle
+    c = step.case
+    threads = os.cpu_count() or 1
+    bt, ctx = c.block_tables.cpu().numpy(), c.context_lens.cpu().numpy()
+    cs, cl = c.chunk_starts.cpu().numpy(), c.chunk_lens.cpu().numpy()
+    cbt, cctx = c.chunk_block_tables.cpu().numpy(), c.chunk_context_lens.cpu().numpy()
+    slots = c.slot_mapping.cpu().numpy()
+    hosts = [dict(k=_u16(c.k_cache[i]).copy(), v=_u16(c.v_cache[i]).copy(), kn=_u16(c.k_new[i]),
+                  vn=_u16(c.v_new[i]), q=_u16(c.q[i]), qp=_u16(c.q_chunks[i])) for i in range(2)]
+    t_total, t_pre, layers = 0.0, 0.0, 0
+    while t_total < seconds:
+        x = hosts[layers % 2]
+        t0 = time.perf_counter()
+        oracle.kv_cache_write(x["k"], x["v"], x["kn"], x["vn"], slots)
+        t1 = time.perf_counter()
+        if step.window:
+            oracle.paged_attn_prefill_window(x["qp"], x["k"], x["v"], cs, cl, cbt, cctx, c.scale, step.window,
+                                             oracle.BF16, num_threads=threads)
+        else:
+            oracle.paged_attn_prefill(x["qp"], x["k"], x["v"], cs, cl, cbt, cctx, c.scale, oracle.BF16,
+                                      num_threads=threads)
+        t2 = time.perf_counter()
+        if step.window:
+            oracle.paged_attn_decode_window(x["q"], x["k"], x["v"], bt, ctx, c.scale, step.window, oracle.BF16,
+                                            num_threads=threads)
+        else:
+            oracle.paged_attn_decode(x["q"], x["k"], x["v"], bt, ctx, c.scale, oracle.BF16, num_threads=threads)
+        t3 = time.perf_counter()
+        t_total += t3 - t0
+        t_pre += t2 - t1
+        layers += 1
+    tokens_per_s = (layers / step.L) * step.tokens / t_total
+    return {"value": round(tokens_per_s, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "prefill_tflops": round(layers * step.flops_layer / t_pre / 1e12, 6),
+            "sample": f"{layers} of the step's {step.L} layers (write of {step.tokens} tokens, prefill of the 3 "
+                      f"chunks, decode of {len(ctx)} sequences; fp64 C oracle, {threads} threads), "
+                      f"{t_total:.2f} s, scaled to the {step.L}-layer step"}
 
 
 def _device_error_check(pa):
@@ -540,52 +704,39 @@ def _device_error_check(pa):
         raise RuntimeError(f"device error {pa.STATUS.get(st, st)} at {detail}")
 
 
-def run_ours(args):
+def decode_line(args, dev, pa, workload: int, kv: str = "16bit", window: int = 0, append: bool = False,
+                early_pages: bool = True, pools: int = 0, cpu: bool = True) -> dict:
+    """The JSON line of one decode workload (steps of write + decode per layer)."""
     import torch
-    rank, world, local = dist_env()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist_init("nccl")
-    import __graft_entry__
-    __graft_entry__.build()
-    import paged_kv_gqa_cache_gb300 as pa
-    if args.block_copy:
-        return run_block_copy(args, dev, pa)
-    if args.fused_write:
-        return run_fused_write(args, dev, pa)
-    if args.workload == 3:
-        return run_mixed(args, dev, pa)
-
-    step = (DecodeStepQ8(dev, args.workload, args.pools, args.kv == "fp8", args.early_pages) if args.kv != "16bit"
-            else DecodeStep(dev, args.workload, args.pools, args.window, args.append, args.early_pages))
+    rank, world, _ = dist_env()
+    step = (DecodeStepQ8(dev, workload, pools, kv == "fp8", early_pages) if kv != "16bit"
+            else DecodeStep(dev, workload, pools, window, append, early_pages))
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_dec = graph_of(step.run_decode_only, 1, stream)
     _device_error_check(pa)
 
-    # warm-up, then K timed steps bracketed by barrier + synchronize
+    # warm-up, then repeats of K timed steps bracketed by barrier + synchronize
     time_replays(g_step, max(args.warmup, 3), stream)
     barrier(dev)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        ms_total = time_replays(g_step, args.steps, stream)
+    with ClockSampler(ClockSampler.gpu_id(dev)) as clk:
+        reps = timed_repeats(lambda: time_replays(g_step, args.steps, stream), args.min_seconds)
         torch.cuda.synchronize()
         barrier(dev)
         # the dominant kernel alone: the step's decode calls, back to back
-        n_dec = max(args.steps // 2, 10)
-        ms_dec = time_replays(g_dec, n_dec, stream) / n_dec
-    ms_total = reduce_max(ms_total, dev)
-    ms_step = ms_total / args.steps
+        dec_reps = timed_repeats(lambda: time_replays(g_dec, args.steps, stream), args.min_seconds / 2)
+        e2e_ms, h2d, d2h = e2e_measure(step, args.steps, max(args.warmup, 3), stream, args.min_seconds / 2)
+    ms_step = reduce_max(statistics.median(reps) / args.steps, dev)
+    e2e_ms = reduce_max(e2e_ms, dev)
+    _device_error_check(pa)
     hbm, bf16, peak_kind = measured_peaks()
     value = world * step.step_bytes / (ms_step * 1e-3) / 1e9
 
-    dec_launch_ms = ms_dec / step.L
+    dec_launch_ms = statistics.median(dec_reps) / args.steps / step.L
     # with append the decode call also moves the new rows (read, written into the pool)
     launch_bytes = step.decode_bytes_layer + (step.write_bytes_layer if getattr(step, "append", False) else 0)
     achieved = launch_bytes / (dec_launch_ms * 1e-3) / 1e9
-    e2e_ms, h2d, d2h = e2e_measure(step, max(args.steps // 20, 10), 3, stream)
-    e2e_ms = reduce_max(e2e_ms, dev)
-    _device_error_check(pa)
 
     q8 = isinstance(step, DecodeStepQ8)
     pool_mib = (step.pool_bytes if q8 else 2 * step.case.k_cache[0].numel() * 2) / 2**20
@@ -607,10 +758,11 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({step.case.n_layers} distinct pools of {pool_mib:.0f} MiB "
                          f"cycled over {step.L} calls per step)",
-                   "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
+                   "timing": "CUDA events around K replays of a CUDA graph of one step, repeated; median repeat"},
+        "timing": timing_summary(reps, args.steps),
         "pct_of_hbm_peak": round(100.0 * value / world / hbm, 1),
         "tokens_per_s": round(world * step.S / (ms_step * 1e-3), 1),
-        "gpu_launches": step.kernels_per_step * args.steps,
+        "gpu_launches": step.kernels_per_step * args.steps * len(reps),
         "e2e": {"value": round(world * step.step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
@@ -619,20 +771,23 @@ def run_ours(args):
                                + ("one cluster per sequence and KV head" if step.decode_kernels == 1
                                   else "split + combine") + ")",
                      "bytes_per_launch": launch_bytes, "launch_ms": round(dec_launch_ms, 5),
-                     "traffic": committed_traffic("decode.cu", f"decode{tag}_workload{args.workload}.md")},
+                     "launches_timed": step.L * args.steps * len(dec_reps),
+                     "traffic": committed_traffic("decode.cu", f"decode{tag}_workload{workload}.md")},
         "clocks": clk.summary(),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and cpu and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(step, args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    del step, g_step, g_dec
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
 
 
-def run_mixed(args, dev, pa):
-    """Diagnostic line for the mixed chunked-prefill step (28 layers)."""
+def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool = True) -> dict:
+    """The JSON line of the mixed chunked-prefill step (28 layers)."""
     import torch
     rank, world, _ = dist_env()
-    step = MixedStep(dev, args.window, args.overlap)
+    step = MixedStep(dev, window, overlap)
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_pre = graph_of(step.run_prefill_only, 1, stream)
@@ -640,35 +795,76 @@ def run_mixed(args, dev, pa):
     time_replays(g_step, max(args.warmup, 3), stream)
     barrier(dev)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        ms_step = time_replays(g_step, args.steps, stream) / args.steps
-        n_pre = max(args.steps // 2, 10)
-        ms_pre = time_replays(g_pre, n_pre, stream) / n_pre / step.L
-    ms_step = reduce_max(ms_step, dev)
+    with ClockSampler(ClockSampler.gpu_id(dev)) as clk:
+        reps = timed_repeats(lambda: time_replays(g_step, args.steps, stream), args.min_seconds)
+        torch.cuda.synchronize()
+        barrier(dev)
+        pre_reps = timed_repeats(lambda: time_replays(g_pre, args.steps, stream), args.min_seconds / 2)
+        e2e_ms, h2d, d2h = e2e_measure_mixed(step, args.steps, max(args.warmup, 3), stream, args.min_seconds / 2)
+    ms_step = reduce_max(statistics.median(reps) / args.steps, dev)
+    e2e_ms = reduce_max(e2e_ms, dev)
+    ms_pre = statistics.median(pre_reps) / args.steps / step.L
     _device_error_check(pa)
     hbm, bf16, peak_kind = measured_peaks()
     tflops = step.flops_layer / (ms_pre * 1e-3) / 1e12
     line = {
-        "metric": METRIC, "value": round(world * step.tokens / (ms_step * 1e-3), 1), "unit": "tokens/s",
+        "metric": "mixed chunked-prefill step tokens/s; prefill-chunk TFLOP/s",
+        "value": round(world * step.tokens / (ms_step * 1e-3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "Qwen3-0.6B mixed chunked-prefill step, 28 layers: chunks (0,512), (512,512), "
-                               "(1536,512) + 512 decode seqs ctx U[16,1024], bf16; 2 distinct pools cycled"
-                               + (f"; sliding window of {args.window} keys (FLOPs of the visible pairs)"
-                                  if args.window else "")
-                               + ("; prefill and decode of each layer on two streams" if args.overlap else ""),
+                               "(1536,512) + 512 decode seqs ctx U[16,1024], Hq=16, Hkv=8, d=128, bf16; "
+                               "2 distinct pools cycled"
+                               + (f"; sliding window of {window} keys (FLOPs of the visible pairs)" if window else "")
+                               + ("; each layer's prefill on a second stream beside its decode" if overlap else ""),
                    "global_batch": 515 * world, "parallelism": f"replicas x{world}",
-                   "timing": "CUDA events around a CUDA graph of one step, replayed K times"},
-        "gpu_launches": step.L * step.kernels_per_layer * args.steps,
+                   "l2": "inputs larger than L2 (2 pools of {:.0f} MiB cycled over 28 layers)".format(
+                       2 * step.case.k_cache[0].numel() * 2 / 2**20),
+                   "timing": "CUDA events around K replays of a CUDA graph of one step, repeated; median repeat"},
+        "timing": timing_summary(reps, args.steps),
+        "decode_kv_gbs": round(step.L * step.decode_bytes_layer / (ms_step * 1e-3) / 1e9, 1),
+        "gpu_launches": step.L * step.kernels_per_layer * args.steps * len(reps),
+        "e2e": {"value": round(world * step.tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(tflops / bf16, 3), "peak_kind": peak_kind,
-                     "kernel": "paged_attn_prefill_chunk" + (f"_window (W={args.window})" if args.window else "")
+                     "kernel": "paged_attn_prefill_chunk" + (f"_window (W={window})" if window else "")
                                + " per layer", "flops_per_launch": step.flops_layer,
-                     "launch_ms": round(ms_pre, 5),
-                     "traffic": committed_traffic("prefill.cu", f"prefill{f'_window{args.window}' if args.window else ''}"
+                     "launch_ms": round(ms_pre, 5), "launches_timed": step.L * args.steps * len(pre_reps),
+                     "traffic": committed_traffic("prefill.cu", f"prefill{f'_window{window}' if window else ''}"
                                                                 f"_workload3.md")},
         "clocks": clk.summary(),
     }
+    if rank == 0 and cpu and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_mixed(step, args.cpu_seconds)
+    del step, g_step, g_pre
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_gqa_cache_gb300 as pa
+    if args.block_copy:
+        return run_block_copy(args, dev, pa)
+    if args.fused_write:
+        return run_fused_write(args, dev, pa)
+    if args.workload == 3:
+        line = mixed_line(args, dev, pa, args.window, args.overlap)
+    else:
+        line = decode_line(args, dev, pa, args.workload, args.kv, args.window, args.append, args.early_pages,
+                           args.pools)
+    if args.sublines:
+        line["prefill"] = mixed_line(args, dev, pa, overlap=True)
+        line["decode_0_6b"] = decode_line(args, dev, pa, 2, early_pages=args.early_pages)
+        line["gpu_launches_sublines"] = line["prefill"]["gpu_launches"] + line["decode_0_6b"]["gpu_launches"]
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -699,8 +895,9 @@ def run_block_copy(args, dev, pa):
     time_replays(g_step, max(args.warmup, 3), stream)
     barrier(dev)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        ms_step = time_replays(g_step, args.steps, stream) / args.steps
+    with ClockSampler(ClockSampler.gpu_id(dev)) as clk:
+        reps = timed_repeats(lambda: time_replays(g_step, args.steps, stream), args.min_seconds)
+        ms_step = statistics.median(reps) / args.steps
     ms_step = reduce_max(ms_step, dev)
     _device_error_check(pa)
     hbm, _, peak_kind = measured_peaks()
@@ -764,8 +961,9 @@ def run_fused_write(args, dev, pa):
     time_replays(g_step, max(args.warmup, 3), stream)
     barrier(dev)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        ms_step = time_replays(g_step, args.steps, stream) / args.steps
+    with ClockSampler(ClockSampler.gpu_id(dev)) as clk:
+        reps = timed_repeats(lambda: time_replays(g_step, args.steps, stream), args.min_seconds)
+        ms_step = statistics.median(reps) / args.steps
     ms_step = reduce_max(ms_step, dev)
     _device_error_check(pa)
     hbm, _, peak_kind = measured_peaks()
@@ -794,37 +992,33 @@ def run_fused_write(args, dev, pa):
 
 def run_reference(args):
     """The reference arm: the fp64 oracle (the pages print no runnable
-    implementation of this path) timed on the host cores, one decode layer of
-    the workload per step."""
+    implementation of this path) timed on the host cores on the default
+    line's workload, one decode layer call of the Qwen3-8B step per step."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import numpy as np
-    import torch
     import oracle
     import workloads
-    case = workloads.qwen3_0_6b_decode(device="cpu", n_layers=1, nan_fill=False)
+    oracle.build()
+    case = workloads.qwen3_8b_decode(device="cpu", n_layers=1, nan_fill=False)
     threads = os.cpu_count() or 1
-    kh = case.k_cache[0].view(torch.int16).numpy().view(np.uint16)
-    vh = case.v_cache[0].view(torch.int16).numpy().view(np.uint16)
-    qh = case.q[0].view(torch.int16).numpy().view(np.uint16)
+    kh, vh, qh = _u16(case.k_cache[0]), _u16(case.v_cache[0]), _u16(case.q[0])
     bt, ctx = case.block_tables.numpy(), case.context_lens.numpy()
     lay_bytes = workloads.decode_kv_bytes(case.meta["decode_lens"], case.hkv)
     for _ in range(max(args.warmup, 1)):
-        oracle.paged_attn_decode(qh, kh, vh, bt, ctx, case.scale, oracle.F16, num_threads=threads)
+        oracle.paged_attn_decode(qh, kh, vh, bt, ctx, case.scale, oracle.BF16, num_threads=threads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.paged_attn_decode(qh, kh, vh, bt, ctx, case.scale, oracle.F16, num_threads=threads)
+        oracle.paged_attn_decode(qh, kh, vh, bt, ctx, case.scale, oracle.BF16, num_threads=threads)
     dt = time.perf_counter() - t0
     ms_step = dt * 1e3 / args.steps
     value = lay_bytes / (dt / args.steps) / 1e9
-    sample = f"1 of 28 decode layers of the workload per step (fp64 C oracle, {threads} threads)"
+    sample = f"1 of the 36 decode layers of the Qwen3-8B step per step (fp64 C oracle, {threads} threads)"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "Qwen3-0.6B decode step, 28 layers: 8 seqs, ctx U[512,1024], Hq=16, Hkv=8, d=128, "
-                               "fp16, 512-block pool per layer", "global_batch": 8, "seq_len": case.max_context_len,
+        "config": {"workload": WORKLOADS[4][0], "global_batch": 64, "seq_len": case.max_context_len,
                    "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},

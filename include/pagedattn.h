@@ -26,6 +26,21 @@
  *     read and clear the word with pa_get_device_error().
  *   - head_dim is 128 and block_size is 16.  q, the pool and out share one
  *     dtype (fp16 or bf16).  Accumulation is fp32.
+ *   - Kernels are launched with programmatic dependent launch: each may start
+ *     while the kernel enqueued just before it on `stream` is finishing, and
+ *     waits for that kernel to complete before it reads the pool, q or k/v.
+ *     The attention calls read block_tables, context_lens and the chunk
+ *     metadata BEFORE that wait.  A caller kernel enqueued right before them
+ *     that signals programmatic launch completion early
+ *     (griddepcontrol.launch_dependents / cudaTriggerProgrammaticLaunchCompletion)
+ *     must therefore not write those arrays after its signal.  Kernels that
+ *     never signal (every PyTorch kernel, for one) are safe: the attention
+ *     kernel then starts only once they have ended.
+ *   - Per-context state: the device addresses of the library's own device
+ *     variables (the error word, the allocation-free decode's scratch) are
+ *     looked up once per CUDA context and keyed on its unique id, so calls
+ *     from a driver-API context of the host application, or after
+ *     cudaDeviceReset(), look them up anew in that context.
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H
@@ -205,11 +220,13 @@ PA_API int32_t pa_decode_kernel_launches(int32_t num_seqs, int32_t num_kv_heads,
  * pa_decode_workspace_bytes(...) exceeds PA_NOALLOC_SCRATCH_BYTES returns
  * PA_ERR_WORKSPACE and enqueues nothing (with 8 KV heads this admits head
  * ratios up to 4: e.g. up to ~7900 (sequence, KV head) pairs at ratio 4; a
- * ratio of 8 never fits).  It calls no allocator.  The first call on a device
- * (with that device current) looks up the array's device address once; make
- * it before any stream capture.  All calls share the array, which keeps the
- * last call's contents (nothing in it needs to start at zero); calls that
- * overlap on the GPU race on it, so serialise them.
+ * ratio of 8 never fits).  Argument errors are checked first, in the order
+ * pa_paged_attn_decode checks them, so a call that is both malformed and too
+ * large returns the argument error.  It calls no allocator.  The first call in
+ * a CUDA context (with that context's device current) looks up the array's
+ * device address; make it before any stream capture.  All calls share the
+ * array, which keeps the last call's contents (nothing in it needs to start at
+ * zero); calls that overlap on the GPU race on it, so serialise them.
  */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
 PA_API pa_status pa_paged_attn_decode_noalloc(const void *q, const pa_kv_pool *pool,

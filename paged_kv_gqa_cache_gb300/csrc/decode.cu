@@ -925,13 +925,9 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
   const int ctas = decode_item_ctas(items, max_pages_per_item);
   if (ctas > 0) {
     const int ismem = item_smem_bytes(G);
-    static bool item_configured = false;
-    if (!item_configured) {
-      cudaError_t e = cudaFuncSetAttribute(decode_item_kernel<T, G, Q8, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           ismem);
-      if (e != cudaSuccess) return e;
-      item_configured = true;
-    }
+    static KernelSetup item_setup;
+    cudaError_t e = kernel_setup(item_setup, decode_item_kernel<T, G, Q8, F8>, ismem, kItemWarps * 32, nullptr);
+    if (e != cudaSuccess) return e;
     return launch_pdl_cluster(decode_item_kernel<T, G, Q8, F8>, dim3(items * ctas), dim3(kItemWarps * 32), ismem, ctas,
                               stream, kmap, vmap, p);
   }
@@ -939,20 +935,10 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
   // Per instantiation: raise the dynamic shared-memory limit and cache the
   // occupancy for the largest size seen (launch-time API calls stay out of
   // the hot path and out of CUDA-graph capture after the first call).
-  static int configured_smem = 0, cached_per_sm = 0;
-  if (smem > configured_smem) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, G, Q8, F8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel<T, G, Q8, F8>, NW * 32, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    configured_smem = smem;
-    cached_per_sm = per_sm;
-  }
-  const int per_sm = cached_per_sm;
-  cudaError_t e;
+  static KernelSetup split_setup;
+  int per_sm = 0;
+  cudaError_t e = kernel_setup(split_setup, decode_split_kernel<T, G, Q8, F8>, smem, NW * 32, &per_sm);
+  if (e != cudaSuccess) return e;
   int grid = sm_count() * per_sm;
   const int want = (max_workers + NW - 1) / NW;
   if (want < grid) grid = want;

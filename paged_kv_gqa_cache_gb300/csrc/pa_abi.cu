@@ -5,8 +5,10 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
+#include "context_cache.h"
 #include "pa_internal.h"
 
 namespace pa {
@@ -17,6 +19,7 @@ __device__ int g_error_word[2];
 namespace {
 
 thread_local int t_last_cuda_error = 0;
+thread_local unsigned long long t_context_id = 0;
 
 struct DeviceState {
   bool ready = false;
@@ -26,39 +29,106 @@ struct DeviceState {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-DeviceState g_devices[kMaxDevices];
+int g_sm_count[kMaxDevices] = {};        // per device, whatever the context
+thread_local DeviceState t_state;        // this thread's current device and context
+ContextCache<int *, kMaxDevices> g_error_word_address;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
 
 pa_status cuda_fail(cudaError_t e) {
   t_last_cuda_error = (int)e;
   return PA_ERR_CUDA;
 }
 
-// Set-up once per device, with that device current.
+// Driver entry points the library calls directly (resolved once).
+std::atomic<bool> g_entry_points_ready{false};
+pa_status driver_entry_points() {
+  if (g_entry_points_ready.load(std::memory_order_acquire)) return PA_OK;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  struct Want {
+    const char *name;
+    void **fn;
+    int version;
+  } want[] = {{"cuTensorMapEncodeTiled", reinterpret_cast<void **>(&g_encode), 12000},
+              {"cuCtxGetCurrent", reinterpret_cast<void **>(&g_ctx_get_current), 4000},
+              {"cuCtxGetId", reinterpret_cast<void **>(&g_ctx_get_id), 12000}};
+  for (const Want &w : want) {
+    if (*w.fn) continue;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion(w.name, &fn, w.version, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (q != cudaDriverEntryPointSuccess || !fn) return PA_ERR_CUDA;
+    *w.fn = fn;
+  }
+  g_entry_points_ready.store(true, std::memory_order_release);
+  return PA_OK;
+}
+
+}  // namespace
+
+// The unique id of the current CUDA context.  With no context current, the
+// current device's primary context is initialised and made current first
+// (what the runtime would do on the next kernel launch).
+pa_status current_context_id(unsigned long long *id) {
+  pa_status st = driver_entry_points();
+  if (st != PA_OK) return st;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return PA_ERR_CUDA;
+  if (!ctx) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);  // initialises the device's primary context
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return PA_ERR_CUDA;
+  }
+  unsigned long long v = 0;
+  if (g_ctx_get_id(ctx, &v) != CUDA_SUCCESS || v == 0) return PA_ERR_CUDA;
+  *id = v;
+  return PA_OK;
+}
+
+unsigned long long launch_context_id() { return t_context_id; }
+
+namespace {
+
+// Set-up per device (SM count) and per context (the error word's address),
+// with that device current.  Every entry point that launches calls it first,
+// which also records the context for launch_context_id().
 pa_status device_state(DeviceState **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  DeviceState &d = g_devices[dev];
-  if (!d.ready) {
-    e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    // The host-side name of a __device__ variable is not a device address;
-    // ask the runtime for the real one.
-    e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_error_word);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (!g_encode) {
-      void *fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cuda_fail(e);
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  unsigned long long ctx = 0;
+  pa_status st = current_context_id(&ctx);
+  if (st != PA_OK) return st;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_sm_count[dev] == 0) {
+      e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(e);
     }
-    d.ready = true;
+    sms = g_sm_count[dev];
   }
-  *out = &d;
+  // The host-side name of a __device__ variable is not a device address;
+  // ask the runtime for the real one, in this context.
+  int *err = nullptr;
+  cudaError_t fetch_err = cudaSuccess;
+  if (!g_error_word_address.get(dev, ctx,
+                                [&](int **v) {
+                                  fetch_err = cudaGetSymbolAddress(reinterpret_cast<void **>(v), g_error_word);
+                                  return fetch_err == cudaSuccess && *v != nullptr;
+                                },
+                                &err))
+    return fetch_err != cudaSuccess ? cuda_fail(fetch_err) : PA_ERR_CUDA;
+  t_state.ready = true;
+  t_state.sm_count = sms;
+  t_state.err = err;
+  t_context_id = ctx;
+  *out = &t_state;
   return PA_OK;
 }
 
@@ -194,6 +264,27 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
 }
 
 }  // namespace
+
+// The checks pa_paged_attn_decode makes before it looks at its workspace, in
+// the same order, for the allocation-free entry point (which has none).
+pa_status decode_check_args(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t max_context_len, float scale, void *out) {
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0) return PA_ERR_SHAPE;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  int group = 0;
+  if ((st = check_group(num_q_heads, pool->num_kv_heads, &group)) != PA_OK) return st;
+  if (max_blocks_per_seq < 1 || max_context_len < 1 ||
+      (int64_t)max_context_len > (int64_t)max_blocks_per_seq * kBlock)
+    return PA_ERR_SHAPE;
+  if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(block_tables) || !aligned4(context_lens)) return PA_ERR_ALIGN;
+  return PA_OK;
+}
 
 int sm_count() {
   DeviceState *d = nullptr;

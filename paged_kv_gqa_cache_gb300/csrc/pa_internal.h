@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "../../include/pagedattn.h"
@@ -206,6 +207,45 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 
 // ---- shared host helpers (pa_abi.cu) ------------------------------------------
 int sm_count();
+// pa_paged_attn_decode's argument checks up to (not including) the workspace.
+pa_status decode_check_args(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t max_context_len, float scale, void *out);
+// Unique id of the current CUDA context (initialising the current device's
+// primary context if none is current).
+pa_status current_context_id(unsigned long long *id);
+// The context id recorded by the entry point now running on this thread
+// (every entry point that launches looks it up first).
+unsigned long long launch_context_id();
+
+// A kernel's launch set-up (its raised dynamic shared-memory limit and the
+// occupancy at that size) belongs to one context: it is redone when the
+// calling thread's context is another one, or a larger size is wanted.
+struct KernelSetup {
+  std::mutex mutex;
+  unsigned long long ctx = 0;
+  int smem = 0;
+  int per_sm = 0;
+};
+template <typename Kernel>
+cudaError_t kernel_setup(KernelSetup &s, Kernel kernel, int smem, int threads, int *per_sm) {
+  std::lock_guard<std::mutex> lock(s.mutex);
+  const unsigned long long ctx = launch_context_id();
+  if (s.ctx != ctx || smem > s.smem) {
+    const int want = (s.ctx == ctx && s.smem > smem) ? s.smem : smem;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, want);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    s.ctx = ctx;
+    s.smem = want;
+    s.per_sm = n;
+  }
+  if (per_sm) *per_sm = s.per_sm;
+  return cudaSuccess;
+}
 bool encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, int rank, void *base,
                        const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                        CUtensorMapSwizzle swizzle,

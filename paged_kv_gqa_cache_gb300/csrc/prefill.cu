@@ -99,6 +99,7 @@ struct Bars {
   uint64_t p_full[kVStages];   // P of the tile written by every softmax thread, each of which saw V land
   uint64_t pv_done[kVStages];  // P V of the tile done: O holds it, V stage free
   uint64_t x_full;
+  uint64_t drain;              // timeout path only: every MMA issued so far has completed
   uint32_t tmem_base;
 };
 
@@ -274,6 +275,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       mbar_init(&bars.pv_done[b], 1);
     }
     mbar_init(&bars.x_full, kSoftmaxThreads);
+    mbar_init(&bars.drain, 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -300,6 +302,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
     }
     const int kb0 = lw, vb0 = (lw + kLoadWarps - 1) % kLoadWarps;  // balances the boxes per warp
+    int k_issued = 0, v_issued = 0;  // tiles whose K / V boxes this warp has issued
     for (int t = 0; t < ntl; ++t) {
       const int ks = t % kKStages, vs = t % kVStages;
       if (t >= kKStages && !mbar_wait(&bars.s_full[ks], ((t - kKStages) / kKStages) & 1)) {
@@ -308,12 +311,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
       load_boxes(smem + OFF_K + ks * 2 * kHalf, &kmap, &bars.k_full[ks], kt0 + t, kb0, h, pg0, npages, false, sbt,
                  bt, p, c, lane);
+      k_issued = t + 1;
       if (t >= kVStages && !mbar_wait(&bars.pv_done[vs], ((t - kVStages) / kVStages) & 1)) {
         timed_out = true;
         break;
       }
       load_boxes(smem + OFF_V + vs * 2 * kHalf, &vmap, &bars.v_full[vs], kt0 + t, vb0, h, pg0, npages, true, sbt,
                  bt, p, c, lane);
+      v_issued = t + 1;
+    }
+    if (timed_out) {
+      // Before the CTA ends (and its shared memory is handed to another CTA),
+      // give this warp's copies still in flight a short, bounded chance to
+      // land: the last tile of each stage it issued (each stage's barrier is
+      // at most at that tile's phase).  A barrier that another warp left
+      // short of its arrivals never completes; the wait then just ends.
+      if (lw == 0) mbar_wait(&bars.q_full, 0, kWaitLimitNs / 8);
+      for (int t = k_issued - kKStages > 0 ? k_issued - kKStages : 0; t < k_issued; ++t)
+        mbar_wait(&bars.k_full[t % kKStages], (t / kKStages) & 1, kWaitLimitNs / 8);
+      for (int t = v_issued - kVStages > 0 ? v_issued - kVStages : 0; t < v_issued; ++t)
+        mbar_wait(&bars.v_full[t % kVStages], (t / kVStages) & 1, kWaitLimitNs / 8);
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
@@ -392,6 +409,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
           tc::commit(&bars.pv_done[jv]);
         }
+      }
+      if (timed_out) {
+        // The MMAs already issued may still be writing TMEM (and reading
+        // shared memory): one more commit tracks all of them; wait for it,
+        // bounded, before the CTA frees its TMEM and ends.
+        tc::commit(&bars.drain);
+        mbar_wait(&bars.drain, 0, kWaitLimitNs / 8);
       }
     }
   } else {
@@ -563,13 +587,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 template <typename T, int G>
 cudaError_t launch_typed(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
                          const CUtensorMap &qmap, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static KernelSetup setup;
+  cudaError_t e = kernel_setup(setup, prefill_kernel<T, G>, SMEM_BYTES, kThreads, nullptr);
+  if (e != cudaSuccess) return e;
   constexpr int TQ = 128 / G;
   dim3 grid((p.max_chunk_len + TQ - 1) / TQ, p.num_kv_heads, p.num_chunks);
   return launch_pdl(prefill_kernel<T, G>, grid, dim3(kThreads), SMEM_BYTES, stream, kmap, vmap, qmap, p);

@@ -12,9 +12,12 @@ import torch.multiprocessing as mp
 import bench
 
 
-def test_default_arguments_are_one_gpu_and_the_decode_step():
+def test_default_arguments_are_one_gpu_and_the_8b_decode_step_with_its_sublines():
     a = bench.parse_args([])
-    assert a.gpus == 1 and a.workload == 2 and a.impl == "ours" and a.warmup >= 3 and a.steps > 0
+    assert a.gpus == 1 and a.workload == 4 and a.impl == "ours" and a.warmup >= 3 and a.steps > 0
+    assert a.sublines and a.min_seconds >= 1.0
+    assert not bench.parse_args(["--workload", "2"]).sublines and not bench.parse_args(["--kv", "int8"]).sublines
+    assert not bench.parse_args(["--no-sublines"]).sublines
     assert a.early_pages and not bench.parse_args(["--no-early-pages"]).early_pages
     assert not bench.parse_args(["--window", "256"]).early_pages and bench.parse_args(["--kv", "int8"]).early_pages
 
@@ -65,3 +68,21 @@ def test_max_over_two_gloo_ranks():
 def test_reduce_max_without_a_process_group_is_the_identity():
     assert not dist.is_initialized()
     assert bench.reduce_max(3.5) == 3.5
+
+
+def test_timed_repeats_reach_the_minimum_time_and_count():
+    reps = bench.timed_repeats(lambda: 100.0, 1.0)          # 100 ms per repeat: 10 repeats for 1 s
+    assert len(reps) == 10
+    assert len(bench.timed_repeats(lambda: 900.0, 1.0)) == 5  # at least 5 repeats
+    t = bench.timing_summary([1.0, 2.0, 3.0], 10)
+    assert t["repeats"] == 3 and t["timed_region_s"] == 0.006 and t["ms_per_step_max"] == 0.3
+
+
+def test_clock_summary_parses_samples():
+    c = bench.ClockSampler("0")
+    c.rows = [["0", "2070", "2070", "900.5", "0x0", "Not Active", "Not Active", "Not Active", "Active"],
+              ["0", "1965", "2070", "1350.0", "0x4", "Not Active", "Not Active", "Not Active", "Not Active"],
+              ["0", "2070", "2070", "1000.0", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]]
+    s = c.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "power_w_max": 1350.0, "reasons": ["sw_power_cap"],
+                 "samples": 3}

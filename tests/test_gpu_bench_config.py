@@ -57,7 +57,7 @@ def test_qwen3_0_6b_decode_step_with_the_fused_append(early):
 
 
 def test_qwen3_8b_decode_as_benchmarked():
-    step = bench.DecodeStep(DEV, workload=4, early_pages=True)      # 36 layers cycling 4 pools of 1 GiB
+    step = bench.DecodeStep(DEV, workload=4, pools=4, early_pages=True)  # 36 layers cycling 4 pools of 1 GiB
     _check_decode_step(step, range(step.case.n_layers))
 
 
@@ -98,3 +98,25 @@ def test_end_to_end_path_returns_the_right_outputs_to_the_host(append):
         assert oracle.kv_cache_write(kh, vh, bits(c.k_new[l]), bits(c.v_new[l]), c.slot_mapping.cpu().numpy()) == 0
         ref = oracle.paged_attn_decode(bits(c.q[l]), kh, vh, bt, ctx, c.scale, ORACLE_DTYPE[c.dtype])
         check_close(step.e2e_outputs[l], ref, f"e2e layer {l}")
+
+
+def test_mixed_step_end_to_end_path_returns_the_right_outputs_to_the_host():
+    # the mixed step's e2e leg: every layer's inputs and the step's metadata
+    # copied from pinned host memory, both outputs of every layer copied back
+    step = bench.MixedStep(DEV, overlap=True)
+    c = step.case
+    before = [(bits(c.k_cache[i]), bits(c.v_cache[i])) for i in range(2)]
+    stream = torch.cuda.Stream(device=DEV)
+    bench.e2e_measure_mixed(step, 1, 0, stream)     # the warm-up call and one timed step
+    for l in (0, step.L - 1):
+        kh, vh = before[l % 2]
+        assert oracle.kv_cache_write(kh, vh, bits(c.k_new[l % 2]), bits(c.v_new[l % 2]),
+                                     c.slot_mapping.cpu().numpy()) == 0
+        out_d, out_p = step.e2e_outputs[l]
+        refp = oracle.paged_attn_prefill(bits(c.q_chunks[l % 2]), kh, vh, c.chunk_starts.cpu().numpy(),
+                                         c.chunk_lens.cpu().numpy(), c.chunk_block_tables.cpu().numpy(),
+                                         c.chunk_context_lens.cpu().numpy(), c.scale, oracle.BF16)
+        check_close(out_p, refp, f"mixed e2e prefill, layer {l}")
+        refd = oracle.paged_attn_decode(bits(c.q[l % 2]), kh, vh, c.block_tables.cpu().numpy(),
+                                        c.context_lens.cpu().numpy(), c.scale, oracle.BF16)
+        check_close(out_d, refd, f"mixed e2e decode, layer {l}")
