@@ -84,6 +84,10 @@ def parse_args(argv=None):
                     help="decode workloads without a window: do not pass PA_DECODE_EARLY_PAGES. By "
                          "default each decode call fetches its cached pages before the preceding KV write has "
                          "finished, which the step allows: that write touches only each sequence's last page")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="decode calls with PA_DECODE_ZEROED_WORKSPACE: one launch over all SMs that merges "
+                         "split sequences itself, instead of the plain plan (one cluster per sequence and KV "
+                         "head when they fit, else split + combine kernels)")
     ap.add_argument("--overlap", action="store_true",
                     help="workload 3: each layer's prefill on a second stream beside its decode (same work)")
     ap.add_argument("--window", type=int, default=0,
@@ -107,6 +111,7 @@ def parse_args(argv=None):
     if args.append and (args.window or args.kv != "16bit" or args.workload == 3):
         ap.error("--append applies to the 16-bit decode workloads 2, 4 and 5 without a window")
     args.early_pages = not args.no_early_pages and not args.window
+    args.fused = args.fused_combine
     args.sublines = (args.workload == 4 and not args.no_sublines and args.kv == "16bit" and not args.window
                      and not args.append and not args.block_copy and not args.fused_write)
     return args
@@ -262,7 +267,7 @@ class DecodeStep:
     cycled when fewer distinct pools than calls are held)."""
 
     def __init__(self, device, workload: int = 2, pools: int = 0, window: int = 0, append: bool = False,
-                 early_pages: bool = False):
+                 early_pages: bool = False, fused: bool = False):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
@@ -271,6 +276,7 @@ class DecodeStep:
         self.window = window
         self.append = append
         self.early_pages = early_pages
+        self.fused = fused            # PA_DECODE_ZEROED_WORKSPACE: one launch over all SMs
         self.desc, default_pools, self.L = WORKLOADS[workload]
         pools = pools or default_pools
         maker = workloads.BY_INDEX[workload]
@@ -290,7 +296,7 @@ class DecodeStep:
                                                                 c.hkv)
         self.write_bytes_layer = 2 * c.k_new[0].numel() * 2 * 2     # K and V rows, read + write
         self.step_bytes = self.L * (self.decode_bytes_layer + self.write_bytes_layer)
-        self.decode_kernels = pa.decode_kernel_launches(self.S, c.hkv, c.max_context_len, window)
+        self.decode_kernels = 1 if fused else pa.decode_kernel_launches(self.S, c.hkv, c.max_context_len, window)
         # write, then the decode's kernels (the write runs inside the decode with append)
         self.kernels_per_step = self.L * ((0 if append else 1) + self.decode_kernels)
 
@@ -312,13 +318,15 @@ class DecodeStep:
             kn, vn = (c.k_new[i], c.v_new[i]) if kn is None else (kn, vn)
             self.pa.paged_attn_decode_append(q, kn, vn, c.k_cache[i], c.v_cache[i], bt, ctx, c.scale, out=out,
                                              workspace=self.ws, max_context_len=c.max_context_len,
-                                             early_pages=self.early_pages)
+                                             early_pages=self.early_pages, zeroed_workspace=self.fused)
         elif self.window:
             self.pa.paged_attn_decode_window(q, c.k_cache[i], c.v_cache[i], bt, ctx, c.scale, self.window, out=out,
-                                             workspace=self.ws, max_context_len=c.max_context_len)
+                                             workspace=self.ws, max_context_len=c.max_context_len,
+                                             zeroed_workspace=self.fused)
         else:
             self.pa.paged_attn_decode(q, c.k_cache[i], c.v_cache[i], bt, ctx, c.scale, out=out, workspace=self.ws,
-                                      max_context_len=c.max_context_len, early_pages=self.early_pages)
+                                      max_context_len=c.max_context_len, early_pages=self.early_pages,
+                                      zeroed_workspace=self.fused)
 
     def run(self):
         for l in range(self.L):
@@ -338,10 +346,11 @@ class DecodeStepQ8(DecodeStep):
     8-bit pool by the library's own write; each layer of the step then
     quantises the new tokens into their slots and decodes."""
 
-    def __init__(self, device, workload: int = 2, pools: int = 0, fp8: bool = False, early_pages: bool = False):
+    def __init__(self, device, workload: int = 2, pools: int = 0, fp8: bool = False, early_pages: bool = False,
+                 fused: bool = False):
         import numpy as np
         import torch
-        super().__init__(device, workload, pools, early_pages=early_pages)
+        super().__init__(device, workload, pools, early_pages=early_pages, fused=fused)
         self.fp8 = fp8
         alloc = self.pa.alloc_pool_f8 if fp8 else self.pa.alloc_pool_q8
         self._write = self.pa.kv_cache_write_f8 if fp8 else self.pa.kv_cache_write_q8
@@ -379,7 +388,7 @@ class DecodeStepQ8(DecodeStep):
         bt, ctx = (c.block_tables, c.context_lens) if meta is None else meta[1:]
         self._decode(c.q[i] if q is None else q, *self.q8[i], bt, ctx, c.scale,
                      out=self.out[i] if out is None else out, workspace=self.ws, max_context_len=c.max_context_len,
-                     early_pages=self.early_pages)
+                     early_pages=self.early_pages, zeroed_workspace=self.fused)
 
 
 class MixedStep:
@@ -387,11 +396,11 @@ class MixedStep:
     kv_cache_write of 2048 new tokens, prefill of 3 chunks of 512 (prefixes 0,
     512, 1536) and decode of 512 sequences; 2 distinct pools cycled over 28."""
 
-    def __init__(self, device, window: int = 0, overlap: bool = False):
+    def __init__(self, device, window: int = 0, overlap: bool = False, fused: bool = False):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
-        self.pa, self.L, self.window, self.overlap = pa, 28, window, overlap
+        self.pa, self.L, self.window, self.overlap, self.fused = pa, 28, window, overlap, fused
         # overlap: each layer's prefill (tensor-bound) runs on a second stream beside its decode (HBM-bound)
         self.side = torch.cuda.Stream(device=device) if overlap else None
         self.case = c = workloads.qwen3_0_6b_mixed_step(device=device, n_layers=2, nan_fill=False)
@@ -403,7 +412,8 @@ class MixedStep:
         self.tokens = c.slot_mapping.numel()
         lens = c.meta["decode_lens"]
         self.decode_bytes_layer = workloads.decode_kv_bytes([min(n, window) if window else n for n in lens], c.hkv)
-        self.kernels_per_layer = 2 + pa.decode_kernel_launches(len(lens), c.hkv, c.max_context_len, window)
+        self.kernels_per_layer = 2 + (1 if fused else pa.decode_kernel_launches(len(lens), c.hkv, c.max_context_len,
+                                                                                window))
 
     def prefill(self, l, qp=None, out=None, meta=None):
         c, i = self.case, l % 2
@@ -430,7 +440,8 @@ class MixedStep:
             self.prefill(l, qp, out_p, meta)
         self.pa.paged_attn_decode_window(c.q[i] if q is None else q, c.k_cache[i], c.v_cache[i], bt, ctx, c.scale,
                                          self.window, out=self.out_d[i] if out_d is None else out_d,
-                                         workspace=self.ws, max_context_len=c.max_context_len)
+                                         workspace=self.ws, max_context_len=c.max_context_len,
+                                         zeroed_workspace=self.fused)
         if self.side is not None:
             main.wait_stream(self.side)
 
@@ -709,8 +720,8 @@ def decode_line(args, dev, pa, workload: int, kv: str = "16bit", window: int = 0
     """The JSON line of one decode workload (steps of write + decode per layer)."""
     import torch
     rank, world, _ = dist_env()
-    step = (DecodeStepQ8(dev, workload, pools, kv == "fp8", early_pages) if kv != "16bit"
-            else DecodeStep(dev, workload, pools, window, append, early_pages))
+    step = (DecodeStepQ8(dev, workload, pools, kv == "fp8", early_pages, args.fused) if kv != "16bit"
+            else DecodeStep(dev, workload, pools, window, append, early_pages, args.fused))
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_dec = graph_of(step.run_decode_only, 1, stream)
@@ -753,7 +764,9 @@ def decode_line(args, dev, pa, workload: int, kv: str = "16bit", window: int = 0
                                + (f", sliding window of {win} keys (bytes of the visible rows)" if win else "")
                                + (", KV write fused into the decode call" if getattr(step, "append", False) else "")
                                + (", cached pages fetched before the preceding write ends (PA_DECODE_EARLY_PAGES)"
-                                  if getattr(step, "early_pages", False) else ""),
+                                  if getattr(step, "early_pages", False) else "")
+                               + (", one decode launch over all SMs merging split sequences itself "
+                                  "(PA_DECODE_ZEROED_WORKSPACE)" if step.fused else ""),
                    "global_batch": step.S * world, "seq_len": step.case.max_context_len,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({step.case.n_layers} distinct pools of {pool_mib:.0f} MiB "
@@ -768,7 +781,8 @@ def decode_line(args, dev, pa, workload: int, kv: str = "16bit", window: int = 0
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "peak_kind": peak_kind,
                      "kernel": "paged_attn_decode" + tag + " per layer ("
-                               + ("one cluster per sequence and KV head" if step.decode_kernels == 1
+                               + ("one launch over all SMs, split sequences merged in it" if step.fused else
+                                  "one cluster per sequence and KV head" if step.decode_kernels == 1
                                   else "split + combine") + ")",
                      "bytes_per_launch": launch_bytes, "launch_ms": round(dec_launch_ms, 5),
                      "launches_timed": step.L * args.steps * len(dec_reps),
@@ -787,7 +801,7 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
     """The JSON line of the mixed chunked-prefill step (28 layers)."""
     import torch
     rank, world, _ = dist_env()
-    step = MixedStep(dev, window, overlap)
+    step = MixedStep(dev, window, overlap, args.fused)
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_pre = graph_of(step.run_prefill_only, 1, stream)
@@ -816,7 +830,9 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
                                "(1536,512) + 512 decode seqs ctx U[16,1024], Hq=16, Hkv=8, d=128, bf16; "
                                "2 distinct pools cycled"
                                + (f"; sliding window of {window} keys (FLOPs of the visible pairs)" if window else "")
-                               + ("; each layer's prefill on a second stream beside its decode" if overlap else ""),
+                               + ("; each layer's prefill on a second stream beside its decode" if overlap else "")
+                               + ("; decode as one launch over all SMs (PA_DECODE_ZEROED_WORKSPACE)"
+                                  if step.fused else ""),
                    "global_batch": 515 * world, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (2 pools of {:.0f} MiB cycled over 28 layers)".format(
                        2 * step.case.k_cache[0].numel() * 2 / 2**20),

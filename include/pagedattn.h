@@ -183,12 +183,23 @@ PA_API pa_status pa_paged_attn_decode_append(const void *q, const void *k_new, c
  *                 promise covers that earlier work too.  The one-launch path
  *                 then starts fetching the other pages before that work has
  *                 finished, overlapping it (the results do not change).
- *                 Breaking the promise gives undefined results.  Other bits:
- *                 PA_ERR_UNSUPPORTED.
+ *                 Breaking the promise gives undefined results.
+ *                 PA_DECODE_ZEROED_WORKSPACE: a promise that the workspace
+ *                 was zero-filled before its first use and has since been
+ *                 used only by calls that completed without PA_ERR_TIMEOUT
+ *                 (every such call leaves the workspace's item counters at
+ *                 zero again).  The call then runs as ONE kernel over all
+ *                 SMs whatever the sizes: pages are dealt evenly to every
+ *                 warp the GPU holds, and the warp that finishes the last
+ *                 piece of a split (sequence, KV head) merges the pieces
+ *                 (log-sum-exp) from L2, counting arrivals in the workspace.
+ *                 After a PA_ERR_TIMEOUT, zero-fill the workspace again.
+ *                 Other bits: PA_ERR_UNSUPPORTED.
  * Other arguments, workspace and errors as pa_paged_attn_decode.  No
  * counterpart on the pages: a library addition.
  */
 #define PA_DECODE_EARLY_PAGES 1u
+#define PA_DECODE_ZEROED_WORKSPACE 2u
 PA_API pa_status pa_paged_attn_decode_ex(const void *q, const pa_kv_pool *pool, const int32_t *block_tables,
                                          int32_t max_blocks_per_seq, const int32_t *context_lens,
                                          int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
@@ -338,10 +349,10 @@ PA_API pa_status pa_paged_attn_decode_f8(const void *q, int32_t dtype, const pa_
  * paged_attn_decode_q8_ex — the decode over an 8-bit pool with flags:
  *   codes   PA_CODES_INT8 (as pa_paged_attn_decode_q8) or PA_CODES_E4M3 (as
  *           pa_paged_attn_decode_f8); anything else: PA_ERR_UNSUPPORTED;
- *   flags   0 or PA_DECODE_EARLY_PAGES, with the promise stated at
- *           pa_paged_attn_decode_ex (pa_kv_cache_write_q8 / _f8 let the next
- *           kernel start beside the tail of the work before them, as
- *           pa_kv_cache_write does); other bits: PA_ERR_UNSUPPORTED.
+ *   flags   PA_DECODE_EARLY_PAGES and PA_DECODE_ZEROED_WORKSPACE, with the
+ *           promises stated at pa_paged_attn_decode_ex (pa_kv_cache_write_q8
+ *           / _f8 let the next kernel start beside the tail of the work before
+ *           them, as pa_kv_cache_write does); other bits: PA_ERR_UNSUPPORTED.
  * Other arguments, workspace and errors as pa_paged_attn_decode_q8.  No
  * counterpart on the pages: a library addition.
  */

@@ -280,9 +280,9 @@ def paged_attn_decode_q8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.
                          v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                          scale: float, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                          max_context_len: Optional[int] = None, stream=None, _fp8: bool = False,
-                         early_pages: bool = False) -> torch.Tensor:
+                         early_pages: bool = False, zeroed_workspace: bool = False) -> torch.Tensor:
     """Decode attention over an int8 pool: q [S, Hq, 128] (fp16 / bf16) → out, same dtype.
-    ``early_pages`` as for :func:`paged_attn_decode`."""
+    ``early_pages`` and ``zeroed_workspace`` as for :func:`paged_attn_decode`."""
     pool = make_pool_q8(k_codes, v_codes, k_scale, v_scale, torch.uint8 if _fp8 else torch.int8)
     _need(q, "q")
     _need(block_tables, "block_tables", torch.int32)
@@ -300,10 +300,11 @@ def paged_attn_decode_q8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.
     _need(workspace, "workspace")
     lib = load_library()
     wsb = workspace.numel() * workspace.element_size()
-    if early_pages:
+    flags = (DECODE_EARLY_PAGES if early_pages else 0) | (DECODE_ZEROED_WORKSPACE if zeroed_workspace else 0)
+    if flags:
         _check(lib.pa_paged_attn_decode_q8_ex(q.data_ptr(), _dtype_code(q), ctypes.byref(pool), 1 if _fp8 else 0,
                                               block_tables.data_ptr(), mb, context_lens.data_ptr(), S, hq, mcl,
-                                              float(scale), DECODE_EARLY_PAGES, out.data_ptr(), workspace.data_ptr(),
+                                              float(scale), flags, out.data_ptr(), workspace.data_ptr(),
                                               wsb, _stream(stream)), "pa_paged_attn_decode_q8_ex")
         return out
     fn, name = (lib.pa_paged_attn_decode_f8, "pa_paged_attn_decode_f8") if _fp8 else \
@@ -323,10 +324,11 @@ def paged_attn_decode_f8(q: torch.Tensor, k_codes: torch.Tensor, v_codes: torch.
                          v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                          scale: float, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                          max_context_len: Optional[int] = None, stream=None,
-                         early_pages: bool = False) -> torch.Tensor:
+                         early_pages: bool = False, zeroed_workspace: bool = False) -> torch.Tensor:
     """Decode attention over an fp8 (E4M3) pool: q [S, Hq, 128] (fp16 / bf16) → out, same dtype."""
     return paged_attn_decode_q8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale, out,
-                                workspace, max_context_len, stream, _fp8=True, early_pages=early_pages)
+                                workspace, max_context_len, stream, _fp8=True, early_pages=early_pages,
+                                zeroed_workspace=zeroed_workspace)
 
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int) -> int:
@@ -345,15 +347,17 @@ def decode_kernel_launches(num_seqs: int, num_kv_heads: int, max_context_len: in
 
 def alloc_decode_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, max_context_len: int,
                            device=None) -> torch.Tensor:
+    """A decode workspace, zero-filled (so it may also serve calls with
+    ``zeroed_workspace=True``, which leave it zeroed)."""
     n = decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, max_context_len)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                       block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                       out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                       max_context_len: Optional[int] = None, stream=None,
-                      early_pages: bool = False) -> torch.Tensor:
+                      early_pages: bool = False, zeroed_workspace: bool = False) -> torch.Tensor:
     """Decode attention: q [S, Hq, 128] → out [S, Hq, 128] (pool dtype).
 
     ``max_context_len`` is a host-side bound on ``context_lens`` (no device
@@ -361,26 +365,32 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     ``early_pages``: the caller promises that the work enqueued just before
     this call writes no page of a sequence but its last visible one (a
     decode step's KV write), so the pages may be fetched before it ends
-    (``pa_paged_attn_decode_ex`` with ``PA_DECODE_EARLY_PAGES``)."""
+    (``pa_paged_attn_decode_ex`` with ``PA_DECODE_EARLY_PAGES``).
+    ``zeroed_workspace``: the caller promises that ``workspace`` was
+    zero-filled (as :func:`alloc_decode_workspace` does) and only used by
+    calls that did not time out since; the decode then runs as one kernel over
+    all SMs that merges split sequences itself
+    (``PA_DECODE_ZEROED_WORKSPACE``)."""
     return _decode(q, k_cache, v_cache, block_tables, context_lens, scale, 0, out, workspace, max_context_len,
-                   stream, flags=DECODE_EARLY_PAGES if early_pages else 0)
+                   stream, flags=_flags(early_pages, zeroed_workspace))
 
 
 def paged_attn_decode_window(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                              block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, window: int,
                              out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                             max_context_len: Optional[int] = None, stream=None) -> torch.Tensor:
+                             max_context_len: Optional[int] = None, stream=None,
+                             zeroed_workspace: bool = False) -> torch.Tensor:
     """Decode attention over the last ``window`` keys of each sequence (window
     0: all of them); otherwise as :func:`paged_attn_decode`."""
     return _decode(q, k_cache, v_cache, block_tables, context_lens, scale, int(window), out, workspace,
-                   max_context_len, stream)
+                   max_context_len, stream, flags=_flags(False, zeroed_workspace))
 
 
 def paged_attn_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
                              v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                              scale: float, out: Optional[torch.Tensor] = None,
                              workspace: Optional[torch.Tensor] = None, max_context_len: Optional[int] = None,
-                             stream=None, early_pages: bool = False) -> torch.Tensor:
+                             stream=None, early_pages: bool = False, zeroed_workspace: bool = False) -> torch.Tensor:
     """Write each sequence's new token (k_new, v_new [S, Hkv, 128]) at position
     context_lens[s] - 1 of its block table and decode, in one call; otherwise
     as :func:`paged_attn_decode`."""
@@ -389,10 +399,15 @@ def paged_attn_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.
     if k_new.shape != (q.shape[0], k_cache.shape[2], q.shape[2]) or v_new.shape != k_new.shape:
         raise ValueError("k_new and v_new must be [S, Hkv, 128]")
     return _decode(q, k_cache, v_cache, block_tables, context_lens, scale, 0, out, workspace, max_context_len,
-                   stream, append=(k_new, v_new), flags=DECODE_EARLY_PAGES if early_pages else 0)
+                   stream, append=(k_new, v_new), flags=_flags(early_pages, zeroed_workspace))
 
 
 DECODE_EARLY_PAGES = 1
+DECODE_ZEROED_WORKSPACE = 2
+
+
+def _flags(early_pages: bool, zeroed_workspace: bool) -> int:
+    return (DECODE_EARLY_PAGES if early_pages else 0) | (DECODE_ZEROED_WORKSPACE if zeroed_workspace else 0)
 
 
 def _decode(q, k_cache, v_cache, block_tables, context_lens, scale, window, out, workspace, max_context_len,

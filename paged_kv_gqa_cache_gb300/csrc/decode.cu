@@ -394,6 +394,89 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
   }
 }
 
+// Warp of the launch whose page range contains global page x, when W warps
+// (W <= P) split P pages as [floor(w P / W), floor((w + 1) P / W)).
+__device__ __forceinline__ int worker_of(int64_t x, int64_t P, int64_t W) {
+  const int64_t w = ((x + 1) * W + P - 1) / P - 1;
+  return (int)(w < W - 1 ? w : W - 1);
+}
+
+// Log-sum-exp merge of the nf fragments (slots item + wf .. item + wf + nf - 1)
+// of query head gg of item (s, h) into its output row; one warp, lane owns
+// dims [4 * lane, 4 * lane + 4).  The (m, l) of up to 32 fragments are read at
+// once (one per lane); the o partials are then streamed CHUNK at a time with
+// independent loads (the combine kernel takes 32; the split kernel, merging
+// in place with its query rows still in registers, takes 8).  The partials
+// are read from L2 (ld.global.cg): in the fused path they were written by
+// other SMs during this kernel.
+template <typename T, int G, int CHUNK>
+__device__ __forceinline__ void merge_fragments(const DecodeParams &p, int s, int h, int gg, int wf, int nf, int lane) {
+  static_assert(32 % CHUNK == 0, "chunks tile a group of 32 fragments");
+  const int64_t slot0 = (int64_t)s * p.num_kv_heads + h + wf;
+  float M = -INFINITY, L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < nf; base += 32) {
+    const int f = base + lane;
+    float mf = -INFINITY, lf = 0.f;
+    if (f < nf) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + ((slot0 + f) * G + gg) * 2));
+      mf = ml.x;
+      lf = ml.y;
+    }
+    float mc = mf;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(FULL, mc, off));
+    const float Mn = fmaxf(M, mc);
+    if (Mn == -INFINITY) continue;  // no valid fragment yet (uniform)
+    const float so = exp2f(M - Mn);
+    const float wgt = (mf > -INFINITY) ? exp2f(mf - Mn) : 0.f;
+    float lw = lf * wgt;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(FULL, lw, off);
+    L = L * so + lw;
+    O.x *= so; O.y *= so; O.z *= so; O.w *= so;
+    M = Mn;
+    const int cnt = min(32, nf - base);
+#pragma unroll 1
+    for (int c0 = 0; c0 < cnt; c0 += CHUNK) {
+      // issue every load of this chunk before using any of them
+      float4 ov[CHUNK];
+#pragma unroll
+      for (int j = 0; j < CHUNK; ++j)
+        if (c0 + j < cnt)
+          ov[j] = __ldcg(
+              reinterpret_cast<const float4 *>(p.ws_o + ((slot0 + base + c0 + j) * G + gg) * kHeadDim + 4 * lane));
+#pragma unroll
+      for (int j = 0; j < CHUNK; ++j) {
+        const float wj = __shfl_sync(FULL, wgt, c0 + j);
+        if (c0 + j < cnt && wj > 0.f) {
+          O.x = fmaf(wj, ov[j].x, O.x);
+          O.y = fmaf(wj, ov[j].y, O.y);
+          O.z = fmaf(wj, ov[j].z, O.z);
+          O.w = fmaf(wj, ov[j].w, O.w);
+        }
+      }
+    }
+  }
+  const float inv = 1.f / L;
+  T *op = reinterpret_cast<T *>(p.out) + ((int64_t)s * p.num_q_heads + h * G + gg) * kHeadDim + 4 * lane;
+  uint2 pk;
+  pk.x = Pack<T>::from_f2(O.x * inv, O.y * inv);
+  pk.y = Pack<T>::from_f2(O.z * inv, O.w * inv);
+  *reinterpret_cast<uint2 *>(op) = pk;
+}
+
+// The fused combine's merge of one item, by the fragment that arrived last;
+// then the item's counter goes back to zero.
+template <typename T, int G>
+__device__ __forceinline__ void merge_item_fused(const DecodeParams &p, int s, int h, int item, int wf, int nf,
+                                              int lane) {
+  __threadfence();  // acquire: the other fragments' partials, published before their arrivals
+#pragma unroll 1
+  for (int gg = 0; gg < G; ++gg) merge_fragments<T, G, 4>(p, s, h, gg, wf, nf, lane);
+  if (lane == 0) p.counters[item] = 0;
+}
+
 // int8 pools: more CTAs per SM (the int16 query leaves room) to hide the
 // latency of the heavier per-byte arithmetic; 16-bit pools: as many as fit.
 template <typename T, int G, bool Q8, bool F8>
@@ -423,10 +506,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
     fence_mbar_init();
   }
-  griddep_wait();
+  // The lengths and block tables are never written by the kernels this one
+  // may overlap (see griddep_wait); with early_pages they are read, and the
+  // first pages fetched, before the wait.
+  if (!p.early_pages) griddep_wait();
   scan_pages(p, prefix, warp_tot);
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i <= p.num_seqs; i += NW * 32) p.meta[i] = prefix[i];
 
   const int n = p.num_seqs, hkv = p.num_kv_heads;
   // With fewer pages than warps only the first P warps work, one page each,
@@ -435,6 +519,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int64_t W = P < p.num_workers ? P : p.num_workers;
   const int w = blockIdx.x * NW + warp;
   if (w >= W) {
+    if (p.early_pages) griddep_wait();
+    if (blockIdx.x == 0 && warp == 0)  // only when no warp has pages (W = 0)
+      for (int i = lane; i <= p.num_seqs; i += 32) p.meta[i] = prefix[i];
     griddep_launch_dependents();
     return;
   }
@@ -454,33 +541,62 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   int win_s = -1, win_base = -1, win_first = 0;
   int32_t win = -1;
   uint32_t bad_mask = 0;
-  auto issue = [&](int st) {
-    const int base = ic.page & ~31;
-    if (ic.s != win_s || base != win_base) {
-      if (ic.s != win_s) win_first = p.window > 0 ? window_lo(__ldg(p.context_lens + ic.s), p.window) / kBlock : 0;
-      win_s = ic.s;
+  auto issue_at = [&](int st, const Cursor &at) {
+    const int base = at.page & ~31;
+    if (at.s != win_s || base != win_base) {
+      if (at.s != win_s) win_first = p.window > 0 ? window_lo(__ldg(p.context_lens + at.s), p.window) / kBlock : 0;
+      win_s = at.s;
       win_base = base;
       const int pg = base + lane;
-      win = (pg < ic.pages)
-                ? __ldg(p.block_tables + (int64_t)ic.s * p.max_blocks_per_seq + win_first + pg)
+      win = (pg < at.pages)
+                ? __ldg(p.block_tables + (int64_t)at.s * p.max_blocks_per_seq + win_first + pg)
                 : -1;
     }
-    const int blk = __shfl_sync(FULL, win, ic.page & 31);
+    const int blk = __shfl_sync(FULL, win, at.page & 31);
     const bool ok = (unsigned)blk < (unsigned)p.num_blocks;
     if (lane == 0) {
       if (ok) {
-        load_page<Q8>(stages + st * SST, &kmap, &vmap, &bars[st], p, ic.h, blk);
+        load_page<Q8>(stages + st * SST, &kmap, &vmap, &bars[st], p, at.h, blk);
       } else {
-        set_error(p.err, PA_ERR_RANGE, ic.s);
+        set_error(p.err, PA_ERR_RANGE, at.s);
         mbar_arrive(&bars[st]);
       }
     }
     bad_mask = ok ? (bad_mask & ~(1u << st)) : (bad_mask | (1u << st));
+  };
+  auto issue = [&](int st) {
+    issue_at(st, ic);
     advance(ic, prefix, n, hkv);
   };
 
   const int npre = (int)(npages < kStages ? npages : kStages);
-  for (int g = 0; g < npre; ++g) issue(g);
+  if (p.early_pages) {
+    // The caller guarantees that the kernels still running write no page but
+    // each sequence's last visible one: fetch the others now, the last pages
+    // after the wait.
+    Cursor deferred[kStages];
+    uint32_t dmask = 0;
+#pragma unroll
+    for (int g = 0; g < kStages; ++g) {
+      if (g < npre) {
+        if (ic.page == ic.pages - 1) {
+          deferred[g] = ic;
+          dmask |= 1u << g;
+          advance(ic, prefix, n, hkv);
+        } else {
+          issue(g);
+        }
+      }
+    }
+    griddep_wait();
+#pragma unroll
+    for (int g = 0; g < kStages; ++g)
+      if ((dmask >> g) & 1u) issue_at(g, deferred[g]);
+  } else {
+    for (int g = 0; g < npre; ++g) issue(g);
+  }
+  if (blockIdx.x == 0 && warp == 0)  // the combine kernel's copy of the page prefix (after the wait: the
+    for (int i = lane; i <= p.num_seqs; i += 32) p.meta[i] = prefix[i];  // previous call may still read it)
 
   // ---- consumer state ---------------------------------------------------------
   // Packed fp32x2 arithmetic (FFMA2): q and the partial scores pair adjacent
@@ -564,6 +680,20 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           if (lane == 0) *reinterpret_cast<float2 *>(p.ws_ml + slot * 2) = make_float2(m[gg], lt);
         }
       }
+      if (!final_out && p.counters) {
+        // Fused combine: publish this fragment (stores, then a device-scope
+        // fence, then the arrival); the fragment that arrives last merges all
+        // of the item's fragments and sets the counter back to zero, so the
+        // counters are zero again when the kernel ends.
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(p.counters + item, 1);
+        prev = __shfl_sync(FULL, prev, 0);
+        const int64_t A = (int64_t)hkv * prefix[cc.s] + (int64_t)cc.h * cc.pages;
+        const int wf = worker_of(A, P, W), wl = worker_of(A + cc.pages - 1, P, W);
+        if (prev == wl - wf) merge_item_fused<T, G>(p, cc.s, cc.h, item, wf, wl - wf + 1, lane);
+      }
       open = false;
     }
     advance(cc, prefix, n, hkv);
@@ -571,17 +701,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   griddep_launch_dependents();
 }
 
-// Warp of the launch whose page range contains global page x, when W warps
-// (W <= P) split P pages as [floor(w P / W), floor((w + 1) P / W)).
-__device__ __forceinline__ int worker_of(int64_t x, int64_t P, int64_t W) {
-  const int64_t w = ((x + 1) * W + P - 1) / P - 1;
-  return (int)(w < W - 1 ? w : W - 1);
-}
 
 // Log-sum-exp merge of the fragments of every item a single warp did not finish.
-// One warp per (sequence, query head); lane owns dims [4 * lane, 4 * lane + 4).
-// The (m, l) of up to 32 fragments are read at once (one per lane); the o
-// partials are then streamed with independent loads.
+// One warp per (sequence, query head).
 template <typename T, int G>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
   griddep_wait();
@@ -596,57 +718,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     const int64_t A = (int64_t)hkv * p.meta[s] + (int64_t)h * pages;
     const int wf = pages ? worker_of(A, P, W) : 0;
     const int wl = pages ? worker_of(A + pages - 1, P, W) : 0;
-    if (pages != 0 && wf != wl) {  // otherwise the split kernel wrote this output directly
-      const int64_t slot0 = (int64_t)s * hkv + h + wf;
-      const int nf = wl - wf + 1;
-      float M = -INFINITY, L = 0.f;
-      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int base = 0; base < nf; base += 32) {
-        const int f = base + lane;
-        float mf = -INFINITY, lf = 0.f;
-        if (f < nf) {
-          const float2 ml = *reinterpret_cast<const float2 *>(p.ws_ml + ((slot0 + f) * G + gg) * 2);
-          mf = ml.x;
-          lf = ml.y;
-        }
-        float mc = mf;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(FULL, mc, off));
-        const float Mn = fmaxf(M, mc);
-        if (Mn == -INFINITY) continue;  // no valid fragment yet (uniform)
-        const float so = exp2f(M - Mn);
-        const float wgt = (mf > -INFINITY) ? exp2f(mf - Mn) : 0.f;
-        float lw = lf * wgt;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(FULL, lw, off);
-        L = L * so + lw;
-        O.x *= so; O.y *= so; O.z *= so; O.w *= so;
-        M = Mn;
-        const int cnt = min(32, nf - base);
-        // issue every load of this chunk before using any of them
-        float4 ov[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < cnt)
-            ov[j] = *reinterpret_cast<const float4 *>(p.ws_o + ((slot0 + base + j) * G + gg) * kHeadDim + 4 * lane);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float wj = __shfl_sync(FULL, wgt, j);
-          if (j < cnt && wj > 0.f) {
-            O.x = fmaf(wj, ov[j].x, O.x);
-            O.y = fmaf(wj, ov[j].y, O.y);
-            O.z = fmaf(wj, ov[j].z, O.z);
-            O.w = fmaf(wj, ov[j].w, O.w);
-          }
-        }
-      }
-      const float inv = 1.f / L;
-      T *op = reinterpret_cast<T *>(p.out) + ((int64_t)s * p.num_q_heads + qh) * kHeadDim + 4 * lane;
-      uint2 pk;
-      pk.x = Pack<T>::from_f2(O.x * inv, O.y * inv);
-      pk.y = Pack<T>::from_f2(O.z * inv, O.w * inv);
-      *reinterpret_cast<uint2 *>(op) = pk;
-    }
+    if (pages != 0 && wf != wl)  // otherwise the split kernel wrote this output directly
+      merge_fragments<T, G, 32>(p, s, h, gg, wf, wl - wf + 1, lane);
   }
   griddep_launch_dependents();
 }
@@ -922,7 +995,7 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
                          int max_workers, int max_pages_per_item, cudaStream_t stream) {
   DecodeParams p = p0;
   const int items = p.num_seqs * p.num_kv_heads;
-  const int ctas = decode_item_ctas(items, max_pages_per_item);
+  const int ctas = p.counters ? 0 : decode_item_ctas(items, max_pages_per_item);
   if (ctas > 0) {
     const int ismem = item_smem_bytes(G);
     static KernelSetup item_setup;
@@ -947,19 +1020,26 @@ cudaError_t launch_typed(const DecodeParams &p0, const CUtensorMap &kmap, const 
   p.num_workers = grid * NW;
   e = launch_pdl(decode_split_kernel<T, G, Q8, F8>, dim3(grid), dim3(NW * 32), smem, stream, kmap, vmap, p);
   if (e != cudaSuccess) return e;
+  if (p.counters) return cudaSuccess;  // the split kernel merged the split items itself
   const int cgrid = (p.num_seqs * p.num_q_heads + 3) / 4;
   return launch_pdl(decode_combine_kernel<T, G>, dim3(cgrid), dim3(128), 0, stream, p);
 }
 
 }  // namespace
 
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads) {
+size_t decode_workspace_counters_offset(int num_seqs, int num_q_heads, int num_kv_heads) {
   const int group = num_q_heads / num_kv_heads;
   const size_t slots = (size_t)num_seqs * num_kv_heads + kDecodeMaxWorkers;
   const size_t meta = (((size_t)num_seqs + 1) * 4 + 255) & ~(size_t)255;
   const size_t ml = (slots * group * 2 * 4 + 255) & ~(size_t)255;
   const size_t o = slots * group * kHeadDim * 4;
   return meta + ml + o;
+}
+
+// page prefix, (m, l) and o partials, then one counter per (sequence, KV head) item
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads) {
+  const size_t counters = ((size_t)num_seqs * num_kv_heads * 4 + 255) & ~(size_t)255;
+  return decode_workspace_counters_offset(num_seqs, num_q_heads, num_kv_heads) + counters;
 }
 
 bool decode_workspace_carve(void *ws, size_t bytes, int num_seqs, int num_q_heads, int num_kv_heads,

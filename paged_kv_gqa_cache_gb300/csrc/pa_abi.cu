@@ -250,6 +250,11 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
   p.num_blocks = num_blocks;
   p.window = window;
   p.early_pages = (flags & PA_DECODE_EARLY_PAGES) ? 1 : 0;
+  // a workspace whose counters the caller keeps zero: one launch over all SMs, split items merged in it
+  p.counters = (flags & PA_DECODE_ZEROED_WORKSPACE)
+                   ? reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) +
+                                                 decode_workspace_counters_offset(num_seqs, num_q_heads, num_kv_heads))
+                   : nullptr;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   // Upper bound on the pages of one item (a window of W keys spans at most
@@ -257,7 +262,9 @@ pa_status decode_call(const void *q, int dtype, const pa_kv_pool *pool16, const 
   int item_pages = (max_context_len + kBlock - 1) / kBlock;
   if (window > 0 && (window - 1) / kBlock + 2 < item_pages) item_pages = (window - 1) / kBlock + 2;
   const int64_t pages_hint = (int64_t)num_seqs * num_kv_heads * item_pages;
-  int64_t workers = (pages_hint + 3) / 4;
+  // one launch with the merge inside: as many warps as fit (every page in flight early); else aim for
+  // at least 4 pages per warp
+  int64_t workers = p.counters ? (pages_hint + 1) / 2 : (pages_hint + 3) / 4;
   if (workers > kDecodeMaxWorkers) workers = kDecodeMaxWorkers;
   cudaError_t e = launch_decode(p, kmap, vmap, dtype, group, (int)workers, item_pages, q8, q8 && f8, stream);
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
@@ -403,7 +410,7 @@ pa_status pa_paged_attn_decode_ex(const void *q, const pa_kv_pool *pool, const i
   if (st != PA_OK) return st;
   if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_NULL;
   if (k_new && window != 0) return PA_ERR_UNSUPPORTED;
-  if (flags & ~(uint32_t)PA_DECODE_EARLY_PAGES) return PA_ERR_UNSUPPORTED;
+  if (flags & ~(uint32_t)(PA_DECODE_EARLY_PAGES | PA_DECODE_ZEROED_WORKSPACE)) return PA_ERR_UNSUPPORTED;
   return decode_call(q, pool->dtype, pool, nullptr, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                      num_q_heads, max_context_len, scale, window, out, workspace, workspace_bytes,
                      static_cast<cudaStream_t>(stream), k_new, v_new, false, flags);
@@ -489,7 +496,7 @@ pa_status pa_paged_attn_decode_q8_ex(const void *q, int32_t dtype, const pa_kv_p
                                      int32_t max_context_len, float scale, uint32_t flags, void *out,
                                      void *workspace, size_t workspace_bytes, pa_stream_t stream) {
   if (codes != PA_CODES_INT8 && codes != PA_CODES_E4M3) return PA_ERR_UNSUPPORTED;
-  if (flags & ~(uint32_t)PA_DECODE_EARLY_PAGES) return PA_ERR_UNSUPPORTED;
+  if (flags & ~(uint32_t)(PA_DECODE_EARLY_PAGES | PA_DECODE_ZEROED_WORKSPACE)) return PA_ERR_UNSUPPORTED;
   return decode_8bit(q, dtype, pool, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
                      max_context_len, scale, out, workspace, workspace_bytes, codes == PA_CODES_E4M3, stream,
                      flags);

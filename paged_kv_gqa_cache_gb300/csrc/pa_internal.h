@@ -119,6 +119,9 @@ struct DecodeParams {
   int32_t window;            // sliding window in keys (0: none)
   int32_t early_pages;       // 1: pages before each sequence's last one are not written by the previous
                              //    kernel, so the one-launch decode fetches them before its dependency wait
+  int32_t *counters;         // workspace: arrivals per (sequence, KV head) item; non-null only when the
+                             //    caller keeps them zero between calls: the split kernel then merges each
+                             //    split item itself (the last fragment to arrive), with no combine launch
   float scale_log2;          // scale * log2(e)
 };
 
@@ -132,10 +135,14 @@ struct DecodeLaunch {
 // max_pages_per_item bounds each item's pages (from the host-side max length);
 // q8: the pool holds 8-bit codes with per-token scales (p.k_scale, p.v_scale):
 // int8 integers, or E4M3 numbers when f8.
+// With p.counters set, the split kernel runs alone (whatever the item count)
+// and merges split items itself.
 cudaError_t launch_decode(const DecodeParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
                           int dtype, int group, int max_workers, int max_pages_per_item, bool q8, bool f8,
                           cudaStream_t stream);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads);
+// Offset and size of the item counters inside the workspace.
+size_t decode_workspace_counters_offset(int num_seqs, int num_q_heads, int num_kv_heads);
 // CTAs per item of the one-launch decode (1 or 2), or 0 when the split path runs.
 int decode_item_ctas(int items, int max_pages_per_item);
 // Carves the workspace into meta / ml / o; returns false if it is too small.

@@ -334,61 +334,66 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
+    // The whole warp runs this loop (waits, barrier phases, descriptors), and
+    // one elected lane issues each batch of MMAs and its commit: from a
+    // warp-uniform loop the MMAs issue at the tensor core's own rate (32.7 ns
+    // each at M = N = 128, K = 16) even while the softmax warps on the same
+    // sub-partition are busy, where a loop run by one lane alone measured
+    // 46-49 ns per MMA.
     // Descriptors are built once; a k-step or a ring stage only moves the start
     // address field (bits 0..13, address >> 4), so each MMA costs a 64-bit add.
     // Shared-memory offsets stay below 256 KB, so the field never carries over.
-    // The tensor core queues only a few MMAs, so any latency in this thread
-    // between two batches leaves it idle: the P barrier of the next P V batch
-    // is probed without blocking two MMAs before the end of the QK^T batch,
-    // when the answer is back by the time it is needed; only a P that really
-    // is not ready yet costs a (bounded) blocking wait.  (The K barrier is not
-    // probed: a probe of a barrier that TMA is still updating costs more than
-    // the wait it saves.)
-    if (lane == 0) {
-      if (!mbar_wait(&bars.q_full, 0)) timed_out = true;
-      const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
-      const uint64_t kdesc0 = tc::desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
-      const uint64_t vdesc0 = tc::desc_sw128(smem_u32(smem + OFF_V), kHalf, 1024);
-      constexpr uint64_t kStageStep = (2 * kHalf) >> 4;   // one ring stage
-      constexpr uint64_t kHalfStep = kHalf >> 4;          // the other 64-dim half
-      bool pv_ok = false;                                  // P (and so V) of the next P V batch is ready
-      for (int kt = 0; kt <= ntl && !timed_out; ++kt) {   // kt: tile index from kt0
-        const int j = kt - 1, sj = j & 1;                  // the tile whose P V is issued in this iteration
-        const int jv = j % kVStages;
-        if (kt < ntl) {
-          const int b = kt % kKStages, sb = kt & 1;
-          if (!mbar_wait(&bars.k_full[b], (kt / kKStages) & 1)) {
-            timed_out = true;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint64_t kdesc = kdesc0 + (uint64_t)b * kStageStep;
-          const uint32_t s_col = tmem + sb * 128;
+    // The tensor core queues only a few MMAs, so any latency between two
+    // batches leaves it idle: the P barrier of the next P V batch is probed
+    // without blocking right after the QK^T batch is issued; only a P that
+    // really is not ready yet costs a (bounded) blocking wait.
+    const bool leader = elect_one();
+    auto wait_all = [&](uint64_t *bar, uint32_t parity) {  // warp-uniform result
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
+    };
+    if (!wait_all(&bars.q_full, 0)) timed_out = true;
+    const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
+    const uint64_t kdesc0 = tc::desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
+    const uint64_t vdesc0 = tc::desc_sw128(smem_u32(smem + OFF_V), kHalf, 1024);
+    constexpr uint64_t kStageStep = (2 * kHalf) >> 4;   // one ring stage
+    constexpr uint64_t kHalfStep = kHalf >> 4;          // the other 64-dim half
+    bool pv_ok = false;                                  // P (and so V) of the next P V batch is ready
+    for (int kt = 0; kt <= ntl && !timed_out; ++kt) {   // kt: tile index from kt0
+      const int j = kt - 1, sj = j & 1;                  // the tile whose P V is issued in this iteration
+      const int jv = j % kVStages;
+      if (kt < ntl) {
+        const int b = kt % kKStages, sb = kt & 1;
+        if (!wait_all(&bars.k_full[b], (kt / kKStages) & 1)) {
+          timed_out = true;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint64_t kdesc = kdesc0 + (uint64_t)b * kStageStep;
+        const uint32_t s_col = tmem + sb * 128;
+        if (leader) {
           tc::mma_f16(s_col, qdesc, kdesc, IDESC_S, 0u);
 #pragma unroll
-          for (int kk = 1; kk < 6; ++kk) {
+          for (int kk = 1; kk < 8; ++kk) {
             const uint64_t off = (uint64_t)((kk >> 2) * kHalfStep + (kk & 3) * 2);   // 16-element k-step
             tc::mma_f16(s_col, qdesc + off, kdesc + off, IDESC_S, 1u);
           }
-          if (kt >= 1) pv_ok = mbar_test_wait(&bars.p_full[jv], (j / kVStages) & 1);
-#pragma unroll
-          for (int kk = 6; kk < 8; ++kk) {
-            const uint64_t off = (uint64_t)((kk >> 2) * kHalfStep + (kk & 3) * 2);
-            tc::mma_f16(s_col, qdesc + off, kdesc + off, IDESC_S, 1u);
-          }
           tc::commit(&bars.s_full[b]);
-        } else {
-          pv_ok = false;
         }
-        if (kt >= 1) {  // O_half += P V of the previous tile: keys 0..63 into O_0, 64..127 into O_1
-          if (!pv_ok && !mbar_wait(&bars.p_full[jv], (j / kVStages) & 1)) {
-            timed_out = true;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint64_t vdesc = vdesc0 + (uint64_t)jv * kStageStep;
-          const uint32_t p_col = tmem + sj * 128;
-          const uint32_t first = j > 0 ? 1u : 0u;
+        __syncwarp();
+        pv_ok = kt >= 1 && __all_sync(0xffffffffu, mbar_test_wait(&bars.p_full[jv], (j / kVStages) & 1));
+      } else {
+        pv_ok = false;
+      }
+      if (kt >= 1) {  // O_half += P V of the previous tile: keys 0..63 into O_0, 64..127 into O_1
+        if (!pv_ok && !wait_all(&bars.p_full[jv], (j / kVStages) & 1)) {
+          timed_out = true;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint64_t vdesc = vdesc0 + (uint64_t)jv * kStageStep;
+        const uint32_t p_col = tmem + sj * 128;
+        const uint32_t first = j > 0 ? 1u : 0u;
+        if (leader) {
           if (j < lo_tiles) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {  // 16-key step: V rows 16 kk .. 16 kk + 15, into O of key half kk / 4
@@ -409,14 +414,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
           tc::commit(&bars.pv_done[jv]);
         }
+        __syncwarp();
       }
-      if (timed_out) {
-        // The MMAs already issued may still be writing TMEM (and reading
-        // shared memory): one more commit tracks all of them; wait for it,
-        // bounded, before the CTA frees its TMEM and ends.
-        tc::commit(&bars.drain);
-        mbar_wait(&bars.drain, 0, kWaitLimitNs / 8);
-      }
+    }
+    if (timed_out) {
+      // The MMAs already issued may still be writing TMEM (and reading
+      // shared memory): one more commit tracks all of them; wait for it,
+      // bounded, before the CTA frees its TMEM and ends.
+      if (leader) tc::commit(&bars.drain);
+      __syncwarp();
+      mbar_wait(&bars.drain, 0, kWaitLimitNs / 8);
     }
   } else {
     // ---------------- softmax + epilogue (warps 0..7) ----------------

@@ -36,6 +36,7 @@ def test_binding_constants_match_the_header():
     text = open(HEADER).read()
     defines = dict(re.findall(r"#define (PA_[A-Z0-9_]+) (\d+)u?\b", text))
     assert int(defines["PA_DECODE_EARLY_PAGES"]) == pa.DECODE_EARLY_PAGES
+    assert int(defines["PA_DECODE_ZEROED_WORKSPACE"]) == pa.DECODE_ZEROED_WORKSPACE
     assert int(defines["PA_HEAD_DIM"]) == 128 and int(defines["PA_BLOCK_SIZE"]) == 16
     codes = dict((name, int(v)) for name, v in re.findall(r"(PA_(?:OK|ERR_[A-Z_]+)) = (-?\d+)", text))
     assert codes == pa.STATUS_CODE
@@ -193,7 +194,7 @@ def test_decode_ex_checks_its_arguments(lib):
         kw.get("flags", 1), kw.get("out", P), P, ws, None)
     assert call(kn=P) == -1 and call(vn=P) == -1   # k_new and v_new go together
     assert call(kn=P, vn=P, window=64) == -4       # the fused write takes no window
-    assert call(flags=2) == -4 and call(flags=0x80000001) == -4
+    assert call(flags=4) == -4 and call(flags=0x80000001) == -4   # bits beyond the two flags
     assert call(window=-1) == -2
     assert call(out=P + 2) == -9                   # the plain call's checks still apply, before any CUDA call
     assert call(kn=P + 8, vn=P, out=P) == -9

@@ -44,9 +44,10 @@ def _check_decode_step(step, layers_to_check):
         check_close(step.out[i], ref, f"{step.desc[:40]}, pool {i}")
 
 
+@pytest.mark.parametrize("fused", [True, False])   # the bench's default: one launch over all SMs
 @pytest.mark.parametrize("early", [True, False])   # the bench's default passes PA_DECODE_EARLY_PAGES
-def test_qwen3_0_6b_decode_step_as_benchmarked(early):
-    step = bench.DecodeStep(DEV, workload=2, early_pages=early)     # 28 layers, 28 distinct pools
+def test_qwen3_0_6b_decode_step_as_benchmarked(early, fused):
+    step = bench.DecodeStep(DEV, workload=2, early_pages=early, fused=fused)     # 28 layers, 28 distinct pools
     _check_decode_step(step, range(step.case.n_layers))
 
 
@@ -56,18 +57,19 @@ def test_qwen3_0_6b_decode_step_with_the_fused_append(early):
     _check_decode_step(step, range(step.case.n_layers))
 
 
-def test_qwen3_8b_decode_as_benchmarked():
-    step = bench.DecodeStep(DEV, workload=4, pools=4, early_pages=True)  # 36 layers cycling 4 pools of 1 GiB
+@pytest.mark.parametrize("fused", [True, False])
+def test_qwen3_8b_decode_as_benchmarked(fused):
+    step = bench.DecodeStep(DEV, workload=4, pools=4, early_pages=True, fused=fused)  # 36 layers, 4 pools of 1 GiB
     _check_decode_step(step, range(step.case.n_layers))
 
 
 def test_prefix_shared_tail_as_benchmarked():
-    step = bench.DecodeStep(DEV, workload=5, early_pages=True)      # 8 calls cycling 4 pools
+    step = bench.DecodeStep(DEV, workload=5, early_pages=True, fused=True)      # 8 calls cycling 4 pools
     _check_decode_step(step, range(step.case.n_layers))
 
 
 def test_mixed_step_as_benchmarked():
-    step = bench.MixedStep(DEV, overlap=True)         # 28 layers, 2 pools, prefill beside decode
+    step = bench.MixedStep(DEV, overlap=True, fused=True)   # 28 layers, 2 pools, prefill beside decode
     c = step.case
     before = [(bits(c.k_cache[i]), bits(c.v_cache[i])) for i in range(2)]
     _replay(step.run)
@@ -87,7 +89,7 @@ def test_mixed_step_as_benchmarked():
 def test_end_to_end_path_returns_the_right_outputs_to_the_host(append):
     # the e2e leg: inputs copied from pinned host memory each step, the library
     # calls reading the copies (metadata included), outputs copied back
-    step = bench.DecodeStep(DEV, workload=2, append=append, early_pages=True)
+    step = bench.DecodeStep(DEV, workload=2, append=append, early_pages=True, fused=True)
     c = step.case
     before = [(bits(c.k_cache[i]), bits(c.v_cache[i])) for i in range(c.n_layers)]
     stream = torch.cuda.Stream(device=DEV)
@@ -103,7 +105,7 @@ def test_end_to_end_path_returns_the_right_outputs_to_the_host(append):
 def test_mixed_step_end_to_end_path_returns_the_right_outputs_to_the_host():
     # the mixed step's e2e leg: every layer's inputs and the step's metadata
     # copied from pinned host memory, both outputs of every layer copied back
-    step = bench.MixedStep(DEV, overlap=True)
+    step = bench.MixedStep(DEV, overlap=True, fused=True)
     c = step.case
     before = [(bits(c.k_cache[i]), bits(c.v_cache[i])) for i in range(2)]
     stream = torch.cuda.Stream(device=DEV)

@@ -97,7 +97,7 @@ def test_early_pages_with_the_fused_append():
     _check(case, out, kc, vc, case.name)
 
 
-def test_early_pages_is_ignored_on_the_split_path():
+def test_early_pages_on_the_split_path():
     lens = [4096] * 40
     case = workloads.build_case("early-split", "bf16", 32, 8, seed=33, device=DEV, decode_lens=lens)
     assert pa.decode_kernel_launches(len(lens), 8, case.max_context_len) == 2
