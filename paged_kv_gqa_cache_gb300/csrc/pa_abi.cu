@@ -170,6 +170,21 @@ bool pool_map(CUtensorMap *map, const pa_kv_pool *pool, void *base, bool whole_p
                            whole_page_box ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The pool's V for the prefill: one box per page of one KV head with both
+// 64-dim halves, as the 5-D tensor {64 dims, 16 slots, 2 halves, kv head,
+// block} (strides: slot Hkv * 256 B, half 128 B, head 256 B, block 16 * Hkv *
+// 256 B).  The box {64, 16, 2, 1, 1} lands in shared memory as the 16 rows of
+// dims 0..63 (2 KB) followed by the 16 rows of dims 64..127, 128-byte
+// swizzled: the MN-major layout the P V product reads with the two halves
+// 2 KB apart.  A key tile then takes 8 boxes of 4 KB instead of 16 of 2 KB.
+bool pool_map_vpages(CUtensorMap *map, const pa_kv_pool *pool, void *base) {
+  const uint64_t hkv = (uint64_t)pool->num_kv_heads;
+  const uint64_t dims[5] = {64, (uint64_t)kBlock, 2, hkv, (uint64_t)pool->num_blocks};
+  const uint64_t strides[4] = {hkv * kHeadDim * 2ull, 128ull, kHeadDim * 2ull, kBlock * hkv * kHeadDim * 2ull};
+  const uint32_t box[5] = {64u, (uint32_t)kBlock, 2u, 1u, 1u};
+  return encode_tensor_map(map, map_dtype(pool->dtype), 5, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // int8 pool [P2 section 5]: codes as a 4-D tensor of bytes {dim, kv head,
 // slot, block}; the decode takes one page of one KV head per box (2 KB).
 pa_status check_pool_q8(const pa_kv_pool_q8 *pool) {
@@ -554,7 +569,7 @@ pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t *chunk
   p.scale_log2 = scale * 1.4426950408889634f;
 
   CUtensorMap kmap, vmap, qmap;
-  if (!pool_map(&kmap, pool, pool->k_cache, false) || !pool_map(&vmap, pool, pool->v_cache, false))
+  if (!pool_map(&kmap, pool, pool->k_cache, false) || !pool_map_vpages(&vmap, pool, pool->v_cache))
     return PA_ERR_CUDA;
   // q as a 3-D tensor {dim, query head, token}; boxes of {64 dims, G heads,
   // 128/G tokens} give 128 rows (token-major, head-minor) of 128 bytes.

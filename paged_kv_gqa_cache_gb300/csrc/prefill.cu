@@ -17,13 +17,14 @@
 // consecutive tokens of the chunk x the G query heads sharing that KV head,
 // so every K/V tile it reads serves all G heads.  Row r of the tile is token
 // t0 + r / G, head h * G + r % G (the Q tile is one TMA box per 64-dim half).
-// Keys stream in tiles of N = 128 (8 pages, two 2 KB TMA boxes per page: the
-// 64-dim halves of 16 keys, 128-byte swizzled): K through a 3-stage ring
-// released as soon as S is computed, V through a 3-stage ring released after
-// the PV product.  Three loader warps fill both rings, each issuing a third
-// of every tile's boxes from parallel lanes: the TMA engine serves each
-// issuing warp at a fixed cost per box, so the warps, not the ring depth, set
-// the ingest rate.  Per key tile kt:
+// Keys stream in tiles of N = 128 (8 pages; K as two 2 KB TMA boxes per page,
+// the 64-dim halves of 16 keys, gathered half by half; V as one 4 KB box per
+// page with its two halves 2 KB apart; 128-byte swizzled): K through a
+// 3-stage ring released as soon as S is computed, V through a 3-stage ring
+// released after the PV product.  Three loader warps fill both rings, each
+// issuing a third of every tile's 24 boxes from parallel lanes: the TMA engine
+// serves each issuing warp at a fixed cost per box, so the box count and the
+// warps, not the ring depth, set the ingest rate.  Per key tile kt:
 //   S = Q K^T     tcgen05.mma kind::f16, A and B from shared memory (K-major),
 //                 fp32 into TMEM columns S[kt % 2].
 //   softmax       8 warps; the two warps on TMEM lane quarter q own rows
@@ -63,10 +64,23 @@ namespace {
 
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kLoadWarps = 3;  // each issues a third of the boxes of every K and V tile
+constexpr int kLoadWarps = 7;  // each issues a seventh of the 24 boxes of every K and V tile
 constexpr int kWarpLoad0 = kSoftmaxWarps, kWarpMma = kSoftmaxWarps + kLoadWarps;
 constexpr int kThreads = (kSoftmaxWarps + kLoadWarps + 1) * 32;
+static_assert(kThreads == 512, "four warpgroups: two of softmax warps, two of loader and MMA warps");
+// Registers: 128 per thread at launch (65536 / 512).  Inside their roles the
+// softmax warpgroups take kRegsSoftmax and the loader / MMA warpgroups keep
+// kRegsOther (2 x 128 x (kRegsSoftmax + kRegsOther) <= 65536, what the launch
+// holds, so an increase never waits forever); every role gives its share back
+// to 128 before the common tail.
+constexpr int kRegsSoftmax = 200, kRegsOther = 56;
+static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther <= 65536, "register split fits the launch");
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 constexpr int kHalf = 16384;                        // 128 rows x 64 elements x 2 bytes
+constexpr int kVPage = 4096;                        // V: one page (16 rows x 128 dims x 2 bytes) per box
 constexpr int kKStages = 3, kVStages = 3;
 constexpr int OFF_Q = 0;                            // Q: two 64-dim halves
 constexpr int OFF_K = 2 * kHalf;                    // K stages: {lo, hi} halves
@@ -103,18 +117,19 @@ struct Bars {
   uint32_t tmem_base;
 };
 
-// Key tile kt of one pool is 16 boxes of 2 KB, box b being the 64-dim half
-// b % 2 of page b / 2, fetched into `dst` and completing on `bar` (which
-// expects one arrival per loader warp).  A TMA engine serves each issuing warp
-// at about one small box per 50 ns, so the boxes are spread over the loader
-// warps: this warp's lane i issues box b0 + kLoadWarps * i.  Pages past the
-// sequence are skipped; pages below pg0 (wholly before the sliding window)
-// are skipped too and, with `zero_below`, zeroed (value rows meet zero
-// probabilities and must stay finite); a page whose block id is out of range
-// is zeroed and reported.  sbt caches the block ids of pages pg0 ...
+// Key tile kt of the K pool is 16 boxes of 2 KB, box b being the 64-dim half
+// b % 2 of page b / 2 (the QK^T product reads each half of all 128 keys as one
+// K-major operand, so the halves of the 8 pages are gathered into two 16 KB
+// blocks), fetched into `dst` and completing on `bar` (which expects one
+// arrival per loader warp).  A TMA engine serves each issuing warp at about
+// one small box per 50 ns, so the boxes are spread over the loader warps: this
+// warp's lane i issues box b0 + kLoadWarps * i.  Pages past the sequence and
+// pages below pg0 (wholly before the sliding window) are skipped: their keys
+// are masked.  A page whose block id is out of range is zeroed and reported.
+// sbt caches the block ids of pages pg0 ...
 __device__ __forceinline__ void load_boxes(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int kt, int b0,
-                                           int h, int pg0, int npages, bool zero_below, const int32_t *sbt,
-                                           const int32_t *bt, const PrefillParams &p, int c, int lane) {
+                                           int h, int pg0, int npages, const int32_t *sbt, const int32_t *bt,
+                                           const PrefillParams &p, int c, int lane) {
   const int b = b0 + kLoadWarps * lane;
   const int page = b >> 1, half = b & 1;
   const int pg = kt * 8 + page;
@@ -124,9 +139,8 @@ __device__ __forceinline__ void load_boxes(uint8_t *dst, const CUtensorMap *map,
   const bool ok = in && (unsigned)id < (unsigned)p.num_blocks;
   const unsigned okmask = __ballot_sync(0xffffffffu, ok);
   uint8_t *box = dst + half * kHalf + page * 2048;
-  const bool zero = (in && !ok) || (zero_below && b < 16 && pg < pg0);
-  if (zero) {  // rare: keep the products finite
-    if (in && half == 0) set_error(p.err, PA_ERR_RANGE, c);  // the error word reports the chunk
+  if (in && !ok) {  // rare: keep the products finite
+    if (half == 0) set_error(p.err, PA_ERR_RANGE, c);  // the error word reports the chunk
     uint4 *z = reinterpret_cast<uint4 *>(box);
     for (int i = 0; i < 128; ++i) z[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
@@ -135,6 +149,36 @@ __device__ __forceinline__ void load_boxes(uint8_t *dst, const CUtensorMap *map,
   if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(okmask) * 2048u);
   __syncwarp();
   if (ok) tma_load_4d(box, map, bar, half * 64, h, 0, id);
+}
+
+// Key tile kt of the V pool is 8 boxes of 4 KB: page p (its 16 rows of dims
+// 0..63, then of dims 64..127, 128-byte swizzled) at dst + 4 KB p, completing
+// on `bar` (one arrival per loader warp).  This warp's lane i fetches page
+// p0 + kLoadWarps * i.  Pages past the sequence are skipped (the softmax warps
+// zero those rows); pages below pg0 (wholly before the sliding window) and
+// pages whose block id is out of range (reported) are zeroed: their rows meet
+// zero probabilities and must stay finite.
+__device__ __forceinline__ void load_vpages(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int kt, int p0,
+                                            int h, int pg0, int npages, const int32_t *sbt, const int32_t *bt,
+                                            const PrefillParams &p, int c, int lane) {
+  const int page = p0 + kLoadWarps * lane;
+  const int pg = kt * 8 + page;
+  const bool in = page < 8 && pg >= pg0 && pg < npages;
+  int id = -1;
+  if (in) id = pg - pg0 < kBtCache ? sbt[pg - pg0] : __ldg(bt + pg);
+  const bool ok = in && (unsigned)id < (unsigned)p.num_blocks;
+  const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+  uint8_t *box = dst + page * kVPage;
+  if ((in && !ok) || (page < 8 && pg < pg0)) {  // rare
+    if (in) set_error(p.err, PA_ERR_RANGE, c);  // the error word reports the chunk
+    uint4 *z = reinterpret_cast<uint4 *>(box);
+    for (int i = 0; i < kVPage / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  __syncwarp();  // the zeroed pages are written before the arrival below releases them
+  if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(okmask) * (uint32_t)kVPage);
+  __syncwarp();
+  if (ok) tma_load_5d(box, map, bar, 0, 0, 0, h, id);
 }
 
 // Each lane of a warp holds 64 contiguous output bytes of its own row (rows are
@@ -166,24 +210,39 @@ __device__ __forceinline__ void store_rows_coalesced(uint4 *stage, void *dst, bo
   }
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // P = 2^(S * scale_log2 - m) for this thread's 64 keys of one tile (two
 // 32-column chunks v[0], v[1]), unless `full` masked outside the row's visible
 // keys (key kb + i of the half is visible when 0 <= kb + i <= span), written over
 // the chunk's first 16 columns as pairs of the input dtype; with LO, the
-// rounding remainder goes into the next 16.  Returns the row sum of P.
-template <typename T, bool LO>
+// rounding remainder goes into the next 16.  With MAX (full tiles only) the
+// tile's maximum score is taken in the same pass and returned in *mx, so that
+// the common tile needs no separate pass over its scores before the
+// exponentials.  Returns the row sum of P.
+template <typename T, bool LO, bool MAX = false>
 __device__ __forceinline__ float exp_pack_store(const uint32_t (&v)[2][32], uint32_t s_addr, float sl2, float m_ref,
-                                                bool full, int kb, int span) {
+                                                bool full, int kb, int span, float *mx = nullptr) {
   const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_ref, -m_ref);
   const float2 neg1 = make_float2(-1.f, -1.f);
   float2 ls = make_float2(0.f, 0.f);
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
     uint32_t pk[LO ? 32 : 16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float2 e = __ffma2_rn(make_float2(__uint_as_float(v[cc][2 * j]), __uint_as_float(v[cc][2 * j + 1])),
-                                  sl2v, negm);
+      const float2 sv = make_float2(__uint_as_float(v[cc][2 * j]), __uint_as_float(v[cc][2 * j + 1]));
+      if constexpr (MAX) {
+        float &a = m4[cc * 2 + (j & 1)];
+        a = fmax3(a, sv.x, sv.y);
+      }
+      const float2 e = __ffma2_rn(sv, sl2v, negm);
       float2 pr = make_float2(ex2(e.x), ex2(e.y));
       if (!full) {
         const int key = kb + cc * 32 + 2 * j;
@@ -203,6 +262,7 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t (&v)[2][32], uint
       tc::st_32x32b_x16(s_addr + cc * 32, pk);
     }
   }
+  if constexpr (MAX) *mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
   return ls.x + ls.y;
 }
 
@@ -288,144 +348,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
   bool timed_out = false;
 
-  if (warp >= kWarpLoad0 && warp < kWarpMma) {
-    // ---------------- loader warps: each tile's K and V boxes, a third per warp ----------------
-    const int lw = warp - kWarpLoad0;
-    int32_t *sbt = reinterpret_cast<int32_t *>(smem + OFF_BT);
-    const int cached = min(min(npages, nkt * 8) - pg0, kBtCache);
-    for (int i = lw * 32 + lane; i < cached; i += kLoadWarps * 32) sbt[i] = __ldg(bt + pg0 + i);
-    named_barrier(1, kLoadWarps * 32);  // the cached block ids are complete
-    griddep_wait();                     // Q, K and V may come from the previous kernel
-    if (lw == 0 && lane == 0) {
-      mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf);
-      tma_load_3d(smem + OFF_Q, &qmap, &bars.q_full, 0, h * G, row0 + t0);
-      tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
-    }
-    const int kb0 = lw, vb0 = (lw + kLoadWarps - 1) % kLoadWarps;  // balances the boxes per warp
-    int k_issued = 0, v_issued = 0;  // tiles whose K / V boxes this warp has issued
-    for (int t = 0; t < ntl; ++t) {
-      const int ks = t % kKStages, vs = t % kVStages;
-      if (t >= kKStages && !mbar_wait(&bars.s_full[ks], ((t - kKStages) / kKStages) & 1)) {
-        timed_out = true;
-        break;
-      }
-      load_boxes(smem + OFF_K + ks * 2 * kHalf, &kmap, &bars.k_full[ks], kt0 + t, kb0, h, pg0, npages, false, sbt,
-                 bt, p, c, lane);
-      k_issued = t + 1;
-      if (t >= kVStages && !mbar_wait(&bars.pv_done[vs], ((t - kVStages) / kVStages) & 1)) {
-        timed_out = true;
-        break;
-      }
-      load_boxes(smem + OFF_V + vs * 2 * kHalf, &vmap, &bars.v_full[vs], kt0 + t, vb0, h, pg0, npages, true, sbt,
-                 bt, p, c, lane);
-      v_issued = t + 1;
-    }
-    if (timed_out) {
-      // Before the CTA ends (and its shared memory is handed to another CTA),
-      // give this warp's copies still in flight a short, bounded chance to
-      // land: the last tile of each stage it issued (each stage's barrier is
-      // at most at that tile's phase).  A barrier that another warp left
-      // short of its arrivals never completes; the wait then just ends.
-      if (lw == 0) mbar_wait(&bars.q_full, 0, kWaitLimitNs / 8);
-      for (int t = k_issued - kKStages > 0 ? k_issued - kKStages : 0; t < k_issued; ++t)
-        mbar_wait(&bars.k_full[t % kKStages], (t / kKStages) & 1, kWaitLimitNs / 8);
-      for (int t = v_issued - kVStages > 0 ? v_issued - kVStages : 0; t < v_issued; ++t)
-        mbar_wait(&bars.v_full[t % kVStages], (t / kVStages) & 1, kWaitLimitNs / 8);
-    }
-  } else if (warp == kWarpMma) {
-    // ---------------- MMA issuer ----------------
-    // The whole warp runs this loop (waits, barrier phases, descriptors), and
-    // one elected lane issues each batch of MMAs and its commit: from a
-    // warp-uniform loop the MMAs issue at the tensor core's own rate (32.7 ns
-    // each at M = N = 128, K = 16) even while the softmax warps on the same
-    // sub-partition are busy, where a loop run by one lane alone measured
-    // 46-49 ns per MMA.
-    // Descriptors are built once; a k-step or a ring stage only moves the start
-    // address field (bits 0..13, address >> 4), so each MMA costs a 64-bit add.
-    // Shared-memory offsets stay below 256 KB, so the field never carries over.
-    // The tensor core queues only a few MMAs, so any latency between two
-    // batches leaves it idle: the P barrier of the next P V batch is probed
-    // without blocking right after the QK^T batch is issued; only a P that
-    // really is not ready yet costs a (bounded) blocking wait.
-    const bool leader = elect_one();
-    auto wait_all = [&](uint64_t *bar, uint32_t parity) {  // warp-uniform result
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
-    };
-    if (!wait_all(&bars.q_full, 0)) timed_out = true;
-    const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
-    const uint64_t kdesc0 = tc::desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
-    const uint64_t vdesc0 = tc::desc_sw128(smem_u32(smem + OFF_V), kHalf, 1024);
-    constexpr uint64_t kStageStep = (2 * kHalf) >> 4;   // one ring stage
-    constexpr uint64_t kHalfStep = kHalf >> 4;          // the other 64-dim half
-    bool pv_ok = false;                                  // P (and so V) of the next P V batch is ready
-    for (int kt = 0; kt <= ntl && !timed_out; ++kt) {   // kt: tile index from kt0
-      const int j = kt - 1, sj = j & 1;                  // the tile whose P V is issued in this iteration
-      const int jv = j % kVStages;
-      if (kt < ntl) {
-        const int b = kt % kKStages, sb = kt & 1;
-        if (!wait_all(&bars.k_full[b], (kt / kKStages) & 1)) {
-          timed_out = true;
-          break;
-        }
-        tc::fence_after_sync();
-        const uint64_t kdesc = kdesc0 + (uint64_t)b * kStageStep;
-        const uint32_t s_col = tmem + sb * 128;
-        if (leader) {
-          tc::mma_f16(s_col, qdesc, kdesc, IDESC_S, 0u);
-#pragma unroll
-          for (int kk = 1; kk < 8; ++kk) {
-            const uint64_t off = (uint64_t)((kk >> 2) * kHalfStep + (kk & 3) * 2);   // 16-element k-step
-            tc::mma_f16(s_col, qdesc + off, kdesc + off, IDESC_S, 1u);
-          }
-          tc::commit(&bars.s_full[b]);
-        }
-        __syncwarp();
-        pv_ok = kt >= 1 && __all_sync(0xffffffffu, mbar_test_wait(&bars.p_full[jv], (j / kVStages) & 1));
-      } else {
-        pv_ok = false;
-      }
-      if (kt >= 1) {  // O_half += P V of the previous tile: keys 0..63 into O_0, 64..127 into O_1
-        if (!pv_ok && !wait_all(&bars.p_full[jv], (j / kVStages) & 1)) {
-          timed_out = true;
-          break;
-        }
-        tc::fence_after_sync();
-        const uint64_t vdesc = vdesc0 + (uint64_t)jv * kStageStep;
-        const uint32_t p_col = tmem + sj * 128;
-        const uint32_t first = j > 0 ? 1u : 0u;
-        if (leader) {
-          if (j < lo_tiles) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {  // 16-key step: V rows 16 kk .. 16 kk + 15, into O of key half kk / 4
-              const uint32_t o_col = tmem + kColO + (kk >> 2) * 128;
-              const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
-              const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
-              tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
-              tc::mma_f16_ts(o_col, a_hi + 16, bdesc, IDESC_O, 1u);
-            }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t o_col = tmem + kColO + (kk >> 2) * 128;
-              const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
-              const uint64_t bdesc = vdesc + (uint64_t)(kk * (2048 >> 4));
-              tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
-            }
-          }
-          tc::commit(&bars.pv_done[jv]);
-        }
-        __syncwarp();
-      }
-    }
-    if (timed_out) {
-      // The MMAs already issued may still be writing TMEM (and reading
-      // shared memory): one more commit tracks all of them; wait for it,
-      // bounded, before the CTA frees its TMEM and ends.
-      if (leader) tc::commit(&bars.drain);
-      __syncwarp();
-      mbar_wait(&bars.drain, 0, kWaitLimitNs / 8);
-    }
-  } else {
+  if (warp < kSoftmaxWarps) {
+    regs_inc<kRegsSoftmax>();
     // ---------------- softmax + epilogue (warps 0..7) ----------------
     const int quad = warp & 3, ch = warp >> 2;       // TMEM lane quarter, key half of every tile
     const int r = quad * 32 + lane;                  // tile row = TMEM lane
@@ -458,14 +382,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       tc::ld_32x32b_x32(s_addr + 32, v[1]);
       tc::wait_ld();
       const bool full = __all_sync(FULL, kb >= 0 && kb + 63 <= span);
-
-      float mx = -INFINITY;
-      if (full) {
+      const bool first = (m_ref == -INFINITY);             // nothing accumulated for this row yet
+      // The common tile (all keys visible, a reference maximum already set,
+      // one-term P) computes P against the current reference and takes the
+      // tile's own maximum in the same pass; only if that maximum exceeds the
+      // reference by more than 2^8 (rare) is P computed again below, from the
+      // scores still in registers, after O and l are rescaled.  Other tiles
+      // take the maximum first.
+      // warp-uniform (the TMEM stores inside are warp-wide): a row whose window
+      // or causal limit hid every key so far still has no reference maximum
+      const bool common = kt >= lo_tiles && __all_sync(FULL, full && !first);
+      float mx = -INFINITY, ls = 0.f;
+      if (common) {
+        ls = exp_pack_store<T, false, true>(v, s_addr, sl2, m_ref, true, kb, span, &mx);
+      } else if (full) {  // four independent chains of three-input maxima
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-          for (int j = 0; j < 32; j += 2)
-            mx = fmaxf(mx, fmaxf(__uint_as_float(v[cc][j]), __uint_as_float(v[cc][j + 1])));
+          for (int j = 0; j < 32; j += 4) {
+            float &a = m4[cc * 2 + ((j >> 2) & 1)];
+            a = fmax3(a, __uint_as_float(v[cc][j]), __uint_as_float(v[cc][j + 1]));
+            a = fmax3(a, __uint_as_float(v[cc][j + 2]), __uint_as_float(v[cc][j + 3]));
+          }
+        mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
       } else {
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
@@ -474,9 +414,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             if ((unsigned)(kb + cc * 32 + j) <= (unsigned)span) mx = fmaxf(mx, __uint_as_float(v[cc][j]));
       }
       const float mc = mx * sl2;   // -inf if no key of this half is visible yet
-      const bool first = (m_ref == -INFINITY);             // nothing accumulated for this row yet
       const bool need = !first && (mc > m_ref + kRescale);
-      if (__any_sync(FULL, need)) {  // warp-uniform: the TMEM accesses below are warp-wide
+      const bool redo = __any_sync(FULL, need);
+      if (redo) {  // warp-uniform: the TMEM accesses below are warp-wide
+        if (common) tc::wait_st();
         const float f = need ? ex2(m_ref - mc) : 1.f;
         if (need) {
           l *= f;
@@ -499,10 +440,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
       }
       if (first) m_ref = mc;
-
-      // P in the input dtype (two terms where the tile needs them), over this half's S columns
-      l += (kt < lo_tiles) ? exp_pack_store<T, true>(v, s_addr, sl2, m_ref, full, kb, span)
-                           : exp_pack_store<T, false>(v, s_addr, sl2, m_ref, full, kb, span);
+      if (!common || redo) {
+        // P in the input dtype (two terms where the tile needs them), over this half's S columns
+        ls = (kt < lo_tiles) ? exp_pack_store<T, true>(v, s_addr, sl2, m_ref, full, kb, span)
+                             : exp_pack_store<T, false>(v, s_addr, sl2, m_ref, full, kb, span);
+      }
+      l += ls;
       tc::wait_st();
 
       if (kt == kt_last) {
@@ -517,8 +460,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         uint8_t *vbase = smem + OFF_V + vb * 2 * kHalf;
         for (int idx = (warp & 3) * 32 + lane; idx < (z1 - z0) * 16; idx += kSoftmaxThreads / 2) {
           const int row = z0 + (idx >> 4), part = idx & 15;
-          *reinterpret_cast<uint4 *>(vbase + (part >> 3) * kHalf + row * 128 + (part & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4 *>(vbase + (row >> 4) * kVPage + (part >> 3) * (kVPage / 2) + (row & 15) * 128 +
+                                     (part & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
@@ -579,8 +522,152 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         timed_out = true;
       }
     }
+    regs_dec<128>();
+  } else {
+    // every loader and MMA warp runs this one decrease (setmaxnreg acts on whole warpgroups)
+    regs_dec<kRegsOther>();
+    if (warp != kWarpMma) {
+      // ---------------- loader warps: each tile's K and V boxes, a seventh per warp ----------------
+      const int lw = warp - kWarpLoad0;
+      int32_t *sbt = reinterpret_cast<int32_t *>(smem + OFF_BT);
+      const int cached = min(min(npages, nkt * 8) - pg0, kBtCache);
+      for (int i = lw * 32 + lane; i < cached; i += kLoadWarps * 32) sbt[i] = __ldg(bt + pg0 + i);
+      named_barrier(1, kLoadWarps * 32);  // the cached block ids are complete
+      griddep_wait();                     // Q, K and V may come from the previous kernel
+      if (lw == 0 && lane == 0) {
+        mbar_arrive_expect_tx(&bars.q_full, 2 * kHalf);
+        tma_load_3d(smem + OFF_Q, &qmap, &bars.q_full, 0, h * G, row0 + t0);
+        tma_load_3d(smem + OFF_Q + kHalf, &qmap, &bars.q_full, 64, h * G, row0 + t0);
+      }
+      // K boxes lw, lw + 7, lw + 14 and V pages (lw + 5) % 7, + 7: at most 4 boxes per warp and tile
+      const int kb0 = lw, vb0 = (lw + 5) % kLoadWarps;
+      int k_issued = 0, v_issued = 0;  // tiles whose K / V boxes this warp has issued
+      for (int t = 0; t < ntl; ++t) {
+        const int ks = t % kKStages, vs = t % kVStages;
+        if (t >= kKStages && !mbar_wait(&bars.s_full[ks], ((t - kKStages) / kKStages) & 1)) {
+          timed_out = true;
+          break;
+        }
+        load_boxes(smem + OFF_K + ks * 2 * kHalf, &kmap, &bars.k_full[ks], kt0 + t, kb0, h, pg0, npages, sbt, bt, p,
+                   c, lane);
+        k_issued = t + 1;
+        if (t >= kVStages && !mbar_wait(&bars.pv_done[vs], ((t - kVStages) / kVStages) & 1)) {
+          timed_out = true;
+          break;
+        }
+        load_vpages(smem + OFF_V + vs * 2 * kHalf, &vmap, &bars.v_full[vs], kt0 + t, vb0, h, pg0, npages, sbt, bt,
+                    p, c, lane);
+        v_issued = t + 1;
+      }
+      if (timed_out) {
+        // Before the CTA ends (and its shared memory is handed to another CTA),
+        // give this warp's copies still in flight a short, bounded chance to
+        // land: the last tile of each stage it issued (each stage's barrier is
+        // at most at that tile's phase).  A barrier that another warp left
+        // short of its arrivals never completes; the wait then just ends.
+        if (lw == 0) mbar_wait(&bars.q_full, 0, kWaitLimitNs / 8);
+        for (int t = k_issued - kKStages > 0 ? k_issued - kKStages : 0; t < k_issued; ++t)
+          mbar_wait(&bars.k_full[t % kKStages], (t / kKStages) & 1, kWaitLimitNs / 8);
+        for (int t = v_issued - kVStages > 0 ? v_issued - kVStages : 0; t < v_issued; ++t)
+          mbar_wait(&bars.v_full[t % kVStages], (t / kVStages) & 1, kWaitLimitNs / 8);
+      }
+    } else {
+      // ---------------- MMA issuer ----------------
+      // The whole warp runs this loop (waits, barrier phases, descriptors), and
+      // one elected lane issues each batch of MMAs and its commit: from a
+      // warp-uniform loop the MMAs issue at the tensor core's own rate (32.7 ns
+      // each at M = N = 128, K = 16) even while the softmax warps on the same
+      // sub-partition are busy, where a loop run by one lane alone measured
+      // 46-49 ns per MMA.
+      // Descriptors are built once; a k-step or a ring stage only moves the start
+      // address field (bits 0..13, address >> 4), so each MMA costs a 64-bit add.
+      // Shared-memory offsets stay below 256 KB, so the field never carries over.
+      // The tensor core queues only a few MMAs, so any latency between two
+      // batches leaves it idle: the P barrier of the next P V batch is probed
+      // without blocking right after the QK^T batch is issued; only a P that
+      // really is not ready yet costs a (bounded) blocking wait.
+      const bool leader = elect_one();
+      auto wait_all = [&](uint64_t *bar, uint32_t parity) {  // warp-uniform result
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
+      };
+      if (!wait_all(&bars.q_full, 0)) timed_out = true;
+      const uint64_t qdesc = tc::desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
+      const uint64_t kdesc0 = tc::desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
+      // V stages hold 8 pages of 4 KB: the dims 64..127 of a page 2 KB after its dims 0..63
+      const uint64_t vdesc0 = tc::desc_sw128(smem_u32(smem + OFF_V), kVPage / 2, 1024);
+      constexpr uint64_t kStageStep = (2 * kHalf) >> 4;   // one ring stage
+      constexpr uint64_t kHalfStep = kHalf >> 4;          // the other 64-dim half
+      bool pv_ok = false;                                  // P (and so V) of the next P V batch is ready
+      for (int kt = 0; kt <= ntl && !timed_out; ++kt) {   // kt: tile index from kt0
+        const int j = kt - 1, sj = j & 1;                  // the tile whose P V is issued in this iteration
+        const int jv = j % kVStages;
+        if (kt < ntl) {
+          const int b = kt % kKStages, sb = kt & 1;
+          if (!wait_all(&bars.k_full[b], (kt / kKStages) & 1)) {
+            timed_out = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t kdesc = kdesc0 + (uint64_t)b * kStageStep;
+          const uint32_t s_col = tmem + sb * 128;
+          if (leader) {
+            tc::mma_f16(s_col, qdesc, kdesc, IDESC_S, 0u);
+  #pragma unroll
+            for (int kk = 1; kk < 8; ++kk) {
+              const uint64_t off = (uint64_t)((kk >> 2) * kHalfStep + (kk & 3) * 2);   // 16-element k-step
+              tc::mma_f16(s_col, qdesc + off, kdesc + off, IDESC_S, 1u);
+            }
+            tc::commit(&bars.s_full[b]);
+          }
+          __syncwarp();
+          pv_ok = kt >= 1 && __all_sync(0xffffffffu, mbar_test_wait(&bars.p_full[jv], (j / kVStages) & 1));
+        } else {
+          pv_ok = false;
+        }
+        if (kt >= 1) {  // O_half += P V of the previous tile: keys 0..63 into O_0, 64..127 into O_1
+          if (!pv_ok && !wait_all(&bars.p_full[jv], (j / kVStages) & 1)) {
+            timed_out = true;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint64_t vdesc = vdesc0 + (uint64_t)jv * kStageStep;
+          const uint32_t p_col = tmem + sj * 128;
+          const uint32_t first = j > 0 ? 1u : 0u;
+          if (leader) {
+            if (j < lo_tiles) {
+  #pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {  // 16-key step: V rows 16 kk .. 16 kk + 15, into O of key half kk / 4
+                const uint32_t o_col = tmem + kColO + (kk >> 2) * 128;
+                const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
+                const uint64_t bdesc = vdesc + (uint64_t)(kk * (kVPage >> 4));   // page kk
+                tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
+                tc::mma_f16_ts(o_col, a_hi + 16, bdesc, IDESC_O, 1u);
+              }
+            } else {
+  #pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t o_col = tmem + kColO + (kk >> 2) * 128;
+                const uint32_t a_hi = p_col + 32 * (kk >> 1) + 8 * (kk & 1);
+                const uint64_t bdesc = vdesc + (uint64_t)(kk * (kVPage >> 4));   // page kk
+                tc::mma_f16_ts(o_col, a_hi, bdesc, IDESC_O, (kk & 3) > 0 ? 1u : first);
+              }
+            }
+            tc::commit(&bars.pv_done[jv]);
+          }
+          __syncwarp();
+        }
+      }
+      if (timed_out) {
+        // The MMAs already issued may still be writing TMEM (and reading
+        // shared memory): one more commit tracks all of them; wait for it,
+        // bounded, before the CTA frees its TMEM and ends.
+        if (leader) tc::commit(&bars.drain);
+        __syncwarp();
+        mbar_wait(&bars.drain, 0, kWaitLimitNs / 8);
+      }
+    }
+    regs_inc<128>();
   }
-
   if (timed_out) set_error(p.err, PA_ERR_TIMEOUT, c);
   tc::fence_before_sync();
   __syncthreads();
