@@ -571,17 +571,20 @@ pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t *chunk
   CUtensorMap kmap, vmap, qmap;
   if (!pool_map(&kmap, pool, pool->k_cache, false) || !pool_map_vpages(&vmap, pool, pool->v_cache))
     return PA_ERR_CUDA;
-  // q as a 3-D tensor {dim, query head, token}; boxes of {64 dims, G heads,
-  // 128/G tokens} give 128 rows (token-major, head-minor) of 128 bytes.
+  // q (and out) as a 3-D tensor {dim, query head, token}; boxes of {64 dims,
+  // G heads, 128/G tokens} give 128 rows (token-major, head-minor) of 128 bytes.
+  CUtensorMap omap;
   {
     const uint64_t dims[3] = {(uint64_t)kHeadDim, (uint64_t)num_q_heads, (uint64_t)total_q_tokens};
     const uint64_t strides[2] = {kHeadDim * 2ull, (uint64_t)num_q_heads * kHeadDim * 2ull};
     const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)(128 / group)};
     if (!encode_tensor_map(&qmap, map_dtype(pool->dtype), 3, const_cast<void *>(q), dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B))
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&omap, map_dtype(pool->dtype), 3, out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return PA_ERR_CUDA;
   }
-  cudaError_t e = launch_prefill(p, kmap, vmap, qmap, pool->dtype, group, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      launch_prefill(p, kmap, vmap, qmap, omap, pool->dtype, group, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }

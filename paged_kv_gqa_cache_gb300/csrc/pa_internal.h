@@ -170,8 +170,11 @@ struct PrefillParams {
   int32_t window;            // sliding window in keys (0: none)
   float scale_log2;
 };
+// omap: `out` as the 3-D tensor {dim, query head, token} with qmap's boxes (for
+// the TMA store of whole query tiles).
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                           const CUtensorMap &qmap, int dtype, int group, cudaStream_t stream);
+                           const CUtensorMap &qmap, const CUtensorMap &omap, int dtype, int group,
+                           cudaStream_t stream);
 
 // ---- launch helper ------------------------------------------------------------
 // Launch with programmatic stream serialization (see griddep_wait()).

@@ -230,13 +230,14 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t (&v)[2][32], uint
                                                 bool full, int kb, int span, float *mx = nullptr) {
   const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_ref, -m_ref);
   const float2 neg1 = make_float2(-1.f, -1.f);
-  float2 ls = make_float2(0.f, 0.f);
+  // the two chunks interleaved and four partial sums: short dependency chains
+  float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  uint32_t pk[2][LO ? 32 : 16];
 #pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {
-    uint32_t pk[LO ? 32 : 16];
+  for (int j = 0; j < 16; ++j) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int cc = 0; cc < 2; ++cc) {
       const float2 sv = make_float2(__uint_as_float(v[cc][2 * j]), __uint_as_float(v[cc][2 * j + 1]));
       if constexpr (MAX) {
         float &a = m4[cc * 2 + (j & 1)];
@@ -249,27 +250,33 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t (&v)[2][32], uint
         pr.x = ((unsigned)key <= (unsigned)span) ? pr.x : 0.f;
         pr.y = ((unsigned)(key + 1) <= (unsigned)span) ? pr.y : 0.f;
       }
-      ls = __fadd2_rn(ls, pr);
-      pk[j] = Pack<T>::from_f2(pr.x, pr.y);
+      float2 &acc = ls[(2 * j + cc) & 3];
+      acc = __fadd2_rn(acc, pr);
+      pk[cc][j] = Pack<T>::from_f2(pr.x, pr.y);
       if constexpr (LO) {
-        const float2 lo = __ffma2_rn(Pack<T>::to_f2(pk[j]), neg1, pr);  // P - P_hi, exact
-        pk[16 + j] = Pack<T>::from_f2(lo.x, lo.y);
+        const float2 lo = __ffma2_rn(Pack<T>::to_f2(pk[cc][j]), neg1, pr);  // P - P_hi, exact
+        pk[cc][16 + j] = Pack<T>::from_f2(lo.x, lo.y);
       }
     }
+  }
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
     if constexpr (LO) {
-      tc::st_32x32b_x32(s_addr + cc * 32, pk);
+      tc::st_32x32b_x32(s_addr + cc * 32, pk[cc]);
     } else {
-      tc::st_32x32b_x16(s_addr + cc * 32, pk);
+      tc::st_32x32b_x16(s_addr + cc * 32, pk[cc]);
     }
   }
   if constexpr (MAX) *mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-  return ls.x + ls.y;
+  const float2 t = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
+  return t.x + t.y;
 }
 
 template <typename T, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-               const __grid_constant__ CUtensorMap qmap, const PrefillParams p) {
+               const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+               const PrefillParams p) {
   constexpr int TQ = 128 / G;  // query tokens per tile
   constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t IDESC_S = tc::idesc_f16(kBF16, 128, 128, false);
@@ -326,6 +333,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
     tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&omap);
     mbar_init(&bars.q_full, 1);
     for (int b = 0; b < kKStages; ++b) {
       mbar_init(&bars.k_full[b], kLoadWarps);
@@ -493,6 +501,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           const float g0 = f0 * inv, g1 = f1 * inv;
           T *op = reinterpret_cast<T *>(p.out) + ((int64_t)(row0 + tq) * p.num_q_heads + head) * kHeadDim + ch * 64;
           const uint32_t o0 = tmem + lane_base + kColO + ch * 64, o1 = o0 + 128;
+          // A query tile wholly inside its chunk leaves through one TMA store per
+          // 64-dim half: each thread puts its row's 64 outputs into the (now idle)
+          // Q buffer in the 128-byte swizzled layout the Q tile came in, which is
+          // the out tensor's own tile shape.  A tile that runs past the chunk's
+          // end (its last rows belong to the next chunk) stores row by row.
+          const bool tile_store = t0 + TQ <= len;
+          uint8_t *otile = smem + OFF_Q + ch * kHalf;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             uint32_t a[32], b[32];
@@ -511,9 +526,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               w[i].z = Pack<T>::from_f2(y[4], y[5]);
               w[i].w = Pack<T>::from_f2(y[6], y[7]);
             }
-            // warp-wide (every lane takes part); rows past the chunk are not stored
-            store_rows_coalesced(reinterpret_cast<uint4 *>(smem + OFF_STAGE + warp * kStageBytes), op + cc * 32,
-                                 tq < len, w, lane);
+            if (tile_store) {  // 16-byte piece cc * 4 + i of row r, XOR-swizzled by r % 8
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint4 *>(otile + r * 128 + (((cc * 4 + i) ^ (r & 7)) << 4)) = w[i];
+            } else {
+              // warp-wide (every lane takes part); rows past the chunk are not stored
+              store_rows_coalesced(reinterpret_cast<uint4 *>(smem + OFF_STAGE + warp * kStageBytes), op + cc * 32,
+                                   tq < len, w, lane);
+            }
+          }
+          if (tile_store) {
+            fence_proxy_async_smem();  // the generic writes reach the TMA engine
+            named_barrier(2, kSoftmaxThreads);
+            if (threadIdx.x == 0) {
+              tma_store_3d(&omap, smem + OFF_Q, 0, h * G, row0 + t0);
+              tma_store_3d(&omap, smem + OFF_Q + kHalf, 64, h * G, row0 + t0);
+              bulk_commit_group();
+              bulk_wait_group_all();  // before the CTA ends and its shared memory is reused
+            }
           }
         } else {
           timed_out = true;
@@ -680,21 +711,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 
 template <typename T, int G>
 cudaError_t launch_typed(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                         const CUtensorMap &qmap, cudaStream_t stream) {
+                         const CUtensorMap &qmap, const CUtensorMap &omap, cudaStream_t stream) {
   static KernelSetup setup;
   cudaError_t e = kernel_setup(setup, prefill_kernel<T, G>, SMEM_BYTES, kThreads, nullptr);
   if (e != cudaSuccess) return e;
   constexpr int TQ = 128 / G;
   dim3 grid((p.max_chunk_len + TQ - 1) / TQ, p.num_kv_heads, p.num_chunks);
-  return launch_pdl(prefill_kernel<T, G>, grid, dim3(kThreads), SMEM_BYTES, stream, kmap, vmap, qmap, p);
+  return launch_pdl(prefill_kernel<T, G>, grid, dim3(kThreads), SMEM_BYTES, stream, kmap, vmap, qmap, omap, p);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
-                           const CUtensorMap &qmap, int dtype, int group, cudaStream_t stream) {
+                           const CUtensorMap &qmap, const CUtensorMap &omap, int dtype, int group,
+                           cudaStream_t stream) {
 #define PA_PREFILL_CASE(T, G) \
-  if (group == G) return launch_typed<T, G>(p, kmap, vmap, qmap, stream);
+  if (group == G) return launch_typed<T, G>(p, kmap, vmap, qmap, omap, stream);
   if (dtype == PA_BF16) {
     PA_PREFILL_CASE(__nv_bfloat16, 1)
     PA_PREFILL_CASE(__nv_bfloat16, 2)
