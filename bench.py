@@ -88,6 +88,10 @@ def parse_args(argv=None):
                     help="decode calls with PA_DECODE_ZEROED_WORKSPACE: one launch over all SMs that merges "
                          "split sequences itself, instead of the plain plan (one cluster per sequence and KV "
                          "head when they fit, else split + combine kernels)")
+    ap.add_argument("--balanced-prefill", action="store_true",
+                    help="workload 3: the prefill as one launch balanced over the SMs "
+                         "(pa_paged_attn_prefill_chunk_ex) instead of one CTA per query tile "
+                         "(pa_paged_attn_prefill_chunk_window)")
     ap.add_argument("--overlap", action="store_true",
                     help="workload 3: each layer's prefill on a second stream beside its decode (same work)")
     ap.add_argument("--window", type=int, default=0,
@@ -396,7 +400,7 @@ class MixedStep:
     kv_cache_write of 2048 new tokens, prefill of 3 chunks of 512 (prefixes 0,
     512, 1536) and decode of 512 sequences; 2 distinct pools cycled over 28."""
 
-    def __init__(self, device, window: int = 0, overlap: bool = False, fused: bool = False):
+    def __init__(self, device, window: int = 0, overlap: bool = False, fused: bool = False, balanced: bool = False):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
@@ -408,6 +412,8 @@ class MixedStep:
         self.out_d = [torch.empty_like(q) for q in c.q]
         self.out_p = [torch.empty_like(q) for q in c.q_chunks]
         self.ws = pa.alloc_decode_workspace(c.q[0].shape[0], c.hq, c.hkv, c.max_context_len, device)
+        # the balanced prefill's workspace (zero-filled; every call leaves it zeroed)
+        self.pws = pa.alloc_prefill_workspace(c.chunk_starts.numel(), c.hq, c.hkv, 512, device) if balanced else None
         self.flops_layer = workloads.prefill_flops(c.meta["chunks"], c.hq, window=window)
         self.tokens = c.slot_mapping.numel()
         lens = c.meta["decode_lens"]
@@ -421,7 +427,8 @@ class MixedStep:
                              if meta is None else meta[3:])
         self.pa.paged_attn_prefill_chunk_window(c.q_chunks[i] if qp is None else qp, cs, cl, c.k_cache[i],
                                                 c.v_cache[i], cbt, cctx, c.scale, self.window,
-                                                out=self.out_p[i] if out is None else out, max_chunk_len=512)
+                                                out=self.out_p[i] if out is None else out, max_chunk_len=512,
+                                                workspace=self.pws)
 
     def layer(self, l, q=None, qp=None, kn=None, vn=None, out_d=None, out_p=None, meta=None):
         """One layer's calls; the end-to-end run passes the copies it made of
@@ -801,7 +808,7 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
     """The JSON line of the mixed chunked-prefill step (28 layers)."""
     import torch
     rank, world, _ = dist_env()
-    step = MixedStep(dev, window, overlap, args.fused)
+    step = MixedStep(dev, window, overlap, args.fused, balanced=args.balanced_prefill)
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_pre = graph_of(step.run_prefill_only, 1, stream)
@@ -831,6 +838,8 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
                                "2 distinct pools cycled"
                                + (f"; sliding window of {window} keys (FLOPs of the visible pairs)" if window else "")
                                + ("; each layer's prefill on a second stream beside its decode" if overlap else "")
+                               + ("; prefill balanced over the SMs (pa_paged_attn_prefill_chunk_ex)"
+                                  if step.pws is not None else "")
                                + ("; decode as one launch over all SMs (PA_DECODE_ZEROED_WORKSPACE)"
                                   if step.fused else ""),
                    "global_batch": 515 * world, "parallelism": f"replicas x{world}",
@@ -844,8 +853,9 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(tflops / bf16, 3), "peak_kind": peak_kind,
-                     "kernel": "paged_attn_prefill_chunk" + (f"_window (W={window})" if window else "")
-                               + " per layer", "flops_per_launch": step.flops_layer,
+                     "kernel": "paged_attn_prefill_chunk" + ("_ex (balanced)" if step.pws is not None else "")
+                               + (f" window W={window}" if window else "") + " per layer",
+                     "flops_per_launch": step.flops_layer,
                      "launch_ms": round(ms_pre, 5), "launches_timed": step.L * args.steps * len(pre_reps),
                      "traffic": committed_traffic("prefill.cu", f"prefill{f'_window{window}' if window else ''}"
                                                                 f"_workload3.md")},

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 7
+#define PA_ABI_VERSION 8
 #define PA_HEAD_DIM 128
 #define PA_BLOCK_SIZE 16
 #define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
@@ -403,6 +403,34 @@ PA_API pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t
                                                     int32_t num_q_heads, int32_t total_q_tokens,
                                                     int32_t max_chunk_len, float scale, int32_t window,
                                                     void *out, pa_stream_t stream);
+
+/*
+ * paged_attn_prefill_chunk_ex — pa_paged_attn_prefill_chunk_window (window 0:
+ * the plain causal chunks) as one launch balanced over the SMs.  No
+ * counterpart on the pages: a library addition.  The causal mask makes a
+ * chunk's last query tiles many times heavier than its first ones (and a long
+ * prefix heavier still); here one CTA per SM takes an equal share of all
+ * (query tile, 128-key tile) pairs, and a query tile split between CTAs is
+ * merged (log-sum-exp) by the CTA whose piece finishes last.
+ *   workspace  at least pa_prefill_workspace_bytes(...) bytes (for the current
+ *              device: it depends on its SM count), 16-byte aligned.  Zero-fill
+ *              it before its first use; every call that completes without
+ *              PA_ERR_TIMEOUT leaves its counters at zero again, so it needs no
+ *              clearing between calls (after a PA_ERR_TIMEOUT, zero-fill it
+ *              again).  Calls sharing a workspace must not overlap on the GPU.
+ * With more than 256 chunks the plain launch runs (the workspace is unused).
+ * Results equal the plain call's up to fp32 rounding (a split tile's pieces
+ * are summed in another order).  Other arguments and errors as
+ * pa_paged_attn_prefill_chunk_window; no workspace: PA_ERR_WORKSPACE.
+ */
+PA_API size_t pa_prefill_workspace_bytes(int32_t num_chunks, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t max_chunk_len);
+PA_API pa_status pa_paged_attn_prefill_chunk_ex(const void *q, const int32_t *chunk_starts, const int32_t *chunk_lens,
+                                                const pa_kv_pool *pool, const int32_t *block_tables,
+                                                int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                                int32_t num_chunks, int32_t num_q_heads, int32_t total_q_tokens,
+                                                int32_t max_chunk_len, float scale, int32_t window, void *out,
+                                                void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * qk_norm_rope_kv_write — [P1, qwen_serve/model.py: rms_norm, _rotate_half,

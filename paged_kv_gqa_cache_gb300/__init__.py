@@ -47,7 +47,8 @@ EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_deco
            "pa_kv_cache_write_f8", "pa_paged_attn_decode_f8",
            "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
            "pa_qk_norm_rope_kv_write", "pa_paged_attn_decode_append", "pa_selftest_bounded_wait",
-           "pa_paged_attn_decode_ex", "pa_paged_attn_decode_q8_ex",
+           "pa_paged_attn_decode_ex", "pa_paged_attn_decode_q8_ex", "pa_prefill_workspace_bytes",
+           "pa_paged_attn_prefill_chunk_ex",
            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
            "pa_allocator_release", "pa_allocator_refcount", "pa_allocator_stats_get", "pa_allocator_take_copies",
            "pa_sequence_create", "pa_sequence_destroy", "pa_sequence_reserve", "pa_sequence_commit",
@@ -136,6 +137,11 @@ def load_library(path: str = LIB_PATH):
         lib.pa_paged_attn_prefill_chunk_window.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
                                                            ctypes.c_float, i32, P, P]
         lib.pa_paged_attn_prefill_chunk_window.restype = i32
+        lib.pa_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        lib.pa_prefill_workspace_bytes.restype = ctypes.c_size_t
+        lib.pa_paged_attn_prefill_chunk_ex.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
+                                                       ctypes.c_float, i32, P, P, ctypes.c_size_t, P]
+        lib.pa_paged_attn_prefill_chunk_ex.restype = i32
         lib.pa_qk_norm_rope_kv_write.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, i32, P, P, i32, i32, P,
                                                  pool_p, P]
         lib.pa_qk_norm_rope_kv_write.restype = i32
@@ -479,25 +485,41 @@ def paged_attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
 def paged_attn_prefill_chunk(q: torch.Tensor, chunk_starts: torch.Tensor, chunk_lens: torch.Tensor,
                              k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                              context_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
-                             max_chunk_len: int = 512, stream=None) -> torch.Tensor:
-    """Causal chunked-prefill attention: q [sum(chunk_lens), Hq, 128] → out (pool dtype)."""
+                             max_chunk_len: int = 512, stream=None,
+                             workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Causal chunked-prefill attention: q [sum(chunk_lens), Hq, 128] → out (pool dtype).
+
+    With ``workspace`` (from :func:`alloc_prefill_workspace`: zero-filled, and
+    kept zero by every call) the call runs as one launch balanced over the
+    SMs (``pa_paged_attn_prefill_chunk_ex``)."""
     return _prefill(q, chunk_starts, chunk_lens, k_cache, v_cache, block_tables, context_lens, scale, 0, out,
-                    max_chunk_len, stream)
+                    max_chunk_len, stream, workspace)
 
 
 def paged_attn_prefill_chunk_window(q: torch.Tensor, chunk_starts: torch.Tensor, chunk_lens: torch.Tensor,
                                     k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                                     context_lens: torch.Tensor, scale: float, window: int,
                                     out: Optional[torch.Tensor] = None, max_chunk_len: int = 512,
-                                    stream=None) -> torch.Tensor:
+                                    stream=None, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Chunked prefill where the query at position p sees keys p - window + 1 .. p
     (window 0: all earlier keys); otherwise as :func:`paged_attn_prefill_chunk`."""
     return _prefill(q, chunk_starts, chunk_lens, k_cache, v_cache, block_tables, context_lens, scale, int(window),
-                    out, max_chunk_len, stream)
+                    out, max_chunk_len, stream, workspace)
+
+
+def prefill_workspace_bytes(num_chunks: int, num_q_heads: int, num_kv_heads: int, max_chunk_len: int) -> int:
+    return int(load_library().pa_prefill_workspace_bytes(num_chunks, num_q_heads, num_kv_heads, max_chunk_len))
+
+
+def alloc_prefill_workspace(num_chunks: int, num_q_heads: int, num_kv_heads: int, max_chunk_len: int,
+                            device=None) -> torch.Tensor:
+    """A zero-filled workspace for the balanced prefill on the current device."""
+    n = prefill_workspace_bytes(num_chunks, num_q_heads, num_kv_heads, max_chunk_len)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def _prefill(q, chunk_starts, chunk_lens, k_cache, v_cache, block_tables, context_lens, scale, window, out,
-             max_chunk_len, stream):
+             max_chunk_len, stream, workspace=None):
     pool = make_pool(k_cache, v_cache)
     _need(q, "q", k_cache.dtype)
     for name, t in (("chunk_starts", chunk_starts), ("chunk_lens", chunk_lens),
@@ -515,7 +537,12 @@ def _prefill(q, chunk_starts, chunk_lens, k_cache, v_cache, block_tables, contex
     args = (q.data_ptr(), chunk_starts.data_ptr(), chunk_lens.data_ptr(), ctypes.byref(pool),
             block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), C, hq, rows,
             int(max_chunk_len), float(scale))
-    if window:
+    if workspace is not None:
+        _need(workspace, "workspace")
+        _check(lib.pa_paged_attn_prefill_chunk_ex(*args, window, out.data_ptr(), workspace.data_ptr(),
+                                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+               "pa_paged_attn_prefill_chunk_ex")
+    elif window:
         _check(lib.pa_paged_attn_prefill_chunk_window(*args, window, out.data_ptr(), _stream(stream)),
                "pa_paged_attn_prefill_chunk_window")
     else:

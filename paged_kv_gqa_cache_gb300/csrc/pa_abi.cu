@@ -526,12 +526,15 @@ pa_status pa_paged_attn_decode_f8(const void *q, int32_t dtype, const pa_kv_pool
                      max_context_len, scale, out, workspace, workspace_bytes, true, stream);
 }
 
-pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t *chunk_starts,
-                                             const int32_t *chunk_lens, const pa_kv_pool *pool,
-                                             const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                             const int32_t *context_lens, int32_t num_chunks, int32_t num_q_heads,
-                                             int32_t total_q_tokens, int32_t max_chunk_len, float scale,
-                                             int32_t window, void *out, pa_stream_t stream) {
+namespace {
+
+// The prefill call; with a workspace (and at most kMaxChunksBalanced chunks)
+// the balanced launch runs, else the plain one.
+pa_status prefill_call(const void *q, const int32_t *chunk_starts, const int32_t *chunk_lens, const pa_kv_pool *pool,
+                       const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                       int32_t num_chunks, int32_t num_q_heads, int32_t total_q_tokens, int32_t max_chunk_len,
+                       float scale, int32_t window, void *out, void *workspace, size_t workspace_bytes,
+                       pa_stream_t stream) {
   pa_status st = check_pool(pool);
   if (st != PA_OK) return st;
   if (num_chunks < 0 || total_q_tokens < 0 || window < 0) return PA_ERR_SHAPE;
@@ -583,10 +586,49 @@ pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t *chunk
         !encode_tensor_map(&omap, map_dtype(pool->dtype), 3, out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return PA_ERR_CUDA;
   }
+  if (workspace && num_chunks <= kMaxChunksBalanced) {
+    if (!aligned16(workspace)) return PA_ERR_ALIGN;
+    if (!prefill_workspace_carve(workspace, workspace_bytes, num_chunks, num_q_heads, pool->num_kv_heads,
+                                 max_chunk_len, d->sm_count, p))
+      return PA_ERR_WORKSPACE;
+  }
   cudaError_t e =
       launch_prefill(p, kmap, vmap, qmap, omap, pool->dtype, group, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+size_t pa_prefill_workspace_bytes(int32_t num_chunks, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t max_chunk_len) {
+  if (num_chunks < 1 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0 ||
+      max_chunk_len < 1 || max_chunk_len > PA_MAX_CHUNK_LEN)
+    return 0;
+  const int sms = sm_count();
+  return prefill_workspace_bytes(num_chunks, num_q_heads, num_kv_heads, max_chunk_len, sms > 0 ? sms : 1);
+}
+
+pa_status pa_paged_attn_prefill_chunk_window(const void *q, const int32_t *chunk_starts,
+                                             const int32_t *chunk_lens, const pa_kv_pool *pool,
+                                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                             const int32_t *context_lens, int32_t num_chunks, int32_t num_q_heads,
+                                             int32_t total_q_tokens, int32_t max_chunk_len, float scale,
+                                             int32_t window, void *out, pa_stream_t stream) {
+  return prefill_call(q, chunk_starts, chunk_lens, pool, block_tables, max_blocks_per_seq, context_lens, num_chunks,
+                      num_q_heads, total_q_tokens, max_chunk_len, scale, window, out, nullptr, 0, stream);
+}
+
+pa_status pa_paged_attn_prefill_chunk_ex(const void *q, const int32_t *chunk_starts, const int32_t *chunk_lens,
+                                         const pa_kv_pool *pool, const int32_t *block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                         int32_t num_chunks, int32_t num_q_heads, int32_t total_q_tokens,
+                                         int32_t max_chunk_len, float scale, int32_t window, void *out,
+                                         void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (!workspace && num_chunks > 0) return PA_ERR_WORKSPACE;
+  return prefill_call(q, chunk_starts, chunk_lens, pool, block_tables, max_blocks_per_seq, context_lens, num_chunks,
+                      num_q_heads, total_q_tokens, max_chunk_len, scale, window, out, workspace, workspace_bytes,
+                      stream);
 }
 
 pa_status pa_paged_attn_prefill_chunk(const void *q, const int32_t *chunk_starts, const int32_t *chunk_lens,

@@ -169,9 +169,23 @@ struct PrefillParams {
   int32_t max_chunk_len;
   int32_t window;            // sliding window in keys (0: none)
   float scale_log2;
+  // balanced (persistent) launch only: a workspace the caller keeps zero-filled
+  // between calls (prefill_workspace_bytes); all null for the plain launch
+  int32_t *ws_counters;      // arrivals per query tile [num_chunks][Hkv][max_tiles]
+  float2 *ws_ml;             // per partial slot and row: (max, sum) of a piece of a split query tile
+  float *ws_o;               // per partial slot, row and dim: that piece's unnormalised output
+  int32_t max_tiles;         // query tiles per chunk and KV head at most: ceil(max_chunk_len / (128 / G))
 };
+// Workspace of the balanced prefill for `sms` CTAs.
+size_t prefill_workspace_bytes(int num_chunks, int num_q_heads, int num_kv_heads, int max_chunk_len, int sms);
+// Carves the workspace into p.ws_* (and sets p.max_tiles); false if it is too small.
+bool prefill_workspace_carve(void *ws, size_t bytes, int num_chunks, int num_q_heads, int num_kv_heads,
+                             int max_chunk_len, int sms, PrefillParams &p);
+// The balanced launch takes at most this many chunks per call.
+constexpr int kMaxChunksBalanced = 256;
 // omap: `out` as the 3-D tensor {dim, query head, token} with qmap's boxes (for
-// the TMA store of whole query tiles).
+// the TMA store of whole query tiles).  With p.ws_counters set the balanced
+// (persistent) kernel runs: one CTA per SM, key tiles dealt evenly.
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
                            const CUtensorMap &qmap, const CUtensorMap &omap, int dtype, int group,
                            cudaStream_t stream);
