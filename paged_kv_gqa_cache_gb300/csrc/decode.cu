@@ -394,6 +394,210 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
   }
 }
 
+// ---- 8-bit pools on the tensor cores ---------------------------------------
+// The split kernel scores int8 / E4M3 pages with mma.sync (m16n8k16, fp16
+// operands, fp32 accumulators): decode's arithmetic is tiny next to its bytes,
+// but per code the CUDA-core path needs a conversion and G multiply-adds,
+// where one packed conversion (E4M3 -> fp16 pair, or int8 -> fp16 pair by a
+// byte permute and one subtraction) feeds the tensor core directly.
+//   S = Q K^T   rows = the G query heads (rows G .. 15 zero), columns = the
+//               16 keys of the page (two n-tiles of 8), k = the 128 dims, in
+//               an order of our choosing: lane (g, t) = (lane / 4, lane % 4)
+//               takes dims 32 t + 4 ks .. 32 t + 4 ks + 3 at k-step ks, so
+//               its K operand is 32 contiguous code bytes of key row g.
+//               Every fp16 product is exact and Q is the 16-bit input times a
+//               power of two (exact while above 2^-14 of its row maximum).
+//   P           the C fragment of S (lane (g, t): head g, keys 2t, 2t + 1,
+//               2t + 8, 2t + 9) is exactly the B fragment the P V product
+//               needs, so P never leaves the registers.  A value's scale
+//               rides on its weight: P'' = P v_scale / R in fp16, with R a
+//               power of two per (sequence, KV head) that moves up (and
+//               rescales the accumulators) whenever a page's largest value
+//               scale exceeds R 2^12, so P'' stays far from fp16 overflow.
+//   O^T += V^T P''^T   rows = dims (m-tile mt, row g -> dim 16 g + 2 mt,
+//               row g + 8 -> dim 16 g + 2 mt + 1), columns = heads, k = the
+//               16 keys: lane (g, t) permutes the bytes of keys 2t, 2t + 1,
+//               2t + 8, 2t + 9 at its 16 dims 16 g .. 16 g + 15 into pairs.
+// At the end of an item lane (g, t) holds heads 2t and 2t + 1 (those below
+// G) at dims 16 g .. 16 g + 15.
+struct Mma8 {
+  float acc[8][4];  // O^T fragments, in units of R
+  float m, l;       // head lane / 4: running maximum (log2 domain), sum of P over this lane's keys
+  float R;          // the item's value-scale unit (a power of two; 0 before the first page)
+};
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Codes 0, 1 (I = 0) or 2, 3 (I = 1) of the word w as an fp16 pair, exactly.
+// int8: the byte c + 128 under the fp16 exponent of 1024 reads 1024 + c + 128;
+// subtracting 1152 leaves c.
+template <bool F8, int I>
+__device__ __forceinline__ uint32_t codes_h2(uint32_t w) {
+  if constexpr (F8) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> (16 * I)), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+  } else {
+    const uint32_t b = __byte_perm(w ^ 0x80808080u, 0x64646464u, I ? 0x4342u : 0x4140u);
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&b), __half2(__half_raw{0x6480}, __half_raw{0x6480}));
+    return *reinterpret_cast<const uint32_t *>(&r);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// The G query rows as the A operand (lane (g, t): head g, dims 32 t .. 32 t +
+// 31, k-step ks in qa[ks]), times 2^e so that the row's largest magnitude
+// lies in [2^14, 2^15); qsc = scale_log2 2^-e.
+template <typename T, int G>
+__device__ __forceinline__ void load_q_mma(const T *qp, float scale_log2, int lane, uint32_t (&qa)[8][2],
+                                           float &qsc) {
+  const int g = lane >> 2, t = lane & 3;
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = 0.f;
+  if (g < G) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(qp + g * kHeadDim + t * 32 + i * 8);
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 v = Pack<T>::to_f2(wd[e]);
+        f[i * 8 + 2 * e] = v.x;
+        f[i * 8 + 2 * e + 1] = v.y;
+      }
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  // e = 14 - floor(log2 amax), kept where 2^e and 2^-e are normal fp32 numbers
+  int e = amax > 0.f ? 14 - (int)((__float_as_uint(amax) >> 23) & 0xff) + 127 : 0;
+  e = max(-120, min(120, e));
+  const float sc = __uint_as_float((uint32_t)(127 + e) << 23);
+  qsc = scale_log2 * __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    qa[ks][0] = pack_h2(f[4 * ks] * sc, f[4 * ks + 1] * sc);
+    qa[ks][1] = pack_h2(f[4 * ks + 2] * sc, f[4 * ks + 3] * sc);
+  }
+}
+
+// One 16-key page of an 8-bit pool (stage layout as load_page<true>): the
+// scores, the online-softmax update and O^T += V^T P''^T; keys nlo .. nv - 1
+// are visible.
+template <int G, bool F8>
+__device__ __forceinline__ void decode_page_mma(const uint8_t *kst, int nlo, int nv, const uint32_t (&qa)[8][2],
+                                                float qsc, Mma8 &st, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint8_t *vst = kst + kQ8V;
+  const float *kscale = reinterpret_cast<const float *>(kst + kQ8KS);
+  const float *vscale = reinterpret_cast<const float *>(kst + kQ8VS);
+
+  // S: this lane's scores of head g for keys 2t, 2t + 1 (n-tile 0) and 2t + 8, 2t + 9 (n-tile 1)
+  float s[4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const uint4 *krow = reinterpret_cast<const uint4 *>(kst + (nt * 8 + g) * kHeadDim + t * 32);
+    const uint4 k0 = krow[0], k1 = krow[1];
+    const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+      const uint32_t b[2] = {codes_h2<F8, 0>(kw[ks]), codes_h2<F8, 1>(kw[ks])};
+      mma_16816(c, a, b);
+    }
+    s[2 * nt] = c[0];
+    s[2 * nt + 1] = c[1];
+  }
+  const float2 ks01 = *reinterpret_cast<const float2 *>(kscale + 2 * t);
+  const float2 ks23 = *reinterpret_cast<const float2 *>(kscale + 8 + 2 * t);
+  const float ksc[4] = {ks01.x, ks01.y, ks23.x, ks23.y};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int key = (i >> 1) * 8 + 2 * t + (i & 1);
+    s[i] = (key >= nlo && key < nv) ? s[i] * (qsc * ksc[i]) : -INFINITY;
+  }
+
+  // online softmax (log2 domain), head g's quad of lanes
+  float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const float mn = fmaxf(st.m, mx);
+  const float base = mn == -INFINITY ? 0.f : mn;  // no visible key yet: every P is 0
+  const float alpha = ex2(st.m - base);            // 0 while nothing was accumulated
+  float p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = ex2(s[i] - base);
+  st.l = st.l * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+  st.m = mn;
+
+  // value scales: the page's largest against R
+  const float2 vs01 = *reinterpret_cast<const float2 *>(vscale + 2 * t);
+  const float2 vs23 = *reinterpret_cast<const float2 *>(vscale + 8 + 2 * t);
+  float vmax = fmaxf(fmaxf(vs01.x, vs01.y), fmaxf(vs23.x, vs23.y));
+  vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+  vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));  // all 16 keys: the same in every lane
+  float rs = 1.f;
+  if (vmax > st.R * 4096.f) {
+    const float Rn = __uint_as_float((__float_as_uint(vmax) + 0x007fffffu) & 0xff800000u);  // 2^ceil(log2 vmax)
+    rs = st.R / Rn;
+    st.R = Rn;
+  }
+  const float invR = __uint_as_float((254u << 23) - __float_as_uint(st.R));  // 1 / R, exact
+  // the accumulators hold heads 2t and 2t + 1: their factors come from those heads' quads
+  const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t) * rs;
+  const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4) * rs;
+  if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      st.acc[mt][0] *= a0;
+      st.acc[mt][1] *= a1;
+      st.acc[mt][2] *= a0;
+      st.acc[mt][3] *= a1;
+    }
+  }
+  uint32_t pb[2] = {pack_h2(p[0] * (vs01.x * invR), p[1] * (vs01.y * invR)),
+                    pack_h2(p[2] * (vs23.x * invR), p[3] * (vs23.y * invR))};
+  if (g >= G) pb[0] = pb[1] = 0u;
+
+  // O^T += V^T P''^T: value rows of keys 2t, 2t + 1, 2t + 8, 2t + 9 at dims 16 g .. 16 g + 15
+  uint4 v0 = *reinterpret_cast<const uint4 *>(vst + (2 * t) * kHeadDim + 16 * g);
+  uint4 v1 = *reinterpret_cast<const uint4 *>(vst + (2 * t + 1) * kHeadDim + 16 * g);
+  uint4 v2 = *reinterpret_cast<const uint4 *>(vst + (2 * t + 8) * kHeadDim + 16 * g);
+  uint4 v3 = *reinterpret_cast<const uint4 *>(vst + (2 * t + 9) * kHeadDim + 16 * g);
+  if (nlo > 0 || nv < kBlock) {  // rows of invisible keys may hold any bytes (an E4M3 NaN): zero them
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    if (2 * t < nlo || 2 * t >= nv) v0 = z;
+    if (2 * t + 1 < nlo || 2 * t + 1 >= nv) v1 = z;
+    if (2 * t + 8 < nlo || 2 * t + 8 >= nv) v2 = z;
+    if (2 * t + 9 < nlo || 2 * t + 9 >= nv) v3 = z;
+  }
+  const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+  const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    // bytes (key a, key b) at dim 16 g + 2 mt, then at dim 16 g + 2 mt + 1
+    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+    const uint32_t x = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
+    const uint32_t y = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
+    const uint32_t a[4] = {codes_h2<F8, 0>(x), codes_h2<F8, 1>(x), codes_h2<F8, 0>(y), codes_h2<F8, 1>(y)};
+    mma_16816(st.acc[mt], a, pb);
+  }
+}
+
 // Warp of the launch whose page range contains global page x, when W warps
 // (W <= P) split P pages as [floor(w P / W), floor((w + 1) P / W)).
 __device__ __forceinline__ int worker_of(int64_t x, int64_t P, int64_t W) {
@@ -477,14 +681,14 @@ __device__ __forceinline__ void merge_item_fused(const DecodeParams &p, int s, i
   if (lane == 0) p.counters[item] = 0;
 }
 
-// int8 pools: more CTAs per SM (the int16 query leaves room) to hide the
-// latency of the heavier per-byte arithmetic; 16-bit pools: as many as fit.
+// 8-bit pools (tensor-core page step, small pages): three CTAs per SM;
+// 16-bit pools: as many as fit.
 template <typename T, int G, bool Q8, bool F8>
-__global__ void __launch_bounds__(NW * 32, (Q8 && !F8) ? (G >= 8 ? 2 : G >= 4 ? 3 : 4) : 1)
+__global__ void __launch_bounds__(NW * 32, Q8 ? 3 : 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const DecodeParams p) {
   using Ly = Layout<G>;
-  constexpr int NQ = Ly::NQ, DPL = Ly::DPL, CPL = Ly::CPL;
+  constexpr int NQ = Ly::NQ, DPL = Ly::DPL;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -528,11 +732,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int64_t x0 = (int64_t)w * P / W;
   const int64_t x1 = (int64_t)(w + 1) * P / W;
   const int64_t npages = x1 - x0;
-
-  // lane roles
-  const int qd = lane % NQ;  // which dim slice of a key this lane scores
-  const int tk = lane / NQ;  // which key of a pass
-  const int rot = tk % CPL;  // chunk rotation of this lane's keys (NT is a multiple of CPL)
 
   Cursor ic = locate(prefix, n, hkv, x0);
   Cursor cc = ic;
@@ -601,10 +800,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   // ---- consumer state ---------------------------------------------------------
   // Packed fp32x2 arithmetic (FFMA2): q and the partial scores pair adjacent
   // dims, the output accumulators pair adjacent dims of one head.
-  QReg<Q8 && !F8> q[G][DPL / 2];
+  // 16-bit pools: the CUDA-core page step's state; 8-bit pools: the tensor-core one's
+  QReg<false> q[G][DPL / 2];
   float qsc[G];
   float2 o[G][2];
   float m[G], l[G];
+  uint32_t qa[8][2];
+  float qsc8 = 0.f;
+  Mma8 st8;
   int ctx = 0, first = 0, lo_in_first = 0;  // first visible page and key of the item
   bool open = false, whole = false;
   const float neg_inf = -INFINITY;
@@ -616,13 +819,22 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       // new item: load its G query rows (pre-scaled into the log2 domain)
       const T *qp = reinterpret_cast<const T *>(p.q) +
                     ((int64_t)cc.s * p.num_q_heads + (int64_t)cc.h * G) * kHeadDim;
-      load_q<T, G, Q8 && !F8>(qp, p.scale_log2, lane, q, qsc);
+      if constexpr (Q8) {
+        load_q_mma<T, G>(qp, p.scale_log2, lane, qa, qsc8);
 #pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        m[gg] = neg_inf;
-        l[gg] = 0.f;
-        o[gg][0] = make_float2(0.f, 0.f);
-        o[gg][1] = make_float2(0.f, 0.f);
+        for (int mt = 0; mt < 8; ++mt) st8.acc[mt][0] = st8.acc[mt][1] = st8.acc[mt][2] = st8.acc[mt][3] = 0.f;
+        st8.m = neg_inf;
+        st8.l = 0.f;
+        st8.R = 0.f;
+      } else {
+        load_q<T, G, false>(qp, p.scale_log2, lane, q, qsc);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          m[gg] = neg_inf;
+          l[gg] = 0.f;
+          o[gg][0] = make_float2(0.f, 0.f);
+          o[gg][1] = make_float2(0.f, 0.f);
+        }
       }
       ctx = __ldg(p.context_lens + cc.s);
       first = window_lo(ctx, p.window) / kBlock;
@@ -649,7 +861,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
           appended = true;
         }
       }
-      decode_page<T, G, Q8, F8>(stages + st * SST, cc.page == 0 ? lo_in_first : 0, nv, q, qsc, o, m, l, pbuf2, lane);
+      if constexpr (Q8)
+        decode_page_mma<G, F8>(stages + st * SST, cc.page == 0 ? lo_in_first : 0, nv, qa, qsc8, st8, lane);
+      else
+        decode_page<T, G, false, false>(stages + st * SST, cc.page == 0 ? lo_in_first : 0, nv, q, qsc, o, m, l,
+                                        pbuf2, lane);
     }
     __syncwarp();  // every lane is done with this stage and with pbuf
     if (appended) fence_proxy_async_smem();  // the generic writes precede the stage's next copy
@@ -660,6 +876,41 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     if (last_of_item || g == npages - 1) {
       const int item = cc.s * hkv + cc.h;
       const bool final_out = whole && last_of_item;
+      if constexpr (Q8) {
+        // lane (gl, tl) holds heads 2 tl and 2 tl + 1 at dims 16 gl .. 16 gl + 15; a head's (m, l) lives
+        // in the quad of lanes 4 head .. 4 head + 3
+        const int gl = lane >> 2, tl = lane & 3;
+        float lq = st8.l;
+        lq += __shfl_xor_sync(FULL, lq, 1);
+        lq += __shfl_xor_sync(FULL, lq, 2);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int hh = 2 * tl + c;
+          const float mh = __shfl_sync(FULL, st8.m, (4 * hh) & 31);
+          const float lh = __shfl_sync(FULL, lq, (4 * hh) & 31);
+          if (hh < G) {
+            if (final_out) {
+              const float f = st8.R / lh;
+              uint32_t pk[8];
+#pragma unroll
+              for (int mt = 0; mt < 8; ++mt) pk[mt] = Pack<T>::from_f2(st8.acc[mt][c] * f, st8.acc[mt][2 + c] * f);
+              uint4 *op = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) +
+                                                    ((int64_t)cc.s * p.num_q_heads + cc.h * G + hh) * kHeadDim +
+                                                    16 * gl);
+              op[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              op[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            } else {
+              const int64_t slot = ((int64_t)item + w) * G + hh;
+              float4 *dst = reinterpret_cast<float4 *>(p.ws_o + slot * kHeadDim + 16 * gl);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_float4(st8.acc[2 * i][c] * st8.R, st8.acc[2 * i][2 + c] * st8.R,
+                                     st8.acc[2 * i + 1][c] * st8.R, st8.acc[2 * i + 1][2 + c] * st8.R);
+              if (gl == 0) *reinterpret_cast<float2 *>(p.ws_ml + slot * 2) = make_float2(mh, lh);
+            }
+          }
+        }
+      } else {
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
         float lt = l[gg];
@@ -679,6 +930,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
               make_float4(o[gg][0].x, o[gg][0].y, o[gg][1].x, o[gg][1].y);
           if (lane == 0) *reinterpret_cast<float2 *>(p.ws_ml + slot * 2) = make_float2(m[gg], lt);
         }
+      }
       }
       if (!final_out && p.counters) {
         // Fused combine: publish this fragment (stores, then a device-scope
@@ -739,7 +991,7 @@ __global__ void __launch_bounds__(kItemWarps * 32, 1)
 decode_item_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                    const DecodeParams p) {
   using Ly = Layout<G>;
-  constexpr int NQ = Ly::NQ, DPL = Ly::DPL, CPL = Ly::CPL;
+  constexpr int NQ = Ly::NQ, DPL = Ly::DPL;
   constexpr int kMerge = 4 + kHeadDim;  // floats per (warp, head): m, l, 2 unused, o[128] (16-byte aligned)
   // full 8 KB stages for int8 too: a larger footprint keeps one CTA per SM, so
   // the two CTAs of an item (and different items) never share an SM's copy engine

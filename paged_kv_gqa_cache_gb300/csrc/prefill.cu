@@ -810,12 +810,15 @@ __device__ __forceinline__ Unit unit_at(int64_t x, int64_t x_end, const int32_t 
   return u;
 }
 
-// CTA owning global pair y when n CTAs split W pairs as [b W / n, (b + 1) W / n).
+// First pair of CTA b when n CTAs split W pairs as [b W / n, (b + 1) W / n)
+// (CTAs b >= n take none), and the CTA owning global pair y.  n is at most W,
+// so no range is empty: every CTA between the first and the last owner of a
+// tile's pairs holds a piece of it (the merge counts them).
+__device__ __forceinline__ int64_t range_start(int b, int64_t W, int n) { return b >= n ? W : (int64_t)b * W / n; }
 __device__ __forceinline__ int owner_of(int64_t y, int64_t W, int n) {
   const int64_t b = ((y + 1) * n + W - 1) / W - 1;
   return (int)(b < n - 1 ? b : n - 1);
 }
-__device__ __forceinline__ int64_t range_start(int b, int64_t W, int n) { return (int64_t)b * W / n; }
 
 template <typename T, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -834,7 +837,7 @@ prefill_balanced_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
   int32_t *rows = reinterpret_cast<int32_t *>(smem + B_OFF_ROW);
   int32_t *misc = reinterpret_cast<int32_t *>(smem + B_OFF_MISC);  // [0..15] scan totals, [16..17] merge flags
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = (int)gridDim.x, b = (int)blockIdx.x;
+  const int b = (int)blockIdx.x;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&kmap);
@@ -915,6 +918,7 @@ prefill_balanced_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
   tc::fence_after_sync();
   const uint32_t tmem = bars.tmem_base;
   const int64_t W = pfx[p.num_chunks];
+  const int nb = W < (int64_t)gridDim.x ? (int)W : (int)gridDim.x;  // CTAs with pairs
   const int64_t x0 = range_start(b, W, nb), x1 = range_start(b + 1, W, nb);
   bool timed_out = false;
 

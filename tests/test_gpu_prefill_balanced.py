@@ -105,6 +105,16 @@ def test_balanced_prefill_sliding_window(window):
     _check(case, f"window {window}", window=window)
 
 
+@pytest.mark.parametrize("start,hq", [(1000, 16), (300, 32), (4000, 8)])
+def test_balanced_prefill_with_fewer_positions_than_sms(start, hq):
+    # one short chunk over a long prefix: fewer work positions than SMs, so
+    # every CTA takes at most one key tile and each query tile is cut into
+    # one piece per key tile, all merged by the last to arrive
+    case = workloads.build_case(f"balanced-few-{start}-{hq}", "bf16", hq, 8, seed=57, device=DEV,
+                                chunks=[(start, 40)])
+    _check(case, f"one 40-token chunk after {start}", calls=2)
+
+
 def test_balanced_prefill_many_small_chunks():
     rng = np.random.default_rng(53)
     chunks = [(int(rng.integers(0, 900)), int(rng.integers(1, 40))) for _ in range(200)]
