@@ -399,7 +399,8 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
 // operands, fp32 accumulators): decode's arithmetic is tiny next to its bytes,
 // but per code the CUDA-core path needs a conversion and G multiply-adds,
 // where one packed conversion (E4M3 -> fp16 pair, or int8 -> fp16 pair by a
-// byte permute and one subtraction) feeds the tensor core directly.
+// byte permute, the offset removed once per score or output, see Mma8)
+// feeds the tensor core directly.
 //   S = Q K^T   rows = the G query heads (rows G .. 15 zero), columns = the
 //               16 keys of the page (two n-tiles of 8), k = the 128 dims, in
 //               an order of our choosing: lane (g, t) = (lane / 4, lane % 4)
@@ -420,33 +421,49 @@ __device__ __forceinline__ void decode_page(const uint8_t *kst, int nlo, int nv,
 //               2t + 8, 2t + 9 at its 16 dims 16 g .. 16 g + 15 into pairs.
 // At the end of an item lane (g, t) holds heads 2t and 2t + 1 (those below
 // G) at dims 16 g .. 16 g + 15.
+// int8 codes enter both products biased, as c + 1152 (the byte permute
+// alone, without the subtraction).  Q K^T then carries 1152 times the query
+// row's sum (subtracted from every score), P V 1152 times the sum of the
+// fp16 weights P'' (ps tracks it, in the same units and with the same
+// rescaling as acc, and the epilogue subtracts it).  |c| <= 127, so the bias
+// is at most 9 times the terms it rides on: the fp32 accumulators keep a
+// score to about 2^-17 of the largest score the row's norm allows (the int16
+// query quantisation of a CUDA-core dot product would give 2^-16), an output
+// to about 2^-21 of its weights' sum.
 struct Mma8 {
   float acc[8][4];  // O^T fragments, in units of R
   float m, l;       // head lane / 4: running maximum (log2 domain), sum of P over this lane's keys
+  float ps;         // int8: sum of this lane's P'' (fp16 values as multiplied), head lane / 4
   float R;          // the item's value-scale unit (a power of two; 0 before the first page)
 };
+constexpr float kQ8Bias = 1152.f;
 
+// (no side effects beyond its outputs: not volatile, so independent products can be interleaved)
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Codes 0, 1 (I = 0) or 2, 3 (I = 1) of the word w as an fp16 pair, exactly.
-// int8: the byte c + 128 under the fp16 exponent of 1024 reads 1024 + c + 128;
-// subtracting 1152 leaves c.
-template <bool F8, int I>
-__device__ __forceinline__ uint32_t codes_h2(uint32_t w) {
-  if constexpr (F8) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> (16 * I)), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
-  } else {
-    const uint32_t b = __byte_perm(w ^ 0x80808080u, 0x64646464u, I ? 0x4342u : 0x4140u);
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&b), __half2(__half_raw{0x6480}, __half_raw{0x6480}));
-    return *reinterpret_cast<const uint32_t *>(&r);
-  }
+// E4M3 codes 0, 1 (I = 0) or 2, 3 (I = 1) of the word w as an fp16 pair,
+// exactly: the hardware conversion of one 16-bit half of w (code 2I into
+// the low fp16).
+template <int I>
+__device__ __forceinline__ uint32_t e4m3_h2(uint32_t w) {
+  uint32_t r;
+  if constexpr (I == 0)
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(r) : "r"(w));
+  else
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}" : "=r"(r) : "r"(w));
+  return r;
+}
+
+// int8 codes 0, 1 (I = 0) or 2, 3 (I = 1) of w as fp16 pairs c + 1152, exactly.
+template <int I>
+__device__ __forceinline__ uint32_t codes_h2_biased(uint32_t w) {
+  return __byte_perm(w ^ 0x80808080u, 0x64646464u, I ? 0x4342u : 0x4140u);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -459,7 +476,7 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 // lies in [2^14, 2^15); qsc = scale_log2 2^-e.
 template <typename T, int G>
 __device__ __forceinline__ void load_q_mma(const T *qp, float scale_log2, int lane, uint32_t (&qa)[8][2],
-                                           float &qsc) {
+                                           float &qsc, float &qbias) {
   const int g = lane >> 2, t = lane & 3;
   float f[32];
 #pragma unroll
@@ -487,11 +504,18 @@ __device__ __forceinline__ void load_q_mma(const T *qp, float scale_log2, int la
   e = max(-120, min(120, e));
   const float sc = __uint_as_float((uint32_t)(127 + e) << 23);
   qsc = scale_log2 * __uint_as_float((uint32_t)(127 - e) << 23);
+  float qs = 0.f;  // the row's sum as the product sees it (the fp16 values)
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     qa[ks][0] = pack_h2(f[4 * ks] * sc, f[4 * ks + 1] * sc);
     qa[ks][1] = pack_h2(f[4 * ks + 2] * sc, f[4 * ks + 3] * sc);
+    const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&qa[ks][0]));
+    const float2 y = __half22float2(*reinterpret_cast<const __half2 *>(&qa[ks][1]));
+    qs += (x.x + x.y) + (y.x + y.y);
   }
+  qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+  qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+  qbias = kQ8Bias * qs;
 }
 
 // One 16-key page of an 8-bit pool (stage layout as load_page<true>): the
@@ -499,36 +523,50 @@ __device__ __forceinline__ void load_q_mma(const T *qp, float scale_log2, int la
 // are visible.
 template <int G, bool F8>
 __device__ __forceinline__ void decode_page_mma(const uint8_t *kst, int nlo, int nv, const uint32_t (&qa)[8][2],
-                                                float qsc, Mma8 &st, int lane) {
+                                                float qsc, float qbias, Mma8 &st, int lane) {
   const int g = lane >> 2, t = lane & 3;
   const uint8_t *vst = kst + kQ8V;
   const float *kscale = reinterpret_cast<const float *>(kst + kQ8KS);
   const float *vscale = reinterpret_cast<const float *>(kst + kQ8VS);
 
-  // S: this lane's scores of head g for keys 2t, 2t + 1 (n-tile 0) and 2t + 8, 2t + 9 (n-tile 1)
-  float s[4];
+  // S: this lane's scores of head g for keys 2t, 2t + 1 (n-tile 0) and 2t + 8, 2t + 9 (n-tile 1);
+  // four independent accumulation chains (n-tile x even / odd k-step)
+  uint32_t kw[2][8];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     const uint4 *krow = reinterpret_cast<const uint4 *>(kst + (nt * 8 + g) * kHeadDim + t * 32);
     const uint4 k0 = krow[0], k1 = krow[1];
-    const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-      const uint32_t b[2] = {codes_h2<F8, 0>(kw[ks]), codes_h2<F8, 1>(kw[ks])};
-      mma_16816(c, a, b);
-    }
-    s[2 * nt] = c[0];
-    s[2 * nt + 1] = c[1];
+    kw[nt][0] = k0.x; kw[nt][1] = k0.y; kw[nt][2] = k0.z; kw[nt][3] = k0.w;
+    kw[nt][4] = k1.x; kw[nt][5] = k1.y; kw[nt][6] = k1.z; kw[nt][7] = k1.w;
   }
+  float c[2][2][4] = {};
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t b[2];
+      if constexpr (F8) {
+        b[0] = e4m3_h2<0>(kw[nt][ks]);
+        b[1] = e4m3_h2<1>(kw[nt][ks]);
+      } else {
+        b[0] = codes_h2_biased<0>(kw[nt][ks]);
+        b[1] = codes_h2_biased<1>(kw[nt][ks]);
+      }
+      mma_16816(c[nt][ks & 1], a, b);
+    }
+  }
+  // (int8 keys entered as c + 1152: the product carries 1152 times the row's sum, qbias)
+  float s[4] = {c[0][0][0] + c[0][1][0] - qbias, c[0][0][1] + c[0][1][1] - qbias, c[1][0][0] + c[1][1][0] - qbias,
+                c[1][0][1] + c[1][1][1] - qbias};
   const float2 ks01 = *reinterpret_cast<const float2 *>(kscale + 2 * t);
   const float2 ks23 = *reinterpret_cast<const float2 *>(kscale + 8 + 2 * t);
   const float ksc[4] = {ks01.x, ks01.y, ks23.x, ks23.y};
+  const bool full = nlo == 0 && nv == kBlock;  // (warp-uniform) every key of the page is visible
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int key = (i >> 1) * 8 + 2 * t + (i & 1);
-    s[i] = (key >= nlo && key < nv) ? s[i] * (qsc * ksc[i]) : -INFINITY;
+    s[i] = (full || (key >= nlo && key < nv)) ? s[i] * (qsc * ksc[i]) : -INFINITY;
   }
 
   // online softmax (log2 domain), head g's quad of lanes
@@ -572,13 +610,18 @@ __device__ __forceinline__ void decode_page_mma(const uint8_t *kst, int nlo, int
   uint32_t pb[2] = {pack_h2(p[0] * (vs01.x * invR), p[1] * (vs01.y * invR)),
                     pack_h2(p[2] * (vs23.x * invR), p[3] * (vs23.y * invR))};
   if (g >= G) pb[0] = pb[1] = 0u;
+  if constexpr (!F8) {  // the weights as the product sees them, for the bias
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&pb[0]));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&pb[1]));
+    st.ps = st.ps * (alpha * rs) + ((f0.x + f0.y) + (f1.x + f1.y));
+  }
 
   // O^T += V^T P''^T: value rows of keys 2t, 2t + 1, 2t + 8, 2t + 9 at dims 16 g .. 16 g + 15
   uint4 v0 = *reinterpret_cast<const uint4 *>(vst + (2 * t) * kHeadDim + 16 * g);
   uint4 v1 = *reinterpret_cast<const uint4 *>(vst + (2 * t + 1) * kHeadDim + 16 * g);
   uint4 v2 = *reinterpret_cast<const uint4 *>(vst + (2 * t + 8) * kHeadDim + 16 * g);
   uint4 v3 = *reinterpret_cast<const uint4 *>(vst + (2 * t + 9) * kHeadDim + 16 * g);
-  if (nlo > 0 || nv < kBlock) {  // rows of invisible keys may hold any bytes (an E4M3 NaN): zero them
+  if (!full) {  // rows of invisible keys may hold any bytes (an E4M3 NaN): zero them
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     if (2 * t < nlo || 2 * t >= nv) v0 = z;
     if (2 * t + 1 < nlo || 2 * t + 1 >= nv) v1 = z;
@@ -593,7 +636,12 @@ __device__ __forceinline__ void decode_page_mma(const uint8_t *kst, int nlo, int
     const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
     const uint32_t x = __byte_perm(w0[mt >> 1], w1[mt >> 1], sel);
     const uint32_t y = __byte_perm(w2[mt >> 1], w3[mt >> 1], sel);
-    const uint32_t a[4] = {codes_h2<F8, 0>(x), codes_h2<F8, 1>(x), codes_h2<F8, 0>(y), codes_h2<F8, 1>(y)};
+    uint32_t a[4];
+    if constexpr (F8) {
+      a[0] = e4m3_h2<0>(x); a[1] = e4m3_h2<1>(x); a[2] = e4m3_h2<0>(y); a[3] = e4m3_h2<1>(y);
+    } else {
+      a[0] = codes_h2_biased<0>(x); a[1] = codes_h2_biased<1>(x); a[2] = codes_h2_biased<0>(y); a[3] = codes_h2_biased<1>(y);
+    }
     mma_16816(st.acc[mt], a, pb);
   }
 }
@@ -806,7 +854,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   float2 o[G][2];
   float m[G], l[G];
   uint32_t qa[8][2];
-  float qsc8 = 0.f;
+  float qsc8 = 0.f, qbias8 = 0.f;
   Mma8 st8;
   int ctx = 0, first = 0, lo_in_first = 0;  // first visible page and key of the item
   bool open = false, whole = false;
@@ -820,11 +868,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       const T *qp = reinterpret_cast<const T *>(p.q) +
                     ((int64_t)cc.s * p.num_q_heads + (int64_t)cc.h * G) * kHeadDim;
       if constexpr (Q8) {
-        load_q_mma<T, G>(qp, p.scale_log2, lane, qa, qsc8);
+        load_q_mma<T, G>(qp, p.scale_log2, lane, qa, qsc8, qbias8);
+        if constexpr (F8) qbias8 = 0.f;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) st8.acc[mt][0] = st8.acc[mt][1] = st8.acc[mt][2] = st8.acc[mt][3] = 0.f;
         st8.m = neg_inf;
         st8.l = 0.f;
+        st8.ps = 0.f;
         st8.R = 0.f;
       } else {
         load_q<T, G, false>(qp, p.scale_log2, lane, q, qsc);
@@ -862,7 +912,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         }
       }
       if constexpr (Q8)
-        decode_page_mma<G, F8>(stages + st * SST, cc.page == 0 ? lo_in_first : 0, nv, qa, qsc8, st8, lane);
+        decode_page_mma<G, F8>(stages + st * SST, cc.page == 0 ? lo_in_first : 0, nv, qa, qsc8, qbias8, st8, lane);
       else
         decode_page<T, G, false, false>(stages + st * SST, cc.page == 0 ? lo_in_first : 0, nv, q, qsc, o, m, l,
                                         pbuf2, lane);
@@ -880,14 +930,22 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
         // lane (gl, tl) holds heads 2 tl and 2 tl + 1 at dims 16 gl .. 16 gl + 15; a head's (m, l) lives
         // in the quad of lanes 4 head .. 4 head + 3
         const int gl = lane >> 2, tl = lane & 3;
-        float lq = st8.l;
+        float lq = st8.l, pq = st8.ps;
         lq += __shfl_xor_sync(FULL, lq, 1);
         lq += __shfl_xor_sync(FULL, lq, 2);
+        pq += __shfl_xor_sync(FULL, pq, 1);
+        pq += __shfl_xor_sync(FULL, pq, 2);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int hh = 2 * tl + c;
           const float mh = __shfl_sync(FULL, st8.m, (4 * hh) & 31);
           const float lh = __shfl_sync(FULL, lq, (4 * hh) & 31);
+          const float bias = F8 ? 0.f : kQ8Bias * __shfl_sync(FULL, pq, (4 * hh) & 31);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            st8.acc[mt][c] -= bias;
+            st8.acc[mt][2 + c] -= bias;
+          }
           if (hh < G) {
             if (final_out) {
               const float f = st8.R / lh;
