@@ -97,6 +97,8 @@ def open_library(path: str):
     lib.oracle_paged_attn_prefill_q8.argtypes = [P, i32, P, P, P, P, i64, i32, i32, i32, P, P, P, i32, P, i32, i32,
                                                  f64, P, i32]
     lib.oracle_paged_attn_prefill_q8.restype = ctypes.c_int
+    lib.oracle_paged_attn_prefill_f8.argtypes = lib.oracle_paged_attn_prefill_q8.argtypes
+    lib.oracle_paged_attn_prefill_f8.restype = ctypes.c_int
     lib.oracle_kv_cache_write_q8.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P, i32, P, i64]
     lib.oracle_kv_cache_write_q8.restype = i64
     lib.oracle_gather_head_q8.argtypes = [P, P, P, P, i64, i32, i32, i32, P, i32, i32, P, P]
@@ -380,6 +382,28 @@ def paged_attn_prefill_q8(q, k_codes, v_codes, k_scale, v_scale, chunk_starts, c
     ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
     out = np.zeros((rows, hq, d), np.float64)
     rc = _load().oracle_paged_attn_prefill_q8(_ptr(qb), dtype, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb, bs, hkv,
+                                              d, _ptr(cs), _ptr(cl), _ptr(bt), bt.shape[1], _ptr(ctx), cs.shape[0],
+                                              hq, float(scale), _ptr(out), num_threads)
+    if rc != 0:
+        raise ValueError(f"oracle prefill rejected its inputs (code {rc})")
+    return out
+
+
+def paged_attn_prefill_f8(q, k_codes, v_codes, k_scale, v_scale, chunk_starts, chunk_lens, block_tables,
+                          context_lens, scale: float, dtype: int, num_threads: int = 0) -> np.ndarray:
+    """fp64 causal chunked prefill over an fp8 (E4M3) pool: keys and values are
+    e4m3 * scale, as in ``paged_attn_decode_f8``."""
+    qb = _bits(q)
+    kc, vc = np.ascontiguousarray(k_codes, np.uint8), np.ascontiguousarray(v_codes, np.uint8)
+    ks, vs = np.ascontiguousarray(k_scale, np.float32), np.ascontiguousarray(v_scale, np.float32)
+    nb, bs, hkv, d = kc.shape
+    rows, hq, dq = qb.shape
+    cs = np.ascontiguousarray(chunk_starts, dtype=np.int32)
+    cl = np.ascontiguousarray(chunk_lens, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros((rows, hq, d), np.float64)
+    rc = _load().oracle_paged_attn_prefill_f8(_ptr(qb), dtype, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb, bs, hkv,
                                               d, _ptr(cs), _ptr(cl), _ptr(bt), bt.shape[1], _ptr(ctx), cs.shape[0],
                                               hq, float(scale), _ptr(out), num_threads)
     if rc != 0:

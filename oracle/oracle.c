@@ -811,6 +811,25 @@ int oracle_paged_attn_prefill_q8(const uint16_t *q, int32_t dtype, const int8_t 
   return prefill_problem(&P, chunk_starts, chunk_lens, context_lens, num_chunks, num_threads);
 }
 
+/* The same chunked prefill on the fp8 (E4M3) pool [P2 sections 5.1, 5.4]:
+ * keys and values are the e4m3 numbers times their scales, as in the fp8 decode. */
+int oracle_paged_attn_prefill_f8(const uint16_t *q, int32_t dtype, const uint8_t *k_cache, const uint8_t *v_cache,
+                                 const float *k_scale, const float *v_scale, int64_t num_blocks,
+                                 int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                 const int32_t *chunk_starts, const int32_t *chunk_lens,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens, int32_t num_chunks, int32_t num_q_heads,
+                                 double scale, double *out, int32_t num_threads) {
+  problem_t P = {q, dtype, NULL, NULL, num_blocks, block_size, num_kv_heads, head_dim,
+                 block_tables, max_blocks_per_seq, num_q_heads, scale, out};
+  P.k8 = (const int8_t *)k_cache;
+  P.v8 = (const int8_t *)v_cache;
+  P.k_scale = k_scale;
+  P.v_scale = v_scale;
+  P.fp8 = 1;
+  return prefill_problem(&P, chunk_starts, chunk_lens, context_lens, num_chunks, num_threads);
+}
+
 static int prefill_problem(problem_t *P, const int32_t *chunk_starts, const int32_t *chunk_lens,
                            const int32_t *context_lens, int32_t num_chunks, int32_t num_threads) {
   const int32_t max_blocks_per_seq = P->max_blocks_per_seq, block_size = P->block_size;

@@ -12,6 +12,9 @@ Each check ties the oracle to something other than itself:
 * the paged layout of codes and scales;
 * decode over the fp8 pool against torch's scaled-dot-product attention on
   the test's own dequantisation of the stored codes;
+* chunked prefill over the fp8 pool against causal SDPA on the same
+  dequantisation, and each chunk's last row against the fp8 decode of its
+  sequence, bit for bit;
 * planted mistakes in mutated copies of the oracle fail this battery.
 """
 import os
@@ -136,6 +139,62 @@ def test_decode_over_fp8_pool_matches_sdpa_on_dequantised_kv(hq, hkv):
     assert _decode_vs_sdpa(hq, hkv, [1, 15, 16, 17, 70], seed=hq + hkv) < 1e-12
 
 
+def _prefill_vs_sdpa(hq, hkv, chunks, seed, dtype=oracle.BF16):
+    """Chunked prefill over an fp8 pool against causal SDPA on the test's own
+    dequantisation (torch's E4M3 decoding times the stored scales); also
+    returns whether each chunk's last row equals the fp8 decode of the same
+    sequence bit for bit."""
+    gen = torch.Generator().manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    tdt = torch.float16 if dtype == oracle.F16 else torch.bfloat16
+    lens = [st + n for st, n in chunks]
+    pages = [-(-n // BS) for n in lens]
+    nb = sum(pages) + 2
+    perm = rng.permutation(nb)
+    bt = np.full((len(lens), max(pages)), -1, np.int32)
+    slots, i = [], 0
+    for s, n in enumerate(lens):
+        for p in range(pages[s]):
+            bt[s, p] = perm[i]
+            i += 1
+        slots.append([int(bt[s, j // BS]) * BS + j % BS for j in range(n)])
+    flat = [x for row in slots for x in row]
+    k = (torch.randn((len(flat), hkv, D), generator=gen) * 2).to(tdt)
+    v = torch.randn((len(flat), hkv, D), generator=gen).to(tdt)
+    k8, v8, ks, vs = _pool(nb, hkv)
+    assert oracle.kv_cache_write_f8(k8, v8, ks, vs, _bits(k), _bits(v), dtype, np.asarray(flat)) == 0
+    rows = sum(n for _, n in chunks)
+    q = torch.randn((rows, hq, D), generator=gen).to(tdt)
+    scale = 1.0 / np.sqrt(D)
+    cs = np.asarray([st for st, _ in chunks], np.int32)
+    cl = np.asarray([n for _, n in chunks], np.int32)
+    ctx = np.asarray(lens, np.int32)
+    out = oracle.paged_attn_prefill_f8(_bits(q), k8, v8, ks, vs, cs, cl, bt, ctx, scale, dtype)
+    worst, r0, same = 0.0, 0, True
+    for c, (st, n) in enumerate(chunks):
+        idx = np.asarray(slots[c])
+        b, o = idx // BS, idx % BS
+        kd = (_torch_decode(k8[b, o]).astype(np.float32) * ks[b, :, o][..., None]).astype(np.float64)
+        vd = (_torch_decode(v8[b, o]).astype(np.float32) * vs[b, :, o][..., None]).astype(np.float64)
+        qq = q[r0:r0 + n].to(torch.float64).permute(1, 0, 2)[None]                  # [1, Hq, n, D]
+        kk = torch.from_numpy(kd).permute(1, 0, 2)[None]                            # [1, Hkv, L, D]
+        vv = torch.from_numpy(vd).permute(1, 0, 2)[None]
+        mask = torch.from_numpy(np.arange(st + n)[None, :] <= (st + np.arange(n))[:, None])
+        ref = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=scale, enable_gqa=True)
+        worst = max(worst, float(np.abs(out[r0:r0 + n] - ref[0].permute(1, 0, 2).numpy()).max()))
+        last = oracle.paged_attn_decode_f8(_bits(q[r0 + n - 1:r0 + n]), k8, v8, ks, vs, bt[c:c + 1], ctx[c:c + 1],
+                                           scale, dtype)
+        same = same and np.array_equal(last[0], out[r0 + n - 1])
+        r0 += n
+    return worst, same
+
+
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (8, 2), (16, 8)])
+def test_prefill_over_fp8_pool_matches_sdpa_and_decode(hq, hkv):
+    worst, same = _prefill_vs_sdpa(hq, hkv, [(0, 20), (17, 33), (100, 9)], seed=hq + 3 * hkv)
+    assert worst < 1e-12 and same
+
+
 # ---- planted mistakes ----------------------------------------------------------------
 
 def _battery():
@@ -151,6 +210,12 @@ def _battery():
             failed.append("decode-sdpa")
     except Exception:
         failed.append("decode-sdpa(raised)")
+    try:
+        worst, same = _prefill_vs_sdpa(4, 2, [(0, 9), (20, 7)], seed=6)
+        if not (worst < 1e-12 and same):
+            failed.append("prefill-sdpa")
+    except Exception:
+        failed.append("prefill-sdpa(raised)")
     return failed
 
 
