@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 8
+#define PA_ABI_VERSION 9
 #define PA_HEAD_DIM 128
 #define PA_BLOCK_SIZE 16
 #define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
@@ -363,6 +363,30 @@ PA_API pa_status pa_paged_attn_decode_q8_ex(const void *q, int32_t dtype, const 
                                             const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                                             int32_t max_context_len, float scale, uint32_t flags, void *out,
                                             void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * paged_attn_prefill_chunk_q8 — [P2 section 5 (KV8Cache: one int8 cache read
+ * by every attention call) and section 5.4 (FP8 KV)]: the causal chunked
+ * prefill of pa_paged_attn_prefill_chunk over an 8-bit pool; every key and
+ * value is the dequantised number code * scale.
+ *   q, out      [total_q_tokens][num_q_heads][128] of `dtype` (PA_F16 or
+ *               PA_BF16; the pool's codes carry no dtype); else PA_ERR_DTYPE.
+ *   codes       PA_CODES_INT8 or PA_CODES_E4M3 (the codes written by
+ *               pa_kv_cache_write_q8 / _f8); else PA_ERR_UNSUPPORTED.
+ * Other arguments, and errors, as pa_paged_attn_prefill_chunk (chunk metadata
+ * and block ids checked on the device; a bad chunk is reported and left
+ * unwritten, a page with a block id outside the pool is reported and
+ * skipped).  No sliding window.  Runs on the mma.sync tensor cores with fp16
+ * operands: codes and the 16-bit query (times a power of two per row) are
+ * exact in fp16, scores and sums fp32; the probabilities, times their values'
+ * scales over a power of two, are rounded to fp16 for the P V product.
+ */
+PA_API pa_status pa_paged_attn_prefill_chunk_q8(const void *q, int32_t dtype, const int32_t *chunk_starts,
+                                                const int32_t *chunk_lens, const pa_kv_pool_q8 *pool, int32_t codes,
+                                                const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                const int32_t *context_lens, int32_t num_chunks,
+                                                int32_t num_q_heads, int32_t total_q_tokens, int32_t max_chunk_len,
+                                                float scale, void *out, pa_stream_t stream);
 
 /*
  * ---- sliding window [P2 section 4 (a ring of capacity W keeps the last W

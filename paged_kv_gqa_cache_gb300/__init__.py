@@ -48,7 +48,7 @@ EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_deco
            "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
            "pa_qk_norm_rope_kv_write", "pa_paged_attn_decode_append", "pa_selftest_bounded_wait",
            "pa_paged_attn_decode_ex", "pa_paged_attn_decode_q8_ex", "pa_prefill_workspace_bytes",
-           "pa_paged_attn_prefill_chunk_ex",
+           "pa_paged_attn_prefill_chunk_ex", "pa_paged_attn_prefill_chunk_q8",
            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
            "pa_allocator_release", "pa_allocator_refcount", "pa_allocator_stats_get", "pa_allocator_take_copies",
            "pa_sequence_create", "pa_sequence_destroy", "pa_sequence_reserve", "pa_sequence_commit",
@@ -142,6 +142,9 @@ def load_library(path: str = LIB_PATH):
         lib.pa_paged_attn_prefill_chunk_ex.argtypes = [P, P, P, pool_p, P, i32, P, i32, i32, i32, i32,
                                                        ctypes.c_float, i32, P, P, ctypes.c_size_t, P]
         lib.pa_paged_attn_prefill_chunk_ex.restype = i32
+        lib.pa_paged_attn_prefill_chunk_q8.argtypes = [P, i32, P, P, q8_p, i32, P, i32, P, i32, i32, i32, i32,
+                                                       ctypes.c_float, P, P]
+        lib.pa_paged_attn_prefill_chunk_q8.restype = i32
         lib.pa_qk_norm_rope_kv_write.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, i32, P, P, i32, i32, P,
                                                  pool_p, P]
         lib.pa_qk_norm_rope_kv_write.restype = i32
@@ -549,6 +552,43 @@ def _prefill(q, chunk_starts, chunk_lens, k_cache, v_cache, block_tables, contex
         _check(lib.pa_paged_attn_prefill_chunk(*args, out.data_ptr(), _stream(stream)),
                "pa_paged_attn_prefill_chunk")
     return out
+
+
+def paged_attn_prefill_chunk_q8(q: torch.Tensor, chunk_starts: torch.Tensor, chunk_lens: torch.Tensor,
+                                k_codes: torch.Tensor, v_codes: torch.Tensor, k_scale: torch.Tensor,
+                                v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                scale: float, out: Optional[torch.Tensor] = None, max_chunk_len: int = 512,
+                                stream=None, _fp8: bool = False) -> torch.Tensor:
+    """Causal chunked-prefill attention over an int8 pool (``pa_paged_attn_prefill_chunk_q8``):
+    q [sum(chunk_lens), Hq, 128] (fp16 / bf16) → out, same dtype."""
+    pool = make_pool_q8(k_codes, v_codes, k_scale, v_scale, torch.uint8 if _fp8 else torch.int8)
+    _need(q, "q")
+    for name, t in (("chunk_starts", chunk_starts), ("chunk_lens", chunk_lens),
+                    ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need(t, name, torch.int32)
+    C = chunk_starts.numel()
+    if chunk_lens.numel() != C or context_lens.numel() != C or block_tables.dim() != 2 \
+            or block_tables.shape[0] != C:
+        raise ValueError("chunk metadata must have one entry (block-table row) per chunk")
+    rows, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype)
+    _check(load_library().pa_paged_attn_prefill_chunk_q8(
+        q.data_ptr(), _dtype_code(q), chunk_starts.data_ptr(), chunk_lens.data_ptr(), ctypes.byref(pool),
+        1 if _fp8 else 0, block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), C, hq, rows,
+        int(max_chunk_len), float(scale), out.data_ptr(), _stream(stream)), "pa_paged_attn_prefill_chunk_q8")
+    return out
+
+
+def paged_attn_prefill_chunk_f8(q: torch.Tensor, chunk_starts: torch.Tensor, chunk_lens: torch.Tensor,
+                                k_codes: torch.Tensor, v_codes: torch.Tensor, k_scale: torch.Tensor,
+                                v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                scale: float, out: Optional[torch.Tensor] = None, max_chunk_len: int = 512,
+                                stream=None) -> torch.Tensor:
+    """Causal chunked-prefill attention over an fp8 (E4M3) pool; as :func:`paged_attn_prefill_chunk_q8`."""
+    return paged_attn_prefill_chunk_q8(q, chunk_starts, chunk_lens, k_codes, v_codes, k_scale, v_scale,
+                                       block_tables, context_lens, scale, out, max_chunk_len, stream, _fp8=True)
 
 
 def selftest_bounded_wait(limit_us: int = 20000, stream=None) -> None:

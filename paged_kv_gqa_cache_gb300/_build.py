@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpagedattn.so")
 
-SOURCES = ["pa_abi.cu", "kv_write.cu", "decode.cu", "prefill.cu", "decode_noalloc.cu", "block_copy.cu",
+SOURCES = ["pa_abi.cu", "kv_write.cu", "decode.cu", "prefill.cu", "prefill8.cu", "decode_noalloc.cu", "block_copy.cu",
            "rope_write.cu", "selftest.cu",
            "allocator.cpp"]
 HEADERS = ["pa_device.cuh", "pa_internal.h", "tcgen05.cuh", "context_cache.h"]

@@ -600,6 +600,56 @@ pa_status prefill_call(const void *q, const int32_t *chunk_starts, const int32_t
 
 }  // namespace
 
+pa_status pa_paged_attn_prefill_chunk_q8(const void *q, int32_t dtype, const int32_t *chunk_starts,
+                                         const int32_t *chunk_lens, const pa_kv_pool_q8 *pool, int32_t codes,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *context_lens, int32_t num_chunks, int32_t num_q_heads,
+                                         int32_t total_q_tokens, int32_t max_chunk_len, float scale, void *out,
+                                         pa_stream_t stream) {
+  pa_status st = check_pool_q8(pool);
+  if (st != PA_OK) return st;
+  if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_DTYPE;
+  if (codes != PA_CODES_INT8 && codes != PA_CODES_E4M3) return PA_ERR_UNSUPPORTED;
+  if (num_chunks < 0 || total_q_tokens < 0) return PA_ERR_SHAPE;
+  if (num_chunks == 0) return PA_OK;
+  if (!q || !chunk_starts || !chunk_lens || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  int group = 0;
+  if ((st = check_group(num_q_heads, pool->num_kv_heads, &group)) != PA_OK) return st;
+  if (max_chunk_len < 1 || max_chunk_len > PA_MAX_CHUNK_LEN || max_blocks_per_seq < 1) return PA_ERR_SHAPE;
+  if (total_q_tokens < 1) return PA_ERR_SHAPE;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(block_tables) || !aligned4(context_lens) ||
+      !aligned4(chunk_starts) || !aligned4(chunk_lens))
+    return PA_ERR_ALIGN;
+  DeviceState *d = nullptr;
+  if ((st = device_state(&d)) != PA_OK) return st;  // also readies the tensor-map encoder
+  CUtensorMap kmap, vmap;
+  if (!pool_map_q8(&kmap, pool, pool->k_cache) || !pool_map_q8(&vmap, pool, pool->v_cache)) return PA_ERR_CUDA;
+  PrefillParams p{};
+  p.q = q;
+  p.k_cache = pool->k_cache;
+  p.v_cache = pool->v_cache;
+  p.k_scale = pool->k_scale;
+  p.v_scale = pool->v_scale;
+  p.chunk_starts = chunk_starts;
+  p.chunk_lens = chunk_lens;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.err = d->err;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_chunks = num_chunks;
+  p.num_kv_heads = pool->num_kv_heads;
+  p.num_q_heads = num_q_heads;
+  p.num_blocks = pool->num_blocks;
+  p.total_q_tokens = total_q_tokens;
+  p.max_chunk_len = max_chunk_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = launch_prefill8(p, kmap, vmap, dtype, group, codes == PA_CODES_E4M3,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 size_t pa_prefill_workspace_bytes(int32_t num_chunks, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t max_chunk_len) {
   if (num_chunks < 1 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0 ||

@@ -169,6 +169,9 @@ struct PrefillParams {
   int32_t max_chunk_len;
   int32_t window;            // sliding window in keys (0: none)
   float scale_log2;
+  // 8-bit pools only: the codes' fp32 scales [num_blocks][Hkv][16]
+  const float *k_scale;
+  const float *v_scale;
   // balanced (persistent) launch only: a workspace the caller keeps zero-filled
   // between calls (prefill_workspace_bytes); all null for the plain launch
   int32_t *ws_counters;      // arrivals per query tile [num_chunks][Hkv][max_tiles]
@@ -189,6 +192,12 @@ constexpr int kMaxChunksBalanced = 256;
 cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
                            const CUtensorMap &qmap, const CUtensorMap &omap, int dtype, int group,
                            cudaStream_t stream);
+
+// Chunked prefill over an 8-bit pool (int8 codes, or E4M3 with f8): kmap /
+// vmap as for the 8-bit decode (one 2 KB box per page of one KV head), the
+// scales in p.k_scale / p.v_scale; q and out of type `dtype`; no window.
+cudaError_t launch_prefill8(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap, int dtype,
+                            int group, bool f8, cudaStream_t stream);
 
 // ---- launch helper ------------------------------------------------------------
 // Launch with programmatic stream serialization (see griddep_wait()).

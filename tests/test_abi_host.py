@@ -57,7 +57,7 @@ def test_only_c_entry_points_are_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 8
+    assert lib.pa_abi_version() == 9
     for code in range(0, -12, -1):
         assert lib.pa_status_string(code).decode().startswith(pa.STATUS[code])
 
@@ -209,6 +209,22 @@ def test_decode_q8_ex_checks_its_arguments(lib):
     assert call(flags=4) == -4
     assert call(dtype=3) == -3
     assert call(codes=1, out=P + 2) == -9 and call(codes=0, out=P + 2) == -9
+
+
+def test_prefill_q8_checks_its_arguments(lib):
+    call = lambda **kw: lib.pa_paged_attn_prefill_chunk_q8(
+        kw.get("q", P), kw.get("dtype", 1), P, P, ctypes.byref(kw.get("pool", _pool_q8())), kw.get("codes", 0), P,
+        128, P, kw.get("C", 3), kw.get("hq", 16), 1536, kw.get("mcl", 512), kw.get("scale", 0.088),
+        kw.get("out", P), None)
+    assert call(C=0) == 0                           # nothing to do
+    assert call(codes=2) == -4 and call(codes=-1) == -4
+    assert call(dtype=3) == -3
+    assert call(C=-1) == -2
+    assert call(hq=12) == -2 and call(hq=24) == -4  # not a multiple of Hkv; a ratio outside {1, 2, 4, 8}
+    assert call(mcl=0) == -2 and call(mcl=513) == -2
+    assert call(scale=float("nan")) == -2
+    assert call(q=0) == -1
+    assert call(q=P + 8) == -9 and call(out=P + 2, codes=1) == -9   # every check before any CUDA call
 
 
 def test_window_calls_check_their_arguments(lib):
