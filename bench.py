@@ -75,8 +75,9 @@ def parse_args(argv=None):
     ap.add_argument("--pools", type=int, default=0,
                     help="distinct layer pools held on the device (0 = the workload's default)")
     ap.add_argument("--kv", choices=["16bit", "int8", "fp8"], default="16bit",
-                    help="decode workloads: the workload's 16-bit pool, or an int8 / fp8 (E4M3) pool (codes + "
-                         "one fp32 scale per token and KV head) holding the same tokens quantised")
+                    help="the workload's 16-bit pool, or an int8 / fp8 (E4M3) pool (codes + one fp32 scale per "
+                         "token and KV head) holding the same tokens quantised (workload 3: the 8-bit write, "
+                         "prefill and decode)")
     ap.add_argument("--append", action="store_true",
                     help="decode workloads: each layer's KV write fused into its decode call "
                          "(paged_attn_decode_append) instead of a separate kv_cache_write")
@@ -461,6 +462,66 @@ class MixedStep:
             self.prefill(l)
 
 
+class MixedStepQ8(MixedStep):
+    """The mixed step over int8 pools, or fp8 E4M3 pools with fp8 ("Модуль 04:
+    KV-кэш и арифметика памяти", sections 5 and 5.4): every position of the
+    two 16-bit layer pools quantised once by the library's own write; per layer
+    the 8-bit write of the 2048 new tokens, the 8-bit prefill of the 3 chunks
+    (pa_paged_attn_prefill_chunk_q8) and the 8-bit decode of the 512 sequences."""
+
+    def __init__(self, device, fp8: bool = False, overlap: bool = False):
+        import numpy as np
+        import torch
+        super().__init__(device, 0, overlap)
+        self.fp8 = fp8
+        pa, c = self.pa, self.case
+        self._write8 = pa.kv_cache_write_f8 if fp8 else pa.kv_cache_write_q8
+        self._prefill8 = pa.paged_attn_prefill_chunk_f8 if fp8 else pa.paged_attn_prefill_chunk_q8
+        self._decode8 = pa.paged_attn_decode_f8 if fp8 else pa.paged_attn_decode_q8
+        slots = []
+        for bt, ctx in ((c.block_tables, c.context_lens), (c.chunk_block_tables, c.chunk_context_lens)):
+            b = bt.cpu().numpy()
+            for s_, n in enumerate(ctx.cpu().numpy()):
+                j = np.arange(int(n))
+                slots.append(b[s_, j // 16].astype(np.int64) * 16 + j % 16)
+        sl = torch.from_numpy(np.unique(np.concatenate(slots))).to(device)
+        alloc = pa.alloc_pool_f8 if fp8 else pa.alloc_pool_q8
+        self.q8 = []
+        for i in range(2):
+            pool = alloc(c.num_blocks, c.hkv, device)
+            self._write8(c.k_cache[i].view(-1, c.hkv, 128)[sl].contiguous(),
+                         c.v_cache[i].view(-1, c.hkv, 128)[sl].contiguous(), sl, *pool)
+            self.q8.append(pool)
+        torch.cuda.synchronize()
+        self.decode_bytes_layer = self.decode_bytes_layer // (2 * c.hkv * 128 * 2) * (c.hkv * (2 * 128 + 2 * 4))
+        self.pool_bytes = sum(t.numel() * t.element_size() for t in self.q8[0])
+
+    def prefill(self, l, qp=None, out=None, meta=None):
+        c, i = self.case, l % 2
+        cs, cl, cbt, cctx = ((c.chunk_starts, c.chunk_lens, c.chunk_block_tables, c.chunk_context_lens)
+                             if meta is None else meta[3:])
+        self._prefill8(c.q_chunks[i] if qp is None else qp, cs, cl, *self.q8[i], cbt, cctx, c.scale,
+                       out=self.out_p[i] if out is None else out, max_chunk_len=512)
+
+    def layer(self, l, q=None, qp=None, kn=None, vn=None, out_d=None, out_p=None, meta=None):
+        import torch
+        c, i = self.case, l % 2
+        main = torch.cuda.current_stream()
+        slots, bt, ctx = (c.slot_mapping, c.block_tables, c.context_lens) if meta is None else meta[:3]
+        self._write8(c.k_new[i] if kn is None else kn, c.v_new[i] if vn is None else vn, slots, *self.q8[i])
+        if self.side is not None:
+            self.side.wait_stream(main)
+            with torch.cuda.stream(self.side):
+                self.prefill(l, qp, out_p, meta)
+        else:
+            self.prefill(l, qp, out_p, meta)
+        self._decode8(c.q[i] if q is None else q, *self.q8[i], bt, ctx, c.scale,
+                      out=self.out_d[i] if out_d is None else out_d, workspace=self.ws,
+                      max_context_len=c.max_context_len)
+        if self.side is not None:
+            main.wait_stream(self.side)
+
+
 def graph_of(fn, reps: int, stream):
     import torch
     fn()                                  # warm once outside capture (kernel attributes, caches)
@@ -684,11 +745,32 @@ def cpu_baseline_mixed(step: MixedStep, seconds: float):
     cs, cl = c.chunk_starts.cpu().numpy(), c.chunk_lens.cpu().numpy()
     cbt, cctx = c.chunk_block_tables.cpu().numpy(), c.chunk_context_lens.cpu().numpy()
     slots = c.slot_mapping.cpu().numpy()
-    hosts = [dict(k=_u16(c.k_cache[i]).copy(), v=_u16(c.v_cache[i]).copy(), kn=_u16(c.k_new[i]),
-                  vn=_u16(c.v_new[i]), q=_u16(c.q[i]), qp=_u16(c.q_chunks[i])) for i in range(2)]
+    q8 = getattr(step, "q8", None)
+    odt = oracle.BF16 if c.dtype == "bf16" else oracle.F16
+    if q8 is not None:
+        hosts = [dict(p8=[t.cpu().numpy().copy() for t in q8[i]], kn=_u16(c.k_new[i]), vn=_u16(c.v_new[i]),
+                      q=_u16(c.q[i]), qp=_u16(c.q_chunks[i])) for i in range(2)]
+        w8 = oracle.kv_cache_write_f8 if step.fp8 else oracle.kv_cache_write_q8
+        p8 = oracle.paged_attn_prefill_f8 if step.fp8 else oracle.paged_attn_prefill_q8
+        d8 = oracle.paged_attn_decode_f8 if step.fp8 else oracle.paged_attn_decode_q8
+    else:
+        hosts = [dict(k=_u16(c.k_cache[i]).copy(), v=_u16(c.v_cache[i]).copy(), kn=_u16(c.k_new[i]),
+                      vn=_u16(c.v_new[i]), q=_u16(c.q[i]), qp=_u16(c.q_chunks[i])) for i in range(2)]
     t_total, t_pre, layers = 0.0, 0.0, 0
     while t_total < seconds:
         x = hosts[layers % 2]
+        if q8 is not None:
+            t0 = time.perf_counter()
+            w8(*x["p8"], x["kn"], x["vn"], odt, slots)
+            t1 = time.perf_counter()
+            p8(x["qp"], *x["p8"], cs, cl, cbt, cctx, c.scale, odt, num_threads=threads)
+            t2 = time.perf_counter()
+            d8(x["q"], *x["p8"], bt, ctx, c.scale, odt, num_threads=threads)
+            t3 = time.perf_counter()
+            t_total += t3 - t0
+            t_pre += t2 - t1
+            layers += 1
+            continue
         t0 = time.perf_counter()
         oracle.kv_cache_write(x["k"], x["v"], x["kn"], x["vn"], slots)
         t1 = time.perf_counter()
@@ -712,7 +794,9 @@ def cpu_baseline_mixed(step: MixedStep, seconds: float):
     return {"value": round(tokens_per_s, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "prefill_tflops": round(layers * step.flops_layer / t_pre / 1e12, 6),
             "sample": f"{layers} of the step's {step.L} layers (write of {step.tokens} tokens, prefill of the 3 "
-                      f"chunks, decode of {len(ctx)} sequences; fp64 C oracle, {threads} threads), "
+                      f"chunks, decode of {len(ctx)} sequences"
+                      + (f", over {'E4M3' if step.fp8 else 'int8'} pools" if q8 is not None else "")
+                      + f"; fp64 C oracle, {threads} threads), "
                       f"{t_total:.2f} s, scaled to the {step.L}-layer step"}
 
 
@@ -804,11 +888,14 @@ def decode_line(args, dev, pa, workload: int, kv: str = "16bit", window: int = 0
     return line
 
 
-def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool = True) -> dict:
-    """The JSON line of the mixed chunked-prefill step (28 layers)."""
+def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool = True, kv: str = "16bit") -> dict:
+    """The JSON line of the mixed chunked-prefill step (28 layers), over 16-bit
+    pools or (kv "int8" / "fp8") 8-bit ones."""
     import torch
     rank, world, _ = dist_env()
-    step = MixedStep(dev, window, overlap, args.fused, balanced=args.balanced_prefill)
+    q8 = kv != "16bit"
+    step = (MixedStepQ8(dev, kv == "fp8", overlap) if q8 else
+            MixedStep(dev, window, overlap, args.fused, balanced=args.balanced_prefill))
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_pre = graph_of(step.run_prefill_only, 1, stream)
@@ -832,10 +919,14 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
         "metric": "mixed chunked-prefill step tokens/s; prefill-chunk TFLOP/s",
         "value": round(world * step.tokens / (ms_step * 1e-3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": (("fp8_e4m3" if step.fp8 else "int8") if q8 else "bf16"), "data": "synthetic",
         "config": {"workload": "Qwen3-0.6B mixed chunked-prefill step, 28 layers: chunks (0,512), (512,512), "
                                "(1536,512) + 512 decode seqs ctx U[16,1024], Hq=16, Hkv=8, d=128, bf16; "
                                "2 distinct pools cycled"
+                               + ((f"; {'fp8 E4M3' if step.fp8 else 'int8'} KV pools (codes + one fp32 scale per "
+                                   "token and KV head): 8-bit write, prefill and decode, bf16 q and out") if q8
+                                  else "")
                                + (f"; sliding window of {window} keys (FLOPs of the visible pairs)" if window else "")
                                + ("; each layer's prefill on a second stream beside its decode" if overlap else "")
                                + ("; prefill balanced over the SMs (pa_paged_attn_prefill_chunk_ex)"
@@ -844,7 +935,7 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
                                   if step.fused else ""),
                    "global_batch": 515 * world, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (2 pools of {:.0f} MiB cycled over 28 layers)".format(
-                       2 * step.case.k_cache[0].numel() * 2 / 2**20),
+                       (step.pool_bytes if q8 else 2 * step.case.k_cache[0].numel() * 2) / 2**20),
                    "timing": "CUDA events around K replays of a CUDA graph of one step, repeated; median repeat"},
         "timing": timing_summary(reps, args.steps),
         "decode_kv_gbs": round(step.L * step.decode_bytes_layer / (ms_step * 1e-3) / 1e9, 1),
@@ -853,12 +944,15 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(tflops / bf16, 3), "peak_kind": peak_kind,
-                     "kernel": "paged_attn_prefill_chunk" + ("_ex (balanced)" if step.pws is not None else "")
+                     "kernel": (f"paged_attn_prefill_chunk_q8 ({'E4M3' if step.fp8 else 'int8'} pool, mma.sync)"
+                                if q8 else "paged_attn_prefill_chunk" + ("_ex (balanced)" if step.pws is not None
+                                                                         else ""))
                                + (f" window W={window}" if window else "") + " per layer",
                      "flops_per_launch": step.flops_layer,
                      "launch_ms": round(ms_pre, 5), "launches_timed": step.L * args.steps * len(pre_reps),
-                     "traffic": committed_traffic("prefill.cu", f"prefill{f'_window{window}' if window else ''}"
-                                                                f"_workload3.md")},
+                     "traffic": (committed_traffic("prefill8.cu", f"prefill8_{kv}_workload3.md") if q8 else
+                                 committed_traffic("prefill.cu", f"prefill{f'_window{window}' if window else ''}"
+                                                                 f"_workload3.md"))},
         "clocks": clk.summary(),
     }
     if rank == 0 and cpu and not args.no_cpu_baseline:
@@ -883,14 +977,20 @@ def run_ours(args):
     if args.fused_write:
         return run_fused_write(args, dev, pa)
     if args.workload == 3:
-        line = mixed_line(args, dev, pa, args.window, args.overlap)
+        line = mixed_line(args, dev, pa, args.window, args.overlap, kv=args.kv)
     else:
         line = decode_line(args, dev, pa, args.workload, args.kv, args.window, args.append, args.early_pages,
                            args.pools)
     if args.sublines:
         line["prefill"] = mixed_line(args, dev, pa, overlap=True)
         line["decode_0_6b"] = decode_line(args, dev, pa, 2, early_pages=args.early_pages)
-        line["gpu_launches_sublines"] = line["prefill"]["gpu_launches"] + line["decode_0_6b"]["gpu_launches"]
+        # the 8-bit pools: the 8B decode layer over int8 and E4M3 codes, the mixed step over int8 codes
+        line["decode_8b_int8"] = decode_line(args, dev, pa, 4, kv="int8", early_pages=args.early_pages, pools=4)
+        line["decode_8b_fp8"] = decode_line(args, dev, pa, 4, kv="fp8", early_pages=args.early_pages, pools=4)
+        line["prefill_int8"] = mixed_line(args, dev, pa, kv="int8")
+        line["gpu_launches_sublines"] = sum(line[k]["gpu_launches"] for k in
+                                            ("prefill", "decode_0_6b", "decode_8b_int8", "decode_8b_fp8",
+                                             "prefill_int8"))
     if rank == 0:
         print(json.dumps(line), flush=True)
 

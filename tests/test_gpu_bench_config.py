@@ -85,6 +85,50 @@ def test_mixed_step_as_benchmarked():
         check_close(step.out_d[i], refd, f"mixed step decode, pool {i}")
 
 
+def _same_pool(gpu, host, what):
+    for g, h, name in zip(gpu, host, ("k codes", "v codes", "k scales", "v scales")):
+        gn = g.cpu().numpy()
+        ok = np.array_equal(gn.view(np.uint32), h.view(np.uint32)) if gn.dtype == np.float32 else \
+            np.array_equal(gn.view(np.uint8), h.view(np.uint8))
+        assert ok, f"{what}: {name} differ from the oracle's"
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_mixed_step_over_8bit_pools_as_benchmarked(fp8):
+    step = bench.MixedStepQ8(DEV, fp8=fp8, overlap=True)   # 8-bit write, prefill and decode per layer
+    c = step.case
+    BS = 16
+    slots = []
+    for bt, ctx in ((c.block_tables, c.context_lens), (c.chunk_block_tables, c.chunk_context_lens)):
+        b = bt.cpu().numpy()
+        for s_, n in enumerate(ctx.cpu().numpy()):
+            j = np.arange(int(n))
+            slots.append(b[s_, j // BS].astype(np.int64) * BS + j % BS)
+    slots = np.unique(np.concatenate(slots))
+    write = oracle.kv_cache_write_f8 if fp8 else oracle.kv_cache_write_q8
+    code_t = np.uint8 if fp8 else np.int8
+    hosts = []
+    for i in range(2):   # the oracle's own pools, quantised from the same 16-bit rows
+        h = (np.zeros((c.num_blocks, BS, c.hkv, 128), code_t), np.zeros((c.num_blocks, BS, c.hkv, 128), code_t),
+             np.zeros((c.num_blocks, c.hkv, BS), np.float32), np.zeros((c.num_blocks, c.hkv, BS), np.float32))
+        rows = lambda t: bits(t[i]).reshape(-1, c.hkv, 128)[slots]
+        assert write(*h, rows(c.k_cache), rows(c.v_cache), oracle.BF16, slots) == 0
+        _same_pool(step.q8[i], h, f"pool {i} before the step")
+        hosts.append(h)
+    _replay(step.run)
+    pre = oracle.paged_attn_prefill_f8 if fp8 else oracle.paged_attn_prefill_q8
+    dec = oracle.paged_attn_decode_f8 if fp8 else oracle.paged_attn_decode_q8
+    for i, h in enumerate(hosts):
+        assert write(*h, bits(c.k_new[i]), bits(c.v_new[i]), oracle.BF16, c.slot_mapping.cpu().numpy()) == 0
+        _same_pool(step.q8[i], h, f"pool {i} after the step")
+        refp = pre(bits(c.q_chunks[i]), *h, c.chunk_starts.cpu().numpy(), c.chunk_lens.cpu().numpy(),
+                   c.chunk_block_tables.cpu().numpy(), c.chunk_context_lens.cpu().numpy(), c.scale, oracle.BF16)
+        check_close(step.out_p[i], refp, f"8-bit mixed step prefill, pool {i}")
+        refd = dec(bits(c.q[i]), *h, c.block_tables.cpu().numpy(), c.context_lens.cpu().numpy(), c.scale,
+                   oracle.BF16)
+        check_close(step.out_d[i], refd, f"8-bit mixed step decode, pool {i}")
+
+
 @pytest.mark.parametrize("append", [False, True])
 def test_end_to_end_path_returns_the_right_outputs_to_the_host(append):
     # the e2e leg: inputs copied from pinned host memory each step, the library
