@@ -237,13 +237,15 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def committed_traffic(kernel_source: str, summary_name: str):
+def committed_traffic(kernel_sources, summary_name: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (the summary records the source's sha256)."""
+    the current kernel source: the summary records the sha256 of the source
+    files (one name, or a tuple whose contents are hashed in that order)."""
     path = os.path.join(ROOT, "profiles", summary_name)
+    names = (kernel_sources,) if isinstance(kernel_sources, str) else tuple(kernel_sources)
     try:
         text = open(path).read()
-        src = open(os.path.join(ROOT, "paged_kv_gqa_cache_gb300", "csrc", kernel_source), "rb").read()
+        src = b"".join(open(os.path.join(ROOT, "paged_kv_gqa_cache_gb300", "csrc", n), "rb").read() for n in names)
     except OSError:
         return None
     want = hashlib.sha256(src).hexdigest()[:16]
@@ -944,15 +946,16 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": bf16, "unit": "TFLOP/s",
                      "frac": round(tflops / bf16, 3), "peak_kind": peak_kind,
-                     "kernel": (f"paged_attn_prefill_chunk_q8 ({'E4M3' if step.fp8 else 'int8'} pool, mma.sync)"
+                     "kernel": (f"paged_attn_prefill_chunk_q8 ({'E4M3' if step.fp8 else 'int8'} pool, tcgen05)"
                                 if q8 else "paged_attn_prefill_chunk" + ("_ex (balanced)" if step.pws is not None
                                                                          else ""))
                                + (f" window W={window}" if window else "") + " per layer",
                      "flops_per_launch": step.flops_layer,
                      "launch_ms": round(ms_pre, 5), "launches_timed": step.L * args.steps * len(pre_reps),
-                     "traffic": (committed_traffic("prefill8.cu", f"prefill8_{kv}_workload3.md") if q8 else
-                                 committed_traffic("prefill.cu", f"prefill{f'_window{window}' if window else ''}"
-                                                                 f"_workload3.md"))},
+                     "traffic": (committed_traffic(("prefill8.cu", "prefill_kernel.cuh"), f"prefill8_{kv}_workload3.md")
+                                 if q8 else
+                                 committed_traffic(("prefill.cu", "prefill_kernel.cuh"),
+                                                   f"prefill{f'_window{window}' if window else ''}_workload3.md"))},
         "clocks": clk.summary(),
     }
     if rank == 0 and cpu and not args.no_cpu_baseline:

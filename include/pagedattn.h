@@ -376,10 +376,12 @@ PA_API pa_status pa_paged_attn_decode_q8_ex(const void *q, int32_t dtype, const 
  * Other arguments, and errors, as pa_paged_attn_prefill_chunk (chunk metadata
  * and block ids checked on the device; a bad chunk is reported and left
  * unwritten, a page with a block id outside the pool is reported and
- * skipped).  No sliding window.  Runs on the mma.sync tensor cores with fp16
- * operands: codes and the 16-bit query (times a power of two per row) are
- * exact in fp16, scores and sums fp32; the probabilities, times their values'
- * scales over a power of two, are rounded to fp16 for the P V product.
+ * skipped).  No sliding window.  Runs on the tcgen05 tensor cores with fp16
+ * operands: each key and value code * scale is rounded once to fp16 in shared
+ * memory; a bf16 query is exact in fp16 after scaling each row by a power of
+ * two (an fp16 query is used as is); scores and sums fp32, the probabilities
+ * rounded to fp16 for the P V product, the output in `dtype`.  A dequantised
+ * key or value beyond the fp16 range (65504) saturates to it.
  */
 PA_API pa_status pa_paged_attn_prefill_chunk_q8(const void *q, int32_t dtype, const int32_t *chunk_starts,
                                                 const int32_t *chunk_lens, const pa_kv_pool_q8 *pool, int32_t codes,

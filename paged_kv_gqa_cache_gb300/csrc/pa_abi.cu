@@ -530,6 +530,18 @@ namespace {
 
 // The prefill call; with a workspace (and at most kMaxChunksBalanced chunks)
 // the balanced launch runs, else the plain one.
+// q (and out) as a 3-D tensor {dim, query head, token}; boxes of {64 dims,
+// G heads, 128/G tokens} give 128 rows (token-major, head-minor) of 128 bytes.
+bool query_maps(CUtensorMap *qmap, CUtensorMap *omap, const void *q, void *out, int dtype, int num_q_heads,
+                int total_q_tokens, int group) {
+  const uint64_t dims[3] = {(uint64_t)kHeadDim, (uint64_t)num_q_heads, (uint64_t)total_q_tokens};
+  const uint64_t strides[2] = {kHeadDim * 2ull, (uint64_t)num_q_heads * kHeadDim * 2ull};
+  const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)(128 / group)};
+  return encode_tensor_map(qmap, map_dtype(dtype), 3, const_cast<void *>(q), dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_tensor_map(omap, map_dtype(dtype), 3, out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 pa_status prefill_call(const void *q, const int32_t *chunk_starts, const int32_t *chunk_lens, const pa_kv_pool *pool,
                        const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                        int32_t num_chunks, int32_t num_q_heads, int32_t total_q_tokens, int32_t max_chunk_len,
@@ -571,21 +583,10 @@ pa_status prefill_call(const void *q, const int32_t *chunk_starts, const int32_t
   p.window = window;
   p.scale_log2 = scale * 1.4426950408889634f;
 
-  CUtensorMap kmap, vmap, qmap;
-  if (!pool_map(&kmap, pool, pool->k_cache, false) || !pool_map_vpages(&vmap, pool, pool->v_cache))
+  CUtensorMap kmap, vmap, qmap, omap;
+  if (!pool_map(&kmap, pool, pool->k_cache, false) || !pool_map_vpages(&vmap, pool, pool->v_cache) ||
+      !query_maps(&qmap, &omap, q, out, pool->dtype, num_q_heads, total_q_tokens, group))
     return PA_ERR_CUDA;
-  // q (and out) as a 3-D tensor {dim, query head, token}; boxes of {64 dims,
-  // G heads, 128/G tokens} give 128 rows (token-major, head-minor) of 128 bytes.
-  CUtensorMap omap;
-  {
-    const uint64_t dims[3] = {(uint64_t)kHeadDim, (uint64_t)num_q_heads, (uint64_t)total_q_tokens};
-    const uint64_t strides[2] = {kHeadDim * 2ull, (uint64_t)num_q_heads * kHeadDim * 2ull};
-    const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)(128 / group)};
-    if (!encode_tensor_map(&qmap, map_dtype(pool->dtype), 3, const_cast<void *>(q), dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map(&omap, map_dtype(pool->dtype), 3, out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return PA_ERR_CUDA;
-  }
   if (workspace && num_chunks <= kMaxChunksBalanced) {
     if (!aligned16(workspace)) return PA_ERR_ALIGN;
     if (!prefill_workspace_carve(workspace, workspace_bytes, num_chunks, num_q_heads, pool->num_kv_heads,
@@ -623,8 +624,10 @@ pa_status pa_paged_attn_prefill_chunk_q8(const void *q, int32_t dtype, const int
     return PA_ERR_ALIGN;
   DeviceState *d = nullptr;
   if ((st = device_state(&d)) != PA_OK) return st;  // also readies the tensor-map encoder
-  CUtensorMap kmap, vmap;
-  if (!pool_map_q8(&kmap, pool, pool->k_cache) || !pool_map_q8(&vmap, pool, pool->v_cache)) return PA_ERR_CUDA;
+  CUtensorMap kmap, vmap, qmap, omap;
+  if (!pool_map_q8(&kmap, pool, pool->k_cache) || !pool_map_q8(&vmap, pool, pool->v_cache) ||
+      !query_maps(&qmap, &omap, q, out, dtype, num_q_heads, total_q_tokens, group))
+    return PA_ERR_CUDA;
   PrefillParams p{};
   p.q = q;
   p.k_cache = pool->k_cache;
@@ -645,7 +648,7 @@ pa_status pa_paged_attn_prefill_chunk_q8(const void *q, int32_t dtype, const int
   p.total_q_tokens = total_q_tokens;
   p.max_chunk_len = max_chunk_len;
   p.scale_log2 = scale * 1.4426950408889634f;
-  cudaError_t e = launch_prefill8(p, kmap, vmap, dtype, group, codes == PA_CODES_E4M3,
+  cudaError_t e = launch_prefill8(p, kmap, vmap, qmap, omap, dtype, group, codes == PA_CODES_E4M3,
                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }

@@ -193,11 +193,13 @@ cudaError_t launch_prefill(const PrefillParams &p, const CUtensorMap &kmap, cons
                            const CUtensorMap &qmap, const CUtensorMap &omap, int dtype, int group,
                            cudaStream_t stream);
 
-// Chunked prefill over an 8-bit pool (int8 codes, or E4M3 with f8): kmap /
-// vmap as for the 8-bit decode (one 2 KB box per page of one KV head), the
-// scales in p.k_scale / p.v_scale; q and out of type `dtype`; no window.
-cudaError_t launch_prefill8(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap, int dtype,
-                            int group, bool f8, cudaStream_t stream);
+// Chunked prefill over an 8-bit pool (int8 codes, or E4M3 with f8) on the
+// tcgen05 tensor cores: kmap / vmap as for the 8-bit decode (one 2 KB box per
+// page of one KV head), the scales in p.k_scale / p.v_scale, qmap / omap as
+// for launch_prefill; q and out of type `dtype`; no window, no workspace.
+cudaError_t launch_prefill8(const PrefillParams &p, const CUtensorMap &kmap, const CUtensorMap &vmap,
+                            const CUtensorMap &qmap, const CUtensorMap &omap, int dtype, int group, bool f8,
+                            cudaStream_t stream);
 
 // ---- launch helper ------------------------------------------------------------
 // Launch with programmatic stream serialization (see griddep_wait()).
