@@ -95,6 +95,9 @@ def parse_args(argv=None):
                          "(pa_paged_attn_prefill_chunk_window)")
     ap.add_argument("--overlap", action="store_true",
                     help="workload 3: each layer's prefill on a second stream beside its decode (same work)")
+    ap.add_argument("--persistent-mixed", action="store_true",
+                    help="workload 3 (16-bit pools, no window): each layer as ONE persistent launch "
+                         "(pa_mixed_step: the write, then the prefill beside the decode on SMs split by their work)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window of W keys for the attention calls of workloads 2, 3 and 4 (0 = none); "
                          "the bytes or FLOPs counted are those of the visible keys")
@@ -403,11 +406,14 @@ class MixedStep:
     kv_cache_write of 2048 new tokens, prefill of 3 chunks of 512 (prefixes 0,
     512, 1536) and decode of 512 sequences; 2 distinct pools cycled over 28."""
 
-    def __init__(self, device, window: int = 0, overlap: bool = False, fused: bool = False, balanced: bool = False):
+    def __init__(self, device, window: int = 0, overlap: bool = False, fused: bool = False, balanced: bool = False,
+                 persistent: bool = False):
         import torch
         import paged_kv_gqa_cache_gb300 as pa
         import workloads
         self.pa, self.L, self.window, self.overlap, self.fused = pa, 28, window, overlap, fused
+        # persistent: each layer is ONE launch (pa_mixed_step): the write, then the prefill beside the decode
+        self.persistent = persistent and not window
         # overlap: each layer's prefill (tensor-bound) runs on a second stream beside its decode (HBM-bound)
         self.side = torch.cuda.Stream(device=device) if overlap else None
         self.case = c = workloads.qwen3_0_6b_mixed_step(device=device, n_layers=2, nan_fill=False)
@@ -423,6 +429,10 @@ class MixedStep:
         self.decode_bytes_layer = workloads.decode_kv_bytes([min(n, window) if window else n for n in lens], c.hkv)
         self.kernels_per_layer = 2 + (1 if fused else pa.decode_kernel_launches(len(lens), c.hkv, c.max_context_len,
                                                                                 window))
+        if self.persistent:  # the new tokens: the chunks' first, then one per decoding sequence
+            self.mws = pa.alloc_mixed_step_workspace(len(lens), c.hq, c.hkv, device)
+            self.chunk_tokens = sum(n for _, n in c.meta["chunks"])
+            self.kernels_per_layer = 1
 
     def prefill(self, l, qp=None, out=None, meta=None):
         c, i = self.case, l % 2
@@ -440,6 +450,17 @@ class MixedStep:
         c, i = self.case, l % 2
         main = torch.cuda.current_stream()
         slots, bt, ctx = (c.slot_mapping, c.block_tables, c.context_lens) if meta is None else meta[:3]
+        if self.persistent:
+            cs, cl, cbt, cctx = ((c.chunk_starts, c.chunk_lens, c.chunk_block_tables, c.chunk_context_lens)
+                                 if meta is None else meta[3:])
+            kn, vn, tc = c.k_new[i] if kn is None else kn, c.v_new[i] if vn is None else vn, self.chunk_tokens
+            self.pa.mixed_step(c.k_cache[i], c.v_cache[i], c.scale, self.mws, k_chunks=kn[:tc], v_chunks=vn[:tc],
+                               chunk_slots=slots[:tc], q_chunks=c.q_chunks[i] if qp is None else qp, chunk_starts=cs,
+                               chunk_lens=cl, chunk_block_tables=cbt, chunk_context_lens=cctx,
+                               q=c.q[i] if q is None else q, k_dec=kn[tc:], v_dec=vn[tc:], block_tables=bt,
+                               context_lens=ctx, out_chunks=self.out_p[i] if out_p is None else out_p,
+                               out=self.out_d[i] if out_d is None else out_d, max_chunk_len=512)
+            return
         self.pa.kv_cache_write(c.k_new[i] if kn is None else kn, c.v_new[i] if vn is None else vn, slots,
                                c.k_cache[i], c.v_cache[i])
         if self.side is not None:  # fork after the write, join before the next layer's write
@@ -897,7 +918,8 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
     rank, world, _ = dist_env()
     q8 = kv != "16bit"
     step = (MixedStepQ8(dev, kv == "fp8", overlap) if q8 else
-            MixedStep(dev, window, overlap, args.fused, balanced=args.balanced_prefill))
+            MixedStep(dev, window, overlap, args.fused, balanced=args.balanced_prefill,
+                      persistent=args.persistent_mixed))
     stream = torch.cuda.Stream(device=dev)
     g_step = graph_of(step.run, 1, stream)
     g_pre = graph_of(step.run_prefill_only, 1, stream)
@@ -930,7 +952,11 @@ def mixed_line(args, dev, pa, window: int = 0, overlap: bool = False, cpu: bool 
                                    "token and KV head): 8-bit write, prefill and decode, bf16 q and out") if q8
                                   else "")
                                + (f"; sliding window of {window} keys (FLOPs of the visible pairs)" if window else "")
-                               + ("; each layer's prefill on a second stream beside its decode" if overlap else "")
+                               + ("; each layer's prefill on a second stream beside its decode"
+                                  if overlap and not getattr(step, "persistent", False) else "")
+                               + ("; each layer as one persistent launch (pa_mixed_step: the chunks' write, then "
+                                  "their prefill, beside the decode that appends the sequences' new tokens)"
+                                  if getattr(step, "persistent", False) else "")
                                + ("; prefill balanced over the SMs (pa_paged_attn_prefill_chunk_ex)"
                                   if step.pws is not None else "")
                                + ("; decode as one launch over all SMs (PA_DECODE_ZEROED_WORKSPACE)"

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 9
+#define PA_ABI_VERSION 10
 #define PA_HEAD_DIM 128
 #define PA_BLOCK_SIZE 16
 #define PA_MAX_CHUNK_LEN 512 /* [P1] scheduler task 12.4: prefill chunks of at most 512 tokens */
@@ -389,6 +389,54 @@ PA_API pa_status pa_paged_attn_prefill_chunk_q8(const void *q, int32_t dtype, co
                                                 const int32_t *context_lens, int32_t num_chunks,
                                                 int32_t num_q_heads, int32_t total_q_tokens, int32_t max_chunk_len,
                                                 float scale, void *out, pa_stream_t stream);
+
+/*
+ * mixed_step — [P2 section 3.4 (a step that prefills chunks of new prompts
+ * while running sequences decode one token each, the chunks reading their
+ * cached prefix); P1 "Куда расти" (production engines fuse the step into
+ * dedicated kernels)]: a whole mixed step over a 16-bit pool in ONE
+ * persistent launch (one CTA per SM, launched cooperatively), its SMs split
+ * between the chunks and the sequences by their work:
+ *   chunks      the KV write of the chunks' num_chunk_tokens new tokens,
+ *               exactly as pa_kv_cache_write (k_chunks, v_chunks
+ *               [num_chunk_tokens][Hkv][128] of the pool's dtype, chunk_slots
+ *               int64; a bad slot is reported and skipped), then, once every
+ *               such row is written (a barrier of the prefill CTAs, bounded:
+ *               PA_ERR_TIMEOUT), the chunked prefill of
+ *               pa_paged_attn_prefill_chunk (q_chunks, chunk_starts,
+ *               chunk_lens, chunk_block_tables [num_chunks][chunk_max_blocks],
+ *               chunk_context_lens, total_q_tokens, max_chunk_len, out_chunks;
+ *               num_chunks <= 256, no window);
+ *   sequences   the decode of pa_paged_attn_decode_append (q, k_dec, v_dec
+ *               [num_seqs][Hkv][128]: each sequence's new token, written at
+ *               position context_lens[s] - 1 by the decode as it reads that
+ *               page; k_dec = v_dec = NULL: the new tokens are already in the
+ *               pool; block_tables [num_seqs][max_blocks_per_seq],
+ *               context_lens, out; num_seqs <= 6000), which does not wait for
+ *               the chunks' write.  No chunk may read a page that holds a
+ *               sequence's new token.
+ * Either part may be empty (num_chunks = num_chunk_tokens = 0, or num_seqs =
+ * 0; its pointers are then not read).  Results as the separate calls (the
+ * chunks' write first).
+ *   workspace   pa_mixed_step_workspace_bytes(num_seqs, num_q_heads,
+ *               num_kv_heads) bytes, 16-byte aligned, zero-filled before its
+ *               first use; every call that completes without PA_ERR_TIMEOUT
+ *               leaves its counters zero again, so it needs no clearing
+ *               between calls.  After a PA_ERR_TIMEOUT, zero-fill it again.
+ *               Missing or too small: PA_ERR_WORKSPACE.
+ * Other checks and errors as the separate calls.  No counterpart on the
+ * pages: a library addition.
+ */
+PA_API size_t pa_mixed_step_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads);
+PA_API pa_status pa_mixed_step(const pa_kv_pool *pool, int32_t num_q_heads, float scale, const void *k_chunks,
+                               const void *v_chunks, const int64_t *chunk_slots, int32_t num_chunk_tokens,
+                               const void *q_chunks, const int32_t *chunk_starts, const int32_t *chunk_lens,
+                               const int32_t *chunk_block_tables, int32_t chunk_max_blocks,
+                               const int32_t *chunk_context_lens, int32_t num_chunks, int32_t total_q_tokens,
+                               int32_t max_chunk_len, void *out_chunks, const void *q, const void *k_dec,
+                               const void *v_dec, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                               const int32_t *context_lens, int32_t num_seqs, void *out, void *workspace,
+                               size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * ---- sliding window [P2 section 4 (a ring of capacity W keeps the last W

@@ -48,7 +48,8 @@ EXPORTS = ("pa_kv_cache_write", "pa_decode_workspace_bytes", "pa_paged_attn_deco
            "pa_paged_attn_decode_window", "pa_paged_attn_prefill_chunk_window", "pa_kv_block_copy",
            "pa_qk_norm_rope_kv_write", "pa_paged_attn_decode_append", "pa_selftest_bounded_wait",
            "pa_paged_attn_decode_ex", "pa_paged_attn_decode_q8_ex", "pa_prefill_workspace_bytes",
-           "pa_paged_attn_prefill_chunk_ex", "pa_paged_attn_prefill_chunk_q8",
+           "pa_paged_attn_prefill_chunk_ex", "pa_paged_attn_prefill_chunk_q8", "pa_mixed_step",
+           "pa_mixed_step_workspace_bytes",
            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate", "pa_allocator_retain",
            "pa_allocator_release", "pa_allocator_refcount", "pa_allocator_stats_get", "pa_allocator_take_copies",
            "pa_sequence_create", "pa_sequence_destroy", "pa_sequence_reserve", "pa_sequence_commit",
@@ -168,6 +169,12 @@ def load_library(path: str = LIB_PATH):
                 ("pa_build_step_tables", [ctypes.POINTER(P), i32, i32, ip, ip, ip, ip], i32)):
             fn = getattr(lib, name)
             fn.argtypes, fn.restype = args, res
+        lib.pa_mixed_step_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.pa_mixed_step_workspace_bytes.restype = ctypes.c_size_t
+        lib.pa_mixed_step.argtypes = [pool_p, i32, ctypes.c_float, P, P, P, i32,
+                                      P, P, P, P, i32, P, i32, i32, i32, P,
+                                      P, P, P, P, i32, P, i32, P, P, ctypes.c_size_t, P]
+        lib.pa_mixed_step.restype = i32
         lib.pa_get_device_error.argtypes = [P, ctypes.POINTER(i32)]
         lib.pa_get_device_error.restype = i32
         lib.pa_status_string.argtypes = [i32]
@@ -589,6 +596,77 @@ def paged_attn_prefill_chunk_f8(q: torch.Tensor, chunk_starts: torch.Tensor, chu
     """Causal chunked-prefill attention over an fp8 (E4M3) pool; as :func:`paged_attn_prefill_chunk_q8`."""
     return paged_attn_prefill_chunk_q8(q, chunk_starts, chunk_lens, k_codes, v_codes, k_scale, v_scale,
                                        block_tables, context_lens, scale, out, max_chunk_len, stream, _fp8=True)
+
+
+def mixed_step_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int) -> int:
+    return int(load_library().pa_mixed_step_workspace_bytes(num_seqs, num_q_heads, num_kv_heads))
+
+
+def alloc_mixed_step_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace for :func:`mixed_step` (every call leaves it zero again)."""
+    n = mixed_step_workspace_bytes(num_seqs, num_q_heads, num_kv_heads)
+    if n == 0:
+        raise ValueError("unsupported sizes for the mixed step")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def mixed_step(k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float, workspace: torch.Tensor,
+               k_chunks: Optional[torch.Tensor] = None, v_chunks: Optional[torch.Tensor] = None,
+               chunk_slots: Optional[torch.Tensor] = None, q_chunks: Optional[torch.Tensor] = None,
+               chunk_starts: Optional[torch.Tensor] = None, chunk_lens: Optional[torch.Tensor] = None,
+               chunk_block_tables: Optional[torch.Tensor] = None, chunk_context_lens: Optional[torch.Tensor] = None,
+               q: Optional[torch.Tensor] = None, k_dec: Optional[torch.Tensor] = None,
+               v_dec: Optional[torch.Tensor] = None, block_tables: Optional[torch.Tensor] = None,
+               context_lens: Optional[torch.Tensor] = None, out_chunks: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None, max_chunk_len: int = 512, stream=None):
+    """A whole mixed step in one persistent launch (``pa_mixed_step``): the
+    write of the chunks' new tokens k_chunks / v_chunks [Tc, Hkv, 128] through
+    chunk_slots, then the chunked prefill of q_chunks, beside the decode of q
+    with each sequence's new token k_dec / v_dec [S, Hkv, 128] (None: already in
+    the pool) written at position context_lens - 1.  Either part may be None.
+    Returns (out_chunks, out)."""
+    pool = make_pool(k_cache, v_cache)
+    hkv = k_cache.shape[2]
+    _need(workspace, "workspace")
+    T = 0 if chunk_slots is None else chunk_slots.numel()
+    if T:
+        _need(chunk_slots, "chunk_slots", torch.int64)
+        _need(k_chunks, "k_chunks", k_cache.dtype)
+        _need(v_chunks, "v_chunks", k_cache.dtype)
+    C = 0 if q_chunks is None else chunk_starts.numel()
+    S = 0 if q is None else q.shape[0]
+    hq = q_chunks.shape[1] if C else (q.shape[1] if S else hkv)
+    if C:
+        _need(q_chunks, "q_chunks", k_cache.dtype)
+        for name, t in (("chunk_starts", chunk_starts), ("chunk_lens", chunk_lens),
+                        ("chunk_block_tables", chunk_block_tables), ("chunk_context_lens", chunk_context_lens)):
+            _need(t, name, torch.int32)
+        if out_chunks is None:
+            out_chunks = torch.empty_like(q_chunks)
+        _need(out_chunks, "out_chunks", q_chunks.dtype)
+    if S:
+        _need(q, "q", k_cache.dtype)
+        _need(block_tables, "block_tables", torch.int32)
+        _need(context_lens, "context_lens", torch.int32)
+        if (k_dec is None) != (v_dec is None):
+            raise ValueError("k_dec and v_dec go together")
+        if k_dec is not None:
+            _need(k_dec, "k_dec", k_cache.dtype)
+            _need(v_dec, "v_dec", k_cache.dtype)
+        if out is None:
+            out = torch.empty_like(q)
+        _need(out, "out", q.dtype)
+    ptr = lambda t, on: t.data_ptr() if (on and t is not None) else None
+    _check(load_library().pa_mixed_step(
+        ctypes.byref(pool), hq, float(scale), ptr(k_chunks, T), ptr(v_chunks, T), ptr(chunk_slots, T), T,
+        ptr(q_chunks, C), ptr(chunk_starts, C), ptr(chunk_lens, C), ptr(chunk_block_tables, C),
+        chunk_block_tables.shape[1] if C else 0, ptr(chunk_context_lens, C), C, q_chunks.shape[0] if C else 0,
+        int(max_chunk_len), ptr(out_chunks, C),
+        ptr(q, S), ptr(k_dec, S), ptr(v_dec, S), ptr(block_tables, S), block_tables.shape[1] if S else 0,
+        ptr(context_lens, S), S, ptr(out, S),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "pa_mixed_step")
+    return out_chunks, out
 
 
 def selftest_bounded_wait(limit_us: int = 20000, stream=None) -> None:

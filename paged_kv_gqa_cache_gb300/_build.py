@@ -19,10 +19,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpagedattn.so")
 
-SOURCES = ["pa_abi.cu", "kv_write.cu", "decode.cu", "prefill.cu", "prefill8.cu", "decode_noalloc.cu", "block_copy.cu",
+SOURCES = ["pa_abi.cu", "kv_write.cu", "decode.cu", "prefill.cu", "prefill8.cu", "mixed.cu", "decode_noalloc.cu", "block_copy.cu",
            "rope_write.cu", "selftest.cu",
            "allocator.cpp"]
-HEADERS = ["pa_device.cuh", "pa_internal.h", "tcgen05.cuh", "context_cache.h", "prefill_kernel.cuh"]
+HEADERS = ["pa_device.cuh", "pa_internal.h", "tcgen05.cuh", "context_cache.h", "prefill_kernel.cuh", "decode_kernel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

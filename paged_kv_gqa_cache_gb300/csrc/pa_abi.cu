@@ -796,4 +796,136 @@ pa_status pa_get_device_error(pa_stream_t stream, int32_t *detail) {
   return static_cast<pa_status>(host[0]);
 }
 
+// ---- one persistent launch for a mixed step --------------------------------------
+
+namespace {
+constexpr size_t kMixedSyncBytes = 256;  // the launch's 4 counters, then the decode's workspace
+constexpr int kMixedMaxSeqs = 6000;
+constexpr int kMixedMaxChunks = 256;
+}  // namespace
+
+size_t pa_mixed_step_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads) {
+  if (num_seqs < 0 || num_seqs > kMixedMaxSeqs || num_kv_heads < 1 || num_q_heads < 1 ||
+      num_q_heads % num_kv_heads != 0)
+    return 0;
+  return kMixedSyncBytes + decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads);
+}
+
+pa_status pa_mixed_step(const pa_kv_pool *pool, int32_t num_q_heads, float scale, const void *k_chunks,
+                        const void *v_chunks, const int64_t *chunk_slots, int32_t num_chunk_tokens,
+                        const void *q_chunks, const int32_t *chunk_starts, const int32_t *chunk_lens,
+                        const int32_t *chunk_block_tables, int32_t chunk_max_blocks,
+                        const int32_t *chunk_context_lens, int32_t num_chunks, int32_t total_q_tokens,
+                        int32_t max_chunk_len, void *out_chunks, const void *q, const void *k_dec, const void *v_dec,
+                        const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                        int32_t num_seqs, void *out, void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+  const int num_tokens = num_chunk_tokens;
+  const void *k_new = k_chunks, *v_new = v_chunks;
+  const int64_t *slot_mapping = chunk_slots;
+  pa_status st = check_pool(pool);
+  if (st != PA_OK) return st;
+  int group = 0;
+  if ((st = check_group(num_q_heads, pool->num_kv_heads, &group)) != PA_OK) return st;
+  if (num_tokens < 0 || num_chunks < 0 || num_seqs < 0 || num_chunks > kMixedMaxChunks ||
+      num_seqs > kMixedMaxSeqs || num_seqs > mixed_max_seqs(group))
+    return PA_ERR_SHAPE;
+  if (num_tokens == 0 && num_chunks == 0 && num_seqs == 0) return PA_OK;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_SHAPE;
+  if (num_tokens > 0) {
+    if (!k_new || !v_new || !slot_mapping) return PA_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)) return PA_ERR_ALIGN;
+  }
+  if (num_chunks > 0) {
+    if (!q_chunks || !chunk_starts || !chunk_lens || !chunk_block_tables || !chunk_context_lens || !out_chunks)
+      return PA_ERR_NULL;
+    if (max_chunk_len < 1 || max_chunk_len > PA_MAX_CHUNK_LEN || chunk_max_blocks < 1 || total_q_tokens < 1)
+      return PA_ERR_SHAPE;
+    if (!aligned16(q_chunks) || !aligned16(out_chunks) || !aligned4(chunk_block_tables) ||
+        !aligned4(chunk_context_lens) || !aligned4(chunk_starts) || !aligned4(chunk_lens))
+      return PA_ERR_ALIGN;
+  }
+  if (num_seqs > 0) {
+    if (!q || !block_tables || !context_lens || !out || (k_dec == nullptr) != (v_dec == nullptr)) return PA_ERR_NULL;
+    if (max_blocks_per_seq < 1) return PA_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(out) || !aligned4(block_tables) || !aligned4(context_lens) ||
+        (k_dec && (!aligned16(k_dec) || !aligned16(v_dec))))
+      return PA_ERR_ALIGN;
+  }
+  if (!workspace) return PA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return PA_ERR_ALIGN;
+  if (workspace_bytes < pa_mixed_step_workspace_bytes(num_seqs, num_q_heads, pool->num_kv_heads))
+    return PA_ERR_WORKSPACE;
+  DeviceState *d = nullptr;
+  if ((st = device_state(&d)) != PA_OK) return st;
+
+  MixedParams mp{};
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  mp.sync = reinterpret_cast<int32_t *>(ws);
+  // the write
+  mp.w.k = k_new;
+  mp.w.v = v_new;
+  mp.w.slots = slot_mapping;
+  mp.w.k_cache = pool->k_cache;
+  mp.w.v_cache = pool->v_cache;
+  mp.w.num_slots = (int64_t)pool->num_blocks * kBlock;
+  mp.w.num_tokens = num_tokens;
+  mp.w.row_vecs = pool->num_kv_heads * kHeadDim * 2 / 16;
+  mp.w.err = d->err;
+  // the prefill (no window, the plain per-tile schedule)
+  PrefillParams &pp = mp.pp;
+  pp.q = q_chunks;
+  pp.k_cache = pool->k_cache;
+  pp.v_cache = pool->v_cache;
+  pp.chunk_starts = chunk_starts;
+  pp.chunk_lens = chunk_lens;
+  pp.block_tables = chunk_block_tables;
+  pp.context_lens = chunk_context_lens;
+  pp.out = out_chunks;
+  pp.err = d->err;
+  pp.max_blocks_per_seq = chunk_max_blocks;
+  pp.num_chunks = num_chunks;
+  pp.num_kv_heads = pool->num_kv_heads;
+  pp.num_q_heads = num_q_heads;
+  pp.num_blocks = pool->num_blocks;
+  pp.total_q_tokens = total_q_tokens;
+  pp.max_chunk_len = num_chunks > 0 ? max_chunk_len : 1;
+  pp.scale_log2 = scale * 1.4426950408889634f;
+  // the decode (split items merged in the launch)
+  DecodeParams &dp = mp.dp;
+  if (!decode_workspace_carve(ws + kMixedSyncBytes, workspace_bytes - kMixedSyncBytes, num_seqs, num_q_heads,
+                              pool->num_kv_heads, dp))
+    return PA_ERR_WORKSPACE;
+  dp.meta = nullptr;
+  dp.counters = reinterpret_cast<int32_t *>(
+      ws + kMixedSyncBytes + decode_workspace_counters_offset(num_seqs, num_q_heads, pool->num_kv_heads));
+  dp.q = q;
+  dp.block_tables = block_tables;
+  dp.context_lens = context_lens;
+  dp.out = out;
+  dp.err = d->err;
+  dp.k_new = num_seqs > 0 ? k_dec : nullptr;  // each sequence's new token, written as its page is read
+  dp.v_new = num_seqs > 0 ? v_dec : nullptr;
+  dp.k_pool = pool->k_cache;
+  dp.v_pool = pool->v_cache;
+  dp.max_blocks_per_seq = num_seqs > 0 ? max_blocks_per_seq : 1;
+  dp.num_seqs = num_seqs;
+  dp.num_kv_heads = pool->num_kv_heads;
+  dp.num_q_heads = num_q_heads;
+  dp.num_blocks = pool->num_blocks;
+  dp.scale_log2 = pp.scale_log2;
+
+  CUtensorMap maps[6];
+  memset(maps, 0, sizeof(maps));
+  if (!pool_map(&maps[0], pool, pool->k_cache, false) || !pool_map_vpages(&maps[1], pool, pool->v_cache) ||
+      !pool_map(&maps[4], pool, pool->k_cache, true) || !pool_map(&maps[5], pool, pool->v_cache, true))
+    return PA_ERR_CUDA;
+  if (num_chunks > 0 &&
+      !query_maps(&maps[2], &maps[3], q_chunks, out_chunks, pool->dtype, num_q_heads, total_q_tokens, group))
+    return PA_ERR_CUDA;
+  cudaError_t e = launch_mixed(mp, maps, pool->dtype, group, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported || e == cudaErrorCooperativeLaunchTooLarge) return PA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 }  // extern "C"
+

@@ -201,6 +201,24 @@ cudaError_t launch_prefill8(const PrefillParams &p, const CUtensorMap &kmap, con
                             const CUtensorMap &qmap, const CUtensorMap &omap, int dtype, int group, bool f8,
                             cudaStream_t stream);
 
+// ---- one persistent launch for a mixed step (16-bit pools) ---------------------
+// The step's KV write (w), its chunks' prefill (pp: no window, no workspace)
+// and its sequences' decode (dp: counters set, split items merged in the
+// launch), in one cooperative launch of one CTA per SM.  sync: 4 counters of
+// the workspace, zero between calls (each call leaves them zero).
+struct MixedParams {
+  WriteParams w;
+  PrefillParams pp;
+  DecodeParams dp;
+  int32_t *sync;
+};
+// maps: prefill K (2 KB half boxes), prefill V (4 KB pages), q, out, decode K,
+// decode V (4 KB page boxes).
+cudaError_t launch_mixed(const MixedParams &mp, const CUtensorMap *maps, int dtype, int group, cudaStream_t stream);
+// Dynamic shared memory of the launch, and the most sequences it takes.
+int mixed_smem_bytes(int group, int num_seqs);
+int mixed_max_seqs(int group);
+
 // ---- launch helper ------------------------------------------------------------
 // Launch with programmatic stream serialization (see griddep_wait()).
 template <typename... KArgs, typename... Args>

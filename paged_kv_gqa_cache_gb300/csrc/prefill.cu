@@ -227,6 +227,7 @@ prefill_balanced_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
 
   if (warp < kSoftmaxWarps) {
     regs_inc<kRegsSoftmax>();
+    regs_taken();
     // ---------------- softmax + epilogue (warps 0..7), unit after unit ----------------
     const int quad = warp & 3, ch = warp >> 2;
     const int r = quad * 32 + lane;
@@ -583,6 +584,7 @@ prefill_balanced_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_c
         mbar_wait(&bars.drain, 0, kWaitLimitNs / 8);
       }
     }
+    regs_wait_taken();  // (the softmax warps hold their registers by now)
     regs_inc<128>();
   }
   if (timed_out) set_error(p.err, PA_ERR_TIMEOUT, b);

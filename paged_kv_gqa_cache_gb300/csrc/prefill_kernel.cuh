@@ -96,6 +96,18 @@ template <int N>
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
 template <int N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+// A warpgroup that gives registers up on entering its role and asks for them
+// back at its end could, with little work, ask before the warpgroups that
+// take those registers have taken them; their increase would then wait
+// forever.  So the warpgroups that take registers arrive on a named barrier
+// once they have them (regs_taken: no waiting), and the ones that gave them
+// up wait on it before asking for them back (regs_wait_taken); every thread of
+// the CTA passes the barrier exactly once.
+constexpr int kRegsBarrier = 4;  // named barrier id (0: __syncthreads, 1-3: the roles' own)
+__device__ __forceinline__ void regs_taken() {
+  asm volatile("bar.arrive %0, %1;" ::"r"(kRegsBarrier), "r"(kThreads) : "memory");
+}
+__device__ __forceinline__ void regs_wait_taken() { named_barrier(kRegsBarrier, kThreads); }
 constexpr int kHalf = 16384;                        // 128 rows x 64 elements x 2 bytes
 constexpr int kVPage = 4096;                        // V: one page (16 rows x 128 dims x 2 bytes) per box
 constexpr int kKStages = 3, kVStages = 3;
@@ -532,14 +544,41 @@ __device__ __forceinline__ bool convert_role(uint8_t *smem, Bars &bars, const CU
   return ok;
 }
 
+// Whether query tile mt of chunk c has rows: 1 yes, 0 none (the chunk is
+// shorter), -1 the chunk's metadata is bad (reported by the caller).  Also its
+// first row in q / out.
+template <int G>
+__device__ __forceinline__ int tile_rows(const PrefillParams &p, int c, int mt, int &row0) {
+  constexpr int TQ = 128 / G;
+  const int start = __ldg(p.chunk_starts + c), len = __ldg(p.chunk_lens + c), ctx = __ldg(p.context_lens + c);
+  row0 = 0;
+  for (int i = 0; i < c; ++i) row0 += __ldg(p.chunk_lens + i);
+  if (len < 1 || len > p.max_chunk_len || start < 0 || ctx != start + len || ctx > p.max_blocks_per_seq * kBlock ||
+      row0 + len > p.total_q_tokens)
+    return -1;
+  return mt * TQ < len ? 1 : 0;
+}
+
+// One query tile (chunk c, KV head h, query tile mt, which has rows: see
+// tile_rows) computed by the whole CTA of kThreads threads, with the shared
+// memory at smem (1024-aligned) and the 512 tensor-memory columns at tmem
+// (allocated by the caller).  The tile's barriers are initialised on entry;
+// with `reuse` they are invalidated before the return, which follows a
+// CTA-wide barrier, so that the CTA may run another tile (the invalidation
+// costs the last CTA about 0.6 µs, so a CTA of one tile skips it).  Returns false, in every thread, if a
+// wait of any thread timed out (reported; asynchronous work of the tile was
+// given a bounded chance to end).
 // CODES: 0 = a 16-bit pool of the query dtype T; 1 = int8 codes, 2 = E4M3
 // codes (kmap and vmap then address the code pools, one page of one KV head
 // per box), the products computed in f16.
-template <typename T, int G, int CODES = 0>
-__global__ void __launch_bounds__(kThreads, 1)
-prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-               const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-               const PrefillParams p) {
+// RS / RO: the registers of the softmax warps and of the loader / converter
+// and MMA warps inside the tile (2 x 128 x (RS + RO) <= 65536).
+template <typename T, int G, int CODES, int RS = (CODES ? kRegsSoftmax8 : kRegsSoftmax),
+          int RO = (CODES ? kRegsOther8 : kRegsOther)>
+__device__ __forceinline__ bool prefill_tile(const CUtensorMap &kmap, const CUtensorMap &vmap,
+                                             const CUtensorMap &qmap, const CUtensorMap &omap,
+                                             const PrefillParams &p, uint8_t *smem, uint32_t tmem, int c, int h,
+                                             int mt, int row0, bool reuse) {
   constexpr int TQ = 128 / G;  // query tokens per tile
   using TC = typename std::conditional<CODES == 0, T, __half>::type;  // the MMA operand type (and P's)
   constexpr bool kBF16 = std::is_same<TC, __nv_bfloat16>::value;
@@ -548,8 +587,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   constexpr uint32_t IDESC_O = tc::idesc_f16(kBF16, 128, 128, true);
   constexpr unsigned FULL = 0xffffffffu;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars &bars = *reinterpret_cast<Bars *>(smem + OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // No kernel of this library writes the chunk metadata or the block tables,
@@ -557,26 +594,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   // kernel may still run; only the loader warps, before their first copy of
   // Q, K or V, wait for it (every other warp consumes what the loaders fetch,
   // so its output stores also come after that wait).
-
-  // Heaviest tiles first: last chunk, last query tile.
-  const int c = p.num_chunks - 1 - (int)blockIdx.z;
-  const int h = blockIdx.y;
-  const int mt = (int)gridDim.x - 1 - (int)blockIdx.x;
   const int start = __ldg(p.chunk_starts + c), len = __ldg(p.chunk_lens + c), ctx = __ldg(p.context_lens + c);
-  int row0 = 0;
-  for (int i = 0; i < c; ++i) row0 += __ldg(p.chunk_lens + i);
-  const bool bad = len < 1 || len > p.max_chunk_len || start < 0 || ctx != start + len ||
-                   ctx > p.max_blocks_per_seq * kBlock || row0 + len > p.total_q_tokens;
-  if (bad) {
-    if (mt == 0 && h == 0 && threadIdx.x == 0) set_error(p.err, PA_ERR_RANGE, c);
-    griddep_launch_dependents();
-    return;
-  }
   const int t0 = mt * TQ;
-  if (t0 >= len) {
-    griddep_launch_dependents();
-    return;
-  }
   const int last_key = min(start + t0 + TQ - 1, ctx - 1);  // largest key any row of the tile sees
   const int nkt = last_key / 128 + 1;
   const int kt_ctx = (ctx - 1) / 128;                       // key tile holding the sequence's last key
@@ -616,18 +635,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     if constexpr (kQConv) mbar_init(&bars.q_conv, kSoftmaxThreads);
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
-    tc::tmem_alloc(&bars.tmem_base, kTmemCols);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
   __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = bars.tmem_base;
   bool timed_out = false;
 
   if (warp < kSoftmaxWarps) {
-    regs_inc<CODES ? kRegsSoftmax8 : kRegsSoftmax>();
+    static_assert(2 * 128 * (RS + RO) <= 65536, "register split fits the launch");
+    regs_inc<RS>();
+    regs_taken();
     // ---------------- softmax + epilogue (warps 0..7) ----------------
     const int quad = warp & 3, ch = warp >> 2;       // TMEM lane quarter, key half of every tile
     const int r = quad * 32 + lane;                  // tile row = TMEM lane
@@ -847,7 +861,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     regs_dec<128>();
   } else {
     // every loader and MMA warp runs this one decrease (setmaxnreg acts on whole warpgroups)
-    regs_dec<CODES ? kRegsOther8 : kRegsOther>();
+    regs_dec<RO>();
     if (warp != kWarpMma) {
       // ---------------- loader warps: each tile's K and V boxes, a seventh per warp ----------------
       const int lw = warp - kWarpLoad0;
@@ -995,15 +1009,65 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         mbar_wait(&bars.drain, 0, kWaitLimitNs / 8);
       }
     }
+    regs_wait_taken();  // (the softmax warps hold their registers by now)
     regs_inc<128>();
   }
   if (timed_out) set_error(p.err, PA_ERR_TIMEOUT, c);
   tc::fence_before_sync();
-  __syncthreads();
-  if (warp == kWarpMma) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
+  const bool any_timed_out = __syncthreads_or(timed_out) != 0;  // (the result is the same in every thread)
+  tc::fence_after_sync();
+  if (!reuse) return !any_timed_out;
+  if (threadIdx.x == 0) {  // nobody waits on the tile's barriers any more: invalidate the ones set up above
+    mbar_inval(&bars.q_full);
+    for (int b = 0; b < kKStages; ++b) {
+      mbar_inval(&bars.k_full[b]);
+      mbar_inval(&bars.v_full[b]);
+      mbar_inval(&bars.s_full[b]);
+      mbar_inval(&bars.p_full[b]);
+      mbar_inval(&bars.pv_done[b]);
+      if constexpr (CODES != 0) {
+        mbar_inval(&bars.kc_full[b]);
+        mbar_inval(&bars.vc_full[b]);
+      }
+    }
+    mbar_inval(&bars.x_full);
+    mbar_inval(&bars.drain);
+    if constexpr (kQConv) mbar_inval(&bars.q_conv);
   }
+  __syncthreads();  // (the next tile's set-up comes after the invalidation)
+  return !any_timed_out;
+}
+
+// One CTA per (query tile, KV head, chunk), heaviest first (last chunk, last
+// query tile).
+template <typename T, int G, int CODES = 0>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+               const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+               const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Bars &bars = *reinterpret_cast<Bars *>(smem + OFF_BAR);
+  const int c = p.num_chunks - 1 - (int)blockIdx.z;
+  const int h = blockIdx.y;
+  const int mt = (int)gridDim.x - 1 - (int)blockIdx.x;
+  int row0 = 0;
+  const int rows = tile_rows<G>(p, c, mt, row0);
+  if (rows <= 0) {
+    if (rows < 0 && mt == 0 && h == 0 && threadIdx.x == 0) set_error(p.err, PA_ERR_RANGE, c);
+    griddep_launch_dependents();
+    return;
+  }
+  if ((threadIdx.x >> 5) == kWarpMma) {
+    tc::tmem_alloc(&bars.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars.tmem_base;
+  prefill_tile<T, G, CODES>(kmap, vmap, qmap, omap, p, smem, tmem, c, h, mt, row0, false);
+  if ((threadIdx.x >> 5) == kWarpMma) tc::tmem_dealloc(tmem, kTmemCols);
   griddep_launch_dependents();
 }
 

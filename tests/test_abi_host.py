@@ -57,7 +57,7 @@ def test_only_c_entry_points_are_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 9
+    assert lib.pa_abi_version() == 10
     for code in range(0, -12, -1):
         assert lib.pa_status_string(code).decode().startswith(pa.STATUS[code])
 
@@ -225,6 +225,35 @@ def test_prefill_q8_checks_its_arguments(lib):
     assert call(scale=float("nan")) == -2
     assert call(q=0) == -1
     assert call(q=P + 8) == -9 and call(out=P + 2, codes=1) == -9   # every check before any CUDA call
+
+
+def test_mixed_step_checks_its_arguments(lib):
+    pool = _pool()
+    ws = lib.pa_mixed_step_workspace_bytes(512, 16, 8)
+    assert ws > lib.pa_decode_workspace_bytes(512, 16, 8, 1024)     # the launch's counters, then the decode's
+    assert lib.pa_mixed_step_workspace_bytes(6001, 16, 8) == 0       # over the sequence bound
+    assert lib.pa_mixed_step_workspace_bytes(4, 12, 8) == 0
+    ws = lib.pa_mixed_step_workspace_bytes(4, 16, 8)   # the calls below have 4 sequences
+
+    def call(**kw):
+        T, C, S = kw.get("T", 4), kw.get("C", 3), kw.get("S", 4)
+        return lib.pa_mixed_step(
+            ctypes.byref(kw.get("pool", pool)), kw.get("hq", 16), kw.get("scale", 0.088),
+            kw.get("k", P), P, kw.get("slots", P), T,
+            kw.get("qc", P), P, P, P, 128, P, C, 1536, kw.get("mcl", 512), kw.get("oc", P),
+            kw.get("q", P), kw.get("kd", P), kw.get("vd", P), P, 64, P, S, kw.get("out", P),
+            kw.get("ws", P), kw.get("wsb", ws), None)
+    assert call(T=0, C=0, S=0) == 0                       # nothing to do
+    assert call(T=-1) == -2 and call(C=257) == -2 and call(S=6001) == -2
+    assert call(hq=12) == -2 and call(hq=24) == -4        # not a multiple of Hkv; a ratio outside {1, 2, 4, 8}
+    assert call(scale=float("nan")) == -2
+    assert call(k=0) == -1 and call(qc=0) == -1 and call(q=0) == -1
+    assert call(kd=0) == -1                               # the sequences' new K and V go together
+    assert call(kd=0, vd=0, ws=0) == -5                   # (both absent: already in the pool)
+    assert call(k=0, T=0, ws=0) == -5                     # a part with no work reads none of its pointers
+    assert call(mcl=513) == -2
+    assert call(qc=P + 8) == -9 and call(out=P + 2) == -9 and call(slots=P + 4) == -9 and call(kd=P + 8) == -9
+    assert call(ws=0) == -5 and call(wsb=ws - 1) == -5 and call(ws=P + 8) == -9   # every check before any CUDA call
 
 
 def test_window_calls_check_their_arguments(lib):

@@ -85,6 +85,24 @@ def test_mixed_step_as_benchmarked():
         check_close(step.out_d[i], refd, f"mixed step decode, pool {i}")
 
 
+def test_persistent_mixed_step_as_benchmarked():
+    step = bench.MixedStep(DEV, persistent=True)   # 28 layers, 2 pools, one pa_mixed_step launch per layer
+    c = step.case
+    before = [(bits(c.k_cache[i]), bits(c.v_cache[i])) for i in range(2)]
+    _replay(step.run)
+    for i, (kh, vh) in enumerate(before):
+        assert oracle.kv_cache_write(kh, vh, bits(c.k_new[i]), bits(c.v_new[i]), c.slot_mapping.cpu().numpy()) == 0
+        assert np.array_equal(bits(c.k_cache[i]), kh) and np.array_equal(bits(c.v_cache[i]), vh)
+        refp = oracle.paged_attn_prefill(bits(c.q_chunks[i]), kh, vh, c.chunk_starts.cpu().numpy(),
+                                         c.chunk_lens.cpu().numpy(), c.chunk_block_tables.cpu().numpy(),
+                                         c.chunk_context_lens.cpu().numpy(), c.scale, oracle.BF16)
+        check_close(step.out_p[i], refp, f"persistent mixed step prefill, pool {i}")
+        refd = oracle.paged_attn_decode(bits(c.q[i]), kh, vh, c.block_tables.cpu().numpy(),
+                                        c.context_lens.cpu().numpy(), c.scale, oracle.BF16)
+        check_close(step.out_d[i], refd, f"persistent mixed step decode, pool {i}")
+    assert int(step.mws[:16].count_nonzero()) == 0   # the launch's counters
+
+
 def _same_pool(gpu, host, what):
     for g, h, name in zip(gpu, host, ("k codes", "v codes", "k scales", "v scales")):
         gn = g.cpu().numpy()
