@@ -126,6 +126,7 @@ static_assert(OFF_STAGE + kSoftmaxWarps * kStageBytes <= OFF_V, "epilogue areas 
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;    // + barriers (< 256 B) + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;                 // S/P 0, S/P 1, O_0, O_1
+constexpr uint32_t kTmemAllocHere = 0xffffffffu;    // prefill_tile: allocate the columns in the tile's set-up
 constexpr uint32_t kColO = 256;
 constexpr float kRescale = 8.f;                     // log2 of the largest P before O is rescaled
 constexpr float kRescaleSum = 256.f;                // 2^kRescale: a half-row sum at most this has no larger P
@@ -562,7 +563,9 @@ __device__ __forceinline__ int tile_rows(const PrefillParams &p, int c, int mt, 
 // One query tile (chunk c, KV head h, query tile mt, which has rows: see
 // tile_rows) computed by the whole CTA of kThreads threads, with the shared
 // memory at smem (1024-aligned) and the 512 tensor-memory columns at tmem
-// (allocated by the caller).  The tile's barriers are initialised on entry;
+// (allocated by the caller, or, when tmem_in is kTmemAllocHere, by this call
+// beside the barriers' set-up and left to the caller to free from
+// bars.tmem_base).  The tile's barriers are initialised on entry;
 // with `reuse` they are invalidated before the return, which follows a
 // CTA-wide barrier, so that the CTA may run another tile (the invalidation
 // costs the last CTA about 0.6 µs, so a CTA of one tile skips it).  Returns false, in every thread, if a
@@ -577,8 +580,8 @@ template <typename T, int G, int CODES, int RS = (CODES ? kRegsSoftmax8 : kRegsS
           int RO = (CODES ? kRegsOther8 : kRegsOther)>
 __device__ __forceinline__ bool prefill_tile(const CUtensorMap &kmap, const CUtensorMap &vmap,
                                              const CUtensorMap &qmap, const CUtensorMap &omap,
-                                             const PrefillParams &p, uint8_t *smem, uint32_t tmem, int c, int h,
-                                             int mt, int row0, bool reuse) {
+                                             const PrefillParams &p, uint8_t *smem, uint32_t tmem_in, int c,
+                                             int h, int mt, int row0, bool reuse) {
   constexpr int TQ = 128 / G;  // query tokens per tile
   using TC = typename std::conditional<CODES == 0, T, __half>::type;  // the MMA operand type (and P's)
   constexpr bool kBF16 = std::is_same<TC, __nv_bfloat16>::value;
@@ -635,7 +638,14 @@ __device__ __forceinline__ bool prefill_tile(const CUtensorMap &kmap, const CUte
     if constexpr (kQConv) mbar_init(&bars.q_conv, kSoftmaxThreads);
     fence_mbar_init();
   }
+  if (tmem_in == kTmemAllocHere && warp == kWarpMma) {  // (beside thread 0's set-up: one barrier for both)
+    tc::tmem_alloc(&bars.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
   __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_in == kTmemAllocHere ? bars.tmem_base : tmem_in;
   bool timed_out = false;
 
   if (warp < kSoftmaxWarps) {
@@ -1058,16 +1068,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     griddep_launch_dependents();
     return;
   }
-  if ((threadIdx.x >> 5) == kWarpMma) {
-    tc::tmem_alloc(&bars.tmem_base, kTmemCols);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = bars.tmem_base;
-  prefill_tile<T, G, CODES>(kmap, vmap, qmap, omap, p, smem, tmem, c, h, mt, row0, false);
-  if ((threadIdx.x >> 5) == kWarpMma) tc::tmem_dealloc(tmem, kTmemCols);
+  prefill_tile<T, G, CODES>(kmap, vmap, qmap, omap, p, smem, kTmemAllocHere, c, h, mt, row0, false);
+  if ((threadIdx.x >> 5) == kWarpMma) tc::tmem_dealloc(bars.tmem_base, kTmemCols);
   griddep_launch_dependents();
 }
 
