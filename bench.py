@@ -900,7 +900,7 @@ def decode_line(args, dev, pa, workload: int, kv: str = "16bit", window: int = 0
                                   else "split + combine") + ")",
                      "bytes_per_launch": launch_bytes, "launch_ms": round(dec_launch_ms, 5),
                      "launches_timed": step.L * args.steps * len(dec_reps),
-                     "traffic": committed_traffic("decode.cu", f"decode{tag}_workload{workload}.md")},
+                     "traffic": committed_traffic(("decode.cu", "decode_kernel.cuh"), f"decode{tag}_workload{workload}.md")},
         "clocks": clk.summary(),
     }
     if rank == 0 and cpu and not args.no_cpu_baseline:

@@ -22,8 +22,8 @@
 // the 64-dim halves of 16 keys, gathered half by half; V as one 4 KB box per
 // page with its two halves 2 KB apart; 128-byte swizzled): K through a
 // 3-stage ring released as soon as S is computed, V through a 3-stage ring
-// released after the PV product.  Three loader warps fill both rings, each
-// issuing a third of every tile's 24 boxes from parallel lanes: the TMA engine
+// released after the PV product.  Seven loader warps fill both rings, each
+// issuing a seventh of every tile's 24 boxes from parallel lanes: the TMA engine
 // serves each issuing warp at a fixed cost per box, so the box count and the
 // warps, not the ring depth, set the ingest rate.  Per key tile kt:
 //   S = Q K^T     tcgen05.mma kind::f16, A and B from shared memory (K-major),
@@ -49,7 +49,7 @@
 // it by more than 2^8, so the threads rarely touch O.  The epilogue merges the
 // two halves of each row, O = O_0 2^(m_0 - M) + O_1 2^(m_1 - M) over
 // l_0 2^(m_0 - M) + l_1 2^(m_1 - M), and stores it in the input dtype.
-// Warps 8..10 load Q, K and V, warp 11 owns TMEM and issues the
+// Warps 8..14 load Q, K and V, warp 15 owns TMEM and issues the
 // MMAs (one thread); mbarriers hand tiles between the roles and every wait is
 // bounded.  Keys above the diagonal are masked per element on the tiles that
 // cross it (a warp-uniform test picks the unmasked path elsewhere) and never
@@ -88,9 +88,9 @@ static_assert(kThreads == 512, "four warpgroups: two of softmax warps, two of lo
 // to 128 before the common tail.
 constexpr int kRegsSoftmax = 200, kRegsOther = 56;
 static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther <= 65536, "register split fits the launch");
-// Over 8-bit pools the converters hold a page's codes and their conversions:
-// 88 registers (the softmax keeping 168) is what they need without spilling.
-constexpr int kRegsSoftmax8 = 168, kRegsOther8 = 88;
+// Over 8-bit pools the converters hold two pages' codes and their conversions:
+// 96 registers (the softmax keeping 160) is what they need without spilling.
+constexpr int kRegsSoftmax8 = 160, kRegsOther8 = 96;
 static_assert(2 * 128 * kRegsSoftmax8 + 2 * 128 * kRegsOther8 <= 65536, "register split fits the launch");
 template <int N>
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
@@ -337,6 +337,41 @@ __device__ __forceinline__ void convert_page(const uint8_t *codes, uint8_t *out0
   }
 }
 
+// Two pages at once (as convert_page each): every lane loads both pages'
+// codes, then converts them, so the 32 conversions of a lane interleave.
+template <int CODES>
+__device__ __forceinline__ void convert_two_pages(const uint8_t *codes0, uint8_t *o00, uint8_t *o01, float s0,
+                                                  uint32_t valid0, const uint8_t *codes1, uint8_t *o10,
+                                                  uint8_t *o11, float s1, uint32_t valid1, int lane) {
+  const int jj = lane & 3, hh = (lane >> 2) & 1, j = 4 * (lane >> 3) + jj;
+  const ScaleH sa = split_scale(__shfl_sync(0xffffffffu, s0, j));
+  const ScaleH sb = split_scale(__shfl_sync(0xffffffffu, s1, j));
+  uint4 ca[4], cb[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int ci = (i + jj + 2 * hh) & 3;
+    ca[i] = *reinterpret_cast<const uint4 *>(codes0 + j * 128 + hh * 64 + ci * 16);
+    cb[i] = *reinterpret_cast<const uint4 *>(codes1 + j * 128 + hh * 64 + ci * 16);
+  }
+  __syncwarp();
+  uint8_t *da = (hh ? o01 : o00) + j * 128, *db = (hh ? o11 : o10) + j * 128;
+  const uint32_t ka = ((valid0 >> j) & 1) ? 0xffffffffu : 0u, kb = ((valid1 >> j) & 1) ? 0xffffffffu : 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int ci = (i + jj + 2 * hh) & 3;
+    const uint2 a = dequant4<CODES>(ca[i].x, sa), b = dequant4<CODES>(ca[i].y, sa);
+    const uint2 e = dequant4<CODES>(ca[i].z, sa), f = dequant4<CODES>(ca[i].w, sa);
+    const uint2 a2 = dequant4<CODES>(cb[i].x, sb), b2 = dequant4<CODES>(cb[i].y, sb);
+    const uint2 e2 = dequant4<CODES>(cb[i].z, sb), f2 = dequant4<CODES>(cb[i].w, sb);
+    *reinterpret_cast<uint4 *>(da + (((2 * ci) ^ (j & 7)) << 4)) = make_uint4(a.x & ka, a.y & ka, b.x & ka, b.y & ka);
+    *reinterpret_cast<uint4 *>(da + (((2 * ci + 1) ^ (j & 7)) << 4)) = make_uint4(e.x & ka, e.y & ka, f.x & ka, f.y & ka);
+    *reinterpret_cast<uint4 *>(db + (((2 * ci) ^ (j & 7)) << 4)) =
+        make_uint4(a2.x & kb, a2.y & kb, b2.x & kb, b2.y & kb);
+    *reinterpret_cast<uint4 *>(db + (((2 * ci + 1) ^ (j & 7)) << 4)) =
+        make_uint4(e2.x & kb, e2.y & kb, f2.x & kb, f2.y & kb);
+  }
+}
+
 // bf16 bits of the largest magnitude in query row r of the Q tile (its two
 // 64-dim halves at q + 128 r and q + kHalf + 128 r; the pieces are visited
 // from a lane-dependent start so that a quarter-warp's loads hit distinct banks).
@@ -429,9 +464,9 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t (&v)[2][32], uint
 // fetch tile t + 1's codes into the stage that tile t - 2 released (K: once
 // its S was computed; V: once its P V product was done), so that no
 // conversion waits for the tensor core's latest step; wait for tile t's
-// codes, rewrite them as f16 rows in place (K: page p's codes in the stage's
-// upper 64-dim half where its rows' dims 64..127 go; V: in the upper half of
-// the page's 4 KB); arrive on the tile's K / V barrier.  The scales of each
+// codes, rewrite them as f16 rows in place, two pages per pass (K: page p's
+// codes in the stage's upper 64-dim half where its rows' dims 64..127 go; V:
+// in the upper half of the page's 4 KB); arrive on the tile's K / V barrier.  The scales of each
 // lane's row are loaded with the codes, and the pages' block ids a tile
 // before that.  Pages past the sequence are not fetched and their rows, like
 // every row of a key >= ctx, become zeros; a block id outside the pool is
@@ -521,16 +556,20 @@ __device__ __forceinline__ bool convert_role(uint8_t *smem, Bars &bars, const CU
       ok = false;
       break;
     }
-#pragma unroll 1
-    for (int k = 0; k < 3; ++k) {
-      const int page = wi + nw * k;
-      if (page < 8) {
-        // rows of the page inside the sequence (none if the page was not fetched)
+    {
+      // pages 0 and 1 of the warp (every converter has at least two), then page 2 if any
+      auto rows_valid = [&](int k, int page) {
         const int nrow = ((fa.okm >> k) & 1) ? ctx - ((kt0 + t) * 128 + page * 16) : 0;
-        const uint32_t valid = nrow >= 16 ? 0xffffu : (nrow > 0 ? (1u << nrow) - 1u : 0u);
-        uint8_t *o0 = out0_of(st, page);
-        convert_page<CODES>(codes_of(st, page), o0, o0 + (kside ? kHalf : kVPage / 2),
-                            k == 0 ? fa.s[0] : (k == 1 ? fa.s[1] : fa.s[2]), valid, lane);
+        return nrow >= 16 ? 0xffffu : (nrow > 0 ? (1u << nrow) - 1u : 0u);
+      };
+      const int p0 = wi, p1 = wi + nw, p2 = wi + 2 * nw;
+      uint8_t *a0 = out0_of(st, p0), *a1 = out0_of(st, p1);
+      const int up = kside ? kHalf : kVPage / 2;
+      convert_two_pages<CODES>(codes_of(st, p0), a0, a0 + up, fa.s[0], rows_valid(0, p0), codes_of(st, p1), a1,
+                               a1 + up, fa.s[1], rows_valid(1, p1), lane);
+      if (p2 < 8) {
+        uint8_t *a2 = out0_of(st, p2);
+        convert_page<CODES>(codes_of(st, p2), a2, a2 + up, fa.s[2], rows_valid(2, p2), lane);
       }
     }
     fence_proxy_async_smem();  // the generic writes reach the tensor core's reads
