@@ -836,75 +836,78 @@ __device__ __forceinline__ bool prefill_tile(const CUtensorMap &kmap, const CUte
       mbar_arrive(&bars.p_full[kt % kVStages]);
     }
 
-    if (!timed_out) {
-      const int j = ntl - 1;
-      if (mbar_wait(&bars.pv_done[j % kVStages], (j / kVStages) & 1)) {
-        tc::fence_after_sync();
-        // merge the two halves of the row
-        float2 *xm = reinterpret_cast<float2 *>(smem + OFF_X);
-        xm[ch * 128 + r] = make_float2(m_ref, l);
-        mbar_arrive(&bars.x_full);
-        if (mbar_wait(&bars.x_full, 0)) {
-          const float2 other = xm[(1 - ch) * 128 + r];
-          const float m0 = ch == 0 ? m_ref : other.x, l0 = ch == 0 ? l : other.y;
-          const float m1 = ch == 0 ? other.x : m_ref, l1 = ch == 0 ? other.y : l;
-          const float M = fmaxf(m0, m1);
-          const float f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M);
-          const float f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M);
-          const float inv = 1.f / (l0 * f0 + l1 * f1);
-          const float g0 = f0 * inv, g1 = f1 * inv;
-          T *op = reinterpret_cast<T *>(p.out) + ((int64_t)(row0 + tq) * p.num_q_heads + head) * kHeadDim + ch * 64;
-          const uint32_t o0 = tmem + lane_base + kColO + ch * 64, o1 = o0 + 128;
-          // A query tile wholly inside its chunk leaves through one TMA store per
-          // 64-dim half: each thread puts its row's 64 outputs into the (now idle)
-          // Q buffer in the 128-byte swizzled layout the Q tile came in, which is
-          // the out tensor's own tile shape.  A tile that runs past the chunk's
-          // end (its last rows belong to the next chunk) stores row by row.
-          const bool tile_store = t0 + TQ <= len;
-          uint8_t *otile = smem + OFF_Q + ch * kHalf;
+    // The row's output, once P V of its last tile has landed and the two halves
+    // have met.  The waits' outcome is made warp-uniform before the output
+    // path, whose tensor-memory loads and row stores are warp-wide: a warp in
+    // which any thread timed out stores nothing.
+    bool ok = !timed_out;
+    const int j = ntl - 1;
+    if (ok) ok = mbar_wait(&bars.pv_done[j % kVStages], (j / kVStages) & 1);
+    float2 *xm = reinterpret_cast<float2 *>(smem + OFF_X);
+    if (ok) {
+      tc::fence_after_sync();
+      // merge the two halves of the row
+      xm[ch * 128 + r] = make_float2(m_ref, l);
+      mbar_arrive(&bars.x_full);
+      ok = mbar_wait(&bars.x_full, 0);
+    }
+    ok = __all_sync(FULL, ok) != 0;
+    if (!ok) timed_out = true;
+    const bool tile_store = t0 + TQ <= len;
+    if (ok) {
+      const float2 other = xm[(1 - ch) * 128 + r];
+      const float m0 = ch == 0 ? m_ref : other.x, l0 = ch == 0 ? l : other.y;
+      const float m1 = ch == 0 ? other.x : m_ref, l1 = ch == 0 ? other.y : l;
+      const float M = fmaxf(m0, m1);
+      const float f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M);
+      const float f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M);
+      const float inv = 1.f / (l0 * f0 + l1 * f1);
+      const float g0 = f0 * inv, g1 = f1 * inv;
+      T *op = reinterpret_cast<T *>(p.out) + ((int64_t)(row0 + tq) * p.num_q_heads + head) * kHeadDim + ch * 64;
+      const uint32_t o0 = tmem + lane_base + kColO + ch * 64, o1 = o0 + 128;
+      // A query tile wholly inside its chunk leaves through one TMA store per
+      // 64-dim half: each thread puts its row's 64 outputs into the (now idle)
+      // Q buffer in the 128-byte swizzled layout the Q tile came in, which is
+      // the out tensor's own tile shape.  A tile that runs past the chunk's
+      // end (its last rows belong to the next chunk) stores row by row.
+      uint8_t *otile = smem + OFF_Q + ch * kHalf;
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t a[32], b[32];
-            tc::ld_32x32b_x32(o0 + cc * 32, a);  // warp-wide; only rows of the chunk are stored
-            tc::ld_32x32b_x32(o1 + cc * 32, b);
-            tc::wait_ld();
-            uint4 w[4];
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t a[32], b[32];
+        tc::ld_32x32b_x32(o0 + cc * 32, a);  // warp-wide; only rows of the chunk are stored
+        tc::ld_32x32b_x32(o1 + cc * 32, b);
+        tc::wait_ld();
+        uint4 w[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float y[8];
+        for (int i = 0; i < 4; ++i) {
+          float y[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                y[e] = __uint_as_float(a[8 * i + e]) * g0 + __uint_as_float(b[8 * i + e]) * g1;
-              w[i].x = Pack<T>::from_f2(y[0], y[1]);
-              w[i].y = Pack<T>::from_f2(y[2], y[3]);
-              w[i].z = Pack<T>::from_f2(y[4], y[5]);
-              w[i].w = Pack<T>::from_f2(y[6], y[7]);
-            }
-            if (tile_store) {  // 16-byte piece cc * 4 + i of row r, XOR-swizzled by r % 8
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<uint4 *>(otile + r * 128 + (((cc * 4 + i) ^ (r & 7)) << 4)) = w[i];
-            } else {
-              // warp-wide (every lane takes part); rows past the chunk are not stored
-              store_rows_coalesced(reinterpret_cast<uint4 *>(smem + OFF_STAGE + warp * kStageBytes), op + cc * 32,
-                                   tq < len, w, lane);
-            }
-          }
-          if (tile_store) {
-            fence_proxy_async_smem();  // the generic writes reach the TMA engine
-            named_barrier(2, kSoftmaxThreads);
-            if (threadIdx.x == 0) {
-              tma_store_3d(&omap, smem + OFF_Q, 0, h * G, row0 + t0);
-              tma_store_3d(&omap, smem + OFF_Q + kHalf, 64, h * G, row0 + t0);
-              bulk_commit_group();
-              bulk_wait_group_all();  // before the CTA ends and its shared memory is reused
-            }
-          }
-        } else {
-          timed_out = true;
+          for (int e = 0; e < 8; ++e)
+            y[e] = __uint_as_float(a[8 * i + e]) * g0 + __uint_as_float(b[8 * i + e]) * g1;
+          w[i].x = Pack<T>::from_f2(y[0], y[1]);
+          w[i].y = Pack<T>::from_f2(y[2], y[3]);
+          w[i].z = Pack<T>::from_f2(y[4], y[5]);
+          w[i].w = Pack<T>::from_f2(y[6], y[7]);
         }
-      } else {
-        timed_out = true;
+        if (tile_store) {  // 16-byte piece cc * 4 + i of row r, XOR-swizzled by r % 8
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4 *>(otile + r * 128 + (((cc * 4 + i) ^ (r & 7)) << 4)) = w[i];
+        } else {
+          // warp-wide (every lane takes part); rows past the chunk are not stored
+          store_rows_coalesced(reinterpret_cast<uint4 *>(smem + OFF_STAGE + warp * kStageBytes), op + cc * 32,
+                               tq < len, w, lane);
+        }
+      }
+    }
+    if (tile_store) {  // every softmax thread joins the barrier of the TMA store, whatever it wrote
+      fence_proxy_async_smem();  // the generic writes reach the TMA engine
+      named_barrier(2, kSoftmaxThreads);
+      if (threadIdx.x == 0 && !timed_out) {
+        tma_store_3d(&omap, smem + OFF_Q, 0, h * G, row0 + t0);
+        tma_store_3d(&omap, smem + OFF_Q + kHalf, 64, h * G, row0 + t0);
+        bulk_commit_group();
+        bulk_wait_group_all();  // before the CTA ends and its shared memory is reused
       }
     }
     regs_dec<128>();
