@@ -1,6 +1,7 @@
 """Host-side pieces of bench.py: argument defaults, the peak-file reader, the
 committed-traffic lookup, and the multi-rank plumbing (max over ranks and the
 barrier) on world_size 2 with the gloo backend on CPU."""
+import hashlib
 import os
 import socket
 
@@ -29,6 +30,35 @@ def test_peaks_come_from_the_measured_file_or_the_fallback():
 
 def test_committed_traffic_is_ignored_when_the_kernel_changed(tmp_path, monkeypatch):
     assert bench.committed_traffic("decode.cu", "no_such_summary.md") is None
+    # a summary names the sha256 of its sources (one file, or several hashed in order)
+    csrc = tmp_path / "paged_kv_gqa_cache_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "a.cu").write_bytes(b"kernel a\n")
+    (csrc / "b.cuh").write_bytes(b"header b\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = lambda *names: hashlib.sha256(b"".join((csrc / n).read_bytes() for n in names)).hexdigest()[:16]
+    (tmp_path / "profiles" / "one.md").write_text(f"source_sha256_16: {sha('a.cu')}\ntraffic_bytes_per_launch: 123\n")
+    (tmp_path / "profiles" / "two.md").write_text(
+        f"source_sha256_16: {sha('a.cu', 'b.cuh')}\ntraffic_bytes_per_launch: 456\n")
+    assert bench.committed_traffic("a.cu", "one.md") == 123
+    assert bench.committed_traffic(("a.cu", "b.cuh"), "two.md") == 456
+    assert bench.committed_traffic(("b.cuh", "a.cu"), "two.md") is None   # the order is part of the hash
+    assert bench.committed_traffic("a.cu", "two.md") is None              # the header is part of the source
+    (csrc / "b.cuh").write_bytes(b"header b, changed\n")
+    assert bench.committed_traffic(("a.cu", "b.cuh"), "two.md") is None   # taken on another source
+    assert bench.committed_traffic("a.cu", "one.md") == 123
+
+
+def test_committed_summaries_match_the_current_sources():
+    # every summary the default bench reads was taken on the kernels as they are
+    for srcs, name in ((("decode.cu", "decode_kernel.cuh"), "decode_workload4.md"),
+                       (("decode.cu", "decode_kernel.cuh"), "decode_workload2.md"),
+                       (("decode.cu", "decode_kernel.cuh"), "decode_q8_workload4.md"),
+                       (("decode.cu", "decode_kernel.cuh"), "decode_f8_workload4.md"),
+                       (("prefill.cu", "prefill_kernel.cuh"), "prefill_workload3.md"),
+                       (("prefill8.cu", "prefill_kernel.cuh"), "prefill8_int8_workload3.md")):
+        assert bench.committed_traffic(srcs, name) is not None, name
 
 
 def _free_port():
