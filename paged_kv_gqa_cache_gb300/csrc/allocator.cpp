@@ -9,7 +9,7 @@
 //     joins the back);
 //   - fork shares every block of the source sequence by reference, and the
 //     first write into a shared, partly filled block copies it (allocate a
-//     fresh block, copy, release the old one; the task text's copy-on-write
+//     fresh block, copy, release the old one; task 12.1's copy-on-write
 //     rule and its worked example);
 //   - adopting a prefix retains full blocks and sets the length to their
 //     tokens, so later writes never land in them;

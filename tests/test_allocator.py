@@ -1,8 +1,8 @@
 """Host-side block allocator and block-table builder of the library (page
 "Модуль 12: Финальный проект: мини-движок инференса", task 12.1 and
 qwen_serve/paged.py: BlockAllocator, SequenceCache), through the C-ABI; no
-GPU involved.  The worked examples and acceptance item 5 of the task are
-checked as printed there; copy-on-write follows the task's rule (fork shares
+GPU involved.  The worked examples and acceptance item 5 of task 12.1 are
+checked as printed there; copy-on-write follows that task's rule (fork shares
 every block, the first write into a shared partly filled block copies it)."""
 import numpy as np
 import pytest
