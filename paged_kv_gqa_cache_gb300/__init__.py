@@ -633,6 +633,8 @@ def mixed_step(k_cache: torch.Tensor, v_cache: torch.Tensor, scale: float, works
         _need(chunk_slots, "chunk_slots", torch.int64)
         _need(k_chunks, "k_chunks", k_cache.dtype)
         _need(v_chunks, "v_chunks", k_cache.dtype)
+    if q_chunks is not None:
+        _need(chunk_starts, "chunk_starts", torch.int32)
     C = 0 if q_chunks is None else chunk_starts.numel()
     S = 0 if q is None else q.shape[0]
     hq = q_chunks.shape[1] if C else (q.shape[1] if S else hkv)
