@@ -43,10 +43,12 @@ def check_close(got: torch.Tensor, ref: np.ndarray, what: str):
     diff = np.abs(g - ref)
     bad = ~(diff <= ATOL + RTOL * np.abs(ref))
     if bad.any():
-        idx = np.argwhere(bad)[0]
+        idx = tuple(int(i) for i in np.argwhere(bad)[0])
+        finite = diff[~np.isnan(diff)]
+        worst = float(finite.max()) if finite.size else float("nan")
         raise AssertionError(
             f"{what}: {int(bad.sum())} of {bad.size} elements outside |d| <= {ATOL} + {RTOL}|ref|; "
-            f"max abs {np.nanmax(diff):.3e}; first bad at {tuple(idx)}: got {g[tuple(idx)]!r} ref {ref[tuple(idx)]!r}")
+            f"max abs {worst:.3e}; first bad at {idx}: got {float(g[idx])!r} ref {float(ref[idx])!r}")
     big = np.abs(ref) >= REL_FLOOR
     max_abs = float(diff.max(initial=0.0))
     max_rel = float((diff[big] / np.abs(ref[big])).max(initial=0.0))
