@@ -415,8 +415,8 @@ PA_API pa_status pa_paged_attn_prefill_chunk_q8(const void *q, int32_t dtype, co
  *               context_lens, out; num_seqs <= 6000), which does not wait for
  *               the chunks' write.  So no sequence may read a slot of the
  *               chunks' write, and no chunk may read a page that holds a
- *               sequence's new token (each holds only in a scheduler that
- *               gives a chunk's new tokens pages of their own).
+ *               sequence's new token (both hold when a scheduler gives the
+ *               new tokens of each chunk and sequence pages of their own).
  * Either part may be empty (num_chunks = num_chunk_tokens = 0, or num_seqs =
  * 0; its pointers are then not read).  Results as the separate calls (the
  * chunks' write first).
